@@ -1,0 +1,183 @@
+"""Q8_0 product oracle -- TEST INFRASTRUCTURE ONLY.
+
+Plain, slow CPU statements of what the Q8_0 path computes, used to check the CUDA library and nothing else. Only
+``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg import this package; the library never
+does, and this package imports nothing from the library (they share only the seeded input generator in
+``synth_inputs.py``, which holds none of the method's arithmetic).
+
+Contents, each citing the passage it follows (page titles as printed on the pages):
+
+* :func:`gemv` -- ``from_q8.rs`` module doc and ``q8_fold``: y[r,n] = sum_b s[b,n] * sum_i x[r,32b+i] q[32b+i,n],
+  done in fp64 by the C file ``q8_oracle.c`` (plain loops, the formula's order), with the error scale
+  A[r,n] = sum_b |s[b,n]| sum_i |x q|.
+* :func:`argmax` -- ``int8_model.rs`` ``decode_step_lg`` ("the first maximal logit") and the tie rule of its CUDA
+  warp arg-max in ``reference_cuda`` (equal values go to the lower index); 0-based here.
+* :func:`quantize` -- ``from_q8.rs`` ``quantize``: the Q8_0 rule and its rejections.
+* :func:`repack` -- ``from_q8.rs`` ``Q8Part`` (the host repacks the checkpoint's blocks into the int8 values and the
+  fp32 scales); the block layout is the reading stated in the design notes (36-byte blocks, fp32 scale first).
+* :func:`dequantize` -- ``from_q8.rs`` module doc, w = q * d.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` to facts the pages and the mathematics fix (brute
+force in exact rational arithmetic, closed forms, a dense fp64 matmul of the dequantized weight, the quantize
+round trip and hand-derived fixtures under ``tests/golden/``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import numpy as np
+
+Q8_BLOCK = 32  # rows of a Q8_0 block (from_q8.rs, ``Q8_BLOCK``)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q8_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle_q8.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``q8_oracle.c`` with gcc (fp64, no fast-math, OpenMP over output columns)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-fno-fast-math",
+                               "-ffp-contract=off", _SRC, "-o", tmp])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.oracle_q8_gemv.restype = ctypes.c_int
+        lib.oracle_q8_gemv.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                       ctypes.c_void_p]
+        lib.oracle_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def threads() -> int:
+    """Threads the oracle's OpenMP loop uses."""
+    return int(_load().oracle_threads())
+
+
+def padded_n(n: int) -> int:
+    """Columns padded to whole 32-column tiles (from_q8.rs ``q8_gemv_applies``: the last tile is zero-padded)."""
+    return -(-n // Q8_BLOCK) * Q8_BLOCK
+
+
+def gemv(x_bits: np.ndarray, q: np.ndarray, s: np.ndarray, cols=None):
+    """fp64 Q8_0 product and its error scale.
+
+    x_bits: uint16 bf16 patterns [m, K]; q: int8 [K, Np]; s: float32 [K/32, Np]; cols: optional column indices.
+    Returns (y, A), fp64 [m, len(cols) or Np].
+    """
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    m, K = x_bits.shape
+    K2, Np = q.shape
+    if K2 != K or s.shape != (K // Q8_BLOCK, Np):
+        raise ValueError("shape mismatch")
+    if cols is None:
+        ncols, cols_arr, cols_ptr = Np, None, None
+    else:
+        cols_arr = np.ascontiguousarray(cols, dtype=np.int64)
+        if cols_arr.size and (cols_arr.min() < 0 or cols_arr.max() >= Np):
+            raise ValueError("column out of range")
+        ncols, cols_ptr = cols_arr.size, cols_arr.ctypes.data
+    y = np.empty((m, ncols), dtype=np.float64)
+    a = np.empty((m, ncols), dtype=np.float64)
+    rc = _load().oracle_q8_gemv(x_bits.ctypes.data, q.ctypes.data, s.ctypes.data, m, K, Np, cols_ptr, ncols,
+                                y.ctypes.data, a.ctypes.data)
+    if rc != 0:
+        raise ValueError("shape the Q8_0 product does not take")
+    return y, a
+
+
+def argmax(y: np.ndarray, n: int) -> np.ndarray:
+    """Per row, the smallest index j < n with y[r, j] equal to the row's maximum over j < n (0-based).
+
+    Pad columns (j >= n) never take part.  +0.0 and -0.0 compare equal.
+    """
+    y = np.asarray(y, dtype=np.float64)
+    out = np.empty(y.shape[0], dtype=np.int64)
+    for r in range(y.shape[0]):
+        row = y[r, :n]
+        best = row.max()
+        out[r] = int(np.flatnonzero(row == best)[0])
+    return out
+
+
+def _round_half_away(v: np.ndarray) -> np.ndarray:
+    return np.where(v >= 0, np.floor(v + 0.5), -np.floor(-v + 0.5))
+
+
+def quantize(w: np.ndarray):
+    """Q8_0 values and scales of a declared weight, or None when the weight is not Q8_0 (from_q8.rs ``quantize``).
+
+    For every 32-row block b and column: amax = max |w|; a zero block keeps q = 0 and d = 0; otherwise
+    d = amax / 127 must survive a round trip through fp32, and every value w / d must lie within 1e-9 of an integer
+    r with |r| <= 127 and r * d == w exactly.  w: float64 [K, N].  Returns (q int8 [K, N], s float32 [K/32, N]).
+    """
+    w = np.asarray(w, dtype=np.float64)
+    K, N = w.shape
+    if K % Q8_BLOCK != 0:
+        return None
+    q = np.zeros((K, N), dtype=np.int8)
+    s = np.zeros((K // Q8_BLOCK, N), dtype=np.float32)
+    for b in range(K // Q8_BLOCK):
+        blk = w[Q8_BLOCK * b:Q8_BLOCK * (b + 1), :]            # [32, N]
+        amax = np.abs(blk).max(axis=0)                          # [N]
+        live = amax != 0.0                                       # zero blocks are skipped
+        d = amax / 127.0
+        if np.any(live & (d.astype(np.float32).astype(np.float64) != d)):
+            return None
+        with np.errstate(divide="ignore", invalid="ignore"):
+            v = blk / np.where(live, d, 1.0)[None, :]
+        r = _round_half_away(v)
+        bad = (np.abs(v - r) > 1e-9) | (np.abs(r) > 127.0) | (r * d[None, :] != blk)
+        if np.any(bad & live[None, :]):
+            return None
+        q[Q8_BLOCK * b:Q8_BLOCK * (b + 1), :] = np.where(live[None, :], r, 0).astype(np.int8)
+        s[b, :] = np.where(live, d, 0.0).astype(np.float32)
+    return q, s
+
+
+def dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """w[k, n] = q[k, n] * s[k // 32, n] in fp64 (exact: 8-bit by 24-bit significands)."""
+    q = np.asarray(q)
+    s = np.asarray(s, dtype=np.float64)
+    return q.astype(np.float64) * np.repeat(s, Q8_BLOCK, axis=0)
+
+
+def repack(blocks: bytes | np.ndarray, K: int, N: int):
+    """The int8 values [K, Np] and fp32 scales [K/32, Np] from checkpoint blocks (from_q8.rs ``Q8Part``).
+
+    The blocks are column-major by block: column n's K/32 blocks one after another, each 36 bytes, a little-endian
+    fp32 scale d followed by 32 int8 values.  Pad columns come out zero.  Returns None when a value is -128 (outside
+    the Q8_0 range |q| <= 127).
+    """
+    if K <= 0 or K % Q8_BLOCK or N <= 0:
+        return None
+    nb = K // Q8_BLOCK
+    raw = np.frombuffer(bytes(blocks), dtype=np.uint8)
+    if raw.size != N * nb * 36:
+        raise ValueError("block buffer size does not match K and N")
+    rec = raw.reshape(N, nb, 36)
+    d = rec[:, :, 0:4].copy().view("<f4").reshape(N, nb)
+    vals = rec[:, :, 4:36].copy().view(np.int8).reshape(N, nb, Q8_BLOCK)
+    if np.any(vals == -128):
+        return None
+    Np = padded_n(N)
+    q = np.zeros((K, Np), dtype=np.int8)
+    s = np.zeros((nb, Np), dtype=np.float32)
+    q[:, :N] = vals.reshape(N, K).T      # column n's blocks b = 0, 1, ... are its rows 32b .. 32b + 31
+    s[:, :N] = d.T
+    return q, s

@@ -1,0 +1,360 @@
+"""Pins of the fp64 oracle to what the pages and the mathematics fix (CPU only).
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped block or lane, a wrong sign, a transposed index
+of q or s, a wrong bf16 decode, a wrong abs in the error scale) fails at least one test:
+
+* brute force in exact rational arithmetic (Python ``fractions``) on one- and two-block products and on the pages'
+  ragged shapes;
+* a dense fp64 matmul of the dequantized weight (a special case that reduces to a library routine);
+* closed forms from ``tests/golden/closed_forms.txt`` and one-hot activations;
+* the exactness of every int8 x bf16 product in fp32 (from_q8.rs module doc);
+* the Q8_0 quantize rule and its round trip (from_q8.rs ``quantize``);
+* the arg-max's first-maximum rule (int8_model.rs ``decode_step_lg`` and the tie rule of ``reference_cuda``).
+"""
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+def _bf16(v: float) -> int:
+    """bf16 bit pattern of a value that bf16 represents exactly."""
+    bits = si.f32_to_bf16_bits(np.array([v], dtype=np.float32))[0]
+    assert float(si.bf16_bits_to_f32(np.array([bits]))[0]) == v
+    return int(bits)
+
+
+def _exact(x_bits, q, s, r, n):
+    """(y, A) of one output in exact rational arithmetic."""
+    xf = si.bf16_bits_to_f32(x_bits[r]).astype(np.float64)
+    K = x_bits.shape[1]
+    y, a = Fraction(0), Fraction(0)
+    for b in range(K // 32):
+        inner, inner_abs = Fraction(0), Fraction(0)
+        for i in range(32):
+            k = 32 * b + i
+            p = Fraction(float(xf[k])) * int(q[k, n])
+            inner += p
+            inner_abs += abs(p)
+        sv = Fraction(float(s[b, n]))
+        y += sv * inner
+        a += abs(sv) * inner_abs
+    return y, a
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# brute force
+# --------------------------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+@pytest.mark.parametrize("m", [1, 3])
+def test_one_block_is_exact(seed, m):
+    """K = 32, N = 1: y = s * sum_i x q has no rounding in fp64, so the oracle equals the rational value exactly."""
+    x, q, s = si.case(m, 32, 1, seed)
+    y, a = oracle.gemv(x, q, s)
+    for r in range(m):
+        ey, ea = _exact(x, q, s, r, 0)
+        assert y[r, 0] == float(ey)
+        assert a[r, 0] == float(ea)
+        assert np.all(y[r, 1:] == 0.0) and np.all(a[r, 1:] == 0.0)    # the 31 pad columns
+
+
+@pytest.mark.parametrize("seed", [4, 5])
+def test_two_blocks_two_columns(seed):
+    """K = 64, N = 2: at most one rounding (the final add), so |y - exact| <= 2^-52 A; distinguishes q[k,n] from
+    q[n,k] and s[b,n] from s[n,b] (both would read other columns' data)."""
+    x, q, s = si.case(2, 64, 2, seed)
+    y, a = oracle.gemv(x, q, s)
+    for r in range(2):
+        for n in range(2):
+            ey, ea = _exact(x, q, s, r, n)
+            assert abs(Fraction(y[r, n]) - ey) <= Fraction(2) ** -52 * ea
+            assert abs(Fraction(a[r, n]) - ea) <= Fraction(2) ** -52 * ea
+
+
+@pytest.mark.parametrize("row", _golden_rows("ragged_shapes.txt"))
+def test_pages_ragged_shapes(row):
+    """The pages' row-split tails (768, 2,176 rows) and width of 40: brute force on sampled outputs, pads zero."""
+    K, N, Np, nblocks, tail = (int(v) for v in row)
+    assert oracle.padded_n(N) == Np and K // 32 == nblocks and (K % 1024) // 32 == tail
+    x, q, s = si.case(2, K, N, 100 + K)
+    y, a = oracle.gemv(x, q, s)
+    assert y.shape == (2, Np)
+    assert np.all(y[:, N:] == 0.0) and np.all(a[:, N:] == 0.0)
+    bound = Fraction(nblocks + 32) * Fraction(2) ** -52
+    for r in range(2):
+        for n in (0, 17, N - 1):
+            ey, ea = _exact(x, q, s, r, n)
+            assert abs(Fraction(y[r, n]) - ey) <= bound * ea
+            assert abs(Fraction(a[r, n]) - ea) <= bound * ea
+
+
+def test_column_subset_matches_full():
+    x, q, s = si.case(3, 256, 100, 9)
+    y, a = oracle.gemv(x, q, s)
+    cols = np.array([99, 0, 57, 57, 127])
+    ys, as_ = oracle.gemv(x, q, s, cols)
+    assert np.array_equal(ys, y[:, cols]) and np.array_equal(as_, a[:, cols])
+
+
+def test_batch_rows_equal_single_rows():
+    """Every row of a batch reads the same weight (from_q8.rs module doc): row r of an m-row product is the
+    one-row product of row r, exactly."""
+    x, q, s = si.case(5, 512, 70, 11)
+    y, _ = oracle.gemv(x, q, s)
+    for r in range(5):
+        y1, _ = oracle.gemv(x[r:r + 1], q, s)
+        assert np.array_equal(y1[0], y[r])
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# dense fp64 matmul and closed forms
+# --------------------------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m,K,N", [(4, 1024, 96), (1, 4096, 40), (16, 256, 33)])
+def test_dense_fp64_matmul(m, K, N):
+    """y equals x @ W with W = q * s dequantized in fp64 (numpy's matmul), within 1e-12 A."""
+    x, q, s = si.case(m, K, N, 20 + m)
+    y, a = oracle.gemv(x, q, s)
+    dense = si.bf16_bits_to_f32(x).astype(np.float64) @ oracle.dequantize(q, s)
+    assert np.all(np.abs(y - dense) <= 1e-12 * a)
+    # A is the same matmul over absolute values
+    dense_abs = np.abs(si.bf16_bits_to_f32(x).astype(np.float64)) @ np.abs(oracle.dequantize(q, s))
+    assert np.all(np.abs(a - dense_abs) <= 1e-12 * a)
+
+
+@pytest.mark.parametrize("row", _golden_rows("closed_forms.txt"))
+def test_closed_forms(row):
+    name, K, N, m, expect = row[0], int(row[1]), int(row[2]), int(row[3]), float(row[4])
+    Np, nb = oracle.padded_n(N), K // 32
+    q = np.zeros((K, Np), np.int8)
+    s = np.zeros((nb, Np), np.float32)
+    x = np.zeros((m, K), np.uint16)
+    if name == "ones":
+        x[:] = _bf16(1.0); q[:, :N] = 1; s[:, :N] = 1.0
+    elif name == "ramp":
+        for r in range(m):
+            x[r] = _bf16(float(r + 1))
+        q[:, :N] = 1
+        s[:, :N] = (2.0 ** -np.arange(nb, dtype=np.float64))[:, None]
+    elif name == "alt":
+        x[:, 0::2] = _bf16(1.0); x[:, 1::2] = _bf16(-1.0); q[:, :N] = 127; s[:, :N] = 1.0 / 128
+    elif name == "signflip":
+        x[:] = _bf16(1.0); q[0::2, :N] = 127; q[1::2, :N] = -127; s[:, :N] = 1.0
+    y, a = oracle.gemv(x, q, s)
+    assert np.all(y[0, :N] == expect)
+    assert np.all(y[:, N:] == 0.0) and np.all(a[:, N:] == 0.0)
+    if name == "ramp" and m > 1:
+        assert np.all(y[1, :N] == 2 * expect)
+
+
+def test_one_hot_activation():
+    """x = e_k: y[n] = s[k/32, n] * q[k, n] exactly, for every k of a block boundary and interior."""
+    K, N = 128, 64
+    _, q, s = si.case(1, K, N, 31)
+    for k in (0, 31, 32, 77, 127):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = _bf16(1.0)
+        y, a = oracle.gemv(x, q, s)
+        want = s[k // 32].astype(np.float64) * q[k].astype(np.float64)
+        assert np.array_equal(y[0], want)
+        assert np.array_equal(a[0], np.abs(want))
+
+
+def test_zero_activation_and_zero_weight():
+    x, q, s = si.case(2, 256, 50, 3)
+    y, a = oracle.gemv(np.zeros_like(x), q, s)
+    assert np.all(y == 0.0) and np.all(a == 0.0)
+    y, a = oracle.gemv(x, np.zeros_like(q), np.zeros_like(s))
+    assert np.all(y == 0.0) and np.all(a == 0.0)
+
+
+def test_sign_symmetry_and_linearity():
+    """y(-x) = -y(x) exactly (rounding is symmetric in sign); y(x1 + x2) = y(x1) + y(x2) within 1e-12 (A1 + A2)
+    for activations whose sum bf16 represents exactly (small integers)."""
+    x, q, s = si.case(3, 512, 64, 41)
+    y, _ = oracle.gemv(x, q, s)
+    yn, _ = oracle.gemv(x ^ np.uint16(0x8000), q, s)
+    assert np.array_equal(yn, -y)
+    rng = np.random.default_rng(5)
+    x1 = rng.integers(-8, 9, size=(3, 512)).astype(np.float32)
+    x2 = rng.integers(-8, 9, size=(3, 512)).astype(np.float32)
+    b = si.f32_to_bf16_bits
+    y1, a1 = oracle.gemv(b(x1), q, s)
+    y2, a2 = oracle.gemv(b(x2), q, s)
+    y12, _ = oracle.gemv(b(x1 + x2), q, s)
+    assert np.all(np.abs(y12 - (y1 + y2)) <= 1e-12 * (a1 + a2))
+
+
+def test_int8_times_bf16_is_exact_in_fp32():
+    """from_q8.rs module doc: an int8 times a bf16 activation is exact in fp32 -- every finite bf16 pattern against
+    every int8 in [-127, 127]; the fp32 product equals the fp64 product."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    xf = si.bf16_bits_to_f32(bits)
+    finite = np.isfinite(xf)
+    xf = xf[finite]
+    # the largest finite bf16 times 127 overflows fp32; exactness is claimed for products fp32 can hold
+    for qv in range(-127, 128):
+        with np.errstate(over="ignore"):
+            p32 = (xf * np.float32(qv)).astype(np.float64)
+        p64 = xf.astype(np.float64) * qv
+        ok = np.abs(p64) < np.float64(np.finfo(np.float32).max)
+        assert np.array_equal(p32[ok], p64[ok]), qv
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# quantize (from_q8.rs `quantize`)
+# --------------------------------------------------------------------------------------------------------------------
+
+def test_quantize_round_trip():
+    """A weight drawn as (q, s) with one +-127 per block dequantizes to values whose Q8_0 quantization is (q, s)."""
+    _, q, s = si.case(1, 256, 48, 17)
+    w = oracle.dequantize(q[:, :48], s[:, :48])
+    got = oracle.quantize(w)
+    assert got is not None
+    assert np.array_equal(got[0], q[:, :48]) and np.array_equal(got[1], s[:, :48])
+
+
+def test_quantize_rejects_one_ulp():
+    _, q, s = si.case(1, 64, 4, 18)
+    w = oracle.dequantize(q[:, :4], s[:, :4])
+    w[5, 2] = np.nextafter(w[5, 2], np.inf)
+    assert oracle.quantize(w) is None
+
+
+def test_quantize_rejects_scale_not_fp32():
+    """amax = 1 gives d = 1/127, which fp32 does not hold: rejected even though every value is an int multiple."""
+    w = np.zeros((32, 1))
+    w[0, 0] = 1.0
+    assert oracle.quantize(w) is None
+
+
+def test_quantize_rejects_half_steps_and_keeps_zero_blocks():
+    d = 2.0 ** -10
+    w = np.zeros((64, 2))
+    w[0, 0] = 127 * d
+    w[1, 0] = 63.5 * d                 # not an int8 multiple of the block's scale
+    assert oracle.quantize(w) is None
+    w[1, 0] = -63 * d
+    q, s = oracle.quantize(w)
+    assert q[0, 0] == 127 and q[1, 0] == -63 and s[0, 0] == np.float32(d)
+    assert np.all(q[32:] == 0) and np.all(s[1] == 0) and np.all(q[:, 1] == 0) and s[0, 1] == 0   # zero blocks
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# arg-max
+# --------------------------------------------------------------------------------------------------------------------
+
+def test_argmax_first_maximum_and_pads():
+    y = np.array([[1.0, 3.0, 3.0, -1.0, 0.0, 0.0],
+                  [-5.0, -4.0, -4.5, -7.0, 0.0, 0.0],      # all real logits negative: the pads (0) must not win
+                  [0.0, -0.0, -1.0, -0.0, 0.0, 0.0]])      # +0 and -0 are equal: the first one wins
+    assert list(oracle.argmax(y, 4)) == [1, 1, 0]
+    y2 = y.copy()
+    y2[2, 0] = -0.0
+    assert oracle.argmax(y2, 4)[2] == 0
+
+
+def test_argmax_of_product_with_planted_winner():
+    x, q, s = si.case(2, 512, 200, 23)
+    y, _ = oracle.gemv(x, q, s)
+    idx = oracle.argmax(y, 200)
+    for r in range(2):
+        assert y[r, idx[r]] == y[r, :200].max()
+        assert np.all(y[r, :idx[r]] < y[r, idx[r]])
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# repack (from_q8.rs `Q8Part`)
+# --------------------------------------------------------------------------------------------------------------------
+
+def _blocks_of(q, s, N):
+    """Checkpoint blocks written field by field with struct (independent of the oracle's numpy views)."""
+    K = q.shape[0]
+    out = bytearray()
+    for n in range(N):
+        for b in range(K // 32):
+            out += struct.pack("<f", float(s[b, n]))
+            out += struct.pack("<32b", *[int(v) for v in q[32 * b:32 * b + 32, n]])
+    return bytes(out)
+
+
+def test_repack_round_trip_and_rejects_minus_128():
+    _, q, s = si.case(1, 128, 40, 29)
+    blk = _blocks_of(q, s, 40)
+    got = oracle.repack(blk, 128, 40)
+    assert np.array_equal(got[0], q) and np.array_equal(got[1], s)
+    q2 = q.copy()
+    q2[3, 7] = -128
+    assert oracle.repack(_blocks_of(q2, s, 40), 128, 40) is None
+
+
+def test_bytes_per_weight_fixture():
+    """The byte figures the pages print (used by the benchmark's algorithmic byte count)."""
+    vals = {r[0]: float(r[1]) for r in _golden_rows("bytes_per_weight.txt")}
+    assert vals["q8_bytes_per_weight"] == 1 + 4 / 32
+    assert round(vals["q8_bytes_per_weight"], 2) == 1.13 or abs(vals["q8_bytes_per_weight"] - 1.13) < 0.01
+    m, wb = 8, 2
+    assert abs(vals["view_overhead_m8_wb2"] - (m * 2) / (1.125 * 32 * wb)) < 1e-15
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# the pins catch planted slips: mutants of the oracle's C source, compiled on the CPU, must fail the brute force
+# --------------------------------------------------------------------------------------------------------------------
+
+MUTANTS = {
+    "scale dropped": ("y += sv * inner;", "y += inner;"),
+    "q transposed": ("q[(int64_t)k * Np + n]", "q[(int64_t)n * K + k]"),
+    "s transposed": ("s[(int64_t)b * Np + n]", "s[(int64_t)n * (K / ORACLE_BLOCK) + b]"),
+    "lane dropped": ("for (int i = 0; i < ORACLE_BLOCK; ++i)", "for (int i = 0; i < ORACLE_BLOCK - 1; ++i)"),
+    "bf16 decode": ("((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
+    "abs dropped": ("inner_abs += absd(xv * qv);", "inner_abs += xv * qv;"),
+    "block dropped": ("for (int b = 0; b < nblocks; ++b)", "for (int b = 1; b < nblocks; ++b)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistakes(name, tmp_path):
+    import ctypes
+    import subprocess
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "q8_oracle.c")).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    lib_path = tmp_path / "mutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", str(path), "-o", str(lib_path)])
+    lib = ctypes.CDLL(str(lib_path))
+    caught = False
+    for seed in (4, 5):
+        x, q, s = si.case(2, 64, 2, seed)
+        Np = q.shape[1]
+        y = np.empty((2, Np))
+        a = np.empty((2, Np))
+        lib.oracle_q8_gemv(ctypes.c_void_p(x.ctypes.data), ctypes.c_void_p(q.ctypes.data),
+                           ctypes.c_void_p(s.ctypes.data), 2, 64, Np, None, ctypes.c_int64(Np),
+                           ctypes.c_void_p(y.ctypes.data), ctypes.c_void_p(a.ctypes.data))
+        for r in range(2):
+            for n in range(2):
+                ey, ea = _exact(x, q, s, r, n)
+                if abs(Fraction(y[r, n]) - ey) > Fraction(2) ** -52 * ea or \
+                        abs(Fraction(a[r, n]) - ea) > Fraction(2) ** -52 * ea:
+                    caught = True
+    assert caught, f"the brute-force pin did not catch: {name}"
