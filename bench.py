@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q8_0 GEMV library on its decode-step workload; prints one JSON line.
+
+Workload (one step): the projection chain of a 32-layer 7B-class decode step over Q8_0 weights -- per layer q, k, v, o
+(4096 x 4096), gate and up (4096 x 14336) and down (14336 x 4096) -- then the tied head (4096 x 128256) with the
+arg-max over its fp32 logits fused.  224 q8_gemv calls and one q8_gemv_argmax, m activation rows each (m = 1 by
+default), 9.36 GB of weights per step at m = 1: every step reads far more than the 129 MB L2, so no flush is needed.
+Weights: q uniform int8 in [-127, 127] with a +-127 per block, s = 2^u/127, u ~ U[-8, -2], drawn on the device from a
+seed; activations bf16 N(0,1), drawn per layer.
+
+value = algorithmic bytes per step (K * Np * 1.125 + m * K * 2 + m * Np * 4 per GEMV; the head writes m * 8 index bytes
+instead of logits) / device time per step, summed over ranks (replicas: every rank runs the whole step on its own GPU).
+
+Arms:
+  --impl ours       (default) the CUDA library, the chain captured as CUDA graphs and replayed per step;
+  --impl reference  the fp64 CPU oracle on the host cores, a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q8_0 GEMV achieved HBM GB/s (% of GB300 peak) and µs/call at m=1..16"
+LAYERS = 32
+HIDDEN, FFN, VOCAB = 4096, 14336, 128256
+WORKLOAD = (f"decode-step Q8_0 projection chain: {LAYERS} layers x (q,k,v,o 4096x4096; gate,up 4096x14336; "
+            f"down 14336x4096) + tied head 4096x128256 with fused arg-max")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def layer_shapes():
+    return [(HIDDEN, HIDDEN)] * 4 + [(HIDDEN, FFN)] * 2 + [(FFN, HIDDEN)]
+
+
+def chain_shapes():
+    return [shape for _ in range(LAYERS) for shape in layer_shapes()]
+
+
+def padded(n):
+    return -(-n // 32) * 32
+
+
+def gemv_bytes(m, K, N, argmax=False):
+    """Algorithmic bytes of one call: the Q8_0 weight (1 byte a value + 4 bytes a 32-value block: 1.125 a weight,
+    "from_q8.rs" module doc), the bf16 activations and the fp32 outputs (the arg-max's int64 indices instead)."""
+    Np = padded(N)
+    return K * Np * 1.125 + m * K * 2 + (m * 8 if argmax else m * Np * 4)
+
+
+def step_bytes(m):
+    return sum(gemv_bytes(m, K, N) for K, N in chain_shapes()) + gemv_bytes(m, HIDDEN, VOCAB, argmax=True)
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "q8_block_quantized_gemv_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        import torch
+        self.index = str(device)
+        try:
+            self.index = f"GPU-{torch.cuda.get_device_properties(device).uuid}"
+        except Exception:
+            pass
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        mhz, maxmhz, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                mhz.append(float(parts[0]))
+                maxmhz.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxmhz), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------------------------------------------------
+# the reference arm and the CPU baseline: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------------------------------------------------
+
+def oracle_sample(m, budget_s, weights=None):
+    """Time the oracle on the chain's GEMVs in step order until `budget_s` seconds of oracle time have run.
+
+    weights: optional callable i -> (x, q, s) host arrays for GEMV i of the chain (the device's inputs copied
+    back); host draws from the seeded generator otherwise.  Returns (GB/s, description, threads)."""
+    import oracle
+    import synth_inputs as si
+    shapes = chain_shapes() + [(HIDDEN, VOCAB)]
+    spent, nbytes, done = 0.0, 0.0, 0
+    for i, (K, N) in enumerate(shapes):
+        if weights is not None:
+            x, q, s = weights(i)
+        else:
+            x, q, s = si.case(m, K, N, si.case_seed(4, m, i))
+        t0 = time.perf_counter()
+        y, _ = oracle.gemv(x, q, s)
+        if i == len(shapes) - 1:
+            oracle.argmax(y, N)
+        spent += time.perf_counter() - t0
+        nbytes += gemv_bytes(m, K, N, argmax=(i == len(shapes) - 1))
+        done += 1
+        if spent >= budget_s:
+            break
+    desc = f"first {done} of {len(shapes)} GEMVs of one step in chain order (m={m}), {spent:.1f} s of oracle time"
+    return nbytes / spent / 1e9, desc, oracle.threads(), spent
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    import synth_inputs as si
+    # one bounded sample per step: the first layer's seven GEMVs (host draws, prepared before the clock)
+    shapes = layer_shapes()
+    cases = [si.case(args.m, K, N, si.case_seed(4, args.m, i)) for i, (K, N) in enumerate(shapes)]
+    per_step = sum(gemv_bytes(args.m, K, N) for K, N in shapes)
+
+    def one_step():
+        for x, q, s in cases:
+            oracle.gemv(x, q, s)
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = per_step / dt / 1e9
+    sample = f"one layer's 7 GEMVs (4 x 4096x4096, 2 x 4096x14336, 14336x4096) per step, m={args.m}"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "m": args.m, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------------------------------------
+
+class Chain:
+    """Device-resident weights, activations and outputs of one decode step, and its CUDA graphs."""
+
+    def __init__(self, torch, m, seed=4000):
+        import synth_inputs as si
+        self.torch, self.m = torch, m
+        self.shapes = chain_shapes()
+        self.w = [si.device_weight(K, N, seed + i) for i, (K, N) in enumerate(self.shapes)]
+        self.head = si.device_weight(HIDDEN, VOCAB, seed + len(self.shapes))
+        # activations: one [m, K] block per call, all in one buffer (the H2D copy of the end-to-end measurement)
+        sizes = [m * K for K, _ in self.shapes] + [m * HIDDEN]
+        self.x_all = torch.empty(sum(sizes), dtype=torch.bfloat16, device="cuda")
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed + 99991)
+        self.x_all.copy_(torch.randn(sum(sizes), generator=g, device="cuda", dtype=torch.float32))
+        self.x, off = [], 0
+        for K, _ in self.shapes + [(HIDDEN, VOCAB)]:
+            self.x.append(self.x_all[off:off + m * K].view(m, K))
+            off += m * K
+        self.y = [torch.empty((m, padded(N)), dtype=torch.float32, device="cuda") for _, N in self.shapes]
+        self.idx = torch.empty((m,), dtype=torch.int64, device="cuda")
+        self.g_layers = self.g_head = None
+
+    def run_layers(self):
+        import q8_block_quantized_gemv_gb300 as q8
+        for i, (K, N) in enumerate(self.shapes):
+            q, s = self.w[i]
+            q8.gemv(self.x[i], q, s, N, y=self.y[i])
+
+    def run_head(self):
+        import q8_block_quantized_gemv_gb300 as q8
+        q, s = self.head
+        q8.gemv_argmax(self.x[-1], q, s, VOCAB, idx=self.idx)
+
+    def capture(self):
+        torch = self.torch
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            self.run_layers()
+            self.run_head()
+        torch.cuda.current_stream().wait_stream(stream)
+        torch.cuda.synchronize()
+        self.g_layers, self.g_head = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_layers):
+            self.run_layers()
+        with torch.cuda.graph(self.g_head):
+            self.run_head()
+        torch.cuda.synchronize()
+
+    def launches_per_step(self):
+        return len(self.shapes) + 2  # 224 GEMV kernels, the head's GEMV kernel and its index decode
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from q8_block_quantized_gemv_gb300 import build
+    build.build()
+    torch.cuda.set_device(local_rank)
+    m = args.m
+    chain = Chain(torch, m)
+    chain.capture()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        chain.g_layers.replay()
+        chain.g_head.replay()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: inputs resident, K steps of graph replay ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            chain.g_layers.replay()
+            ev[i][1].record(stream)
+            chain.g_head.replay()
+            ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = start.elapsed_time(end) / args.steps
+    layers_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    head_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ms = max_over_ranks(ms)
+    bytes_step = step_bytes(m)
+    value = world * bytes_step / (ms * 1e-3) / 1e9
+
+    # ---- end-to-end: host activations in, the step's tokens out, every step ----
+    x_host = torch.empty(chain.x_all.shape, dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(chain.x_all.cpu())
+    idx_host = torch.empty((m,), dtype=torch.int64, pin_memory=True)
+    for _ in range(2):
+        chain.x_all.copy_(x_host, non_blocking=True)
+        chain.g_layers.replay()
+        chain.g_head.replay()
+        idx_host.copy_(chain.idx, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        chain.x_all.copy_(x_host, non_blocking=True)
+        chain.g_layers.replay()
+        chain.g_head.replay()
+        idx_host.copy_(chain.idx, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    barrier()
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    layer_bytes = sum(gemv_bytes(m, K, N) for K, N in chain.shapes)
+    achieved = layer_bytes / (layers_ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+        if rec.get("source_hash") == source_hash() and rec.get("m") == m:
+            traffic = rec.get("traffic_bytes_per_step_layers")
+    except (OSError, ValueError):
+        pass
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "m": m, "calls_per_step": len(chain.shapes) + 1,
+                   "bytes_per_step": bytes_step, "us_per_call": ms * 1e3 / (len(chain.shapes) + 1),
+                   "pct_of_8TBps": 100.0 * bytes_step / (ms * 1e-3) / 8e12,
+                   "layers_ms": layers_ms, "head_ms": head_ms,
+                   "operands": "x bf16, W Q8_0 (int8 + fp32 scale per 32 rows), fp32 accumulation",
+                   "l2": "inputs larger than L2 (9.4 GB of weights per step against 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "q8_gemv (the 224 layer GEMVs of a step, back to back)",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic},
+        "e2e": {"value": world * bytes_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": chain.x_all.numel() * 2, "d2h_bytes_per_step": m * 8},
+        "gpu_launches": chain.launches_per_step() * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        def host_case(i):
+            if i < len(chain.shapes):
+                q, s = chain.w[i]
+            else:
+                q, s = chain.head
+            return (chain.x[i].view(torch.int16).cpu().numpy().view("uint16"), q.cpu().numpy(), s.cpu().numpy())
+        gbs, desc, cores, _ = oracle_sample(m, args.cpu_budget, host_case)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--m", type=int, default=1, help="activation rows per call (1..16)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if not 1 <= args.m <= 16:
+        ap.error("m must be in 1..16")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

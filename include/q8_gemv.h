@@ -1,0 +1,122 @@
+/*
+ * q8_gemv.h -- C ABI of the GB300 Q8_0 block-quantized GEMV library (libq8gemv.so).
+ *
+ * The product (source: "logicaffeine_compile/spatial/passes/from_q8.rs", module doc):
+ *
+ *     y[r, n] = sum_b s[b, n] * sum_{i<32} x[r, 32b + i] * q[32b + i, n]        r < m, n < N
+ *
+ * over a weight stored Q8_0: int8 values q (`W__q8`, K x N) and one fp32 scale per 32-row block of each column
+ * (`W__q8_scale`, K/32 x N), about 1.125 bytes a weight against 2 for bf16.  Activations x are bf16, accumulation is
+ * fp32, and a batch of m <= 16 rows reads the weight once for all its rows.
+ *
+ * Layouts (all row-major, no strides):
+ *   x  bf16    [m][K]        row pitch K elements
+ *   q  int8    [K][Np]       row pitch Np bytes; Np = q8_padded_n(N) = N rounded up to a multiple of 32
+ *   s  fp32    [K/32][Np]    row pitch Np elements
+ *   y  fp32    [m][Np]       row pitch Np elements
+ * Columns N .. Np-1 are the zero-padded last 32-column tile ("from_q8.rs", `q8_gemv_applies`): their q and s should
+ * be 0 (q8_repack and q8_quantize write them so); the GEMV writes exactly 0.0f into y's pad columns regardless.
+ *
+ * Conventions shared by every entry point:
+ *   - The caller owns every buffer; the library keeps no state and allocates no memory.
+ *   - Device entry points take device pointers and enqueue work on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  They are asynchronous: Q8_OK means the work was enqueued.  An argument error is returned
+ *     before anything is enqueued.  A CUDA error at launch returns Q8_ERR_CUDA; q8_last_cuda_error() then gives the
+ *     cudaError_t value for the calling thread.
+ *   - Host entry points take host pointers and run synchronously on the calling thread.
+ *   - No entry point aborts, throws or prints.
+ *   - Every call is thread-safe; calls on one stream run in order.
+ */
+#ifndef Q8_GEMV_H
+#define Q8_GEMV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-identical to cudaStream_t; declared here so that the header needs no CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *q8_stream_t;
+
+/* Rows of a Q8_0 block ("from_q8.rs", `Q8_BLOCK`). */
+#define Q8_BLOCK 32
+/* The most activation rows one call takes ("plan.rs", `GEMV_ROWS`: a GEMV launch multiplies at most 16 rows). */
+#define Q8_MAX_ROWS 16
+
+typedef enum {
+    Q8_OK = 0,
+    Q8_ERR_ARG = 1,      /* a required pointer is NULL, or an enum argument is out of range */
+    Q8_ERR_SHAPE = 2,    /* m outside 1..16, K <= 0, K % 32 != 0, N <= 0, or a size that overflows */
+    Q8_ERR_ALIGN = 3,    /* a device pointer is not 16-byte aligned */
+    Q8_ERR_NOT_Q8_0 = 4, /* a weight or block that is not Q8_0 (see q8_quantize, q8_repack) */
+    Q8_ERR_CUDA = 5      /* the CUDA runtime reported an error; see q8_last_cuda_error() */
+} q8_status;
+
+/* Kernel family selector for q8_gemv_ex (benchmarking and testing; q8_gemv picks by m). */
+typedef enum {
+    Q8_VARIANT_AUTO = 0,
+    Q8_VARIANT_SIMT = 1, /* CUDA-core fp32 FMA, m-row accumulators per thread */
+    Q8_VARIANT_MMA = 2   /* int8 -> bf16 exact dequant in registers, bf16 tensor-core MMA, fp32 per-block scale fold */
+} q8_variant;
+
+/* N rounded up to whole 32-column tiles ("from_q8.rs", `q8_gemv_applies`: the last tile is zero-padded).
+ * Returns -1 when N <= 0 or the result would overflow an int. */
+int q8_padded_n(int N);
+
+/* y = x . W over the Q8_0 weight (q, s), m rows (source: "from_q8.rs", module doc and `q8_fold`).
+ *   x  device, bf16 [m][K], 16-byte aligned        q  device, int8 [K][Np], 16-byte aligned
+ *   s  device, fp32 [K/32][Np], 16-byte aligned    y  device, fp32 [m][Np] (written), 16-byte aligned
+ *   1 <= m <= 16, K > 0, K % 32 == 0 ("from_q8.rs", `q8_gemv_applies`), N > 0.
+ * y must not overlap x, q or s.  Every output n < Np is written; outputs n >= N are 0.0f.
+ * Each y[r, n] equals the real-number product within 1e-5 * sum_b |s[b,n]| sum_i |x[r,32b+i] q[32b+i,n]|; the
+ * summation order is fixed for a given (m, K, N) and device, so repeated calls give identical bits. */
+q8_status q8_gemv(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N, q8_stream_t stream);
+
+/* q8_gemv with an explicit kernel family (q8_variant).  Same arguments, results within the same bound. */
+q8_status q8_gemv_ex(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N, int variant,
+                     q8_stream_t stream);
+
+/* The product followed by the arg-max that closes a decode step (source: "plan.rs", `Launch::ArgMax`, and
+ * "int8_model.rs", `decode_step_lg`: the index of the first maximal logit; its CUDA arg-max sends equal values to the
+ * lower index).
+ *   idx     device, int64 [m] (written), 8-byte aligned: idx[r] = the smallest n < N with y[r, n] equal to the
+ *           largest y[r, n'] over n' < N, 0-based.  Pad columns never take part.  +0.0 and -0.0 count as equal.
+ *           The buffer also serves as the call's cross-block scratch: its contents before the call do not matter.
+ *   logits  device, fp32 [m][Np] (written, as q8_gemv's y) or NULL to skip storing the logits.
+ * Other arguments as q8_gemv.  Logits that are NaN order above +inf (not reached for finite inputs). */
+q8_status q8_gemv_argmax(const void *x, const int8_t *q, const float *s, int64_t *idx, float *logits, int m, int K,
+                         int N, q8_stream_t stream);
+
+/* Host repack of checkpoint blocks into the two stored tensors (source: "from_q8.rs", `Q8Part`: the host repacks the
+ * checkpoint's blocks into the int8 values `q8_0.values` and the fp32 scales `q8_0.scales`).
+ *   blocks  host, N * (K/32) blocks of 36 bytes, column-major by block: column n's blocks b = 0 .. K/32-1 in order;
+ *           each block is a little-endian fp32 scale d followed by 32 int8 values (rows 32b .. 32b+31).
+ *   q       host, int8 [K][Np] (written, pad columns 0)     s  host, fp32 [K/32][Np] (written, pad columns 0)
+ * Returns Q8_ERR_NOT_Q8_0 when a value is -128 (outside the Q8_0 range |q| <= 127) or a scale is not finite; q and s
+ * are then left partly written. */
+q8_status q8_repack(const void *blocks, int K, int N, int8_t *q, float *s);
+
+/* Host Q8_0 quantization of a declared weight (source: "from_q8.rs", `quantize`).
+ *   w  host, fp64 [K][N] row-major (the declared values, as the pages' rule takes them)
+ *   q  host, int8 [K][Np] (written, pad columns 0)     s  host, fp32 [K/32][Np] (written, pad columns 0)
+ * For every 32-row block and column: amax = max |w|; an all-zero block gets q = 0 and s = 0; otherwise
+ * d = amax / 127 (in fp64) must be exactly an fp32 value, and every w / d must lie within 1e-9 of an integer r with
+ * |r| <= 127 and r * d == w exactly.  Any failure returns Q8_ERR_NOT_Q8_0 (q and s then hold no meaning). */
+q8_status q8_quantize(const double *w, int K, int N, int8_t *q, float *s);
+
+/* A static, human-readable name for a status code. */
+const char *q8_status_string(q8_status status);
+
+/* The cudaError_t of the last CUDA failure on the calling thread (0 when none). */
+int q8_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int q8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8_GEMV_H */

@@ -162,7 +162,7 @@ def repack(blocks: bytes | np.ndarray, K: int, N: int):
 
     The blocks are column-major by block: column n's K/32 blocks one after another, each 36 bytes, a little-endian
     fp32 scale d followed by 32 int8 values.  Pad columns come out zero.  Returns None when a value is -128 (outside
-    the Q8_0 range |q| <= 127).
+    the Q8_0 range |q| <= 127) or a scale is not finite.
     """
     if K <= 0 or K % Q8_BLOCK or N <= 0:
         return None
@@ -173,7 +173,7 @@ def repack(blocks: bytes | np.ndarray, K: int, N: int):
     rec = raw.reshape(N, nb, 36)
     d = rec[:, :, 0:4].copy().view("<f4").reshape(N, nb)
     vals = rec[:, :, 4:36].copy().view(np.int8).reshape(N, nb, Q8_BLOCK)
-    if np.any(vals == -128):
+    if np.any(vals == -128) or not np.all(np.isfinite(d)):
         return None
     Np = padded_n(N)
     q = np.zeros((K, Np), dtype=np.int8)

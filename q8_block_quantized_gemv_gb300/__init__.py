@@ -1,0 +1,170 @@
+"""Python binding of libq8gemv, the GB300 Q8_0 block-quantized GEMV library.
+
+Argument marshalling only: every step of the product runs in the library's CUDA kernels (device entry points) or its
+C++ host code (repack, quantize).  PyTorch supplies device memory and streams.  The names follow the C ABI in
+``include/q8_gemv.h``:
+
+* :func:`gemv` -- ``q8_gemv`` / ``q8_gemv_ex``: y[r, n] = sum_b s[b, n] sum_i x[r, 32b+i] q[32b+i, n]
+  ("from_q8.rs", module doc), bf16 x [m, K], int8 q [K, Np], fp32 s [K/32, Np] -> fp32 y [m, Np];
+* :func:`gemv_argmax` -- ``q8_gemv_argmax``: the product and the first-maximum arg-max that closes a decode step;
+* :func:`repack` -- ``q8_repack``: 36-byte checkpoint blocks -> (q, s) on the host;
+* :func:`quantize` -- ``q8_quantize``: the Q8_0 rule of "from_q8.rs" ``quantize`` on the host.
+
+The library must have been built (``python -m q8_block_quantized_gemv_gb300.build``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB as _LIB_PATH
+
+Q8_BLOCK = 32
+MAX_ROWS = 16
+VARIANTS = {"auto": 0, "simt": 1, "mma": 2}
+
+_STATUS = {0: "Q8_OK", 1: "Q8_ERR_ARG", 2: "Q8_ERR_SHAPE", 3: "Q8_ERR_ALIGN", 4: "Q8_ERR_NOT_Q8_0", 5: "Q8_ERR_CUDA"}
+
+# Every symbol include/q8_gemv.h declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = {
+    "q8_padded_n": (_I, [_I]),
+    "q8_gemv": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "q8_gemv_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "q8_gemv_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "q8_repack": (_I, [_P, _I, _I, _P, _P]),
+    "q8_quantize": (_I, [_P, _I, _I, _P, _P]),
+    "q8_status_string": (ctypes.c_char_p, [_I]),
+    "q8_last_cuda_error": (_I, []),
+    "q8_version": (_I, []),
+}
+
+_lib = None
+
+
+class Q8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        detail = lib().q8_status_string(status).decode()
+        if status == 5:
+            detail += f" (cudaError {lib().q8_last_cuda_error()})"
+        super().__init__(f"{where}: {_STATUS.get(status, status)}: {detail}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises when it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libq8gemv is not built ({_LIB_PATH} missing); run "
+                               "`python -m q8_block_quantized_gemv_gb300.build`")
+        handle = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise Q8Error(status, where)
+
+
+def padded_n(N: int) -> int:
+    return lib().q8_padded_n(N)
+
+
+def status_string(status: int) -> str:
+    return lib().q8_status_string(status).decode()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_operands(x, q, s, N):
+    import torch
+    if not (x.is_cuda and q.is_cuda and s.is_cuda):
+        raise ValueError("x, q and s must be CUDA tensors")
+    if x.dtype != torch.bfloat16 or q.dtype != torch.int8 or s.dtype != torch.float32:
+        raise TypeError("x must be bfloat16, q int8 and s float32")
+    if not (x.is_contiguous() and q.is_contiguous() and s.is_contiguous()):
+        raise ValueError("x, q and s must be contiguous")
+    if x.dim() != 2 or q.dim() != 2 or s.dim() != 2:
+        raise ValueError("x, q and s must be 2-D")
+    m, K = x.shape
+    Np = padded_n(N) if N > 0 else -1
+    if q.shape != (K, Np) or s.shape != (K // Q8_BLOCK, Np):
+        raise ValueError(f"q must be [K, Np] = [{K}, {Np}] and s [K/32, Np]; got {tuple(q.shape)}, {tuple(s.shape)}")
+    return m, K, Np
+
+
+def gemv(x, q, s, N: int, y=None, variant: str = "auto", stream=None):
+    """y = x . W over the Q8_0 weight (q, s); returns y, fp32 [m, Np] (columns N .. Np-1 are 0)."""
+    import torch
+    m, K, Np = _check_operands(x, q, s, N)
+    if y is None:
+        y = torch.empty((m, Np), dtype=torch.float32, device=x.device)
+    elif y.dtype != torch.float32 or y.shape != (m, Np) or not y.is_contiguous() or not y.is_cuda:
+        raise ValueError("y must be a contiguous fp32 CUDA tensor [m, Np]")
+    _check(lib().q8_gemv_ex(x.data_ptr(), q.data_ptr(), s.data_ptr(), y.data_ptr(), m, K, N, VARIANTS[variant],
+                            _stream_handle(stream)), "q8_gemv")
+    return y
+
+
+def gemv_argmax(x, q, s, N: int, idx=None, logits=None, stream=None):
+    """The product and its first-maximum arg-max per row: returns idx, int64 [m] (0-based).
+
+    ``logits``: None (not stored) or a contiguous fp32 [m, Np] CUDA tensor that receives y.
+    """
+    import torch
+    m, K, Np = _check_operands(x, q, s, N)
+    if idx is None:
+        idx = torch.empty((m,), dtype=torch.int64, device=x.device)
+    elif idx.dtype != torch.int64 or idx.numel() < m or not idx.is_contiguous() or not idx.is_cuda:
+        raise ValueError("idx must be a contiguous int64 CUDA tensor of m elements")
+    lp = None
+    if logits is not None:
+        if logits.dtype != torch.float32 or logits.shape != (m, Np) or not logits.is_contiguous():
+            raise ValueError("logits must be a contiguous fp32 CUDA tensor [m, Np]")
+        lp = logits.data_ptr()
+    _check(lib().q8_gemv_argmax(x.data_ptr(), q.data_ptr(), s.data_ptr(), idx.data_ptr(), lp, m, K, N,
+                                _stream_handle(stream)), "q8_gemv_argmax")
+    return idx
+
+
+def repack(blocks, K: int, N: int):
+    """(q int8 [K, Np], s fp32 [K/32, Np]) from N * K/32 checkpoint blocks of 36 bytes (host)."""
+    raw = np.frombuffer(bytes(blocks), dtype=np.uint8) if not isinstance(blocks, np.ndarray) else \
+        np.ascontiguousarray(blocks).view(np.uint8).reshape(-1)
+    Np = padded_n(N) if N > 0 else 1
+    nb = max(K // Q8_BLOCK, 1)
+    if K > 0 and N > 0 and raw.size != N * nb * 36:
+        raise ValueError("block buffer size does not match K and N")
+    q = np.empty((max(K, 1), Np), dtype=np.int8)
+    s = np.empty((nb, Np), dtype=np.float32)
+    _check(lib().q8_repack(raw.ctypes.data, K, N, q.ctypes.data, s.ctypes.data), "q8_repack")
+    return q, s
+
+
+def quantize(w):
+    """(q int8 [K, Np], s fp32 [K/32, Np]) for a declared fp64 weight [K, N] (host); raises Q8Error if not Q8_0."""
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    K, N = w.shape
+    Np = padded_n(N) if N > 0 else 1
+    q = np.empty((max(K, 1), Np), dtype=np.int8)
+    s = np.empty((max(K // Q8_BLOCK, 1), Np), dtype=np.float32)
+    _check(lib().q8_quantize(w.ctypes.data, K, N, q.ctypes.data, s.ctypes.data), "q8_quantize")
+    return q, s

@@ -1,0 +1,162 @@
+// Device entry points of libq8gemv: argument checks, the launch plan, and the arg-max finish.
+#include <stdint.h>
+
+#include <atomic>
+
+#include "../../include/q8_gemv.h"
+#include "q8_launch.h"
+
+namespace q8 {
+void set_last_cuda_error(int e);  // q8_host.cpp
+}
+
+using q8::Args;
+
+namespace {
+
+q8_status cuda_fail(cudaError_t e) {
+    q8::set_last_cuda_error((int)e);
+    return Q8_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// SM count of the current device, cached per device (a read-only property).
+int sm_count(int *out) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *out = c;
+            return 0;
+        }
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    *out = n;
+    return 0;
+}
+
+struct Plan {
+    int variant;  // Q8_VARIANT_SIMT or Q8_VARIANT_MMA
+    int V;        // columns per lane
+    int ksplit;   // CTAs of a cluster splitting K
+};
+
+// Kernel family, per-lane width and K split for a shape.  The widest tile that still gives every SM a CTA is
+// preferred; K is split across a cluster (at most 8 CTAs, the portable size) until the grid holds about two CTAs per
+// SM, the residency the kernels are built for.
+Plan make_plan(int m, int K, int Np, int variant, int sms) {
+    if (variant == Q8_VARIANT_AUTO) variant = m <= 2 ? Q8_VARIANT_SIMT : Q8_VARIANT_MMA;
+    if (variant == Q8_VARIANT_SIMT && !q8::simt_has(m, 4)) variant = Q8_VARIANT_MMA;
+    static const int widths[3] = {16, 8, 4};
+    const int nb = K / Q8_BLOCK;
+    Plan best = {variant, 0, 1};
+    for (int i = 0; i < 3; ++i) {
+        const int V = widths[i];
+        const bool has = variant == Q8_VARIANT_SIMT ? q8::simt_has(m, V) : q8::mma_has(m, V);
+        if (!has) continue;
+        const int TC = variant == Q8_VARIANT_SIMT ? q8::simt_tile(V) : q8::mma_tile(V);
+        const long long tiles = (Np + TC - 1) / TC;
+        long long ks = (2LL * sms + tiles - 1) / tiles;
+        if (ks > 8) ks = 8;
+        if (ks > nb) ks = nb;
+        if (ks < 1) ks = 1;
+        best.V = V;
+        best.ksplit = (int)ks;
+        if (tiles * ks >= sms) break;
+    }
+    return best;
+}
+
+q8_status check_gemv_args(const void *x, const int8_t *q, const float *s, int m, int K, int N) {
+    if (!x || !q || !s) return Q8_ERR_ARG;
+    if (m < 1 || m > Q8_MAX_ROWS || K <= 0 || K % Q8_BLOCK != 0 || N <= 0) return Q8_ERR_SHAPE;
+    if (q8_padded_n(N) < 0) return Q8_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(s, 16)) return Q8_ERR_ALIGN;
+    return Q8_OK;
+}
+
+q8_status run(const Args &a, int variant, bool argmax, cudaStream_t stream) {
+    int sms = 0;
+    int e = sm_count(&sms);
+    if (e != 0) return cuda_fail((cudaError_t)e);
+    const Plan p = make_plan(a.m, a.K, a.Np, variant, sms);
+    Args b = a;
+    b.ksplit = p.ksplit;
+    cudaError_t ce = p.variant == Q8_VARIANT_SIMT ? q8::launch_simt(b, p.V, argmax, stream)
+                                                  : q8::launch_mma(b, p.V, argmax, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    return Q8_OK;
+}
+
+// keys[r] (the packed maximum written by the GEMV) -> the 0-based index it encodes, in place.
+__global__ void argmax_decode(int64_t *idx, int m) {
+    const int r = threadIdx.x;
+    if (r < m) {
+        const unsigned long long key = (unsigned long long)idx[r];
+        idx[r] = (int64_t)(0xFFFFFFFFull - (key & 0xFFFFFFFFull));
+    }
+}
+
+}  // namespace
+
+extern "C" q8_status q8_gemv_ex(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N,
+                                int variant, q8_stream_t stream) {
+    q8_status st = check_gemv_args(x, q, s, m, K, N);
+    if (st != Q8_OK) return st;
+    if (!y) return Q8_ERR_ARG;
+    if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_MMA) return Q8_ERR_ARG;
+    if (!aligned(y, 16)) return Q8_ERR_ALIGN;
+    const int Np = q8_padded_n(N);
+    const size_t ybytes = (size_t)m * Np * 4;
+    if (overlaps(y, ybytes, x, (size_t)m * K * 2) || overlaps(y, ybytes, q, (size_t)K * Np) ||
+        overlaps(y, ybytes, s, (size_t)(K / Q8_BLOCK) * Np * 4))
+        return Q8_ERR_ARG;
+    Args a = {static_cast<const uint16_t *>(x), q, s, y, nullptr, m, K, N, Np, K / Q8_BLOCK, 1};
+    return run(a, variant, false, (cudaStream_t)stream);
+}
+
+extern "C" q8_status q8_gemv(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N,
+                             q8_stream_t stream) {
+    return q8_gemv_ex(x, q, s, y, m, K, N, Q8_VARIANT_AUTO, stream);
+}
+
+extern "C" q8_status q8_gemv_argmax(const void *x, const int8_t *q, const float *s, int64_t *idx, float *logits,
+                                    int m, int K, int N, q8_stream_t stream) {
+    q8_status st = check_gemv_args(x, q, s, m, K, N);
+    if (st != Q8_OK) return st;
+    if (!idx) return Q8_ERR_ARG;
+    if (!aligned(idx, 8) || (logits && !aligned(logits, 16))) return Q8_ERR_ALIGN;
+    const int Np = q8_padded_n(N);
+    if (logits) {
+        const size_t ybytes = (size_t)m * Np * 4;
+        if (overlaps(logits, ybytes, x, (size_t)m * K * 2) || overlaps(logits, ybytes, q, (size_t)K * Np) ||
+            overlaps(logits, ybytes, s, (size_t)(K / Q8_BLOCK) * Np * 4) || overlaps(logits, ybytes, idx, m * 8))
+            return Q8_ERR_ARG;
+    }
+    cudaStream_t cs = (cudaStream_t)stream;
+    cudaError_t ce = cudaMemsetAsync(idx, 0, (size_t)m * sizeof(int64_t), cs);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    Args a = {static_cast<const uint16_t *>(x), q, s, logits, reinterpret_cast<unsigned long long *>(idx),
+              m, K, N, Np, K / Q8_BLOCK, 1};
+    st = run(a, Q8_VARIANT_AUTO, true, cs);
+    if (st != Q8_OK) return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(32, 1, 1);
+    cfg.stream = cs;
+    ce = cudaLaunchKernelEx(&cfg, argmax_decode, idx, m);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    return Q8_OK;
+}

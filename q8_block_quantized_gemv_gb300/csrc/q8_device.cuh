@@ -1,0 +1,177 @@
+// Device building blocks shared by the Q8_0 GEMV kernels (sm_103a).
+//
+// The product, from "logicaffeine_compile/spatial/passes/from_q8.rs" (module doc and `q8_fold`):
+//     y[r, n] = sum_b s[b, n] * sum_{i<32} x[r, 32b + i] * q[32b + i, n]
+// with bf16 activations, int8 values, one fp32 scale per 32-row block and column, and fp32 accumulation.
+//
+// Work decomposition used by every kernel here:
+//   - a CTA owns one tile of TC output columns for all m rows and a contiguous range of the K/32 blocks;
+//   - its 8 warps split that range again, each streaming whole 32-row blocks of its columns;
+//   - per block, the 32 lane products are summed first and then multiplied by the block's scale, as the formula
+//     groups them, and added into an fp32 carry that starts at zero;
+//   - the warps' carries are summed in shared memory in warp order, then, when K is split across the CTAs of a
+//     thread-block cluster (N too narrow to fill the SMs: "plan.rs", `split_counts`, k cut to give the chip's blocks
+//     work), each CTA sums one slice of the columns over the cluster's ranks through distributed shared memory, in
+//     rank order.  Every sum has a fixed order, so results are bit-reproducible and need no scratch memory.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q8 {
+
+constexpr int kBlock = 32;   // rows of a Q8_0 block
+constexpr int kWarps = 8;    // warps per CTA
+constexpr int kThreads = 32 * kWarps;
+
+struct Args {
+    const uint16_t *x;         // bf16 bit patterns [m][K]
+    const int8_t *q;           // [K][Np]
+    const float *s;            // [K/32][Np]
+    float *y;                  // [m][Np], or null (arg-max without logits)
+    unsigned long long *keys;  // [m] packed arg-max keys, or null
+    int m, K, N, Np, nb;       // nb = K / 32
+    int ksplit;                // CTAs of a cluster splitting K (grid.y)
+};
+
+// ------------------------------------------------------------------------------------------------------------------
+// loads
+// ------------------------------------------------------------------------------------------------------------------
+
+template <int BYTES> struct Vec;
+template <> struct Vec<4> { using T = uint32_t; };
+template <> struct Vec<8> { using T = uint2; };
+template <> struct Vec<16> { using T = uint4; };
+
+__device__ __forceinline__ uint32_t word_of(const uint32_t &v, int) { return v; }
+__device__ __forceinline__ uint32_t word_of(const uint2 &v, int i) { return i == 0 ? v.x : v.y; }
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// The weight is read exactly once per call: bypass L1 (the data has no reuse inside an SM).
+__device__ __forceinline__ void ld_stream(uint32_t &v, const void *p) {
+    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(uint2 &v, const void *p) {
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(uint4 &v, const void *p) {
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+}
+
+// ------------------------------------------------------------------------------------------------------------------
+// exact conversions
+// ------------------------------------------------------------------------------------------------------------------
+
+// int8 -> fp32, exactly.  `u` is four int8 values with their sign bits flipped (x ^ 0x80808080), so byte e holds
+// q + 128 in 0..255.  Placing that byte in the low mantissa of 2^23 gives the float 2^23 + q + 128 (the mantissa's
+// unit is 1 at this exponent); subtracting 2^23 + 128, an exact difference of two floats in [2^23, 2^24), gives q.
+__device__ __forceinline__ float q8_to_f32(uint32_t u, int e) {
+    return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u | (uint32_t)e)) - 8388736.0f;
+}
+
+// bf16 -> fp32 of the low or high half of a 32-bit pair: bf16 is the top half of an fp32.
+__device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
+
+// Two small integers (|v| <= 127, at most 8 significant bits) as a bf16 pair, exactly: lo in the low half.
+__device__ __forceinline__ uint32_t bf16x2_exact(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// ------------------------------------------------------------------------------------------------------------------
+// arg-max keys
+// ------------------------------------------------------------------------------------------------------------------
+
+// A 64-bit key whose unsigned order is (logit, then lower index first): the logit's bits made order-preserving in
+// the high word (-0.0 counted as +0.0), 0xFFFFFFFF - n in the low word.  Every real key is nonzero, so 0 is the
+// identity of the max.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int n) {
+    uint32_t b = (v == 0.0f) ? 0u : __float_as_uint(v);
+    const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)n);
+}
+
+// ------------------------------------------------------------------------------------------------------------------
+// work ranges
+// ------------------------------------------------------------------------------------------------------------------
+
+// Blocks [b0, b1) this warp streams: the CTA's share of the K/32 blocks (rank blockIdx.y of ksplit), then the warp's
+// share of that.
+__device__ __forceinline__ void warp_blocks(const Args &a, int warp, int &b0, int &b1) {
+    const int rank = blockIdx.y;
+    const int c0 = (int)((long long)a.nb * rank / a.ksplit);
+    const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
+    b0 = c0 + (c1 - c0) * warp / kWarps;
+    b1 = c0 + (c1 - c0) * (warp + 1) / kWarps;
+}
+
+// Shared-memory bytes of the epilogue for MR rows and TC columns.
+__host__ __device__ constexpr int finish_smem_bytes(int MR, int TC) {
+    return (kWarps * MR * TC + MR * TC) * 4 + MR * 8;
+}
+
+// The epilogue.  On entry every warp has written its carry into red[warp][row][column] (rows < MR, columns < TC of
+// this CTA's tile) and the CTA has synchronised.  Sums the warps in order, then (ksplit > 1) the cluster's ranks in
+// order, writes y (0 in the pad columns) and folds this CTA's columns into the per-row arg-max keys.
+template <int MR, int TC, bool ARGMAX>
+__device__ __forceinline__ void finish(const Args &a, float *smem) {
+    namespace cg = cooperative_groups;
+    float *red = smem;                                                        // [kWarps][MR][TC]
+    float *part = red + kWarps * MR * TC;                                     // [MR][TC]
+    unsigned long long *rowkey = reinterpret_cast<unsigned long long *>(part + MR * TC);  // [MR]
+    const int rows = a.m < MR ? a.m : MR;
+    const int tile = blockIdx.x;
+
+    for (int i = threadIdx.x; i < rows * TC; i += kThreads) {
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += red[w * MR * TC + i];
+        part[i] = v;
+    }
+    if (ARGMAX)
+        for (int r = threadIdx.x; r < MR; r += kThreads) rowkey[r] = 0ull;
+
+    const int ks = a.ksplit;
+    if (ks > 1)
+        cg::this_cluster().sync();
+    else
+        __syncthreads();
+
+    const int rank = blockIdx.y;
+    const int c0 = ks > 1 ? TC * rank / ks : 0;
+    const int c1 = ks > 1 ? TC * (rank + 1) / ks : TC;
+    const int width = c1 - c0;
+    for (int i = threadIdx.x; i < rows * width; i += kThreads) {
+        const int r = i / width;
+        const int c = c0 + (i - r * width);
+        float v;
+        if (ks > 1) {
+            cg::cluster_group cluster = cg::this_cluster();
+            v = 0.0f;
+            for (int p = 0; p < ks; ++p) v += cluster.map_shared_rank(part, p)[r * TC + c];
+        } else {
+            v = part[r * TC + c];
+        }
+        const int n = tile * TC + c;
+        if (n < a.Np) {
+            const float out = n < a.N ? v : 0.0f;
+            if (a.y) a.y[(size_t)r * a.Np + n] = out;
+            if (ARGMAX && n < a.N) atomicMax(&rowkey[r], argmax_key(out, n));
+        }
+    }
+    if (ARGMAX) {
+        __syncthreads();
+        for (int r = threadIdx.x; r < rows; r += kThreads)
+            if (rowkey[r]) atomicMax(&a.keys[r], rowkey[r]);
+    }
+    if (ks > 1) cg::this_cluster().sync();  // keep this CTA's shared memory alive until every rank has read it
+}
+
+}  // namespace q8

@@ -1,0 +1,48 @@
+// Host-side launch helpers shared by the kernel translation units of libq8gemv.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "q8_device.cuh"
+
+namespace q8 {
+
+// Launch `kernel` over the column tiles of width TC (grid.x) and the K split (grid.y, one thread-block cluster of
+// ksplit CTAs per tile when ksplit > 1).
+template <typename Kernel>
+inline cudaError_t launch_tiles(Kernel kernel, const Args &a, int TC, int smem_bytes, cudaStream_t stream) {
+    if (smem_bytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((a.Np + TC - 1) / TC), (unsigned)a.ksplit, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (a.ksplit > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)a.ksplit;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// Column tile width of each kernel family for a given per-thread width V.
+constexpr int simt_tile(int V) { return 32 * V; }
+constexpr int mma_tile(int V) { return 8 * V; }
+
+// Defined in q8_simt.cu / q8_mma.cu.  Return cudaErrorInvalidValue for a combination that is not built.
+cudaError_t launch_simt(const Args &a, int V, bool argmax, cudaStream_t stream);
+cudaError_t launch_mma(const Args &a, int V, bool argmax, cudaStream_t stream);
+
+// Widths built for each family (descending), used by the planner.
+bool simt_has(int m, int V);
+bool mma_has(int m, int V);
+
+}  // namespace q8

@@ -1,0 +1,270 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, element by element.
+
+Bar (the product's stated bound): |y_gpu - y_oracle| <= 1e-5 * A for every output, A = sum_b |s| sum_i |x q|; where
+A = 0 the GPU value must be exactly 0.  Arg-max: the oracle's first maximum wherever its gap to every other column
+exceeds the two columns' bounds, otherwise one of the columns within the bound; constructed ties go to the lowest
+index.  Sizes span several column tiles, K splits and a ragged last tile; the largest shapes are checked on sampled
+columns in the launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from q8_block_quantized_gemv_gb300 import build
+    build.build()
+    return torch
+
+
+def _to_dev(torch, x, q, s):
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    return xd, torch.from_numpy(np.ascontiguousarray(q)).cuda(), torch.from_numpy(np.ascontiguousarray(s)).cuda()
+
+
+def _gemv(torch, x, q, s, N, variant="auto"):
+    import q8_block_quantized_gemv_gb300 as q8
+    xd, qd, sd = _to_dev(torch, x, q, s)
+    y = q8.gemv(xd, qd, sd, N, variant=variant)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def _assert_close(y_gpu, y_o, a_o, what=""):
+    err = np.abs(y_gpu.astype(np.float64) - y_o)
+    bad = err > TOL * a_o
+    if bad.any():
+        r, c = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} outputs out of bound; first at ({r},{c}): gpu {y_gpu[r, c]!r} "
+                             f"oracle {y_o[r, c]!r} A {a_o[r, c]!r}")
+
+
+def _variants(m):
+    import q8_block_quantized_gemv_gb300 as q8
+    out = ["auto", "mma"]
+    if m in (1, 2, 3, 4, 8):
+        out.append("simt")
+    return out
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# element-by-element parity
+# --------------------------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m", list(range(1, 17)))
+def test_single_gemv_1024(dev, m):
+    """The single 1024 x 1024 GEMV workload (x bf16 N(0,1), q uniform int8 with a +-127 per block, s = 2^u/127),
+    every row count 1..16, every kernel family."""
+    x, q, s = si.case(m, 1024, 1024, si.case_seed(0, m))
+    y_o, a_o = oracle.gemv(x, q, s)
+    for v in _variants(m):
+        _assert_close(_gemv(dev, x, q, s, 1024, v), y_o, a_o, f"m={m} {v}")
+
+
+@pytest.mark.parametrize("N", [40, 3000, 6144])
+def test_ragged_tp_shapes(dev, N):
+    """Ragged tensor-parallel shapes, K = 5120, m = 3, zero-padded last tile; pads written as exactly 0."""
+    x, q, s = si.case(3, 5120, N, si.case_seed(3, 3, N))
+    y_o, a_o = oracle.gemv(x, q, s)
+    for v in _variants(3):
+        y = _gemv(dev, x, q, s, N, v)
+        _assert_close(y, y_o, a_o, f"N={N} {v}")
+        assert np.all(y[:, N:] == 0.0)
+
+
+@pytest.mark.parametrize("K", [768, 2176])
+@pytest.mark.parametrize("m", [1, 2, 16])
+def test_pages_row_split_tails(dev, K, m):
+    """The pages' row-split weights (768 and 2,176 rows: K not whole 1,024-row blocks) at a width of 40."""
+    x, q, s = si.case(m, K, 40, 500 + K + m)
+    y_o, a_o = oracle.gemv(x, q, s)
+    for v in _variants(m):
+        _assert_close(_gemv(dev, x, q, s, 40, v), y_o, a_o, f"K={K} m={m} {v}")
+
+
+@pytest.mark.parametrize("m,K,N", [(1, 32, 1), (16, 32, 1), (3, 32, 33), (5, 64, 2), (16, 14336, 32),
+                                   (1, 14336, 64), (8, 4096, 96), (2, 256, 100000)])
+def test_edge_shapes(dev, m, K, N):
+    """One block; one column; narrow N with deep K (the cluster split of K); very wide N with few blocks."""
+    x, q, s = si.case(m, K, N, 700 + m + K + N)
+    cols = None if N <= 6144 else np.r_[0:64, N - 64:oracle.padded_n(N)]
+    y_o, a_o = oracle.gemv(x, q, s, cols)
+    for v in _variants(m):
+        y = _gemv(dev, x, q, s, N, v)
+        _assert_close(y if cols is None else y[:, cols], y_o, a_o, f"m={m} K={K} N={N} {v}")
+
+
+@pytest.mark.parametrize("m", [1, 4, 16])
+def test_attention_projection_4096(dev, m):
+    """The 7B-class attention projection, K = N = 4096, m = 1, 4, 16: every output."""
+    x, q, s = si.case(m, 4096, 4096, si.case_seed(1, m))
+    y_o, a_o = oracle.gemv(x, q, s)
+    _assert_close(_gemv(dev, x, q, s, 4096), y_o, a_o, f"m={m}")
+
+
+@pytest.mark.parametrize("K,N", [(4096, 14336), (14336, 4096)])
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 16])
+def test_ffn_projections_sampled(dev, K, N, m):
+    """FFN up/gate (4096 x 14336) and down (14336 x 4096) at full size, m = 1, 2, 4, 8, 16, in the benchmark's
+    launch configuration; checked on 384 sampled columns (tile edges, the last columns and random ones)."""
+    x, q, s = si.case(m, K, N, si.case_seed(2, m, 1 if K > N else 0))
+    rng = np.random.default_rng(m)
+    cols = np.unique(np.r_[0:32, 120:136, 248:264, 504:520, N - 32:N, rng.integers(0, N, 256)])
+    y_o, a_o = oracle.gemv(x, q, s, cols)
+    y = _gemv(dev, x, q, s, N)
+    _assert_close(y[:, cols], y_o, a_o, f"K={K} N={N} m={m}")
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# properties
+# --------------------------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m", [1, 3, 9, 16])
+def test_deterministic_and_sign_symmetric(dev, m):
+    """Repeated calls give identical bits; y(-x) = -y(x) bit for bit (every rounding is sign-symmetric)."""
+    x, q, s = si.case(m, 4096, 1000, 900 + m)
+    for v in _variants(m):
+        y1 = _gemv(dev, x, q, s, 1000, v)
+        y2 = _gemv(dev, x, q, s, 1000, v)
+        yn = _gemv(dev, x ^ np.uint16(0x8000), q, s, 1000, v)
+        assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32)), v
+        assert np.array_equal(yn, -y1), v
+
+
+def test_batch_rows_match_single_rows(dev):
+    x, q, s = si.case(7, 2048, 700, 77)
+    y7 = _gemv(dev, x, q, s, 700)
+    y_o, a_o = oracle.gemv(x, q, s)
+    for r in range(7):
+        y1 = _gemv(dev, x[r:r + 1], q, s, 700)
+        _assert_close(y1, y_o[r:r + 1], a_o[r:r + 1], f"row {r}")
+        assert np.all(np.abs(y1[0].astype(np.float64) - y7[r]) <= 2 * TOL * a_o[r])
+
+
+def test_guards_and_dirty_pads(dev):
+    """Nothing outside y[m, Np] is written; garbage in the pad columns of q and s does not reach real columns and
+    the pad outputs are still exactly 0."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    m, K, N = 5, 1024, 3000
+    x, q, s = si.case(m, K, N, 31)
+    y_o, a_o = oracle.gemv(x, q, s)
+    q2, s2 = q.copy(), s.copy()
+    q2[:, N:] = 99
+    s2[:, N:] = 3.0
+    xd, qd, sd = _to_dev(torch, x, q2, s2)
+    Np = oracle.padded_n(N)
+    guard = 4096
+    buf = torch.full((m * Np + 2 * guard,), 12345.0, dtype=torch.float32, device="cuda")
+    y = buf[guard:guard + m * Np].view(m, Np)
+    for v in _variants(m):
+        q8.gemv(xd, qd, sd, N, y=y, variant=v)
+        torch.cuda.synchronize()
+        host = buf.cpu().numpy()
+        assert np.all(host[:guard] == 12345.0) and np.all(host[guard + m * Np:] == 12345.0)
+        yy = host[guard:guard + m * Np].reshape(m, Np)
+        assert np.all(yy[:, N:] == 0.0)
+        _assert_close(yy[:, :N], y_o[:, :N], a_o[:, :N], v)
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# arg-max
+# --------------------------------------------------------------------------------------------------------------------
+
+def _argmax_ok(idx, y_o, a_o, N):
+    """The acceptance rule: exact where the oracle's winner clears every other column's bound, else within it."""
+    for r in range(y_o.shape[0]):
+        best = int(oracle.argmax(y_o[r:r + 1], N)[0])
+        close = (y_o[r, best] - y_o[r, :N]) <= TOL * (a_o[r, best] + a_o[r, :N])
+        close[best] = True
+        if close.sum() == 1:
+            assert idx[r] == best, (r, idx[r], best)
+        else:
+            assert close[idx[r]], (r, idx[r], best)
+
+
+def _argmax(torch, x, q, s, N, with_logits=True):
+    import q8_block_quantized_gemv_gb300 as q8
+    xd, qd, sd = _to_dev(torch, x, q, s)
+    logits = torch.empty((x.shape[0], q.shape[1]), dtype=torch.float32, device="cuda") if with_logits else None
+    idx = q8.gemv_argmax(xd, qd, sd, N, logits=logits)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), (logits.cpu().numpy() if with_logits else None)
+
+
+@pytest.mark.parametrize("m", [1, 2])
+def test_argmax_tied_head_full(dev, m):
+    """The tied head, K = 4096, N = 128256, every logit against the oracle; the fused arg-max under the rule."""
+    x, q, s = si.case(m, 4096, 128256, si.case_seed(4, m))
+    y_o, a_o = oracle.gemv(x, q, s)
+    idx, logits = _argmax(dev, x, q, s, 128256)
+    _assert_close(logits, y_o, a_o, "head logits")
+    _argmax_ok(idx, y_o, a_o, 128256)
+    # the fused arg-max is exactly the first maximum of the logits the same call wrote
+    for r in range(m):
+        assert idx[r] == int(np.flatnonzero(logits[r, :128256] == logits[r, :128256].max())[0])
+    idx2, _ = _argmax(dev, x, q, s, 128256, with_logits=False)
+    assert np.array_equal(idx, idx2)
+
+
+def test_argmax_head_m16_sampled_rows(dev):
+    x, q, s = si.case(16, 4096, 128256, si.case_seed(4, 16))
+    idx, logits = _argmax(dev, x, q, s, 128256)
+    for r in (0, 7, 15):
+        y_o, a_o = oracle.gemv(x[r:r + 1], q, s)
+        _assert_close(logits[r:r + 1], y_o, a_o, f"row {r}")
+        _argmax_ok(idx[r:r + 1], y_o, a_o, 128256)
+    for r in range(16):
+        assert idx[r] == int(np.flatnonzero(logits[r, :128256] == logits[r, :128256].max())[0])
+
+
+@pytest.mark.parametrize("m", [1, 5, 16])
+def test_argmax_planted_ties_and_pads(dev, m):
+    K, N = 1024, 3000
+    x, q, s = si.case(m, K, N, 1300 + m)
+    xf = si.bf16_bits_to_f32(x)
+    # a planted winner for row 0: column 1234 aligned with the signs of row 0's activations
+    q[:, 1234] = np.where(xf[0] >= 0, 127, -127).astype(np.int8)
+    s[:, 1234] = s[:, :N].max()
+    # ties: copies of the winner further right
+    for c in (1500, 2999):
+        q[:, c] = q[:, 1234]
+        s[:, c] = s[:, 1234]
+    y_o, a_o = oracle.gemv(x, q, s)
+    idx, _ = _argmax(dev, x, q, s, N)
+    assert idx[0] == 1234
+    _argmax_ok(idx, y_o, a_o, N)
+    # every real logit negative: the pad columns (exactly 0) must not win
+    xa = si.f32_to_bf16_bits(np.abs(xf))
+    qn = -np.abs(q.astype(np.int16)).astype(np.int8)
+    qn[:, 0] = -1                         # keep every column strictly negative
+    qn[:, N:] = 0
+    y_o, a_o = oracle.gemv(xa, qn, s)
+    assert np.all(y_o[:, :N] < 0)
+    idx, _ = _argmax(dev, xa, qn, s, N)
+    assert np.all(idx < N)
+    _argmax_ok(idx, y_o, a_o, N)
+
+
+def test_argmax_scratch_contents_do_not_matter(dev):
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    x, q, s = si.case(4, 1024, 2000, 55)
+    xd, qd, sd = _to_dev(torch, x, q, s)
+    idx = torch.full((4,), -1, dtype=torch.int64, device="cuda")
+    a = q8.gemv_argmax(xd, qd, sd, 2000, idx=idx).cpu().numpy()
+    idx.fill_(2**62)
+    b = q8.gemv_argmax(xd, qd, sd, 2000, idx=idx).cpu().numpy()
+    assert np.array_equal(a, b)
+    y_o, a_o = oracle.gemv(x, q, s)
+    _argmax_ok(a, y_o, a_o, 2000)

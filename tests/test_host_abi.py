@@ -1,0 +1,188 @@
+"""The C ABI on the CPU: the library loads and exports every declared symbol; host entry points agree with the oracle;
+device entry points reject bad arguments before touching CUDA (no compute call runs here)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth_inputs as si
+import q8_block_quantized_gemv_gb300 as q8
+from q8_block_quantized_gemv_gb300 import build as q8build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "q8_gemv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    q8build.build()
+    return q8.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(q8_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 9
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(q8.SIGNATURES), "binding signatures and header disagree"
+
+
+def test_padded_n(lib):
+    for n, want in [(1, 32), (32, 32), (33, 64), (40, 64), (3000, 3008), (6144, 6144), (128256, 128256),
+                    (0, -1), (-7, -1), (2**31 - 1, -1)]:
+        assert q8.padded_n(n) == want, n
+        if n > 0 and want > 0:
+            assert want == oracle.padded_n(n)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert q8.status_string(code)
+    assert q8.status_string(99) == "unknown status"
+    assert lib.q8_version() >= 10000
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# host entry points against the oracle
+# --------------------------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K,N,seed", [(256, 40, 1), (1024, 96, 2), (64, 1, 3)])
+def test_quantize_matches_oracle(lib, K, N, seed):
+    _, q, s = si.case(1, K, N, seed)
+    w = oracle.dequantize(q[:, :N], s[:, :N])
+    gq, gs = q8.quantize(w)
+    oq, os_ = oracle.quantize(w)
+    assert np.array_equal(gq[:, :N], oq) and np.array_equal(gs[:, :N], os_)
+    assert np.all(gq[:, N:] == 0) and np.all(gs[:, N:] == 0)
+    assert np.array_equal(gq, q) and np.array_equal(gs, s)
+
+
+def test_quantize_rejections_match_oracle(lib):
+    _, q, s = si.case(1, 64, 4, 18)
+    w = oracle.dequantize(q[:, :4], s[:, :4])
+    w[5, 2] = np.nextafter(w[5, 2], np.inf)
+    assert oracle.quantize(w) is None
+    with pytest.raises(q8.Q8Error) as e:
+        q8.quantize(w)
+    assert e.value.status == 4
+    one = np.zeros((32, 1))
+    one[0, 0] = 1.0                      # d = 1/127 is not an fp32
+    assert oracle.quantize(one) is None
+    with pytest.raises(q8.Q8Error):
+        q8.quantize(one)
+    d = 2.0 ** -10
+    half = np.zeros((32, 1))
+    half[0, 0], half[1, 0] = 127 * d, 63.5 * d
+    with pytest.raises(q8.Q8Error):
+        q8.quantize(half)
+    for bad in (np.nan, np.inf):
+        w2 = np.zeros((32, 2))
+        w2[3, 1] = bad
+        with pytest.raises(q8.Q8Error):
+            q8.quantize(w2)
+    zero = np.zeros((64, 3))
+    gq, gs = q8.quantize(zero)
+    assert not gq.any() and not gs.any()
+
+
+def test_quantize_shape_errors(lib):
+    with pytest.raises(q8.Q8Error) as e:
+        q8.quantize(np.zeros((33, 2)))
+    assert e.value.status == 2
+
+
+def _blocks(q, s, N):
+    K = q.shape[0]
+    nb = K // 32
+    rec = np.zeros((N, nb, 36), dtype=np.uint8)
+    rec[:, :, :4] = s[:, :N].T.astype("<f4").copy().view(np.uint8).reshape(N, nb, 4)
+    rec[:, :, 4:] = q[:, :N].T.reshape(N, nb, 32).view(np.uint8)
+    return rec.tobytes()
+
+
+@pytest.mark.parametrize("K,N", [(128, 40), (64, 3000), (32, 1)])
+def test_repack_matches_oracle(lib, K, N):
+    _, q, s = si.case(1, K, N, K + N)
+    blk = _blocks(q, s, N)
+    gq, gs = q8.repack(blk, K, N)
+    oq, os_ = oracle.repack(blk, K, N)
+    assert np.array_equal(gq, oq) and np.array_equal(gs, os_)
+    assert np.array_equal(gq, q) and np.array_equal(gs, s)
+
+
+def test_repack_rejects(lib):
+    _, q, s = si.case(1, 64, 8, 5)
+    q2 = q.copy()
+    q2[7, 3] = -128
+    with pytest.raises(q8.Q8Error) as e:
+        q8.repack(_blocks(q2, s, 8), 64, 8)
+    assert e.value.status == 4
+    s2 = s.copy()
+    s2[1, 2] = np.inf
+    with pytest.raises(q8.Q8Error):
+        q8.repack(_blocks(q, s2, 8), 64, 8)
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# device entry points: argument errors come back before any CUDA call
+# --------------------------------------------------------------------------------------------------------------------
+
+A16 = 0x10000      # fake, 16-byte aligned addresses: never dereferenced, the calls fail their checks first
+B16 = 0x20000
+C16 = 0x30000
+D16 = 0x40000
+
+
+@pytest.mark.parametrize("args,want", [
+    ((None, B16, C16, D16, 1, 32, 32), 1),          # null x
+    ((A16, None, C16, D16, 1, 32, 32), 1),          # null q
+    ((A16, B16, None, D16, 1, 32, 32), 1),          # null s
+    ((A16, B16, C16, None, 1, 32, 32), 1),          # null y
+    ((A16, B16, C16, D16, 0, 32, 32), 2),           # m = 0
+    ((A16, B16, C16, D16, 17, 32, 32), 2),          # m > 16
+    ((A16, B16, C16, D16, 1, 0, 32), 2),            # K = 0
+    ((A16, B16, C16, D16, 1, 48, 32), 2),           # K % 32 != 0
+    ((A16, B16, C16, D16, 1, 32, 0), 2),            # N = 0
+    ((A16, B16, C16, D16, 1, 32, 2**31 - 1), 2),    # Np overflows
+    ((A16 + 2, B16, C16, D16, 1, 32, 32), 3),       # misaligned x
+    ((A16, B16 + 8, C16, D16, 1, 32, 32), 3),       # misaligned q
+    ((A16, B16, C16 + 4, D16, 1, 32, 32), 3),       # misaligned s
+    ((A16, B16, C16, D16 + 4, 1, 32, 32), 3),       # misaligned y
+    ((A16, B16, C16, B16, 1, 32, 32), 1),           # y overlaps q
+])
+def test_gemv_argument_errors(lib, args, want):
+    assert lib.q8_gemv(*args, None) == want
+    assert lib.q8_gemv_ex(*args, 0, None) == want
+
+
+def test_gemv_ex_rejects_unknown_variant(lib):
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, 3, None) == 1
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, -1, None) == 1
+
+
+@pytest.mark.parametrize("args,want", [
+    ((A16, B16, C16, None, D16, 1, 32, 32), 1),     # null idx
+    ((A16, B16, C16, D16 + 4, None, 1, 32, 32), 3),  # misaligned idx
+    ((A16, B16, C16, D16, 0x50004, 1, 32, 32), 3),  # misaligned logits
+    ((A16, B16, C16, D16, None, 0, 32, 32), 2),
+    ((A16, B16, C16, D16, None, 1, 31, 32), 2),
+    ((A16, B16, C16, D16, B16, 1, 32, 32), 1),      # logits overlap q
+])
+def test_argmax_argument_errors(lib, args, want):
+    assert lib.q8_gemv_argmax(*args, None) == want
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros((1, 32), dtype=torch.bfloat16)
+    q = torch.zeros((32, 32), dtype=torch.int8)
+    s = torch.zeros((1, 32), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        q8.gemv(x, q, s, 32)
