@@ -217,8 +217,13 @@ class Chain:
         import synth_inputs as si
         self.torch, self.m = torch, m
         self.shapes = chain_shapes()
+        import q8_block_quantized_gemv_gb300 as q8
+        # row-major weights as drawn, and the tiled storage the library streams (made once, as at model load)
         self.w = [si.device_weight(K, N, seed + i) for i, (K, N) in enumerate(self.shapes)]
         self.head = si.device_weight(HIDDEN, VOCAB, seed + len(self.shapes))
+        self.wt = [q8.tile_device(q, s, N) for (q, s), (_, N) in zip(self.w, self.shapes)]
+        self.head_t = q8.tile_device(self.head[0], self.head[1], VOCAB)
+        torch.cuda.synchronize()
         # activations: one [m, K] block per call, all in one buffer (the H2D copy of the end-to-end measurement)
         sizes = [m * K for K, _ in self.shapes] + [m * HIDDEN]
         self.x_all = torch.empty(sum(sizes), dtype=torch.bfloat16, device="cuda")
@@ -236,13 +241,13 @@ class Chain:
     def run_layers(self):
         import q8_block_quantized_gemv_gb300 as q8
         for i, (K, N) in enumerate(self.shapes):
-            q, s = self.w[i]
-            q8.gemv(self.x[i], q, s, N, y=self.y[i])
+            q, s = self.wt[i]
+            q8.gemv(self.x[i], q, s, N, y=self.y[i], constant_weights=True, tiled=True)
 
     def run_head(self):
         import q8_block_quantized_gemv_gb300 as q8
-        q, s = self.head
-        q8.gemv_argmax(self.x[-1], q, s, VOCAB, idx=self.idx)
+        q, s = self.head_t
+        q8.gemv_argmax(self.x[-1], q, s, VOCAB, idx=self.idx, constant_weights=True, tiled=True)
 
     def capture(self):
         torch = self.torch

@@ -54,11 +54,14 @@ typedef enum {
     Q8_ERR_CUDA = 5      /* the CUDA runtime reported an error; see q8_last_cuda_error() */
 } q8_status;
 
-/* Kernel family selector for q8_gemv_ex (benchmarking and testing; q8_gemv picks by m). */
+/* Kernel family selector for q8_gemv_ex (benchmarking and testing; q8_gemv picks one by shape). */
 typedef enum {
     Q8_VARIANT_AUTO = 0,
-    Q8_VARIANT_SIMT = 1, /* CUDA-core fp32 FMA, m-row accumulators per thread */
-    Q8_VARIANT_MMA = 2   /* int8 -> bf16 exact dequant in registers, bf16 tensor-core MMA, fp32 per-block scale fold */
+    Q8_VARIANT_SIMT = 1, /* CUDA-core fp32 FMA, m-row accumulators per thread, weights loaded straight to registers */
+    Q8_VARIANT_MMA = 2,  /* int8 -> bf16 exact dequant in registers, bf16 tensor-core MMA, fp32 per-block scale fold */
+    Q8_VARIANT_TMA = 3   /* as MMA, the weight streamed by TMA through a 16-stage shared-memory pipeline by a producer
+                            warp; launched with programmatic dependent launch.  Needs N > 96 (Np >= 128); smaller N
+                            falls back to MMA. */
 } q8_variant;
 
 /* N rounded up to whole 32-column tiles ("from_q8.rs", `q8_gemv_applies`: the last tile is zero-padded).
@@ -74,9 +77,18 @@ int q8_padded_n(int N);
  * summation order is fixed for a given (m, K, N) and device, so repeated calls give identical bits. */
 q8_status q8_gemv(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N, q8_stream_t stream);
 
-/* q8_gemv with an explicit kernel family (q8_variant).  Same arguments, results within the same bound. */
+/* Flags of q8_gemv_ex. */
+#define Q8_FLAG_CONSTANT_WEIGHTS 1u /* no work enqueued before this call on `stream` writes q or s: the pipelined
+                                       kernel may start streaming them before the previous kernel on the stream has
+                                       finished (programmatic dependent launch); x and y are still ordered */
+
+#define Q8_FLAG_TILED 2u            /* q and s are in the tiled layout of q8_tile (below), not row-major; read by the
+                                       per-warp cp.async streaming kernel (variant must be AUTO) */
+
+/* q8_gemv with an explicit kernel family (q8_variant) and flags (Q8_FLAG_*; 0 for none).  Same arguments and
+ * bound; Q8_ERR_ARG for an unknown variant or flag, or for Q8_FLAG_TILED with a variant other than AUTO. */
 q8_status q8_gemv_ex(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N, int variant,
-                     q8_stream_t stream);
+                     unsigned int flags, q8_stream_t stream);
 
 /* The product followed by the arg-max that closes a decode step (source: "plan.rs", `Launch::ArgMax`, and
  * "int8_model.rs", `decode_step_lg`: the index of the first maximal logit; its CUDA arg-max sends equal values to the
@@ -88,6 +100,29 @@ q8_status q8_gemv_ex(const void *x, const int8_t *q, const float *s, float *y, i
  * Other arguments as q8_gemv.  Logits that are NaN order above +inf (not reached for finite inputs). */
 q8_status q8_gemv_argmax(const void *x, const int8_t *q, const float *s, int64_t *idx, float *logits, int m, int K,
                          int N, q8_stream_t stream);
+
+/* q8_gemv_argmax with flags (Q8_FLAG_CONSTANT_WEIGHTS, Q8_FLAG_TILED). */
+q8_status q8_gemv_argmax_ex(const void *x, const int8_t *q, const float *s, int64_t *idx, float *logits, int m,
+                            int K, int N, unsigned int flags, q8_stream_t stream);
+
+/* The tiled storage of a Q8_0 weight, for Q8_FLAG_TILED (no counterpart on the pages: a GPU storage order of the
+ * same two tensors, made once when the weight is loaded, as the host repack of "from_q8.rs" `Q8Part` is).  Every
+ * 32-row x 128-column block becomes one contiguous 4 KB unit laid out in the order the kernel's lanes load it, so a
+ * warp streaming one column tile along K reads contiguous memory.  With Nt = q8_tiled_n(N), T = Nt / 128 tiles and
+ * nb = K / 32 blocks:
+ *   values  int8 [T][nb][4096]: in unit (t, b), segment 4s + j (s = 0, 1; j = 0..3, 512 bytes each) holds at byte
+ *           16 * (4g + u) (g = 0..7, u = 0..3) the 16 values of weight row 32b + 16s + 4u + j, columns
+ *           128t + 16g .. 128t + 16g + 15, in column order
+ *   scales  fp32 [T][nb][128]: element c of unit (t, b) is s[b][128t + c]
+ * Columns >= N are zero.  Sizes: K * Nt bytes of values, (K / 32) * Nt * 4 bytes of scales. */
+int q8_tiled_n(int N); /* N rounded up to a multiple of 128; -1 when N <= 0 or on overflow */
+
+/* Host: row-major q [K][Np], s [K/32][Np] (as q8_gemv takes them) -> tiled qt, st (host buffers, written). */
+q8_status q8_tile(const int8_t *q, const float *s, int K, int N, int8_t *qt, float *st);
+
+/* Device: the same transform on device buffers, enqueued on `stream` (q, qt 16-byte aligned; s, st 4-byte aligned;
+ * the input and output must not overlap). */
+q8_status q8_tile_device(const int8_t *q, const float *s, int K, int N, int8_t *qt, float *st, q8_stream_t stream);
 
 /* Host repack of checkpoint blocks into the two stored tensors (source: "from_q8.rs", `Q8Part`: the host repacks the
  * checkpoint's blocks into the int8 values `q8_0.values` and the fp32 scales `q8_0.scales`).
@@ -105,6 +140,12 @@ q8_status q8_repack(const void *blocks, int K, int N, int8_t *q, float *s);
  * d = amax / 127 (in fp64) must be exactly an fp32 value, and every w / d must lie within 1e-9 of an integer r with
  * |r| <= 127 and r * d == w exactly.  Any failure returns Q8_ERR_NOT_Q8_0 (q and s then hold no meaning). */
 q8_status q8_quantize(const double *w, int K, int N, int8_t *q, float *s);
+
+/* Reads the device fault word of the current device: nonzero when a kernel's bounded wait on a pipeline barrier ran
+ * out (bit 0: a consumer waited about two seconds for a stage's data; bit 1: the producer waited as long for a free
+ * stage) and the kernel finished early -- that call's outputs are then wrong.  Synchronous with respect to the
+ * device.  `clear` != 0 resets the word to 0.  Returns Q8_ERR_ARG for a NULL `fault`, Q8_ERR_CUDA on a CUDA error. */
+q8_status q8_device_fault(unsigned int *fault, int clear);
 
 /* A static, human-readable name for a status code. */
 const char *q8_status_string(q8_status status);

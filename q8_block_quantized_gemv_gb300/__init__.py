@@ -23,7 +23,7 @@ from .build import LIB as _LIB_PATH
 
 Q8_BLOCK = 32
 MAX_ROWS = 16
-VARIANTS = {"auto": 0, "simt": 1, "mma": 2}
+VARIANTS = {"auto": 0, "simt": 1, "mma": 2, "tma": 3}
 
 _STATUS = {0: "Q8_OK", 1: "Q8_ERR_ARG", 2: "Q8_ERR_SHAPE", 3: "Q8_ERR_ALIGN", 4: "Q8_ERR_NOT_Q8_0", 5: "Q8_ERR_CUDA"}
 
@@ -33,13 +33,18 @@ _I = ctypes.c_int
 SIGNATURES = {
     "q8_padded_n": (_I, [_I]),
     "q8_gemv": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
-    "q8_gemv_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "q8_gemv_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_gemv_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "q8_gemv_argmax_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
+    "q8_tiled_n": (_I, [_I]),
+    "q8_tile": (_I, [_P, _P, _I, _I, _P, _P]),
+    "q8_tile_device": (_I, [_P, _P, _I, _I, _P, _P, _P]),
     "q8_repack": (_I, [_P, _I, _I, _P, _P]),
     "q8_quantize": (_I, [_P, _I, _I, _P, _P]),
     "q8_status_string": (ctypes.c_char_p, [_I]),
     "q8_last_cuda_error": (_I, []),
     "q8_version": (_I, []),
+    "q8_device_fault": (_I, [_P, _I]),
 }
 
 _lib = None
@@ -94,7 +99,11 @@ def _stream_handle(stream):
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _check_operands(x, q, s, N):
+def tiled_n(N: int) -> int:
+    return lib().q8_tiled_n(N)
+
+
+def _check_operands(x, q, s, N, tiled=False):
     import torch
     if not (x.is_cuda and q.is_cuda and s.is_cuda):
         raise ValueError("x, q and s must be CUDA tensors")
@@ -102,35 +111,53 @@ def _check_operands(x, q, s, N):
         raise TypeError("x must be bfloat16, q int8 and s float32")
     if not (x.is_contiguous() and q.is_contiguous() and s.is_contiguous()):
         raise ValueError("x, q and s must be contiguous")
-    if x.dim() != 2 or q.dim() != 2 or s.dim() != 2:
-        raise ValueError("x, q and s must be 2-D")
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [m, K]")
     m, K = x.shape
     Np = padded_n(N) if N > 0 else -1
-    if q.shape != (K, Np) or s.shape != (K // Q8_BLOCK, Np):
+    if tiled:
+        Nt = tiled_n(N) if N > 0 else -1
+        if q.numel() != K * Nt or s.numel() != (K // Q8_BLOCK) * Nt:
+            raise ValueError(f"tiled q must hold K * Nt = {K * Nt} values and s (K/32) * Nt scales")
+    elif q.shape != (K, Np) or s.shape != (K // Q8_BLOCK, Np):
         raise ValueError(f"q must be [K, Np] = [{K}, {Np}] and s [K/32, Np]; got {tuple(q.shape)}, {tuple(s.shape)}")
     return m, K, Np
 
 
-def gemv(x, q, s, N: int, y=None, variant: str = "auto", stream=None):
-    """y = x . W over the Q8_0 weight (q, s); returns y, fp32 [m, Np] (columns N .. Np-1 are 0)."""
+FLAG_CONSTANT_WEIGHTS = 1
+FLAG_TILED = 2
+
+
+def _flags(constant_weights, tiled):
+    return (FLAG_CONSTANT_WEIGHTS if constant_weights else 0) | (FLAG_TILED if tiled else 0)
+
+
+def gemv(x, q, s, N: int, y=None, variant: str = "auto", constant_weights: bool = False, tiled: bool = False,
+         stream=None):
+    """y = x . W over the Q8_0 weight (q, s); returns y, fp32 [m, Np] (columns N .. Np-1 are 0).
+
+    constant_weights: nothing enqueued earlier on the stream writes q or s (Q8_FLAG_CONSTANT_WEIGHTS), so the
+    kernel may stream them before the previous kernel finishes.  tiled: q and s are in the tiled layout
+    (:func:`tile_device`, Q8_FLAG_TILED)."""
     import torch
-    m, K, Np = _check_operands(x, q, s, N)
+    m, K, Np = _check_operands(x, q, s, N, tiled)
     if y is None:
         y = torch.empty((m, Np), dtype=torch.float32, device=x.device)
     elif y.dtype != torch.float32 or y.shape != (m, Np) or not y.is_contiguous() or not y.is_cuda:
         raise ValueError("y must be a contiguous fp32 CUDA tensor [m, Np]")
     _check(lib().q8_gemv_ex(x.data_ptr(), q.data_ptr(), s.data_ptr(), y.data_ptr(), m, K, N, VARIANTS[variant],
-                            _stream_handle(stream)), "q8_gemv")
+                            _flags(constant_weights, tiled), _stream_handle(stream)), "q8_gemv")
     return y
 
 
-def gemv_argmax(x, q, s, N: int, idx=None, logits=None, stream=None):
+def gemv_argmax(x, q, s, N: int, idx=None, logits=None, constant_weights: bool = False, tiled: bool = False,
+                stream=None):
     """The product and its first-maximum arg-max per row: returns idx, int64 [m] (0-based).
 
     ``logits``: None (not stored) or a contiguous fp32 [m, Np] CUDA tensor that receives y.
     """
     import torch
-    m, K, Np = _check_operands(x, q, s, N)
+    m, K, Np = _check_operands(x, q, s, N, tiled)
     if idx is None:
         idx = torch.empty((m,), dtype=torch.int64, device=x.device)
     elif idx.dtype != torch.int64 or idx.numel() < m or not idx.is_contiguous() or not idx.is_cuda:
@@ -140,9 +167,41 @@ def gemv_argmax(x, q, s, N: int, idx=None, logits=None, stream=None):
         if logits.dtype != torch.float32 or logits.shape != (m, Np) or not logits.is_contiguous():
             raise ValueError("logits must be a contiguous fp32 CUDA tensor [m, Np]")
         lp = logits.data_ptr()
-    _check(lib().q8_gemv_argmax(x.data_ptr(), q.data_ptr(), s.data_ptr(), idx.data_ptr(), lp, m, K, N,
-                                _stream_handle(stream)), "q8_gemv_argmax")
+    _check(lib().q8_gemv_argmax_ex(x.data_ptr(), q.data_ptr(), s.data_ptr(), idx.data_ptr(), lp, m, K, N,
+                                   _flags(constant_weights, tiled), _stream_handle(stream)), "q8_gemv_argmax")
     return idx
+
+
+def tile(q, s, N: int):
+    """Host: row-major (q [K, Np], s [K/32, Np]) numpy arrays -> the tiled layout (qt int8 [K * Nt], st fp32
+    [K/32 * Nt]) (q8_tile)."""
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    K = q.shape[0]
+    Nt = tiled_n(N) if N > 0 else 1
+    qt = np.empty(max(K * Nt, 1), dtype=np.int8)
+    st = np.empty(max((K // Q8_BLOCK) * Nt, 1), dtype=np.float32)
+    _check(lib().q8_tile(q.ctypes.data, s.ctypes.data, K, N, qt.ctypes.data, st.ctypes.data), "q8_tile")
+    return qt, st
+
+
+def tile_device(q, s, N: int, stream=None):
+    """Device: row-major CUDA tensors (q [K, Np] int8, s [K/32, Np] fp32) -> tiled CUDA tensors (q8_tile_device)."""
+    import torch
+    K = q.shape[0]
+    Nt = tiled_n(N)
+    qt = torch.empty((K * Nt,), dtype=torch.int8, device=q.device)
+    st = torch.empty(((K // Q8_BLOCK) * Nt,), dtype=torch.float32, device=q.device)
+    _check(lib().q8_tile_device(q.data_ptr(), s.data_ptr(), K, N, qt.data_ptr(), st.data_ptr(),
+                                _stream_handle(stream)), "q8_tile_device")
+    return qt, st
+
+
+def device_fault(clear: bool = False) -> int:
+    """The device fault word (nonzero when a kernel's bounded pipeline wait ran out); see q8_device_fault."""
+    word = ctypes.c_uint(0)
+    _check(lib().q8_device_fault(ctypes.byref(word), int(clear)), "q8_device_fault")
+    return word.value
 
 
 def repack(blocks, K: int, N: int):

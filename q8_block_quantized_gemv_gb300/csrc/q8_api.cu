@@ -1,6 +1,8 @@
 // Device entry points of libq8gemv: argument checks, the launch plan, and the arg-max finish.
 #include <stdint.h>
 
+#include <stdlib.h>
+
 #include <atomic>
 
 #include "../../include/q8_gemv.h"
@@ -47,6 +49,8 @@ int sm_count(int *out) {
     return 0;
 }
 
+constexpr int kVariantStream = 100;  // internal: the tiled-layout kernel
+
 struct Plan {
     int variant;  // Q8_VARIANT_SIMT or Q8_VARIANT_MMA
     int V;        // columns per lane
@@ -56,11 +60,56 @@ struct Plan {
 // Kernel family, per-lane width and K split for a shape.  The widest tile that still gives every SM a CTA is
 // preferred; K is split across a cluster (at most 8 CTAs, the portable size) until the grid holds about two CTAs per
 // SM, the residency the kernels are built for.
-Plan make_plan(int m, int K, int Np, int variant, int sms) {
-    if (variant == Q8_VARIANT_AUTO) variant = m <= 2 ? Q8_VARIANT_SIMT : Q8_VARIANT_MMA;
+Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms) {
+    const int nb = K / Q8_BLOCK;
+    if (tiled) {
+        // The tiled layout: per-warp cp.async streams, 128-column tiles.  The kernel is bound by the SMs' issue rate,
+        // so an SM's time is the work of all the CTAs it runs: the K split is the one whose busiest SM (CTAs per SM,
+        // each its blocks plus about two blocks of fixed work) finishes first.
+        const long long tiles = (Np + q8::kTmaColumns - 1) / q8::kTmaColumns;
+        int best = 1;
+        double best_cost = 1e300;
+        for (int ks = 1; ks <= 8 && ks <= nb; ++ks) {
+            const long long per_sm = (tiles * ks + sms - 1) / sms;
+            const double cost = (double)per_sm * (2.0 + (double)((nb + ks - 1) / ks));
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = ks;
+            }
+        }
+        const char *force = getenv("Q8_KSPLIT");
+        if (force) {
+            const int f = atoi(force);
+            if (f >= 1 && f <= 8 && f <= nb) best = f;
+        }
+        return Plan{kVariantStream, 16, best};
+    }
+    if (variant == Q8_VARIANT_AUTO) variant = Q8_VARIANT_TMA;
+    if (variant == Q8_VARIANT_TMA && Np < q8::kTmaColumns) variant = Q8_VARIANT_MMA;
+    if (variant == Q8_VARIANT_TMA) {
+        // 128-column tiles, two resident CTAs per SM.  A CTA costs its blocks plus a fixed overhead (pipeline fill,
+        // epilogue, cluster reduction) of about eight blocks; the K split is the one whose waves of CTAs finish first.
+        const long long tiles = (Np + q8::kTmaColumns - 1) / q8::kTmaColumns;
+        const long long slots = 2LL * sms;
+        int best = 1;
+        double best_cost = 1e300;
+        for (int ks = 1; ks <= 8 && ks <= nb; ++ks) {
+            const long long waves = (tiles * ks + slots - 1) / slots;
+            const double cost = (double)waves * (8.0 + (double)((nb + ks - 1) / ks));
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = ks;
+            }
+        }
+        const char *force = getenv("Q8_KSPLIT");
+        if (force) {
+            const int f = atoi(force);
+            if (f >= 1 && f <= 8 && f <= nb) best = f;
+        }
+        return Plan{Q8_VARIANT_TMA, 16, best};
+    }
     if (variant == Q8_VARIANT_SIMT && !q8::simt_has(m, 4)) variant = Q8_VARIANT_MMA;
     static const int widths[3] = {16, 8, 4};
-    const int nb = K / Q8_BLOCK;
     Plan best = {variant, 0, 1};
     for (int i = 0; i < 3; ++i) {
         const int V = widths[i];
@@ -87,15 +136,19 @@ q8_status check_gemv_args(const void *x, const int8_t *q, const float *s, int m,
     return Q8_OK;
 }
 
-q8_status run(const Args &a, int variant, bool argmax, cudaStream_t stream) {
+q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStream_t stream) {
     int sms = 0;
     int e = sm_count(&sms);
     if (e != 0) return cuda_fail((cudaError_t)e);
-    const Plan p = make_plan(a.m, a.K, a.Np, variant, sms);
+    const bool tiled = (flags & Q8_FLAG_TILED) != 0;
+    const Plan p = make_plan(a.m, a.K, a.Np, variant, tiled, sms);
     Args b = a;
     b.ksplit = p.ksplit;
-    cudaError_t ce = p.variant == Q8_VARIANT_SIMT ? q8::launch_simt(b, p.V, argmax, stream)
-                                                  : q8::launch_mma(b, p.V, argmax, stream);
+    const bool prefetch = (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0;
+    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, argmax, stream, true, prefetch)
+                     : p.variant == Q8_VARIANT_TMA  ? q8::launch_tma(b, argmax, stream, true, prefetch)
+                     : p.variant == Q8_VARIANT_SIMT ? q8::launch_simt(b, p.V, argmax, stream)
+                                                    : q8::launch_mma(b, p.V, argmax, stream);
     if (ce != cudaSuccess) return cuda_fail(ce);
     return Q8_OK;
 }
@@ -112,37 +165,45 @@ __global__ void argmax_decode(int64_t *idx, int m) {
 }  // namespace
 
 extern "C" q8_status q8_gemv_ex(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N,
-                                int variant, q8_stream_t stream) {
+                                int variant, unsigned int flags, q8_stream_t stream) {
     q8_status st = check_gemv_args(x, q, s, m, K, N);
     if (st != Q8_OK) return st;
     if (!y) return Q8_ERR_ARG;
-    if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_MMA) return Q8_ERR_ARG;
+    if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_TMA) return Q8_ERR_ARG;
+    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if ((flags & Q8_FLAG_TILED) && variant != Q8_VARIANT_AUTO) return Q8_ERR_ARG;
+    if ((flags & Q8_FLAG_TILED) && q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
     if (!aligned(y, 16)) return Q8_ERR_ALIGN;
     const int Np = q8_padded_n(N);
+    const size_t wcols = (flags & Q8_FLAG_TILED) ? (size_t)q8_tiled_n(N) : (size_t)Np;
     const size_t ybytes = (size_t)m * Np * 4;
-    if (overlaps(y, ybytes, x, (size_t)m * K * 2) || overlaps(y, ybytes, q, (size_t)K * Np) ||
-        overlaps(y, ybytes, s, (size_t)(K / Q8_BLOCK) * Np * 4))
+    if (overlaps(y, ybytes, x, (size_t)m * K * 2) || overlaps(y, ybytes, q, (size_t)K * wcols) ||
+        overlaps(y, ybytes, s, (size_t)(K / Q8_BLOCK) * wcols * 4))
         return Q8_ERR_ARG;
     Args a = {static_cast<const uint16_t *>(x), q, s, y, nullptr, m, K, N, Np, K / Q8_BLOCK, 1};
-    return run(a, variant, false, (cudaStream_t)stream);
+    return run(a, variant, flags, false, (cudaStream_t)stream);
 }
 
 extern "C" q8_status q8_gemv(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N,
                              q8_stream_t stream) {
-    return q8_gemv_ex(x, q, s, y, m, K, N, Q8_VARIANT_AUTO, stream);
+    return q8_gemv_ex(x, q, s, y, m, K, N, Q8_VARIANT_AUTO, 0u, stream);
 }
 
-extern "C" q8_status q8_gemv_argmax(const void *x, const int8_t *q, const float *s, int64_t *idx, float *logits,
-                                    int m, int K, int N, q8_stream_t stream) {
+extern "C" q8_status q8_gemv_argmax_ex(const void *x, const int8_t *q, const float *s, int64_t *idx, float *logits,
+                                       int m, int K, int N, unsigned int flags, q8_stream_t stream) {
     q8_status st = check_gemv_args(x, q, s, m, K, N);
     if (st != Q8_OK) return st;
     if (!idx) return Q8_ERR_ARG;
+    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if ((flags & Q8_FLAG_TILED) && q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
     if (!aligned(idx, 8) || (logits && !aligned(logits, 16))) return Q8_ERR_ALIGN;
     const int Np = q8_padded_n(N);
+    const size_t wcols = (flags & Q8_FLAG_TILED) ? (size_t)q8_tiled_n(N) : (size_t)Np;
     if (logits) {
         const size_t ybytes = (size_t)m * Np * 4;
-        if (overlaps(logits, ybytes, x, (size_t)m * K * 2) || overlaps(logits, ybytes, q, (size_t)K * Np) ||
-            overlaps(logits, ybytes, s, (size_t)(K / Q8_BLOCK) * Np * 4) || overlaps(logits, ybytes, idx, m * 8))
+        if (overlaps(logits, ybytes, x, (size_t)m * K * 2) || overlaps(logits, ybytes, q, (size_t)K * wcols) ||
+            overlaps(logits, ybytes, s, (size_t)(K / Q8_BLOCK) * wcols * 4) ||
+            overlaps(logits, ybytes, idx, (size_t)m * 8))
             return Q8_ERR_ARG;
     }
     cudaStream_t cs = (cudaStream_t)stream;
@@ -150,7 +211,7 @@ extern "C" q8_status q8_gemv_argmax(const void *x, const int8_t *q, const float 
     if (ce != cudaSuccess) return cuda_fail(ce);
     Args a = {static_cast<const uint16_t *>(x), q, s, logits, reinterpret_cast<unsigned long long *>(idx),
               m, K, N, Np, K / Q8_BLOCK, 1};
-    st = run(a, Q8_VARIANT_AUTO, true, cs);
+    st = run(a, Q8_VARIANT_AUTO, flags, true, cs);
     if (st != Q8_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
@@ -158,5 +219,17 @@ extern "C" q8_status q8_gemv_argmax(const void *x, const int8_t *q, const float 
     cfg.stream = cs;
     ce = cudaLaunchKernelEx(&cfg, argmax_decode, idx, m);
     if (ce != cudaSuccess) return cuda_fail(ce);
+    return Q8_OK;
+}
+
+extern "C" q8_status q8_gemv_argmax(const void *x, const int8_t *q, const float *s, int64_t *idx, float *logits,
+                                    int m, int K, int N, q8_stream_t stream) {
+    return q8_gemv_argmax_ex(x, q, s, idx, logits, m, K, N, 0u, stream);
+}
+
+extern "C" q8_status q8_device_fault(unsigned int *fault, int clear) {
+    if (!fault) return Q8_ERR_ARG;
+    cudaError_t e = q8::read_fault_word(fault, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
     return Q8_OK;
 }

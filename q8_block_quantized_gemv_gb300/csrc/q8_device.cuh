@@ -79,6 +79,20 @@ __device__ __forceinline__ float q8_to_f32(uint32_t u, int e) {
 __device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
 
+// Byte e of two sign-flipped int8 words (see q8_to_f32) as one exact bf16 pair, lo from `ua` in the low half: the two
+// magic floats are made by byte permutes, reduced to the integers by one packed fp32x2 subtract, then packed to bf16
+// (exact: |q| <= 127 needs 8 significant bits).
+__device__ __forceinline__ uint32_t q8x2_to_bf16x2(uint32_t ua, uint32_t ub, int e) {
+    const uint32_t fa = __byte_perm(ua, 0x4B000000u, 0x7540u | (uint32_t)e);
+    const uint32_t fb = __byte_perm(ub, 0x4B000000u, 0x7540u | (uint32_t)e);
+    uint32_t out;
+    asm("{\n .reg .b64 a, c, d;\n .reg .f32 lo, hi;\n mov.b64 a, {%1, %2};\n mov.b64 c, {%3, %3};\n"
+        " sub.rn.f32x2 d, a, c;\n mov.b64 {lo, hi}, d;\n cvt.rn.bf16x2.f32 %0, hi, lo;\n}"
+        : "=r"(out)
+        : "r"(fa), "r"(fb), "r"(0x4B000080u));
+    return out;
+}
+
 // Two small integers (|v| <= 127, at most 8 significant bits) as a bf16 pair, exactly: lo in the low half.
 __device__ __forceinline__ uint32_t bf16x2_exact(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
@@ -112,31 +126,29 @@ __device__ __forceinline__ void warp_blocks(const Args &a, int warp, int &b0, in
     b1 = c0 + (c1 - c0) * (warp + 1) / kWarps;
 }
 
-// Shared-memory bytes of the epilogue for MR rows and TC columns.
-__host__ __device__ constexpr int finish_smem_bytes(int MR, int TC) {
-    return (kWarps * MR * TC + MR * TC) * 4 + MR * 8;
-}
+// Shared-memory bytes of the epilogue: NRED partial slabs of MR rows and TC columns, the CTA's sum, the row keys.
+__host__ __device__ constexpr int finish_smem_n(int NRED, int MR, int TC) { return (NRED * MR * TC + MR * TC) * 4 + MR * 8; }
+__host__ __device__ constexpr int finish_smem_bytes(int MR, int TC) { return finish_smem_n(kWarps, MR, TC); }
 
-// The epilogue.  On entry every warp has written its carry into red[warp][row][column] (rows < MR, columns < TC of
-// this CTA's tile) and the CTA has synchronised.  Sums the warps in order, then (ksplit > 1) the cluster's ranks in
-// order, writes y (0 in the pad columns) and folds this CTA's columns into the per-row arg-max keys.
-template <int MR, int TC, bool ARGMAX>
-__device__ __forceinline__ void finish(const Args &a, float *smem) {
+// The epilogue.  On entry the CTA's NRED partial carries sit in red[NRED][MR][TC] (rows < MR, columns < TC of this
+// CTA's tile) and the CTA has synchronised.  Sums the slabs in order, then (ksplit > 1) the cluster's ranks in order,
+// writes y (0 in the pad columns) and folds this CTA's columns into the per-row arg-max keys.
+template <int NRED, int MR, int TC, int NTHREADS, bool ARGMAX>
+__device__ __forceinline__ void finish_n(const Args &a, float *red) {
     namespace cg = cooperative_groups;
-    float *red = smem;                                                        // [kWarps][MR][TC]
-    float *part = red + kWarps * MR * TC;                                     // [MR][TC]
+    float *part = red + NRED * MR * TC;                                                   // [MR][TC]
     unsigned long long *rowkey = reinterpret_cast<unsigned long long *>(part + MR * TC);  // [MR]
     const int rows = a.m < MR ? a.m : MR;
     const int tile = blockIdx.x;
 
-    for (int i = threadIdx.x; i < rows * TC; i += kThreads) {
+    for (int i = threadIdx.x; i < rows * TC; i += NTHREADS) {
         float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += red[w * MR * TC + i];
+        for (int w = 0; w < NRED; ++w) v += red[w * MR * TC + i];
         part[i] = v;
     }
     if (ARGMAX)
-        for (int r = threadIdx.x; r < MR; r += kThreads) rowkey[r] = 0ull;
+        for (int r = threadIdx.x; r < MR; r += NTHREADS) rowkey[r] = 0ull;
 
     const int ks = a.ksplit;
     if (ks > 1)
@@ -148,7 +160,7 @@ __device__ __forceinline__ void finish(const Args &a, float *smem) {
     const int c0 = ks > 1 ? TC * rank / ks : 0;
     const int c1 = ks > 1 ? TC * (rank + 1) / ks : TC;
     const int width = c1 - c0;
-    for (int i = threadIdx.x; i < rows * width; i += kThreads) {
+    for (int i = threadIdx.x; i < rows * width; i += NTHREADS) {
         const int r = i / width;
         const int c = c0 + (i - r * width);
         float v;
@@ -168,10 +180,15 @@ __device__ __forceinline__ void finish(const Args &a, float *smem) {
     }
     if (ARGMAX) {
         __syncthreads();
-        for (int r = threadIdx.x; r < rows; r += kThreads)
+        for (int r = threadIdx.x; r < rows; r += NTHREADS)
             if (rowkey[r]) atomicMax(&a.keys[r], rowkey[r]);
     }
     if (ks > 1) cg::this_cluster().sync();  // keep this CTA's shared memory alive until every rank has read it
+}
+
+template <int MR, int TC, bool ARGMAX>
+__device__ __forceinline__ void finish(const Args &a, float *smem) {
+    finish_n<kWarps, MR, TC, kThreads, ARGMAX>(a, smem);
 }
 
 }  // namespace q8

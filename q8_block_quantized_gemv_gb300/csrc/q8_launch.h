@@ -34,12 +34,22 @@ inline cudaError_t launch_tiles(Kernel kernel, const Args &a, int TC, int smem_b
 }
 
 // Column tile width of each kernel family for a given per-thread width V.
-constexpr int simt_tile(int V) { return 32 * V; }
-constexpr int mma_tile(int V) { return 8 * V; }
+__host__ __device__ constexpr int simt_tile(int V) { return 32 * V; }
+__host__ __device__ constexpr int mma_tile(int V) { return 8 * V; }
 
 // Defined in q8_simt.cu / q8_mma.cu.  Return cudaErrorInvalidValue for a combination that is not built.
 cudaError_t launch_simt(const Args &a, int V, bool argmax, cudaStream_t stream);
 cudaError_t launch_mma(const Args &a, int V, bool argmax, cudaStream_t stream);
+
+// Defined in q8_tma.cu.
+bool tma_supported(const Args &a);
+cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl, bool prefetch_weights);
+
+// Defined in q8_stream.cu (the tiled layout).
+int stream_ctas_per_sm(int m);
+cudaError_t launch_stream(const Args &a, bool argmax, cudaStream_t stream, bool pdl, bool prefetch_weights);
+cudaError_t read_fault_word(unsigned *out, bool clear);
+constexpr int kTmaColumns = 128;
 
 // Widths built for each family (descending), used by the planner.
 bool simt_has(int m, int V);

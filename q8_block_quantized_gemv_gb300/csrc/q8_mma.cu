@@ -59,71 +59,74 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(const Args a) {
         xrow[nt] = a.x + (size_t)(xlive[nt] ? r : 0) * a.K + 4 * t;
     }
 
-    if (col < a.Np) {
-        for (int b = b0; b < b1; ++b) {
-            float d[NT][NP][4];
+    // Every lane runs the loop (mma.sync needs the whole warp); lanes past the last column load zeros.
+    const bool live = col < a.Np;
+    for (int b = b0; b < b1; ++b) {
+        float d[NT][NP][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int p = 0; p < NP; ++p)
+            for (int p = 0; p < NP; ++p)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) d[nt][p][i] = 0.0f;
+                for (int i = 0; i < 4; ++i) d[nt][p][i] = 0.0f;
 #pragma unroll
-            for (int step = 0; step < 2; ++step) {
-                const int k0 = b * kBlock + 16 * step + 4 * t;
-                VT w[4];
+        for (int step = 0; step < 2; ++step) {
+            const int k0 = b * kBlock + 16 * step + 4 * t;
+            VT w[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) ld_stream(w[j], a.q + (size_t)(k0 + j) * a.Np + col);
-                uint32_t bx[NT][2];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    uint2 xv = make_uint2(0u, 0u);
-                    if (xlive[nt]) xv = __ldg(reinterpret_cast<const uint2 *>(xrow[nt] + b * kBlock + 16 * step));
-                    bx[nt][0] = xv.x;
-                    bx[nt][1] = xv.y;
-                }
-#pragma unroll
-                for (int wi = 0; wi < NW; ++wi) {
-                    const uint32_t u0 = word_of(w[0], wi) ^ 0x80808080u;
-                    const uint32_t u1 = word_of(w[1], wi) ^ 0x80808080u;
-                    const uint32_t u2 = word_of(w[2], wi) ^ 0x80808080u;
-                    const uint32_t u3 = word_of(w[3], wi) ^ 0x80808080u;
-                    uint32_t lo[4], hi[4];  // per column: rows (4t, 4t+1) and (4t+2, 4t+3) as bf16 pairs
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        lo[e] = bf16x2_exact(q8_to_f32(u0, e), q8_to_f32(u1, e));
-                        hi[e] = bf16x2_exact(q8_to_f32(u2, e), q8_to_f32(u3, e));
-                    }
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {  // the two column pairs of this word
-                        const int p = 2 * wi + h;
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma_bf16_16816(d[nt][p], lo[2 * h], lo[2 * h + 1], hi[2 * h], hi[2 * h + 1], bx[nt][0],
-                                           bx[nt][1]);
-                    }
-                }
+            for (int j = 0; j < 4; ++j) {
+                w[j] = VT{};
+                if (live) ld_stream(w[j], a.q + (size_t)(k0 + j) * a.Np + col);
             }
-            float sc[V];
+            uint32_t bx[NT][2];
 #pragma unroll
-            for (int v4 = 0; v4 < V / 4; ++v4) {
-                uint4 tt;
-                ld_stream(tt, a.s + (size_t)b * a.Np + col + 4 * v4);
-                sc[4 * v4 + 0] = __uint_as_float(tt.x);
-                sc[4 * v4 + 1] = __uint_as_float(tt.y);
-                sc[4 * v4 + 2] = __uint_as_float(tt.z);
-                sc[4 * v4 + 3] = __uint_as_float(tt.w);
+            for (int nt = 0; nt < NT; ++nt) {
+                uint2 xv = make_uint2(0u, 0u);
+                if (xlive[nt]) xv = __ldg(reinterpret_cast<const uint2 *>(xrow[nt] + b * kBlock + 16 * step));
+                bx[nt][0] = xv.x;
+                bx[nt][1] = xv.y;
             }
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int wi = 0; wi < NW; ++wi) {
+                const uint32_t u0 = word_of(w[0], wi) ^ 0x80808080u;
+                const uint32_t u1 = word_of(w[1], wi) ^ 0x80808080u;
+                const uint32_t u2 = word_of(w[2], wi) ^ 0x80808080u;
+                const uint32_t u3 = word_of(w[3], wi) ^ 0x80808080u;
+                uint32_t lo[4], hi[4];  // per column: rows (4t, 4t+1) and (4t+2, 4t+3) as bf16 pairs
 #pragma unroll
-                for (int p = 0; p < NP; ++p) {
-                    acc[nt][p][0] = fmaf(sc[2 * p], d[nt][p][0], acc[nt][p][0]);
-                    acc[nt][p][1] = fmaf(sc[2 * p], d[nt][p][1], acc[nt][p][1]);
-                    acc[nt][p][2] = fmaf(sc[2 * p + 1], d[nt][p][2], acc[nt][p][2]);
-                    acc[nt][p][3] = fmaf(sc[2 * p + 1], d[nt][p][3], acc[nt][p][3]);
+                for (int e = 0; e < 4; ++e) {
+                    lo[e] = q8x2_to_bf16x2(u0, u1, e);
+                    hi[e] = q8x2_to_bf16x2(u2, u3, e);
                 }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // the two column pairs of this word
+                    const int p = 2 * wi + h;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_bf16_16816(d[nt][p], lo[2 * h], lo[2 * h + 1], hi[2 * h], hi[2 * h + 1], bx[nt][0],
+                                       bx[nt][1]);
+                }
+            }
         }
+        float sc[V];
+#pragma unroll
+        for (int v4 = 0; v4 < V / 4; ++v4) {
+            uint4 tt = make_uint4(0u, 0u, 0u, 0u);
+            if (live) ld_stream(tt, a.s + (size_t)b * a.Np + col + 4 * v4);
+            sc[4 * v4 + 0] = __uint_as_float(tt.x);
+            sc[4 * v4 + 1] = __uint_as_float(tt.y);
+            sc[4 * v4 + 2] = __uint_as_float(tt.z);
+            sc[4 * v4 + 3] = __uint_as_float(tt.w);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                acc[nt][p][0] = fmaf(sc[2 * p], d[nt][p][0], acc[nt][p][0]);
+                acc[nt][p][1] = fmaf(sc[2 * p], d[nt][p][1], acc[nt][p][1]);
+                acc[nt][p][2] = fmaf(sc[2 * p + 1], d[nt][p][2], acc[nt][p][2]);
+                acc[nt][p][3] = fmaf(sc[2 * p + 1], d[nt][p][3], acc[nt][p][3]);
+            }
     }
 
     // D fragment: element 0/1 -> activation rows 2t, 2t+1 of MMA row g (column cl + 2p); 2/3 -> the same rows of

@@ -1,0 +1,273 @@
+// Q8_0 GEMV over the tiled weight storage: every warp streams its own contiguous run of weight units.
+//
+// The tiled storage (q8_tile) keeps every 32-row x 128-column block of the weight as one contiguous 4 KB unit, in
+// MMA-fragment order: the unit is eight 512-byte segments (16-row step s = 0, 1; row group j = 0..3), and in segment
+// (s, j) lane L = 4g + t of a warp finds its 16 bytes at L * 16: weight row 16s + 4t + j, columns 16g .. 16g + 15 of
+// the tile.  The scales of the unit follow in their own storage, 128 fp32 in column order.  So one warp instruction
+// copies 512 contiguous bytes, and the units of a column tile follow each other along K: a warp that owns a run of K
+// blocks of one tile reads one contiguous range of memory.
+//
+// A CTA owns one 128-column tile and a range of its K blocks (split across a thread-block cluster when N is too
+// narrow to fill the SMs); its eight warps split that range into contiguous runs.  Each warp keeps a private ring of
+// three stages in shared memory, filled with cp.async (16 bytes a lane, bypassing L1): it issues block i + 2 while
+// it computes block i, so about two units per warp -- 150 KB per SM -- are in flight without holding registers.  Per
+// block a lane converts its 4 x 16 int8 values exactly to bf16 pairs, runs the 8 (or 16) bf16 m16n8k16 MMAs of the
+// block into a fresh fp32 accumulator, and folds the block sums into its fp32 carry with the block's scales
+// ("from_q8.rs", module doc: the lanes contracted over the int8 rows, then folded down each column with their scales,
+// into an fp32 carry).  The MMA's K order is the relabeling of the register-fed kernel: MMA reduction index 2t, 2t+1,
+// 2t+8, 2t+9 is weight row 4t, 4t+1, 4t+2, 4t+3, so a lane's activation fragment is 4 consecutive activations.
+//
+// Activations are read from L2 (ld.global.cg), one block ahead.  With programmatic dependent launch every thread
+// waits for the previous kernel (griddepcontrol.wait) before it reads x or writes y; with Q8_FLAG_CONSTANT_WEIGHTS
+// the first two stages' weights are already requested before that wait.
+#include "q8_launch.h"
+
+namespace q8 {
+
+namespace {
+
+constexpr int kWarpsS = 8;
+constexpr int kThreadsS = 32 * kWarpsS;
+constexpr int kUnit = kBlock * kTmaColumns;  // 4096 bytes of values per 32 x 128 unit
+constexpr int kUnitScales = kTmaColumns;     // 128 fp32
+constexpr int kStageS = kUnit + kUnitScales * 4;
+// Ring stages per warp: three with two CTAs per SM (m <= 8), five with one (m > 8, twice the accumulators).
+template <int NT> struct StreamShape {
+    static constexpr int kDepth = NT == 1 ? 3 : 5;
+    static constexpr int kSmem = kWarpsS * kDepth * kStageS;
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint2 ld_cg_u2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// Copy unit `u` (values and scales) into `stage`: 8 + 1 cp.async of 16 bytes per lane.
+__device__ __forceinline__ void issue_unit(unsigned char *stage, const int8_t *q, const float *s, size_t u, int lane) {
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(q) + u * kUnit + lane * 16;
+#pragma unroll
+    for (int seg = 0; seg < 8; ++seg) cp_async16(stage + seg * 512 + lane * 16, src + seg * 512);
+    cp_async16(stage + kUnit + lane * 16, reinterpret_cast<const unsigned char *>(s + u * kUnitScales) + lane * 16);
+}
+
+template <int NT, bool ARGMAX>
+__global__ void __launch_bounds__(kThreadsS, NT == 1 ? 2 : 1)
+    stream_kernel(const Args a, const int prefetch_weights) {
+    constexpr int MR = 8 * NT;
+    constexpr int kDepth = StreamShape<NT>::kDepth;
+    extern __shared__ __align__(16) unsigned char smem_s[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int tile = blockIdx.x;
+    const int rank = blockIdx.y;
+    const int c0 = (int)((long long)a.nb * rank / a.ksplit);
+    const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
+    const int b0 = c0 + (c1 - c0) * warp / kWarpsS;
+    const int b1 = c0 + (c1 - c0) * (warp + 1) / kWarpsS;
+    const int n = b1 - b0;
+    unsigned char *ring = smem_s + warp * kDepth * kStageS;
+    const size_t unit0 = (size_t)tile * a.nb + b0;
+
+    float acc[NT][8][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][p][i] = 0.0f;
+
+    // Prologue: the first kDepth - 1 units (one commit group each, empty past the run).
+    if (prefetch_weights) {
+#pragma unroll
+        for (int i = 0; i < kDepth - 1; ++i) {
+            if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
+            cp_async_commit();
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!prefetch_weights) {
+#pragma unroll
+        for (int i = 0; i < kDepth - 1; ++i) {
+            if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
+            cp_async_commit();
+        }
+    }
+
+    // Activation rows this lane feeds to the MMA (rows at or past m are zeros).
+    const uint16_t *xrow[NT];
+    bool xlive[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int r = 8 * nt + g;
+        xlive[nt] = r < a.m;
+        xrow[nt] = a.x + (size_t)(xlive[nt] ? r : 0) * a.K + 4 * t;
+    }
+    uint2 xf[2][NT];  // this block's activation fragments, one step per entry
+    auto load_x = [&](int b) {
+#pragma unroll
+        for (int step = 0; step < 2; ++step)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                xf[step][nt] = xlive[nt] ? ld_cg_u2(xrow[nt] + (size_t)b * kBlock + 16 * step) : make_uint2(0u, 0u);
+    };
+    if (n > 0) load_x(b0);
+
+    for (int i = 0; i < n; ++i) {
+        const int ahead = i + kDepth - 1;
+        if (ahead < n) issue_unit(ring + (ahead % kDepth) * kStageS, a.q, a.s, unit0 + ahead, lane);
+        cp_async_commit();
+        cp_async_wait<kDepth - 1>();  // this lane's copies of unit i have landed
+        __syncwarp();                 // ... and every other lane's (the scales are read across lanes)
+        const unsigned char *st = ring + (i % kDepth) * kStageS;
+        uint2 xc[2][NT];
+#pragma unroll
+        for (int step = 0; step < 2; ++step)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) xc[step][nt] = xf[step][nt];
+        if (i + 1 < n) load_x(b0 + i + 1);
+
+        float d[NT][8][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[nt][p][e] = 0.0f;
+#pragma unroll
+        for (int step = 0; step < 2; ++step) {
+            uint4 w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint4 *>(st + (step * 4 + j) * 512 + lane * 16);
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+                const uint32_t u0 = word_of(w[0], wi) ^ 0x80808080u;
+                const uint32_t u1 = word_of(w[1], wi) ^ 0x80808080u;
+                const uint32_t u2 = word_of(w[2], wi) ^ 0x80808080u;
+                const uint32_t u3 = word_of(w[3], wi) ^ 0x80808080u;
+                uint32_t lo[4], hi[4];  // per column: rows (4t, 4t+1) and (4t+2, 4t+3) as bf16 pairs
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    lo[e] = q8x2_to_bf16x2(u0, u1, e);
+                    hi[e] = q8x2_to_bf16x2(u2, u3, e);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int p = 2 * wi + h;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_16816(d[nt][p], lo[2 * h], lo[2 * h + 1], hi[2 * h], hi[2 * h + 1], xc[step][nt].x,
+                                  xc[step][nt].y);
+                }
+            }
+        }
+        const float *ss = reinterpret_cast<const float *>(st + kUnit) + 16 * g;
+        float sc[16];
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+            const float4 f = *reinterpret_cast<const float4 *>(ss + 4 * v4);
+            sc[4 * v4 + 0] = f.x;
+            sc[4 * v4 + 1] = f.y;
+            sc[4 * v4 + 2] = f.z;
+            sc[4 * v4 + 3] = f.w;
+        }
+        __syncwarp();  // every lane is done with this stage before it is refilled
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                acc[nt][p][0] = fmaf(sc[2 * p], d[nt][p][0], acc[nt][p][0]);
+                acc[nt][p][1] = fmaf(sc[2 * p], d[nt][p][1], acc[nt][p][1]);
+                acc[nt][p][2] = fmaf(sc[2 * p + 1], d[nt][p][2], acc[nt][p][2]);
+                acc[nt][p][3] = fmaf(sc[2 * p + 1], d[nt][p][3], acc[nt][p][3]);
+            }
+    }
+    cp_async_wait<0>();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __syncthreads();  // every warp is done with its ring: the shared memory holds the epilogue now
+
+    // D fragment: element 0/1 -> activation rows 2t, 2t+1 of MMA row g (column 16g + 2p); 2/3 -> the same rows of
+    // MMA row g + 8 (column 16g + 2p + 1).
+    float *red = reinterpret_cast<float *>(smem_s);  // [kWarpsS][MR][128]
+    float *mine = red + warp * MR * kTmaColumns;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const int r = 8 * nt + 2 * t;
+            const int c = 16 * g + 2 * p;
+            *reinterpret_cast<float2 *>(mine + r * kTmaColumns + c) = make_float2(acc[nt][p][0], acc[nt][p][2]);
+            *reinterpret_cast<float2 *>(mine + (r + 1) * kTmaColumns + c) = make_float2(acc[nt][p][1], acc[nt][p][3]);
+        }
+    __syncthreads();
+    finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, ARGMAX>(a, red);
+}
+
+static_assert(finish_smem_n(kWarpsS, 8, kTmaColumns) <= StreamShape<1>::kSmem, "the epilogue fits in the rings");
+static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns) <= StreamShape<2>::kSmem, "the epilogue fits in the rings");
+static_assert(2 * StreamShape<1>::kSmem <= 227 * 1024 && StreamShape<2>::kSmem <= 227 * 1024, "residency");
+
+template <int NT, bool ARGMAX>
+cudaError_t launch_stream_nt(const Args &a, cudaStream_t stream, bool pdl, bool prefetch) {
+    auto kernel = stream_kernel<NT, ARGMAX>;
+    constexpr int kSmemS = StreamShape<NT>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((a.Np + kTmaColumns - 1) / kTmaColumns), (unsigned)a.ksplit, 1);
+    cfg.blockDim = dim3(kThreadsS, 1, 1);
+    cfg.dynamicSmemBytes = kSmemS;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (a.ksplit > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = (unsigned)a.ksplit;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kernel, a, prefetch ? 1 : 0);
+}
+
+}  // namespace
+
+int stream_ctas_per_sm(int m) { return m <= 8 ? 2 : 1; }
+
+cudaError_t launch_stream(const Args &a, bool argmax, cudaStream_t stream, bool pdl, bool prefetch_weights) {
+    if (a.m <= 8)
+        return argmax ? launch_stream_nt<1, true>(a, stream, pdl, prefetch_weights)
+                      : launch_stream_nt<1, false>(a, stream, pdl, prefetch_weights);
+    return argmax ? launch_stream_nt<2, true>(a, stream, pdl, prefetch_weights)
+                  : launch_stream_nt<2, false>(a, stream, pdl, prefetch_weights);
+}
+
+}  // namespace q8

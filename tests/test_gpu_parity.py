@@ -33,9 +33,14 @@ def _to_dev(torch, x, q, s):
 
 
 def _gemv(torch, x, q, s, N, variant="auto"):
+    """One call through the C ABI; variant "tiled" first rearranges the weight with q8_tile_device."""
     import q8_block_quantized_gemv_gb300 as q8
     xd, qd, sd = _to_dev(torch, x, q, s)
-    y = q8.gemv(xd, qd, sd, N, variant=variant)
+    if variant == "tiled":
+        qt, st = q8.tile_device(qd, sd, N)
+        y = q8.gemv(xd, qt, st, N, tiled=True)
+    else:
+        y = q8.gemv(xd, qd, sd, N, variant=variant)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
@@ -51,7 +56,7 @@ def _assert_close(y_gpu, y_o, a_o, what=""):
 
 def _variants(m):
     import q8_block_quantized_gemv_gb300 as q8
-    out = ["auto", "mma"]
+    out = ["auto", "mma", "tma", "tiled"]
     if m in (1, 2, 3, 4, 8):
         out.append("simt")
     return out
@@ -168,7 +173,11 @@ def test_guards_and_dirty_pads(dev):
     buf = torch.full((m * Np + 2 * guard,), 12345.0, dtype=torch.float32, device="cuda")
     y = buf[guard:guard + m * Np].view(m, Np)
     for v in _variants(m):
-        q8.gemv(xd, qd, sd, N, y=y, variant=v)
+        if v == "tiled":
+            qt, st = q8.tile_device(qd, sd, N)
+            q8.gemv(xd, qt, st, N, y=y, tiled=True)
+        else:
+            q8.gemv(xd, qd, sd, N, y=y, variant=v)
         torch.cuda.synchronize()
         host = buf.cpu().numpy()
         assert np.all(host[:guard] == 12345.0) and np.all(host[guard + m * Np:] == 12345.0)
@@ -193,11 +202,13 @@ def _argmax_ok(idx, y_o, a_o, N):
             assert close[idx[r]], (r, idx[r], best)
 
 
-def _argmax(torch, x, q, s, N, with_logits=True):
+def _argmax(torch, x, q, s, N, with_logits=True, tiled=False):
     import q8_block_quantized_gemv_gb300 as q8
     xd, qd, sd = _to_dev(torch, x, q, s)
     logits = torch.empty((x.shape[0], q.shape[1]), dtype=torch.float32, device="cuda") if with_logits else None
-    idx = q8.gemv_argmax(xd, qd, sd, N, logits=logits)
+    if tiled:
+        qd, sd = q8.tile_device(qd, sd, N)
+    idx = q8.gemv_argmax(xd, qd, sd, N, logits=logits, tiled=tiled)
     torch.cuda.synchronize()
     return idx.cpu().numpy(), (logits.cpu().numpy() if with_logits else None)
 
@@ -215,6 +226,9 @@ def test_argmax_tied_head_full(dev, m):
         assert idx[r] == int(np.flatnonzero(logits[r, :128256] == logits[r, :128256].max())[0])
     idx2, _ = _argmax(dev, x, q, s, 128256, with_logits=False)
     assert np.array_equal(idx, idx2)
+    idx3, logits3 = _argmax(dev, x, q, s, 128256, tiled=True)
+    _assert_close(logits3, y_o, a_o, "head logits, tiled")
+    _argmax_ok(idx3, y_o, a_o, 128256)
 
 
 def test_argmax_head_m16_sampled_rows(dev):
@@ -241,9 +255,10 @@ def test_argmax_planted_ties_and_pads(dev, m):
         q[:, c] = q[:, 1234]
         s[:, c] = s[:, 1234]
     y_o, a_o = oracle.gemv(x, q, s)
-    idx, _ = _argmax(dev, x, q, s, N)
-    assert idx[0] == 1234
-    _argmax_ok(idx, y_o, a_o, N)
+    for tiled in (False, True):
+        idx, _ = _argmax(dev, x, q, s, N, tiled=tiled)
+        assert idx[0] == 1234
+        _argmax_ok(idx, y_o, a_o, N)
     # every real logit negative: the pad columns (exactly 0) must not win
     xa = si.f32_to_bf16_bits(np.abs(xf))
     qn = -np.abs(q.astype(np.int16)).astype(np.int8)
@@ -268,3 +283,84 @@ def test_argmax_scratch_contents_do_not_matter(dev):
     assert np.array_equal(a, b)
     y_o, a_o = oracle.gemv(x, q, s)
     _argmax_ok(a, y_o, a_o, 2000)
+
+
+@pytest.mark.parametrize("ks", [1, 2, 3, 5, 8])
+def test_tma_every_cluster_split(dev, ks, monkeypatch):
+    """The pipelined kernel at every K split across a cluster (the planner's choice forced), m = 1 and 16, against
+    the oracle; the device fault word stays clear (no bounded wait ran out)."""
+    import q8_block_quantized_gemv_gb300 as q8
+    monkeypatch.setenv("Q8_KSPLIT", str(ks))
+    for m in (1, 16):
+        x, q, s = si.case(m, 2048, 1000, 1700 + ks + m)
+        y_o, a_o = oracle.gemv(x, q, s)
+        for v in ("tma", "tiled"):
+            _assert_close(_gemv(dev, x, q, s, 1000, v), y_o, a_o, f"ks={ks} m={m} {v}")
+    assert q8.device_fault() == 0
+
+
+def test_no_device_fault_after_suite(dev):
+    import q8_block_quantized_gemv_gb300 as q8
+    assert q8.device_fault(clear=True) == 0
+
+
+@pytest.mark.parametrize("tiled", [False, True])
+@pytest.mark.parametrize("m", [1, 16])
+def test_graph_chain_with_constant_weights(dev, m, tiled):
+    """Back-to-back calls captured in a CUDA graph and replayed, weights declared constant (programmatic dependent
+    launch lets each call start streaming its weights before the previous call ends) -- the benchmark's launch
+    configuration -- each output against the oracle; the last call reads the first call's output as its activation
+    (a true dependency through x)."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    shapes = [(1024, 2048), (2048, 1024), (1024, 4096), (4096, 1024)]
+    host = [si.case(m, K, N, 3100 + 10 * i + m) for i, (K, N) in enumerate(shapes)]
+    devs = [_to_dev(torch, *h) for h in host]
+    if tiled:
+        devs = [(xd,) + q8.tile_device(qd, sd, N) for (xd, qd, sd), (_, N) in zip(devs, shapes)]
+    ys = [torch.empty((m, N), dtype=torch.float32, device="cuda") for _, N in shapes]
+    xdep = torch.empty((m, 2048), dtype=torch.bfloat16, device="cuda")
+
+    def run():
+        for i, (K, N) in enumerate(shapes):
+            xd, qd, sd = devs[i]
+            if i == 1:
+                xd = xdep
+            q8.gemv(xd, qd, sd, N, y=ys[i], constant_weights=True, tiled=tiled)
+            if i == 0:
+                xdep.copy_(ys[0].to(torch.bfloat16))   # a torch kernel between two calls, on the same stream
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for i, (K, N) in enumerate(shapes):
+            x, q, s_ = host[i]
+            if i == 1:
+                x = xdep.view(torch.int16).cpu().numpy().view(np.uint16)
+            y_o, a_o = oracle.gemv(x, q, s_)
+            _assert_close(ys[i].cpu().numpy(), y_o, a_o, f"call {i} m={m}")
+    assert q8.device_fault() == 0
+
+
+@pytest.mark.parametrize("K,N", [(64, 40), (1024, 3000), (4096, 128256)])
+def test_tile_device_matches_host(dev, K, N):
+    """q8_tile_device writes exactly the bytes q8_tile writes (the host transform is pinned on the CPU)."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    _, q, s = si.case(1, K, N, 4400 + N)
+    q[:, N:] = 3
+    qt, st = q8.tile(q, s, N)
+    qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    qtd, std = q8.tile_device(qd, sd, N)
+    torch.cuda.synchronize()
+    assert np.array_equal(qtd.cpu().numpy(), qt) and np.array_equal(std.cpu().numpy(), st)

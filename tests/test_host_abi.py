@@ -159,12 +159,13 @@ D16 = 0x40000
 ])
 def test_gemv_argument_errors(lib, args, want):
     assert lib.q8_gemv(*args, None) == want
-    assert lib.q8_gemv_ex(*args, 0, None) == want
+    assert lib.q8_gemv_ex(*args, 0, 0, None) == want
 
 
 def test_gemv_ex_rejects_unknown_variant(lib):
-    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, 3, None) == 1
-    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, -1, None) == 1
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, 4, 0, None) == 1
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, -1, 0, None) == 1
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, 0, 4, None) == 1       # unknown flag
 
 
 @pytest.mark.parametrize("args,want", [
@@ -179,6 +180,10 @@ def test_argmax_argument_errors(lib, args, want):
     assert lib.q8_gemv_argmax(*args, None) == want
 
 
+def test_device_fault_rejects_null(lib):
+    assert lib.q8_device_fault(None, 0) == 1
+
+
 def test_binding_refuses_cpu_tensors(lib):
     torch = pytest.importorskip("torch")
     x = torch.zeros((1, 32), dtype=torch.bfloat16)
@@ -186,3 +191,50 @@ def test_binding_refuses_cpu_tensors(lib):
     s = torch.zeros((1, 32), dtype=torch.float32)
     with pytest.raises(ValueError):
         q8.gemv(x, q, s, 32)
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# the tiled storage order (q8_tile): checked against the index map written out independently here
+# --------------------------------------------------------------------------------------------------------------------
+
+def _tile_reference(q, s, N):
+    K = q.shape[0]
+    nb, Nt = K // 32, -(-N // 128) * 128
+    T = Nt // 128
+    qt = np.zeros((T, nb, 32, 128), dtype=np.int8)
+    st = np.zeros((T, nb, 128), dtype=np.float32)
+    qt = qt.reshape(T, nb, 4096)
+    for t in range(T):
+        for b in range(nb):
+            for r in range(32):
+                step, u, j = r // 16, (r % 16) // 4, r % 4
+                for c in range(128):
+                    n = 128 * t + c
+                    if n < N:
+                        lane = 4 * (c // 16) + u
+                        qt[t, b, (4 * step + j) * 512 + 16 * lane + c % 16] = q[32 * b + r, n]
+            for c in range(128):
+                if 128 * t + c < N:
+                    st[t, b, c] = s[b, 128 * t + c]
+    return qt.reshape(-1), st.reshape(-1)
+
+
+@pytest.mark.parametrize("K,N", [(64, 40), (96, 300), (32, 128)])
+def test_tile_host_matches_index_map(lib, K, N):
+    _, q, s = si.case(1, K, N, 77 + N)
+    q[:, N:] = 5          # dirty pads must not reach the tiled form
+    qt, st = q8.tile(q, s, N)
+    rq, rs = _tile_reference(q, s, N)
+    assert np.array_equal(qt, rq) and np.array_equal(st, rs)
+    assert q8.tiled_n(N) == -(-N // 128) * 128
+
+
+def test_tile_argument_errors(lib):
+    assert lib.q8_tile(None, C16, 32, 32, A16, B16) == 1
+    assert lib.q8_tile(A16, C16, 33, 32, A16, B16) == 2
+    assert lib.q8_tile_device(A16 + 1, C16, 32, 32, B16, D16, None) == 3
+    assert lib.q8_tiled_n(0) == -1 and lib.q8_tiled_n(1) == 128 and lib.q8_tiled_n(129) == 256
+    # tiled flag only with the pipelined kernel
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, 1, 2, None) == 1
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, 3, 2, None) == 1
+    assert lib.q8_gemv_argmax_ex(A16, B16, C16, D16, None, 1, 32, 32, 4, None) == 1
