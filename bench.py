@@ -3,13 +3,16 @@
 
 Workload (one step): the projection chain of a 32-layer 7B-class decode step over Q8_0 weights -- per layer q, k, v, o
 (4096 x 4096), gate and up (4096 x 14336) and down (14336 x 4096) -- then the tied head (4096 x 128256) with the
-arg-max over its fp32 logits fused.  224 q8_gemv calls and one q8_gemv_argmax, m activation rows each (m = 1 by
-default), 9.36 GB of weights per step at m = 1: every step reads far more than the 129 MB L2, so no flush is needed.
+arg-max over its fp32 logits fused.  Per layer q/k/v read one activation and gate/up another, as in a transformer
+layer, so each pair or triple is one q8_gemv_parts launch; o and down are q8_gemv launches: 128 layer launches and
+one q8_gemv_argmax, m activation rows each (m = 1 by default), 9.36 GB of weights per step at m = 1: every step reads
+far more than the 129 MB L2, so no flush is needed.
 Weights: q uniform int8 in [-127, 127] with a +-127 per block, s = 2^u/127, u ~ U[-8, -2], drawn on the device from a
 seed; activations bf16 N(0,1), drawn per layer.
 
-value = algorithmic bytes per step (K * Np * 1.125 + m * K * 2 + m * Np * 4 per GEMV; the head writes m * 8 index bytes
-instead of logits) / device time per step, summed over ranks (replicas: every rank runs the whole step on its own GPU).
+value = algorithmic bytes per step (K * Np * 1.125 per weight and m * Np * 4 per output, m * K * 2 per activation read
+by a launch; the head writes m * 8 index bytes instead of logits) / device time per step, summed over ranks (replicas:
+every rank runs the whole step on its own GPU).
 
 Arms:
   --impl ours       (default) the CUDA library, the chain captured as CUDA graphs and replayed per step;
@@ -34,7 +37,8 @@ METRIC = "Q8_0 GEMV achieved HBM GB/s (% of GB300 peak) and µs/call at m=1..16"
 LAYERS = 32
 HIDDEN, FFN, VOCAB = 4096, 14336, 128256
 WORKLOAD = (f"decode-step Q8_0 projection chain: {LAYERS} layers x (q,k,v,o 4096x4096; gate,up 4096x14336; "
-            f"down 14336x4096) + tied head 4096x128256 with fused arg-max")
+            f"down 14336x4096) + tied head 4096x128256 with fused arg-max; per layer q/k/v share one activation and "
+            f"gate/up another (one multi-projection launch each), o and down their own")
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -211,38 +215,52 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------------------------------------------------------------
 
 class Chain:
-    """Device-resident weights, activations and outputs of one decode step, and its CUDA graphs."""
+    """Device-resident weights, activations and outputs of one decode step, and its CUDA graphs.
+
+    The step's data flow is a transformer layer's: q, k and v multiply one activation (one q8_gemv_parts launch),
+    o its own, gate and up one more (one q8_gemv_parts launch), down its own; then the tied head with its arg-max.
+    Weights are stored tiled (q8_tile_device), as a model would store them once at load time."""
 
     def __init__(self, torch, m, seed=4000):
         import synth_inputs as si
+        import q8_block_quantized_gemv_gb300 as q8
         self.torch, self.m = torch, m
         self.shapes = chain_shapes()
-        import q8_block_quantized_gemv_gb300 as q8
-        # row-major weights as drawn, and the tiled storage the library streams (made once, as at model load)
+        # row-major weights as drawn, and the tiled storage the library streams
         self.w = [si.device_weight(K, N, seed + i) for i, (K, N) in enumerate(self.shapes)]
         self.head = si.device_weight(HIDDEN, VOCAB, seed + len(self.shapes))
         self.wt = [q8.tile_device(q, s, N) for (q, s), (_, N) in zip(self.w, self.shapes)]
         self.head_t = q8.tile_device(self.head[0], self.head[1], VOCAB)
-        torch.cuda.synchronize()
-        # activations: one [m, K] block per call, all in one buffer (the H2D copy of the end-to-end measurement)
-        sizes = [m * K for K, _ in self.shapes] + [m * HIDDEN]
+        # activations: per layer one for q/k/v, one for o, one for gate/up, one for down; then the head's
+        self.x_shapes = [K for _ in range(LAYERS) for K in (HIDDEN, HIDDEN, HIDDEN, FFN)] + [HIDDEN]
+        sizes = [m * K for K in self.x_shapes]
         self.x_all = torch.empty(sum(sizes), dtype=torch.bfloat16, device="cuda")
         g = torch.Generator(device="cuda")
         g.manual_seed(seed + 99991)
         self.x_all.copy_(torch.randn(sum(sizes), generator=g, device="cuda", dtype=torch.float32))
         self.x, off = [], 0
-        for K, _ in self.shapes + [(HIDDEN, VOCAB)]:
+        for K in self.x_shapes:
             self.x.append(self.x_all[off:off + m * K].view(m, K))
             off += m * K
         self.y = [torch.empty((m, padded(N)), dtype=torch.float32, device="cuda") for _, N in self.shapes]
         self.idx = torch.empty((m,), dtype=torch.int64, device="cuda")
         self.g_layers = self.g_head = None
+        torch.cuda.synchronize()
+
+    def layer_calls(self):
+        """(activation index, [GEMV indices]) of every launch of the layers, in order."""
+        calls = []
+        for layer in range(LAYERS):
+            base, xb = 7 * layer, 4 * layer
+            calls += [(xb, [base, base + 1, base + 2]), (xb + 1, [base + 3]), (xb + 2, [base + 4, base + 5]),
+                      (xb + 3, [base + 6])]
+        return calls
 
     def run_layers(self):
         import q8_block_quantized_gemv_gb300 as q8
-        for i, (K, N) in enumerate(self.shapes):
-            q, s = self.wt[i]
-            q8.gemv(self.x[i], q, s, N, y=self.y[i], constant_weights=True, tiled=True)
+        for xi, gis in self.layer_calls():
+            q8.gemv_parts(self.x[xi], [(self.wt[i][0], self.wt[i][1], self.shapes[i][1]) for i in gis],
+                          ys=[self.y[i] for i in gis], constant_weights=True, tiled=True)
 
     def run_head(self):
         import q8_block_quantized_gemv_gb300 as q8
@@ -266,7 +284,18 @@ class Chain:
         torch.cuda.synchronize()
 
     def launches_per_step(self):
-        return len(self.shapes) + 2  # 224 GEMV kernels, the head's GEMV kernel and its index decode
+        return len(self.layer_calls()) + 2  # the layers' launches, the head's GEMV kernel and its index decode
+
+    def layer_bytes(self):
+        """Algorithmic bytes of the layers' launches: weights, each activation once, outputs."""
+        m = self.m
+        total = 0.0
+        for xi, gis in self.layer_calls():
+            total += m * self.x_shapes[xi] * 2
+            for i in gis:
+                K, N = self.shapes[i]
+                total += K * padded(N) * 1.125 + m * padded(N) * 4
+        return total
 
 
 def run_ours(args, rank, world, local_rank):
@@ -316,7 +345,7 @@ def run_ours(args, rank, world, local_rank):
     layers_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     head_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     ms = max_over_ranks(ms)
-    bytes_step = step_bytes(m)
+    bytes_step = chain.layer_bytes() + gemv_bytes(m, HIDDEN, VOCAB, argmax=True)
     value = world * bytes_step / (ms * 1e-3) / 1e9
 
     # ---- end-to-end: host activations in, the step's tokens out, every step ----
@@ -344,7 +373,7 @@ def run_ours(args, rank, world, local_rank):
 
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    layer_bytes = sum(gemv_bytes(m, K, N) for K, N in chain.shapes)
+    layer_bytes = chain.layer_bytes()
     achieved = layer_bytes / (layers_ms * 1e-3) / 1e9
     traffic = None
     try:
@@ -359,14 +388,15 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "m": m, "calls_per_step": len(chain.shapes) + 1,
-                   "bytes_per_step": bytes_step, "us_per_call": ms * 1e3 / (len(chain.shapes) + 1),
+        "config": {"workload": WORKLOAD, "m": m, "gemvs_per_step": len(chain.shapes) + 1,
+                   "launches_per_step": chain.launches_per_step(),
+                   "bytes_per_step": bytes_step, "us_per_gemv": ms * 1e3 / (len(chain.shapes) + 1),
                    "pct_of_8TBps": 100.0 * bytes_step / (ms * 1e-3) / 8e12,
                    "layers_ms": layers_ms, "head_ms": head_ms,
                    "operands": "x bf16, W Q8_0 (int8 + fp32 scale per 32 rows), fp32 accumulation",
                    "l2": "inputs larger than L2 (9.4 GB of weights per step against 129 MB)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "q8_gemv (the 224 layer GEMVs of a step, back to back)",
+        "roofline": {"bound": "hbm", "kernel": "q8 stream kernel (the 128 layer launches of a step, back to back)",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic},
         "e2e": {"value": world * bytes_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -378,9 +408,11 @@ def run_ours(args, rank, world, local_rank):
         def host_case(i):
             if i < len(chain.shapes):
                 q, s = chain.w[i]
+                xi = [c[0] for c in chain.layer_calls() for _ in c[1]][i]
             else:
                 q, s = chain.head
-            return (chain.x[i].view(torch.int16).cpu().numpy().view("uint16"), q.cpu().numpy(), s.cpu().numpy())
+                xi = len(chain.x) - 1
+            return (chain.x[xi].view(torch.int16).cpu().numpy().view("uint16"), q.cpu().numpy(), s.cpu().numpy())
         gbs, desc, cores, _ = oracle_sample(m, args.cpu_budget, host_case)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
     if rank == 0:

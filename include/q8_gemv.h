@@ -124,6 +124,26 @@ q8_status q8_tile(const int8_t *q, const float *s, int K, int N, int8_t *qt, flo
  * the input and output must not overlap). */
 q8_status q8_tile_device(const int8_t *q, const float *s, int K, int N, int8_t *qt, float *st, q8_stream_t stream);
 
+/* One weight of a multi-projection call: its Q8_0 values and scales (row-major, or tiled with Q8_FLAG_TILED), its
+ * output y [m][q8_padded_n(N)] (written) and its N. */
+typedef struct q8_part {
+    const int8_t *q;
+    const float *s;
+    float *y;
+    int N;
+} q8_part;
+
+#define Q8_MAX_PARTS 8
+
+/* Several Q8_0 products of one activation: y_p = x . W_p for every part p (source: "plan.rs", `Launch::GemmParts`:
+ * projections of one activation -- q/k/v, or gate/up -- as one launch over their outputs side by side).
+ *   x      device bf16 [m][K], read once for all parts       parts  host array of nparts q8_part (read during the call)
+ *   1 <= nparts <= Q8_MAX_PARTS; every part has the same K; N may differ.  Each y_p is as q8_gemv writes it.
+ * With Q8_FLAG_TILED (weights in the q8_tile layout) the parts run as one kernel launch; row-major parts run one
+ * launch each.  Flags and errors as q8_gemv_ex; an output overlapping x, a weight or another output is Q8_ERR_ARG. */
+q8_status q8_gemv_parts(const void *x, const q8_part *parts, int nparts, int m, int K, unsigned int flags,
+                        q8_stream_t stream);
+
 /* Host repack of checkpoint blocks into the two stored tensors (source: "from_q8.rs", `Q8Part`: the host repacks the
  * checkpoint's blocks into the int8 values `q8_0.values` and the fp32 scales `q8_0.scales`).
  *   blocks  host, N * (K/32) blocks of 36 bytes, column-major by block: column n's blocks b = 0 .. K/32-1 in order;

@@ -45,7 +45,12 @@ SIGNATURES = {
     "q8_last_cuda_error": (_I, []),
     "q8_version": (_I, []),
     "q8_device_fault": (_I, [_P, _I]),
+    "q8_gemv_parts": (_I, [_P, _P, _I, _I, _I, ctypes.c_uint, _P]),
 }
+
+
+class _Part(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int)]
 
 _lib = None
 
@@ -195,6 +200,28 @@ def tile_device(q, s, N: int, stream=None):
     _check(lib().q8_tile_device(q.data_ptr(), s.data_ptr(), K, N, qt.data_ptr(), st.data_ptr(),
                                 _stream_handle(stream)), "q8_tile_device")
     return qt, st
+
+
+def gemv_parts(x, weights, ys=None, constant_weights: bool = False, tiled: bool = False, stream=None):
+    """Several products of one activation in one call (q8_gemv_parts): weights is a list of (q, s, N); returns the
+    list of outputs y_p, fp32 [m, Np_p]."""
+    import torch
+    if not weights or len(weights) > 8:
+        raise ValueError("1 to 8 parts")
+    m, K = x.shape
+    arr = (_Part * len(weights))()
+    outs = []
+    for i, (q, s, N) in enumerate(weights):
+        _check_operands(x, q, s, N, tiled)
+        Np = padded_n(N)
+        y = ys[i] if ys is not None else torch.empty((m, Np), dtype=torch.float32, device=x.device)
+        if y.dtype != torch.float32 or y.shape != (m, Np) or not y.is_contiguous() or not y.is_cuda:
+            raise ValueError("each y must be a contiguous fp32 CUDA tensor [m, Np]")
+        arr[i] = _Part(q.data_ptr(), s.data_ptr(), y.data_ptr(), N)
+        outs.append(y)
+    _check(lib().q8_gemv_parts(x.data_ptr(), ctypes.cast(arr, ctypes.c_void_p), len(weights), m, K,
+                               _flags(constant_weights, tiled), _stream_handle(stream)), "q8_gemv_parts")
+    return outs
 
 
 def device_fault(clear: bool = False) -> int:

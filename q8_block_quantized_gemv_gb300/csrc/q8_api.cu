@@ -60,23 +60,19 @@ struct Plan {
 // Kernel family, per-lane width and K split for a shape.  The widest tile that still gives every SM a CTA is
 // preferred; K is split across a cluster (at most 8 CTAs, the portable size) until the grid holds about two CTAs per
 // SM, the residency the kernels are built for.
-Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms) {
+Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long tiled_tiles = 0) {
     const int nb = K / Q8_BLOCK;
     if (tiled) {
-        // The tiled layout: per-warp cp.async streams, 128-column tiles.  The kernel is bound by the SMs' issue rate,
-        // so an SM's time is the work of all the CTAs it runs: the K split is the one whose busiest SM (CTAs per SM,
-        // each its blocks plus about two blocks of fixed work) finishes first.
-        const long long tiles = (Np + q8::kTmaColumns - 1) / q8::kTmaColumns;
-        int best = 1;
-        double best_cost = 1e300;
-        for (int ks = 1; ks <= 8 && ks <= nb; ++ks) {
-            const long long per_sm = (tiles * ks + sms - 1) / sms;
-            const double cost = (double)per_sm * (2.0 + (double)((nb + ks - 1) / ks));
-            if (cost < best_cost) {
-                best_cost = cost;
-                best = ks;
-            }
-        }
+        // The tiled layout: per-warp cp.async streams, 128-column tiles.  Measured on GB300, the best K split is
+        // the largest one whose CTAs still fit in one wave of resident CTAs (a second, partial wave and the cluster
+        // reduction both cost more than the idle SMs of a short wave): ks = resident slots / tiles, at least 1.
+        const long long tiles = tiled_tiles > 0 ? tiled_tiles : (Np + q8::kTmaColumns - 1) / q8::kTmaColumns;
+        const long long slots = (long long)q8::stream_ctas_per_sm(m) * sms;
+        long long ks = slots / tiles;
+        if (ks > 8) ks = 8;
+        if (ks > nb) ks = nb;
+        if (ks < 1) ks = 1;
+        int best = (int)ks;
         const char *force = getenv("Q8_KSPLIT");
         if (force) {
             const int f = atoi(force);
@@ -136,16 +132,29 @@ q8_status check_gemv_args(const void *x, const int8_t *q, const float *s, int m,
     return Q8_OK;
 }
 
-q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStream_t stream) {
+int tiles_of(int N) { return (N + q8::kTmaColumns - 1) / q8::kTmaColumns; }
+
+q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStream_t stream,
+              const q8::Parts *parts = nullptr) {
     int sms = 0;
     int e = sm_count(&sms);
     if (e != 0) return cuda_fail((cudaError_t)e);
     const bool tiled = (flags & Q8_FLAG_TILED) != 0;
-    const Plan p = make_plan(a.m, a.K, a.Np, variant, tiled, sms);
+    q8::Parts one = {};
+    if (tiled && !parts) {
+        one.q[0] = a.q;
+        one.s[0] = a.s;
+        one.y[0] = a.y;
+        one.N[0] = a.N;
+        one.tile_end[0] = tiles_of(a.N);
+        one.count = 1;
+        parts = &one;
+    }
+    const Plan p = make_plan(a.m, a.K, a.Np, variant, tiled, sms, parts ? parts->tile_end[parts->count - 1] : 0);
     Args b = a;
     b.ksplit = p.ksplit;
     const bool prefetch = (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0;
-    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, argmax, stream, true, prefetch)
+    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, argmax, stream, true, prefetch)
                      : p.variant == Q8_VARIANT_TMA  ? q8::launch_tma(b, argmax, stream, true, prefetch)
                      : p.variant == Q8_VARIANT_SIMT ? q8::launch_simt(b, p.V, argmax, stream)
                                                     : q8::launch_mma(b, p.V, argmax, stream);
@@ -225,6 +234,58 @@ extern "C" q8_status q8_gemv_argmax_ex(const void *x, const int8_t *q, const flo
 extern "C" q8_status q8_gemv_argmax(const void *x, const int8_t *q, const float *s, int64_t *idx, float *logits,
                                     int m, int K, int N, q8_stream_t stream) {
     return q8_gemv_argmax_ex(x, q, s, idx, logits, m, K, N, 0u, stream);
+}
+
+extern "C" q8_status q8_gemv_parts(const void *x, const q8_part *parts, int nparts, int m, int K,
+                                   unsigned int flags, q8_stream_t stream) {
+    if (!x || !parts) return Q8_ERR_ARG;
+    if (nparts < 1 || nparts > Q8_MAX_PARTS) return Q8_ERR_ARG;
+    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    const bool tiled = (flags & Q8_FLAG_TILED) != 0;
+    for (int i = 0; i < nparts; ++i) {
+        const q8_part &p = parts[i];
+        q8_status st = check_gemv_args(x, p.q, p.s, m, K, p.N);
+        if (st != Q8_OK) return st;
+        if (!p.y) return Q8_ERR_ARG;
+        if (!aligned(p.y, 16)) return Q8_ERR_ALIGN;
+        if (tiled && q8_tiled_n(p.N) < 0) return Q8_ERR_SHAPE;
+    }
+    // No output may overlap the activation, any weight or any other output.
+    for (int i = 0; i < nparts; ++i) {
+        const size_t ybytes = (size_t)m * q8_padded_n(parts[i].N) * 4;
+        if (overlaps(parts[i].y, ybytes, x, (size_t)m * K * 2)) return Q8_ERR_ARG;
+        for (int j = 0; j < nparts; ++j) {
+            const size_t wcols = tiled ? (size_t)q8_tiled_n(parts[j].N) : (size_t)q8_padded_n(parts[j].N);
+            if (overlaps(parts[i].y, ybytes, parts[j].q, (size_t)K * wcols) ||
+                overlaps(parts[i].y, ybytes, parts[j].s, (size_t)(K / Q8_BLOCK) * wcols * 4))
+                return Q8_ERR_ARG;
+            if (j != i && overlaps(parts[i].y, ybytes, parts[j].y, (size_t)m * q8_padded_n(parts[j].N) * 4))
+                return Q8_ERR_ARG;
+        }
+    }
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (!tiled) {  // the row-major kernels take one weight a launch
+        for (int i = 0; i < nparts; ++i) {
+            q8_status st = q8_gemv_ex(x, parts[i].q, parts[i].s, parts[i].y, m, K, parts[i].N, Q8_VARIANT_AUTO,
+                                      flags, stream);
+            if (st != Q8_OK) return st;
+        }
+        return Q8_OK;
+    }
+    q8::Parts pt = {};
+    int tiles = 0;
+    for (int i = 0; i < nparts; ++i) {
+        pt.q[i] = parts[i].q;
+        pt.s[i] = parts[i].s;
+        pt.y[i] = parts[i].y;
+        pt.N[i] = parts[i].N;
+        tiles += tiles_of(parts[i].N);
+        pt.tile_end[i] = tiles;
+    }
+    pt.count = nparts;
+    Args a = {static_cast<const uint16_t *>(x), parts[0].q, parts[0].s, parts[0].y, nullptr, m, K, parts[0].N,
+              q8_padded_n(parts[0].N), K / Q8_BLOCK, 1};
+    return run(a, Q8_VARIANT_AUTO, flags, false, cs, &pt);
 }
 
 extern "C" q8_status q8_device_fault(unsigned int *fault, int clear) {

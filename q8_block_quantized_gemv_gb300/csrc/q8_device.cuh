@@ -36,6 +36,35 @@ struct Args {
     int ksplit;                // CTAs of a cluster splitting K (grid.y)
 };
 
+// Several weights that multiply one activation in one launch ("plan.rs", `Launch::GemmParts`: projections of one
+// activation as one launch over their outputs side by side).  Part p owns the column tiles [tile_end[p-1],
+// tile_end[p]) of the launch's grid; q, s and y are its own, as is N.
+constexpr int kMaxParts = 8;
+struct Parts {
+    const int8_t *q[kMaxParts];
+    const float *s[kMaxParts];
+    float *y[kMaxParts];
+    int N[kMaxParts];
+    int tile_end[kMaxParts];
+    int count;
+};
+
+// The part owning grid tile `tile` and the tile's index within it; `a` gets that part's q, s, y and N.
+__device__ __forceinline__ int select_part(const Parts &pt, int tile, Args &a) {
+    int p = 0, first = 0;
+#pragma unroll 1
+    while (p + 1 < pt.count && tile >= pt.tile_end[p]) {
+        first = pt.tile_end[p];
+        ++p;
+    }
+    a.q = pt.q[p];
+    a.s = pt.s[p];
+    a.y = pt.y[p];
+    a.N = pt.N[p];
+    a.Np = (pt.N[p] + kBlock - 1) / kBlock * kBlock;
+    return tile - first;
+}
+
 // ------------------------------------------------------------------------------------------------------------------
 // loads
 // ------------------------------------------------------------------------------------------------------------------
@@ -131,15 +160,14 @@ __host__ __device__ constexpr int finish_smem_n(int NRED, int MR, int TC) { retu
 __host__ __device__ constexpr int finish_smem_bytes(int MR, int TC) { return finish_smem_n(kWarps, MR, TC); }
 
 // The epilogue.  On entry the CTA's NRED partial carries sit in red[NRED][MR][TC] (rows < MR, columns < TC of this
-// CTA's tile) and the CTA has synchronised.  Sums the slabs in order, then (ksplit > 1) the cluster's ranks in order,
+// CTA's column tile `tile` of the output) and the CTA has synchronised.  Sums the slabs in order, then (ksplit > 1) the cluster's ranks in order,
 // writes y (0 in the pad columns) and folds this CTA's columns into the per-row arg-max keys.
 template <int NRED, int MR, int TC, int NTHREADS, bool ARGMAX>
-__device__ __forceinline__ void finish_n(const Args &a, float *red) {
+__device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
     namespace cg = cooperative_groups;
     float *part = red + NRED * MR * TC;                                                   // [MR][TC]
     unsigned long long *rowkey = reinterpret_cast<unsigned long long *>(part + MR * TC);  // [MR]
     const int rows = a.m < MR ? a.m : MR;
-    const int tile = blockIdx.x;
 
     for (int i = threadIdx.x; i < rows * TC; i += NTHREADS) {
         float v = 0.0f;
@@ -188,7 +216,7 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red) {
 
 template <int MR, int TC, bool ARGMAX>
 __device__ __forceinline__ void finish(const Args &a, float *smem) {
-    finish_n<kWarps, MR, TC, kThreads, ARGMAX>(a, smem);
+    finish_n<kWarps, MR, TC, kThreads, ARGMAX>(a, smem, blockIdx.x);
 }
 
 }  // namespace q8

@@ -47,7 +47,8 @@ cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl
 
 // Defined in q8_stream.cu (the tiled layout).
 int stream_ctas_per_sm(int m);
-cudaError_t launch_stream(const Args &a, bool argmax, cudaStream_t stream, bool pdl, bool prefetch_weights);
+cudaError_t launch_stream(const Args &a, const Parts &parts, bool argmax, cudaStream_t stream, bool pdl,
+                          bool prefetch_weights);
 cudaError_t read_fault_word(unsigned *out, bool clear);
 constexpr int kTmaColumns = 128;
 

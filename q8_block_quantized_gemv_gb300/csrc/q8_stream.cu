@@ -62,6 +62,32 @@ __device__ __forceinline__ uint2 ld_cg_u2(const void *p) {
     return v;
 }
 
+// Packed fp32 pairs (one 64-bit register pair) for the CUDA-core inner loop.
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+    unsigned long long d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void unpack_f32x2(unsigned long long v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// Bytes e and e + 1 of a sign-flipped int8 word (see q8_to_f32) as the exact fp32 pair {q_e, q_e+1}: two byte
+// permutes into the mantissa of 2^23 and one packed subtract of 2^23 + 128.
+template <int E> __device__ __forceinline__ unsigned long long q8x2_to_f32x2(uint32_t u) {
+    unsigned long long d;
+    asm("{\n .reg .b32 a, b;\n .reg .b64 p, c;\n prmt.b32 a, %1, 0x4B000000, %2;\n prmt.b32 b, %1, 0x4B000000, %3;\n"
+        " mov.b64 p, {a, b};\n mov.b64 c, {%4, %4};\n sub.rn.f32x2 %0, p, c;\n}"
+        : "=l"(d)
+        : "r"(u), "n"(0x7540 + E), "n"(0x7540 + E + 1), "r"(0x4B000080u));
+    return d;
+}
+
 // Copy unit `u` (values and scales) into `stage`: 8 + 1 cp.async of 16 bytes per lane.
 __device__ __forceinline__ void issue_unit(unsigned char *stage, const int8_t *q, const float *s, size_t u, int lane) {
     const unsigned char *src = reinterpret_cast<const unsigned char *>(q) + u * kUnit + lane * 16;
@@ -72,13 +98,13 @@ __device__ __forceinline__ void issue_unit(unsigned char *stage, const int8_t *q
 
 template <int NT, bool ARGMAX>
 __global__ void __launch_bounds__(kThreadsS, NT == 1 ? 2 : 1)
-    stream_kernel(const Args a, const int prefetch_weights) {
+    stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     constexpr int MR = 8 * NT;
     constexpr int kDepth = StreamShape<NT>::kDepth;
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int tile = blockIdx.x;
+    const int tile = select_part(parts, blockIdx.x, a);
     const int rank = blockIdx.y;
     const int c0 = (int)((long long)a.nb * rank / a.ksplit);
     const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
@@ -219,23 +245,156 @@ __global__ void __launch_bounds__(kThreadsS, NT == 1 ? 2 : 1)
             *reinterpret_cast<float2 *>(mine + (r + 1) * kTmaColumns + c) = make_float2(acc[nt][p][1], acc[nt][p][3]);
         }
     __syncthreads();
-    finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, ARGMAX>(a, red);
+    finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
+}
+
+
+// The CUDA-core inner loop over the same stream, for m <= 2 (where the per-row FMAs are cheaper than packing bf16
+// MMA operands).  In segment (s, j) lane L = 4g + u holds 16 columns 16g .. 16g + 15 of weight row 16s + 4u + j: it
+// converts each pair of values to an exact fp32 pair and accumulates x[r, row] * q into the block's sums with packed
+// fp32x2 FMAs, folds the sums into its carry with the block's scales, and at the end the four lanes u of a column
+// group add their carries (rows 4u + j of every step) in a fixed order.
+template <int M, bool ARGMAX>
+__global__ void __launch_bounds__(kThreadsS, 2)
+    stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
+    constexpr int kDepth = StreamShape<1>::kDepth;
+    extern __shared__ __align__(16) unsigned char smem_s[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, u = lane & 3;
+    const int tile = select_part(parts, blockIdx.x, a);
+    const int rank = blockIdx.y;
+    const int c0 = (int)((long long)a.nb * rank / a.ksplit);
+    const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
+    const int b0 = c0 + (c1 - c0) * warp / kWarpsS;
+    const int b1 = c0 + (c1 - c0) * (warp + 1) / kWarpsS;
+    const int n = b1 - b0;
+    unsigned char *ring = smem_s + warp * kDepth * kStageS;
+    const size_t unit0 = (size_t)tile * a.nb + b0;
+
+    unsigned long long acc[M][8];  // fp32 pairs: columns 16g + 2p, 16g + 2p + 1
+#pragma unroll
+    for (int r = 0; r < M; ++r)
+#pragma unroll
+        for (int p = 0; p < 8; ++p) acc[r][p] = 0ull;
+
+    if (prefetch_weights) {
+#pragma unroll
+        for (int i = 0; i < kDepth - 1; ++i) {
+            if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
+            cp_async_commit();
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!prefetch_weights) {
+#pragma unroll
+        for (int i = 0; i < kDepth - 1; ++i) {
+            if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
+            cp_async_commit();
+        }
+    }
+
+    // x[r][32b + 16s + 4u .. + 3]: the activations of this lane's rows, two 8-byte loads per row and block.
+    uint2 xf[M][2];
+    auto load_x = [&](int b) {
+#pragma unroll
+        for (int r = 0; r < M; ++r)
+#pragma unroll
+            for (int s = 0; s < 2; ++s) xf[r][s] = ld_cg_u2(a.x + (size_t)r * a.K + (size_t)b * kBlock + 16 * s + 4 * u);
+    };
+    if (n > 0) load_x(b0);
+
+    for (int i = 0; i < n; ++i) {
+        const int ahead = i + kDepth - 1;
+        if (ahead < n) issue_unit(ring + (ahead % kDepth) * kStageS, a.q, a.s, unit0 + ahead, lane);
+        cp_async_commit();
+        cp_async_wait<kDepth - 1>();
+        __syncwarp();
+        const unsigned char *st = ring + (i % kDepth) * kStageS;
+        uint2 xc[M][2];
+#pragma unroll
+        for (int r = 0; r < M; ++r)
+#pragma unroll
+            for (int s = 0; s < 2; ++s) xc[r][s] = xf[r][s];
+        if (i + 1 < n) load_x(b0 + i + 1);
+
+        unsigned long long part[M][8];
+#pragma unroll
+        for (int r = 0; r < M; ++r)
+#pragma unroll
+            for (int p = 0; p < 8; ++p) part[r][p] = 0ull;
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(st + (s * 4 + j) * 512 + lane * 16);
+                unsigned long long xx[M];
+#pragma unroll
+                for (int r = 0; r < M; ++r) {
+                    const uint32_t pr = (j < 2) ? xc[r][s].x : xc[r][s].y;
+                    const float xv = (j & 1) ? bf16_hi(pr) : bf16_lo(pr);
+                    xx[r] = pack_f32x2(xv, xv);
+                }
+#pragma unroll
+                for (int wi = 0; wi < 4; ++wi) {
+                    const uint32_t uw = word_of(w, wi) ^ 0x80808080u;
+                    const unsigned long long q01 = q8x2_to_f32x2<0>(uw);
+                    const unsigned long long q23 = q8x2_to_f32x2<2>(uw);
+#pragma unroll
+                    for (int r = 0; r < M; ++r) {
+                        part[r][2 * wi] = fma_f32x2(q01, xx[r], part[r][2 * wi]);
+                        part[r][2 * wi + 1] = fma_f32x2(q23, xx[r], part[r][2 * wi + 1]);
+                    }
+                }
+            }
+        unsigned long long sc[8];
+        const uint4 *ss = reinterpret_cast<const uint4 *>(st + kUnit) + 4 * g;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+            const uint4 f = ss[v4];
+            sc[2 * v4] = ((unsigned long long)f.y << 32) | f.x;
+            sc[2 * v4 + 1] = ((unsigned long long)f.w << 32) | f.z;
+        }
+        __syncwarp();  // every lane is done with this stage before it is refilled
+#pragma unroll
+        for (int r = 0; r < M; ++r)
+#pragma unroll
+            for (int p = 0; p < 8; ++p) acc[r][p] = fma_f32x2(sc[p], part[r][p], acc[r][p]);
+    }
+    cp_async_wait<0>();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __syncthreads();
+
+    float *red = reinterpret_cast<float *>(smem_s);  // [kWarpsS][M][128]
+    float *mine = red + warp * M * kTmaColumns;
+#pragma unroll
+    for (int r = 0; r < M; ++r)
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            float lo, hi;
+            unpack_f32x2(acc[r][p], lo, hi);
+            lo += __shfl_xor_sync(0xffffffffu, lo, 1);
+            hi += __shfl_xor_sync(0xffffffffu, hi, 1);
+            lo += __shfl_xor_sync(0xffffffffu, lo, 2);
+            hi += __shfl_xor_sync(0xffffffffu, hi, 2);
+            if (u == 0) *reinterpret_cast<float2 *>(mine + r * kTmaColumns + 16 * g + 2 * p) = make_float2(lo, hi);
+        }
+    __syncthreads();
+    finish_n<kWarpsS, M, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
 }
 
 static_assert(finish_smem_n(kWarpsS, 8, kTmaColumns) <= StreamShape<1>::kSmem, "the epilogue fits in the rings");
 static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns) <= StreamShape<2>::kSmem, "the epilogue fits in the rings");
 static_assert(2 * StreamShape<1>::kSmem <= 227 * 1024 && StreamShape<2>::kSmem <= 227 * 1024, "residency");
 
-template <int NT, bool ARGMAX>
-cudaError_t launch_stream_nt(const Args &a, cudaStream_t stream, bool pdl, bool prefetch) {
-    auto kernel = stream_kernel<NT, ARGMAX>;
-    constexpr int kSmemS = StreamShape<NT>::kSmem;
+template <typename Kernel>
+cudaError_t launch_stream_kernel(Kernel kernel, int kSmemS, const Args &a, const Parts &pt, cudaStream_t stream,
+                                 bool pdl, bool prefetch) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.Np + kTmaColumns - 1) / kTmaColumns), (unsigned)a.ksplit, 1);
+    cfg.gridDim = dim3((unsigned)pt.tile_end[pt.count - 1], (unsigned)a.ksplit, 1);
     cfg.blockDim = dim3(kThreadsS, 1, 1);
     cfg.dynamicSmemBytes = kSmemS;
     cfg.stream = stream;
@@ -255,19 +414,32 @@ cudaError_t launch_stream_nt(const Args &a, cudaStream_t stream, bool pdl, bool 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kernel, a, prefetch ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, kernel, a, pt, prefetch ? 1 : 0);
 }
 
 }  // namespace
 
 int stream_ctas_per_sm(int m) { return m <= 8 ? 2 : 1; }
 
-cudaError_t launch_stream(const Args &a, bool argmax, cudaStream_t stream, bool pdl, bool prefetch_weights) {
+cudaError_t launch_stream(const Args &a, const Parts &pt, bool argmax, cudaStream_t stream, bool pdl,
+                          bool prefetch_weights) {
+    constexpr int s1 = StreamShape<1>::kSmem, s2 = StreamShape<2>::kSmem;
+    const bool p = prefetch_weights;
+    switch (a.m) {
+        case 1:
+            return argmax ? launch_stream_kernel(stream_simt_kernel<1, true>, s1, a, pt, stream, pdl, p)
+                          : launch_stream_kernel(stream_simt_kernel<1, false>, s1, a, pt, stream, pdl, p);
+        case 2:
+            return argmax ? launch_stream_kernel(stream_simt_kernel<2, true>, s1, a, pt, stream, pdl, p)
+                          : launch_stream_kernel(stream_simt_kernel<2, false>, s1, a, pt, stream, pdl, p);
+        default:
+            break;
+    }
     if (a.m <= 8)
-        return argmax ? launch_stream_nt<1, true>(a, stream, pdl, prefetch_weights)
-                      : launch_stream_nt<1, false>(a, stream, pdl, prefetch_weights);
-    return argmax ? launch_stream_nt<2, true>(a, stream, pdl, prefetch_weights)
-                  : launch_stream_nt<2, false>(a, stream, pdl, prefetch_weights);
+        return argmax ? launch_stream_kernel(stream_kernel<1, true>, s1, a, pt, stream, pdl, p)
+                      : launch_stream_kernel(stream_kernel<1, false>, s1, a, pt, stream, pdl, p);
+    return argmax ? launch_stream_kernel(stream_kernel<2, true>, s2, a, pt, stream, pdl, p)
+                  : launch_stream_kernel(stream_kernel<2, false>, s2, a, pt, stream, pdl, p);
 }
 
 }  // namespace q8

@@ -323,7 +323,7 @@ __global__ void __maxnreg__(128)
             }
     }
     __syncthreads();
-    finish_n<NCLS, MR, kTmaColumns, S::kThreads, ARGMAX>(a, red);
+    finish_n<NCLS, MR, kTmaColumns, S::kThreads, ARGMAX>(a, red, blockIdx.x);
 }
 
 static_assert(finish_smem_n(TmaShape<1>::kClasses, 8, kTmaColumns) <= kStages * kWeightStage, "epilogue fits");

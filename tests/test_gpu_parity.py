@@ -364,3 +364,37 @@ def test_tile_device_matches_host(dev, K, N):
     qtd, std = q8.tile_device(qd, sd, N)
     torch.cuda.synchronize()
     assert np.array_equal(qtd.cpu().numpy(), qt) and np.array_equal(std.cpu().numpy(), st)
+
+
+@pytest.mark.parametrize("tiled", [True, False])
+@pytest.mark.parametrize("m", [1, 3, 16])
+def test_gemv_parts(dev, m, tiled, monkeypatch):
+    """Several weights of one activation in one call (q/k/v-style widths and a ragged one): each output against the
+    oracle, and -- with the K split pinned, so that both calls sum in the same order -- bit-identical to the
+    single-weight call on the same layout."""
+    monkeypatch.setenv("Q8_KSPLIT", "2")
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    K = 2048
+    Ns = [1024, 3000, 512, 40]
+    x, _, _ = si.case(m, K, 32, 5100 + m)
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    ws, devw = [], []
+    for i, N in enumerate(Ns):
+        _, q, s = si.case(1, K, N, 5200 + 10 * i)
+        ws.append((q, s))
+        qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+        if tiled:
+            qd, sd = q8.tile_device(qd, sd, N)
+        devw.append((qd, sd, N))
+    ys = q8.gemv_parts(xd, devw, tiled=tiled, constant_weights=True)
+    torch.cuda.synchronize()
+    for i, N in enumerate(Ns):
+        q, s = ws[i]
+        y_o, a_o = oracle.gemv(x, q, s)
+        got = ys[i].cpu().numpy()
+        _assert_close(got, y_o, a_o, f"part {i} N={N}")
+        assert np.all(got[:, N:] == 0.0)
+        single = q8.gemv(xd, devw[i][0], devw[i][1], N, tiled=tiled).cpu().numpy()
+        if tiled:
+            assert np.array_equal(single.view(np.uint32), got.view(np.uint32))

@@ -238,3 +238,22 @@ def test_tile_argument_errors(lib):
     assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, 1, 2, None) == 1
     assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 32, 3, 2, None) == 1
     assert lib.q8_gemv_argmax_ex(A16, B16, C16, D16, None, 1, 32, 32, 4, None) == 1
+
+
+def test_gemv_parts_argument_errors(lib):
+    import ctypes
+    P = q8._Part
+    good = (P * 2)(P(B16, C16, D16, 64), P(0x50000, 0x60000, 0x70000, 96))
+    assert lib.q8_gemv_parts(None, ctypes.cast(good, ctypes.c_void_p), 2, 1, 32, 0, None) == 1   # null x
+    assert lib.q8_gemv_parts(A16, None, 2, 1, 32, 0, None) == 1                                  # null parts
+    assert lib.q8_gemv_parts(A16, ctypes.cast(good, ctypes.c_void_p), 0, 1, 32, 0, None) == 1     # no parts
+    assert lib.q8_gemv_parts(A16, ctypes.cast(good, ctypes.c_void_p), 9, 1, 32, 0, None) == 1     # too many
+    assert lib.q8_gemv_parts(A16, ctypes.cast(good, ctypes.c_void_p), 2, 17, 32, 0, None) == 2    # m > 16
+    assert lib.q8_gemv_parts(A16, ctypes.cast(good, ctypes.c_void_p), 2, 1, 33, 0, None) == 2     # K % 32
+    assert lib.q8_gemv_parts(A16, ctypes.cast(good, ctypes.c_void_p), 2, 1, 32, 8, None) == 1     # unknown flag
+    bad = (P * 2)(P(B16, C16, D16, 64), P(0x50000, 0x60000, 0x70004, 96))
+    assert lib.q8_gemv_parts(A16, ctypes.cast(bad, ctypes.c_void_p), 2, 1, 32, 0, None) == 3      # misaligned y
+    clash = (P * 2)(P(B16, C16, D16, 64), P(0x50000, 0x60000, D16, 96))
+    assert lib.q8_gemv_parts(A16, ctypes.cast(clash, ctypes.c_void_p), 2, 1, 32, 0, None) == 1    # outputs overlap
+    zero = (P * 1)(P(B16, C16, D16, 0))
+    assert lib.q8_gemv_parts(A16, ctypes.cast(zero, ctypes.c_void_p), 1, 1, 32, 0, None) == 2     # N = 0
