@@ -108,17 +108,20 @@ __device__ __forceinline__ float q8_to_f32(uint32_t u, int e) {
 __device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
 
+// The packed fp32 pair {2^23 + 128, 2^23 + 128}: subtracted from two magic floats it leaves two int8 values.
+constexpr unsigned long long kMagicPair = 0x4B0000804B000080ull;
+
 // Byte e of two sign-flipped int8 words (see q8_to_f32) as one exact bf16 pair, lo from `ua` in the low half: the two
 // magic floats are made by byte permutes, reduced to the integers by one packed fp32x2 subtract, then packed to bf16
-// (exact: |q| <= 127 needs 8 significant bits).
-__device__ __forceinline__ uint32_t q8x2_to_bf16x2(uint32_t ua, uint32_t ub, int e) {
-    const uint32_t fa = __byte_perm(ua, 0x4B000000u, 0x7540u | (uint32_t)e);
-    const uint32_t fb = __byte_perm(ub, 0x4B000000u, 0x7540u | (uint32_t)e);
+// (exact: |q| <= 127 needs 8 significant bits).  `magic` is kMagicPair, held in a register pair by the caller.
+template <int E>
+__device__ __forceinline__ uint32_t q8x2_to_bf16x2(uint32_t ua, uint32_t ub, unsigned long long magic) {
     uint32_t out;
-    asm("{\n .reg .b64 a, c, d;\n .reg .f32 lo, hi;\n mov.b64 a, {%1, %2};\n mov.b64 c, {%3, %3};\n"
-        " sub.rn.f32x2 d, a, c;\n mov.b64 {lo, hi}, d;\n cvt.rn.bf16x2.f32 %0, hi, lo;\n}"
+    asm("{\n .reg .b32 a, b;\n .reg .b64 p, d;\n .reg .f32 lo, hi;\n prmt.b32 a, %1, 0x4B000000, %3;\n"
+        " prmt.b32 b, %2, 0x4B000000, %3;\n mov.b64 p, {a, b};\n sub.rn.f32x2 d, p, %4;\n mov.b64 {lo, hi}, d;\n"
+        " cvt.rn.bf16x2.f32 %0, hi, lo;\n}"
         : "=r"(out)
-        : "r"(fa), "r"(fb), "r"(0x4B000080u));
+        : "r"(ua), "r"(ub), "n"(0x7540 + E), "l"(magic));
     return out;
 }
 

@@ -93,11 +93,14 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(const Args a) {
                 const uint32_t u2 = word_of(w[2], wi) ^ 0x80808080u;
                 const uint32_t u3 = word_of(w[3], wi) ^ 0x80808080u;
                 uint32_t lo[4], hi[4];  // per column: rows (4t, 4t+1) and (4t+2, 4t+3) as bf16 pairs
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    lo[e] = q8x2_to_bf16x2(u0, u1, e);
-                    hi[e] = q8x2_to_bf16x2(u2, u3, e);
-                }
+                lo[0] = q8x2_to_bf16x2<0>(u0, u1, kMagicPair);
+                lo[1] = q8x2_to_bf16x2<1>(u0, u1, kMagicPair);
+                lo[2] = q8x2_to_bf16x2<2>(u0, u1, kMagicPair);
+                lo[3] = q8x2_to_bf16x2<3>(u0, u1, kMagicPair);
+                hi[0] = q8x2_to_bf16x2<0>(u2, u3, kMagicPair);
+                hi[1] = q8x2_to_bf16x2<1>(u2, u3, kMagicPair);
+                hi[2] = q8x2_to_bf16x2<2>(u2, u3, kMagicPair);
+                hi[3] = q8x2_to_bf16x2<3>(u2, u3, kMagicPair);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {  // the two column pairs of this word
                     const int p = 2 * wi + h;

@@ -17,7 +17,7 @@
 // into an fp32 carry).  The MMA's K order is the relabeling of the register-fed kernel: MMA reduction index 2t, 2t+1,
 // 2t+8, 2t+9 is weight row 4t, 4t+1, 4t+2, 4t+3, so a lane's activation fragment is 4 consecutive activations.
 //
-// Activations are read from L2 (ld.global.cg), one block ahead.  With programmatic dependent launch every thread
+// Activations are read from L2 (ld.global.cg), two blocks ahead.  With programmatic dependent launch every thread
 // waits for the previous kernel (griddepcontrol.wait) before it reads x or writes y; with Q8_FLAG_CONSTANT_WEIGHTS
 // the first two stages' weights are already requested before that wait.
 #include "q8_launch.h"
@@ -56,6 +56,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same MMA into a fresh accumulator (C = 0): the first 16 rows of a block start the block's sums.
+__device__ __forceinline__ void mma_16816_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 __device__ __forceinline__ uint2 ld_cg_u2(const void *p) {
     uint2 v;
     asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
@@ -79,12 +89,12 @@ __device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, un
 }
 // Bytes e and e + 1 of a sign-flipped int8 word (see q8_to_f32) as the exact fp32 pair {q_e, q_e+1}: two byte
 // permutes into the mantissa of 2^23 and one packed subtract of 2^23 + 128.
-template <int E> __device__ __forceinline__ unsigned long long q8x2_to_f32x2(uint32_t u) {
+template <int E> __device__ __forceinline__ unsigned long long q8x2_to_f32x2(uint32_t u, unsigned long long magic) {
     unsigned long long d;
-    asm("{\n .reg .b32 a, b;\n .reg .b64 p, c;\n prmt.b32 a, %1, 0x4B000000, %2;\n prmt.b32 b, %1, 0x4B000000, %3;\n"
-        " mov.b64 p, {a, b};\n mov.b64 c, {%4, %4};\n sub.rn.f32x2 %0, p, c;\n}"
+    asm("{\n .reg .b32 a, b;\n .reg .b64 p;\n prmt.b32 a, %1, 0x4B000000, %2;\n prmt.b32 b, %1, 0x4B000000, %3;\n"
+        " mov.b64 p, {a, b};\n sub.rn.f32x2 %0, p, %4;\n}"
         : "=l"(d)
-        : "r"(u), "n"(0x7540 + E), "n"(0x7540 + E + 1), "r"(0x4B000080u));
+        : "r"(u), "n"(0x7540 + E), "n"(0x7540 + E + 1), "l"(magic));
     return d;
 }
 
@@ -148,15 +158,17 @@ __global__ void __launch_bounds__(kThreadsS, NT == 1 ? 2 : 1)
         xlive[nt] = r < a.m;
         xrow[nt] = a.x + (size_t)(xlive[nt] ? r : 0) * a.K + 4 * t;
     }
-    uint2 xf[2][NT];  // this block's activation fragments, one step per entry
-    auto load_x = [&](int b) {
+    // Activation fragments two blocks ahead (L2 latency exceeds a block's work): xn1 for block i + 1, xn2 for i + 2.
+    uint2 xn1[2][NT], xn2[2][NT];
+    auto load_x = [&](uint2 (&dst)[2][NT], int b) {
 #pragma unroll
         for (int step = 0; step < 2; ++step)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-                xf[step][nt] = xlive[nt] ? ld_cg_u2(xrow[nt] + (size_t)b * kBlock + 16 * step) : make_uint2(0u, 0u);
+                dst[step][nt] = xlive[nt] ? ld_cg_u2(xrow[nt] + (size_t)b * kBlock + 16 * step) : make_uint2(0u, 0u);
     };
-    if (n > 0) load_x(b0);
+    if (n > 0) load_x(xn1, b0);
+    if (n > 1) load_x(xn2, b0 + 1);
 
     for (int i = 0; i < n; ++i) {
         const int ahead = i + kDepth - 1;
@@ -169,16 +181,13 @@ __global__ void __launch_bounds__(kThreadsS, NT == 1 ? 2 : 1)
 #pragma unroll
         for (int step = 0; step < 2; ++step)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) xc[step][nt] = xf[step][nt];
-        if (i + 1 < n) load_x(b0 + i + 1);
+            for (int nt = 0; nt < NT; ++nt) {
+                xc[step][nt] = xn1[step][nt];
+                xn1[step][nt] = xn2[step][nt];
+            }
+        if (i + 2 < n) load_x(xn2, b0 + i + 2);
 
-        float d[NT][8][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int p = 0; p < 8; ++p)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) d[nt][p][e] = 0.0f;
+        float d[NT][8][4];  // the block's sums, started by the first step's MMAs
 #pragma unroll
         for (int step = 0; step < 2; ++step) {
             uint4 w[4];
@@ -191,18 +200,26 @@ __global__ void __launch_bounds__(kThreadsS, NT == 1 ? 2 : 1)
                 const uint32_t u2 = word_of(w[2], wi) ^ 0x80808080u;
                 const uint32_t u3 = word_of(w[3], wi) ^ 0x80808080u;
                 uint32_t lo[4], hi[4];  // per column: rows (4t, 4t+1) and (4t+2, 4t+3) as bf16 pairs
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    lo[e] = q8x2_to_bf16x2(u0, u1, e);
-                    hi[e] = q8x2_to_bf16x2(u2, u3, e);
-                }
+                lo[0] = q8x2_to_bf16x2<0>(u0, u1, kMagicPair);
+                lo[1] = q8x2_to_bf16x2<1>(u0, u1, kMagicPair);
+                lo[2] = q8x2_to_bf16x2<2>(u0, u1, kMagicPair);
+                lo[3] = q8x2_to_bf16x2<3>(u0, u1, kMagicPair);
+                hi[0] = q8x2_to_bf16x2<0>(u2, u3, kMagicPair);
+                hi[1] = q8x2_to_bf16x2<1>(u2, u3, kMagicPair);
+                hi[2] = q8x2_to_bf16x2<2>(u2, u3, kMagicPair);
+                hi[3] = q8x2_to_bf16x2<3>(u2, u3, kMagicPair);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int p = 2 * wi + h;
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma_16816(d[nt][p], lo[2 * h], lo[2 * h + 1], hi[2 * h], hi[2 * h + 1], xc[step][nt].x,
-                                  xc[step][nt].y);
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (step == 0)
+                            mma_16816_first(d[nt][p], lo[2 * h], lo[2 * h + 1], hi[2 * h], hi[2 * h + 1],
+                                            xc[step][nt].x, xc[step][nt].y);
+                        else
+                            mma_16816(d[nt][p], lo[2 * h], lo[2 * h + 1], hi[2 * h], hi[2 * h + 1], xc[step][nt].x,
+                                      xc[step][nt].y);
+                    }
                 }
             }
         }
@@ -294,14 +311,15 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     }
 
     // x[r][32b + 16s + 4u .. + 3]: the activations of this lane's rows, two 8-byte loads per row and block.
-    uint2 xf[M][2];
-    auto load_x = [&](int b) {
+    uint2 xn1[M][2], xn2[M][2];  // blocks i + 1 and i + 2
+    auto load_x = [&](uint2 (&dst)[M][2], int b) {
 #pragma unroll
         for (int r = 0; r < M; ++r)
 #pragma unroll
-            for (int s = 0; s < 2; ++s) xf[r][s] = ld_cg_u2(a.x + (size_t)r * a.K + (size_t)b * kBlock + 16 * s + 4 * u);
+            for (int s = 0; s < 2; ++s) dst[r][s] = ld_cg_u2(a.x + (size_t)r * a.K + (size_t)b * kBlock + 16 * s + 4 * u);
     };
-    if (n > 0) load_x(b0);
+    if (n > 0) load_x(xn1, b0);
+    if (n > 1) load_x(xn2, b0 + 1);
 
     for (int i = 0; i < n; ++i) {
         const int ahead = i + kDepth - 1;
@@ -314,8 +332,11 @@ __global__ void __launch_bounds__(kThreadsS, 2)
 #pragma unroll
         for (int r = 0; r < M; ++r)
 #pragma unroll
-            for (int s = 0; s < 2; ++s) xc[r][s] = xf[r][s];
-        if (i + 1 < n) load_x(b0 + i + 1);
+            for (int s = 0; s < 2; ++s) {
+                xc[r][s] = xn1[r][s];
+                xn1[r][s] = xn2[r][s];
+            }
+        if (i + 2 < n) load_x(xn2, b0 + i + 2);
 
         unsigned long long part[M][8];
 #pragma unroll
@@ -337,8 +358,8 @@ __global__ void __launch_bounds__(kThreadsS, 2)
 #pragma unroll
                 for (int wi = 0; wi < 4; ++wi) {
                     const uint32_t uw = word_of(w, wi) ^ 0x80808080u;
-                    const unsigned long long q01 = q8x2_to_f32x2<0>(uw);
-                    const unsigned long long q23 = q8x2_to_f32x2<2>(uw);
+                    const unsigned long long q01 = q8x2_to_f32x2<0>(uw, kMagicPair);
+                    const unsigned long long q23 = q8x2_to_f32x2<2>(uw, kMagicPair);
 #pragma unroll
                     for (int r = 0; r < M; ++r) {
                         part[r][2 * wi] = fma_f32x2(q01, xx[r], part[r][2 * wi]);
@@ -382,6 +403,188 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     finish_n<kWarpsS, M, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
 }
 
+
+// m = 9..16: two tiles of 8 activation rows.  The accumulators of 16 rows x 128 columns would not fit one warp's
+// registers at two CTAs per SM, so a block's columns are split between a warp pair: warp 2k + h streams and converts
+// columns 64h .. 64h + 63 of every unit of its K range (each value is still converted once).  Each warp keeps its
+// own ring of five half-units (2 KB of values and 256 B of scales each); lane (g, t) of warp h holds 8 columns
+// 64h + 8g .. 64h + 8g + 7, the second half of chunk 4h + g/2 of its row group t.
+constexpr int kHalfUnit = kUnit / 2;
+constexpr int kHalfStage = kHalfUnit + kUnitScales * 2;
+constexpr int kPairDepth = 5;
+constexpr int kPairSmem = kWarpsS * kPairDepth * kHalfStage;
+
+__device__ __forceinline__ void issue_half_unit(unsigned char *stage, const int8_t *q, const float *s, size_t u,
+                                                int h, int lane) {
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(q) + u * kUnit + 256 * h + (lane & 15) * 16;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int seg = 2 * c + (lane >> 4);
+        cp_async16(stage + seg * 256 + (lane & 15) * 16, src + seg * 512);
+    }
+    if (lane < 16)
+        cp_async16(stage + kHalfUnit + lane * 16,
+                   reinterpret_cast<const unsigned char *>(s + u * kUnitScales + 64 * h) + lane * 16);
+}
+
+template <bool ARGMAX>
+__global__ void __launch_bounds__(kThreadsS, 2)
+    stream_pair_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
+    constexpr int NT = 2, MR = 16, NP = 4, kDepth = kPairDepth, kRanges = kWarpsS / 2;
+    extern __shared__ __align__(16) unsigned char smem_s[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int h = warp & 1, kr = warp >> 1;
+    const int tile = select_part(parts, blockIdx.x, a);
+    const int rank = blockIdx.y;
+    const int c0 = (int)((long long)a.nb * rank / a.ksplit);
+    const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
+    const int b0 = c0 + (c1 - c0) * kr / kRanges;
+    const int b1 = c0 + (c1 - c0) * (kr + 1) / kRanges;
+    const int n = b1 - b0;
+    unsigned char *ring = smem_s + warp * kDepth * kHalfStage;
+    const size_t unit0 = (size_t)tile * a.nb + b0;
+
+    float acc[NT][NP][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int p = 0; p < NP; ++p)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][p][i] = 0.0f;
+
+    if (prefetch_weights) {
+#pragma unroll
+        for (int i = 0; i < kDepth - 1; ++i) {
+            if (i < n) issue_half_unit(ring + i * kHalfStage, a.q, a.s, unit0 + i, h, lane);
+            cp_async_commit();
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!prefetch_weights) {
+#pragma unroll
+        for (int i = 0; i < kDepth - 1; ++i) {
+            if (i < n) issue_half_unit(ring + i * kHalfStage, a.q, a.s, unit0 + i, h, lane);
+            cp_async_commit();
+        }
+    }
+
+    const uint16_t *xrow[NT];
+    bool xlive[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int r = 8 * nt + g;
+        xlive[nt] = r < a.m;
+        xrow[nt] = a.x + (size_t)(xlive[nt] ? r : 0) * a.K + 4 * t;
+    }
+    uint2 xn1[2][NT], xn2[2][NT];
+    auto load_x = [&](uint2 (&dst)[2][NT], int b) {
+#pragma unroll
+        for (int step = 0; step < 2; ++step)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                dst[step][nt] = xlive[nt] ? ld_cg_u2(xrow[nt] + (size_t)b * kBlock + 16 * step) : make_uint2(0u, 0u);
+    };
+    if (n > 0) load_x(xn1, b0);
+    if (n > 1) load_x(xn2, b0 + 1);
+    const int woff = (4 * (g >> 1) + t) * 16 + 8 * (g & 1);  // this lane's 8 bytes within a 256-byte half-segment
+
+    for (int i = 0; i < n; ++i) {
+        const int ahead = i + kDepth - 1;
+        if (ahead < n) issue_half_unit(ring + (ahead % kDepth) * kHalfStage, a.q, a.s, unit0 + ahead, h, lane);
+        cp_async_commit();
+        cp_async_wait<kDepth - 1>();
+        __syncwarp();
+        const unsigned char *st = ring + (i % kDepth) * kHalfStage;
+        uint2 xc[2][NT];
+#pragma unroll
+        for (int step = 0; step < 2; ++step)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                xc[step][nt] = xn1[step][nt];
+                xn1[step][nt] = xn2[step][nt];
+            }
+        if (i + 2 < n) load_x(xn2, b0 + i + 2);
+
+        float d[NT][NP][4];  // the block's sums, started by the first step's MMAs
+#pragma unroll
+        for (int step = 0; step < 2; ++step) {
+            uint2 w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint2 *>(st + (step * 4 + j) * 256 + woff);
+#pragma unroll
+            for (int wi = 0; wi < 2; ++wi) {
+                const uint32_t u0 = word_of(w[0], wi) ^ 0x80808080u;
+                const uint32_t u1 = word_of(w[1], wi) ^ 0x80808080u;
+                const uint32_t u2 = word_of(w[2], wi) ^ 0x80808080u;
+                const uint32_t u3 = word_of(w[3], wi) ^ 0x80808080u;
+                uint32_t lo[4], hi[4];
+                lo[0] = q8x2_to_bf16x2<0>(u0, u1, kMagicPair);
+                lo[1] = q8x2_to_bf16x2<1>(u0, u1, kMagicPair);
+                lo[2] = q8x2_to_bf16x2<2>(u0, u1, kMagicPair);
+                lo[3] = q8x2_to_bf16x2<3>(u0, u1, kMagicPair);
+                hi[0] = q8x2_to_bf16x2<0>(u2, u3, kMagicPair);
+                hi[1] = q8x2_to_bf16x2<1>(u2, u3, kMagicPair);
+                hi[2] = q8x2_to_bf16x2<2>(u2, u3, kMagicPair);
+                hi[3] = q8x2_to_bf16x2<3>(u2, u3, kMagicPair);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int p = 2 * wi + hh;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (step == 0)
+                            mma_16816_first(d[nt][p], lo[2 * hh], lo[2 * hh + 1], hi[2 * hh], hi[2 * hh + 1],
+                                            xc[step][nt].x, xc[step][nt].y);
+                        else
+                            mma_16816(d[nt][p], lo[2 * hh], lo[2 * hh + 1], hi[2 * hh], hi[2 * hh + 1],
+                                      xc[step][nt].x, xc[step][nt].y);
+                    }
+                }
+            }
+        }
+        const float *ss = reinterpret_cast<const float *>(st + kHalfUnit) + 8 * g;
+        float sc[8];
+#pragma unroll
+        for (int v4 = 0; v4 < 2; ++v4) {
+            const float4 f = *reinterpret_cast<const float4 *>(ss + 4 * v4);
+            sc[4 * v4 + 0] = f.x;
+            sc[4 * v4 + 1] = f.y;
+            sc[4 * v4 + 2] = f.z;
+            sc[4 * v4 + 3] = f.w;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                acc[nt][p][0] = fmaf(sc[2 * p], d[nt][p][0], acc[nt][p][0]);
+                acc[nt][p][1] = fmaf(sc[2 * p], d[nt][p][1], acc[nt][p][1]);
+                acc[nt][p][2] = fmaf(sc[2 * p + 1], d[nt][p][2], acc[nt][p][2]);
+                acc[nt][p][3] = fmaf(sc[2 * p + 1], d[nt][p][3], acc[nt][p][3]);
+            }
+    }
+    cp_async_wait<0>();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __syncthreads();
+
+    float *red = reinterpret_cast<float *>(smem_s);  // [kRanges][MR][128]
+    float *mine = red + kr * MR * kTmaColumns;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int r = 8 * nt + 2 * t;
+            const int c = 64 * h + 8 * g + 2 * p;
+            *reinterpret_cast<float2 *>(mine + r * kTmaColumns + c) = make_float2(acc[nt][p][0], acc[nt][p][2]);
+            *reinterpret_cast<float2 *>(mine + (r + 1) * kTmaColumns + c) = make_float2(acc[nt][p][1], acc[nt][p][3]);
+        }
+    __syncthreads();
+    finish_n<kRanges, MR, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
+}
+
+static_assert(finish_smem_n(kWarpsS / 2, 16, kTmaColumns) <= kPairSmem, "the epilogue fits in the rings");
+static_assert(2 * kPairSmem <= 227 * 1024, "two CTAs per SM");
+
 static_assert(finish_smem_n(kWarpsS, 8, kTmaColumns) <= StreamShape<1>::kSmem, "the epilogue fits in the rings");
 static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns) <= StreamShape<2>::kSmem, "the epilogue fits in the rings");
 static_assert(2 * StreamShape<1>::kSmem <= 227 * 1024 && StreamShape<2>::kSmem <= 227 * 1024, "residency");
@@ -419,11 +622,11 @@ cudaError_t launch_stream_kernel(Kernel kernel, int kSmemS, const Args &a, const
 
 }  // namespace
 
-int stream_ctas_per_sm(int m) { return m <= 8 ? 2 : 1; }
+int stream_ctas_per_sm(int) { return 2; }
 
 cudaError_t launch_stream(const Args &a, const Parts &pt, bool argmax, cudaStream_t stream, bool pdl,
                           bool prefetch_weights) {
-    constexpr int s1 = StreamShape<1>::kSmem, s2 = StreamShape<2>::kSmem;
+    constexpr int s1 = StreamShape<1>::kSmem;
     const bool p = prefetch_weights;
     switch (a.m) {
         case 1:
@@ -438,8 +641,8 @@ cudaError_t launch_stream(const Args &a, const Parts &pt, bool argmax, cudaStrea
     if (a.m <= 8)
         return argmax ? launch_stream_kernel(stream_kernel<1, true>, s1, a, pt, stream, pdl, p)
                       : launch_stream_kernel(stream_kernel<1, false>, s1, a, pt, stream, pdl, p);
-    return argmax ? launch_stream_kernel(stream_kernel<2, true>, s2, a, pt, stream, pdl, p)
-                  : launch_stream_kernel(stream_kernel<2, false>, s2, a, pt, stream, pdl, p);
+    return argmax ? launch_stream_kernel(stream_pair_kernel<true>, kPairSmem, a, pt, stream, pdl, p)
+                  : launch_stream_kernel(stream_pair_kernel<false>, kPairSmem, a, pt, stream, pdl, p);
 }
 
 }  // namespace q8

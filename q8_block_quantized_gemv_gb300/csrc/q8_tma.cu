@@ -256,11 +256,15 @@ __global__ void __maxnreg__(128)
                     const uint32_t u2 = word_of(w[2], wi) ^ 0x80808080u;
                     const uint32_t u3 = word_of(w[3], wi) ^ 0x80808080u;
                     uint32_t lo[4], hi[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        lo[e] = q8x2_to_bf16x2(u0, u1, e);  // rows 2t, 2t+8
-                        hi[e] = q8x2_to_bf16x2(u2, u3, e);  // rows 2t+1, 2t+9
-                    }
+                    // rows 2t, 2t+8 (lo) and 2t+1, 2t+9 (hi) of each of the word's four columns
+                    lo[0] = q8x2_to_bf16x2<0>(u0, u1, kMagicPair);
+                    lo[1] = q8x2_to_bf16x2<1>(u0, u1, kMagicPair);
+                    lo[2] = q8x2_to_bf16x2<2>(u0, u1, kMagicPair);
+                    lo[3] = q8x2_to_bf16x2<3>(u0, u1, kMagicPair);
+                    hi[0] = q8x2_to_bf16x2<0>(u2, u3, kMagicPair);
+                    hi[1] = q8x2_to_bf16x2<1>(u2, u3, kMagicPair);
+                    hi[2] = q8x2_to_bf16x2<2>(u2, u3, kMagicPair);
+                    hi[3] = q8x2_to_bf16x2<3>(u2, u3, kMagicPair);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int p = 2 * wi + h;
