@@ -110,11 +110,12 @@ q8_status q8_gemv_argmax_ex(const void *x, const int8_t *q, const float *s, int6
  * 32-row x 128-column block becomes one contiguous 4 KB unit laid out in the order the kernel's lanes load it, so a
  * warp streaming one column tile along K reads contiguous memory.  With Nt = q8_tiled_n(N), T = Nt / 128 tiles and
  * nb = K / 32 blocks:
- *   values  int8 [T][nb][4096]: in unit (t, b), segment 4s + j (s = 0, 1; j = 0..3, 512 bytes each) holds at byte
- *           16 * (4g + u) (g = 0..7, u = 0..3) the 16 values of weight row 32b + 16s + 4u + j, columns
- *           128t + 16g .. 128t + 16g + 15, in column order
+ *   values  uint8 [T][nb][4096]: in unit (t, b), segment 4s + h (s = 0, 1; h = 0..3; 512 bytes each) holds at byte
+ *           16 * (4g + u) (g = 0..7, u = 0..3) four words; word w holds weight rows 32b + 16s + 4u + k (byte k,
+ *           k = 0..3) of column 128t + 8(4h + w) + g, each value stored as q + 128 (offset binary)
  *   scales  fp32 [T][nb][128]: element c of unit (t, b) is s[b][128t + c]
- * Columns >= N are zero.  Sizes: K * Nt bytes of values, (K / 32) * Nt * 4 bytes of scales. */
+ * Columns >= N hold q = 0 (byte 128) and scale 0.  Sizes: K * Nt bytes of values, (K / 32) * Nt * 4 bytes of
+ * scales. */
 int q8_tiled_n(int N); /* N rounded up to a multiple of 128; -1 when N <= 0 or on overflow */
 
 /* Host: row-major q [K][Np], s [K/32][Np] (as q8_gemv takes them) -> tiled qt, st (host buffers, written). */

@@ -1,21 +1,36 @@
-// Q8_0 GEMV over the tiled weight storage: every warp streams its own contiguous run of weight units.
+// Q8_0 GEMV over the tiled weight storage: every warp streams its own contiguous run of weight units and contracts
+// them on the tensor cores with fp16 operands.
 //
-// The tiled storage (q8_tile) keeps every 32-row x 128-column block of the weight as one contiguous 4 KB unit, in
-// MMA-fragment order: the unit is eight 512-byte segments (16-row step s = 0, 1; row group j = 0..3), and in segment
-// (s, j) lane L = 4g + t of a warp finds its 16 bytes at L * 16: weight row 16s + 4t + j, columns 16g .. 16g + 15 of
-// the tile.  The scales of the unit follow in their own storage, 128 fp32 in column order.  So one warp instruction
-// copies 512 contiguous bytes, and the units of a column tile follow each other along K: a warp that owns a run of K
-// blocks of one tile reads one contiguous range of memory.
+// The tiled storage (q8_tile) keeps every 32-row x 128-column block of the weight as one contiguous 4 KB unit in
+// MMA-fragment order: eight 512-byte segments (16-row half s = 0, 1; group h = 0..3 of four 8-column slices); in
+// segment (s, h) lane L = 4g + t finds at L * 16 four words, word w holding weight rows 16s + 4t + 0..3 of column
+// 8(4h + w) + g, offset by +128.  The unit's 128 scales follow in their own storage, in column order.  One warp
+// instruction copies 512 contiguous bytes, and the units of a column tile follow each other along K, so a warp that
+// owns a run of K blocks of one tile reads one contiguous range of memory.
 //
 // A CTA owns one 128-column tile and a range of its K blocks (split across a thread-block cluster when N is too
-// narrow to fill the SMs); its eight warps split that range into contiguous runs.  Each warp keeps a private ring of
-// three stages in shared memory, filled with cp.async (16 bytes a lane, bypassing L1): it issues block i + 2 while
-// it computes block i, so about two units per warp -- 150 KB per SM -- are in flight without holding registers.  Per
-// block a lane converts its 4 x 16 int8 values exactly to bf16 pairs, runs the 8 (or 16) bf16 m16n8k16 MMAs of the
-// block into a fresh fp32 accumulator, and folds the block sums into its fp32 carry with the block's scales
-// ("from_q8.rs", module doc: the lanes contracted over the int8 rows, then folded down each column with their scales,
-// into an fp32 carry).  The MMA's K order is the relabeling of the register-fed kernel: MMA reduction index 2t, 2t+1,
-// 2t+8, 2t+9 is weight row 4t, 4t+1, 4t+2, 4t+3, so a lane's activation fragment is 4 consecutive activations.
+// narrow to fill the SMs); its eight warps split that range again into contiguous runs.  Each warp keeps a private
+// ring of three stages in shared memory, filled with cp.async (16 bytes a lane, bypassing L1): it issues block i + 2
+// while it computes block i, so about two units per warp -- 150 KB per SM -- are in flight without holding registers.
+//
+// The block's contraction runs on m16n8k16 MMAs with the activations as the A operand (rows r and r + 8 of the lane's
+// fragment are activation rows g and g + 8) and the weights as B (one 8-column slice per MMA, fp32 accumulators):
+//   - weights: the byte permute of a stored word into the low mantissa bytes of the fp16 1024 gives 1024 + q + 128
+//     exactly, and one packed fp16 subtract of 1152 leaves q -- one permute and one subtract per pair of weights;
+//   - activations: bf16 has a wider exponent than fp16, so each activation row of the block (m <= 8; for m > 8 the
+//     whole block) is scaled by one power of two 2^p that puts its largest magnitude in [2^15, 2^16).  If every
+//     nonzero activation then lies in fp16's normal range, the conversion is exact (bf16's 8 significant bits fit
+//     fp16's 11) and the products q * x * 2^p are exact in fp32; the block's scale is multiplied by 2^-p (exact)
+//     before the fold.  A block with a row whose nonzero activations span more than 30 binades, or that holds inf or
+//     NaN, is contracted instead with bf16 operands from the raw activations, exactly as well;
+//   - MMA reduction index 2t, 2t+1, 2t+8, 2t+9 is weight row 4t .. 4t+3 of the 16-row half, so a lane's activation
+//     fragment is 4 consecutive activations and its weight fragment the 4 bytes of one stored word;
+//   - the block's sums (fresh accumulators) are folded into the fp32 carry with the block's scales, a packed
+//     fp32x2 FMA over the pair of columns a lane holds ("from_q8.rs", module doc: the lanes contracted over the int8
+//     rows, then folded down each column with their scales, into an fp32 carry).
+//
+// For m <= 2 the CUDA cores do the contraction instead (stream_simt_kernel): there the per-row FMAs cost less than
+// the MMA operands' conversion and the per-block exponent choice.
 //
 // Activations are read from L2 (ld.global.cg), two blocks ahead.  With programmatic dependent launch every thread
 // waits for the previous kernel (griddepcontrol.wait) before it reads x or writes y; with Q8_FLAG_CONSTANT_WEIGHTS
@@ -31,11 +46,9 @@ constexpr int kThreadsS = 32 * kWarpsS;
 constexpr int kUnit = kBlock * kTmaColumns;  // 4096 bytes of values per 32 x 128 unit
 constexpr int kUnitScales = kTmaColumns;     // 128 fp32
 constexpr int kStageS = kUnit + kUnitScales * 4;
-// Ring stages per warp: three with two CTAs per SM (m <= 8), five with one (m > 8, twice the accumulators).
-template <int NT> struct StreamShape {
-    static constexpr int kDepth = NT == 1 ? 3 : 5;
-    static constexpr int kSmem = kWarpsS * kDepth * kStageS;
-};
+constexpr int kDepthS = 3;                   // ring stages per warp (two CTAs per SM)
+constexpr int kSmemS = kWarpsS * kDepthS * kStageS;
+constexpr int kSlices = kTmaColumns / 8;     // 8-column MMA slices of a tile
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -47,32 +60,13 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// The same MMA into a fresh accumulator (C = 0): the first 16 rows of a block start the block's sums.
-__device__ __forceinline__ void mma_16816_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                                uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%10, %10, %10, %10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
-}
-
 __device__ __forceinline__ uint2 ld_cg_u2(const void *p) {
     uint2 v;
     asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
 
-// Packed fp32 pairs (one 64-bit register pair) for the CUDA-core inner loop.
+// fp32 pairs in one 64-bit register pair.
 __device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
     unsigned long long d;
     asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
@@ -87,15 +81,95 @@ __device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, un
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
-// Bytes e and e + 1 of a sign-flipped int8 word (see q8_to_f32) as the exact fp32 pair {q_e, q_e+1}: two byte
-// permutes into the mantissa of 2^23 and one packed subtract of 2^23 + 128.
-template <int E> __device__ __forceinline__ unsigned long long q8x2_to_f32x2(uint32_t u, unsigned long long magic) {
+__device__ __forceinline__ unsigned long long mul_f32x2(unsigned long long a, unsigned long long b) {
     unsigned long long d;
-    asm("{\n .reg .b32 a, b;\n .reg .b64 p;\n prmt.b32 a, %1, 0x4B000000, %2;\n prmt.b32 b, %1, 0x4B000000, %3;\n"
-        " mov.b64 p, {a, b};\n sub.rn.f32x2 %0, p, %4;\n}"
-        : "=l"(d)
-        : "r"(u), "n"(0x7540 + E), "n"(0x7540 + E + 1), "l"(magic));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+
+// Stored bytes E, E + 1 of a word (q + 128 each) as the exact fp16 pair {q_E, q_E+1}: the permute writes each byte
+// under the fp16 exponent of 1024 (bits 0x64), whose mantissa unit is 1, giving 1024 + q + 128; the packed subtract
+// of 1152 is exact.
+template <int E> __device__ __forceinline__ uint32_t q8x2_to_f16x2(uint32_t u) {
+    uint32_t d;
+    asm("{\n .reg .b32 p;\n prmt.b32 p, %1, 0x64646464, %2;\n sub.rn.f16x2 %0, p, %3;\n}"
+        : "=r"(d)
+        : "r"(u), "n"(E == 0 ? 0x4140 : 0x4342), "r"(0x64806480u));
+    return d;
+}
+
+// The same bytes as an exact bf16 pair (for the bf16 contraction of a block whose activations do not fit fp16):
+// each byte in the low mantissa of 2^23 gives 2^23 + q + 128, one packed subtract leaves q, packed to bf16 (exact:
+// |q| <= 128 needs 8 significant bits).
+template <int E> __device__ __forceinline__ uint32_t q8x2_to_bf16x2(uint32_t u) {
+    uint32_t d;
+    asm("{\n .reg .b32 a, b;\n .reg .b64 p, r;\n .reg .f32 lo, hi;\n prmt.b32 a, %1, 0x4B000000, %2;\n"
+        " prmt.b32 b, %1, 0x4B000000, %3;\n mov.b64 p, {a, b};\n sub.rn.f32x2 r, p, %4;\n mov.b64 {lo, hi}, r;\n"
+        " cvt.rn.bf16x2.f32 %0, hi, lo;\n}"
+        : "=r"(d)
+        : "r"(u), "n"(0x7540 + E), "n"(0x7540 + E + 1), "l"(kMagicPair));
+    return d;
+}
+
+// A bf16 pair scaled by the power of two `scale` (both halves of the fp32 pair) as an fp16 pair; exact when the
+// caller has checked that every nonzero scaled value is an fp16 normal.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, unsigned long long scale) {
+    uint32_t d;
+    asm("{\n .reg .b32 lo, hi;\n .reg .b64 p, r;\n .reg .f32 a, b;\n shl.b32 lo, %1, 16;\n"
+        " and.b32 hi, %1, 0xFFFF0000;\n mov.b64 p, {lo, hi};\n mul.rn.f32x2 r, p, %2;\n mov.b64 {a, b}, r;\n"
+        " cvt.rn.f16x2.f32 %0, b, a;\n}"
+        : "=r"(d)
+        : "r"(x), "l"(scale));
+    return d;
+}
+
+// Per-half unsigned 16-bit max / min / decrement.
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t vmin_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t vdec_u16x2(uint32_t a) {  // a - 1 in each half, 0 wrapping to 0xFFFF
+    uint32_t d;
+    asm("add.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(0xFFFFFFFFu));
+    return d;
+}
+
+// D = A * B (+ D) on fp16 or bf16 operands, fp32 accumulators; FIRST starts D from zero.
+template <bool F16, bool FIRST>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if (F16) {
+        if (FIRST)
+            asm(
+                "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                "{%10, %10, %10, %10};"
+                : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+        else
+            asm(
+                "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                "{%0, %1, %2, %3};"
+                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        if (FIRST)
+            asm(
+                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                "{%10, %10, %10, %10};"
+                : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+        else
+            asm(
+                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                "{%0, %1, %2, %3};"
+                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
 }
 
 // Copy unit `u` (values and scales) into `stage`: 8 + 1 cp.async of 16 bytes per lane.
@@ -106,11 +180,114 @@ __device__ __forceinline__ void issue_unit(unsigned char *stage, const int8_t *q
     cp_async16(stage + kUnit + lane * 16, reinterpret_cast<const unsigned char *>(s + u * kUnitScales) + lane * 16);
 }
 
-template <int NT, bool ARGMAX>
-__global__ void __launch_bounds__(kThreadsS, NT == 1 ? 2 : 1)
+// How a block's activations enter the MMA: scaled fp16 or raw bf16.  scale[i] = 2^p and sf[i] = 2^-p (in both halves
+// of an fp32 pair) for the lane's activation row g + 8i.
+struct XPlan {
+    unsigned long long scale[2], sf[2];
+    bool f16;
+};
+
+// The range of the lane's activation words of one row: its largest |x| in the low half and 0xFFFF minus (its smallest
+// nonzero |x| - 1) in the high half, as bf16 bit patterns, so that one per-half max combines two ranges.
+__device__ __forceinline__ uint32_t row_range(const uint2 (&x)[2]) {
+    uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const uint32_t v0 = x[s].x & 0x7FFF7FFFu, v1 = x[s].y & 0x7FFF7FFFu;
+        mx = vmax_u16x2(mx, vmax_u16x2(v0, v1));
+        mn = vmin_u16x2(mn, vmin_u16x2(vdec_u16x2(v0), vdec_u16x2(v1)));
+    }
+    mx = vmax_u16x2(mx, __byte_perm(mx, 0, 0x1032));
+    mn = vmin_u16x2(mn, __byte_perm(mn, 0, 0x1032));
+    return (mx & 0xFFFFu) | (~mn << 16);
+}
+
+// From a reduced range: whether one power of two maps every nonzero value into fp16's normal range -- all values
+// finite, the largest binade at least 2^-111 (so 2^p = 2^(142 - emax) is a normal fp32) and every nonzero value
+// within 29 binades below it -- or every value is zero; and the factors 2^p, 2^-p.
+__device__ __forceinline__ bool range_plan(uint32_t range, unsigned long long &scale, unsigned long long &sf) {
+    const uint32_t xmax = range & 0xFFFFu;
+    const uint32_t xmin = ((~range >> 16) & 0xFFFFu) + 1u;  // 0x10000 when every value is zero
+    const int emax = (int)(xmax >> 7), emin = (int)(xmin >> 7);
+    const bool zero = xmax == 0u;
+    const uint32_t up = zero ? 0x3F800000u : (uint32_t)(269 - emax) << 23;
+    const uint32_t down = zero ? 0x3F800000u : (uint32_t)(emax - 15) << 23;
+    scale = ((unsigned long long)up << 32) | up;
+    sf = ((unsigned long long)down << 32) | down;
+    return zero || (xmax < 0x7F80u && emax >= 16 && emin >= 1 && emin >= emax - 29);
+}
+
+// The plan of one block from the lane's activation words x[row][half] (rows g and g + 8 when NR = 2).  PER_ROW: one
+// power of two per activation row (the range over the four lanes of the row), fp16 only if every row fits; else one
+// power of two for the whole block (the range over the warp).  Warp-uniform f16.
+template <int NR, bool PER_ROW> __device__ __forceinline__ XPlan plan_block(const uint2 (&x)[NR][2]) {
+    XPlan pl;
+    if (PER_ROW) {
+        uint32_t rg[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) rg[r] = row_range(x[r]);
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1)
+#pragma unroll
+            for (int r = 0; r < NR; ++r) rg[r] = vmax_u16x2(rg[r], __shfl_xor_sync(0xffffffffu, rg[r], o));
+        bool ok = true;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) ok = range_plan(rg[r < NR ? r : 0], pl.scale[r], pl.sf[r]) && ok;
+        pl.f16 = __all_sync(0xffffffffu, ok);
+    } else {
+        uint32_t rg = row_range(x[0]);
+#pragma unroll
+        for (int r = 1; r < NR; ++r) rg = vmax_u16x2(rg, row_range(x[r]));
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) rg = vmax_u16x2(rg, __shfl_xor_sync(0xffffffffu, rg, o));
+        pl.f16 = range_plan(rg, pl.scale[0], pl.sf[0]);
+        pl.scale[1] = pl.scale[0];
+        pl.sf[1] = pl.sf[0];
+    }
+    return pl;
+}
+
+// One block of the warp's run: the 16 slices' MMAs over both 16-row halves and the fold into the carry.  `a` holds
+// the A fragments of the two halves (fp16 scaled, or raw bf16), `pl` the factors of the block's scales (2^-p per
+// activation row, unused for bf16), ROWS16 whether activation rows 8..15 exist and SAME whether both rows share 2^-p.
+template <bool F16, bool ROWS16, bool SAME>
+__device__ __forceinline__ void block_contract(const unsigned char *st, int lane, const uint32_t (&a)[2][4],
+                                               const XPlan &pl,
+                                               unsigned long long (&acc)[ROWS16 ? 2 : 1][kSlices]) {
+    const int t = lane & 3;
+    const unsigned long long *sp = reinterpret_cast<const unsigned long long *>(st + kUnit) + t;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const uint4 w0 = *reinterpret_cast<const uint4 *>(st + h * 512 + lane * 16);
+        const uint4 w1 = *reinterpret_cast<const uint4 *>(st + (4 + h) * 512 + lane * 16);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const int j = 4 * h + w;
+            const uint32_t u0 = word_of(w0, w), u1 = word_of(w1, w);
+            float d[4];
+            if (F16) {
+                mma_16816<true, true>(d, a[0], q8x2_to_f16x2<0>(u0), q8x2_to_f16x2<2>(u0));
+                mma_16816<true, false>(d, a[1], q8x2_to_f16x2<0>(u1), q8x2_to_f16x2<2>(u1));
+            } else {
+                mma_16816<false, true>(d, a[0], q8x2_to_bf16x2<0>(u0), q8x2_to_bf16x2<2>(u0));
+                mma_16816<false, false>(d, a[1], q8x2_to_bf16x2<0>(u1), q8x2_to_bf16x2<2>(u1));
+            }
+            // the scales of columns 8j + 2t, 8j + 2t + 1 (the D fragment's columns), times the row's factor
+            const unsigned long long sc = F16 ? mul_f32x2(sp[4 * j], pl.sf[0]) : sp[4 * j];
+            acc[0][j] = fma_f32x2(sc, pack_f32x2(d[0], d[1]), acc[0][j]);
+            if (ROWS16) {
+                const unsigned long long sc1 = (!F16 || SAME) ? sc : mul_f32x2(sp[4 * j], pl.sf[1]);
+                acc[ROWS16 ? 1 : 0][j] = fma_f32x2(sc1, pack_f32x2(d[2], d[3]), acc[ROWS16 ? 1 : 0][j]);
+            }
+        }
+    }
+}
+
+template <bool ROWS16, bool ARGMAX>
+__global__ void __launch_bounds__(kThreadsS, 2)
     stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
-    constexpr int MR = 8 * NT;
-    constexpr int kDepth = StreamShape<NT>::kDepth;
+    constexpr int MR = ROWS16 ? 16 : 8;
+    constexpr int NR = ROWS16 ? 2 : 1;  // activation rows per lane: g and g + 8
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -121,21 +298,20 @@ __global__ void __launch_bounds__(kThreadsS, NT == 1 ? 2 : 1)
     const int b0 = c0 + (c1 - c0) * warp / kWarpsS;
     const int b1 = c0 + (c1 - c0) * (warp + 1) / kWarpsS;
     const int n = b1 - b0;
-    unsigned char *ring = smem_s + warp * kDepth * kStageS;
+    unsigned char *ring = smem_s + warp * kDepthS * kStageS;
     const size_t unit0 = (size_t)tile * a.nb + b0;
 
-    float acc[NT][8][4];
+    // acc[i][j]: rows g + 8i, columns 8j + 2t and 8j + 2t + 1 of the tile
+    unsigned long long acc[NR][kSlices];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int i = 0; i < NR; ++i)
 #pragma unroll
-        for (int p = 0; p < 8; ++p)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[nt][p][i] = 0.0f;
+        for (int j = 0; j < kSlices; ++j) acc[i][j] = 0ull;
 
-    // Prologue: the first kDepth - 1 units (one commit group each, empty past the run).
+    // Prologue: the first kDepthS - 1 units (one commit group each, empty past the run).
     if (prefetch_weights) {
 #pragma unroll
-        for (int i = 0; i < kDepth - 1; ++i) {
+        for (int i = 0; i < kDepthS - 1; ++i) {
             if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
             cp_async_commit();
         }
@@ -143,141 +319,112 @@ __global__ void __launch_bounds__(kThreadsS, NT == 1 ? 2 : 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!prefetch_weights) {
 #pragma unroll
-        for (int i = 0; i < kDepth - 1; ++i) {
+        for (int i = 0; i < kDepthS - 1; ++i) {
             if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
             cp_async_commit();
         }
     }
 
-    // Activation rows this lane feeds to the MMA (rows at or past m are zeros).
-    const uint16_t *xrow[NT];
-    bool xlive[NT];
+    // The lane's activations x[g + 8i][32b + 16s + 4t .. + 3] (rows at or past m are zeros).
+    const uint16_t *xrow[NR];
+    bool xlive[NR];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int r = 8 * nt + g;
-        xlive[nt] = r < a.m;
-        xrow[nt] = a.x + (size_t)(xlive[nt] ? r : 0) * a.K + 4 * t;
+    for (int i = 0; i < NR; ++i) {
+        const int r = g + 8 * i;
+        xlive[i] = r < a.m;
+        xrow[i] = a.x + (size_t)(xlive[i] ? r : 0) * a.K + 4 * t;
     }
-    // Activation fragments two blocks ahead (L2 latency exceeds a block's work): xn1 for block i + 1, xn2 for i + 2.
-    uint2 xn1[2][NT], xn2[2][NT];
-    auto load_x = [&](uint2 (&dst)[2][NT], int b) {
+    uint2 xn1[NR][2], xn2[NR][2];  // blocks i + 1 and i + 2
+    auto load_x = [&](uint2 (&dst)[NR][2], int b) {
 #pragma unroll
-        for (int step = 0; step < 2; ++step)
+        for (int i = 0; i < NR; ++i)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                dst[step][nt] = xlive[nt] ? ld_cg_u2(xrow[nt] + (size_t)b * kBlock + 16 * step) : make_uint2(0u, 0u);
+            for (int s = 0; s < 2; ++s)
+                dst[i][s] = xlive[i] ? ld_cg_u2(xrow[i] + (size_t)b * kBlock + 16 * s) : make_uint2(0u, 0u);
     };
     if (n > 0) load_x(xn1, b0);
     if (n > 1) load_x(xn2, b0 + 1);
 
     for (int i = 0; i < n; ++i) {
-        const int ahead = i + kDepth - 1;
-        if (ahead < n) issue_unit(ring + (ahead % kDepth) * kStageS, a.q, a.s, unit0 + ahead, lane);
+        const int ahead = i + kDepthS - 1;
+        if (ahead < n) issue_unit(ring + (ahead % kDepthS) * kStageS, a.q, a.s, unit0 + ahead, lane);
         cp_async_commit();
-        cp_async_wait<kDepth - 1>();  // this lane's copies of unit i have landed
-        __syncwarp();                 // ... and every other lane's (the scales are read across lanes)
-        const unsigned char *st = ring + (i % kDepth) * kStageS;
-        uint2 xc[2][NT];
+        uint2 xc[NR][2];
 #pragma unroll
-        for (int step = 0; step < 2; ++step)
+        for (int r = 0; r < NR; ++r)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                xc[step][nt] = xn1[step][nt];
-                xn1[step][nt] = xn2[step][nt];
+            for (int s = 0; s < 2; ++s) {
+                xc[r][s] = xn1[r][s];
+                xn1[r][s] = xn2[r][s];
             }
         if (i + 2 < n) load_x(xn2, b0 + i + 2);
+        const XPlan plan = plan_block<NR, !ROWS16>(xc);
 
-        float d[NT][8][4];  // the block's sums, started by the first step's MMAs
+        cp_async_wait<kDepthS - 1>();  // this lane's copies of unit i have landed
+        __syncwarp();                  // ... and every other lane's
+        const unsigned char *st = ring + (i % kDepthS) * kStageS;
+        if (plan.f16) {
+            uint32_t af[2][4];
 #pragma unroll
-        for (int step = 0; step < 2; ++step) {
-            uint4 w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint4 *>(st + (step * 4 + j) * 512 + lane * 16);
-#pragma unroll
-            for (int wi = 0; wi < 4; ++wi) {
-                const uint32_t u0 = word_of(w[0], wi) ^ 0x80808080u;
-                const uint32_t u1 = word_of(w[1], wi) ^ 0x80808080u;
-                const uint32_t u2 = word_of(w[2], wi) ^ 0x80808080u;
-                const uint32_t u3 = word_of(w[3], wi) ^ 0x80808080u;
-                uint32_t lo[4], hi[4];  // per column: rows (4t, 4t+1) and (4t+2, 4t+3) as bf16 pairs
-                lo[0] = q8x2_to_bf16x2<0>(u0, u1, kMagicPair);
-                lo[1] = q8x2_to_bf16x2<1>(u0, u1, kMagicPair);
-                lo[2] = q8x2_to_bf16x2<2>(u0, u1, kMagicPair);
-                lo[3] = q8x2_to_bf16x2<3>(u0, u1, kMagicPair);
-                hi[0] = q8x2_to_bf16x2<0>(u2, u3, kMagicPair);
-                hi[1] = q8x2_to_bf16x2<1>(u2, u3, kMagicPair);
-                hi[2] = q8x2_to_bf16x2<2>(u2, u3, kMagicPair);
-                hi[3] = q8x2_to_bf16x2<3>(u2, u3, kMagicPair);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int p = 2 * wi + h;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (step == 0)
-                            mma_16816_first(d[nt][p], lo[2 * h], lo[2 * h + 1], hi[2 * h], hi[2 * h + 1],
-                                            xc[step][nt].x, xc[step][nt].y);
-                        else
-                            mma_16816(d[nt][p], lo[2 * h], lo[2 * h + 1], hi[2 * h], hi[2 * h + 1], xc[step][nt].x,
-                                      xc[step][nt].y);
-                    }
-                }
+            for (int s = 0; s < 2; ++s) {
+                af[s][0] = bf16x2_to_f16x2(xc[0][s].x, plan.scale[0]);
+                af[s][2] = bf16x2_to_f16x2(xc[0][s].y, plan.scale[0]);
+                af[s][1] = ROWS16 ? bf16x2_to_f16x2(xc[NR - 1][s].x, plan.scale[1]) : 0u;
+                af[s][3] = ROWS16 ? bf16x2_to_f16x2(xc[NR - 1][s].y, plan.scale[1]) : 0u;
             }
-        }
-        const float *ss = reinterpret_cast<const float *>(st + kUnit) + 16 * g;
-        float sc[16];
+            block_contract<true, ROWS16, ROWS16>(st, lane, af, plan, acc);
+        } else {
+            uint32_t ab[2][4];
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-            const float4 f = *reinterpret_cast<const float4 *>(ss + 4 * v4);
-            sc[4 * v4 + 0] = f.x;
-            sc[4 * v4 + 1] = f.y;
-            sc[4 * v4 + 2] = f.z;
-            sc[4 * v4 + 3] = f.w;
+            for (int s = 0; s < 2; ++s) {
+                ab[s][0] = xc[0][s].x;
+                ab[s][2] = xc[0][s].y;
+                ab[s][1] = ROWS16 ? xc[NR - 1][s].x : 0u;
+                ab[s][3] = ROWS16 ? xc[NR - 1][s].y : 0u;
+            }
+            block_contract<false, ROWS16, ROWS16>(st, lane, ab, plan, acc);
         }
         __syncwarp();  // every lane is done with this stage before it is refilled
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                acc[nt][p][0] = fmaf(sc[2 * p], d[nt][p][0], acc[nt][p][0]);
-                acc[nt][p][1] = fmaf(sc[2 * p], d[nt][p][1], acc[nt][p][1]);
-                acc[nt][p][2] = fmaf(sc[2 * p + 1], d[nt][p][2], acc[nt][p][2]);
-                acc[nt][p][3] = fmaf(sc[2 * p + 1], d[nt][p][3], acc[nt][p][3]);
-            }
     }
     cp_async_wait<0>();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();  // every warp is done with its ring: the shared memory holds the epilogue now
 
-    // D fragment: element 0/1 -> activation rows 2t, 2t+1 of MMA row g (column 16g + 2p); 2/3 -> the same rows of
-    // MMA row g + 8 (column 16g + 2p + 1).
     float *red = reinterpret_cast<float *>(smem_s);  // [kWarpsS][MR][128]
     float *mine = red + warp * MR * kTmaColumns;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            const int r = 8 * nt + 2 * t;
-            const int c = 16 * g + 2 * p;
-            *reinterpret_cast<float2 *>(mine + r * kTmaColumns + c) = make_float2(acc[nt][p][0], acc[nt][p][2]);
-            *reinterpret_cast<float2 *>(mine + (r + 1) * kTmaColumns + c) = make_float2(acc[nt][p][1], acc[nt][p][3]);
+        for (int j = 0; j < kSlices; ++j) {
+            float lo, hi;
+            unpack_f32x2(acc[r][j], lo, hi);
+            *reinterpret_cast<float2 *>(mine + (g + 8 * r) * kTmaColumns + 8 * j + 2 * t) = make_float2(lo, hi);
         }
     __syncthreads();
     finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
 }
 
+// m <= 2 on CUDA cores: in segment (s, h) lane (g, t) holds words w = 0..3, each four weight rows 16s + 4t + 0..3 of
+// column 8(4h + w) + g; they meet the lane's four activations of each row with two packed fp32x2 FMAs (exact
+// products), the block's sums of a column are folded with its scale, and at the end the four lanes t of a column
+// add their carries.
+// Stored bytes E, E + 1 of a word as the exact fp32 pair {q_E, q_E+1}: each byte in the low mantissa of 2^23 gives
+// 2^23 + q + 128, and one packed subtract of 2^23 + 128 leaves q.
+template <int E> __device__ __forceinline__ unsigned long long q8x2_to_f32x2(uint32_t u) {
+    unsigned long long d;
+    asm("{\n .reg .b32 a, b;\n .reg .b64 p;\n prmt.b32 a, %1, 0x4B000000, %2;\n prmt.b32 b, %1, 0x4B000000, %3;\n"
+        " mov.b64 p, {a, b};\n sub.rn.f32x2 %0, p, %4;\n}"
+        : "=l"(d)
+        : "r"(u), "n"(0x7540 + E), "n"(0x7540 + E + 1), "l"(kMagicPair));
+    return d;
+}
 
-// The CUDA-core inner loop over the same stream, for m <= 2 (where the per-row FMAs are cheaper than packing bf16
-// MMA operands).  In segment (s, j) lane L = 4g + u holds 16 columns 16g .. 16g + 15 of weight row 16s + 4u + j: it
-// converts each pair of values to an exact fp32 pair and accumulates x[r, row] * q into the block's sums with packed
-// fp32x2 FMAs, folds the sums into its carry with the block's scales, and at the end the four lanes u of a column
-// group add their carries (rows 4u + j of every step) in a fixed order.
 template <int M, bool ARGMAX>
 __global__ void __launch_bounds__(kThreadsS, 2)
     stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
-    constexpr int kDepth = StreamShape<1>::kDepth;
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, u = lane & 3;
+    const int g = lane >> 2, t = lane & 3;
     const int tile = select_part(parts, blockIdx.x, a);
     const int rank = blockIdx.y;
     const int c0 = (int)((long long)a.nb * rank / a.ksplit);
@@ -285,18 +432,18 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     const int b0 = c0 + (c1 - c0) * warp / kWarpsS;
     const int b1 = c0 + (c1 - c0) * (warp + 1) / kWarpsS;
     const int n = b1 - b0;
-    unsigned char *ring = smem_s + warp * kDepth * kStageS;
+    unsigned char *ring = smem_s + warp * kDepthS * kStageS;
     const size_t unit0 = (size_t)tile * a.nb + b0;
 
-    unsigned long long acc[M][8];  // fp32 pairs: columns 16g + 2p, 16g + 2p + 1
+    unsigned long long acc[M][kSlices];  // per row and column 8j + g: the carry of rows 4t, 4t+2 | 4t+1, 4t+3
 #pragma unroll
     for (int r = 0; r < M; ++r)
 #pragma unroll
-        for (int p = 0; p < 8; ++p) acc[r][p] = 0ull;
+        for (int j = 0; j < kSlices; ++j) acc[r][j] = 0ull;
 
     if (prefetch_weights) {
 #pragma unroll
-        for (int i = 0; i < kDepth - 1; ++i) {
+        for (int i = 0; i < kDepthS - 1; ++i) {
             if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
             cp_async_commit();
         }
@@ -304,30 +451,26 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!prefetch_weights) {
 #pragma unroll
-        for (int i = 0; i < kDepth - 1; ++i) {
+        for (int i = 0; i < kDepthS - 1; ++i) {
             if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
             cp_async_commit();
         }
     }
 
-    // x[r][32b + 16s + 4u .. + 3]: the activations of this lane's rows, two 8-byte loads per row and block.
-    uint2 xn1[M][2], xn2[M][2];  // blocks i + 1 and i + 2
+    uint2 xn1[M][2], xn2[M][2];
     auto load_x = [&](uint2 (&dst)[M][2], int b) {
 #pragma unroll
         for (int r = 0; r < M; ++r)
 #pragma unroll
-            for (int s = 0; s < 2; ++s) dst[r][s] = ld_cg_u2(a.x + (size_t)r * a.K + (size_t)b * kBlock + 16 * s + 4 * u);
+            for (int s = 0; s < 2; ++s) dst[r][s] = ld_cg_u2(a.x + (size_t)r * a.K + (size_t)b * kBlock + 16 * s + 4 * t);
     };
     if (n > 0) load_x(xn1, b0);
     if (n > 1) load_x(xn2, b0 + 1);
 
     for (int i = 0; i < n; ++i) {
-        const int ahead = i + kDepth - 1;
-        if (ahead < n) issue_unit(ring + (ahead % kDepth) * kStageS, a.q, a.s, unit0 + ahead, lane);
+        const int ahead = i + kDepthS - 1;
+        if (ahead < n) issue_unit(ring + (ahead % kDepthS) * kStageS, a.q, a.s, unit0 + ahead, lane);
         cp_async_commit();
-        cp_async_wait<kDepth - 1>();
-        __syncwarp();
-        const unsigned char *st = ring + (i % kDepth) * kStageS;
         uint2 xc[M][2];
 #pragma unroll
         for (int r = 0; r < M; ++r)
@@ -337,49 +480,48 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 xn1[r][s] = xn2[r][s];
             }
         if (i + 2 < n) load_x(xn2, b0 + i + 2);
-
-        unsigned long long part[M][8];
+        // activations as fp32 pairs {x[4t], x[4t+1]} and {x[4t+2], x[4t+3]} of each row and half
+        unsigned long long xp[M][2][2];
 #pragma unroll
         for (int r = 0; r < M; ++r)
 #pragma unroll
-            for (int p = 0; p < 8; ++p) part[r][p] = 0ull;
+            for (int s = 0; s < 2; ++s) {
+                xp[r][s][0] = pack_f32x2(bf16_lo(xc[r][s].x), bf16_hi(xc[r][s].x));
+                xp[r][s][1] = pack_f32x2(bf16_lo(xc[r][s].y), bf16_hi(xc[r][s].y));
+            }
+        cp_async_wait<kDepthS - 1>();
+        __syncwarp();
+        const unsigned char *st = ring + (i % kDepthS) * kStageS;
+        unsigned long long part[M][kSlices];
 #pragma unroll
         for (int s = 0; s < 2; ++s)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(st + (s * 4 + j) * 512 + lane * 16);
-                unsigned long long xx[M];
+            for (int h = 0; h < 4; ++h) {
+                const uint4 wv = *reinterpret_cast<const uint4 *>(st + (4 * s + h) * 512 + lane * 16);
 #pragma unroll
-                for (int r = 0; r < M; ++r) {
-                    const uint32_t pr = (j < 2) ? xc[r][s].x : xc[r][s].y;
-                    const float xv = (j & 1) ? bf16_hi(pr) : bf16_lo(pr);
-                    xx[r] = pack_f32x2(xv, xv);
-                }
-#pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-                    const uint32_t uw = word_of(w, wi) ^ 0x80808080u;
-                    const unsigned long long q01 = q8x2_to_f32x2<0>(uw, kMagicPair);
-                    const unsigned long long q23 = q8x2_to_f32x2<2>(uw, kMagicPair);
+                for (int w = 0; w < 4; ++w) {
+                    const int j = 4 * h + w;
+                    const uint32_t u = word_of(wv, w);
+                    const unsigned long long q01 = q8x2_to_f32x2<0>(u), q23 = q8x2_to_f32x2<2>(u);
 #pragma unroll
                     for (int r = 0; r < M; ++r) {
-                        part[r][2 * wi] = fma_f32x2(q01, xx[r], part[r][2 * wi]);
-                        part[r][2 * wi + 1] = fma_f32x2(q23, xx[r], part[r][2 * wi + 1]);
+                        if (s == 0)
+                            part[r][j] = mul_f32x2(q01, xp[r][0][0]);
+                        else
+                            part[r][j] = fma_f32x2(q01, xp[r][1][0], part[r][j]);
+                        part[r][j] = fma_f32x2(q23, xp[r][s][1], part[r][j]);
                     }
                 }
             }
-        unsigned long long sc[8];
-        const uint4 *ss = reinterpret_cast<const uint4 *>(st + kUnit) + 4 * g;
+        const float *ss = reinterpret_cast<const float *>(st + kUnit) + g;
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-            const uint4 f = ss[v4];
-            sc[2 * v4] = ((unsigned long long)f.y << 32) | f.x;
-            sc[2 * v4 + 1] = ((unsigned long long)f.w << 32) | f.z;
+        for (int j = 0; j < kSlices; ++j) {
+            const float sv = ss[8 * j];
+            const unsigned long long s2 = pack_f32x2(sv, sv);
+#pragma unroll
+            for (int r = 0; r < M; ++r) acc[r][j] = fma_f32x2(s2, part[r][j], acc[r][j]);
         }
-        __syncwarp();  // every lane is done with this stage before it is refilled
-#pragma unroll
-        for (int r = 0; r < M; ++r)
-#pragma unroll
-            for (int p = 0; p < 8; ++p) acc[r][p] = fma_f32x2(sc[p], part[r][p], acc[r][p]);
+        __syncwarp();
     }
     cp_async_wait<0>();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -390,208 +532,24 @@ __global__ void __launch_bounds__(kThreadsS, 2)
 #pragma unroll
     for (int r = 0; r < M; ++r)
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
+        for (int j = 0; j < kSlices; ++j) {
             float lo, hi;
-            unpack_f32x2(acc[r][p], lo, hi);
-            lo += __shfl_xor_sync(0xffffffffu, lo, 1);
-            hi += __shfl_xor_sync(0xffffffffu, hi, 1);
-            lo += __shfl_xor_sync(0xffffffffu, lo, 2);
-            hi += __shfl_xor_sync(0xffffffffu, hi, 2);
-            if (u == 0) *reinterpret_cast<float2 *>(mine + r * kTmaColumns + 16 * g + 2 * p) = make_float2(lo, hi);
+            unpack_f32x2(acc[r][j], lo, hi);
+            float v = lo + hi;
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (t == 0) mine[r * kTmaColumns + 8 * j + g] = v;
         }
     __syncthreads();
     finish_n<kWarpsS, M, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
 }
 
-
-// m = 9..16: two tiles of 8 activation rows.  The accumulators of 16 rows x 128 columns would not fit one warp's
-// registers at two CTAs per SM, so a block's columns are split between a warp pair: warp 2k + h streams and converts
-// columns 64h .. 64h + 63 of every unit of its K range (each value is still converted once).  Each warp keeps its
-// own ring of five half-units (2 KB of values and 256 B of scales each); lane (g, t) of warp h holds 8 columns
-// 64h + 8g .. 64h + 8g + 7, the second half of chunk 4h + g/2 of its row group t.
-constexpr int kHalfUnit = kUnit / 2;
-constexpr int kHalfStage = kHalfUnit + kUnitScales * 2;
-constexpr int kPairDepth = 5;
-constexpr int kPairSmem = kWarpsS * kPairDepth * kHalfStage;
-
-__device__ __forceinline__ void issue_half_unit(unsigned char *stage, const int8_t *q, const float *s, size_t u,
-                                                int h, int lane) {
-    const unsigned char *src = reinterpret_cast<const unsigned char *>(q) + u * kUnit + 256 * h + (lane & 15) * 16;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int seg = 2 * c + (lane >> 4);
-        cp_async16(stage + seg * 256 + (lane & 15) * 16, src + seg * 512);
-    }
-    if (lane < 16)
-        cp_async16(stage + kHalfUnit + lane * 16,
-                   reinterpret_cast<const unsigned char *>(s + u * kUnitScales + 64 * h) + lane * 16);
-}
-
-template <bool ARGMAX>
-__global__ void __launch_bounds__(kThreadsS, 2)
-    stream_pair_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
-    constexpr int NT = 2, MR = 16, NP = 4, kDepth = kPairDepth, kRanges = kWarpsS / 2;
-    extern __shared__ __align__(16) unsigned char smem_s[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int h = warp & 1, kr = warp >> 1;
-    const int tile = select_part(parts, blockIdx.x, a);
-    const int rank = blockIdx.y;
-    const int c0 = (int)((long long)a.nb * rank / a.ksplit);
-    const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
-    const int b0 = c0 + (c1 - c0) * kr / kRanges;
-    const int b1 = c0 + (c1 - c0) * (kr + 1) / kRanges;
-    const int n = b1 - b0;
-    unsigned char *ring = smem_s + warp * kDepth * kHalfStage;
-    const size_t unit0 = (size_t)tile * a.nb + b0;
-
-    float acc[NT][NP][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int p = 0; p < NP; ++p)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[nt][p][i] = 0.0f;
-
-    if (prefetch_weights) {
-#pragma unroll
-        for (int i = 0; i < kDepth - 1; ++i) {
-            if (i < n) issue_half_unit(ring + i * kHalfStage, a.q, a.s, unit0 + i, h, lane);
-            cp_async_commit();
-        }
-    }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (!prefetch_weights) {
-#pragma unroll
-        for (int i = 0; i < kDepth - 1; ++i) {
-            if (i < n) issue_half_unit(ring + i * kHalfStage, a.q, a.s, unit0 + i, h, lane);
-            cp_async_commit();
-        }
-    }
-
-    const uint16_t *xrow[NT];
-    bool xlive[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int r = 8 * nt + g;
-        xlive[nt] = r < a.m;
-        xrow[nt] = a.x + (size_t)(xlive[nt] ? r : 0) * a.K + 4 * t;
-    }
-    uint2 xn1[2][NT], xn2[2][NT];
-    auto load_x = [&](uint2 (&dst)[2][NT], int b) {
-#pragma unroll
-        for (int step = 0; step < 2; ++step)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                dst[step][nt] = xlive[nt] ? ld_cg_u2(xrow[nt] + (size_t)b * kBlock + 16 * step) : make_uint2(0u, 0u);
-    };
-    if (n > 0) load_x(xn1, b0);
-    if (n > 1) load_x(xn2, b0 + 1);
-    const int woff = (4 * (g >> 1) + t) * 16 + 8 * (g & 1);  // this lane's 8 bytes within a 256-byte half-segment
-
-    for (int i = 0; i < n; ++i) {
-        const int ahead = i + kDepth - 1;
-        if (ahead < n) issue_half_unit(ring + (ahead % kDepth) * kHalfStage, a.q, a.s, unit0 + ahead, h, lane);
-        cp_async_commit();
-        cp_async_wait<kDepth - 1>();
-        __syncwarp();
-        const unsigned char *st = ring + (i % kDepth) * kHalfStage;
-        uint2 xc[2][NT];
-#pragma unroll
-        for (int step = 0; step < 2; ++step)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                xc[step][nt] = xn1[step][nt];
-                xn1[step][nt] = xn2[step][nt];
-            }
-        if (i + 2 < n) load_x(xn2, b0 + i + 2);
-
-        float d[NT][NP][4];  // the block's sums, started by the first step's MMAs
-#pragma unroll
-        for (int step = 0; step < 2; ++step) {
-            uint2 w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint2 *>(st + (step * 4 + j) * 256 + woff);
-#pragma unroll
-            for (int wi = 0; wi < 2; ++wi) {
-                const uint32_t u0 = word_of(w[0], wi) ^ 0x80808080u;
-                const uint32_t u1 = word_of(w[1], wi) ^ 0x80808080u;
-                const uint32_t u2 = word_of(w[2], wi) ^ 0x80808080u;
-                const uint32_t u3 = word_of(w[3], wi) ^ 0x80808080u;
-                uint32_t lo[4], hi[4];
-                lo[0] = q8x2_to_bf16x2<0>(u0, u1, kMagicPair);
-                lo[1] = q8x2_to_bf16x2<1>(u0, u1, kMagicPair);
-                lo[2] = q8x2_to_bf16x2<2>(u0, u1, kMagicPair);
-                lo[3] = q8x2_to_bf16x2<3>(u0, u1, kMagicPair);
-                hi[0] = q8x2_to_bf16x2<0>(u2, u3, kMagicPair);
-                hi[1] = q8x2_to_bf16x2<1>(u2, u3, kMagicPair);
-                hi[2] = q8x2_to_bf16x2<2>(u2, u3, kMagicPair);
-                hi[3] = q8x2_to_bf16x2<3>(u2, u3, kMagicPair);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int p = 2 * wi + hh;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (step == 0)
-                            mma_16816_first(d[nt][p], lo[2 * hh], lo[2 * hh + 1], hi[2 * hh], hi[2 * hh + 1],
-                                            xc[step][nt].x, xc[step][nt].y);
-                        else
-                            mma_16816(d[nt][p], lo[2 * hh], lo[2 * hh + 1], hi[2 * hh], hi[2 * hh + 1],
-                                      xc[step][nt].x, xc[step][nt].y);
-                    }
-                }
-            }
-        }
-        const float *ss = reinterpret_cast<const float *>(st + kHalfUnit) + 8 * g;
-        float sc[8];
-#pragma unroll
-        for (int v4 = 0; v4 < 2; ++v4) {
-            const float4 f = *reinterpret_cast<const float4 *>(ss + 4 * v4);
-            sc[4 * v4 + 0] = f.x;
-            sc[4 * v4 + 1] = f.y;
-            sc[4 * v4 + 2] = f.z;
-            sc[4 * v4 + 3] = f.w;
-        }
-        __syncwarp();
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int p = 0; p < NP; ++p) {
-                acc[nt][p][0] = fmaf(sc[2 * p], d[nt][p][0], acc[nt][p][0]);
-                acc[nt][p][1] = fmaf(sc[2 * p], d[nt][p][1], acc[nt][p][1]);
-                acc[nt][p][2] = fmaf(sc[2 * p + 1], d[nt][p][2], acc[nt][p][2]);
-                acc[nt][p][3] = fmaf(sc[2 * p + 1], d[nt][p][3], acc[nt][p][3]);
-            }
-    }
-    cp_async_wait<0>();
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __syncthreads();
-
-    float *red = reinterpret_cast<float *>(smem_s);  // [kRanges][MR][128]
-    float *mine = red + kr * MR * kTmaColumns;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int p = 0; p < NP; ++p) {
-            const int r = 8 * nt + 2 * t;
-            const int c = 64 * h + 8 * g + 2 * p;
-            *reinterpret_cast<float2 *>(mine + r * kTmaColumns + c) = make_float2(acc[nt][p][0], acc[nt][p][2]);
-            *reinterpret_cast<float2 *>(mine + (r + 1) * kTmaColumns + c) = make_float2(acc[nt][p][1], acc[nt][p][3]);
-        }
-    __syncthreads();
-    finish_n<kRanges, MR, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
-}
-
-static_assert(finish_smem_n(kWarpsS / 2, 16, kTmaColumns) <= kPairSmem, "the epilogue fits in the rings");
-static_assert(2 * kPairSmem <= 227 * 1024, "two CTAs per SM");
-
-static_assert(finish_smem_n(kWarpsS, 8, kTmaColumns) <= StreamShape<1>::kSmem, "the epilogue fits in the rings");
-static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns) <= StreamShape<2>::kSmem, "the epilogue fits in the rings");
-static_assert(2 * StreamShape<1>::kSmem <= 227 * 1024 && StreamShape<2>::kSmem <= 227 * 1024, "residency");
+static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns) <= kSmemS, "the epilogue fits in the rings");
+static_assert(2 * kSmemS <= 227 * 1024, "two CTAs per SM");
 
 template <typename Kernel>
-cudaError_t launch_stream_kernel(Kernel kernel, int kSmemS, const Args &a, const Parts &pt, cudaStream_t stream,
-                                 bool pdl, bool prefetch) {
+cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, cudaStream_t stream, bool pdl,
+                                 bool prefetch) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -626,23 +584,18 @@ int stream_ctas_per_sm(int) { return 2; }
 
 cudaError_t launch_stream(const Args &a, const Parts &pt, bool argmax, cudaStream_t stream, bool pdl,
                           bool prefetch_weights) {
-    constexpr int s1 = StreamShape<1>::kSmem;
     const bool p = prefetch_weights;
-    switch (a.m) {
-        case 1:
-            return argmax ? launch_stream_kernel(stream_simt_kernel<1, true>, s1, a, pt, stream, pdl, p)
-                          : launch_stream_kernel(stream_simt_kernel<1, false>, s1, a, pt, stream, pdl, p);
-        case 2:
-            return argmax ? launch_stream_kernel(stream_simt_kernel<2, true>, s1, a, pt, stream, pdl, p)
-                          : launch_stream_kernel(stream_simt_kernel<2, false>, s1, a, pt, stream, pdl, p);
-        default:
-            break;
-    }
+    if (a.m == 1)
+        return argmax ? launch_stream_kernel(stream_simt_kernel<1, true>, a, pt, stream, pdl, p)
+                      : launch_stream_kernel(stream_simt_kernel<1, false>, a, pt, stream, pdl, p);
+    if (a.m == 2)
+        return argmax ? launch_stream_kernel(stream_simt_kernel<2, true>, a, pt, stream, pdl, p)
+                      : launch_stream_kernel(stream_simt_kernel<2, false>, a, pt, stream, pdl, p);
     if (a.m <= 8)
-        return argmax ? launch_stream_kernel(stream_kernel<1, true>, s1, a, pt, stream, pdl, p)
-                      : launch_stream_kernel(stream_kernel<1, false>, s1, a, pt, stream, pdl, p);
-    return argmax ? launch_stream_kernel(stream_pair_kernel<true>, kPairSmem, a, pt, stream, pdl, p)
-                  : launch_stream_kernel(stream_pair_kernel<false>, kPairSmem, a, pt, stream, pdl, p);
+        return argmax ? launch_stream_kernel(stream_kernel<false, true>, a, pt, stream, pdl, p)
+                      : launch_stream_kernel(stream_kernel<false, false>, a, pt, stream, pdl, p);
+    return argmax ? launch_stream_kernel(stream_kernel<true, true>, a, pt, stream, pdl, p)
+                  : launch_stream_kernel(stream_kernel<true, false>, a, pt, stream, pdl, p);
 }
 
 }  // namespace q8

@@ -5,11 +5,12 @@
 // where that lane loads them.
 //
 // Layout (Nt = N rounded up to a multiple of 128, T = Nt / 128 tiles, nb = K / 32 blocks):
-//   values  int8  unit (t, b) at byte (t * nb + b) * 4096: eight 512-byte segments, segment 4s + j (s = 0, 1;
-//                 j = 0..3) holding, at byte 16 * L for L = 4g + u (g = 0..7, u = 0..3), the 16 values of weight row
-//                 32b + 16s + 4u + j, columns 128t + 16g .. 128t + 16g + 15, in column order
+//   values  uint8 unit (t, b) at byte (t * nb + b) * 4096: eight 512-byte segments, segment 4s + h (s = 0, 1: the
+//                 16-row half of the block; h = 0..3: a group of four 8-column slices).  In segment (s, h) the 16 bytes
+//                 at 16 * L, L = 4g + u (g = 0..7, u = 0..3), are four words; word w holds the values of weight rows
+//                 32b + 16s + 4u + k (k = 0..3, byte k) in column 128t + 8(4h + w) + g, each stored as q + 128
 //   scales  fp32  unit (t, b) at element (t * nb + b) * 128; element c = s[b][128t + c]
-//   columns >= N are zero.
+//   columns >= N hold q = 0 (byte 128) and scale 0.
 #include <string.h>
 
 #include "../../include/q8_gemv.h"
@@ -23,8 +24,8 @@ namespace {
 
 constexpr int kTileCols = 128;
 
-// One thread per 16-byte chunk of the tiled values (the chunk's row and 16 columns); the first 8 threads of a unit
-// also write its scales.
+// One thread per 16-byte chunk of the tiled values (four rows of four columns); the first 8 threads of a unit also
+// write its scales.
 __global__ void tile_values_kernel(const int8_t *__restrict__ q, const float *__restrict__ s, int K, int N, int Np,
                                    int8_t *__restrict__ qt, float *__restrict__ st, long long chunks) {
     const long long id = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -33,19 +34,17 @@ __global__ void tile_values_kernel(const int8_t *__restrict__ q, const float *__
     const long long unit = id / 256;  // 4096 B = 256 chunks per unit
     const int within = (int)(id % 256);
     const int seg = within / 32, L = within % 32;
-    const int step = seg / 4, j = seg % 4, g = L / 4, u = L % 4;
+    const int step = seg / 4, h = seg % 4, g = L / 4, u = L % 4;
     const int t = (int)(unit / nb), b = (int)(unit % nb);
-    const int r = 16 * step + 4 * u + j;        // row within the 32-row block
-    const int c0 = kTileCols * t + 16 * g;      // first weight column of the chunk
-    const long long krow = (long long)Q8_BLOCK * b + r;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (c0 + 16 <= N) {
-        v = *reinterpret_cast<const uint4 *>(q + krow * Np + c0);
-    } else if (c0 < N) {
-        unsigned char tmp[16];
-        for (int i = 0; i < 16; ++i) tmp[i] = c0 + i < N ? (unsigned char)q[krow * Np + c0 + i] : 0;
-        memcpy(&v, tmp, 16);
+    const long long krow = (long long)Q8_BLOCK * b + 16 * step + 4 * u;  // first of the chunk's four weight rows
+    unsigned char tmp[16];
+    for (int w = 0; w < 4; ++w) {
+        const int c = kTileCols * t + 8 * (4 * h + w) + g;
+        for (int k = 0; k < 4; ++k)
+            tmp[4 * w + k] = (unsigned char)((c < N ? (int)q[(krow + k) * Np + c] : 0) + 128);
     }
+    uint4 v;
+    memcpy(&v, tmp, 16);
     *reinterpret_cast<uint4 *>(qt + id * 16) = v;
     if (within < 8) {  // the unit's scales: 8 threads x 16 fp32
         for (int i = 0; i < 16; ++i) {
@@ -79,12 +78,13 @@ extern "C" q8_status q8_tile(const int8_t *q, const float *s, int K, int N, int8
             const size_t unit = (size_t)t * nb + b;
             int8_t *dst = qt + unit * (Q8_BLOCK * kTileCols);
             for (int r = 0; r < Q8_BLOCK; ++r) {
-                const int step = r / 16, u = (r % 16) / 4, j = r % 4;
+                const int step = r / 16, u = (r % 16) / 4, k = r % 4;
                 for (int c = 0; c < kTileCols; ++c) {
                     const int n = kTileCols * t + c;
-                    const int L = 4 * (c / 16) + u;
-                    const size_t at = (size_t)(4 * step + j) * 512 + 16 * L + c % 16;
-                    dst[at] = n < N ? q[((size_t)Q8_BLOCK * b + r) * Np + n] : 0;
+                    const int j = c / 8, g = c % 8;
+                    const size_t at = (size_t)(4 * step + j / 4) * 512 + 16 * (4 * g + u) + 4 * (j % 4) + k;
+                    const int v = n < N ? (int)q[((size_t)Q8_BLOCK * b + r) * Np + n] : 0;
+                    dst[at] = (int8_t)(unsigned char)(v + 128);
                 }
             }
             for (int c = 0; c < kTileCols; ++c) {

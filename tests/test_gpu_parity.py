@@ -111,23 +111,127 @@ def test_edge_shapes(dev, m, K, N):
 
 @pytest.mark.parametrize("m", [1, 4, 16])
 def test_attention_projection_4096(dev, m):
-    """The 7B-class attention projection, K = N = 4096, m = 1, 4, 16: every output."""
+    """The 7B-class attention projection, K = N = 4096, m = 1, 4, 16: every output, row-major and tiled."""
     x, q, s = si.case(m, 4096, 4096, si.case_seed(1, m))
     y_o, a_o = oracle.gemv(x, q, s)
-    _assert_close(_gemv(dev, x, q, s, 4096), y_o, a_o, f"m={m}")
+    for v in ("auto", "tiled"):
+        _assert_close(_gemv(dev, x, q, s, 4096, v), y_o, a_o, f"m={m} {v}")
 
 
 @pytest.mark.parametrize("K,N", [(4096, 14336), (14336, 4096)])
 @pytest.mark.parametrize("m", [1, 2, 4, 8, 16])
 def test_ffn_projections_sampled(dev, K, N, m):
     """FFN up/gate (4096 x 14336) and down (14336 x 4096) at full size, m = 1, 2, 4, 8, 16, in the benchmark's
-    launch configuration; checked on 384 sampled columns (tile edges, the last columns and random ones)."""
+    launch configuration (tiled) and row-major; checked on 384 sampled columns (tile edges, the last columns and
+    random ones)."""
     x, q, s = si.case(m, K, N, si.case_seed(2, m, 1 if K > N else 0))
     rng = np.random.default_rng(m)
     cols = np.unique(np.r_[0:32, 120:136, 248:264, 504:520, N - 32:N, rng.integers(0, N, 256)])
     y_o, a_o = oracle.gemv(x, q, s, cols)
-    y = _gemv(dev, x, q, s, N)
-    _assert_close(y[:, cols], y_o, a_o, f"K={K} N={N} m={m}")
+    for v in ("auto", "tiled"):
+        y = _gemv(dev, x, q, s, N, v)
+        _assert_close(y[:, cols], y_o, a_o, f"K={K} N={N} m={m} {v}")
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# activation magnitude ranges (the tiled path's exact fp16 scaling and its bf16 alternative)
+# --------------------------------------------------------------------------------------------------------------------
+
+def _bits(v):
+    a = np.asarray(v, dtype=np.float32)
+    return si.f32_to_bf16_bits(a).reshape(a.shape)
+
+
+def _ranged_case(m, kinds=tuple(range(12)), nb_each=2, N=300, seed=4242):
+    """Activations built block by block (all rows of a 32-row block share a kind), every kind twice:
+    0 N(0,1); 1 N(0,1) * 1e30; 2 N(0,1) * 1e-30; 3 N(0,1) * 1e-36 (below the scalable range); 4 rows alternating
+    1e10 and 1e-10 (a 66-binade span); 5 one 1.0 per row and 1e-12 * N(0,1) elsewhere, with the weight row of the
+    1.0 zeroed in 150 columns (the large activation meets zero weights); 6 signed powers 2^-26 .. 2^3 with random
+    mantissas, both ends present (a 29-binade span: the widest exact fp16 scaling); 7 as 6 plus one 2^-27 (one binade
+    more); 8 N(0,1) with a few bf16 subnormals; 9 zeros and negative zeros; 10 zeros with a few N(0,1) values;
+    11 values +-1.9921875 * 2^k, k in -10..9 (the largest bf16 mantissa in the top binade: 65280 after scaling).
+    Blocks cycle through `kinds`."""
+    nb = len(kinds) * nb_each
+    K = 32 * nb
+    rng = np.random.default_rng(seed)
+    x = np.zeros((m, K), dtype=np.uint16)
+    _, q, s = si.case(1, K, N, seed)
+    for b in range(nb):
+        kind = kinds[b % len(kinds)]
+        sl = slice(32 * b, 32 * b + 32)
+        g = rng.standard_normal((m, 32)).astype(np.float32)
+        if kind == 0:
+            v = _bits(g)
+        elif kind == 1:
+            v = _bits(g * np.float32(1e30))
+        elif kind == 2:
+            v = _bits(g * np.float32(1e-30))
+        elif kind == 3:
+            v = _bits(g * np.float32(1e-36))
+        elif kind == 4:
+            f = np.where(np.arange(m)[:, None] % 2 == 0, np.float32(1e10), np.float32(1e-10))
+            v = _bits(g * f)
+        elif kind == 5:
+            v = _bits(g * np.float32(1e-12))
+            v[:, 0] = _bits(np.float32(1.0))
+            q[32 * b, :150] = 0
+        elif kind in (6, 7):
+            e = rng.integers(-26, 4, size=(m, 32))
+            e[:, 0], e[:, 1] = 3, -26
+            mant = 1.0 + rng.integers(0, 128, size=(m, 32)) / 128.0
+            sign = np.where(rng.integers(0, 2, size=(m, 32)) == 1, -1.0, 1.0)
+            v = _bits((sign * mant * np.exp2(e)).astype(np.float32))
+            if kind == 7:
+                v[m - 1, 5] = _bits(np.float32(-1.5 * 2.0 ** -27))
+        elif kind == 8:
+            v = _bits(g)
+            v[:, 3] = np.uint16(0x0041)
+            v[0, 7] = np.uint16(0x8005)
+        elif kind == 9:
+            v = np.where(rng.integers(0, 2, size=(m, 32)) == 1, np.uint16(0x8000), np.uint16(0)).astype(np.uint16)
+        elif kind == 10:
+            v = np.zeros((m, 32), dtype=np.uint16)
+            v[:, 4] = _bits(g[:, 4])
+            v[0, 31] = _bits(g[0, 31])
+        else:
+            k = rng.integers(-10, 10, size=(m, 32))
+            k[:, 0] = 9
+            v = _bits((1.9921875 * np.exp2(k) * np.sign(g + 0.5)).astype(np.float32))
+        x[:, sl] = v
+    return x, q, s, N
+
+
+@pytest.mark.parametrize("kinds", [tuple(range(12))] + [(k,) for k in range(12)], ids=lambda k: "-".join(map(str, k)))
+@pytest.mark.parametrize("m", [5, 16])
+def test_activation_magnitude_ranges(dev, m, kinds):
+    """Every activation range the scaled fp16 operands must either represent exactly or hand to bf16 operands: the
+    bound holds for every output of every kernel family, all kinds mixed and each kind alone (so that the bound is
+    set by that kind's own magnitudes), including the columns whose large activations meet zero weights (A is then
+    set by the 1e-12 values alone)."""
+    x, q, s, N = _ranged_case(m, kinds, nb_each=24 // len(kinds))
+    y_o, a_o = oracle.gemv(x, q, s)
+    for v in _variants(m):
+        _assert_close(_gemv(dev, x, q, s, N, v), y_o, a_o, f"m={m} kinds={kinds} {v}")
+
+
+@pytest.mark.parametrize("m", [3, 12])
+def test_nonfinite_activations_propagate(dev, m):
+    """inf, -inf and NaN activations give the oracle's NaN / +-inf pattern in the outputs (IEEE: inf * 0 and
+    inf - inf are NaN); every finite output meets the bound."""
+    K, N = 512, 260
+    x, q, s = si.case(m, K, N, 515 + m)
+    x[0, 40] = np.uint16(0x7F80)           # +inf
+    x[m - 1, 300] = np.uint16(0xFF80)      # -inf
+    x[1, 77] = np.uint16(0x7FC0)           # NaN
+    y_o, a_o = oracle.gemv(x, q, s)
+    for v in _variants(m):
+        y = _gemv(dev, x, q, s, N, v).astype(np.float64)[:, :N]
+        yo, ao = y_o[:, :N], a_o[:, :N]
+        assert np.array_equal(np.isnan(y), np.isnan(yo)), v
+        inf = np.isinf(yo)
+        assert np.array_equal(np.isinf(y), inf) and np.array_equal(y[inf], yo[inf]), v
+        fin = np.isfinite(yo)
+        assert np.all(np.abs(y[fin] - yo[fin]) <= TOL * ao[fin]), v
 
 
 # --------------------------------------------------------------------------------------------------------------------

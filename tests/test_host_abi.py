@@ -198,25 +198,28 @@ def test_binding_refuses_cpu_tensors(lib):
 # --------------------------------------------------------------------------------------------------------------------
 
 def _tile_reference(q, s, N):
+    """The documented tiled order, written as the index map of the header: the byte of weight row 32b + 16s + 4u + k
+    in column 128t + 8(4h + w) + g sits at 512(4s + h) + 16(4g + u) + 4w + k of unit (t, b), stored as q + 128;
+    columns >= N hold byte 128 (q = 0) and scale 0."""
     K = q.shape[0]
     nb, Nt = K // 32, -(-N // 128) * 128
     T = Nt // 128
-    qt = np.zeros((T, nb, 32, 128), dtype=np.int8)
+    qt = np.full((T, nb, 4096), 128, dtype=np.uint8)
     st = np.zeros((T, nb, 128), dtype=np.float32)
-    qt = qt.reshape(T, nb, 4096)
     for t in range(T):
         for b in range(nb):
             for r in range(32):
-                step, u, j = r // 16, (r % 16) // 4, r % 4
+                step, u, k = r // 16, (r % 16) // 4, r % 4
                 for c in range(128):
                     n = 128 * t + c
                     if n < N:
-                        lane = 4 * (c // 16) + u
-                        qt[t, b, (4 * step + j) * 512 + 16 * lane + c % 16] = q[32 * b + r, n]
+                        j, g = c // 8, c % 8
+                        at = 512 * (4 * step + j // 4) + 16 * (4 * g + u) + 4 * (j % 4) + k
+                        qt[t, b, at] = int(q[32 * b + r, n]) + 128
             for c in range(128):
                 if 128 * t + c < N:
                     st[t, b, c] = s[b, 128 * t + c]
-    return qt.reshape(-1), st.reshape(-1)
+    return qt.reshape(-1).view(np.int8), st.reshape(-1)
 
 
 @pytest.mark.parametrize("K,N", [(64, 40), (96, 300), (32, 128)])
