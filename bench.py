@@ -379,8 +379,8 @@ def run_ours(args, rank, world, local_rank):
     try:
         with open(PROFILE_TRAFFIC) as f:
             rec = json.load(f)
-        if rec.get("source_hash") == source_hash() and rec.get("m") == m:
-            traffic = rec.get("traffic_bytes_per_launch")
+        if rec.get("source_hash") == source_hash():
+            traffic = rec.get("by_m", {}).get(str(m), {}).get("traffic_bytes_per_launch")
     except (OSError, ValueError):
         pass
     n_layer_launches = len(chain.layer_calls())
@@ -422,6 +422,93 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------------------------------------------------
+# single launch shapes: the per-call sweep and the profiling case
+# ---------------------------------------------------------------------------------------------------------------------
+
+# One launch of each kind of the chain: (K, [N of each projection]) -- a multi-projection launch for q/k/v and gate/up.
+LAUNCHES = {"qkv": (HIDDEN, [HIDDEN] * 3), "o": (HIDDEN, [HIDDEN]), "gateup": (HIDDEN, [FFN] * 2),
+            "down": (FFN, [HIDDEN]), "head": (HIDDEN, [VOCAB])}
+# The single-GEMV workloads: the attention projection, the FFN projections and the ragged tensor-parallel shapes.
+SWEEP_SHAPES = [(4096, 4096), (4096, 14336), (14336, 4096), (5120, 40), (5120, 3000), (5120, 6144)]
+
+
+def _tiled_weights(K, Ns, copies, seed):
+    import synth_inputs as si
+    import q8_block_quantized_gemv_gb300 as q8
+    return [[q8.tile_device(*si.device_weight(K, N, seed + 10 * c + i), N) + (N,) for i, N in enumerate(Ns)]
+            for c in range(copies)]
+
+
+def run_profile_case(args):
+    """A few calls of one launch kind (tiled weights, constant-weights flag, as in the chain), for a profiler to
+    capture the fourth: `ncu ... -k regex:stream -s 3 -c 1 python bench.py --profile-case gateup --m 16`."""
+    import torch
+    import synth_inputs as si
+    import q8_block_quantized_gemv_gb300 as q8
+    from q8_block_quantized_gemv_gb300 import build
+    build.build()
+    K, Ns = LAUNCHES[args.profile_case]
+    w = _tiled_weights(K, Ns, 2, 21)[0]
+    x = si.device_activations(args.m, K, 3)
+    for _ in range(4):
+        if args.profile_case == "head":
+            q8.gemv_argmax(x, w[0][0], w[0][1], VOCAB, constant_weights=True, tiled=True)
+        else:
+            q8.gemv_parts(x, w, tiled=True, constant_weights=True)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_case, "m": args.m, "device_fault": q8.device_fault()}))
+
+
+def run_sweep(args):
+    """µs per call and GB/s of the single-GEMV workloads at each m: every call reads its own weight copy (copies
+    totalling over 4 x L2, so each call streams from HBM), calls back to back in a CUDA graph with the
+    constant-weights flag, CUDA events around 5 replays after 3 warm-up replays.  One JSON line per (shape, m)."""
+    import torch
+    import synth_inputs as si
+    import q8_block_quantized_gemv_gb300 as q8
+    from q8_block_quantized_gemv_gb300 import build
+    build.build()
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    ms = [int(v) for v in args.sweep_m.split(",")]
+    for K, N in SWEEP_SHAPES:
+        wb = K * padded(N) * 1.125
+        copies = max(2, int(4 * l2 // wb) + 1)
+        ws = _tiled_weights(K, [N], copies, 7)
+        for m in ms:
+            x = si.device_activations(m, K, 3)
+            y = torch.empty((m, padded(N)), dtype=torch.float32, device="cuda")
+            per = max(copies, 32)
+
+            def calls():
+                for i in range(per):
+                    qt, st, _ = ws[i % copies][0]
+                    q8.gemv(x, qt, st, N, y=y, tiled=True, constant_weights=True)
+            calls()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                calls()
+            for _ in range(3):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (5 * per)
+            gbs = gemv_bytes(m, K, N) / (us * 1e-6) / 1e9
+            print(json.dumps({"sweep": "single GEMV, tiled, back to back", "K": K, "N": N, "m": m,
+                              "us_per_call": us, "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak,
+                              "peak_kind": peak_kind, "pct_of_8TBps": 100.0 * gbs / 8000.0}), flush=True)
+            del g
+        del ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,6 +518,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the step: µs/call of the single-GEMV workloads, one JSON line each")
+    ap.add_argument("--sweep-m", default="1,2,4,8,16", help="row counts of --sweep")
+    ap.add_argument("--profile-case", choices=sorted(LAUNCHES),
+                    help="instead of the step: four calls of one launch kind of the step, for a profiler")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -441,6 +533,12 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.profile_case:
+        run_profile_case(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     if world > 1:
         import torch

@@ -23,6 +23,7 @@
 namespace q8 {
 
 constexpr int kBlock = 32;   // rows of a Q8_0 block
+constexpr int kMaxClusterRanks = 8;  // the largest K split across a cluster (the portable cluster size)
 constexpr int kWarps = 8;    // warps per CTA
 constexpr int kThreads = 32 * kWarps;
 
@@ -158,24 +159,29 @@ __device__ __forceinline__ void warp_blocks(const Args &a, int warp, int &b0, in
     b1 = c0 + (c1 - c0) * (warp + 1) / kWarps;
 }
 
-// Shared-memory bytes of the epilogue: NRED partial slabs of MR rows and TC columns, the CTA's sum, the row keys.
-__host__ __device__ constexpr int finish_smem_n(int NRED, int MR, int TC) { return (NRED * MR * TC + MR * TC) * 4 + MR * 8; }
+// Shared-memory bytes of the epilogue: NRED partial slabs of MR rows of RS floats (TC columns used), the CTA's sum,
+// the row keys.
+__host__ __device__ constexpr int finish_smem_n(int NRED, int MR, int TC, int RS = 0) {
+    return (NRED * MR * (RS ? RS : TC) + MR * TC) * 4 + MR * 8;
+}
 __host__ __device__ constexpr int finish_smem_bytes(int MR, int TC) { return finish_smem_n(kWarps, MR, TC); }
 
-// The epilogue.  On entry the CTA's NRED partial carries sit in red[NRED][MR][TC] (rows < MR, columns < TC of this
-// CTA's column tile `tile` of the output) and the CTA has synchronised.  Sums the slabs in order, then (ksplit > 1) the cluster's ranks in order,
-// writes y (0 in the pad columns) and folds this CTA's columns into the per-row arg-max keys.
-template <int NRED, int MR, int TC, int NTHREADS, bool ARGMAX>
+// The epilogue.  On entry the CTA's NRED partial carries sit in red[NRED][MR][RS] (rows < MR, columns < TC of this
+// CTA's column tile `tile` of the output; RS >= TC is the slab row stride) and the CTA has synchronised.  Sums the
+// slabs in order, then (ksplit > 1) the cluster's ranks in order, writes y (0 in the pad columns) and folds this
+// CTA's columns into the per-row arg-max keys.
+template <int NRED, int MR, int TC, int NTHREADS, bool ARGMAX, int RS = TC>
 __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
     namespace cg = cooperative_groups;
-    float *part = red + NRED * MR * TC;                                                   // [MR][TC]
+    float *part = red + NRED * MR * RS;                                                   // [MR][TC]
     unsigned long long *rowkey = reinterpret_cast<unsigned long long *>(part + MR * TC);  // [MR]
     const int rows = a.m < MR ? a.m : MR;
 
     for (int i = threadIdx.x; i < rows * TC; i += NTHREADS) {
+        const int at = (i / TC) * RS + i % TC;
         float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < NRED; ++w) v += red[w * MR * TC + i];
+        for (int w = 0; w < NRED; ++w) v += red[w * MR * RS + at];
         part[i] = v;
     }
     if (ARGMAX)
@@ -196,9 +202,16 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
         const int c = c0 + (i - r * width);
         float v;
         if (ks > 1) {
+            // every rank's value is requested before the first is added, then summed in rank order
             cg::cluster_group cluster = cg::this_cluster();
+            float pv[kMaxClusterRanks];
+#pragma unroll
+            for (int p = 0; p < kMaxClusterRanks; ++p)
+                pv[p] = p < ks ? cluster.map_shared_rank(part, p)[r * TC + c] : 0.0f;
             v = 0.0f;
-            for (int p = 0; p < ks; ++p) v += cluster.map_shared_rank(part, p)[r * TC + c];
+#pragma unroll
+            for (int p = 0; p < kMaxClusterRanks; ++p)
+                if (p < ks) v += pv[p];
         } else {
             v = part[r * TC + c];
         }

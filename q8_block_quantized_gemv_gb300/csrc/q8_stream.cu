@@ -49,6 +49,7 @@ constexpr int kStageS = kUnit + kUnitScales * 4;
 constexpr int kDepthS = 3;                   // ring stages per warp (two CTAs per SM)
 constexpr int kSmemS = kWarpsS * kDepthS * kStageS;
 constexpr int kSlices = kTmaColumns / 8;     // 8-column MMA slices of a tile
+constexpr int kSlabStride = kTmaColumns + 8; // epilogue slab row stride (floats)
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -390,18 +391,20 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();  // every warp is done with its ring: the shared memory holds the epilogue now
 
-    float *red = reinterpret_cast<float *>(smem_s);  // [kWarpsS][MR][128]
-    float *mine = red + warp * MR * kTmaColumns;
+    // [kWarpsS][MR][kSlabStride]: rows padded by 8 floats, so that a half-warp's 8-byte stores (rows g, columns
+    // 8j + 2t) fall on 32 distinct banks
+    float *red = reinterpret_cast<float *>(smem_s);
+    float *mine = red + warp * MR * kSlabStride;
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
         for (int j = 0; j < kSlices; ++j) {
             float lo, hi;
             unpack_f32x2(acc[r][j], lo, hi);
-            *reinterpret_cast<float2 *>(mine + (g + 8 * r) * kTmaColumns + 8 * j + 2 * t) = make_float2(lo, hi);
+            *reinterpret_cast<float2 *>(mine + (g + 8 * r) * kSlabStride + 8 * j + 2 * t) = make_float2(lo, hi);
         }
     __syncthreads();
-    finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
+    finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, ARGMAX, kSlabStride>(a, red, tile);
 }
 
 // m <= 2 on CUDA cores: in segment (s, h) lane (g, t) holds words w = 0..3, each four weight rows 16s + 4t + 0..3 of
@@ -544,7 +547,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     finish_n<kWarpsS, M, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
 }
 
-static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns) <= kSmemS, "the epilogue fits in the rings");
+static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns, kSlabStride) <= kSmemS, "the epilogue fits in the rings");
 static_assert(2 * kSmemS <= 227 * 1024, "two CTAs per SM");
 
 template <typename Kernel>
