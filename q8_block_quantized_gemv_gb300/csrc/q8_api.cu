@@ -65,13 +65,20 @@ Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long
     if (tiled) {
         // The tiled layout: per-warp cp.async streams, 128-column tiles.  Measured on GB300, the best K split is
         // the largest one whose CTAs still fit in one wave of resident CTAs (a second, partial wave and the cluster
-        // reduction both cost more than the idle SMs of a short wave): ks = resident slots / tiles, at least 1.
+        // reduction both cost more than the idle SMs of a short wave): ks = resident slots / tiles, at least 1,
+        // lowered while the tiles' clusters of ks CTAs would not all be resident at once (a cluster's CTAs share
+        // one GPC, so fewer clusters fit than slots / ks).
         const long long tiles = tiled_tiles > 0 ? tiled_tiles : (Np + q8::kTmaColumns - 1) / q8::kTmaColumns;
         const long long slots = (long long)q8::stream_ctas_per_sm(m) * sms;
         long long ks = slots / tiles;
         if (ks > 8) ks = 8;
         if (ks > nb) ks = nb;
         if (ks < 1) ks = 1;
+        while (ks > 1) {
+            const int fit = q8::stream_max_clusters((int)ks);
+            if (fit <= 0 || tiles <= fit) break;
+            --ks;
+        }
         int best = (int)ks;
         const char *force = getenv("Q8_KSPLIT");
         if (force) {

@@ -35,6 +35,8 @@
 // Activations are read from L2 (ld.global.cg), two blocks ahead.  With programmatic dependent launch every thread
 // waits for the previous kernel (griddepcontrol.wait) before it reads x or writes y; with Q8_FLAG_CONSTANT_WEIGHTS
 // the first two stages' weights are already requested before that wait.
+#include <atomic>
+
 #include "q8_launch.h"
 
 namespace q8 {
@@ -584,6 +586,41 @@ cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, 
 }  // namespace
 
 int stream_ctas_per_sm(int) { return 2; }
+
+int stream_max_clusters(int ks) {
+    // Clusters of ks CTAs are placed within one GPC, so fewer of them fit at once than slots / ks.  Asked once per
+    // device and size (a deterministic answer: concurrent first calls store the same value); every stream kernel has
+    // the same block size, registers and shared memory.
+    static std::atomic<int> cache[64][9];  // 0: not asked yet; else the count + 1
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > 8) return 0;
+    const int known = cache[dev][ks].load(std::memory_order_relaxed);
+    if (known > 0) return known - 1;
+    auto kernel = stream_kernel<true, false>;
+    int n = 0;
+    bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS) == cudaSuccess &&
+              cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+    if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, (unsigned)ks, 1);
+        cfg.blockDim = dim3(kThreadsS, 1, 1);
+        cfg.dynamicSmemBytes = kSmemS;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)ks;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = ks > 1 ? 1 : 0;
+        ok = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess;
+    }
+    if (!ok) {
+        cudaGetLastError();  // the failed query's error is not the caller's
+        return 0;
+    }
+    cache[dev][ks].store(n + 1, std::memory_order_relaxed);
+    return n;
+}
 
 cudaError_t launch_stream(const Args &a, const Parts &pt, bool argmax, cudaStream_t stream, bool pdl,
                           bool prefetch_weights) {
