@@ -16,6 +16,9 @@ Contents, each citing the passage it follows (page titles as printed on the page
 * :func:`repack` -- ``from_q8.rs`` ``Q8Part`` (the host repacks the checkpoint's blocks into the int8 values and the
   fp32 scales); the block layout is the reading stated in the design notes (36-byte blocks, fp32 scale first).
 * :func:`dequantize` -- ``from_q8.rs`` module doc, w = q * d.
+* :func:`glu` -- ``plan.rs`` ``Launch::GemvGlu``: two projections of one activation through a gate,
+  out = act(x.wg + bg) * (x.wu + bu), SwiGLU when ``act`` is none; here without biases, so
+  out = silu(g) * u with g = x.Wg, u = x.Wu (each as :func:`gemv`) and silu(g) = g / (1 + exp(-g)), in fp64.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` to facts the pages and the mathematics fix (brute
 force in exact rational arithmetic, closed forms, a dense fp64 matmul of the dequantized weight, the quantize
@@ -181,3 +184,21 @@ def repack(blocks: bytes | np.ndarray, K: int, N: int):
     q[:, :N] = vals.reshape(N, K).T      # column n's blocks b = 0, 1, ... are its rows 32b .. 32b + 31
     s[:, :N] = d.T
     return q, s
+
+
+def silu(g: np.ndarray) -> np.ndarray:
+    """The SiLU of SwiGLU (``plan.rs`` ``Launch::GemvGlu``): g * sigmoid(g) = g / (1 + exp(-g)), in fp64; exp(-g)
+    overflows to inf for g below about -709, giving -0 or +0 as the limit does."""
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def glu(x_bits: np.ndarray, qg: np.ndarray, sg: np.ndarray, qu: np.ndarray, su: np.ndarray, cols=None):
+    """The gated pair of ``plan.rs`` ``Launch::GemvGlu`` (SwiGLU, no biases): out = silu(x.Wg) * (x.Wu), fp64.
+
+    Returns (out, g, u, a_g, a_u): the two products and their error scales as :func:`gemv` returns them, for the
+    bound a GPU result is judged by."""
+    g, a_g = gemv(x_bits, qg, sg, cols)
+    u, a_u = gemv(x_bits, qu, su, cols)
+    return silu(g) * u, g, u, a_g, a_u

@@ -9,7 +9,10 @@ of q or s, a wrong bf16 decode, a wrong abs in the error scale) fails at least o
 * closed forms from ``tests/golden/closed_forms.txt`` and one-hot activations;
 * the exactness of every int8 x bf16 product in fp32 (from_q8.rs module doc);
 * the Q8_0 quantize rule and its round trip (from_q8.rs ``quantize``);
-* the arg-max's first-maximum rule (int8_model.rs ``decode_step_lg`` and the tie rule of ``reference_cuda``).
+* the arg-max's first-maximum rule (int8_model.rs ``decode_step_lg`` and the tie rule of ``reference_cuda``);
+* the gated pair (plan.rs ``Launch::GemvGlu``, SwiGLU): the identities silu(g) - silu(-g) = g and
+  silu(g) + silu(-g) = g tanh(g/2), which together fix silu(g) = g sigmoid(g), and exact g, u against SiLU evaluated
+  in 40-digit decimal arithmetic.
 """
 import os
 import struct
@@ -358,3 +361,65 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
                         abs(Fraction(a[r, n]) - ea) > Fraction(2) ** -52 * ea:
                     caught = True
     assert caught, f"the brute-force pin did not catch: {name}"
+# --------------------------------------------------------------------------------------------------------------------
+# the gated pair (SwiGLU)
+# --------------------------------------------------------------------------------------------------------------------
+
+def test_glu_odd_and_even_parts_fix_silu():
+    """With the gate's weight negated (g -> -g exactly, by the product's sign symmetry):
+    glu(Wg) - glu(-Wg) = (silu(g) - silu(-g)) u = g u and glu(Wg) + glu(-Wg) = g tanh(g/2) u (math.tanh), the odd and
+    even parts of g sigmoid(g) -- a swapped sign in the exponent or a missing factor fails one of them."""
+    import math
+    x, qg, sg = si.case(3, 256, 70, 611)
+    _, qu, su = si.case(3, 256, 70, 612)
+    out, g, u, _, _ = oracle.glu(x, qg, sg, qu, su)
+    out_n, g_n, _, _, _ = oracle.glu(x, -qg, sg, qu, su)
+    assert np.array_equal(g_n, -g)
+    odd = out - out_n
+    even = out + out_n
+    tanh = np.vectorize(math.tanh)(g / 2.0)
+    scale = np.abs(g * u) + 1e-300
+    assert np.all(np.abs(odd - g * u) <= 1e-14 * scale)
+    assert np.all(np.abs(even - g * tanh * u) <= 1e-14 * scale)
+
+
+@pytest.mark.parametrize("wrong", ["exp_sign", "no_gate", "sigmoid_only"])
+def test_glu_pins_catch_planted_mistakes(wrong, monkeypatch):
+    """A wrong SiLU planted in the oracle fails the pins: exp(+g) for exp(-g), silu = g, silu = sigmoid(g)."""
+    bad = {"exp_sign": lambda g: g / (1.0 + np.exp(np.asarray(g, dtype=np.float64))),
+           "no_gate": lambda g: np.asarray(g, dtype=np.float64),
+           "sigmoid_only": lambda g: 1.0 / (1.0 + np.exp(-np.asarray(g, dtype=np.float64)))}[wrong]
+    monkeypatch.setattr(oracle, "silu", bad)
+    failed = 0
+    for pin in (test_glu_odd_and_even_parts_fix_silu, lambda: test_glu_exact_inputs_against_decimal_silu(100, 5)):
+        try:
+            with np.errstate(over="ignore"):
+                pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1
+
+
+@pytest.mark.parametrize("c,e", [(1, 0), (-1, 0), (100, 5), (-100, 5), (127, 2), (-127, 2), (3, 9), (0, 0)])
+def test_glu_exact_inputs_against_decimal_silu(c, e):
+    """One-hot activation: g = c 2^-e and u = 1/2 exactly (s = 2^-e with q = c; s = 2^-8 with q = 128 is not int8,
+    so u = 64 * 2^-7); out = silu(g) / 2 against g / (1 + exp(-g)) in 40-digit decimal arithmetic."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 40
+    K, N = 32, 1
+    x = np.zeros((1, K), dtype=np.uint16)
+    x[0, 5] = _bf16(1.0)
+    qg = np.zeros((K, 32), dtype=np.int8)
+    qu = np.zeros((K, 32), dtype=np.int8)
+    qg[5, 0], qu[5, 0] = c, 64
+    sg = np.zeros((1, 32), dtype=np.float32)
+    su = np.zeros((1, 32), dtype=np.float32)
+    sg[0, 0], su[0, 0] = 2.0 ** -e, 2.0 ** -7
+    out, g, u, _, _ = oracle.glu(x, qg, sg, qu, su)
+    gd = Decimal(c) / (Decimal(2) ** e)
+    ref = gd / (1 + (-gd).exp()) / 2
+    assert g[0, 0] == float(gd) and u[0, 0] == 0.5
+    assert abs(Decimal(float(out[0, 0])) - ref) <= Decimal(2) ** -52 * (abs(ref) + Decimal(10) ** -300)
+    assert np.all(out[0, 1:] == 0.0)
+
+
