@@ -40,6 +40,8 @@ WORKLOAD = (f"decode-step Q8_0 projection chain: {LAYERS} layers x (q,k,v,o 4096
             f"down 14336x4096) + tied head 4096x128256 with fused arg-max; per layer q/k/v share one activation and "
             f"gate/up another (one multi-projection launch each), o and down their own")
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+GLU_NOTE = ("; --ffn glu: gate and up as one gated-pair launch (q8_gemv_glu, SwiGLU) writing bf16 silu(gate) * up, "
+            "which the down projection reads")
 
 
 def layer_shapes():
@@ -221,10 +223,10 @@ class Chain:
     o its own, gate and up one more (one q8_gemv_parts launch), down its own; then the tied head with its arg-max.
     Weights are stored tiled (q8_tile_device), as a model would store them once at load time."""
 
-    def __init__(self, torch, m, seed=4000):
+    def __init__(self, torch, m, seed=4000, glu=False):
         import synth_inputs as si
         import q8_block_quantized_gemv_gb300 as q8
-        self.torch, self.m = torch, m
+        self.torch, self.m, self.glu = torch, m, glu
         self.shapes = chain_shapes()
         # row-major weights as drawn, and the tiled storage the library streams
         self.w = [si.device_weight(K, N, seed + i) for i, (K, N) in enumerate(self.shapes)]
@@ -243,6 +245,8 @@ class Chain:
             self.x.append(self.x_all[off:off + m * K].view(m, K))
             off += m * K
         self.y = [torch.empty((m, padded(N)), dtype=torch.float32, device="cuda") for _, N in self.shapes]
+        # gated-pair FFN: the gate/up launch writes silu(gate) * up as bf16, which the down projection reads
+        self.h = torch.empty((m, padded(FFN)), dtype=torch.bfloat16, device="cuda") if glu else None
         self.idx = torch.empty((m,), dtype=torch.int64, device="cuda")
         self.g_layers = self.g_head = None
         torch.cuda.synchronize()
@@ -259,8 +263,15 @@ class Chain:
     def run_layers(self):
         import q8_block_quantized_gemv_gb300 as q8
         for xi, gis in self.layer_calls():
-            q8.gemv_parts(self.x[xi], [(self.wt[i][0], self.wt[i][1], self.shapes[i][1]) for i in gis],
-                          ys=[self.y[i] for i in gis], constant_weights=True, tiled=True)
+            if self.glu and len(gis) == 2:  # gate, up -> h
+                q8.gemv_glu(self.x[xi], self.wt[gis[0]], self.wt[gis[1]], FFN, out_bf16=self.h, want=(),
+                            constant_weights=True)
+            elif self.glu and self.shapes[gis[0]] == (FFN, HIDDEN):  # down reads h
+                q8.gemv_parts(self.h, [(self.wt[gis[0]][0], self.wt[gis[0]][1], HIDDEN)], ys=[self.y[gis[0]]],
+                              constant_weights=True, tiled=True)
+            else:
+                q8.gemv_parts(self.x[xi], [(self.wt[i][0], self.wt[i][1], self.shapes[i][1]) for i in gis],
+                              ys=[self.y[i] for i in gis], constant_weights=True, tiled=True)
 
     def run_head(self):
         import q8_block_quantized_gemv_gb300 as q8
@@ -295,6 +306,8 @@ class Chain:
             for i in gis:
                 K, N = self.shapes[i]
                 total += K * padded(N) * 1.125 + m * padded(N) * 4
+            if self.glu and len(gis) == 2:  # one bf16 output instead of two fp32 ones
+                total -= 2 * m * padded(FFN) * 4 - m * padded(FFN) * 2
         return total
 
 
@@ -305,7 +318,7 @@ def run_ours(args, rank, world, local_rank):
     build.build()
     torch.cuda.set_device(local_rank)
     m = args.m
-    chain = Chain(torch, m)
+    chain = Chain(torch, m, glu=args.ffn == "glu")
     chain.capture()
     stream = torch.cuda.current_stream()
 
@@ -389,7 +402,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "m": m, "gemvs_per_step": len(chain.shapes) + 1,
+        "config": {"workload": WORKLOAD if args.ffn == "parts" else WORKLOAD + GLU_NOTE, "m": m,
+                   "gemvs_per_step": len(chain.shapes) + 1,
                    "launches_per_step": chain.launches_per_step(),
                    "bytes_per_step": bytes_step, "us_per_gemv": ms * 1e3 / (len(chain.shapes) + 1),
                    "pct_of_8TBps": 100.0 * bytes_step / (ms * 1e-3) / 8e12,
@@ -518,6 +532,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--ffn", choices=["parts", "glu"], default="parts",
+                    help="the layers' gate/up launch: two fp32 outputs (default) or the fused gated pair")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step: µs/call of the single-GEMV workloads, one JSON line each")
     ap.add_argument("--sweep-m", default="1,2,4,8,16", help="row counts of --sweep")

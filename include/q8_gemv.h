@@ -125,6 +125,24 @@ q8_status q8_tile(const int8_t *q, const float *s, int K, int N, int8_t *qt, flo
  * the input and output must not overlap). */
 q8_status q8_tile_device(const int8_t *q, const float *s, int K, int N, int8_t *qt, float *st, q8_stream_t stream);
 
+/* The gated pair ("plan.rs", `Launch::GemvGlu`: two projections of one activation through a gate,
+ * out = act(x.wg + bg) * (x.wu + bu), SwiGLU when act is none; here without biases):
+ *     out[r, n] = silu(g[r, n]) * u[r, n],   g = x . Wg,  u = x . Wu,   silu(g) = g / (1 + exp(-g)),
+ * g and u each the Q8_0 product of q8_gemv (fp32 accumulation), silu and the product in fp32 (CUDA's expf, IEEE
+ * division).  One launch: the gate's and the up projection's CTAs of a column tile run side by side in a cluster.
+ *   x         device, bf16 [m][K], 16-byte aligned
+ *   qg, sg    device, the gate's weight in the tiled storage (q8_tile), 16-byte aligned
+ *   qu, su    device, the up projection's weight, tiled, 16-byte aligned
+ *   out       device, fp32 [m][Np] (written; pad columns 0), 16-byte aligned, or NULL
+ *   out_bf16  device, bf16 [m][Np] (written: out rounded to nearest even; pads 0), 16-byte aligned, or NULL
+ *             -- a down projection's activation as q8_gemv takes it (row pitch Np)
+ *   flags     Q8_FLAG_TILED (required) | Q8_FLAG_CONSTANT_WEIGHTS
+ * Errors: Q8_ERR_ARG (null inputs, both outputs null, flags without Q8_FLAG_TILED or with unknown bits, an output
+ * overlapping an input or the other output), Q8_ERR_SHAPE, Q8_ERR_ALIGN, Q8_ERR_CUDA; nothing is launched on an
+ * error.  inf and NaN propagate as IEEE arithmetic does (silu(-inf) = -inf / inf = NaN). */
+q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const int8_t *qu, const float *su, float *out,
+                      void *out_bf16, int m, int K, int N, unsigned int flags, q8_stream_t stream);
+
 /* One weight of a multi-projection call: its Q8_0 values and scales (row-major, or tiled with Q8_FLAG_TILED), its
  * output y [m][q8_padded_n(N)] (written) and its N. */
 typedef struct q8_part {

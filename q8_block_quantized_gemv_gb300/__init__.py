@@ -46,6 +46,7 @@ SIGNATURES = {
     "q8_version": (_I, []),
     "q8_device_fault": (_I, [_P, _I]),
     "q8_gemv_parts": (_I, [_P, _P, _I, _I, _I, ctypes.c_uint, _P]),
+    "q8_gemv_glu": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
 }
 
 
@@ -222,6 +223,31 @@ def gemv_parts(x, weights, ys=None, constant_weights: bool = False, tiled: bool 
     _check(lib().q8_gemv_parts(x.data_ptr(), ctypes.cast(arr, ctypes.c_void_p), len(weights), m, K,
                                _flags(constant_weights, tiled), _stream_handle(stream)), "q8_gemv_parts")
     return outs
+
+
+def gemv_glu(x, gate, up, N: int, out=None, out_bf16=None, want=("f32",), constant_weights: bool = False,
+             stream=None):
+    """The gated pair (q8_gemv_glu, SwiGLU): silu(x.Wg) * (x.Wu) with both weights tiled; gate and up are (q, s).
+
+    ``want``: which outputs to allocate when not given -- "f32" (fp32 [m, Np]) and/or "bf16" (bf16 [m, Np]).
+    Returns (out, out_bf16), either None when not requested."""
+    import torch
+    m, K, Np = _check_operands(x, gate[0], gate[1], N, True)
+    _check_operands(x, up[0], up[1], N, True)
+    if out is None and "f32" in want:
+        out = torch.empty((m, Np), dtype=torch.float32, device=x.device)
+    if out_bf16 is None and "bf16" in want:
+        out_bf16 = torch.empty((m, Np), dtype=torch.bfloat16, device=x.device)
+    if out is not None and (out.dtype != torch.float32 or out.shape != (m, Np) or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous fp32 CUDA tensor [m, Np]")
+    if out_bf16 is not None and (out_bf16.dtype != torch.bfloat16 or out_bf16.shape != (m, Np)
+                                 or not out_bf16.is_contiguous()):
+        raise ValueError("out_bf16 must be a contiguous bf16 CUDA tensor [m, Np]")
+    _check(lib().q8_gemv_glu(x.data_ptr(), gate[0].data_ptr(), gate[1].data_ptr(), up[0].data_ptr(),
+                             up[1].data_ptr(), out.data_ptr() if out is not None else None,
+                             out_bf16.data_ptr() if out_bf16 is not None else None, m, K, N,
+                             _flags(constant_weights, True), _stream_handle(stream)), "q8_gemv_glu")
+    return out, out_bf16
 
 
 def device_fault(clear: bool = False) -> int:

@@ -143,6 +143,7 @@ int tiles_of(int N) { return (N + q8::kTmaColumns - 1) / q8::kTmaColumns; }
 
 q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStream_t stream,
               const q8::Parts *parts = nullptr) {
+    const int epi = argmax ? q8::kEpiArgmax : q8::kEpiStore;
     int sms = 0;
     int e = sm_count(&sms);
     if (e != 0) return cuda_fail((cudaError_t)e);
@@ -161,7 +162,7 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
     Args b = a;
     b.ksplit = p.ksplit;
     const bool prefetch = (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0;
-    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, argmax, stream, true, prefetch)
+    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, epi, stream, true, prefetch)
                      : p.variant == Q8_VARIANT_TMA  ? q8::launch_tma(b, argmax, stream, true, prefetch)
                      : p.variant == Q8_VARIANT_SIMT ? q8::launch_simt(b, p.V, argmax, stream)
                                                     : q8::launch_mma(b, p.V, argmax, stream);
@@ -293,6 +294,74 @@ extern "C" q8_status q8_gemv_parts(const void *x, const q8_part *parts, int npar
     Args a = {static_cast<const uint16_t *>(x), parts[0].q, parts[0].s, parts[0].y, nullptr, m, K, parts[0].N,
               q8_padded_n(parts[0].N), K / Q8_BLOCK, 1};
     return run(a, Q8_VARIANT_AUTO, flags, false, cs, &pt);
+}
+
+// The K split of a gated-pair launch: its clusters are (2, ks), a gate's and an up projection's CTA for each K range
+// of one column tile, so the one-wave rule counts 2 * tiles * ks CTAs and clusters of 2 * ks (at most 8).
+int plan_glu(long long tiles, int nb, int sms) {
+    const long long slots = (long long)q8::stream_ctas_per_sm(1) * sms;
+    long long ks = slots / (2 * tiles);
+    if (ks > 4) ks = 4;
+    if (ks > nb) ks = nb;
+    if (ks < 1) ks = 1;
+    while (ks > 1) {
+        const int fit = q8::stream_max_clusters((int)(2 * ks));
+        if (fit <= 0 || tiles <= fit) break;
+        --ks;
+    }
+    const char *force = getenv("Q8_KSPLIT");
+    if (force) {
+        const int f = atoi(force);
+        if (f >= 1 && f <= 4 && f <= nb) ks = f;
+    }
+    return (int)ks;
+}
+
+extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const int8_t *qu,
+                                 const float *su, float *out, void *out_bf16, int m, int K, int N, unsigned int flags,
+                                 q8_stream_t stream) {
+    q8_status st = check_gemv_args(x, qg, sg, m, K, N);
+    if (st != Q8_OK) return st;
+    st = check_gemv_args(x, qu, su, m, K, N);
+    if (st != Q8_OK) return st;
+    if (!out && !out_bf16) return Q8_ERR_ARG;
+    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if (!(flags & Q8_FLAG_TILED)) return Q8_ERR_ARG;  // the gated pair runs on the tiled storage only
+    if (q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
+    if ((out && !aligned(out, 16)) || (out_bf16 && !aligned(out_bf16, 16))) return Q8_ERR_ALIGN;
+    const int Np = q8_padded_n(N);
+    const size_t wcols = (size_t)q8_tiled_n(N);
+    const size_t obytes[2] = {(size_t)m * Np * 4, (size_t)m * Np * 2};
+    const void *outs[2] = {out, out_bf16};
+    for (int o = 0; o < 2; ++o) {
+        if (!outs[o]) continue;
+        if (overlaps(outs[o], obytes[o], x, (size_t)m * K * 2) ||
+            overlaps(outs[o], obytes[o], qg, (size_t)K * wcols) || overlaps(outs[o], obytes[o], qu, (size_t)K * wcols) ||
+            overlaps(outs[o], obytes[o], sg, (size_t)(K / Q8_BLOCK) * wcols * 4) ||
+            overlaps(outs[o], obytes[o], su, (size_t)(K / Q8_BLOCK) * wcols * 4))
+            return Q8_ERR_ARG;
+    }
+    if (out && out_bf16 && overlaps(out, obytes[0], out_bf16, obytes[1])) return Q8_ERR_ARG;
+    int sms = 0;
+    int e = sm_count(&sms);
+    if (e != 0) return cuda_fail((cudaError_t)e);
+    const int tiles = tiles_of(N);
+    q8::Parts pt = {};
+    pt.q[0] = qg;
+    pt.s[0] = sg;
+    pt.q[1] = qu;
+    pt.s[1] = su;
+    pt.N[0] = pt.N[1] = N;
+    pt.tile_end[0] = tiles;
+    pt.tile_end[1] = 2 * tiles;  // grid x: the two parts' CTAs of each tile side by side
+    pt.count = 2;
+    Args a = {static_cast<const uint16_t *>(x), qg, sg, out, nullptr, m, K, N, Np, K / Q8_BLOCK, 1,
+              static_cast<uint16_t *>(out_bf16)};
+    a.ksplit = plan_glu(tiles, K / Q8_BLOCK, sms);
+    cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true,
+                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    return Q8_OK;
 }
 
 extern "C" q8_status q8_device_fault(unsigned int *fault, int clear) {

@@ -31,10 +31,11 @@ struct Args {
     const uint16_t *x;         // bf16 bit patterns [m][K]
     const int8_t *q;           // [K][Np]
     const float *s;            // [K/32][Np]
-    float *y;                  // [m][Np], or null (arg-max without logits)
+    float *y;                  // [m][Np], or null (arg-max without logits; gated pair with only a bf16 output)
     unsigned long long *keys;  // [m] packed arg-max keys, or null
     int m, K, N, Np, nb;       // nb = K / 32
     int ksplit;                // CTAs of a cluster splitting K (grid.y)
+    uint16_t *ybf;             // gated pair: bf16 [m][Np] copy of the output, or null
 };
 
 // Several weights that multiply one activation in one launch ("plan.rs", `Launch::GemmParts`: projections of one
@@ -64,6 +65,20 @@ __device__ __forceinline__ int select_part(const Parts &pt, int tile, Args &a) {
     a.N = pt.N[p];
     a.Np = (pt.N[p] + kBlock - 1) / kBlock * kBlock;
     return tile - first;
+}
+
+// What a launch's epilogue does with the product.
+constexpr int kEpiStore = 0;   // write y
+constexpr int kEpiArgmax = 1;  // write y (if any) and fold the row arg-max keys
+constexpr int kEpiGlu = 2;     // gated pair: part 0 is the gate, part 1 the up projection; write silu(g) * u
+
+// A gated-pair launch interleaves the two weights' CTAs: grid x = 2 * tile + part, clusters of 2 along x (the
+// gate's and the up projection's CTAs of one tile and K range side by side).  `a` gets the part's q and s.
+__device__ __forceinline__ int select_glu(const Parts &pt, Args &a) {
+    const int p = blockIdx.x & 1;
+    a.q = pt.q[p];
+    a.s = pt.s[p];
+    return blockIdx.x >> 1;
 }
 
 // ------------------------------------------------------------------------------------------------------------------
@@ -202,16 +217,9 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
         const int c = c0 + (i - r * width);
         float v;
         if (ks > 1) {
-            // every rank's value is requested before the first is added, then summed in rank order
             cg::cluster_group cluster = cg::this_cluster();
-            float pv[kMaxClusterRanks];
-#pragma unroll
-            for (int p = 0; p < kMaxClusterRanks; ++p)
-                pv[p] = p < ks ? cluster.map_shared_rank(part, p)[r * TC + c] : 0.0f;
             v = 0.0f;
-#pragma unroll
-            for (int p = 0; p < kMaxClusterRanks; ++p)
-                if (p < ks) v += pv[p];
+            for (int p = 0; p < ks; ++p) v += cluster.map_shared_rank(part, p)[r * TC + c];  // rank order
         } else {
             v = part[r * TC + c];
         }
@@ -228,6 +236,50 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
             if (rowkey[r]) atomicMax(&a.keys[r], rowkey[r]);
     }
     if (ks > 1) cg::this_cluster().sync();  // keep this CTA's shared memory alive until every rank has read it
+}
+
+// The gated pair's epilogue ("plan.rs", `Launch::GemvGlu`, SwiGLU: out = silu(x.wg) * (x.wu), silu(g) = g / (1 +
+// exp(-g))).  The cluster is (2, ks): rank p + 2k holds part p's sums over K range k.  Each rank first sums its
+// column slice over its part's K ranges (rank order), then the gate's rank of a slice reads the up projection's sums
+// of the same slice and writes silu(g) * u (0 in the pad columns) to y and/or its bf16 copy.
+template <int NRED, int MR, int TC, int NTHREADS, int RS = TC>
+__device__ __forceinline__ void finish_glu(const Args &a, float *red, int tile) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    float *part = red + NRED * MR * RS;  // [MR][TC]: this CTA's sums over its K range
+    float *mine = part + MR * TC;        // [MR][width]: this rank's slice summed over its part's K ranges
+    const int rows = a.m < MR ? a.m : MR;
+    for (int i = threadIdx.x; i < rows * TC; i += NTHREADS) {
+        const int at = (i / TC) * RS + i % TC;
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NRED; ++w) v += red[w * MR * RS + at];
+        part[i] = v;
+    }
+    cluster.sync();
+    const int ks = a.ksplit, p = blockIdx.x & 1, k = blockIdx.y;
+    const int c0 = TC * k / ks, c1 = TC * (k + 1) / ks, width = c1 - c0;
+    for (int i = threadIdx.x; i < rows * width; i += NTHREADS) {
+        const int r = i / width, c = c0 + (i - r * width);
+        float v = 0.0f;
+        for (int j = 0; j < ks; ++j) v += cluster.map_shared_rank(part, p + 2 * j)[r * TC + c];  // rank order
+        mine[i] = v;
+    }
+    cluster.sync();
+    if (p == 0) {
+        const float *up = cluster.map_shared_rank(mine, 1 + 2 * k);
+        for (int i = threadIdx.x; i < rows * width; i += NTHREADS) {
+            const int r = i / width, c = c0 + (i - r * width);
+            const int n = tile * TC + c;
+            if (n < a.Np) {
+                const float g = mine[i];
+                const float o = n < a.N ? g / (1.0f + expf(-g)) * up[i] : 0.0f;
+                if (a.y) a.y[(size_t)r * a.Np + n] = o;
+                if (a.ybf) a.ybf[(size_t)r * a.Np + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+            }
+        }
+    }
+    cluster.sync();  // the up projection's rank keeps its shared memory until the gate's rank has read it
 }
 
 template <int MR, int TC, bool ARGMAX>

@@ -48,7 +48,8 @@ cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl
 // Defined in q8_stream.cu (the tiled layout).
 int stream_ctas_per_sm(int m);
 int stream_max_clusters(int ks);  // clusters of ks stream-kernel CTAs resident at once on this device (0: unknown)
-cudaError_t launch_stream(const Args &a, const Parts &parts, bool argmax, cudaStream_t stream, bool pdl,
+// epi: kEpiStore, kEpiArgmax or kEpiGlu (parts 0 and 1 the gate and up weights, grid x = 2 * tiles).
+cudaError_t launch_stream(const Args &a, const Parts &parts, int epi, cudaStream_t stream, bool pdl,
                           bool prefetch_weights);
 cudaError_t read_fault_word(unsigned *out, bool clear);
 constexpr int kTmaColumns = 128;

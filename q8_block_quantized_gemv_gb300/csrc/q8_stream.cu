@@ -286,7 +286,7 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
     }
 }
 
-template <bool ROWS16, bool ARGMAX>
+template <bool ROWS16, int EPI>
 __global__ void __launch_bounds__(kThreadsS, 2)
     stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     constexpr int MR = ROWS16 ? 16 : 8;
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int tile = select_part(parts, blockIdx.x, a);
+    const int tile = EPI == kEpiGlu ? select_glu(parts, a) : select_part(parts, blockIdx.x, a);
     const int rank = blockIdx.y;
     const int c0 = (int)((long long)a.nb * rank / a.ksplit);
     const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
@@ -406,7 +406,10 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             *reinterpret_cast<float2 *>(mine + (g + 8 * r) * kSlabStride + 8 * j + 2 * t) = make_float2(lo, hi);
         }
     __syncthreads();
-    finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, ARGMAX, kSlabStride>(a, red, tile);
+    if constexpr (EPI == kEpiGlu)
+        finish_glu<kWarpsS, MR, kTmaColumns, kThreadsS, kSlabStride>(a, red, tile);
+    else
+        finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, EPI == kEpiArgmax, kSlabStride>(a, red, tile);
 }
 
 // m <= 2 on CUDA cores: in segment (s, h) lane (g, t) holds words w = 0..3, each four weight rows 16s + 4t + 0..3 of
@@ -424,13 +427,13 @@ template <int E> __device__ __forceinline__ unsigned long long q8x2_to_f32x2(uin
     return d;
 }
 
-template <int M, bool ARGMAX>
+template <int M, int EPI>
 __global__ void __launch_bounds__(kThreadsS, 2)
     stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int tile = select_part(parts, blockIdx.x, a);
+    const int tile = EPI == kEpiGlu ? select_glu(parts, a) : select_part(parts, blockIdx.x, a);
     const int rank = blockIdx.y;
     const int c0 = (int)((long long)a.nb * rank / a.ksplit);
     const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
@@ -546,15 +549,19 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             if (t == 0) mine[r * kTmaColumns + 8 * j + g] = v;
         }
     __syncthreads();
-    finish_n<kWarpsS, M, kTmaColumns, kThreadsS, ARGMAX>(a, red, tile);
+    if constexpr (EPI == kEpiGlu)
+        finish_glu<kWarpsS, M, kTmaColumns, kThreadsS>(a, red, tile);
+    else
+        finish_n<kWarpsS, M, kTmaColumns, kThreadsS, EPI == kEpiArgmax>(a, red, tile);
 }
 
 static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns, kSlabStride) <= kSmemS, "the epilogue fits in the rings");
+static_assert((kWarpsS * 16 * kSlabStride + 2 * 16 * kTmaColumns) * 4 <= kSmemS, "the gated pair's epilogue fits");
 static_assert(2 * kSmemS <= 227 * 1024, "two CTAs per SM");
 
 template <typename Kernel>
 cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, cudaStream_t stream, bool pdl,
-                                 bool prefetch) {
+                                 bool prefetch, bool pair) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -566,9 +573,9 @@ cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, 
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (a.ksplit > 1) {
+    if (a.ksplit > 1 || pair) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.x = pair ? 2 : 1;
         attr[na].val.clusterDim.y = (unsigned)a.ksplit;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -622,20 +629,23 @@ int stream_max_clusters(int ks) {
     return n;
 }
 
-cudaError_t launch_stream(const Args &a, const Parts &pt, bool argmax, cudaStream_t stream, bool pdl,
+template <int EPI>
+cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, bool p) {
+    const bool pair = EPI == kEpiGlu;
+    if (a.m == 1) return launch_stream_kernel(stream_simt_kernel<1, EPI>, a, pt, stream, pdl, p, pair);
+    if (a.m == 2) return launch_stream_kernel(stream_simt_kernel<2, EPI>, a, pt, stream, pdl, p, pair);
+    if (a.m <= 8) return launch_stream_kernel(stream_kernel<false, EPI>, a, pt, stream, pdl, p, pair);
+    return launch_stream_kernel(stream_kernel<true, EPI>, a, pt, stream, pdl, p, pair);
+}
+
+cudaError_t launch_stream(const Args &a, const Parts &pt, int epi, cudaStream_t stream, bool pdl,
                           bool prefetch_weights) {
-    const bool p = prefetch_weights;
-    if (a.m == 1)
-        return argmax ? launch_stream_kernel(stream_simt_kernel<1, true>, a, pt, stream, pdl, p)
-                      : launch_stream_kernel(stream_simt_kernel<1, false>, a, pt, stream, pdl, p);
-    if (a.m == 2)
-        return argmax ? launch_stream_kernel(stream_simt_kernel<2, true>, a, pt, stream, pdl, p)
-                      : launch_stream_kernel(stream_simt_kernel<2, false>, a, pt, stream, pdl, p);
-    if (a.m <= 8)
-        return argmax ? launch_stream_kernel(stream_kernel<false, true>, a, pt, stream, pdl, p)
-                      : launch_stream_kernel(stream_kernel<false, false>, a, pt, stream, pdl, p);
-    return argmax ? launch_stream_kernel(stream_kernel<true, true>, a, pt, stream, pdl, p)
-                  : launch_stream_kernel(stream_kernel<true, false>, a, pt, stream, pdl, p);
+    switch (epi) {
+        case kEpiStore: return launch_stream_epi<kEpiStore>(a, pt, stream, pdl, prefetch_weights);
+        case kEpiArgmax: return launch_stream_epi<kEpiArgmax>(a, pt, stream, pdl, prefetch_weights);
+        case kEpiGlu: return launch_stream_epi<kEpiGlu>(a, pt, stream, pdl, prefetch_weights);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace q8

@@ -2,7 +2,8 @@
 //
 // One CTA owns a tile of 128 output columns for all m rows and a contiguous range of the K/32 Q8_0 blocks (the
 // range is split across a thread-block cluster when N is too narrow to fill the SMs).  Its warps are specialised:
-//   - one producer warp: a single lane streams the CTA's blocks through a ring of 16 stages guarded by mbarriers
+//   - one producer warp: a single lane streams the CTA's blocks through a ring of 14 (m <= 8) or 15 stages guarded
+//     by mbarriers
 //     (full: bytes landed; empty: consumers done).  A stage is one 32-row Q8_0 block: its 32 x 128 int8 values (a
 //     2-D TMA box with the 128-byte swizzle), its 128 fp32 scales and the matching 32 activations of every row
 //     (a box of 8 or 16 rows; rows at or past m arrive as zeros from the box's out-of-range fill);
@@ -16,8 +17,8 @@
 // index 2t, 2t+1, 2t+8, 2t+9), and its activation fragment pairs x[2t] with x[2t+8] and x[2t+1] with x[2t+9].  MMA
 // row g is weight column c + 2p and row g+8 is column c + 2p + 1.
 //
-// Two CTAs are resident per SM (eight warps each at 128 registers; 82-90 KB of shared memory each), so up to 32
-// stages -- about 160 KB -- are in flight per SM.
+// Two CTAs are resident per SM (eight warps each at 128 registers; 72-85 KB of shared memory each), so up to 30
+// stages -- about 140 KB -- are in flight per SM.
 //
 // Programmatic dependent launch: the kernel's CTAs may start before the previous kernel on the stream has finished.
 // Every thread waits for it (griddepcontrol.wait) before touching memory that kernel may write -- the activations,
@@ -37,7 +38,7 @@ namespace q8 {
 
 __device__ unsigned int g_fault_word = 0;
 
-constexpr int kStages = 16;                         // pipeline depth (one 32-row Q8_0 block each)
+constexpr int kMaxStages = 16;                      // pipeline depth bound (one 32-row Q8_0 block a stage)
 constexpr int kWeightStage = kBlock * kTmaColumns;  // 4 KB of int8 values
 constexpr int kScaleStage = kTmaColumns * 4;        // 512 B of fp32 scales
 
@@ -47,10 +48,15 @@ constexpr unsigned kFaultEmptyWait = 2u;
 template <int NT> struct TmaShape {
     static constexpr int kConsumers = NT == 1 ? 7 : 6;
     static constexpr int kClasses = kConsumers / NT;  // blocks in flight across the consumers
+    // Stages: a multiple of the classes, so that every block of a stage is consumed by the same class, in order.
+    // An mbarrier parity wait is defined only for the barrier's current or preceding phase; with a stage shared by
+    // two classes a class that ran ahead could wait two phases ahead and see the older phase of its parity as
+    // complete.  With one class a stage, a class waits for the next fill of its stage only after consuming the last.
+    static constexpr int kStages = (kMaxStages / kClasses) * kClasses;
     static constexpr int kThreads = 32 * (kConsumers + 1);
     static constexpr int MR = 8 * NT;                 // activation rows held (zeros past m)
     static constexpr int kXStage = MR * kBlock * 2;   // bf16 activations of one block
-    static constexpr int kScaleOff = kStages * kWeightStage;
+    static constexpr int kScaleOff = kStages * kWeightStage;  // (kStages of this shape)
     static constexpr int kXOff = kScaleOff + kStages * kScaleStage;
     static constexpr int kBarOff = kXOff + kStages * kXStage;
     static constexpr int kSmem = 1024 /* alignment slack */ + kBarOff + 2 * kStages * 8;
@@ -126,6 +132,7 @@ __global__ void __maxnreg__(128)
     tma_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap smap,
                    const __grid_constant__ CUtensorMap xmap, const Args a, const int prefetch_weights) {
     using S = TmaShape<NT>;
+    constexpr int kStages = S::kStages;
     constexpr int V = 16 / NT;  // columns per lane
     constexpr int NP = V / 2;   // MMAs per 16-row step and row tile
     constexpr int MR = S::MR;
@@ -330,8 +337,12 @@ __global__ void __maxnreg__(128)
     finish_n<NCLS, MR, kTmaColumns, S::kThreads, ARGMAX>(a, red, blockIdx.x);
 }
 
-static_assert(finish_smem_n(TmaShape<1>::kClasses, 8, kTmaColumns) <= kStages * kWeightStage, "epilogue fits");
-static_assert(finish_smem_n(TmaShape<2>::kClasses, 16, kTmaColumns) <= kStages * kWeightStage, "epilogue fits");
+static_assert(finish_smem_n(TmaShape<1>::kClasses, 8, kTmaColumns) <= TmaShape<1>::kStages * kWeightStage,
+              "epilogue fits");
+static_assert(finish_smem_n(TmaShape<2>::kClasses, 16, kTmaColumns) <= TmaShape<2>::kStages * kWeightStage,
+              "epilogue fits");
+static_assert(TmaShape<1>::kStages % TmaShape<1>::kClasses == 0 && TmaShape<2>::kStages % TmaShape<2>::kClasses == 0,
+              "one consumer class a stage");
 static_assert(TmaShape<1>::kSmem * 2 <= 227 * 1024 && TmaShape<2>::kSmem * 2 <= 227 * 1024, "two CTAs per SM");
 
 // ---------------------------------------------------------------------------------------------------------------------

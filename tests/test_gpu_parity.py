@@ -502,3 +502,92 @@ def test_gemv_parts(dev, m, tiled, monkeypatch):
         single = q8.gemv(xd, devw[i][0], devw[i][1], N, tiled=tiled).cpu().numpy()
         if tiled:
             assert np.array_equal(single.view(np.uint32), got.view(np.uint32))
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# the gated pair (plan.rs `Launch::GemvGlu`, SwiGLU)
+# --------------------------------------------------------------------------------------------------------------------
+
+def _glu_bound(g_o, u_o, a_g, a_u, out_o):
+    """The product's bound carried through silu(g) * u: |silu'| <= 1.1, so an error e_g in g moves the output by at
+    most 1.1 |e_g| |u| and e_u by |silu(g)| |e_u|; plus a few fp32 ulps of the output for expf, the division and the
+    product."""
+    return (TOL * (1.1 * a_g * np.abs(u_o) + np.abs(oracle.silu(g_o)) * a_u) + 1.1 * TOL * TOL * a_g * a_u
+            + 1e-6 * np.abs(out_o))
+
+
+def _glu_run(torch, x, qg, sg, qu, su, N, want=("f32", "bf16")):
+    import q8_block_quantized_gemv_gb300 as q8
+    xd, qgd, sgd = _to_dev(torch, x, qg, sg)
+    _, qud, sud = _to_dev(torch, x, qu, su)
+    gate = q8.tile_device(qgd, sgd, N)
+    up = q8.tile_device(qud, sud, N)
+    out, outb = q8.gemv_glu(xd, gate, up, N, want=want)
+    torch.cuda.synchronize()
+    return (out.cpu().numpy() if out is not None else None,
+            outb.view(torch.int16).cpu().numpy().view(np.uint16) if outb is not None else None)
+
+
+def _glu_check(out, outb, x, qg, sg, qu, su, N, cols=None, what=""):
+    out_o, g_o, u_o, a_g, a_u = oracle.glu(x, qg, sg, qu, su, cols)
+    got = out if cols is None else out[:, cols]
+    err = np.abs(got.astype(np.float64) - out_o)
+    bound = _glu_bound(g_o, u_o, a_g, a_u, out_o)
+    bad = err > bound
+    if bad.any():
+        r, c = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} outputs out of bound; first at ({r},{c}): gpu {got[r, c]!r} "
+                             f"oracle {out_o[r, c]!r} bound {bound[r, c]!r}")
+    if outb is not None:
+        assert np.array_equal(outb, si.f32_to_bf16_bits(out)), f"{what}: bf16 output is not the fp32 output rounded"
+    if cols is None:
+        assert np.all(out[:, N:] == 0.0) and (outb is None or np.all(outb[:, N:] == 0))
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 8, 9, 16])
+def test_glu_small(dev, m):
+    """The gated pair on K = 1024, N = 1000 (8 column tiles, a ragged last one), every output: fp32 against the oracle
+    within the carried bound, the bf16 copy equal to the fp32 output rounded to nearest even, pads exactly 0."""
+    x, qg, sg = si.case(m, 1024, 1000, 2100 + m)
+    _, qu, su = si.case(m, 1024, 1000, 2200 + m)
+    out, outb = _glu_run(dev, x, qg, sg, qu, su, 1000)
+    _glu_check(out, outb, x, qg, sg, qu, su, 1000, what=f"m={m}")
+
+
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 16])
+def test_glu_ffn_gate_up_sampled(dev, m):
+    """The FFN's gate and up projections (4096 x 14336) as one gated-pair launch, in the benchmark's configuration;
+    384 sampled columns."""
+    x, qg, sg = si.case(m, 4096, 14336, si.case_seed(2, m, 7))
+    _, qu, su = si.case(m, 4096, 14336, si.case_seed(2, m, 8))
+    rng = np.random.default_rng(50 + m)
+    cols = np.unique(np.r_[0:32, 120:136, 248:264, 14304:14336, rng.integers(0, 14336, 290)])
+    out, outb = _glu_run(dev, x, qg, sg, qu, su, 14336)
+    _glu_check(out, outb, x, qg, sg, qu, su, 14336, cols, what=f"m={m}")
+
+
+@pytest.mark.parametrize("ks", [1, 2, 3, 4])
+@pytest.mark.parametrize("m", [2, 16])
+def test_glu_every_cluster_split(dev, ks, m, monkeypatch):
+    """Every K split of the gated pair's clusters (2 x ks CTAs): K = 4096 over 3 column tiles, every output."""
+    monkeypatch.setenv("Q8_KSPLIT", str(ks))
+    x, qg, sg = si.case(m, 4096, 300, 2300 + 10 * ks + m)
+    _, qu, su = si.case(m, 4096, 300, 2400 + 10 * ks + m)
+    out, outb = _glu_run(dev, x, qg, sg, qu, su, 300)
+    _glu_check(out, outb, x, qg, sg, qu, su, 300, what=f"ks={ks} m={m}")
+
+
+@pytest.mark.parametrize("want", [("f32",), ("bf16",)])
+def test_glu_single_output_and_determinism(dev, want):
+    """Either output alone is written correctly; repeated calls give identical bits."""
+    x, qg, sg = si.case(5, 512, 200, 2501)
+    _, qu, su = si.case(5, 512, 200, 2502)
+    a = _glu_run(dev, x, qg, sg, qu, su, 200, want)
+    b = _glu_run(dev, x, qg, sg, qu, su, 200, want)
+    if want == ("f32",):
+        assert a[1] is None and np.array_equal(a[0].view(np.uint32), b[0].view(np.uint32))
+        _glu_check(a[0], None, x, qg, sg, qu, su, 200, what="f32 only")
+    else:
+        assert a[0] is None and np.array_equal(a[1], b[1])
+        ref, _ = _glu_run(dev, x, qg, sg, qu, su, 200, ("f32",))
+        assert np.array_equal(a[1], si.f32_to_bf16_bits(ref))

@@ -243,6 +243,23 @@ def test_tile_argument_errors(lib):
     assert lib.q8_gemv_argmax_ex(A16, B16, C16, D16, None, 1, 32, 32, 4, None) == 1
 
 
+def test_gemv_glu_argument_errors(lib):
+    G, GS, U, US = B16, C16, 0x50000, 0x60000
+    F32, BF = D16, 0x70000
+    assert lib.q8_gemv_glu(None, G, GS, U, US, F32, BF, 1, 32, 64, 2, None) == 1      # null x
+    assert lib.q8_gemv_glu(A16, G, GS, None, US, F32, BF, 1, 32, 64, 2, None) == 1    # null up weight
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, None, None, 1, 32, 64, 2, None) == 1    # no output
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 1, 32, 64, 0, None) == 1       # not tiled
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 1, 32, 64, 8 | 2, None) == 1   # unknown flag
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 17, 32, 64, 2, None) == 2      # m > 16
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 1, 33, 64, 2, None) == 2       # K % 32
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 1, 32, 0, 2, None) == 2        # N = 0
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32 + 4, BF, 1, 32, 64, 2, None) == 3   # misaligned out
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF + 2, 1, 32, 64, 2, None) == 3   # misaligned bf16 out
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, F32, 1, 32, 64, 2, None) == 1      # outputs overlap
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, A16, None, 1, 32, 64, 2, None) == 1     # output over x
+
+
 def test_gemv_parts_argument_errors(lib):
     import ctypes
     P = q8._Part
