@@ -16,6 +16,9 @@ Contents, each citing the passage it follows (page titles as printed on the page
 * :func:`repack` -- ``from_q8.rs`` ``Q8Part`` (the host repacks the checkpoint's blocks into the int8 values and the
   fp32 scales); the block layout is the reading stated in the design notes (36-byte blocks, fp32 scale first).
 * :func:`dequantize` -- ``from_q8.rs`` module doc, w = q * d.
+* :func:`residual_norm` -- ``plan.rs`` ``Launch::Fold`` of a projection with ``Launch::Norm`` (``gemv_norm_epilogue``:
+  a projection with the residual add and the next norm in its epilogue; the norm launch is the lane's "rmsnorm"):
+  h = residual + x.W, out = h / sqrt(mean_n h^2 + eps) * gamma, in fp64.
 * :func:`glu` -- ``plan.rs`` ``Launch::GemvGlu``: two projections of one activation through a gate,
   out = act(x.wg + bg) * (x.wu + bu), SwiGLU when ``act`` is none; here without biases, so
   out = silu(g) * u with g = x.Wg, u = x.Wu (each as :func:`gemv`) and silu(g) = g / (1 + exp(-g)), in fp64.
@@ -202,3 +205,25 @@ def glu(x_bits: np.ndarray, qg: np.ndarray, sg: np.ndarray, qu: np.ndarray, su: 
     g, a_g = gemv(x_bits, qg, sg, cols)
     u, a_u = gemv(x_bits, qu, su, cols)
     return silu(g) * u, g, u, a_g, a_u
+
+
+def rmsnorm(h: np.ndarray, gamma: np.ndarray, eps: float, N: int) -> np.ndarray:
+    """RMS norm of each row's first N values (the lane's "rmsnorm", ``plan.rs`` ``Launch::Norm``):
+    h / sqrt(mean(h^2) + eps) * gamma, fp64; columns >= N are 0."""
+    h = np.asarray(h, dtype=np.float64)
+    ms = np.mean(h[:, :N] ** 2, axis=1, keepdims=True)
+    out = np.zeros_like(h)
+    out[:, :N] = h[:, :N] / np.sqrt(ms + float(eps)) * np.asarray(gamma, dtype=np.float64)[:N]
+    return out
+
+
+def residual_norm(x_bits: np.ndarray, q: np.ndarray, s: np.ndarray, residual: np.ndarray, gamma: np.ndarray,
+                  eps: float, N: int):
+    """A projection folded with the residual add and the next norm (``plan.rs`` ``Launch::Fold`` /
+    ``gemv_norm_epilogue``): h = residual + x.W (each output as :func:`gemv`), out = rmsnorm(h) * gamma.
+
+    Returns (h, out, y, a): the new residual stream, the normed activation, the product and its error scale."""
+    y, a = gemv(x_bits, q, s)
+    h = np.asarray(residual, dtype=np.float64)[:, : y.shape[1]] + y
+    h[:, N:] = 0.0
+    return h, rmsnorm(h, gamma, eps, N), y, a

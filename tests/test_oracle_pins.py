@@ -12,7 +12,10 @@ of q or s, a wrong bf16 decode, a wrong abs in the error scale) fails at least o
 * the arg-max's first-maximum rule (int8_model.rs ``decode_step_lg`` and the tie rule of ``reference_cuda``);
 * the gated pair (plan.rs ``Launch::GemvGlu``, SwiGLU): the identities silu(g) - silu(-g) = g and
   silu(g) + silu(-g) = g tanh(g/2), which together fix silu(g) = g sigmoid(g), and exact g, u against SiLU evaluated
-  in 40-digit decimal arithmetic.
+  in 40-digit decimal arithmetic;
+* the residual add and RMS norm (plan.rs ``Launch::Fold`` with ``Launch::Norm``): constant rows normalise to their sign,
+  the norm is invariant to scaling the row (eps = 0), the normed row's mean square is 1, a hand-derived 3-4 row in
+  decimal arithmetic, and h - residual is the product.
 """
 import os
 import struct
@@ -361,6 +364,89 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
                         abs(Fraction(a[r, n]) - ea) > Fraction(2) ** -52 * ea:
                     caught = True
     assert caught, f"the brute-force pin did not catch: {name}"
+# --------------------------------------------------------------------------------------------------------------------
+# residual add and RMS norm
+# --------------------------------------------------------------------------------------------------------------------
+
+def test_norm_constant_row_is_its_sign():
+    """x = 0 (so h = residual): a row of equal values c normalises to sign(c) * gamma exactly when eps = 0."""
+    K, N = 64, 40
+    x = np.zeros((2, K), dtype=np.uint16)
+    _, q, s = si.case(1, K, N, 77)
+    res = np.zeros((2, oracle.padded_n(N)), dtype=np.float32)
+    res[0, :N], res[1, :N] = 0.75, -3.0
+    gamma = np.linspace(0.5, 2.0, oracle.padded_n(N)).astype(np.float32)
+    h, out, y, _ = oracle.residual_norm(x, q, s, res, gamma, 0.0, N)
+    assert np.all(y == 0.0) and np.array_equal(h[:, :N], res[:, :N].astype(np.float64))
+    assert np.array_equal(out[0, :N], gamma[:N].astype(np.float64))
+    assert np.array_equal(out[1, :N], -gamma[:N].astype(np.float64))
+    assert np.all(out[:, N:] == 0.0)
+
+
+def test_norm_scale_invariance_and_unit_mean_square():
+    """With gamma = 1 and eps = 0: rmsnorm(alpha h) = rmsnorm(h) (alpha a power of two: exact) and the normed row's
+    mean square is 1 -- a missing square root or a sum where a mean belongs fails one of them."""
+    x, q, s = si.case(3, 256, 300, 78)
+    res = np.random.default_rng(3).standard_normal((3, oracle.padded_n(300))).astype(np.float32)
+    ones = np.ones(oracle.padded_n(300), dtype=np.float32)
+    h, out, _, _ = oracle.residual_norm(x, q, s, res, ones, 0.0, 300)
+    out2 = oracle.rmsnorm(8.0 * h, ones, 0.0, 300)
+    assert np.allclose(out2, out, rtol=1e-15, atol=0)
+    assert np.allclose(np.mean(out[:, :300] ** 2, axis=1), 1.0, rtol=1e-14)
+
+
+@pytest.mark.parametrize("eps", ["0", "0.000001", "0.5"])
+def test_norm_three_four_row_against_decimal(eps):
+    """h = (3, 4) (N = 2, x = 0): out = h / sqrt(12.5 + eps) * gamma, in 40-digit decimal arithmetic."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 40
+    x = np.zeros((1, 32), dtype=np.uint16)
+    q = np.zeros((32, 32), dtype=np.int8)
+    s = np.zeros((1, 32), dtype=np.float32)
+    res = np.zeros((1, 32), dtype=np.float32)
+    res[0, 0], res[0, 1] = 3.0, 4.0
+    gamma = np.zeros(32, dtype=np.float32)
+    gamma[0], gamma[1] = 1.5, -0.25
+    _, out, _, _ = oracle.residual_norm(x, q, s, res, gamma, float(eps), 2)
+    e = Decimal(float(eps))
+    r = (Decimal("12.5") + e).sqrt()
+    for n, (hv, gv) in enumerate([(3, Decimal("1.5")), (4, Decimal("-0.25"))]):
+        ref = Decimal(hv) / r * gv
+        assert abs(Decimal(float(out[0, n])) - ref) <= Decimal(2) ** -50 * abs(ref)
+
+
+@pytest.mark.parametrize("wrong", ["sum_not_mean", "no_sqrt", "eps_outside"])
+def test_norm_pins_catch_planted_mistakes(wrong, monkeypatch):
+    """A wrong RMS norm planted in the oracle fails the pins."""
+    def bad(h, gamma, eps, N):
+        h = np.asarray(h, dtype=np.float64)
+        sq = np.sum(h[:, :N] ** 2, axis=1, keepdims=True)
+        ms = sq if wrong == "sum_not_mean" else sq / N
+        d = {"sum_not_mean": np.sqrt(ms + eps), "no_sqrt": ms + eps, "eps_outside": np.sqrt(ms) + eps}[wrong]
+        out = np.zeros_like(h)
+        out[:, :N] = h[:, :N] / d * np.asarray(gamma, dtype=np.float64)[:N]
+        return out
+    monkeypatch.setattr(oracle, "rmsnorm", bad)
+    failed = 0
+    for pin in (test_norm_constant_row_is_its_sign, test_norm_scale_invariance_and_unit_mean_square,
+                lambda: test_norm_three_four_row_against_decimal("0.5")):
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1
+
+
+def test_norm_residual_is_added_to_the_product():
+    """h - residual equals the product of gemv, column by column (fp64: the add of an fp32 and an fp64 value is
+    exact when their magnitudes are close; here checked to 1 ulp of h)."""
+    x, q, s = si.case(2, 128, 70, 79)
+    res = np.random.default_rng(4).standard_normal((2, oracle.padded_n(70))).astype(np.float32)
+    h, _, y, _ = oracle.residual_norm(x, q, s, res, np.ones(96, np.float32), 1e-6, 70)
+    assert np.all(np.abs(h[:, :70] - res[:, :70] - y[:, :70]) <= 2.0 ** -52 * np.abs(h[:, :70]) * 2)
+    assert np.all(h[:, 70:] == 0.0)
+
+
 # --------------------------------------------------------------------------------------------------------------------
 # the gated pair (SwiGLU)
 # --------------------------------------------------------------------------------------------------------------------
