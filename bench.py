@@ -40,6 +40,8 @@ WORKLOAD = (f"decode-step Q8_0 projection chain: {LAYERS} layers x (q,k,v,o 4096
             f"down 14336x4096) + tied head 4096x128256 with fused arg-max; per layer q/k/v share one activation and "
             f"gate/up another (one multi-projection launch each), o and down their own")
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+FUSED_NOTE = ("; --fused: q/k/v read the previous layer's normed output, o and down add into the fp32 residual "
+              "stream in place and write the next RMS norm (q8_gemv_residual_norm), gate/up is the gated pair")
 GLU_NOTE = ("; --ffn glu: gate and up as one gated-pair launch (q8_gemv_glu, SwiGLU) writing bf16 silu(gate) * up, "
             "which the down projection reads")
 
@@ -223,10 +225,10 @@ class Chain:
     o its own, gate and up one more (one q8_gemv_parts launch), down its own; then the tied head with its arg-max.
     Weights are stored tiled (q8_tile_device), as a model would store them once at load time."""
 
-    def __init__(self, torch, m, seed=4000, glu=False):
+    def __init__(self, torch, m, seed=4000, glu=False, fused=False):
         import synth_inputs as si
         import q8_block_quantized_gemv_gb300 as q8
-        self.torch, self.m, self.glu = torch, m, glu
+        self.torch, self.m, self.glu, self.fused = torch, m, glu or fused, fused
         self.shapes = chain_shapes()
         # row-major weights as drawn, and the tiled storage the library streams
         self.w = [si.device_weight(K, N, seed + i) for i, (K, N) in enumerate(self.shapes)]
@@ -246,7 +248,15 @@ class Chain:
             off += m * K
         self.y = [torch.empty((m, padded(N)), dtype=torch.float32, device="cuda") for _, N in self.shapes]
         # gated-pair FFN: the gate/up launch writes silu(gate) * up as bf16, which the down projection reads
-        self.h = torch.empty((m, padded(FFN)), dtype=torch.bfloat16, device="cuda") if glu else None
+        self.h = torch.empty((m, padded(FFN)), dtype=torch.bfloat16, device="cuda") if self.glu else None
+        # fused layers: the residual stream (fp32, updated in place by o and down), the norms' weights, and the
+        # normed activations o and down write for the next launch
+        if fused:
+            g = torch.Generator(device="cuda")
+            g.manual_seed(seed + 7)
+            self.res = torch.randn((m, HIDDEN), generator=g, device="cuda", dtype=torch.float32)
+            self.gammas = [0.5 + torch.rand(HIDDEN, generator=g, device="cuda") for _ in range(2 * LAYERS)]
+            self.xn = [torch.empty((m, HIDDEN), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
         self.idx = torch.empty((m,), dtype=torch.int64, device="cuda")
         self.g_layers = self.g_head = None
         torch.cuda.synchronize()
@@ -262,6 +272,8 @@ class Chain:
 
     def run_layers(self):
         import q8_block_quantized_gemv_gb300 as q8
+        if self.fused:
+            return self.run_fused_layers()
         for xi, gis in self.layer_calls():
             if self.glu and len(gis) == 2:  # gate, up -> h
                 q8.gemv_glu(self.x[xi], self.wt[gis[0]], self.wt[gis[1]], FFN, out_bf16=self.h, want=(),
@@ -272,6 +284,26 @@ class Chain:
             else:
                 q8.gemv_parts(self.x[xi], [(self.wt[i][0], self.wt[i][1], self.shapes[i][1]) for i in gis],
                               ys=[self.y[i] for i in gis], constant_weights=True, tiled=True)
+
+    def run_fused_layers(self):
+        """A decode layer's data flow with every fusion: q/k/v read the previous layer's normed output (the first
+        layer its drawn activation); o (over a drawn attention output) adds into the residual stream in place and
+        writes the norm the FFN reads; gate/up is the gated pair; down adds into the residual stream and writes the
+        norm the next layer reads."""
+        import q8_block_quantized_gemv_gb300 as q8
+        for layer in range(LAYERS):
+            base, xb = 7 * layer, 4 * layer
+            x_in = self.x[xb] if layer == 0 else self.xn[1]
+            q8.gemv_parts(x_in, [(self.wt[i][0], self.wt[i][1], HIDDEN) for i in (base, base + 1, base + 2)],
+                          ys=[self.y[base], self.y[base + 1], self.y[base + 2]], constant_weights=True, tiled=True)
+            q8.gemv_residual_norm(self.x[xb + 1], self.wt[base + 3][0], self.wt[base + 3][1], HIDDEN, self.res,
+                                  self.gammas[2 * layer], 1e-6, h=self.res, out_bf16=self.xn[0],
+                                  constant_weights=True)
+            q8.gemv_glu(self.xn[0], self.wt[base + 4], self.wt[base + 5], FFN, out_bf16=self.h, want=(),
+                        constant_weights=True)
+            q8.gemv_residual_norm(self.h, self.wt[base + 6][0], self.wt[base + 6][1], HIDDEN, self.res,
+                                  self.gammas[2 * layer + 1], 1e-6, h=self.res, out_bf16=self.xn[1],
+                                  constant_weights=True)
 
     def run_head(self):
         import q8_block_quantized_gemv_gb300 as q8
@@ -308,6 +340,9 @@ class Chain:
                 total += K * padded(N) * 1.125 + m * padded(N) * 4
             if self.glu and len(gis) == 2:  # one bf16 output instead of two fp32 ones
                 total -= 2 * m * padded(FFN) * 4 - m * padded(FFN) * 2
+            if self.fused and self.shapes[gis[0]][1] == HIDDEN and len(gis) == 1:
+                # o and down: the residual read, h written over it, the normed bf16 row and the norm's weight
+                total += m * HIDDEN * 4 + m * HIDDEN * 2 + HIDDEN * 4
         return total
 
 
@@ -318,7 +353,7 @@ def run_ours(args, rank, world, local_rank):
     build.build()
     torch.cuda.set_device(local_rank)
     m = args.m
-    chain = Chain(torch, m, glu=args.ffn == "glu")
+    chain = Chain(torch, m, glu=args.ffn == "glu", fused=args.fused)
     chain.capture()
     stream = torch.cuda.current_stream()
 
@@ -402,7 +437,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD if args.ffn == "parts" else WORKLOAD + GLU_NOTE, "m": m,
+        "config": {"workload": WORKLOAD + (FUSED_NOTE if args.fused else GLU_NOTE if args.ffn == "glu" else ""), "m": m,
                    "gemvs_per_step": len(chain.shapes) + 1,
                    "launches_per_step": chain.launches_per_step(),
                    "bytes_per_step": bytes_step, "us_per_gemv": ms * 1e3 / (len(chain.shapes) + 1),
@@ -534,6 +569,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--ffn", choices=["parts", "glu"], default="parts",
                     help="the layers' gate/up launch: two fp32 outputs (default) or the fused gated pair")
+    ap.add_argument("--fused", action="store_true",
+                    help="the layers with every fusion: residual add + RMS norm after o and down, the gated pair")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step: µs/call of the single-GEMV workloads, one JSON line each")
     ap.add_argument("--sweep-m", default="1,2,4,8,16", help="row counts of --sweep")

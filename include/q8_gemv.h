@@ -143,6 +143,30 @@ q8_status q8_tile_device(const int8_t *q, const float *s, int K, int N, int8_t *
 q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const int8_t *qu, const float *su, float *out,
                       void *out_bf16, int m, int K, int N, unsigned int flags, q8_stream_t stream);
 
+/* A projection folded with the residual add and the next RMS norm ("plan.rs", `Launch::Fold` of a projection with
+ * `Launch::Norm`, `gemv_norm_epilogue`: the projection's blocks count in as they finish, and the finishing block
+ * reads their results back through L2 and runs the norm; the norm launch is the lane's "rmsnorm"):
+ *     y = x . W (the Q8_0 product of q8_gemv),   h = residual + y,
+ *     out[r, n] = h[r, n] / sqrt(mean_{n' < N} h[r, n']^2 + eps) * gamma[n]
+ * in one launch.  Every CTA writes its columns of h; the last CTA to finish (a completion counter from a fixed set of
+ * 64 held in static device memory: the library allocates nothing) reads the rows of h back, forms each row's mean
+ * square in a fixed order (the result does not depend on which CTA is last) and writes out.
+ *   x, q, s   as q8_gemv, the weight in the tiled storage (q8_tile)
+ *   residual  device, fp32 [m][Np], 4-byte aligned (read)
+ *   gamma     device, fp32 [N] (at least N values), 4-byte aligned
+ *   eps       >= 0 and finite
+ *   h         device, fp32 [m][Np] (written: residual + y, pads 0), 16-byte aligned; may be residual itself
+ *   out_bf16  device, bf16 [m][Np] (written: out rounded to nearest even, pads 0), 16-byte aligned -- the next
+ *             projection's activation as q8_gemv takes it (row pitch Np)
+ *   flags     Q8_FLAG_TILED (required) | Q8_FLAG_CONSTANT_WEIGHTS
+ * At most 64 calls may be in flight at once (each takes the next counter in turn; a counter is back to 0 when its
+ * launch ends).  Errors: Q8_ERR_ARG (null pointers, flags without Q8_FLAG_TILED or unknown bits, eps < 0 or not
+ * finite, outputs overlapping an input or each other other than h == residual), Q8_ERR_SHAPE, Q8_ERR_ALIGN,
+ * Q8_ERR_CUDA; nothing is launched on an error. */
+q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const float *s, const float *residual,
+                                const float *gamma, float eps, float *h, void *out_bf16, int m, int K, int N,
+                                unsigned int flags, q8_stream_t stream);
+
 /* One weight of a multi-projection call: its Q8_0 values and scales (row-major, or tiled with Q8_FLAG_TILED), its
  * output y [m][q8_padded_n(N)] (written) and its N. */
 typedef struct q8_part {

@@ -47,6 +47,7 @@ SIGNATURES = {
     "q8_device_fault": (_I, [_P, _I]),
     "q8_gemv_parts": (_I, [_P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_gemv_glu": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
+    "q8_gemv_residual_norm": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
 }
 
 
@@ -248,6 +249,28 @@ def gemv_glu(x, gate, up, N: int, out=None, out_bf16=None, want=("f32",), consta
                              out_bf16.data_ptr() if out_bf16 is not None else None, m, K, N,
                              _flags(constant_weights, True), _stream_handle(stream)), "q8_gemv_glu")
     return out, out_bf16
+
+
+def gemv_residual_norm(x, q, s, N: int, residual, gamma, eps: float, h=None, out_bf16=None,
+                       constant_weights: bool = False, stream=None):
+    """A projection folded with the residual add and the next RMS norm (q8_gemv_residual_norm), tiled weight:
+    h = residual + x.W, out = h / sqrt(mean(h^2) + eps) * gamma.  Returns (h fp32 [m, Np], out bf16 [m, Np]);
+    ``h`` may be ``residual`` (in place)."""
+    import torch
+    m, K, Np = _check_operands(x, q, s, N, True)
+    if residual.dtype != torch.float32 or residual.shape != (m, Np) or not residual.is_contiguous():
+        raise ValueError("residual must be a contiguous fp32 CUDA tensor [m, Np]")
+    if gamma.dtype != torch.float32 or gamma.numel() < N or not gamma.is_contiguous():
+        raise ValueError("gamma must be a contiguous fp32 CUDA tensor of at least N values")
+    if h is None:
+        h = torch.empty((m, Np), dtype=torch.float32, device=x.device)
+    if out_bf16 is None:
+        out_bf16 = torch.empty((m, Np), dtype=torch.bfloat16, device=x.device)
+    _check(lib().q8_gemv_residual_norm(x.data_ptr(), q.data_ptr(), s.data_ptr(), residual.data_ptr(),
+                                       gamma.data_ptr(), float(eps), h.data_ptr(), out_bf16.data_ptr(), m, K, N,
+                                       _flags(constant_weights, True), _stream_handle(stream)),
+           "q8_gemv_residual_norm")
+    return h, out_bf16
 
 
 def device_fault(clear: bool = False) -> int:

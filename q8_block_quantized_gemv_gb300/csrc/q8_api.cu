@@ -364,6 +364,50 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
     return Q8_OK;
 }
 
+extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const float *s, const float *residual,
+                                           const float *gamma, float eps, float *h, void *out_bf16, int m, int K,
+                                           int N, unsigned int flags, q8_stream_t stream) {
+    q8_status st = check_gemv_args(x, q, s, m, K, N);
+    if (st != Q8_OK) return st;
+    if (!residual || !gamma || !h || !out_bf16) return Q8_ERR_ARG;
+    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if (!(flags & Q8_FLAG_TILED)) return Q8_ERR_ARG;  // the tiled storage only
+    if (!(eps >= 0.0f) || !(eps < INFINITY)) return Q8_ERR_ARG;
+    if (q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
+    if (!aligned(h, 16) || !aligned(out_bf16, 16) || !aligned(residual, 4) || !aligned(gamma, 4)) return Q8_ERR_ALIGN;
+    const int Np = q8_padded_n(N);
+    const size_t wcols = (size_t)q8_tiled_n(N);
+    const size_t hbytes = (size_t)m * Np * 4, obytes = (size_t)m * Np * 2;
+    // h may be the residual itself (in place) but may not overlap it otherwise, nor any other operand.
+    if (h != residual && overlaps(h, hbytes, residual, hbytes)) return Q8_ERR_ARG;
+    const void *ins[4] = {x, q, s, gamma};
+    const size_t inb[4] = {(size_t)m * K * 2, (size_t)K * wcols, (size_t)(K / Q8_BLOCK) * wcols * 4, (size_t)Np * 4};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(h, hbytes, ins[i], inb[i]) || overlaps(out_bf16, obytes, ins[i], inb[i])) return Q8_ERR_ARG;
+    if (overlaps(out_bf16, obytes, h, hbytes) || overlaps(out_bf16, obytes, residual, hbytes)) return Q8_ERR_ARG;
+    static std::atomic<unsigned> next_counter{0};
+    unsigned int *count = q8::norm_counter(next_counter.fetch_add(1u, std::memory_order_relaxed));
+    if (!count) return cuda_fail(cudaGetLastError());
+    Args a = {static_cast<const uint16_t *>(x), q, s, h, nullptr, m, K, N, Np, K / Q8_BLOCK, 1,
+              static_cast<uint16_t *>(out_bf16), residual, gamma, eps, count};
+    int sms = 0;
+    int e = sm_count(&sms);
+    if (e != 0) return cuda_fail((cudaError_t)e);
+    q8::Parts pt = {};
+    pt.q[0] = q;
+    pt.s[0] = s;
+    pt.y[0] = h;
+    pt.N[0] = N;
+    pt.tile_end[0] = tiles_of(N);
+    pt.count = 1;
+    const Plan p = make_plan(m, K, Np, Q8_VARIANT_AUTO, true, sms, pt.tile_end[0]);
+    a.ksplit = p.ksplit;
+    cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiNorm, (cudaStream_t)stream, true,
+                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    return Q8_OK;
+}
+
 extern "C" q8_status q8_device_fault(unsigned int *fault, int clear) {
     if (!fault) return Q8_ERR_ARG;
     cudaError_t e = q8::read_fault_word(fault, clear != 0);

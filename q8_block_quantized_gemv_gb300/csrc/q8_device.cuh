@@ -35,7 +35,11 @@ struct Args {
     unsigned long long *keys;  // [m] packed arg-max keys, or null
     int m, K, N, Np, nb;       // nb = K / 32
     int ksplit;                // CTAs of a cluster splitting K (grid.y)
-    uint16_t *ybf;             // gated pair: bf16 [m][Np] copy of the output, or null
+    uint16_t *ybf;             // gated pair: bf16 [m][Np] copy of the output; norm: the normed bf16 [m][Np]
+    const float *res;          // norm: residual fp32 [m][Np] (h = res + y is written to y; may be y itself)
+    const float *gamma;        // norm: fp32 [Np]
+    float eps;                 // norm: added to the mean square
+    unsigned int *count;       // norm: this launch's completion counter (0 on entry, reset to 0 by the last CTA)
 };
 
 // Several weights that multiply one activation in one launch ("plan.rs", `Launch::GemmParts`: projections of one
@@ -71,6 +75,7 @@ __device__ __forceinline__ int select_part(const Parts &pt, int tile, Args &a) {
 constexpr int kEpiStore = 0;   // write y
 constexpr int kEpiArgmax = 1;  // write y (if any) and fold the row arg-max keys
 constexpr int kEpiGlu = 2;     // gated pair: part 0 is the gate, part 1 the up projection; write silu(g) * u
+constexpr int kEpiNorm = 3;    // residual add, then the last CTA writes the rows' RMS norm
 
 // A gated-pair launch interleaves the two weights' CTAs: grid x = 2 * tile + part, clusters of 2 along x (the
 // gate's and the up projection's CTAs of one tile and K range side by side).  `a` gets the part's q and s.
@@ -280,6 +285,132 @@ __device__ __forceinline__ void finish_glu(const Args &a, float *red, int tile) 
         }
     }
     cluster.sync();  // the up projection's rank keeps its shared memory until the gate's rank has read it
+}
+
+// A projection folded with the residual add and the next RMS norm ("plan.rs", `Launch::Fold` of a projection with
+// `Launch::Norm`, `gemv_norm_epilogue`: the projection's blocks count in as they finish, and the finishing block
+// reads their results back through L2 and runs the norm).  Every CTA finishes its columns as finish_n does, writing
+// h = residual + y to y; then it counts itself in.  The CTA that counts last reads the m rows of h back (through L2),
+// forms each row's sum of squares in a fixed order (so the result does not depend on which CTA is last) and writes
+// out = h / sqrt(mean + eps) * gamma as bf16 (0 in the pad columns).  Nothing waits on another CTA.
+template <int NRED, int MR, int TC, int NTHREADS, int RS = TC>
+__device__ __forceinline__ void finish_norm(const Args &a, float *red, int tile) {
+    namespace cg = cooperative_groups;
+    float *part = red + NRED * MR * RS;  // [MR][TC]
+    const int rows = a.m < MR ? a.m : MR;
+    for (int i = threadIdx.x; i < rows * TC; i += NTHREADS) {
+        const int at = (i / TC) * RS + i % TC;
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NRED; ++w) v += red[w * MR * RS + at];
+        part[i] = v;
+    }
+    const int ks = a.ksplit;
+    if (ks > 1)
+        cg::this_cluster().sync();
+    else
+        __syncthreads();
+    const int rank = blockIdx.y;
+    const int c0 = ks > 1 ? TC * rank / ks : 0;
+    const int c1 = ks > 1 ? TC * (rank + 1) / ks : TC;
+    const int width = c1 - c0;
+    for (int i = threadIdx.x; i < rows * width; i += NTHREADS) {
+        const int r = i / width;
+        const int c = c0 + (i - r * width);
+        float v;
+        if (ks > 1) {
+            cg::cluster_group cluster = cg::this_cluster();
+            v = 0.0f;
+            for (int p = 0; p < ks; ++p) v += cluster.map_shared_rank(part, p)[r * TC + c];  // rank order
+        } else {
+            v = part[r * TC + c];
+        }
+        const int n = tile * TC + c;
+        if (n < a.Np) {
+            const size_t at = (size_t)r * a.Np + n;
+            a.y[at] = n < a.N ? a.res[at] + v : 0.0f;
+        }
+    }
+    if (ks > 1) cg::this_cluster().sync();  // keep this CTA's shared memory alive until every rank has read it
+
+    // Count in; the last CTA runs the norm.
+    __shared__ unsigned int last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();  // this CTA's h is visible before its count
+        const unsigned total = gridDim.x * gridDim.y;
+        last = atomicAdd(a.count, 1u) == total - 1 ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();  // every other CTA's h is visible to the reads below
+    // Sums of squares: thread t takes the 16-byte column chunks t, t + NTHREADS, ... of every row at once (the
+    // rows' loads are independent), then the threads' sums are added by a fixed shuffle tree and in warp order.
+    constexpr int kWarpsN = NTHREADS / 32;
+    const int chunks = a.Np / 4;  // Np is a multiple of 32; h is 16-byte aligned with a row pitch of Np floats
+    float ss[MR];
+#pragma unroll
+    for (int r = 0; r < MR; ++r) ss[r] = 0.0f;
+    // Rows past m read row m - 1 again (branch-free, so that every row's load is issued before the first add); their
+    // sums are never used.
+    for (int j = threadIdx.x; j < chunks; j += NTHREADS) {
+        float4 v[MR];
+#pragma unroll
+        for (int r = 0; r < MR; ++r)
+            v[r] = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)(r < rows ? r : rows - 1) * a.Np) + j);
+#pragma unroll
+        for (int r = 0; r < MR; ++r) {
+            ss[r] = fmaf(v[r].x, v[r].x, ss[r]);
+            ss[r] = fmaf(v[r].y, v[r].y, ss[r]);
+            ss[r] = fmaf(v[r].z, v[r].z, ss[r]);
+            ss[r] = fmaf(v[r].w, v[r].w, ss[r]);
+        }
+    }
+    float *wsum = red;              // [kWarpsN][MR]
+    float *rstd = red + kWarpsN * MR;  // [MR]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int r = 0; r < MR; ++r) {
+        float v = ss[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) wsum[warp * MR + r] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < rows) {
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarpsN; ++w) v += wsum[w * MR + threadIdx.x];
+        rstd[threadIdx.x] = 1.0f / sqrtf(v / (float)a.N + a.eps);
+    }
+    __syncthreads();
+    // out = h * rstd * gamma, four columns a store; the pad columns get 0.
+    for (int j = threadIdx.x; j < chunks; j += NTHREADS) {
+        const int n = 4 * j;
+        float g[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) g[e] = n + e < a.N ? a.gamma[n + e] : 0.0f;
+        float4 hv[MR];
+#pragma unroll
+        for (int r = 0; r < MR; ++r)
+            hv[r] = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)(r < rows ? r : rows - 1) * a.Np) + j);
+#pragma unroll
+        for (int r = 0; r < MR; ++r)
+            if (r < rows) {
+                const float4 v = hv[r];
+                const float rs = rstd[r];
+                const float o0 = n < a.N ? v.x * rs * g[0] : 0.0f;
+                const float o1 = n + 1 < a.N ? v.y * rs * g[1] : 0.0f;
+                const float o2 = n + 2 < a.N ? v.z * rs * g[2] : 0.0f;
+                const float o3 = n + 3 < a.N ? v.w * rs * g[3] : 0.0f;
+                const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o0)) |
+                                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o1)) << 16);
+                const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o2)) |
+                                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o3)) << 16);
+                *reinterpret_cast<uint2 *>(a.ybf + (size_t)r * a.Np + n) = make_uint2(lo, hi);
+            }
+    }
+    if (threadIdx.x == 0) *a.count = 0u;  // ready for the next launch that takes this counter
 }
 
 template <int MR, int TC, bool ARGMAX>

@@ -408,6 +408,8 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     __syncthreads();
     if constexpr (EPI == kEpiGlu)
         finish_glu<kWarpsS, MR, kTmaColumns, kThreadsS, kSlabStride>(a, red, tile);
+    else if constexpr (EPI == kEpiNorm)
+        finish_norm<kWarpsS, MR, kTmaColumns, kThreadsS, kSlabStride>(a, red, tile);
     else
         finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, EPI == kEpiArgmax, kSlabStride>(a, red, tile);
 }
@@ -551,6 +553,8 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     __syncthreads();
     if constexpr (EPI == kEpiGlu)
         finish_glu<kWarpsS, M, kTmaColumns, kThreadsS>(a, red, tile);
+    else if constexpr (EPI == kEpiNorm)
+        finish_norm<kWarpsS, M, kTmaColumns, kThreadsS>(a, red, tile);
     else
         finish_n<kWarpsS, M, kTmaColumns, kThreadsS, EPI == kEpiArgmax>(a, red, tile);
 }
@@ -591,6 +595,17 @@ cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, 
 }
 
 }  // namespace
+
+// The completion counters of the residual-norm launches: the library's only scratch memory, static so that the
+// entry point allocates nothing.  A launch takes one counter (round robin over the calls); its last CTA leaves it
+// at 0 again.
+__device__ __align__(256) unsigned int g_norm_count[kNormCounters];
+
+unsigned int *norm_counter(unsigned slot) {
+    void *base = nullptr;
+    if (cudaGetSymbolAddress(&base, g_norm_count) != cudaSuccess) return nullptr;
+    return static_cast<unsigned int *>(base) + slot % kNormCounters;
+}
 
 int stream_ctas_per_sm(int) { return 2; }
 
@@ -644,6 +659,7 @@ cudaError_t launch_stream(const Args &a, const Parts &pt, int epi, cudaStream_t 
         case kEpiStore: return launch_stream_epi<kEpiStore>(a, pt, stream, pdl, prefetch_weights);
         case kEpiArgmax: return launch_stream_epi<kEpiArgmax>(a, pt, stream, pdl, prefetch_weights);
         case kEpiGlu: return launch_stream_epi<kEpiGlu>(a, pt, stream, pdl, prefetch_weights);
+        case kEpiNorm: return launch_stream_epi<kEpiNorm>(a, pt, stream, pdl, prefetch_weights);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -591,3 +591,87 @@ def test_glu_single_output_and_determinism(dev, want):
         assert a[0] is None and np.array_equal(a[1], b[1])
         ref, _ = _glu_run(dev, x, qg, sg, qu, su, 200, ("f32",))
         assert np.array_equal(a[1], si.f32_to_bf16_bits(ref))
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# residual add + RMS norm folded after a projection (plan.rs `Launch::Fold` / `gemv_norm_epilogue`)
+# --------------------------------------------------------------------------------------------------------------------
+
+def _norm_inputs(m, K, N, seed):
+    x, q, s = si.case(m, K, N, seed)
+    rng = np.random.default_rng(seed)
+    Np = oracle.padded_n(N)
+    res = np.zeros((m, Np), dtype=np.float32)
+    res[:, :N] = rng.standard_normal((m, N)).astype(np.float32)
+    gamma = (0.5 + rng.random(Np)).astype(np.float32)
+    return x, q, s, res, gamma
+
+
+def _norm_run(torch, x, q, s, res, gamma, eps, N, in_place=False):
+    import q8_block_quantized_gemv_gb300 as q8
+    xd, qd, sd = _to_dev(torch, x, q, s)
+    qt, st = q8.tile_device(qd, sd, N)
+    rd = torch.from_numpy(res).cuda()
+    gd = torch.from_numpy(gamma).cuda()
+    h, out = q8.gemv_residual_norm(xd, qt, st, N, rd, gd, eps, h=rd if in_place else None)
+    torch.cuda.synchronize()
+    return h.cpu().numpy(), out.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _norm_check(h, outb, x, q, s, res, gamma, eps, N, what=""):
+    h_o, out_o, _, a_o = oracle.residual_norm(x, q, s, res, gamma, eps, N)
+    tol_h = TOL * a_o + 2.0 ** -24 * np.abs(h_o)
+    bad = np.abs(h.astype(np.float64) - h_o) > tol_h
+    assert not bad.any(), f"{what}: h out of bound at {np.argwhere(bad)[0]}"
+    assert np.all(h[:, N:] == 0.0)
+    ms = np.mean(h_o[:, :N] ** 2, axis=1, keepdims=True) + eps
+    rstd = 1.0 / np.sqrt(ms)
+    carried = np.abs(gamma[None, :]) * rstd * (tol_h + np.abs(h_o) * np.sum(np.abs(h_o[:, :N]) * tol_h[:, :N], axis=1,
+                                                                             keepdims=True) / (N * ms))
+    bound = 2.0 ** -8 * np.abs(out_o) + carried + 1e-4 * np.abs(out_o)
+    got = si.bf16_bits_to_f32(outb).astype(np.float64)
+    bad = np.abs(got - out_o) > bound
+    if bad.any():
+        r, c = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: out of bound at ({r},{c}): gpu {got[r, c]!r} oracle {out_o[r, c]!r}")
+    assert np.all(outb[:, N:] == 0)
+
+
+@pytest.mark.parametrize("m", [1, 2, 8, 16])
+@pytest.mark.parametrize("K", [4096, 14336])
+def test_residual_norm_hidden_width(dev, m, K):
+    """The attention output (K = 4096) and FFN down (K = 14336) projections onto the 4096-wide residual stream, folded
+    with the residual add and the next RMS norm; every output of h and of the normed bf16 rows."""
+    x, q, s, res, gamma = _norm_inputs(m, K, 4096, 3100 + m + K)
+    h, out = _norm_run(dev, x, q, s, res, gamma, 1e-6, 4096)
+    _norm_check(h, out, x, q, s, res, gamma, 1e-6, 4096, what=f"m={m} K={K}")
+
+
+@pytest.mark.parametrize("ks", [1, 2, 3, 8])
+def test_residual_norm_every_cluster_split_and_in_place(dev, ks, monkeypatch):
+    """Ragged width (N = 300, three column tiles) under each K split, with h written over the residual in place."""
+    monkeypatch.setenv("Q8_KSPLIT", str(ks))
+    x, q, s, res, gamma = _norm_inputs(5, 1024, 300, 3200 + ks)
+    h, out = _norm_run(dev, x, q, s, res.copy(), gamma, 0.5, 300, in_place=True)
+    _norm_check(h, out, x, q, s, res, gamma, 0.5, 300, what=f"ks={ks}")
+
+
+def test_residual_norm_counters_reused_and_deterministic(dev):
+    """More calls than the 64 completion counters, back to back: every call's result is bit-identical (the last CTA's
+    fixed-order mean square does not depend on which CTA is last) and within the bound."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    x, q, s, res, gamma = _norm_inputs(3, 2048, 4096, 3300)
+    xd, qd, sd = _to_dev(torch, x, q, s)
+    qt, st = q8.tile_device(qd, sd, 4096)
+    rd, gd = torch.from_numpy(res).cuda(), torch.from_numpy(gamma).cuda()
+    outs = []
+    for _ in range(70):
+        h, out = q8.gemv_residual_norm(xd, qt, st, 4096, rd, gd, 1e-5, constant_weights=True)
+        outs.append((h, out))
+    torch.cuda.synchronize()
+    h0, o0 = outs[0][0].cpu().numpy(), outs[0][1].view(torch.int16).cpu().numpy().view(np.uint16)
+    for h, out in outs[1:]:
+        assert np.array_equal(h.cpu().numpy().view(np.uint32), h0.view(np.uint32))
+        assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), o0)
+    _norm_check(h0, o0, x, q, s, res, gamma, 1e-5, 4096, what="repeated")

@@ -260,6 +260,38 @@ def test_gemv_glu_argument_errors(lib):
     assert lib.q8_gemv_glu(A16, G, GS, U, US, A16, None, 1, 32, 64, 2, None) == 1     # output over x
 
 
+def test_gemv_residual_norm_argument_errors(lib):
+    import ctypes
+    R, G, H, O = 0x50000, 0x60000, 0x70000, 0x80000
+    f = ctypes.c_float
+    ok = (A16, B16, C16, R, G, f(1e-6), H, O, 2, 64, 96, 2, None)
+    def call(**kw):
+        args = list(ok)
+        names = ["x", "q", "s", "res", "gamma", "eps", "h", "out", "m", "K", "N", "flags", "stream"]
+        for k, v in kw.items():
+            args[names.index(k)] = v
+        return lib.q8_gemv_residual_norm(*args)
+    assert call(x=None) == 1
+    assert call(res=None) == 1
+    assert call(gamma=None) == 1
+    assert call(h=None) == 1
+    assert call(out=None) == 1
+    assert call(flags=0) == 1                  # not tiled
+    assert call(flags=2 | 8) == 1              # unknown flag
+    assert call(eps=f(-1.0)) == 1
+    assert call(eps=f(float("inf"))) == 1
+    assert call(eps=f(float("nan"))) == 1
+    assert call(m=17) == 2
+    assert call(K=33) == 2
+    assert call(N=0) == 2
+    assert call(h=H + 4) == 3                  # misaligned h
+    assert call(out=O + 2) == 3                # misaligned bf16 out
+    assert call(res=R + 2) == 3                # misaligned residual
+    assert call(h=R + 16) == 1                 # h partly over the residual
+    assert call(out=H) == 1                    # out over h
+    assert call(h=A16) == 1                    # h over x
+
+
 def test_gemv_parts_argument_errors(lib):
     import ctypes
     P = q8._Part
