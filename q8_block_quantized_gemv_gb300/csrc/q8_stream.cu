@@ -126,6 +126,15 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, unsigned long lo
     return d;
 }
 
+// A bf16 pair as an fp16 pair without scaling; exact when both are fp16 normals or zero.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_plain(uint32_t x) {
+    uint32_t d;
+    asm("{\n .reg .b32 lo, hi;\n shl.b32 lo, %1, 16;\n and.b32 hi, %1, 0xFFFF0000;\n cvt.rn.f16x2.f32 %0, hi, lo;\n}"
+        : "=r"(d)
+        : "r"(x));
+    return d;
+}
+
 // Per-half unsigned 16-bit max / min / decrement.
 __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -183,11 +192,11 @@ __device__ __forceinline__ void issue_unit(unsigned char *stage, const int8_t *q
     cp_async16(stage + kUnit + lane * 16, reinterpret_cast<const unsigned char *>(s + u * kUnitScales) + lane * 16);
 }
 
-// How a block's activations enter the MMA: scaled fp16 or raw bf16.  scale[i] = 2^p and sf[i] = 2^-p (in both halves
-// of an fp32 pair) for the lane's activation row g + 8i.
+// How a block's activations enter the MMA: fp16 as they are (plain), scaled fp16, or raw bf16.  scale[i] = 2^p and
+// sf[i] = 2^-p (in both halves of an fp32 pair) for the lane's activation row g + 8i.
 struct XPlan {
     unsigned long long scale[2], sf[2];
-    bool f16;
+    bool f16, plain;
 };
 
 // The range of the lane's activation words of one row: its largest |x| in the low half and 0xFFFF minus (its smallest
@@ -208,11 +217,15 @@ __device__ __forceinline__ uint32_t row_range(const uint2 (&x)[2]) {
 // From a reduced range: whether one power of two maps every nonzero value into fp16's normal range -- all values
 // finite, the largest binade at least 2^-111 (so 2^p = 2^(142 - emax) is a normal fp32) and every nonzero value
 // within 29 binades below it -- or every value is zero; and the factors 2^p, 2^-p.
-__device__ __forceinline__ bool range_plan(uint32_t range, unsigned long long &scale, unsigned long long &sf) {
+// plain: every value already is an fp16 normal or zero (largest binade at most 2^15, smallest nonzero at least 2^-14),
+// so no scaling is needed.
+__device__ __forceinline__ bool range_plan(uint32_t range, unsigned long long &scale, unsigned long long &sf,
+                                           bool &plain) {
     const uint32_t xmax = range & 0xFFFFu;
     const uint32_t xmin = ((~range >> 16) & 0xFFFFu) + 1u;  // 0x10000 when every value is zero
     const int emax = (int)(xmax >> 7), emin = (int)(xmin >> 7);
     const bool zero = xmax == 0u;
+    plain = zero || (emax <= 142 && emin >= 113);
     const uint32_t up = zero ? 0x3F800000u : (uint32_t)(269 - emax) << 23;
     const uint32_t down = zero ? 0x3F800000u : (uint32_t)(emax - 15) << 23;
     scale = ((unsigned long long)up << 32) | up;
@@ -233,17 +246,18 @@ template <int NR, bool PER_ROW> __device__ __forceinline__ XPlan plan_block(cons
         for (int o = 1; o < 4; o <<= 1)
 #pragma unroll
             for (int r = 0; r < NR; ++r) rg[r] = vmax_u16x2(rg[r], __shfl_xor_sync(0xffffffffu, rg[r], o));
-        bool ok = true;
+        bool ok = true, plain;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) ok = range_plan(rg[r < NR ? r : 0], pl.scale[r], pl.sf[r]) && ok;
+        for (int r = 0; r < 2; ++r) ok = range_plan(rg[r < NR ? r : 0], pl.scale[r], pl.sf[r], plain) && ok;
         pl.f16 = __all_sync(0xffffffffu, ok);
+        pl.plain = false;
     } else {
         uint32_t rg = row_range(x[0]);
 #pragma unroll
         for (int r = 1; r < NR; ++r) rg = vmax_u16x2(rg, row_range(x[r]));
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) rg = vmax_u16x2(rg, __shfl_xor_sync(0xffffffffu, rg, o));
-        pl.f16 = range_plan(rg, pl.scale[0], pl.sf[0]);
+        pl.f16 = range_plan(rg, pl.scale[0], pl.sf[0], pl.plain);
         pl.scale[1] = pl.scale[0];
         pl.sf[1] = pl.sf[0];
     }
@@ -251,9 +265,10 @@ template <int NR, bool PER_ROW> __device__ __forceinline__ XPlan plan_block(cons
 }
 
 // One block of the warp's run: the 16 slices' MMAs over both 16-row halves and the fold into the carry.  `a` holds
-// the A fragments of the two halves (fp16 scaled, or raw bf16), `pl` the factors of the block's scales (2^-p per
-// activation row, unused for bf16), ROWS16 whether activation rows 8..15 exist and SAME whether both rows share 2^-p.
-template <bool F16, bool ROWS16, bool SAME>
+// the A fragments of the two halves (fp16, or raw bf16), `pl` the factors of the block's scales (2^-p per activation
+// row; unused for bf16 and for PLAIN fp16, which is unscaled), ROWS16 whether activation rows 8..15 exist and SAME
+// whether both rows share 2^-p.
+template <bool F16, bool ROWS16, bool SAME, bool PLAIN = false>
 __device__ __forceinline__ void block_contract(const unsigned char *st, int lane, const uint32_t (&a)[2][4],
                                                const XPlan &pl,
                                                unsigned long long (&acc)[ROWS16 ? 2 : 1][kSlices]) {
@@ -276,10 +291,10 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
                 mma_16816<false, false>(d, a[1], q8x2_to_bf16x2<0>(u1), q8x2_to_bf16x2<2>(u1));
             }
             // the scales of columns 8j + 2t, 8j + 2t + 1 (the D fragment's columns), times the row's factor
-            const unsigned long long sc = F16 ? mul_f32x2(sp[4 * j], pl.sf[0]) : sp[4 * j];
+            const unsigned long long sc = (F16 && !PLAIN) ? mul_f32x2(sp[4 * j], pl.sf[0]) : sp[4 * j];
             acc[0][j] = fma_f32x2(sc, pack_f32x2(d[0], d[1]), acc[0][j]);
             if (ROWS16) {
-                const unsigned long long sc1 = (!F16 || SAME) ? sc : mul_f32x2(sp[4 * j], pl.sf[1]);
+                const unsigned long long sc1 = (!F16 || SAME || PLAIN) ? sc : mul_f32x2(sp[4 * j], pl.sf[1]);
                 acc[ROWS16 ? 1 : 0][j] = fma_f32x2(sc1, pack_f32x2(d[2], d[3]), acc[ROWS16 ? 1 : 0][j]);
             }
         }
@@ -348,9 +363,13 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     if (n > 0) load_x(xn1, b0);
     if (n > 1) load_x(xn2, b0 + 1);
 
+    // Stage indices: counted round for the 16-row kernel (measured faster there), i % depth for the 8-row one (its
+    // register allocation is at its limit; the counters cost it more than they save).
+    int cur = 0, nxt = kDepthS - 1;
     for (int i = 0; i < n; ++i) {
         const int ahead = i + kDepthS - 1;
-        if (ahead < n) issue_unit(ring + (ahead % kDepthS) * kStageS, a.q, a.s, unit0 + ahead, lane);
+        if (ahead < n)
+            issue_unit(ring + (ROWS16 ? nxt : ahead % kDepthS) * kStageS, a.q, a.s, unit0 + ahead, lane);
         cp_async_commit();
         uint2 xc[NR][2];
 #pragma unroll
@@ -365,8 +384,22 @@ __global__ void __launch_bounds__(kThreadsS, 2)
 
         cp_async_wait<kDepthS - 1>();  // this lane's copies of unit i have landed
         __syncwarp();                  // ... and every other lane's
-        const unsigned char *st = ring + (i % kDepthS) * kStageS;
-        if (plan.f16) {
+        const unsigned char *st = ring + (ROWS16 ? cur : i % kDepthS) * kStageS;
+        if (ROWS16) {
+            cur = cur == kDepthS - 1 ? 0 : cur + 1;
+            nxt = nxt == kDepthS - 1 ? 0 : nxt + 1;
+        }
+        if (ROWS16 && plan.plain) {
+            uint32_t af[2][4];
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                af[s][0] = bf16x2_to_f16x2_plain(xc[0][s].x);
+                af[s][2] = bf16x2_to_f16x2_plain(xc[0][s].y);
+                af[s][1] = bf16x2_to_f16x2_plain(xc[NR - 1][s].x);
+                af[s][3] = bf16x2_to_f16x2_plain(xc[NR - 1][s].y);
+            }
+            block_contract<true, ROWS16, ROWS16, true>(st, lane, af, plan, acc);
+        } else if (plan.f16) {
             uint32_t af[2][4];
 #pragma unroll
             for (int s = 0; s < 2; ++s) {

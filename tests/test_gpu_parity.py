@@ -142,14 +142,16 @@ def _bits(v):
     return si.f32_to_bf16_bits(a).reshape(a.shape)
 
 
-def _ranged_case(m, kinds=tuple(range(12)), nb_each=2, N=300, seed=4242):
+def _ranged_case(m, kinds=tuple(range(14)), nb_each=2, N=300, seed=4242):
     """Activations built block by block (all rows of a 32-row block share a kind), every kind twice:
     0 N(0,1); 1 N(0,1) * 1e30; 2 N(0,1) * 1e-30; 3 N(0,1) * 1e-36 (below the scalable range); 4 rows alternating
     1e10 and 1e-10 (a 66-binade span); 5 one 1.0 per row and 1e-12 * N(0,1) elsewhere, with the weight row of the
     1.0 zeroed in 150 columns (the large activation meets zero weights); 6 signed powers 2^-26 .. 2^3 with random
     mantissas, both ends present (a 29-binade span: the widest exact fp16 scaling); 7 as 6 plus one 2^-27 (one binade
     more); 8 N(0,1) with a few bf16 subnormals; 9 zeros and negative zeros; 10 zeros with a few N(0,1) values;
-    11 values +-1.9921875 * 2^k, k in -10..9 (the largest bf16 mantissa in the top binade: 65280 after scaling).
+    11 values +-1.9921875 * 2^k, k in -10..9 (the largest bf16 mantissa in the top binade: 65280 after scaling);
+    12 signed values m * 2^e, e in -14..15, with 2^-14 and 1.9921875 * 2^15 = 65280 present (the widest range that is
+    already fp16 normal, so that no scaling is needed); 13 as 12 plus one -1.5 * 2^-15 (one binade below it).
     Blocks cycle through `kinds`."""
     nb = len(kinds) * nb_each
     K = 32 * nb
@@ -189,6 +191,15 @@ def _ranged_case(m, kinds=tuple(range(12)), nb_each=2, N=300, seed=4242):
             v[0, 7] = np.uint16(0x8005)
         elif kind == 9:
             v = np.where(rng.integers(0, 2, size=(m, 32)) == 1, np.uint16(0x8000), np.uint16(0)).astype(np.uint16)
+        elif kind in (12, 13):
+            e = rng.integers(-14, 16, size=(m, 32))
+            mant = 1.0 + rng.integers(0, 128, size=(m, 32)) / 128.0
+            e[:, 0], mant[:, 0] = 15, 1.9921875
+            e[:, 1] = -14
+            sign = np.where(rng.integers(0, 2, size=(m, 32)) == 1, -1.0, 1.0)
+            v = _bits((sign * mant * np.exp2(e)).astype(np.float32))
+            if kind == 13:
+                v[m // 2, 9] = _bits(np.float32(-1.5 * 2.0 ** -15))
         elif kind == 10:
             v = np.zeros((m, 32), dtype=np.uint16)
             v[:, 4] = _bits(g[:, 4])
@@ -201,14 +212,14 @@ def _ranged_case(m, kinds=tuple(range(12)), nb_each=2, N=300, seed=4242):
     return x, q, s, N
 
 
-@pytest.mark.parametrize("kinds", [tuple(range(12))] + [(k,) for k in range(12)], ids=lambda k: "-".join(map(str, k)))
+@pytest.mark.parametrize("kinds", [tuple(range(14))] + [(k,) for k in range(14)], ids=lambda k: "-".join(map(str, k)))
 @pytest.mark.parametrize("m", [5, 16])
 def test_activation_magnitude_ranges(dev, m, kinds):
     """Every activation range the scaled fp16 operands must either represent exactly or hand to bf16 operands: the
     bound holds for every output of every kernel family, all kinds mixed and each kind alone (so that the bound is
     set by that kind's own magnitudes), including the columns whose large activations meet zero weights (A is then
     set by the 1e-12 values alone)."""
-    x, q, s, N = _ranged_case(m, kinds, nb_each=24 // len(kinds))
+    x, q, s, N = _ranged_case(m, kinds, nb_each=max(2, 24 // len(kinds)))
     y_o, a_o = oracle.gemv(x, q, s)
     for v in _variants(m):
         _assert_close(_gemv(dev, x, q, s, N, v), y_o, a_o, f"m={m} kinds={kinds} {v}")
