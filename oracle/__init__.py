@@ -19,6 +19,11 @@ Contents, each citing the passage it follows (page titles as printed on the page
 * :func:`residual_norm` -- ``plan.rs`` ``Launch::Fold`` of a projection with ``Launch::Norm`` (``gemv_norm_epilogue``:
   a projection with the residual add and the next norm in its epilogue; the norm launch is the lane's "rmsnorm"):
   h = residual + x.W, out = h / sqrt(mean_n h^2 + eps) * gamma, in fp64.
+* :func:`quantize_act` -- ``plan.rs`` ``QBLOCK`` / ``Buffer::quantized`` and the quantized numerics of
+  ``Launch::projected_input`` (an activation a projection reads quantized: int8 values and one scale per 32 values),
+  with the weight rule's shape (``from_q8.rs`` ``quantize``: d = amax / 127, q = round(x / d)) taken in fp32.
+* :func:`gemv_q8act` -- the product under those numerics: y[r,n] = sum_b s[b,n] d[r,b] sum_i xq[r,32b+i] q[32b+i,n],
+  the inner sums exact integers, the rest in fp64, with its error scale.
 * :func:`glu` -- ``plan.rs`` ``Launch::GemvGlu``: two projections of one activation through a gate,
   out = act(x.wg + bg) * (x.wu + bu), SwiGLU when ``act`` is none; here without biases, so
   out = silu(g) * u with g = x.Wg, u = x.Wu (each as :func:`gemv`) and silu(g) = g / (1 + exp(-g)), in fp64.
@@ -227,3 +232,73 @@ def residual_norm(x_bits: np.ndarray, q: np.ndarray, s: np.ndarray, residual: np
     h = np.asarray(residual, dtype=np.float64)[:, : y.shape[1]] + y
     h[:, N:] = 0.0
     return h, rmsnorm(h, gamma, eps, N), y, a
+
+
+def _f32_div(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """The IEEE fp32 quotient of fp32 values, correctly rounded (to nearest, ties to even): the fp64 quotient rounded
+    to fp32.  Rounding twice is harmless for a quotient when the wider format has at least 2p + 2 significant bits
+    (53 >= 2 * 24 + 2), subnormal results included."""
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore", under="ignore"):
+        return (np.asarray(a, dtype=np.float64) / np.asarray(b, dtype=np.float64)).astype(np.float32)
+
+
+def quantize_act(x_bits: np.ndarray):
+    """The quantized form of an activation (``plan.rs`` ``QBLOCK``: 32 values share one scale; ``Buffer::quantized``:
+    int8 values and a scale per 32).
+
+    The pages name the form but not its rounding; the reading here is the weight rule of ``from_q8.rs``
+    ``quantize`` in the precision the values have (fp32): for each row and block of 32 values,
+    amax = max |x|, d = fp32(amax / 127), q = round-half-away-from-zero(fp32(x / d)), clamped to [-127, 127] (the
+    clamp never binds for bf16 inputs: d's relative error is at most 2^-10 even at the smallest bf16 subnormal).
+    A block of zeros has d = 0 and q = 0; a block holding inf or NaN has d = NaN and q = 0.
+
+    x_bits: uint16 bf16 patterns [m, K] (K a multiple of 32).  Returns (xq int8 [m, K], xd float32 [m, K/32]).
+    """
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    m, K = x_bits.shape
+    if K % Q8_BLOCK:
+        raise ValueError("K must be a multiple of 32")
+    nb = K // Q8_BLOCK
+    x = (x_bits.astype(np.uint32) << 16).view(np.float32).reshape(m, nb, Q8_BLOCK)
+    amax = np.abs(x).max(axis=2)                                   # NaN when the block holds NaN
+    bad = ~np.isfinite(amax)
+    zero = amax == 0.0
+    d = _f32_div(amax, np.float32(127.0))
+    safe = np.where(bad | zero, np.float32(1.0), d)
+    v = _f32_div(x, safe[:, :, None]).astype(np.float64)
+    r = np.clip(_round_half_away(v), -127.0, 127.0)
+    r[bad | zero] = 0.0
+    xq = r.astype(np.int8).reshape(m, K)
+    xd = np.where(bad, np.float32(np.nan), np.where(zero, np.float32(0.0), d)).astype(np.float32)
+    return xq, xd
+
+
+def gemv_q8act(xq: np.ndarray, xd: np.ndarray, q: np.ndarray, s: np.ndarray, cols=None):
+    """The Q8_0 product of a quantized activation (the quantized numerics of ``plan.rs``): per row r and column n,
+    y = sum_b s[b, n] * d[r, b] * sum_i xq[r, 32b + i] * q[32b + i, n].
+
+    The inner sums are exact integers (int64); each is multiplied by s * d (exact in fp64: 24 by 24 bits) and added
+    to the fp64 carry, block b ascending.  A[r, n] = sum_b |s d| sum_i |xq q| is the error scale.
+    xq int8 [m, K]; xd float32 [m, K/32]; q int8 [K, Np]; s float32 [K/32, Np]; cols: optional column indices.
+    Returns (y, A), fp64 [m, len(cols) or Np]."""
+    xq = np.asarray(xq, dtype=np.int8)
+    xd = np.asarray(xd, dtype=np.float32)
+    m, K = xq.shape
+    nb = K // Q8_BLOCK
+    if K % Q8_BLOCK or xd.shape != (m, nb) or q.shape[0] != K or s.shape != (nb, q.shape[1]):
+        raise ValueError("shape mismatch")
+    cols = np.arange(q.shape[1]) if cols is None else np.asarray(cols, dtype=np.int64)
+    qc = np.asarray(q, dtype=np.int8)[:, cols].astype(np.int64).reshape(nb, Q8_BLOCK, cols.size)
+    sc = np.asarray(s, dtype=np.float32)[:, cols].astype(np.float64)          # [nb, ncols]
+    xb = xq.astype(np.int64).reshape(m, nb, Q8_BLOCK).transpose(1, 0, 2)     # [nb, m, 32]
+    inner = np.matmul(xb, qc)                                                # [nb, m, ncols], exact
+    inner_abs = np.matmul(np.abs(xb), np.abs(qc))
+    y = np.zeros((m, cols.size), dtype=np.float64)
+    a = np.zeros((m, cols.size), dtype=np.float64)
+    dd = xd.astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        for b in range(nb):
+            f = sc[b][None, :] * dd[:, b][:, None]                               # s[b, n] * d[r, b]
+            y += f * inner[b].astype(np.float64)
+            a += np.abs(f) * inner_abs[b].astype(np.float64)
+    return y, a

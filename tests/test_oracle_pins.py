@@ -15,7 +15,12 @@ of q or s, a wrong bf16 decode, a wrong abs in the error scale) fails at least o
   in 40-digit decimal arithmetic;
 * the residual add and RMS norm (plan.rs ``Launch::Fold`` with ``Launch::Norm``): constant rows normalise to their sign,
   the norm is invariant to scaling the row (eps = 0), the normed row's mean square is 1, a hand-derived 3-4 row in
-  decimal arithmetic, and h - residual is the product.
+  decimal arithmetic, and h - residual is the product;
+* the quantized activation (plan.rs ``QBLOCK``, ``Buffer::quantized``) and the product that reads it: exact codes
+  where d is a power of two, ties away from zero, zero and non-finite blocks, every d and code against the rule in
+  exact rational arithmetic with binary32 rounding written out (normal, tiny and subnormal d), the code bounds and
+  the d/2 error over every bf16 magnitude, brute force of the product, its integer and one-hot special cases, a
+  dense fp64 matmul of the dequantized operands, and the distance to the bf16 product.
 """
 import os
 import struct
@@ -509,3 +514,213 @@ def test_glu_exact_inputs_against_decimal_silu(c, e):
     assert np.all(out[0, 1:] == 0.0)
 
 
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# quantized activations (int8 values and one scale per 32 values)
+# --------------------------------------------------------------------------------------------------------------------
+
+def _fp32_round(v: Fraction) -> Fraction:
+    """The binary32 value nearest to v (ties to even), subnormals included, in exact rational arithmetic."""
+    if v == 0:
+        return Fraction(0)
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()  # 2^e <= a < 2^(e+2)
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, -126) - 23)
+    return sign * round(a / quantum) * quantum  # round() of a Fraction: nearest, ties to even
+
+
+def _half_away(v: Fraction) -> int:
+    n = int((abs(v) + Fraction(1, 2)) // 1)
+    return -n if v < 0 else n
+
+
+def _act_block(values):
+    """bf16 bit patterns [1, 32] of exactly representable values."""
+    return np.array([[_bf16(float(v)) for v in values]], dtype=np.uint16)
+
+
+@pytest.mark.parametrize("e", [-100, -20, -7, 0, 3, 60])
+def test_act_quantize_exact_codes(e):
+    """x = k 2^e with integers |k| <= 127 and 127 present: d = 127 2^e / 127 = 2^e exactly and every code is k."""
+    rng = np.random.default_rng(e + 200)
+    k = rng.integers(-127, 128, size=32)
+    k[7] = 127 if e % 2 else -127
+    x = _act_block([int(v) * 2.0 ** e for v in k])
+    xq, xd = oracle.quantize_act(x)
+    assert float(xd[0, 0]) == 2.0 ** e
+    assert np.array_equal(xq[0].astype(np.int64), k)
+
+
+def test_act_quantize_ties_go_away_from_zero():
+    """With d = 1 (amax = 127): values j + 1/2 are exact ties and go away from zero (62.5 -> 63, -0.5 -> -1); ties to
+    even would give 62 and 0."""
+    vals = [127.0, 62.5, -62.5, 0.5, -0.5, 1.5, -2.5, 126.5] + [0.0] * 24
+    xq, xd = oracle.quantize_act(_act_block(vals))
+    assert float(xd[0, 0]) == 1.0
+    assert list(xq[0, :8]) == [127, 63, -63, 1, -1, 2, -3, 127]
+
+
+def test_act_quantize_zero_and_nonfinite_blocks():
+    """A block of (signed) zeros gives d = 0 and codes 0; a block holding inf or NaN gives d = NaN and codes 0; the
+    other blocks of the row are unaffected."""
+    x = np.zeros((3, 64), dtype=np.uint16)
+    x[0, :32] = np.uint16(0x8000)
+    x[1, 3] = np.uint16(0x7F80)       # +inf
+    x[2, 40] = np.uint16(0x7FC0)      # NaN
+    x[1, 32:] = _act_block(np.arange(32) - 16.0)
+    xq, xd = oracle.quantize_act(x)
+    assert xd[0, 0] == 0.0 and not np.signbit(xd[0, 0]) and np.all(xq[0] == 0)
+    assert np.isnan(xd[1, 0]) and np.all(xq[1, :32] == 0)
+    assert np.isnan(xd[2, 1]) and np.all(xq[2, 32:] == 0)
+    assert float(xd[1, 1]) == float(np.float32(16.0) / np.float32(127.0))
+    assert xq[1, 32] == -127
+
+
+@pytest.mark.parametrize("scale", [1.0, 1e-30, 1e-38, 1e30])
+def test_act_quantize_against_exact_rational_rounding(scale):
+    """Random blocks (N(0,1) times `scale`, so that d is normal, tiny or subnormal): every d and every code equals the
+    rule evaluated in exact rational arithmetic with binary32 rounding written out (d = round32(amax / 127),
+    q = half-away(round32(x / d)))."""
+    rng = np.random.default_rng(int(abs(np.log10(scale))) + 17)
+    x = si.f32_to_bf16_bits((rng.standard_normal((4, 96)) * scale).astype(np.float32)).reshape(4, 96)
+    xq, xd = oracle.quantize_act(x)
+    xf = si.bf16_bits_to_f32(x.reshape(-1)).reshape(4, 96)
+    for r in range(4):
+        for b in range(3):
+            blk = [Fraction(float(v)) for v in xf[r, 32 * b:32 * b + 32]]
+            amax = max(abs(v) for v in blk)
+            d = _fp32_round(amax / 127)
+            assert Fraction(float(xd[r, b])) == d
+            for i, v in enumerate(blk):
+                assert int(xq[r, 32 * b + i]) == max(-127, min(127, _half_away(_fp32_round(v / d))))
+
+
+def test_act_quantize_invariants_over_every_bf16_magnitude():
+    """For every positive finite bf16 value a as a block's amax (with -a, a/3 and a small value beside it): the code
+    at +-a is +-127, every code lies in [-127, 127], and every value is within d/2 (plus the fp32 quotient's
+    rounding) of q d."""
+    mags = np.arange(1, 0x7F80, dtype=np.uint16)
+    n = mags.size
+    x = np.zeros((n, 32), dtype=np.uint16)
+    x[:, 0] = mags
+    x[:, 1] = mags | np.uint16(0x8000)
+    third = si.bf16_bits_to_f32(mags) / np.float32(3.0)
+    x[:, 2] = si.f32_to_bf16_bits(third.astype(np.float32))
+    x[:, 3] = np.uint16(1)
+    xq, xd = oracle.quantize_act(x)
+    assert np.all(xq[:, 0] == 127) and np.all(xq[:, 1] == -127)
+    assert np.abs(xq.astype(np.int64)).max() <= 127
+    xf = si.bf16_bits_to_f32(x.reshape(-1)).reshape(n, 32).astype(np.float64)
+    d = xd[:, 0].astype(np.float64)[:, None]
+    err = np.abs(xf - xq.astype(np.float64) * d)
+    assert np.all(err <= d * (0.5 + 2.0 ** -9) + 2.0 ** -149)
+
+
+def _exact_q8act(xq, xd, q, s, r, n):
+    K = xq.shape[1]
+    y = Fraction(0)
+    for b in range(K // 32):
+        inner = sum(int(xq[r, 32 * b + i]) * int(q[32 * b + i, n]) for i in range(32))
+        y += Fraction(float(s[b, n])) * Fraction(float(xd[r, b])) * inner
+    return y
+
+
+@pytest.mark.parametrize("K,N,m", [(32, 1, 1), (32, 3, 2), (64, 2, 3), (96, 33, 1)])
+def test_q8act_product_brute_force(K, N, m):
+    """Exact rational y = sum_b s d sum_i xq q for every output; the oracle's fp64 result is within a few ulps."""
+    x, q, s = si.case(m, K, N, 300 + K + N)
+    xq, xd = oracle.quantize_act(x)
+    y, a = oracle.gemv_q8act(xq, xd, q, s)
+    for r in range(m):
+        for n in range(q.shape[1]):
+            ref = _exact_q8act(xq, xd, q, s, r, n)
+            assert abs(Fraction(float(y[r, n])) - ref) <= Fraction(2) ** -50 * Fraction(float(a[r, n]))
+
+
+def test_q8act_integer_case_and_one_hot():
+    """s = d = 1: y is the integer dot sum_k xq[k] q[k, n] exactly (Python integers); a one-hot xq = c e_k gives
+    y[n] = s[k/32, n] d c q[k, n]."""
+    rng = np.random.default_rng(8)
+    K, N = 2048, 64
+    xq = rng.integers(-127, 128, size=(2, K)).astype(np.int8)
+    q = rng.integers(-127, 128, size=(K, N)).astype(np.int8)
+    ones_s = np.ones((K // 32, N), dtype=np.float32)
+    ones_d = np.ones((2, K // 32), dtype=np.float32)
+    y, _ = oracle.gemv_q8act(xq, ones_d, q, ones_s)
+    for r in range(2):
+        for n in (0, 17, 63):
+            assert y[r, n] == sum(int(xq[r, k]) * int(q[k, n]) for k in range(K))
+    _, q2, s2 = si.case(1, 256, 40, 9)
+    oh = np.zeros((1, 256), dtype=np.int8)
+    oh[0, 77] = -93
+    d = np.full((1, 8), 0.375, dtype=np.float32)
+    y2, _ = oracle.gemv_q8act(oh, d, q2, s2)
+    expect = s2[77 // 32].astype(np.float64) * 0.375 * -93 * q2[77].astype(np.float64)
+    assert np.array_equal(y2[0], expect)
+
+
+@pytest.mark.parametrize("m,K,N", [(4, 1024, 96), (16, 256, 33)])
+def test_q8act_dense_fp64_matmul(m, K, N):
+    """y = (xq d) @ (q s), the dequantized activation and weight multiplied by numpy's fp64 matmul: within 1e-12 A."""
+    x, q, s = si.case(m, K, N, 410 + m)
+    xq, xd = oracle.quantize_act(x)
+    y, a = oracle.gemv_q8act(xq, xd, q, s)
+    xdq = xq.astype(np.float64) * np.repeat(xd.astype(np.float64), 32, axis=1)
+    ref = xdq @ oracle.dequantize(q, s)
+    assert np.all(np.abs(y - ref) <= 1e-12 * a)
+
+
+def test_q8act_close_to_the_bf16_product():
+    """The quantized numerics differ from the bf16 product by at most the quantization error carried through the
+    weight: |y_q8 - y_bf16| <= sum_b |s| sum_i |x - d xq| |q| (+ fp64 rounding)."""
+    x, q, s = si.case(3, 512, 70, 420)
+    xq, xd = oracle.quantize_act(x)
+    y8, a8 = oracle.gemv_q8act(xq, xd, q, s)
+    y, a = oracle.gemv(x, q, s)
+    xf = si.bf16_bits_to_f32(x.reshape(-1)).reshape(x.shape).astype(np.float64)
+    dx = np.abs(xf - xq.astype(np.float64) * np.repeat(xd.astype(np.float64), 32, axis=1))
+    bound = dx @ np.abs(oracle.dequantize(q, s))
+    assert np.all(np.abs(y8 - y) <= bound + 1e-12 * (a + a8))
+    assert np.all(bound <= 0.02 * a + 1e-30)
+
+
+@pytest.mark.parametrize("wrong", ["row_scale_of_other_row", "no_act_scale", "block_scale_shifted", "round_to_even"])
+def test_q8act_pins_catch_planted_mistakes(wrong, monkeypatch):
+    """Wrong quantized numerics planted in the oracle fail the pins."""
+    good_q, good_p = oracle.quantize_act, oracle.gemv_q8act
+
+    def bad_product(xq, xd, q, s, cols=None):
+        xd = np.asarray(xd, dtype=np.float32)
+        if wrong == "row_scale_of_other_row":
+            xd = xd[::-1].copy()
+        elif wrong == "no_act_scale":
+            xd = np.ones_like(xd)
+        elif wrong == "block_scale_shifted":
+            xd = np.roll(xd, 1, axis=1)
+        return good_p(xq, xd, q, s, cols)
+
+    def bad_quantize(x_bits):
+        xq, xd = good_q(x_bits)
+        xf = si.bf16_bits_to_f32(np.asarray(x_bits).reshape(-1)).reshape(xq.shape).astype(np.float64)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            v = xf / np.repeat(xd.astype(np.float64), 32, axis=1)
+        return np.where(np.isfinite(v), np.clip(np.round(v), -127, 127), 0).astype(np.int8), xd
+
+    if wrong == "round_to_even":
+        monkeypatch.setattr(oracle, "quantize_act", bad_quantize)
+    else:
+        monkeypatch.setattr(oracle, "gemv_q8act", bad_product)
+    failed = 0
+    for pin in (test_act_quantize_ties_go_away_from_zero, lambda: test_q8act_product_brute_force(64, 2, 3),
+                lambda: test_q8act_dense_fp64_matmul(4, 1024, 96)):
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1
