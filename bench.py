@@ -44,6 +44,18 @@ FUSED_NOTE = ("; --fused: q/k/v read the previous layer's normed output, o and d
               "stream in place and write the next RMS norm (q8_gemv_residual_norm), gate/up is the gated pair")
 GLU_NOTE = ("; --ffn glu: gate and up as one gated-pair launch (q8_gemv_glu, SwiGLU) writing bf16 silu(gate) * up, "
             "which the down projection reads")
+Q8ACT_NOTE = ("; --act q8: every launch's activation quantized on the device first (q8_quantize_act: int8 codes and "
+              "an fp32 scale per 32 values), the products under the quantized numerics (Q8_FLAG_Q8_ACT)")
+
+
+def act_read_bytes(m, K, q8act=False):
+    """Bytes of an activation one launch reads: bf16, or the quantized form (1 byte a value + 4 bytes a 32)."""
+    return m * K * (1.125 if q8act else 2)
+
+
+def quantize_bytes(m, K):
+    """Bytes of one q8_quantize_act: the bf16 values read, the quantized form written."""
+    return m * K * (2 + 1.125)
 
 
 def layer_shapes():
@@ -152,11 +164,12 @@ class ClockSampler:
 # the reference arm and the CPU baseline: the fp64 oracle on the host cores
 # ---------------------------------------------------------------------------------------------------------------------
 
-def oracle_sample(m, budget_s, weights=None):
+def oracle_sample(m, budget_s, weights=None, q8act=False):
     """Time the oracle on the chain's GEMVs in step order until `budget_s` seconds of oracle time have run.
 
     weights: optional callable i -> (x, q, s) host arrays for GEMV i of the chain (the device's inputs copied
-    back); host draws from the seeded generator otherwise.  Returns (GB/s, description, threads)."""
+    back); host draws from the seeded generator otherwise.  q8act: each activation quantized first and the product
+    taken under the quantized numerics.  Returns (GB/s, description, threads)."""
     import oracle
     import synth_inputs as si
     shapes = chain_shapes() + [(HIDDEN, VOCAB)]
@@ -167,11 +180,17 @@ def oracle_sample(m, budget_s, weights=None):
         else:
             x, q, s = si.case(m, K, N, si.case_seed(4, m, i))
         t0 = time.perf_counter()
-        y, _ = oracle.gemv(x, q, s)
+        if q8act:
+            xq, xd = oracle.quantize_act(x)
+            y, _ = oracle.gemv_q8act(xq, xd, q, s)
+        else:
+            y, _ = oracle.gemv(x, q, s)
         if i == len(shapes) - 1:
             oracle.argmax(y, N)
         spent += time.perf_counter() - t0
         nbytes += gemv_bytes(m, K, N, argmax=(i == len(shapes) - 1))
+        if q8act:
+            nbytes += act_read_bytes(m, K, True) - act_read_bytes(m, K) + quantize_bytes(m, K)
         done += 1
         if spent >= budget_s:
             break
@@ -225,10 +244,10 @@ class Chain:
     o its own, gate and up one more (one q8_gemv_parts launch), down its own; then the tied head with its arg-max.
     Weights are stored tiled (q8_tile_device), as a model would store them once at load time."""
 
-    def __init__(self, torch, m, seed=4000, glu=False, fused=False):
+    def __init__(self, torch, m, seed=4000, glu=False, fused=False, q8act=False):
         import synth_inputs as si
         import q8_block_quantized_gemv_gb300 as q8
-        self.torch, self.m, self.glu, self.fused = torch, m, glu or fused, fused
+        self.torch, self.m, self.glu, self.fused, self.q8act = torch, m, glu or fused, fused, q8act
         self.shapes = chain_shapes()
         # row-major weights as drawn, and the tiled storage the library streams
         self.w = [si.device_weight(K, N, seed + i) for i, (K, N) in enumerate(self.shapes)]
@@ -258,8 +277,18 @@ class Chain:
             self.gammas = [0.5 + torch.rand(HIDDEN, generator=g, device="cuda") for _ in range(2 * LAYERS)]
             self.xn = [torch.empty((m, HIDDEN), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
         self.idx = torch.empty((m,), dtype=torch.int64, device="cuda")
+        # quantized activations: one buffer per width, rewritten before each launch that reads it (stream order)
+        self.xa = {K: q8.QuantAct(torch.empty((q8.act_bytes(m, K),), dtype=torch.uint8, device="cuda"), m, K)
+                   for K in (HIDDEN, FFN)} if q8act else None
         self.g_layers = self.g_head = None
         torch.cuda.synchronize()
+
+    def a(self, x):
+        """The activation a launch reads: x itself, or (--act q8) its quantized form, quantized now."""
+        if not self.q8act:
+            return x
+        import q8_block_quantized_gemv_gb300 as q8
+        return q8.quantize_act(x, out=self.xa[x.shape[1]])
 
     def layer_calls(self):
         """(activation index, [GEMV indices]) of every launch of the layers, in order."""
@@ -276,13 +305,13 @@ class Chain:
             return self.run_fused_layers()
         for xi, gis in self.layer_calls():
             if self.glu and len(gis) == 2:  # gate, up -> h
-                q8.gemv_glu(self.x[xi], self.wt[gis[0]], self.wt[gis[1]], FFN, out_bf16=self.h, want=(),
+                q8.gemv_glu(self.a(self.x[xi]), self.wt[gis[0]], self.wt[gis[1]], FFN, out_bf16=self.h, want=(),
                             constant_weights=True)
             elif self.glu and self.shapes[gis[0]] == (FFN, HIDDEN):  # down reads h
-                q8.gemv_parts(self.h, [(self.wt[gis[0]][0], self.wt[gis[0]][1], HIDDEN)], ys=[self.y[gis[0]]],
-                              constant_weights=True, tiled=True)
+                q8.gemv_parts(self.a(self.h), [(self.wt[gis[0]][0], self.wt[gis[0]][1], HIDDEN)],
+                              ys=[self.y[gis[0]]], constant_weights=True, tiled=True)
             else:
-                q8.gemv_parts(self.x[xi], [(self.wt[i][0], self.wt[i][1], self.shapes[i][1]) for i in gis],
+                q8.gemv_parts(self.a(self.x[xi]), [(self.wt[i][0], self.wt[i][1], self.shapes[i][1]) for i in gis],
                               ys=[self.y[i] for i in gis], constant_weights=True, tiled=True)
 
     def run_fused_layers(self):
@@ -294,21 +323,21 @@ class Chain:
         for layer in range(LAYERS):
             base, xb = 7 * layer, 4 * layer
             x_in = self.x[xb] if layer == 0 else self.xn[1]
-            q8.gemv_parts(x_in, [(self.wt[i][0], self.wt[i][1], HIDDEN) for i in (base, base + 1, base + 2)],
+            q8.gemv_parts(self.a(x_in), [(self.wt[i][0], self.wt[i][1], HIDDEN) for i in (base, base + 1, base + 2)],
                           ys=[self.y[base], self.y[base + 1], self.y[base + 2]], constant_weights=True, tiled=True)
-            q8.gemv_residual_norm(self.x[xb + 1], self.wt[base + 3][0], self.wt[base + 3][1], HIDDEN, self.res,
-                                  self.gammas[2 * layer], 1e-6, h=self.res, out_bf16=self.xn[0],
+            q8.gemv_residual_norm(self.a(self.x[xb + 1]), self.wt[base + 3][0], self.wt[base + 3][1], HIDDEN,
+                                  self.res, self.gammas[2 * layer], 1e-6, h=self.res, out_bf16=self.xn[0],
                                   constant_weights=True)
-            q8.gemv_glu(self.xn[0], self.wt[base + 4], self.wt[base + 5], FFN, out_bf16=self.h, want=(),
+            q8.gemv_glu(self.a(self.xn[0]), self.wt[base + 4], self.wt[base + 5], FFN, out_bf16=self.h, want=(),
                         constant_weights=True)
-            q8.gemv_residual_norm(self.h, self.wt[base + 6][0], self.wt[base + 6][1], HIDDEN, self.res,
+            q8.gemv_residual_norm(self.a(self.h), self.wt[base + 6][0], self.wt[base + 6][1], HIDDEN, self.res,
                                   self.gammas[2 * layer + 1], 1e-6, h=self.res, out_bf16=self.xn[1],
                                   constant_weights=True)
 
     def run_head(self):
         import q8_block_quantized_gemv_gb300 as q8
         q, s = self.head_t
-        q8.gemv_argmax(self.x[-1], q, s, VOCAB, idx=self.idx, constant_weights=True, tiled=True)
+        q8.gemv_argmax(self.a(self.x[-1]), q, s, VOCAB, idx=self.idx, constant_weights=True, tiled=True)
 
     def capture(self):
         torch = self.torch
@@ -327,14 +356,23 @@ class Chain:
         torch.cuda.synchronize()
 
     def launches_per_step(self):
-        return len(self.layer_calls()) + 2  # the layers' launches, the head's GEMV kernel and its index decode
+        # the layers' launches, the head's GEMV kernel and its index decode (and, --act q8, one quantize a launch)
+        n = len(self.layer_calls()) + 2
+        return n + (len(self.layer_calls()) + 1 if self.q8act else 0)
+
+    def head_bytes(self):
+        m = self.m
+        return (gemv_bytes(m, HIDDEN, VOCAB, argmax=True) + (act_read_bytes(m, HIDDEN, True) - act_read_bytes(m, HIDDEN)
+                + quantize_bytes(m, HIDDEN) if self.q8act else 0.0))
 
     def layer_bytes(self):
         """Algorithmic bytes of the layers' launches: weights, each activation once, outputs."""
         m = self.m
         total = 0.0
         for xi, gis in self.layer_calls():
-            total += m * self.x_shapes[xi] * 2
+            total += act_read_bytes(m, self.x_shapes[xi], self.q8act)
+            if self.q8act:
+                total += quantize_bytes(m, self.x_shapes[xi])
             for i in gis:
                 K, N = self.shapes[i]
                 total += K * padded(N) * 1.125 + m * padded(N) * 4
@@ -353,7 +391,7 @@ def run_ours(args, rank, world, local_rank):
     build.build()
     torch.cuda.set_device(local_rank)
     m = args.m
-    chain = Chain(torch, m, glu=args.ffn == "glu", fused=args.fused)
+    chain = Chain(torch, m, glu=args.ffn == "glu", fused=args.fused, q8act=args.act == "q8")
     chain.capture()
     stream = torch.cuda.current_stream()
 
@@ -393,7 +431,7 @@ def run_ours(args, rank, world, local_rank):
     layers_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     head_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     ms = max_over_ranks(ms)
-    bytes_step = chain.layer_bytes() + gemv_bytes(m, HIDDEN, VOCAB, argmax=True)
+    bytes_step = chain.layer_bytes() + chain.head_bytes()
     value = world * bytes_step / (ms * 1e-3) / 1e9
 
     # ---- end-to-end: host activations in, the step's tokens out, every step ----
@@ -427,7 +465,9 @@ def run_ours(args, rank, world, local_rank):
     try:
         with open(PROFILE_TRAFFIC) as f:
             rec = json.load(f)
-        if rec.get("source_hash") == source_hash():
+        # the capture covers the default step (bf16 activations, two-output gate/up, no fused epilogues)
+        default_step = not (chain.q8act or chain.glu or chain.fused)
+        if rec.get("source_hash") == source_hash() and default_step:
             traffic = rec.get("by_m", {}).get(str(m), {}).get("traffic_bytes_per_launch")
     except (OSError, ValueError):
         pass
@@ -437,16 +477,20 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD + (FUSED_NOTE if args.fused else GLU_NOTE if args.ffn == "glu" else ""), "m": m,
+        "config": {"workload": WORKLOAD + (FUSED_NOTE if args.fused else GLU_NOTE if args.ffn == "glu" else "")
+                   + (Q8ACT_NOTE if chain.q8act else ""), "m": m,
                    "gemvs_per_step": len(chain.shapes) + 1,
                    "launches_per_step": chain.launches_per_step(),
                    "bytes_per_step": bytes_step, "us_per_gemv": ms * 1e3 / (len(chain.shapes) + 1),
                    "pct_of_8TBps": 100.0 * bytes_step / (ms * 1e-3) / 8e12,
                    "layers_ms": layers_ms, "head_ms": head_ms,
-                   "operands": "x bf16, W Q8_0 (int8 + fp32 scale per 32 rows), fp32 accumulation",
+                   "operands": ("x int8 + fp32 scale per 32 values (quantized on the device), W Q8_0 (int8 + fp32 "
+                                "scale per 32 rows), exact integer block sums, fp32 fold" if chain.q8act else
+                                "x bf16, W Q8_0 (int8 + fp32 scale per 32 rows), fp32 accumulation"),
                    "l2": "inputs larger than L2 (9.4 GB of weights per step against 129 MB)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "q8 stream kernel (the 128 layer launches of a step, back to back)",
+        "roofline": {"bound": "hbm", "kernel": "q8 stream kernel (the 128 layer launches of a step, back to back)"
+                     + (", with their activation quantizer launches" if chain.q8act else ""),
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": layer_bytes / n_layer_launches,
@@ -465,7 +509,7 @@ def run_ours(args, rank, world, local_rank):
                 q, s = chain.head
                 xi = len(chain.x) - 1
             return (chain.x[xi].view(torch.int16).cpu().numpy().view("uint16"), q.cpu().numpy(), s.cpu().numpy())
-        gbs, desc, cores, _ = oracle_sample(m, args.cpu_budget, host_case)
+        gbs, desc, cores, _ = oracle_sample(m, args.cpu_budget, host_case, q8act=chain.q8act)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -571,6 +615,9 @@ def main():
                     help="the layers' gate/up launch: two fp32 outputs (default) or the fused gated pair")
     ap.add_argument("--fused", action="store_true",
                     help="the layers with every fusion: residual add + RMS norm after o and down, the gated pair")
+    ap.add_argument("--act", choices=["bf16", "q8"], default="bf16",
+                    help="activations as bf16 (default) or quantized on the device before each launch (int8 + scale "
+                         "per 32, the quantized numerics)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step: µs/call of the single-GEMV workloads, one JSON line each")
     ap.add_argument("--sweep-m", default="1,2,4,8,16", help="row counts of --sweep")

@@ -85,8 +85,15 @@ q8_status q8_gemv(const void *x, const int8_t *q, const float *s, float *y, int 
 #define Q8_FLAG_TILED 2u            /* q and s are in the tiled layout of q8_tile (below), not row-major; read by the
                                        per-warp cp.async streaming kernel (variant must be AUTO) */
 
+#define Q8_FLAG_Q8_ACT 4u           /* x is the quantized form of the activation written by q8_quantize_act (below),
+                                       not bf16 values, and the product is the quantized numerics'
+                                           y[r, n] = sum_b s[b, n] * d[r, b] * sum_i xq[r, 32b+i] * q[32b+i, n]
+                                       (its integer inner sums exact); requires Q8_FLAG_TILED.  Every product entry
+                                       point takes it; the bound is as before with xq * d in place of x */
+
 /* q8_gemv with an explicit kernel family (q8_variant) and flags (Q8_FLAG_*; 0 for none).  Same arguments and
- * bound; Q8_ERR_ARG for an unknown variant or flag, or for Q8_FLAG_TILED with a variant other than AUTO. */
+ * bound; Q8_ERR_ARG for an unknown variant or flag, for Q8_FLAG_TILED with a variant other than AUTO, or for
+ * Q8_FLAG_Q8_ACT without Q8_FLAG_TILED. */
 q8_status q8_gemv_ex(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N, int variant,
                      unsigned int flags, q8_stream_t stream);
 
@@ -186,6 +193,25 @@ typedef struct q8_part {
  * launch each.  Flags and errors as q8_gemv_ex; an output overlapping x, a weight or another output is Q8_ERR_ARG. */
 q8_status q8_gemv_parts(const void *x, const q8_part *parts, int nparts, int m, int K, unsigned int flags,
                         q8_stream_t stream);
+
+/* The quantized form of an activation (source: "plan.rs", `QBLOCK`: the values of an activation's quantized form
+ * that share one scale, 32; `Buffer::quantized`: int8 values and a scale per 32; `Launch::projected_input`: a product
+ * by checkpoint rows reads its activation quantized under every numerics but the precise one).  One buffer of
+ * q8_act_bytes(m, K) bytes:
+ *   values  int8 [m][K]      at byte 0
+ *   scales  fp32 [m][K/32]   at byte m * K (16-byte aligned when the buffer is, since K % 32 == 0)
+ * The pages fix the form but not its rounding; the rule here is the weight rule of "from_q8.rs" `quantize`
+ * (d = amax / 127, q = round(x / d)) in fp32: for each row and block of 32 values, amax = max |x|,
+ * d = amax / 127 and q = x / d rounded half away from zero, both quotients IEEE fp32 (round to nearest even,
+ * subnormals kept), q clamped to [-127, 127] (a guard: for bf16 input |x / d| <= 127 * (1 + 2^-10)).  A block of
+ * zeros gets d = 0 and q = 0; a block holding inf or NaN gets d = NaN and q = 0, so every product over it is NaN. */
+int64_t q8_act_bytes(int m, int K); /* m * K + m * (K / 32) * 4; -1 when m < 1, K <= 0 or K % 32 != 0 */
+
+/* Device: quantize x into xa, enqueued on `stream` (asynchronous; errors as q8_gemv).
+ *   x   device, bf16 [m][K] row-major, 16-byte aligned
+ *   xa  device, q8_act_bytes(m, K) bytes (written), 16-byte aligned, not overlapping x
+ * Any m >= 1 (not limited to 16). */
+q8_status q8_quantize_act(const void *x, void *xa, int m, int K, q8_stream_t stream);
 
 /* Host repack of checkpoint blocks into the two stored tensors (source: "from_q8.rs", `Q8Part`: the host repacks the
  * checkpoint's blocks into the int8 values `q8_0.values` and the fp32 scales `q8_0.scales`).

@@ -202,13 +202,19 @@ def silu(g: np.ndarray) -> np.ndarray:
         return g / (1.0 + np.exp(-g))
 
 
-def glu(x_bits: np.ndarray, qg: np.ndarray, sg: np.ndarray, qu: np.ndarray, su: np.ndarray, cols=None):
+def _product(x_bits, q, s, cols=None, act=None):
+    """:func:`gemv` of bf16 x, or :func:`gemv_q8act` of the quantized activation ``act`` = (xq, xd) when given."""
+    return gemv(x_bits, q, s, cols) if act is None else gemv_q8act(act[0], act[1], q, s, cols)
+
+
+def glu(x_bits: np.ndarray, qg: np.ndarray, sg: np.ndarray, qu: np.ndarray, su: np.ndarray, cols=None, act=None):
     """The gated pair of ``plan.rs`` ``Launch::GemvGlu`` (SwiGLU, no biases): out = silu(x.Wg) * (x.Wu), fp64.
 
     Returns (out, g, u, a_g, a_u): the two products and their error scales as :func:`gemv` returns them, for the
-    bound a GPU result is judged by."""
-    g, a_g = gemv(x_bits, qg, sg, cols)
-    u, a_u = gemv(x_bits, qu, su, cols)
+    bound a GPU result is judged by.  ``act`` = (xq, xd): the products of the quantized activation instead
+    (:func:`gemv_q8act`; x_bits is then unused)."""
+    g, a_g = _product(x_bits, qg, sg, cols, act)
+    u, a_u = _product(x_bits, qu, su, cols, act)
     return silu(g) * u, g, u, a_g, a_u
 
 
@@ -223,12 +229,13 @@ def rmsnorm(h: np.ndarray, gamma: np.ndarray, eps: float, N: int) -> np.ndarray:
 
 
 def residual_norm(x_bits: np.ndarray, q: np.ndarray, s: np.ndarray, residual: np.ndarray, gamma: np.ndarray,
-                  eps: float, N: int):
+                  eps: float, N: int, act=None):
     """A projection folded with the residual add and the next norm (``plan.rs`` ``Launch::Fold`` /
     ``gemv_norm_epilogue``): h = residual + x.W (each output as :func:`gemv`), out = rmsnorm(h) * gamma.
 
-    Returns (h, out, y, a): the new residual stream, the normed activation, the product and its error scale."""
-    y, a = gemv(x_bits, q, s)
+    Returns (h, out, y, a): the new residual stream, the normed activation, the product and its error scale.
+    ``act`` = (xq, xd): the product of the quantized activation instead (:func:`gemv_q8act`)."""
+    y, a = _product(x_bits, q, s, None, act)
     h = np.asarray(residual, dtype=np.float64)[:, : y.shape[1]] + y
     h[:, N:] = 0.0
     return h, rmsnorm(h, gamma, eps, N), y, a

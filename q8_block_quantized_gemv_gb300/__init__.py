@@ -7,6 +7,9 @@ C++ host code (repack, quantize).  PyTorch supplies device memory and streams.  
 * :func:`gemv` -- ``q8_gemv`` / ``q8_gemv_ex``: y[r, n] = sum_b s[b, n] sum_i x[r, 32b+i] q[32b+i, n]
   ("from_q8.rs", module doc), bf16 x [m, K], int8 q [K, Np], fp32 s [K/32, Np] -> fp32 y [m, Np];
 * :func:`gemv_argmax` -- ``q8_gemv_argmax``: the product and the first-maximum arg-max that closes a decode step;
+* :func:`quantize_act` -- ``q8_quantize_act``: the quantized form of an activation (int8 values and an fp32 scale per
+  32, "plan.rs" ``QBLOCK``); every product function takes the :class:`QuantAct` it returns in place of bf16 x
+  (``Q8_FLAG_Q8_ACT``, tiled weights);
 * :func:`repack` -- ``q8_repack``: 36-byte checkpoint blocks -> (q, s) on the host;
 * :func:`quantize` -- ``q8_quantize``: the Q8_0 rule of "from_q8.rs" ``quantize`` on the host.
 
@@ -48,6 +51,8 @@ SIGNATURES = {
     "q8_gemv_parts": (_I, [_P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_gemv_glu": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_gemv_residual_norm": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
+    "q8_act_bytes": (ctypes.c_int64, [_I, _I]),
+    "q8_quantize_act": (_I, [_P, _P, _I, _I, _P]),
 }
 
 
@@ -110,17 +115,79 @@ def tiled_n(N: int) -> int:
     return lib().q8_tiled_n(N)
 
 
+class QuantAct:
+    """The quantized form of an activation (q8_quantize_act): one uint8 CUDA buffer of ``act_bytes(m, K)`` bytes
+    holding int8 values [m, K] followed by fp32 scales [m, K/32].  Pass it as ``x`` to any product function (tiled
+    weights only)."""
+
+    def __init__(self, buf, m: int, K: int):
+        self.buf, self.shape = buf, (m, K)
+
+    @property
+    def device(self):
+        return self.buf.device
+
+    @property
+    def is_cuda(self):
+        return self.buf.is_cuda
+
+    def data_ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def values(self):
+        """int8 [m, K] view of the codes."""
+        import torch
+        m, K = self.shape
+        return self.buf[: m * K].view(torch.int8).view(m, K)
+
+    def scales(self):
+        """fp32 [m, K/32] view of the scales."""
+        import torch
+        m, K = self.shape
+        return self.buf[m * K:].view(torch.float32).view(m, K // Q8_BLOCK)
+
+
+def act_bytes(m: int, K: int) -> int:
+    return int(lib().q8_act_bytes(m, K))
+
+
+def quantize_act(x, out: QuantAct | None = None, stream=None) -> QuantAct:
+    """bf16 x [m, K] (CUDA, contiguous) -> its quantized form (q8_quantize_act)."""
+    import torch
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D bfloat16 CUDA tensor")
+    m, K = x.shape
+    nbytes = act_bytes(m, K)
+    if nbytes < 0:
+        raise ValueError("K must be a positive multiple of 32")
+    if out is None:
+        out = QuantAct(torch.empty((nbytes,), dtype=torch.uint8, device=x.device), m, K)
+    elif out.shape != (m, K) or out.buf.numel() != nbytes:
+        raise ValueError("out must be a QuantAct of the same shape")
+    _check(lib().q8_quantize_act(x.data_ptr(), out.data_ptr(), m, K, _stream_handle(stream)), "q8_quantize_act")
+    return out
+
+
 def _check_operands(x, q, s, N, tiled=False):
     import torch
-    if not (x.is_cuda and q.is_cuda and s.is_cuda):
-        raise ValueError("x, q and s must be CUDA tensors")
-    if x.dtype != torch.bfloat16 or q.dtype != torch.int8 or s.dtype != torch.float32:
-        raise TypeError("x must be bfloat16, q int8 and s float32")
-    if not (x.is_contiguous() and q.is_contiguous() and s.is_contiguous()):
-        raise ValueError("x, q and s must be contiguous")
-    if x.dim() != 2:
-        raise ValueError("x must be 2-D [m, K]")
-    m, K = x.shape
+    if isinstance(x, QuantAct):
+        if not tiled:
+            raise ValueError("a quantized activation takes tiled weights")
+        if not (q.is_cuda and s.is_cuda and x.is_cuda):
+            raise ValueError("x, q and s must be CUDA tensors")
+        if q.dtype != torch.int8 or s.dtype != torch.float32 or not (q.is_contiguous() and s.is_contiguous()):
+            raise TypeError("q must be contiguous int8 and s contiguous float32")
+        m, K = x.shape
+    else:
+        if not (x.is_cuda and q.is_cuda and s.is_cuda):
+            raise ValueError("x, q and s must be CUDA tensors")
+        if x.dtype != torch.bfloat16 or q.dtype != torch.int8 or s.dtype != torch.float32:
+            raise TypeError("x must be bfloat16, q int8 and s float32")
+        if not (x.is_contiguous() and q.is_contiguous() and s.is_contiguous()):
+            raise ValueError("x, q and s must be contiguous")
+        if x.dim() != 2:
+            raise ValueError("x must be 2-D [m, K]")
+        m, K = x.shape
     Np = padded_n(N) if N > 0 else -1
     if tiled:
         Nt = tiled_n(N) if N > 0 else -1
@@ -133,10 +200,12 @@ def _check_operands(x, q, s, N, tiled=False):
 
 FLAG_CONSTANT_WEIGHTS = 1
 FLAG_TILED = 2
+FLAG_Q8_ACT = 4
 
 
-def _flags(constant_weights, tiled):
-    return (FLAG_CONSTANT_WEIGHTS if constant_weights else 0) | (FLAG_TILED if tiled else 0)
+def _flags(constant_weights, tiled, x=None):
+    return ((FLAG_CONSTANT_WEIGHTS if constant_weights else 0) | (FLAG_TILED if tiled else 0)
+            | (FLAG_Q8_ACT if isinstance(x, QuantAct) else 0))
 
 
 def gemv(x, q, s, N: int, y=None, variant: str = "auto", constant_weights: bool = False, tiled: bool = False,
@@ -153,7 +222,7 @@ def gemv(x, q, s, N: int, y=None, variant: str = "auto", constant_weights: bool 
     elif y.dtype != torch.float32 or y.shape != (m, Np) or not y.is_contiguous() or not y.is_cuda:
         raise ValueError("y must be a contiguous fp32 CUDA tensor [m, Np]")
     _check(lib().q8_gemv_ex(x.data_ptr(), q.data_ptr(), s.data_ptr(), y.data_ptr(), m, K, N, VARIANTS[variant],
-                            _flags(constant_weights, tiled), _stream_handle(stream)), "q8_gemv")
+                            _flags(constant_weights, tiled, x), _stream_handle(stream)), "q8_gemv")
     return y
 
 
@@ -175,7 +244,7 @@ def gemv_argmax(x, q, s, N: int, idx=None, logits=None, constant_weights: bool =
             raise ValueError("logits must be a contiguous fp32 CUDA tensor [m, Np]")
         lp = logits.data_ptr()
     _check(lib().q8_gemv_argmax_ex(x.data_ptr(), q.data_ptr(), s.data_ptr(), idx.data_ptr(), lp, m, K, N,
-                                   _flags(constant_weights, tiled), _stream_handle(stream)), "q8_gemv_argmax")
+                                   _flags(constant_weights, tiled, x), _stream_handle(stream)), "q8_gemv_argmax")
     return idx
 
 
@@ -222,7 +291,7 @@ def gemv_parts(x, weights, ys=None, constant_weights: bool = False, tiled: bool 
         arr[i] = _Part(q.data_ptr(), s.data_ptr(), y.data_ptr(), N)
         outs.append(y)
     _check(lib().q8_gemv_parts(x.data_ptr(), ctypes.cast(arr, ctypes.c_void_p), len(weights), m, K,
-                               _flags(constant_weights, tiled), _stream_handle(stream)), "q8_gemv_parts")
+                               _flags(constant_weights, tiled, x), _stream_handle(stream)), "q8_gemv_parts")
     return outs
 
 
@@ -247,7 +316,7 @@ def gemv_glu(x, gate, up, N: int, out=None, out_bf16=None, want=("f32",), consta
     _check(lib().q8_gemv_glu(x.data_ptr(), gate[0].data_ptr(), gate[1].data_ptr(), up[0].data_ptr(),
                              up[1].data_ptr(), out.data_ptr() if out is not None else None,
                              out_bf16.data_ptr() if out_bf16 is not None else None, m, K, N,
-                             _flags(constant_weights, True), _stream_handle(stream)), "q8_gemv_glu")
+                             _flags(constant_weights, True, x), _stream_handle(stream)), "q8_gemv_glu")
     return out, out_bf16
 
 
@@ -268,7 +337,7 @@ def gemv_residual_norm(x, q, s, N: int, residual, gamma, eps: float, h=None, out
         out_bf16 = torch.empty((m, Np), dtype=torch.bfloat16, device=x.device)
     _check(lib().q8_gemv_residual_norm(x.data_ptr(), q.data_ptr(), s.data_ptr(), residual.data_ptr(),
                                        gamma.data_ptr(), float(eps), h.data_ptr(), out_bf16.data_ptr(), m, K, N,
-                                       _flags(constant_weights, True), _stream_handle(stream)),
+                                       _flags(constant_weights, True, x), _stream_handle(stream)),
            "q8_gemv_residual_norm")
     return h, out_bf16
 

@@ -141,6 +141,18 @@ q8_status check_gemv_args(const void *x, const int8_t *q, const float *s, int m,
 
 int tiles_of(int N) { return (N + q8::kTmaColumns - 1) / q8::kTmaColumns; }
 
+constexpr unsigned kKnownFlags = Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED | Q8_FLAG_Q8_ACT;
+
+// Flags a product entry point takes: the known ones, the quantized activation only over the tiled storage.
+bool flags_ok(unsigned flags) {
+    return (flags & ~kKnownFlags) == 0 && (!(flags & Q8_FLAG_Q8_ACT) || (flags & Q8_FLAG_TILED));
+}
+
+// Bytes of the activation operand: bf16 [m][K], or the quantized form (int8 [m][K] and fp32 [m][K/32]).
+size_t x_bytes(unsigned flags, int m, int K) {
+    return (flags & Q8_FLAG_Q8_ACT) ? (size_t)q8_act_bytes(m, K) : (size_t)m * K * 2;
+}
+
 q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStream_t stream,
               const q8::Parts *parts = nullptr) {
     const int epi = argmax ? q8::kEpiArgmax : q8::kEpiStore;
@@ -162,7 +174,8 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
     Args b = a;
     b.ksplit = p.ksplit;
     const bool prefetch = (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0;
-    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, epi, stream, true, prefetch)
+    const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
+    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, epi, stream, true, prefetch, qact)
                      : p.variant == Q8_VARIANT_TMA  ? q8::launch_tma(b, argmax, stream, true, prefetch)
                      : p.variant == Q8_VARIANT_SIMT ? q8::launch_simt(b, p.V, argmax, stream)
                                                     : q8::launch_mma(b, p.V, argmax, stream);
@@ -187,14 +200,14 @@ extern "C" q8_status q8_gemv_ex(const void *x, const int8_t *q, const float *s, 
     if (st != Q8_OK) return st;
     if (!y) return Q8_ERR_ARG;
     if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_TMA) return Q8_ERR_ARG;
-    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if (!flags_ok(flags)) return Q8_ERR_ARG;
     if ((flags & Q8_FLAG_TILED) && variant != Q8_VARIANT_AUTO) return Q8_ERR_ARG;
     if ((flags & Q8_FLAG_TILED) && q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
     if (!aligned(y, 16)) return Q8_ERR_ALIGN;
     const int Np = q8_padded_n(N);
     const size_t wcols = (flags & Q8_FLAG_TILED) ? (size_t)q8_tiled_n(N) : (size_t)Np;
     const size_t ybytes = (size_t)m * Np * 4;
-    if (overlaps(y, ybytes, x, (size_t)m * K * 2) || overlaps(y, ybytes, q, (size_t)K * wcols) ||
+    if (overlaps(y, ybytes, x, x_bytes(flags, m, K)) || overlaps(y, ybytes, q, (size_t)K * wcols) ||
         overlaps(y, ybytes, s, (size_t)(K / Q8_BLOCK) * wcols * 4))
         return Q8_ERR_ARG;
     Args a = {static_cast<const uint16_t *>(x), q, s, y, nullptr, m, K, N, Np, K / Q8_BLOCK, 1};
@@ -211,18 +224,19 @@ extern "C" q8_status q8_gemv_argmax_ex(const void *x, const int8_t *q, const flo
     q8_status st = check_gemv_args(x, q, s, m, K, N);
     if (st != Q8_OK) return st;
     if (!idx) return Q8_ERR_ARG;
-    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if (!flags_ok(flags)) return Q8_ERR_ARG;
     if ((flags & Q8_FLAG_TILED) && q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
     if (!aligned(idx, 8) || (logits && !aligned(logits, 16))) return Q8_ERR_ALIGN;
     const int Np = q8_padded_n(N);
     const size_t wcols = (flags & Q8_FLAG_TILED) ? (size_t)q8_tiled_n(N) : (size_t)Np;
     if (logits) {
         const size_t ybytes = (size_t)m * Np * 4;
-        if (overlaps(logits, ybytes, x, (size_t)m * K * 2) || overlaps(logits, ybytes, q, (size_t)K * wcols) ||
+        if (overlaps(logits, ybytes, x, x_bytes(flags, m, K)) || overlaps(logits, ybytes, q, (size_t)K * wcols) ||
             overlaps(logits, ybytes, s, (size_t)(K / Q8_BLOCK) * wcols * 4) ||
             overlaps(logits, ybytes, idx, (size_t)m * 8))
             return Q8_ERR_ARG;
     }
+    if (overlaps(idx, (size_t)m * 8, x, x_bytes(flags, m, K))) return Q8_ERR_ARG;
     cudaStream_t cs = (cudaStream_t)stream;
     cudaError_t ce = cudaMemsetAsync(idx, 0, (size_t)m * sizeof(int64_t), cs);
     if (ce != cudaSuccess) return cuda_fail(ce);
@@ -248,7 +262,7 @@ extern "C" q8_status q8_gemv_parts(const void *x, const q8_part *parts, int npar
                                    unsigned int flags, q8_stream_t stream) {
     if (!x || !parts) return Q8_ERR_ARG;
     if (nparts < 1 || nparts > Q8_MAX_PARTS) return Q8_ERR_ARG;
-    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if (!flags_ok(flags)) return Q8_ERR_ARG;
     const bool tiled = (flags & Q8_FLAG_TILED) != 0;
     for (int i = 0; i < nparts; ++i) {
         const q8_part &p = parts[i];
@@ -261,7 +275,7 @@ extern "C" q8_status q8_gemv_parts(const void *x, const q8_part *parts, int npar
     // No output may overlap the activation, any weight or any other output.
     for (int i = 0; i < nparts; ++i) {
         const size_t ybytes = (size_t)m * q8_padded_n(parts[i].N) * 4;
-        if (overlaps(parts[i].y, ybytes, x, (size_t)m * K * 2)) return Q8_ERR_ARG;
+        if (overlaps(parts[i].y, ybytes, x, x_bytes(flags, m, K))) return Q8_ERR_ARG;
         for (int j = 0; j < nparts; ++j) {
             const size_t wcols = tiled ? (size_t)q8_tiled_n(parts[j].N) : (size_t)q8_padded_n(parts[j].N);
             if (overlaps(parts[i].y, ybytes, parts[j].q, (size_t)K * wcols) ||
@@ -325,7 +339,7 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
     st = check_gemv_args(x, qu, su, m, K, N);
     if (st != Q8_OK) return st;
     if (!out && !out_bf16) return Q8_ERR_ARG;
-    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if (!flags_ok(flags)) return Q8_ERR_ARG;
     if (!(flags & Q8_FLAG_TILED)) return Q8_ERR_ARG;  // the gated pair runs on the tiled storage only
     if (q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
     if ((out && !aligned(out, 16)) || (out_bf16 && !aligned(out_bf16, 16))) return Q8_ERR_ALIGN;
@@ -335,7 +349,7 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
     const void *outs[2] = {out, out_bf16};
     for (int o = 0; o < 2; ++o) {
         if (!outs[o]) continue;
-        if (overlaps(outs[o], obytes[o], x, (size_t)m * K * 2) ||
+        if (overlaps(outs[o], obytes[o], x, x_bytes(flags, m, K)) ||
             overlaps(outs[o], obytes[o], qg, (size_t)K * wcols) || overlaps(outs[o], obytes[o], qu, (size_t)K * wcols) ||
             overlaps(outs[o], obytes[o], sg, (size_t)(K / Q8_BLOCK) * wcols * 4) ||
             overlaps(outs[o], obytes[o], su, (size_t)(K / Q8_BLOCK) * wcols * 4))
@@ -359,7 +373,7 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
               static_cast<uint16_t *>(out_bf16)};
     a.ksplit = plan_glu(tiles, K / Q8_BLOCK, sms);
     cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true,
-                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0);
+                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0, (flags & Q8_FLAG_Q8_ACT) != 0);
     if (ce != cudaSuccess) return cuda_fail(ce);
     return Q8_OK;
 }
@@ -370,7 +384,7 @@ extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const
     q8_status st = check_gemv_args(x, q, s, m, K, N);
     if (st != Q8_OK) return st;
     if (!residual || !gamma || !h || !out_bf16) return Q8_ERR_ARG;
-    if (flags & ~(Q8_FLAG_CONSTANT_WEIGHTS | Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if (!flags_ok(flags)) return Q8_ERR_ARG;
     if (!(flags & Q8_FLAG_TILED)) return Q8_ERR_ARG;  // the tiled storage only
     if (!(eps >= 0.0f) || !(eps < INFINITY)) return Q8_ERR_ARG;
     if (q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
@@ -381,7 +395,7 @@ extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const
     // h may be the residual itself (in place) but may not overlap it otherwise, nor any other operand.
     if (h != residual && overlaps(h, hbytes, residual, hbytes)) return Q8_ERR_ARG;
     const void *ins[4] = {x, q, s, gamma};
-    const size_t inb[4] = {(size_t)m * K * 2, (size_t)K * wcols, (size_t)(K / Q8_BLOCK) * wcols * 4, (size_t)Np * 4};
+    const size_t inb[4] = {x_bytes(flags, m, K), (size_t)K * wcols, (size_t)(K / Q8_BLOCK) * wcols * 4, (size_t)Np * 4};
     for (int i = 0; i < 4; ++i)
         if (overlaps(h, hbytes, ins[i], inb[i]) || overlaps(out_bf16, obytes, ins[i], inb[i])) return Q8_ERR_ARG;
     if (overlaps(out_bf16, obytes, h, hbytes) || overlaps(out_bf16, obytes, residual, hbytes)) return Q8_ERR_ARG;
@@ -403,7 +417,7 @@ extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const
     const Plan p = make_plan(m, K, Np, Q8_VARIANT_AUTO, true, sms, pt.tile_end[0]);
     a.ksplit = p.ksplit;
     cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiNorm, (cudaStream_t)stream, true,
-                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0);
+                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0, (flags & Q8_FLAG_Q8_ACT) != 0);
     if (ce != cudaSuccess) return cuda_fail(ce);
     return Q8_OK;
 }

@@ -48,9 +48,10 @@ cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl
 // Defined in q8_stream.cu (the tiled layout).
 int stream_ctas_per_sm(int m);
 int stream_max_clusters(int ks);  // clusters of ks stream-kernel CTAs resident at once on this device (0: unknown)
-// epi: kEpiStore, kEpiArgmax or kEpiGlu (parts 0 and 1 the gate and up weights, grid x = 2 * tiles).
+// epi: kEpiStore, kEpiArgmax, kEpiGlu (parts 0 and 1 the gate and up weights, grid x = 2 * tiles) or kEpiNorm.
+// qact: a.x is a quantized activation (int8 values [m][K], then fp32 scales [m][K/32]) instead of bf16 values.
 cudaError_t launch_stream(const Args &a, const Parts &parts, int epi, cudaStream_t stream, bool pdl,
-                          bool prefetch_weights);
+                          bool prefetch_weights, bool qact);
 cudaError_t read_fault_word(unsigned *out, bool clear);
 constexpr unsigned kNormCounters = 64;  // residual-norm launches that may be in flight at once
 unsigned int *norm_counter(unsigned slot);  // device address of completion counter `slot` (null on a CUDA error)

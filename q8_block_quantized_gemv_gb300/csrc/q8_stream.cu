@@ -69,6 +69,12 @@ __device__ __forceinline__ uint2 ld_cg_u2(const void *p) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_cg_u32(const void *p) {
+    uint32_t v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 // fp32 pairs in one 64-bit register pair.
 __device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
     unsigned long long d;
@@ -301,7 +307,10 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
     }
 }
 
-template <bool ROWS16, int EPI>
+// QACT: x is a quantized activation (int8 values [m][K], then fp32 scales [m][K/32]); each block's A fragments are its
+// int8 codes as exact fp16, its integer sums are exact in the fp32 accumulators (|sum| <= 32 * 127 * 127 < 2^24),
+// and its factor per activation row is that row's scale d.
+template <bool ROWS16, int EPI, bool QACT = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
     stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     constexpr int MR = ROWS16 ? 16 : 8;
@@ -343,22 +352,36 @@ __global__ void __launch_bounds__(kThreadsS, 2)
         }
     }
 
-    // The lane's activations x[g + 8i][32b + 16s + 4t .. + 3] (rows at or past m are zeros).
+    // The lane's activations x[g + 8i][32b + 16s + 4t .. + 3] (rows at or past m are zeros).  QACT: [i][0] holds the
+    // two int8 words (s = 0, 1) and [i][1].x the bits of the row's block scale.
     const uint16_t *xrow[NR];
+    const unsigned char *qrow[NR];
+    const float *drow[NR];
     bool xlive[NR];
 #pragma unroll
     for (int i = 0; i < NR; ++i) {
         const int r = g + 8 * i;
         xlive[i] = r < a.m;
-        xrow[i] = a.x + (size_t)(xlive[i] ? r : 0) * a.K + 4 * t;
+        const size_t rr = (size_t)(xlive[i] ? r : 0);
+        xrow[i] = a.x + rr * a.K + 4 * t;
+        const unsigned char *xq = reinterpret_cast<const unsigned char *>(a.x);
+        qrow[i] = xq + rr * a.K + 4 * t;
+        drow[i] = reinterpret_cast<const float *>(xq + (size_t)a.m * a.K) + rr * a.nb;
     }
     uint2 xn1[NR][2], xn2[NR][2];  // blocks i + 1 and i + 2
     auto load_x = [&](uint2 (&dst)[NR][2], int b) {
 #pragma unroll
-        for (int i = 0; i < NR; ++i)
+        for (int i = 0; i < NR; ++i) {
+            if constexpr (QACT) {
+                const unsigned char *p = qrow[i] + (size_t)b * kBlock;
+                dst[i][0] = xlive[i] ? make_uint2(ld_cg_u32(p), ld_cg_u32(p + 16)) : make_uint2(0u, 0u);
+                dst[i][1] = make_uint2(xlive[i] ? ld_cg_u32(drow[i] + b) : 0u, 0u);
+            } else {
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                dst[i][s] = xlive[i] ? ld_cg_u2(xrow[i] + (size_t)b * kBlock + 16 * s) : make_uint2(0u, 0u);
+                for (int s = 0; s < 2; ++s)
+                    dst[i][s] = xlive[i] ? ld_cg_u2(xrow[i] + (size_t)b * kBlock + 16 * s) : make_uint2(0u, 0u);
+            }
+        }
     };
     if (n > 0) load_x(xn1, b0);
     if (n > 1) load_x(xn2, b0 + 1);
@@ -380,7 +403,13 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 xn1[r][s] = xn2[r][s];
             }
         if (i + 2 < n) load_x(xn2, b0 + i + 2);
-        const XPlan plan = plan_block<NR, !ROWS16>(xc);
+        XPlan plan;
+        if constexpr (QACT) {
+            plan.sf[0] = pack_f32x2(__uint_as_float(xc[0][1].x), __uint_as_float(xc[0][1].x));
+            plan.sf[1] = pack_f32x2(__uint_as_float(xc[NR - 1][1].x), __uint_as_float(xc[NR - 1][1].x));
+        } else {
+            plan = plan_block<NR, !ROWS16>(xc);
+        }
 
         cp_async_wait<kDepthS - 1>();  // this lane's copies of unit i have landed
         __syncwarp();                  // ... and every other lane's
@@ -389,7 +418,20 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             cur = cur == kDepthS - 1 ? 0 : cur + 1;
             nxt = nxt == kDepthS - 1 ? 0 : nxt + 1;
         }
-        if (ROWS16 && plan.plain) {
+        if constexpr (QACT) {
+            // int8 codes as the stored-weight form (x + 128 = x ^ 0x80 per byte), then the same exact fp16 pairs
+            uint32_t af[2][4];
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const uint32_t u0 = (s ? xc[0][0].y : xc[0][0].x) ^ 0x80808080u;
+                const uint32_t u1 = (s ? xc[NR - 1][0].y : xc[NR - 1][0].x) ^ 0x80808080u;
+                af[s][0] = q8x2_to_f16x2<0>(u0);
+                af[s][2] = q8x2_to_f16x2<2>(u0);
+                af[s][1] = ROWS16 ? q8x2_to_f16x2<0>(u1) : 0u;
+                af[s][3] = ROWS16 ? q8x2_to_f16x2<2>(u1) : 0u;
+            }
+            block_contract<true, ROWS16, false>(st, lane, af, plan, acc);
+        } else if (ROWS16 && plan.plain) {
             uint32_t af[2][4];
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
@@ -462,7 +504,17 @@ template <int E> __device__ __forceinline__ unsigned long long q8x2_to_f32x2(uin
     return d;
 }
 
-template <int M, int EPI>
+// dp4a with unsigned bytes in a (the stored weights, q + 128) and signed bytes in b: c + sum a_i * b_i.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// QACT (quantized activations, m <= 2): the lane's eight codes of a row and block meet each column's eight stored
+// bytes in two dp4a (integer products, exact); the offset is removed by starting the sum at -128 times the sum of the
+// eight codes, the exact integer is converted to fp32 and folded with s[b, n] * d[r, b].
+template <int M, int EPI, bool QACT = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
     stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     extern __shared__ __align__(16) unsigned char smem_s[];
@@ -479,10 +531,14 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     const size_t unit0 = (size_t)tile * a.nb + b0;
 
     unsigned long long acc[M][kSlices];  // per row and column 8j + g: the carry of rows 4t, 4t+2 | 4t+1, 4t+3
+    float accq[M][kSlices];              // QACT: per row and column 8j + g, the carry of the lane's rows
 #pragma unroll
     for (int r = 0; r < M; ++r)
 #pragma unroll
-        for (int j = 0; j < kSlices; ++j) acc[r][j] = 0ull;
+        for (int j = 0; j < kSlices; ++j) {
+            acc[r][j] = 0ull;
+            accq[r][j] = 0.0f;
+        }
 
     if (prefetch_weights) {
 #pragma unroll
@@ -500,12 +556,23 @@ __global__ void __launch_bounds__(kThreadsS, 2)
         }
     }
 
+    // QACT: [r][0] holds the row's two code words (s = 0, 1), [r][1].x the bits of its block scale
+    const unsigned char *xq = reinterpret_cast<const unsigned char *>(a.x);
+    const float *xd = reinterpret_cast<const float *>(xq + (size_t)a.m * a.K);
     uint2 xn1[M][2], xn2[M][2];
     auto load_x = [&](uint2 (&dst)[M][2], int b) {
 #pragma unroll
-        for (int r = 0; r < M; ++r)
+        for (int r = 0; r < M; ++r) {
+            if constexpr (QACT) {
+                const unsigned char *p = xq + (size_t)r * a.K + (size_t)b * kBlock + 4 * t;
+                dst[r][0] = make_uint2(ld_cg_u32(p), ld_cg_u32(p + 16));
+                dst[r][1] = make_uint2(ld_cg_u32(xd + (size_t)r * a.nb + b), 0u);
+            } else {
 #pragma unroll
-            for (int s = 0; s < 2; ++s) dst[r][s] = ld_cg_u2(a.x + (size_t)r * a.K + (size_t)b * kBlock + 16 * s + 4 * t);
+                for (int s = 0; s < 2; ++s)
+                    dst[r][s] = ld_cg_u2(a.x + (size_t)r * a.K + (size_t)b * kBlock + 16 * s + 4 * t);
+            }
+        }
     };
     if (n > 0) load_x(xn1, b0);
     if (n > 1) load_x(xn2, b0 + 1);
@@ -523,6 +590,33 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 xn1[r][s] = xn2[r][s];
             }
         if (i + 2 < n) load_x(xn2, b0 + i + 2);
+        if constexpr (QACT) {
+            int base[M];  // -128 * (the lane's eight codes of the row summed)
+#pragma unroll
+            for (int r = 0; r < M; ++r)
+                base[r] = -128 * dp4a_us(0x01010101u, xc[r][0].y, dp4a_us(0x01010101u, xc[r][0].x, 0));
+            cp_async_wait<kDepthS - 1>();
+            __syncwarp();
+            const unsigned char *st = ring + (i % kDepthS) * kStageS;
+            const float *ss = reinterpret_cast<const float *>(st + kUnit) + g;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(st + h * 512 + lane * 16);
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(st + (4 + h) * 512 + lane * 16);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int j = 4 * h + w;
+                    const float sv = ss[8 * j];
+#pragma unroll
+                    for (int r = 0; r < M; ++r) {
+                        const int p = dp4a_us(word_of(w1, w), xc[r][0].y, dp4a_us(word_of(w0, w), xc[r][0].x, base[r]));
+                        accq[r][j] = fmaf(sv * __uint_as_float(xc[r][1].x), (float)p, accq[r][j]);
+                    }
+                }
+            }
+            __syncwarp();
+            continue;
+        }
         // activations as fp32 pairs {x[4t], x[4t+1]} and {x[4t+2], x[4t+3]} of each row and half
         unsigned long long xp[M][2][2];
 #pragma unroll
@@ -578,7 +672,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
         for (int j = 0; j < kSlices; ++j) {
             float lo, hi;
             unpack_f32x2(acc[r][j], lo, hi);
-            float v = lo + hi;
+            float v = QACT ? accq[r][j] : lo + hi;
             v += __shfl_xor_sync(0xffffffffu, v, 1);
             v += __shfl_xor_sync(0xffffffffu, v, 2);
             if (t == 0) mine[r * kTmaColumns + 8 * j + g] = v;
@@ -678,8 +772,14 @@ int stream_max_clusters(int ks) {
 }
 
 template <int EPI>
-cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, bool p) {
+cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, bool p, bool qact) {
     const bool pair = EPI == kEpiGlu;
+    if (qact) {
+        if (a.m == 1) return launch_stream_kernel(stream_simt_kernel<1, EPI, true>, a, pt, stream, pdl, p, pair);
+        if (a.m == 2) return launch_stream_kernel(stream_simt_kernel<2, EPI, true>, a, pt, stream, pdl, p, pair);
+        if (a.m <= 8) return launch_stream_kernel(stream_kernel<false, EPI, true>, a, pt, stream, pdl, p, pair);
+        return launch_stream_kernel(stream_kernel<true, EPI, true>, a, pt, stream, pdl, p, pair);
+    }
     if (a.m == 1) return launch_stream_kernel(stream_simt_kernel<1, EPI>, a, pt, stream, pdl, p, pair);
     if (a.m == 2) return launch_stream_kernel(stream_simt_kernel<2, EPI>, a, pt, stream, pdl, p, pair);
     if (a.m <= 8) return launch_stream_kernel(stream_kernel<false, EPI>, a, pt, stream, pdl, p, pair);
@@ -687,12 +787,12 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
 }
 
 cudaError_t launch_stream(const Args &a, const Parts &pt, int epi, cudaStream_t stream, bool pdl,
-                          bool prefetch_weights) {
+                          bool prefetch_weights, bool qact) {
     switch (epi) {
-        case kEpiStore: return launch_stream_epi<kEpiStore>(a, pt, stream, pdl, prefetch_weights);
-        case kEpiArgmax: return launch_stream_epi<kEpiArgmax>(a, pt, stream, pdl, prefetch_weights);
-        case kEpiGlu: return launch_stream_epi<kEpiGlu>(a, pt, stream, pdl, prefetch_weights);
-        case kEpiNorm: return launch_stream_epi<kEpiNorm>(a, pt, stream, pdl, prefetch_weights);
+        case kEpiStore: return launch_stream_epi<kEpiStore>(a, pt, stream, pdl, prefetch_weights, qact);
+        case kEpiArgmax: return launch_stream_epi<kEpiArgmax>(a, pt, stream, pdl, prefetch_weights, qact);
+        case kEpiGlu: return launch_stream_epi<kEpiGlu>(a, pt, stream, pdl, prefetch_weights, qact);
+        case kEpiNorm: return launch_stream_epi<kEpiNorm>(a, pt, stream, pdl, prefetch_weights, qact);
         default: return cudaErrorInvalidValue;
     }
 }

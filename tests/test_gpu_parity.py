@@ -539,8 +539,8 @@ def _glu_run(torch, x, qg, sg, qu, su, N, want=("f32", "bf16")):
             outb.view(torch.int16).cpu().numpy().view(np.uint16) if outb is not None else None)
 
 
-def _glu_check(out, outb, x, qg, sg, qu, su, N, cols=None, what=""):
-    out_o, g_o, u_o, a_g, a_u = oracle.glu(x, qg, sg, qu, su, cols)
+def _glu_check(out, outb, x, qg, sg, qu, su, N, cols=None, what="", act=None):
+    out_o, g_o, u_o, a_g, a_u = oracle.glu(x, qg, sg, qu, su, cols, act=act)
     got = out if cols is None else out[:, cols]
     err = np.abs(got.astype(np.float64) - out_o)
     bound = _glu_bound(g_o, u_o, a_g, a_u, out_o)
@@ -629,8 +629,8 @@ def _norm_run(torch, x, q, s, res, gamma, eps, N, in_place=False):
     return h.cpu().numpy(), out.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def _norm_check(h, outb, x, q, s, res, gamma, eps, N, what=""):
-    h_o, out_o, _, a_o = oracle.residual_norm(x, q, s, res, gamma, eps, N)
+def _norm_check(h, outb, x, q, s, res, gamma, eps, N, what="", act=None):
+    h_o, out_o, _, a_o = oracle.residual_norm(x, q, s, res, gamma, eps, N, act=act)
     tol_h = TOL * a_o + 2.0 ** -24 * np.abs(h_o)
     bad = np.abs(h.astype(np.float64) - h_o) > tol_h
     assert not bad.any(), f"{what}: h out of bound at {np.argwhere(bad)[0]}"

@@ -309,3 +309,34 @@ def test_gemv_parts_argument_errors(lib):
     assert lib.q8_gemv_parts(A16, ctypes.cast(clash, ctypes.c_void_p), 2, 1, 32, 0, None) == 1    # outputs overlap
     zero = (P * 1)(P(B16, C16, D16, 0))
     assert lib.q8_gemv_parts(A16, ctypes.cast(zero, ctypes.c_void_p), 1, 1, 32, 0, None) == 2     # N = 0
+
+
+def test_act_bytes(lib):
+    assert lib.q8_act_bytes(1, 32) == 36
+    assert lib.q8_act_bytes(3, 64) == 3 * 64 + 3 * 2 * 4
+    assert lib.q8_act_bytes(16, 14336) == 16 * 14336 + 16 * 448 * 4
+    assert lib.q8_act_bytes(0, 32) == -1 and lib.q8_act_bytes(1, 0) == -1 and lib.q8_act_bytes(1, 48) == -1
+
+
+def test_quantize_act_argument_errors(lib):
+    XA = 0x80000
+    assert lib.q8_quantize_act(None, XA, 1, 32, None) == 1
+    assert lib.q8_quantize_act(A16, None, 1, 32, None) == 1
+    assert lib.q8_quantize_act(A16, XA, 0, 32, None) == 2
+    assert lib.q8_quantize_act(A16, XA, 1, 33, None) == 2
+    assert lib.q8_quantize_act(A16, XA, 1, 0, None) == 2
+    assert lib.q8_quantize_act(A16 + 8, XA, 1, 32, None) == 3
+    assert lib.q8_quantize_act(A16, XA + 4, 1, 32, None) == 3
+    assert lib.q8_quantize_act(A16, A16 + 48, 1, 32, None) == 1     # output inside x (64 bytes)
+    assert lib.q8_quantize_act(A16 + 16, A16, 1, 32, None) == 1     # x inside the output (36 bytes)
+
+
+def test_quantized_activation_flag_rules(lib):
+    """Q8_FLAG_Q8_ACT (4) needs Q8_FLAG_TILED on every product entry point; an output over the quantized form
+    (whose size is q8_act_bytes, not 2 m K) is an overlap."""
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 1, 32, 64, 0, 4, None) == 1
+    assert lib.q8_gemv_argmax_ex(A16, B16, C16, D16, None, 1, 32, 64, 4, None) == 1
+    assert lib.q8_gemv_glu(A16, B16, C16, 0x50000, 0x60000, D16, None, 1, 32, 64, 4, None) == 1
+    # m = 1, K = 64: 72 bytes of quantized form, so y at x + 64 overlaps it
+    assert lib.q8_gemv_ex(A16, B16, C16, A16 + 64, 1, 64, 64, 0, 4 | 2, None) == 1
+    assert lib.q8_gemv_parts(A16, None, 1, 1, 64, 4 | 2, None) == 1
