@@ -45,6 +45,12 @@ typedef struct CUstream_st *q8_stream_t;
 /* The most activation rows one call takes ("plan.rs", `GEMV_ROWS`: a GEMV launch multiplies at most 16 rows). */
 #define Q8_MAX_ROWS 16
 
+/* The most activation rows one call over the tiled storage takes ("plan.rs", `MAX_CHUNK`: the largest prefill chunk
+ * a lane compiles, 512; its projections of more rows than the GEMV's 16 run on the tensor cores).  With
+ * Q8_FLAG_TILED, m may be 1 .. 512: the rows run as ceil(m / 16) groups of 16 in one launch, each group's CTAs of a
+ * column tile side by side so that the weight is streamed from HBM about once. */
+#define Q8_MAX_CHUNK 512
+
 typedef enum {
     Q8_OK = 0,
     Q8_ERR_ARG = 1,      /* a required pointer is NULL, or an enum argument is out of range */
@@ -71,7 +77,8 @@ int q8_padded_n(int N);
 /* y = x . W over the Q8_0 weight (q, s), m rows (source: "from_q8.rs", module doc and `q8_fold`).
  *   x  device, bf16 [m][K], 16-byte aligned        q  device, int8 [K][Np], 16-byte aligned
  *   s  device, fp32 [K/32][Np], 16-byte aligned    y  device, fp32 [m][Np] (written), 16-byte aligned
- *   1 <= m <= 16, K > 0, K % 32 == 0 ("from_q8.rs", `q8_gemv_applies`), N > 0.
+ *   1 <= m <= 16 (1 <= m <= 512 over the tiled storage, Q8_MAX_CHUNK), K > 0, K % 32 == 0 ("from_q8.rs",
+ *   `q8_gemv_applies`), N > 0.
  * y must not overlap x, q or s.  Every output n < Np is written; outputs n >= N are 0.0f.
  * Each y[r, n] equals the real-number product within 1e-5 * sum_b |s[b,n]| sum_i |x[r,32b+i] q[32b+i,n]|; the
  * summation order is fixed for a given (m, K, N) and device, so repeated calls give identical bits. */
@@ -166,8 +173,8 @@ q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const in
  *   out_bf16  device, bf16 [m][Np] (written: out rounded to nearest even, pads 0), 16-byte aligned -- the next
  *             projection's activation as q8_gemv takes it (row pitch Np)
  *   flags     Q8_FLAG_TILED (required) | Q8_FLAG_CONSTANT_WEIGHTS
- * At most 64 calls may be in flight at once (each takes the next counter in turn; a counter is back to 0 when its
- * launch ends).  Errors: Q8_ERR_ARG (null pointers, flags without Q8_FLAG_TILED or unknown bits, eps < 0 or not
+ * Each group of 16 rows takes the next of 64 static completion counters in turn (a counter is back to 0 when its
+ * launch ends), so at most 64 row groups -- 64 calls of m <= 16 -- may be in flight at once.  Errors: Q8_ERR_ARG (null pointers, flags without Q8_FLAG_TILED or unknown bits, eps < 0 or not
  * finite, outputs overlapping an input or each other other than h == residual), Q8_ERR_SHAPE, Q8_ERR_ALIGN,
  * Q8_ERR_CUDA; nothing is launched on an error. */
 q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const float *s, const float *residual,

@@ -26,6 +26,7 @@ from .build import LIB as _LIB_PATH
 
 Q8_BLOCK = 32
 MAX_ROWS = 16
+MAX_CHUNK = 512  # rows one call over tiled weights takes
 VARIANTS = {"auto": 0, "simt": 1, "mma": 2, "tma": 3}
 
 _STATUS = {0: "Q8_OK", 1: "Q8_ERR_ARG", 2: "Q8_ERR_SHAPE", 3: "Q8_ERR_ALIGN", 4: "Q8_ERR_NOT_Q8_0", 5: "Q8_ERR_CUDA"}

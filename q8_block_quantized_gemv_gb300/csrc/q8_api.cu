@@ -68,7 +68,8 @@ Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long
         // reduction both cost more than the idle SMs of a short wave): ks = resident slots / tiles, at least 1,
         // lowered while the tiles' clusters of ks CTAs would not all be resident at once (a cluster's CTAs share
         // one GPC, so fewer clusters fit than slots / ks).
-        const long long tiles = tiled_tiles > 0 ? tiled_tiles : (Np + q8::kTmaColumns - 1) / q8::kTmaColumns;
+        const long long groups = (m + q8::kGroupRows - 1) / q8::kGroupRows;
+        const long long tiles = groups * (tiled_tiles > 0 ? tiled_tiles : (Np + q8::kTmaColumns - 1) / q8::kTmaColumns);
         const long long slots = (long long)q8::stream_ctas_per_sm(m) * sms;
         long long ks = slots / tiles;
         if (ks > 8) ks = 8;
@@ -131,9 +132,11 @@ Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long
     return best;
 }
 
-q8_status check_gemv_args(const void *x, const int8_t *q, const float *s, int m, int K, int N) {
+// m may be 1 .. 16, or 1 .. 512 over the tiled storage (row groups of 16 in one launch).
+q8_status check_gemv_args(const void *x, const int8_t *q, const float *s, int m, int K, int N, unsigned flags) {
     if (!x || !q || !s) return Q8_ERR_ARG;
-    if (m < 1 || m > Q8_MAX_ROWS || K <= 0 || K % Q8_BLOCK != 0 || N <= 0) return Q8_ERR_SHAPE;
+    const int max_rows = (flags & Q8_FLAG_TILED) ? Q8_MAX_CHUNK : Q8_MAX_ROWS;
+    if (m < 1 || m > max_rows || K <= 0 || K % Q8_BLOCK != 0 || N <= 0) return Q8_ERR_SHAPE;
     if (q8_padded_n(N) < 0) return Q8_ERR_SHAPE;
     if (!aligned(x, 16) || !aligned(q, 16) || !aligned(s, 16)) return Q8_ERR_ALIGN;
     return Q8_OK;
@@ -185,8 +188,7 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
 
 // keys[r] (the packed maximum written by the GEMV) -> the 0-based index it encodes, in place.
 __global__ void argmax_decode(int64_t *idx, int m) {
-    const int r = threadIdx.x;
-    if (r < m) {
+    for (int r = threadIdx.x; r < m; r += blockDim.x) {
         const unsigned long long key = (unsigned long long)idx[r];
         idx[r] = (int64_t)(0xFFFFFFFFull - (key & 0xFFFFFFFFull));
     }
@@ -196,7 +198,7 @@ __global__ void argmax_decode(int64_t *idx, int m) {
 
 extern "C" q8_status q8_gemv_ex(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N,
                                 int variant, unsigned int flags, q8_stream_t stream) {
-    q8_status st = check_gemv_args(x, q, s, m, K, N);
+    q8_status st = check_gemv_args(x, q, s, m, K, N, flags);
     if (st != Q8_OK) return st;
     if (!y) return Q8_ERR_ARG;
     if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_TMA) return Q8_ERR_ARG;
@@ -221,7 +223,7 @@ extern "C" q8_status q8_gemv(const void *x, const int8_t *q, const float *s, flo
 
 extern "C" q8_status q8_gemv_argmax_ex(const void *x, const int8_t *q, const float *s, int64_t *idx, float *logits,
                                        int m, int K, int N, unsigned int flags, q8_stream_t stream) {
-    q8_status st = check_gemv_args(x, q, s, m, K, N);
+    q8_status st = check_gemv_args(x, q, s, m, K, N, flags);
     if (st != Q8_OK) return st;
     if (!idx) return Q8_ERR_ARG;
     if (!flags_ok(flags)) return Q8_ERR_ARG;
@@ -246,7 +248,7 @@ extern "C" q8_status q8_gemv_argmax_ex(const void *x, const int8_t *q, const flo
     if (st != Q8_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
-    cfg.blockDim = dim3(32, 1, 1);
+    cfg.blockDim = dim3(m > 32 ? 128 : 32, 1, 1);
     cfg.stream = cs;
     ce = cudaLaunchKernelEx(&cfg, argmax_decode, idx, m);
     if (ce != cudaSuccess) return cuda_fail(ce);
@@ -266,7 +268,7 @@ extern "C" q8_status q8_gemv_parts(const void *x, const q8_part *parts, int npar
     const bool tiled = (flags & Q8_FLAG_TILED) != 0;
     for (int i = 0; i < nparts; ++i) {
         const q8_part &p = parts[i];
-        q8_status st = check_gemv_args(x, p.q, p.s, m, K, p.N);
+        q8_status st = check_gemv_args(x, p.q, p.s, m, K, p.N, flags);
         if (st != Q8_OK) return st;
         if (!p.y) return Q8_ERR_ARG;
         if (!aligned(p.y, 16)) return Q8_ERR_ALIGN;
@@ -334,9 +336,9 @@ int plan_glu(long long tiles, int nb, int sms) {
 extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const int8_t *qu,
                                  const float *su, float *out, void *out_bf16, int m, int K, int N, unsigned int flags,
                                  q8_stream_t stream) {
-    q8_status st = check_gemv_args(x, qg, sg, m, K, N);
+    q8_status st = check_gemv_args(x, qg, sg, m, K, N, flags);
     if (st != Q8_OK) return st;
-    st = check_gemv_args(x, qu, su, m, K, N);
+    st = check_gemv_args(x, qu, su, m, K, N, flags);
     if (st != Q8_OK) return st;
     if (!out && !out_bf16) return Q8_ERR_ARG;
     if (!flags_ok(flags)) return Q8_ERR_ARG;
@@ -360,6 +362,7 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
     int e = sm_count(&sms);
     if (e != 0) return cuda_fail((cudaError_t)e);
     const int tiles = tiles_of(N);
+    const int groups = (m + q8::kGroupRows - 1) / q8::kGroupRows;
     q8::Parts pt = {};
     pt.q[0] = qg;
     pt.s[0] = sg;
@@ -371,7 +374,7 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
     pt.count = 2;
     Args a = {static_cast<const uint16_t *>(x), qg, sg, out, nullptr, m, K, N, Np, K / Q8_BLOCK, 1,
               static_cast<uint16_t *>(out_bf16)};
-    a.ksplit = plan_glu(tiles, K / Q8_BLOCK, sms);
+    a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms);
     cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true,
                                        (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0, (flags & Q8_FLAG_Q8_ACT) != 0);
     if (ce != cudaSuccess) return cuda_fail(ce);
@@ -381,7 +384,7 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
 extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const float *s, const float *residual,
                                            const float *gamma, float eps, float *h, void *out_bf16, int m, int K,
                                            int N, unsigned int flags, q8_stream_t stream) {
-    q8_status st = check_gemv_args(x, q, s, m, K, N);
+    q8_status st = check_gemv_args(x, q, s, m, K, N, flags);
     if (st != Q8_OK) return st;
     if (!residual || !gamma || !h || !out_bf16) return Q8_ERR_ARG;
     if (!flags_ok(flags)) return Q8_ERR_ARG;
@@ -399,11 +402,14 @@ extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const
     for (int i = 0; i < 4; ++i)
         if (overlaps(h, hbytes, ins[i], inb[i]) || overlaps(out_bf16, obytes, ins[i], inb[i])) return Q8_ERR_ARG;
     if (overlaps(out_bf16, obytes, h, hbytes) || overlaps(out_bf16, obytes, residual, hbytes)) return Q8_ERR_ARG;
+    // one completion counter per row group, taken round robin
     static std::atomic<unsigned> next_counter{0};
-    unsigned int *count = q8::norm_counter(next_counter.fetch_add(1u, std::memory_order_relaxed));
+    const unsigned groups = (unsigned)((m + q8::kGroupRows - 1) / q8::kGroupRows);
+    const int slot = (int)(next_counter.fetch_add(groups, std::memory_order_relaxed) % q8::kNormSlots);
+    unsigned int *count = q8::norm_counters();
     if (!count) return cuda_fail(cudaGetLastError());
     Args a = {static_cast<const uint16_t *>(x), q, s, h, nullptr, m, K, N, Np, K / Q8_BLOCK, 1,
-              static_cast<uint16_t *>(out_bf16), residual, gamma, eps, count};
+              static_cast<uint16_t *>(out_bf16), residual, gamma, eps, count, slot};
     int sms = 0;
     int e = sm_count(&sms);
     if (e != 0) return cuda_fail((cudaError_t)e);

@@ -39,8 +39,34 @@ struct Args {
     const float *res;          // norm: residual fp32 [m][Np] (h = res + y is written to y; may be y itself)
     const float *gamma;        // norm: fp32 [Np]
     float eps;                 // norm: added to the mean square
-    unsigned int *count;       // norm: this launch's completion counter (0 on entry, reset to 0 by the last CTA)
+    unsigned int *count;       // norm: the completion counters (0 on entry, reset to 0 by the last CTA of a group)
+    int count_slot;            // norm: row group g counts in at count[(count_slot + g) % kNormSlots]
+    int groups;                // set on the device: the launch's row groups (ceil(m / 16))
 };
+
+constexpr int kGroupRows = 16;   // activation rows of one row group (m > 16 runs ceil(m / 16) groups in one grid)
+constexpr int kNormSlots = 64;   // completion counters of the residual-norm launches (row groups in flight at once)
+
+// Row groups: grid x holds `groups` = ceil(m / 16) consecutive CTAs per column tile (the row groups of a tile side
+// by side, so that they read the tile's weight units at about the same time and the later ones find them in L2).
+__device__ __forceinline__ int row_groups(const Args &a) { return (a.m + kGroupRows - 1) / kGroupRows; }
+
+// The Args of row group `group`'s rows, applied just before the epilogue (so that the main loop keeps no extra
+// pointers live): y, its bf16 copy, the residual and the arg-max keys move to the group's first row, m becomes the
+// group's row count and the norm counter the group's own.
+__device__ __forceinline__ void apply_group(Args &a, int group, int groups) {
+    a.groups = groups;
+    if (groups > 1) {
+        const int row0 = group * kGroupRows;
+        const size_t off = (size_t)row0 * a.Np;
+        if (a.y) a.y += off;
+        if (a.ybf) a.ybf += off;
+        if (a.res) a.res += off;
+        if (a.keys) a.keys += row0;
+        a.count_slot += group;
+        a.m = a.m - row0 < kGroupRows ? a.m - row0 : kGroupRows;
+    }
+}
 
 // Several weights that multiply one activation in one launch ("plan.rs", `Launch::GemmParts`: projections of one
 // activation as one launch over their outputs side by side).  Part p owns the column tiles [tile_end[p-1],
@@ -77,13 +103,35 @@ constexpr int kEpiArgmax = 1;  // write y (if any) and fold the row arg-max keys
 constexpr int kEpiGlu = 2;     // gated pair: part 0 is the gate, part 1 the up projection; write silu(g) * u
 constexpr int kEpiNorm = 3;    // residual add, then the last CTA writes the rows' RMS norm
 
-// A gated-pair launch interleaves the two weights' CTAs: grid x = 2 * tile + part, clusters of 2 along x (the
-// gate's and the up projection's CTAs of one tile and K range side by side).  `a` gets the part's q and s.
-__device__ __forceinline__ int select_glu(const Parts &pt, Args &a) {
-    const int p = blockIdx.x & 1;
-    a.q = pt.q[p];
-    a.s = pt.s[p];
-    return blockIdx.x >> 1;
+// A gated-pair launch interleaves the two weights' CTAs: grid x = 2 * (tile * groups + group) + part, clusters of 2
+// along x (the gate's and the up projection's CTAs of one tile, row group and K range side by side).
+
+// The CTA's column tile within its part and its row group (GROUPS: the kernel takes m > 16), with its part's q, s,
+// y, N and Np in `a`; the gated pair interleaves the parts (x = 2 * (tile * groups + group) + p).
+template <int EPI, bool GROUPS>
+__device__ __forceinline__ int select_cta(const Parts &pt, Args &a, int &group) {
+    const int groups = GROUPS ? row_groups(a) : 1;
+    int x = blockIdx.x;
+    if (EPI == kEpiGlu) {
+        const int p = x & 1;
+        a.q = pt.q[p];
+        a.s = pt.s[p];
+        x >>= 1;
+    }
+    group = GROUPS ? x % groups : 0;
+    x = GROUPS ? x / groups : x;
+    return EPI == kEpiGlu ? x : select_part(pt, x, a);
+}
+
+// apply_group for the CTA's own row group, found again from the grid index (m is still the launch's).
+template <int EPI, bool GROUPS> __device__ __forceinline__ void apply_cta_group(Args &a) {
+    if (!GROUPS) {
+        a.groups = 1;
+        return;
+    }
+    const int groups = row_groups(a);
+    const int x = EPI == kEpiGlu ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    apply_group(a, x % groups, groups);
 }
 
 // ------------------------------------------------------------------------------------------------------------------
@@ -338,8 +386,8 @@ __device__ __forceinline__ void finish_norm(const Args &a, float *red, int tile)
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();  // this CTA's h is visible before its count
-        const unsigned total = gridDim.x * gridDim.y;
-        last = atomicAdd(a.count, 1u) == total - 1 ? 1u : 0u;
+        const unsigned total = gridDim.x * gridDim.y / (unsigned)a.groups;  // this row group's CTAs
+        last = atomicAdd(a.count + a.count_slot % kNormSlots, 1u) == total - 1 ? 1u : 0u;
     }
     __syncthreads();
     if (!last) return;
@@ -410,7 +458,7 @@ __device__ __forceinline__ void finish_norm(const Args &a, float *red, int tile)
                 *reinterpret_cast<uint2 *>(a.ybf + (size_t)r * a.Np + n) = make_uint2(lo, hi);
             }
     }
-    if (threadIdx.x == 0) *a.count = 0u;  // ready for the next launch that takes this counter
+    if (threadIdx.x == 0) a.count[a.count_slot % kNormSlots] = 0u;  // ready for the next launch that takes it
 }
 
 template <int MR, int TC, bool ARGMAX>

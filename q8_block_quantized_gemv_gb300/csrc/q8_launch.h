@@ -53,8 +53,7 @@ int stream_max_clusters(int ks);  // clusters of ks stream-kernel CTAs resident 
 cudaError_t launch_stream(const Args &a, const Parts &parts, int epi, cudaStream_t stream, bool pdl,
                           bool prefetch_weights, bool qact);
 cudaError_t read_fault_word(unsigned *out, bool clear);
-constexpr unsigned kNormCounters = 64;  // residual-norm launches that may be in flight at once
-unsigned int *norm_counter(unsigned slot);  // device address of completion counter `slot` (null on a CUDA error)
+unsigned int *norm_counters();  // device address of the kNormSlots completion counters (null on a CUDA error)
 constexpr int kTmaColumns = 128;
 
 // Widths built for each family (descending), used by the planner.

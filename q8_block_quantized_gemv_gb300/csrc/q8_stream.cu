@@ -310,15 +310,22 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
 // QACT: x is a quantized activation (int8 values [m][K], then fp32 scales [m][K/32]); each block's A fragments are its
 // int8 codes as exact fp16, its integer sums are exact in the fp32 accumulators (|sum| <= 32 * 127 * 127 < 2^24),
 // and its factor per activation row is that row's scale d.
-template <bool ROWS16, int EPI, bool QACT = false>
+// GROUPS: m > 16, the rows in groups of 16 (grid x = tiles * groups, ROWS16 only).
+template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
     stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
+    static_assert(ROWS16 || !GROUPS, "row groups are groups of 16 rows");
     constexpr int MR = ROWS16 ? 16 : 8;
     constexpr int NR = ROWS16 ? 2 : 1;  // activation rows per lane: g and g + 8
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int tile = EPI == kEpiGlu ? select_glu(parts, a) : select_part(parts, blockIdx.x, a);
+    // the activation bases of the whole launch (all m rows), before the row group's Args replace m
+    const unsigned char *xq_all = reinterpret_cast<const unsigned char *>(a.x);
+    const float *xd_all = reinterpret_cast<const float *>(xq_all + (size_t)a.m * a.K);
+    int group;
+    const int tile = select_cta<EPI, GROUPS>(parts, a, group);
+    const int row0 = group * kGroupRows;
     const int rank = blockIdx.y;
     const int c0 = (int)((long long)a.nb * rank / a.ksplit);
     const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
@@ -360,13 +367,12 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     bool xlive[NR];
 #pragma unroll
     for (int i = 0; i < NR; ++i) {
-        const int r = g + 8 * i;
+        const int r = row0 + g + 8 * i;  // the launch's row (m is still the launch's here)
         xlive[i] = r < a.m;
         const size_t rr = (size_t)(xlive[i] ? r : 0);
         xrow[i] = a.x + rr * a.K + 4 * t;
-        const unsigned char *xq = reinterpret_cast<const unsigned char *>(a.x);
-        qrow[i] = xq + rr * a.K + 4 * t;
-        drow[i] = reinterpret_cast<const float *>(xq + (size_t)a.m * a.K) + rr * a.nb;
+        qrow[i] = xq_all + rr * a.K + 4 * t;
+        drow[i] = xd_all + rr * a.nb;
     }
     uint2 xn1[NR][2], xn2[NR][2];  // blocks i + 1 and i + 2
     auto load_x = [&](uint2 (&dst)[NR][2], int b) {
@@ -481,6 +487,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             *reinterpret_cast<float2 *>(mine + (g + 8 * r) * kSlabStride + 8 * j + 2 * t) = make_float2(lo, hi);
         }
     __syncthreads();
+    apply_cta_group<EPI, GROUPS>(a);
     if constexpr (EPI == kEpiGlu)
         finish_glu<kWarpsS, MR, kTmaColumns, kThreadsS, kSlabStride>(a, red, tile);
     else if constexpr (EPI == kEpiNorm)
@@ -520,7 +527,8 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int tile = EPI == kEpiGlu ? select_glu(parts, a) : select_part(parts, blockIdx.x, a);
+    int group;  // one row group (m <= 2)
+    const int tile = select_cta<EPI, false>(parts, a, group);
     const int rank = blockIdx.y;
     const int c0 = (int)((long long)a.nb * rank / a.ksplit);
     const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
@@ -678,6 +686,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             if (t == 0) mine[r * kTmaColumns + 8 * j + g] = v;
         }
     __syncthreads();
+    apply_cta_group<EPI, false>(a);
     if constexpr (EPI == kEpiGlu)
         finish_glu<kWarpsS, M, kTmaColumns, kThreadsS>(a, red, tile);
     else if constexpr (EPI == kEpiNorm)
@@ -698,7 +707,8 @@ cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, 
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pt.tile_end[pt.count - 1], (unsigned)a.ksplit, 1);
+    const unsigned groups = (unsigned)((a.m + kGroupRows - 1) / kGroupRows);
+    cfg.gridDim = dim3((unsigned)pt.tile_end[pt.count - 1] * groups, (unsigned)a.ksplit, 1);
     cfg.blockDim = dim3(kThreadsS, 1, 1);
     cfg.dynamicSmemBytes = kSmemS;
     cfg.stream = stream;
@@ -724,14 +734,14 @@ cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, 
 }  // namespace
 
 // The completion counters of the residual-norm launches: the library's only scratch memory, static so that the
-// entry point allocates nothing.  A launch takes one counter (round robin over the calls); its last CTA leaves it
-// at 0 again.
-__device__ __align__(256) unsigned int g_norm_count[kNormCounters];
+// entry point allocates nothing.  Each row group of a launch takes one counter (round robin over the calls); the
+// group's last CTA leaves it at 0 again.
+__device__ __align__(256) unsigned int g_norm_count[kNormSlots];
 
-unsigned int *norm_counter(unsigned slot) {
+unsigned int *norm_counters() {
     void *base = nullptr;
     if (cudaGetSymbolAddress(&base, g_norm_count) != cudaSuccess) return nullptr;
-    return static_cast<unsigned int *>(base) + slot % kNormCounters;
+    return static_cast<unsigned int *>(base);
 }
 
 int stream_ctas_per_sm(int) { return 2; }
@@ -778,12 +788,14 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
         if (a.m == 1) return launch_stream_kernel(stream_simt_kernel<1, EPI, true>, a, pt, stream, pdl, p, pair);
         if (a.m == 2) return launch_stream_kernel(stream_simt_kernel<2, EPI, true>, a, pt, stream, pdl, p, pair);
         if (a.m <= 8) return launch_stream_kernel(stream_kernel<false, EPI, true>, a, pt, stream, pdl, p, pair);
-        return launch_stream_kernel(stream_kernel<true, EPI, true>, a, pt, stream, pdl, p, pair);
+        if (a.m <= kGroupRows) return launch_stream_kernel(stream_kernel<true, EPI, true>, a, pt, stream, pdl, p, pair);
+        return launch_stream_kernel(stream_kernel<true, EPI, true, true>, a, pt, stream, pdl, p, pair);
     }
     if (a.m == 1) return launch_stream_kernel(stream_simt_kernel<1, EPI>, a, pt, stream, pdl, p, pair);
     if (a.m == 2) return launch_stream_kernel(stream_simt_kernel<2, EPI>, a, pt, stream, pdl, p, pair);
     if (a.m <= 8) return launch_stream_kernel(stream_kernel<false, EPI>, a, pt, stream, pdl, p, pair);
-    return launch_stream_kernel(stream_kernel<true, EPI>, a, pt, stream, pdl, p, pair);
+    if (a.m <= kGroupRows) return launch_stream_kernel(stream_kernel<true, EPI>, a, pt, stream, pdl, p, pair);
+    return launch_stream_kernel(stream_kernel<true, EPI, false, true>, a, pt, stream, pdl, p, pair);
 }
 
 cudaError_t launch_stream(const Args &a, const Parts &pt, int epi, cudaStream_t stream, bool pdl,

@@ -251,7 +251,7 @@ def test_gemv_glu_argument_errors(lib):
     assert lib.q8_gemv_glu(A16, G, GS, U, US, None, None, 1, 32, 64, 2, None) == 1    # no output
     assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 1, 32, 64, 0, None) == 1       # not tiled
     assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 1, 32, 64, 8 | 2, None) == 1   # unknown flag
-    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 17, 32, 64, 2, None) == 2      # m > 16
+    assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 513, 32, 64, 2, None) == 2     # m > 512 (tiled)
     assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 1, 33, 64, 2, None) == 2       # K % 32
     assert lib.q8_gemv_glu(A16, G, GS, U, US, F32, BF, 1, 32, 0, 2, None) == 2        # N = 0
     assert lib.q8_gemv_glu(A16, G, GS, U, US, F32 + 4, BF, 1, 32, 64, 2, None) == 3   # misaligned out
@@ -281,7 +281,7 @@ def test_gemv_residual_norm_argument_errors(lib):
     assert call(eps=f(-1.0)) == 1
     assert call(eps=f(float("inf"))) == 1
     assert call(eps=f(float("nan"))) == 1
-    assert call(m=17) == 2
+    assert call(m=513) == 2
     assert call(K=33) == 2
     assert call(N=0) == 2
     assert call(h=H + 4) == 3                  # misaligned h
@@ -340,3 +340,11 @@ def test_quantized_activation_flag_rules(lib):
     # m = 1, K = 64: 72 bytes of quantized form, so y at x + 64 overlaps it
     assert lib.q8_gemv_ex(A16, B16, C16, A16 + 64, 1, 64, 64, 0, 4 | 2, None) == 1
     assert lib.q8_gemv_parts(A16, None, 1, 1, 64, 4 | 2, None) == 1
+
+
+def test_row_limits(lib):
+    """m > 16 needs the tiled storage (row groups of 16, up to Q8_MAX_CHUNK = 512 rows); 513 rows never."""
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 17, 32, 64, 0, 0, None) == 2
+    assert lib.q8_gemv_ex(A16, B16, C16, D16, 513, 32, 64, 0, 2, None) == 2
+    assert lib.q8_gemv_argmax_ex(A16, B16, C16, D16, None, 17, 32, 64, 0, None) == 2
+    assert lib.q8_gemv_argmax_ex(A16, B16, C16, D16, None, 513, 32, 64, 2, None) == 2
