@@ -81,10 +81,13 @@ def step_bytes(m):
     return sum(gemv_bytes(m, K, N) for K, N in chain_shapes()) + gemv_bytes(m, HIDDEN, VOCAB, argmax=True)
 
 
+STREAM_SOURCES = ("q8_stream.cu", "q8_device.cuh")  # the sources of the kernels the traffic record covers
+
+
 def source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "q8_block_quantized_gemv_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in STREAM_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

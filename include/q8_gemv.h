@@ -47,8 +47,10 @@ typedef struct CUstream_st *q8_stream_t;
 
 /* The most activation rows one call over the tiled storage takes ("plan.rs", `MAX_CHUNK`: the largest prefill chunk
  * a lane compiles, 512; its projections of more rows than the GEMV's 16 run on the tensor cores).  With
- * Q8_FLAG_TILED, m may be 1 .. 512: the rows run as ceil(m / 16) groups of 16 in one launch, each group's CTAs of a
- * column tile side by side so that the weight is streamed from HBM about once. */
+ * Q8_FLAG_TILED, m may be 1 .. 512: from 128 rows a plain product of bf16 activations runs as a tensor-core GEMM
+ * (tcgen05, 128 x 128 output tiles, each 32-row block contracted exactly and folded with its scales); otherwise the
+ * rows run as ceil(m / 16) groups of 16 in one launch, each group's CTAs of a column tile side by side so that the
+ * weight is streamed from HBM about once. */
 #define Q8_MAX_CHUNK 512
 
 typedef enum {
@@ -239,7 +241,8 @@ q8_status q8_quantize(const double *w, int K, int N, int8_t *q, float *s);
 
 /* Reads the device fault word of the current device: nonzero when a kernel's bounded wait on a pipeline barrier ran
  * out (bit 0: a consumer waited about two seconds for a stage's data; bit 1: the producer waited as long for a free
- * stage) and the kernel finished early -- that call's outputs are then wrong.  Synchronous with respect to the
+ * stage; bit 2: a wait of the prefill GEMM ran out) and the kernel finished early -- that call's outputs are then
+ * wrong.  Synchronous with respect to the
  * device.  `clear` != 0 resets the word to 0.  Returns Q8_ERR_ARG for a NULL `fault`, Q8_ERR_CUDA on a CUDA error. */
 q8_status q8_device_fault(unsigned int *fault, int clear);
 

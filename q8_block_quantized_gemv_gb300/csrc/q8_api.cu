@@ -156,6 +156,14 @@ size_t x_bytes(unsigned flags, int m, int K) {
     return (flags & Q8_FLAG_Q8_ACT) ? (size_t)q8_act_bytes(m, K) : (size_t)m * K * 2;
 }
 
+// Whether a tiled call runs on the tcgen05 GEMM (prefill chunks of bf16 activations with a plain store) rather than
+// the row groups of the streaming kernel.  Q8_GEMM=0 in the environment keeps the row groups (for comparison).
+bool use_gemm(int m, int epi, bool qact) {
+    if (m < q8::gemm_min_rows() || epi != q8::kEpiStore || qact) return false;
+    const char *env = getenv("Q8_GEMM");
+    return !(env && env[0] == '0');
+}
+
 q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStream_t stream,
               const q8::Parts *parts = nullptr) {
     const int epi = argmax ? q8::kEpiArgmax : q8::kEpiStore;
@@ -178,6 +186,11 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
     b.ksplit = p.ksplit;
     const bool prefetch = (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0;
     const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
+    if (p.variant == kVariantStream && use_gemm(a.m, epi, qact)) {
+        cudaError_t ce = q8::launch_gemm(b, *parts, stream);
+        if (ce != cudaSuccess) return cuda_fail(ce);
+        return Q8_OK;
+    }
     cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, epi, stream, true, prefetch, qact)
                      : p.variant == Q8_VARIANT_TMA  ? q8::launch_tma(b, argmax, stream, true, prefetch)
                      : p.variant == Q8_VARIANT_SIMT ? q8::launch_simt(b, p.V, argmax, stream)
@@ -430,7 +443,10 @@ extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const
 
 extern "C" q8_status q8_device_fault(unsigned int *fault, int clear) {
     if (!fault) return Q8_ERR_ARG;
+    unsigned gemm = 0;
     cudaError_t e = q8::read_fault_word(fault, clear != 0);
+    if (e == cudaSuccess) e = q8::read_gemm_fault(&gemm, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
+    *fault |= gemm;
     return Q8_OK;
 }

@@ -53,6 +53,11 @@ int stream_max_clusters(int ks);  // clusters of ks stream-kernel CTAs resident 
 cudaError_t launch_stream(const Args &a, const Parts &parts, int epi, cudaStream_t stream, bool pdl,
                           bool prefetch_weights, bool qact);
 cudaError_t read_fault_word(unsigned *out, bool clear);
+
+// Defined in q8_gemm.cu: the tcgen05 GEMM for prefill chunks (tiled storage, bf16 activations, plain store).
+int gemm_min_rows();  // the row count from which the planner takes it
+cudaError_t launch_gemm(const Args &a, const Parts &parts, cudaStream_t stream);
+cudaError_t read_gemm_fault(unsigned *out, bool clear);
 unsigned int *norm_counters();  // device address of the kNormSlots completion counters (null on a CUDA error)
 constexpr int kTmaColumns = 128;
 
