@@ -9,17 +9,18 @@
 // scales into an fp32 carry).  The exact int8 -> bf16 weights and the bf16 activations make every product exact; the
 // block's sums are fp32.
 //
-// Warp roles (288 threads, one CTA per SM; nine warps, so no scheduler holds more than three and each thread may
+// Warp roles (320 threads, one CTA per SM; ten warps, so no scheduler holds more than three and each thread may
 // have 168 registers):
-//   warps 0-7  workers.  For block b they cp.async the activations of block b + 4 (128 rows x 32 values, zero past
-//              m) into a ring stage while thread 0 bulk-copies its weight unit (4 KB, stored q + 128) and 128 scales;
-//              they turn block b's unit into exact bf16 in the canonical no-swizzle K-major layout (8 x 16-byte core
-//              matrices) and signal its stage full; then they fold block b - 3: each thread reads its accumulator
-//              lane (one output row) over half of the columns, multiplies by the block's scales and adds into its
-//              fp32 carry (packed fp32x2), and the warp frees the accumulator buffer;
-//   warp 8     one thread issues each block's two MMAs into one of four accumulator buffers and commits them to the
-//              stage's `empty` barrier and the buffer's `full` barrier.
-// Four accumulator buffers let the MMAs of blocks b - 2 .. b run while block b - 3 is folded.  When the tiles are too
+//   warp 0     one thread loads block b + 4 into a ring stage: the activations (128 rows x 32 values) by a TMA tensor
+//              copy with 64-byte swizzle (rows past m read as zeros), the weight unit (4 KB, stored q + 128) and its
+//              128 scales by two bulk copies, all completing one `loaded` barrier;
+//   warp 1     one thread issues each block's two MMAs into one of four accumulator buffers and commits them to the
+//              stage's `empty` barrier and the buffer's `full` barrier;
+//   warps 2-9  workers: they turn block b's unit into exact bf16 in the canonical no-swizzle K-major layout (8 x
+//              16-byte core matrices) and signal the stage full, then fold block b - 2: each thread reads its
+//              accumulator lane (one output row) over half of the columns, multiplies by the block's scales and adds
+//              into its fp32 carry (packed fp32x2); the warp frees the buffer and its share of the stage.
+// Four accumulator buffers let the MMAs of later blocks run while a block is folded.  When the tiles are too
 // few to fill the SMs, K is split across a thread-block cluster of up to 4 CTAs; their carries are summed through
 // distributed shared memory in rank order (deterministic).  Every mbarrier wait is bounded (about two seconds); a
 // wait that runs out records a fault bit, makes the CTA stop issuing work and drain, and the kernel returns with its
@@ -37,22 +38,21 @@ namespace {
 constexpr int kGM = 128;               // activation rows of a CTA tile (the MMA's M)
 constexpr int kGN = kTmaColumns;       // columns of a CTA tile: one 128-column tile of the tiled storage
 constexpr int kGStages = 8;            // ring stages (one 32-row block each)
-constexpr int kGAhead = 4;             // blocks whose copies a worker keeps in flight
 constexpr int kAccBufs = 4;            // accumulator buffers in tensor memory (128 columns each)
-constexpr int kFoldLag = 3;            // a worker folds block b - 3 after preparing block b
-// A stage is refilled (block b + kGAhead, at the start of iteration b) only after the MMAs and the fold of its
-// previous block (b + kGAhead - kGStages) are done: the fold of that block ran in an earlier iteration.
-static_assert(kGAhead - kGStages < -kFoldLag, "a stage outlives the fold of its block");
-static_assert(kFoldLag < kAccBufs, "the MMAs of a block do not wait for the fold that precedes them in the loop");
+constexpr int kLoadWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kWorkWarp0 = 2;             // warps 2..9: TMEM lane quarters 2, 3, 0, 1 (twice: two column halves)
 constexpr int kWorkWarps = 8;
-constexpr int kMmaWarp = kWorkWarps;      // warp 8
-constexpr int kWorkers = 32 * kWorkWarps;
-constexpr int kGThreads = kWorkers + 32;
-constexpr int kFoldCols = kGN / 2;        // columns one worker folds (warps 0-3 the first half, 4-7 the second)
+constexpr int kGThreads = 32 * (kWorkWarp0 + kWorkWarps);
+constexpr int kFoldCols = kGN / 2;        // columns one worker folds
+constexpr int kFoldLag = 2;               // a worker folds block b - 2 after converting block b
 
-// Stage layout (bytes): bf16 A [128 x 32] and B [128 x 32] in core-matrix order, the raw unit, its 128 scales.
-constexpr int kAOff = 0, kBOff = 8192, kRawOff = 16384, kSOff = 20480, kStageBytes = 20992;
-constexpr int kUnitTx = 4096 + 512;        // bytes the bulk copies of one block deliver
+// Stage layout (bytes): bf16 A [128 rows x 64 bytes] as the TMA writes it (64-byte swizzle), B [128 x 32] in
+// core-matrix order, the raw unit, its 128 scales; stages 1024-byte aligned (the swizzle pattern repeats every 512).
+constexpr int kAOff = 0, kBOff = 8192, kRawOff = 16384, kSOff = 20480, kStageBytes = 21504;
+constexpr int kBlockTx = 8192 + 4096 + 512;  // bytes the copies of one block deliver
+static_assert(kFoldLag < kAccBufs, "the MMAs of a block never wait for a fold that comes after it");
+static_assert(kStageBytes % 1024 == 0, "swizzled stages stay aligned");
 constexpr int kMaxSplit = 4;               // CTAs of a cluster splitting K
 constexpr int kRedStride = kGN + 4;        // floats a row of the split-K reduction slab (padded)
 static_assert(kGM * kRedStride * 4 <= kGStages * kStageBytes, "the reduction slab fits in the ring");
@@ -115,22 +115,24 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, unsigned parity, volatil
     }
 }
 
-__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, unsigned bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Shared-memory matrix descriptor: no swizzle, K-major core matrices of 8 rows x 16 bytes; lbo = byte step between
-// core matrices along K, sbo = byte step between 8-row groups; bits 46-48 hold the fixed 0b001.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor, K-major: lbo = byte step between core matrices along K (unused with a swizzle),
+// sbo = byte step between 8-row groups, layout = 0 (no swizzle: core matrices of 8 rows x 16 bytes) or 4 (64-byte
+// swizzle: rows of 64 bytes, 16-byte chunks XOR-ed with row bits 1-2); bits 46-48 hold the fixed 0b001.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout = 0) {
     return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
-           (1ull << 46);
+           (1ull << 46) | ((uint64_t)layout << 61);
+}
+
+__device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int k, int row, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(map), "r"(k), "r"(row), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // Instruction descriptor of kind::f16: fp32 D (bits 4-5 = 1), bf16 A and B (bits 7-9, 10-12 = 1), both K-major,
@@ -187,7 +189,7 @@ template <int E> __device__ __forceinline__ uint32_t stored_to_bf16x2(uint32_t u
 }
 
 __global__ void __maxnreg__(168)
-    gemm_kernel(Args a, const __grid_constant__ Parts parts) {
+    gemm_kernel(Args a, const __grid_constant__ Parts parts, const __grid_constant__ CUtensorMap xmap) {
     namespace cg = cooperative_groups;
     extern __shared__ __align__(1024) unsigned char smem_g[];
     uint64_t *loaded = reinterpret_cast<uint64_t *>(smem_g + kBarOff);
@@ -208,9 +210,9 @@ __global__ void __maxnreg__(168)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kGStages; ++i) {
-            bar_init(&loaded[i], 1);       // thread 0's expect_tx; the bulk copies' bytes complete it
-            bar_init(&full[i], kWorkWarps);  // one thread of each worker warp
-            bar_init(&empty[i], 1 + kWorkWarps);  // the MMA commit and the folds (they read the stage's scales)
+            bar_init(&loaded[i], 1);               // thread 0's expect_tx; the bulk copies' bytes complete it
+            bar_init(&full[i], kWorkWarps);        // one thread of each worker warp
+            bar_init(&empty[i], 1 + kWorkWarps);   // the MMA commit and the folds (they read the stage's scales)
         }
         for (int i = 0; i < kAccBufs; ++i) {
             bar_init(&acc_full[i], 1);
@@ -232,117 +234,44 @@ __global__ void __maxnreg__(168)
     const uint32_t tbase = *tmem_slot;
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    const int quarter = warp & 3;              // the TMEM lanes a worker warp may read
-    const int col0 = kFoldCols * (warp >> 2);  // the columns it folds
-    const int r = 32 * quarter + lane;         // the output row a worker thread folds
+    const int quarter = warp & 3;                            // the TMEM lanes a worker warp may read
+    const int col0 = kFoldCols * ((warp - kWorkWarp0) >> 2);  // the columns it folds
+    const int r = 32 * quarter + lane;                       // the output row a worker thread folds
     unsigned long long acc[kFoldCols / 2];
 #pragma unroll
     for (int j = 0; j < kFoldCols / 2; ++j) acc[j] = 0ull;
 
-    if (warp < kWorkWarps) {
-        // ---- workers: load block i + 4, convert block i, fold block i - 3 (i counts this CTA's blocks) ----
-        const int l = threadIdx.x;
-        const unsigned char *qbase =
-            reinterpret_cast<const unsigned char *>(a.q) + ((size_t)tile * a.nb + kb0) * 4096;
-        const float *sbase = a.s + ((size_t)tile * a.nb + kb0) * kGN;
-        auto issue = [&](int i) {
-            unsigned char *st = smem_g + (i % kGStages) * kStageBytes;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {  // activations: 128 rows x 4 chunks of 8 values
-                const int c = l + kWorkers * k, rr = c >> 2, kc = c & 3;
-                const int row = row0 + rr;
-                const bool live = row < a.m;
-                const uint16_t *src =
-                    a.x + (size_t)(live ? row : 0) * a.K + (size_t)(kb0 + i) * kBlock + 8 * kc;
-                cp_async16_zfill(st + kAOff + (rr >> 3) * 512 + kc * 128 + (rr & 7) * 16, src, live ? 16u : 0u);
-            }
-            if (l == 0) {  // the weight unit and its scales: two bulk copies
-                bar_arrive_tx(&loaded[i % kGStages], kUnitTx);
-                bulk_copy(st + kRawOff, qbase + (size_t)i * 4096, 4096, &loaded[i % kGStages]);
-                bulk_copy(st + kSOff, sbase + (size_t)i * kGN, 512, &loaded[i % kGStages]);
-            }
-        };
-        auto fold = [&](int f) -> bool {
-            const int buf = f % kAccBufs;
-            if (!bar_wait(&acc_full[buf], (f / kAccBufs) & 1, abort)) return false;
-            tc_fence_after();
-            uint32_t v[kFoldCols / 32][32];
-#pragma unroll
-            for (int c = 0; c < kFoldCols / 32; ++c)
-                tmem_ld32(tbase + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kGN + col0 + 32 * c), v[c]);
-            // the block's scales: landed before the stage's `loaded` wait of block f; the stage is refilled only
-            // after every warp's fold of block f has arrived on its `empty` barrier
-            const unsigned long long *sp = reinterpret_cast<const unsigned long long *>(
-                smem_g + (f % kGStages) * kStageBytes + kSOff + col0 * 4);
-            tmem_wait();
-#pragma unroll
-            for (int c = 0; c < kFoldCols / 32; ++c)
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    acc[16 * c + j] = fma2(sp[16 * c + j], pack2(v[c][2 * j], v[c][2 * j + 1]), acc[16 * c + j]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                bar_arrive(&acc_empty[buf]);
-                bar_arrive(&empty[f % kGStages]);
-            }
-            return true;
-        };
-
-        bool ok = true;
-        int issued = 0;  // blocks whose copies were issued
-        for (int i = 0; i < kGAhead; ++i) {  // one commit group per block, empty past the last
-            if (i < n) {
-                issue(i);
+    if (warp == kLoadWarp) {
+        // ---- loader (one thread): the copies of block i (i counts this CTA's blocks) ----
+        if (lane == 0) {
+            const unsigned char *qbase =
+                reinterpret_cast<const unsigned char *>(a.q) + ((size_t)tile * a.nb + kb0) * 4096;
+            const float *sbase = a.s + ((size_t)tile * a.nb + kb0) * kGN;
+            int issued = 0;
+            for (int i = 0; i < n; ++i) {
+                const int st = i % kGStages;
+                // the stage was last used by block i - kGStages: its MMAs and every worker's fold are done
+                if (i >= kGStages && !bar_wait(&empty[st], ((i / kGStages) - 1) & 1, abort)) break;
+                unsigned char *sp = smem_g + st * kStageBytes;
+                bar_arrive_tx(&loaded[st], kBlockTx);
+                tma_rows(sp + kAOff, &xmap, (kb0 + i) * kBlock, row0, &loaded[st]);
+                bulk_copy(sp + kRawOff, qbase + (size_t)i * 4096, 4096, &loaded[st]);
+                bulk_copy(sp + kSOff, sbase + (size_t)i * kGN, 512, &loaded[st]);
                 ++issued;
             }
-            cp_commit();
-        }
-        for (int i = 0; i < n && ok; ++i) {
-            const int ahead = i + kGAhead;
-            if (ahead < n) {
-                // the stage of block `ahead` was last used by block ahead - kGStages
-                if (ahead >= kGStages) ok = bar_wait(&empty[ahead % kGStages], ((ahead / kGStages) - 1) & 1, abort);
-                if (ok) {
-                    issue(ahead);
-                    ++issued;
-                }
-            }
-            cp_commit();
-            cp_wait<kGAhead>();  // this thread's activation copies of block i have landed
-            if (ok) ok = bar_wait(&loaded[i % kGStages], (i / kGStages) & 1, abort);  // and the unit
-            if (!ok) break;
-            unsigned char *st = smem_g + (i % kGStages) * kStageBytes;
-            {
-                // this thread's chunk of the unit: segment 4s + h = warp, lane 4g + u
-                const int s = warp >> 2, h = warp & 3, g = lane >> 2, u = lane & 3;
-                const uint4 raw = *reinterpret_cast<const uint4 *>(st + kRawOff + l * 16);
-                const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int j = 4 * h + w;  // 8-column slice: B rows 8j .. 8j + 7, this word's row 8j + g
-                    const uint2 cv = make_uint2(stored_to_bf16x2<0>(words[w]), stored_to_bf16x2<2>(words[w]));
-                    *reinterpret_cast<uint2 *>(st + kBOff + j * 512 + (2 * s + (u >> 1)) * 128 + g * 16 +
-                                               (u & 1) * 8) = cv;
-                }
-            }
-            fence_async_smem();  // this thread's generic-proxy writes (and landed copies) before the MMAs read them
-            __syncwarp();
-            if (lane == 0) bar_arrive(&full[i % kGStages]);
-            if (i >= kFoldLag) ok = fold(i - kFoldLag);
-        }
-        for (int f = n - kFoldLag < 0 ? 0 : n - kFoldLag; f < n && ok; ++f) ok = fold(f);
-        cp_wait<0>();
-        if (!ok && l == 0) {
-            // after an abort: the bulk copies thread 0 started land before the shared memory is reused or freed
-            // (the last fill of each stage; earlier fills were waited for before their stage was refilled)
-            for (int i = issued - kGStages < 0 ? 0 : issued - kGStages; i < issued; ++i) {
-                const uint64_t t0 = now_ns();
-                while (!bar_try_wait(&loaded[i % kGStages], (i / kGStages) & 1) && now_ns() - t0 < 2000000000ull) {
+            if (*abort) {
+                // the copies started land before the shared memory is reused or freed (the last fill of each
+                // stage; earlier fills were waited for before their stage was refilled)
+                for (int i = issued - kGStages < 0 ? 0 : issued - kGStages; i < issued; ++i) {
+                    const uint64_t t0 = now_ns();
+                    while (!bar_try_wait(&loaded[i % kGStages], (i / kGStages) & 1) &&
+                           now_ns() - t0 < 2000000000ull) {
+                    }
                 }
             }
         }
-    } else {
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
         // ---- MMA issue (one thread) ----
         if (lane == 0) {
             for (int i = 0; i < n; ++i) {
@@ -354,17 +283,67 @@ __global__ void __maxnreg__(168)
                 const uint32_t sb = smem_u32(smem_g + st * kStageBytes + kBOff);
                 const uint32_t td = tbase + (uint32_t)(buf * kGN);
 #pragma unroll
-                for (int k = 0; k < 2; ++k)  // K = 16 each: core matrices 2k, 2k + 1 along K
-                    mma_bf16(td, smem_desc(sa + 256 * k, 128, 512), smem_desc(sb + 256 * k, 128, 512), k);
+                for (int k = 0; k < 2; ++k)  // K = 16 each: 32 bytes into A's 64-byte rows; B core matrices 2k, 2k + 1
+                    mma_bf16(td, smem_desc(sa + 32 * k, 16, 512, 4), smem_desc(sb + 256 * k, 128, 512), k);
                 mma_commit(&empty[st]);
                 mma_commit(&acc_full[buf]);
             }
         }
         __syncwarp();
+    } else {
+        // ---- workers: convert block i, fold block i - kFoldLag ----
+        const int c = (warp - kWorkWarp0) * 32 + lane;  // this thread's 16-byte chunk of a unit
+        const int seg = c >> 5, L = c & 31;
+        const int s = seg >> 2, h = seg & 3, g = L >> 2, u = L & 3;  // segment 4s + h, lane 4g + u
+        auto fold = [&](int f) -> bool {
+            const int buf = f % kAccBufs, st = f % kGStages;
+            if (!bar_wait(&acc_full[buf], (f / kAccBufs) & 1, abort)) return false;
+            tc_fence_after();
+            uint32_t v[kFoldCols / 32][32];
+#pragma unroll
+            for (int cc = 0; cc < kFoldCols / 32; ++cc)
+                tmem_ld32(tbase + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kGN + col0 + 32 * cc), v[cc]);
+            // the block's scales (landed with the `loaded` wait of block f; the stage is refilled only after every
+            // worker's fold of block f has arrived on its `empty` barrier)
+            const unsigned long long *sp = reinterpret_cast<const unsigned long long *>(
+                smem_g + st * kStageBytes + kSOff + col0 * 4);
+            tmem_wait();
+#pragma unroll
+            for (int cc = 0; cc < kFoldCols / 32; ++cc)
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    acc[16 * cc + j] = fma2(sp[16 * cc + j], pack2(v[cc][2 * j], v[cc][2 * j + 1]), acc[16 * cc + j]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                bar_arrive(&acc_empty[buf]);
+                bar_arrive(&empty[st]);
+            }
+            return true;
+        };
+        bool ok = true;
+        for (int i = 0; i < n && ok; ++i) {
+            const int st = i % kGStages;
+            if (!bar_wait(&loaded[st], (i / kGStages) & 1, abort)) break;
+            unsigned char *sp = smem_g + st * kStageBytes;
+            const uint4 raw = *reinterpret_cast<const uint4 *>(sp + kRawOff + c * 16);
+            const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int j = 4 * h + w;  // 8-column slice: B rows 8j .. 8j + 7, this word's row 8j + g
+                const uint2 cv = make_uint2(stored_to_bf16x2<0>(words[w]), stored_to_bf16x2<2>(words[w]));
+                *reinterpret_cast<uint2 *>(sp + kBOff + j * 512 + (2 * s + (u >> 1)) * 128 + g * 16 + (u & 1) * 8) = cv;
+            }
+            fence_async_smem();  // this thread's generic-proxy writes before the MMAs read them
+            __syncwarp();
+            if (lane == 0) bar_arrive(&full[st]);
+            if (i >= kFoldLag) ok = fold(i - kFoldLag);
+        }
+        for (int f = n - kFoldLag < 0 ? 0 : n - kFoldLag; f < n && ok; ++f) ok = fold(f);
     }
 
     // Drain: every MMA this CTA issued has completed (the last block's commit reached acc_full, waited on by the
-    // workers) and every copy has landed, unless the CTA aborted; after an abort, one more commit waited on with a
+    // fold warps) and every copy has landed, unless the CTA aborted; after an abort, one more commit waited on with a
     // bound covers any MMA still running.
     tc_fence_before();
     __syncthreads();
@@ -380,7 +359,7 @@ __global__ void __maxnreg__(168)
     // The carries to y (rows < m; pad columns n >= N exactly 0): directly, or through the cluster when K is split.
     if (ks == 1) {
         const int row = row0 + r;
-        if (warp < kWorkWarps && row < a.m && !*abort) {
+        if (warp >= kWorkWarp0 && row < a.m && !*abort) {
             float *yrow = a.y + (size_t)row * a.Np;
 #pragma unroll
             for (int j = 0; j < kFoldCols / 4; ++j) {
@@ -398,7 +377,7 @@ __global__ void __maxnreg__(168)
     } else {
         // every CTA's carries into its slab (the ring is idle: all copies landed, all MMAs done)
         float *red = reinterpret_cast<float *>(smem_g);
-        if (warp < kWorkWarps) {
+        if (warp >= kWorkWarp0) {
 #pragma unroll
             for (int j = 0; j < kFoldCols / 4; ++j) {
                 float lo0, hi0, lo1, hi1;
@@ -476,7 +455,9 @@ cudaError_t launch_gemm(const Args &a, const Parts &pt, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_kernel, a, pt);
+    CUtensorMap xmap;
+    if (!encode_bf16_rows(&xmap, a.x, a.m, a.K, kBlock, kGM)) return cudaErrorNotSupported;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel, a, pt, xmap);
 }
 
 }  // namespace q8

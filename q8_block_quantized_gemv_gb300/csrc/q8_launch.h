@@ -1,6 +1,7 @@
 // Host-side launch helpers shared by the kernel translation units of libq8gemv.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "q8_device.cuh"
@@ -43,6 +44,9 @@ cudaError_t launch_mma(const Args &a, int V, bool argmax, cudaStream_t stream);
 
 // Defined in q8_tma.cu.
 bool tma_supported(const Args &a);
+// A tensor map of bf16 rows [rows][K] (row pitch K), boxes of box_k x box_rows values, 64-byte swizzle, zero fill
+// past the last row; false when the driver entry point or the encoding fails.
+bool encode_bf16_rows(CUtensorMap *map, const void *base, int rows, int K, int box_k, int box_rows);
 cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl, bool prefetch_weights);
 
 // Defined in q8_stream.cu (the tiled layout).

@@ -375,6 +375,12 @@ static bool encode_2d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map
                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_bf16_rows(CUtensorMap *map, const void *base, int rows, int K, int box_k, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+    return encode && encode_2d(encode, map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, (cuuint64_t)K, (cuuint64_t)rows,
+                               (cuuint64_t)K * 2, (cuuint32_t)box_k, (cuuint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 template <int NT, bool ARGMAX>
 static cudaError_t launch_tma_nt(const Args &a, const CUtensorMap &qmap, const CUtensorMap &smap,
                                  const CUtensorMap &xmap, cudaStream_t stream, bool pdl, bool prefetch) {
