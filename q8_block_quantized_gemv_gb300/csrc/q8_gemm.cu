@@ -9,17 +9,17 @@
 // scales into an fp32 carry).  The exact int8 -> bf16 weights and the bf16 activations make every product exact; the
 // block's sums are fp32.
 //
-// Warp roles (320 threads, one CTA per SM; ten warps, so no scheduler holds more than three and each thread may
-// have 168 registers):
+// Warp roles (576 threads, one CTA per SM; 18 warps, at most five a scheduler, 96 registers a thread):
 //   warp 0     one thread loads block b + 4 into a ring stage: the activations (128 rows x 32 values) by a TMA tensor
 //              copy with 64-byte swizzle (rows past m read as zeros), the weight unit (4 KB, stored q + 128) and its
 //              128 scales by two bulk copies, all completing one `loaded` barrier;
 //   warp 1     one thread issues each block's two MMAs into one of four accumulator buffers and commits them to the
 //              stage's `empty` barrier and the buffer's `full` barrier;
-//   warps 2-9  workers: they turn block b's unit into exact bf16 in the canonical no-swizzle K-major layout (8 x
-//              16-byte core matrices) and signal the stage full, then fold block b - 2: each thread reads its
-//              accumulator lane (one output row) over half of the columns, multiplies by the block's scales and adds
-//              into its fp32 carry (packed fp32x2); the warp frees the buffer and its share of the stage.
+//   warps 2-17 workers: they turn block b's unit into exact bf16 in the canonical no-swizzle K-major layout (8 x
+//              16-byte core matrices; two words a thread) and signal the stage full, then fold block b - 2: each
+//              thread reads its accumulator lane (one output row) over a quarter of the columns, multiplies by the
+//              block's scales and adds into its fp32 carry (packed fp32x2); the warp frees the buffer and its share
+//              of the stage.
 // Four accumulator buffers let the MMAs of later blocks run while a block is folded.  When the tiles are too
 // few to fill the SMs, K is split across a thread-block cluster of up to 4 CTAs; their carries are summed through
 // distributed shared memory in rank order (deterministic).  Every mbarrier wait is bounded (about two seconds); a
@@ -41,10 +41,10 @@ constexpr int kGStages = 8;            // ring stages (one 32-row block each)
 constexpr int kAccBufs = 4;            // accumulator buffers in tensor memory (128 columns each)
 constexpr int kLoadWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kWorkWarp0 = 2;             // warps 2..9: TMEM lane quarters 2, 3, 0, 1 (twice: two column halves)
-constexpr int kWorkWarps = 8;
+constexpr int kWorkWarp0 = 2;             // warps 2..17: TMEM lane quarters 2, 3, 0, 1 (four times: column quarters)
+constexpr int kWorkWarps = 16;
 constexpr int kGThreads = 32 * (kWorkWarp0 + kWorkWarps);
-constexpr int kFoldCols = kGN / 2;        // columns one worker folds
+constexpr int kFoldCols = kGN / 4;        // columns one worker folds
 constexpr int kFoldLag = 2;               // a worker folds block b - 2 after converting block b
 
 // Stage layout (bytes): bf16 A [128 rows x 64 bytes] as the TMA writes it (64-byte swizzle), B [128 x 32] in
@@ -188,7 +188,7 @@ template <int E> __device__ __forceinline__ uint32_t stored_to_bf16x2(uint32_t u
     return d;
 }
 
-__global__ void __maxnreg__(168)
+__global__ void __maxnreg__(96)
     gemm_kernel(Args a, const __grid_constant__ Parts parts, const __grid_constant__ CUtensorMap xmap) {
     namespace cg = cooperative_groups;
     extern __shared__ __align__(1024) unsigned char smem_g[];
@@ -235,7 +235,7 @@ __global__ void __maxnreg__(168)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int quarter = warp & 3;                            // the TMEM lanes a worker warp may read
-    const int col0 = kFoldCols * ((warp - kWorkWarp0) >> 2);  // the columns it folds
+    const int col0 = kFoldCols * ((warp - kWorkWarp0) >> 2);  // the columns it folds (one quarter of them)
     const int r = 32 * quarter + lane;                       // the output row a worker thread folds
     unsigned long long acc[kFoldCols / 2];
 #pragma unroll
@@ -292,7 +292,8 @@ __global__ void __maxnreg__(168)
         __syncwarp();
     } else {
         // ---- workers: convert block i, fold block i - kFoldLag ----
-        const int c = (warp - kWorkWarp0) * 32 + lane;  // this thread's 16-byte chunk of a unit
+        const int idx = (warp - kWorkWarp0) * 32 + lane;
+        const int c = idx >> 1, half = idx & 1;  // this thread's 16-byte chunk of a unit, and which two of its words
         const int seg = c >> 5, L = c & 31;
         const int s = seg >> 2, h = seg & 3, g = L >> 2, u = L & 3;  // segment 4s + h, lane 4g + u
         auto fold = [&](int f) -> bool {
@@ -326,12 +327,13 @@ __global__ void __maxnreg__(168)
             const int st = i % kGStages;
             if (!bar_wait(&loaded[st], (i / kGStages) & 1, abort)) break;
             unsigned char *sp = smem_g + st * kStageBytes;
-            const uint4 raw = *reinterpret_cast<const uint4 *>(sp + kRawOff + c * 16);
-            const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+            const uint2 raw = *reinterpret_cast<const uint2 *>(sp + kRawOff + c * 16 + half * 8);
+            const uint32_t words[2] = {raw.x, raw.y};
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
+            for (int ww = 0; ww < 2; ++ww) {
+                const int w = 2 * half + ww;
                 const int j = 4 * h + w;  // 8-column slice: B rows 8j .. 8j + 7, this word's row 8j + g
-                const uint2 cv = make_uint2(stored_to_bf16x2<0>(words[w]), stored_to_bf16x2<2>(words[w]));
+                const uint2 cv = make_uint2(stored_to_bf16x2<0>(words[ww]), stored_to_bf16x2<2>(words[ww]));
                 *reinterpret_cast<uint2 *>(sp + kBOff + j * 512 + (2 * s + (u >> 1)) * 128 + g * 16 + (u & 1) * 8) = cv;
             }
             fence_async_smem();  // this thread's generic-proxy writes before the MMAs read them
