@@ -15,8 +15,8 @@
 //              128 scales by two bulk copies, all completing one `loaded` barrier;
 //   warp 1     one thread issues each block's two MMAs into one of four accumulator buffers and commits them to the
 //              stage's `empty` barrier and the buffer's `full` barrier;
-//   warps 2-17 workers: they turn block b's unit into exact bf16 in the canonical no-swizzle K-major layout (8 x
-//              16-byte core matrices; two words a thread) and signal the stage full, then fold block b - 2: each
+//   warps 2-17 workers: they turn block b's unit into exact bf16 in the same 64-byte swizzled K-major layout (two
+//              words a thread) and signal the stage full, then fold block b - 3: each
 //              thread reads its accumulator lane (one output row) over a quarter of the columns, multiplies by the
 //              block's scales and adds into its fp32 carry (packed fp32x2); the warp frees the buffer and its share
 //              of the stage.
@@ -45,10 +45,11 @@ constexpr int kWorkWarp0 = 2;             // warps 2..17: TMEM lane quarters 2, 
 constexpr int kWorkWarps = 16;
 constexpr int kGThreads = 32 * (kWorkWarp0 + kWorkWarps);
 constexpr int kFoldCols = kGN / 4;        // columns one worker folds
-constexpr int kFoldLag = 2;               // a worker folds block b - 2 after converting block b
+constexpr int kFoldLag = 3;               // a worker folds block b - 3 after converting block b
 
-// Stage layout (bytes): bf16 A [128 rows x 64 bytes] as the TMA writes it (64-byte swizzle), B [128 x 32] in
-// core-matrix order, the raw unit, its 128 scales; stages 1024-byte aligned (the swizzle pattern repeats every 512).
+// Stage layout (bytes): bf16 A [128 rows x 64 bytes] as the TMA writes it (64-byte swizzle), B [128 weight columns x
+// 64 bytes] in the same swizzle, the raw unit, its 128 scales; stages 1024-byte aligned (the swizzle pattern repeats
+// every 512 bytes).
 constexpr int kAOff = 0, kBOff = 8192, kRawOff = 16384, kSOff = 20480, kStageBytes = 21504;
 constexpr int kBlockTx = 8192 + 4096 + 512;  // bytes the copies of one block deliver
 static_assert(kFoldLag < kAccBufs, "the MMAs of a block never wait for a fold that comes after it");
@@ -283,8 +284,8 @@ __global__ void __maxnreg__(96)
                 const uint32_t sb = smem_u32(smem_g + st * kStageBytes + kBOff);
                 const uint32_t td = tbase + (uint32_t)(buf * kGN);
 #pragma unroll
-                for (int k = 0; k < 2; ++k)  // K = 16 each: 32 bytes into A's 64-byte rows; B core matrices 2k, 2k + 1
-                    mma_bf16(td, smem_desc(sa + 32 * k, 16, 512, 4), smem_desc(sb + 256 * k, 128, 512), k);
+                for (int k = 0; k < 2; ++k)  // K = 16 each: 32 bytes into the 64-byte rows of A and B
+                    mma_bf16(td, smem_desc(sa + 32 * k, 16, 512, 4), smem_desc(sb + 32 * k, 16, 512, 4), k);
                 mma_commit(&empty[st]);
                 mma_commit(&acc_full[buf]);
             }
@@ -334,7 +335,10 @@ __global__ void __maxnreg__(96)
                 const int w = 2 * half + ww;
                 const int j = 4 * h + w;  // 8-column slice: B rows 8j .. 8j + 7, this word's row 8j + g
                 const uint2 cv = make_uint2(stored_to_bf16x2<0>(words[ww]), stored_to_bf16x2<2>(words[ww]));
-                *reinterpret_cast<uint2 *>(sp + kBOff + j * 512 + (2 * s + (u >> 1)) * 128 + g * 16 + (u & 1) * 8) = cv;
+                // B row (weight column) nr = 8j + g holds its 32 K values in 64 bytes; 16-byte chunk kc = 2s + u / 2
+                // sits at chunk kc ^ ((nr >> 1) & 3) (the 64-byte swizzle), 8 bytes in for odd u
+                const int nr = 8 * j + g, kc = 2 * s + (u >> 1);
+                *reinterpret_cast<uint2 *>(sp + kBOff + nr * 64 + ((kc ^ ((nr >> 1) & 3)) << 4) + (u & 1) * 8) = cv;
             }
             fence_async_smem();  // this thread's generic-proxy writes before the MMAs read them
             __syncwarp();
