@@ -157,11 +157,16 @@ size_t x_bytes(unsigned flags, int m, int K) {
 }
 
 // Whether a tiled call runs on the tcgen05 GEMM (prefill chunks of bf16 activations with a plain store) rather than
-// the row groups of the streaming kernel.  Q8_GEMM=0 in the environment keeps the row groups (for comparison).
-bool use_gemm(int m, int epi, bool qact) {
+// the row groups of the streaming kernel: from gemm_min_rows() rows, when its 128 x 128 tiles (times the largest K
+// split, 4) give at least 64 CTAs; a narrow weight keeps the row groups, whose grid is 8 times finer.  Q8_GEMM=0 in
+// the environment keeps the row groups, Q8_GEMM=1 takes the GEMM for every such call whatever its width (both for
+// comparison and tests).
+bool use_gemm(int m, int epi, bool qact, long long col_tiles) {
     if (m < q8::gemm_min_rows() || epi != q8::kEpiStore || qact) return false;
     const char *env = getenv("Q8_GEMM");
-    return !(env && env[0] == '0');
+    if (env && env[0] == '0') return false;
+    if (env && env[0] == '1') return true;
+    return col_tiles * ((m + 127) / 128) * 4 >= 64;
 }
 
 q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStream_t stream,
@@ -186,7 +191,7 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
     b.ksplit = p.ksplit;
     const bool prefetch = (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0;
     const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
-    if (p.variant == kVariantStream && use_gemm(a.m, epi, qact)) {
+    if (p.variant == kVariantStream && use_gemm(a.m, epi, qact, parts->tile_end[parts->count - 1])) {
         cudaError_t ce = q8::launch_gemm(b, *parts, stream);
         if (ce != cudaSuccess) return cuda_fail(ce);
         return Q8_OK;

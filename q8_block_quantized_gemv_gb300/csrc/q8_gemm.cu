@@ -27,6 +27,7 @@
 // tensor memory freed.
 #include <stdlib.h>
 
+#include <atomic>
 #include <cooperative_groups.h>
 
 #include "q8_launch.h"
@@ -430,18 +431,51 @@ cudaError_t read_gemm_fault(unsigned *out, bool clear) {
     return cudaMemcpyToSymbol(g_gemm_fault, &zero, sizeof(unsigned));
 }
 
+// Clusters of ks GEMM CTAs resident at once on this device (0: unknown); asked once per device and size.
+static int max_clusters(int ks) {
+    static std::atomic<int> cache[64][kMaxSplit + 1];  // 0: not asked yet; else the count + 1
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > kMaxSplit) return 0;
+    const int known = cache[dev][ks].load(std::memory_order_relaxed);
+    if (known > 0) return known - 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, (unsigned)ks);
+    cfg.blockDim = dim3(kGThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)ks;
+    cfg.attrs = attr;
+    cfg.numAttrs = ks > 1 ? 1 : 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // the failed query's error is not the caller's
+        return 0;
+    }
+    cache[dev][ks].store(n + 1, std::memory_order_relaxed);
+    return n;
+}
+
 cudaError_t launch_gemm(const Args &a, const Parts &pt, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
     if (e != cudaSuccess) return e;
-    // K split: the largest of 1 .. 4 that keeps every CTA of one wave resident (one CTA per SM)
+    // K split: the largest of 1 .. 4 that keeps every CTA of one wave resident (one CTA per SM), lowered while the
+    // clusters of ks CTAs would not all fit at once (a cluster's CTAs share one GPC)
     const long long ctas = (long long)pt.tile_end[pt.count - 1] * ((a.m + kGM - 1) / kGM);
     long long ks = sms / ctas;
     if (ks > kMaxSplit) ks = kMaxSplit;
     if (ks > a.nb) ks = a.nb;
     if (ks < 1) ks = 1;
+    while (ks > 1) {
+        const int fit = max_clusters((int)ks);
+        if (fit <= 0 || ctas <= fit) break;
+        --ks;
+    }
     const char *force = getenv("Q8_KSPLIT");
     if (force) {
         const int f = atoi(force);

@@ -14,6 +14,12 @@ from test_gpu_parity import _assert_close
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True)
+def _gemm_whatever_the_width(monkeypatch):
+    """Narrow weights would otherwise take the row groups; these tests are about the GEMM."""
+    monkeypatch.setenv("Q8_GEMM", "1")
+
+
 @pytest.fixture(scope="module")
 def dev():
     torch = pytest.importorskip("torch")
