@@ -15,6 +15,8 @@ Contents, each citing the passage it follows (page titles as printed on the page
 * :func:`quantize` -- ``from_q8.rs`` ``quantize``: the Q8_0 rule and its rejections.
 * :func:`repack` -- ``from_q8.rs`` ``Q8Part`` (the host repacks the checkpoint's blocks into the int8 values and the
   fp32 scales); the block layout is the reading stated in the design notes (36-byte blocks, fp32 scale first).
+* :func:`repack_f16` -- the same repack from GGML-style blocks (``plan.rs`` names the checkpoint format
+  ``GgmlType::Q8_0``): 34-byte blocks, an IEEE binary16 scale then 32 int8 values.
 * :func:`dequantize` -- ``from_q8.rs`` module doc, w = q * d.
 * :func:`residual_norm` -- ``plan.rs`` ``Launch::Fold`` of a projection with ``Launch::Norm`` (``gemv_norm_epilogue``:
   a projection with the residual add and the next norm in its epilogue; the norm launch is the lane's "rmsnorm"):
@@ -190,6 +192,32 @@ def repack(blocks: bytes | np.ndarray, K: int, N: int):
     q = np.zeros((K, Np), dtype=np.int8)
     s = np.zeros((nb, Np), dtype=np.float32)
     q[:, :N] = vals.reshape(N, K).T      # column n's blocks b = 0, 1, ... are its rows 32b .. 32b + 31
+    s[:, :N] = d.T
+    return q, s
+
+
+def repack_f16(blocks: bytes | np.ndarray, K: int, N: int):
+    """The int8 values [K, Np] and fp32 scales [K/32, Np] from GGML-style checkpoint blocks (``plan.rs``
+    ``GgmlType::Q8_0``; ``from_q8.rs`` ``Q8Part``).
+
+    The blocks are column-major by block as :func:`repack` reads them, each 34 bytes: a little-endian IEEE binary16
+    scale d (widened to fp32 exactly: every binary16 value is a binary32 value) followed by 32 int8 values.  Pad
+    columns come out zero.  Returns None when a value is -128 or a scale is not finite."""
+    if K <= 0 or K % Q8_BLOCK or N <= 0:
+        return None
+    nb = K // Q8_BLOCK
+    raw = np.frombuffer(bytes(blocks), dtype=np.uint8)
+    if raw.size != N * nb * 34:
+        raise ValueError("block buffer size does not match K and N")
+    rec = raw.reshape(N, nb, 34)
+    d = rec[:, :, 0:2].copy().view("<f2").reshape(N, nb).astype(np.float32)
+    vals = rec[:, :, 2:34].copy().view(np.int8).reshape(N, nb, Q8_BLOCK)
+    if np.any(vals == -128) or not np.all(np.isfinite(d)):
+        return None
+    Np = padded_n(N)
+    q = np.zeros((K, Np), dtype=np.int8)
+    s = np.zeros((nb, Np), dtype=np.float32)
+    q[:, :N] = vals.reshape(N, K).T
     s[:, :N] = d.T
     return q, s
 

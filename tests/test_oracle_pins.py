@@ -317,6 +317,50 @@ def test_repack_round_trip_and_rejects_minus_128():
     assert oracle.repack(_blocks_of(q2, s, 40), 128, 40) is None
 
 
+def _f16_blocks_of(q, d_bits, N):
+    """GGML-style blocks written field by field: the binary16 scale's bit pattern, then the 32 values."""
+    K = q.shape[0]
+    out = bytearray()
+    for n in range(N):
+        for b in range(K // 32):
+            out += struct.pack("<H", int(d_bits[b, n]))
+            out += struct.pack("<32b", *[int(v) for v in q[32 * b:32 * b + 32, n]])
+    return bytes(out)
+
+
+def _half_value(bits: int) -> Fraction:
+    """A binary16 bit pattern's value from the IEEE 754 definition (finite patterns)."""
+    sign = -1 if bits & 0x8000 else 1
+    e, f = (bits >> 10) & 0x1F, bits & 0x3FF
+    if e == 0:
+        return sign * Fraction(f, 1 << 10) * Fraction(1, 1 << 14)
+    return sign * (1 + Fraction(f, 1 << 10)) * Fraction(2) ** (e - 15)
+
+
+def test_repack_f16_round_trip_and_scales_exact():
+    """Every scale comes out as its binary16 value exactly (subnormals, the largest finite, signed zero included);
+    values land at [32b + i, n]; -128 and non-finite scales are rejected."""
+    rng = np.random.default_rng(31)
+    K, N = 96, 40
+    q = rng.integers(-127, 128, size=(K, N)).astype(np.int8)
+    d_bits = rng.integers(0, 0x7C00, size=(K // 32, N)).astype(np.uint16)
+    d_bits[0, 0], d_bits[0, 1], d_bits[1, 2], d_bits[2, 3] = 0x0001, 0x03FF, 0x7BFF, 0x8000
+    d_bits[1, 5] |= 0x8000
+    got = oracle.repack_f16(_f16_blocks_of(q, d_bits, N), K, N)
+    assert got is not None and np.array_equal(got[0][:, :N], q) and np.all(got[0][:, N:] == 0)
+    for b in range(K // 32):
+        for n in range(N):
+            assert Fraction(float(got[1][b, n])) == _half_value(int(d_bits[b, n]))
+    assert np.all(got[1][:, N:] == 0)
+    q2 = q.copy()
+    q2[40, 9] = -128
+    assert oracle.repack_f16(_f16_blocks_of(q2, d_bits, N), K, N) is None
+    for bad in (0x7C00, 0xFC00, 0x7E00):
+        d2 = d_bits.copy()
+        d2[1, 7] = bad
+        assert oracle.repack_f16(_f16_blocks_of(q, d2, N), K, N) is None
+
+
 def test_bytes_per_weight_fixture():
     """The byte figures the pages print (used by the benchmark's algorithmic byte count)."""
     vals = {r[0]: float(r[1]) for r in _golden_rows("bytes_per_weight.txt")}
