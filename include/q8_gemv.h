@@ -231,6 +231,12 @@ q8_status q8_quantize_act(const void *x, void *xa, int m, int K, q8_stream_t str
  * are then left partly written. */
 q8_status q8_repack(const void *blocks, int K, int N, int8_t *q, float *s);
 
+/* q8_repack for GGML-style checkpoint blocks ("plan.rs" names the checkpoint format `GgmlType::Q8_0`): each block is
+ * 34 bytes, a little-endian IEEE binary16 scale d followed by 32 int8 values, in the same column-major block order.
+ * The scale is widened to fp32 exactly (subnormals kept).  Errors as q8_repack (a non-finite scale or a value of
+ * -128 is Q8_ERR_NOT_Q8_0). */
+q8_status q8_repack_f16(const void *blocks, int K, int N, int8_t *q, float *s);
+
 /* Host Q8_0 quantization of a declared weight (source: "from_q8.rs", `quantize`).
  *   w  host, fp64 [K][N] row-major (the declared values, as the pages' rule takes them)
  *   q  host, int8 [K][Np] (written, pad columns 0)     s  host, fp32 [K/32][Np] (written, pad columns 0)

@@ -53,6 +53,7 @@ SIGNATURES = {
     "q8_gemv_glu": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_gemv_residual_norm": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_act_bytes": (ctypes.c_int64, [_I, _I]),
+    "q8_repack_f16": (_I, [_P, _I, _I, _P, _P]),
     "q8_quantize_act": (_I, [_P, _P, _I, _I, _P]),
 }
 
@@ -350,17 +351,21 @@ def device_fault(clear: bool = False) -> int:
     return word.value
 
 
-def repack(blocks, K: int, N: int):
-    """(q int8 [K, Np], s fp32 [K/32, Np]) from N * K/32 checkpoint blocks of 36 bytes (host)."""
+def repack(blocks, K: int, N: int, scale: str = "f32"):
+    """(q int8 [K, Np], s fp32 [K/32, Np]) from N * K/32 checkpoint blocks (host): 36-byte blocks with an fp32 scale
+    (q8_repack), or with scale="f16" GGML-style 34-byte blocks with a binary16 scale (q8_repack_f16)."""
+    size = {"f32": 36, "f16": 34}[scale]
     raw = np.frombuffer(bytes(blocks), dtype=np.uint8) if not isinstance(blocks, np.ndarray) else \
         np.ascontiguousarray(blocks).view(np.uint8).reshape(-1)
     Np = padded_n(N) if N > 0 else 1
     nb = max(K // Q8_BLOCK, 1)
-    if K > 0 and N > 0 and raw.size != N * nb * 36:
+    if K > 0 and N > 0 and raw.size != N * nb * size:
         raise ValueError("block buffer size does not match K and N")
     q = np.empty((max(K, 1), Np), dtype=np.int8)
     s = np.empty((nb, Np), dtype=np.float32)
-    _check(lib().q8_repack(raw.ctypes.data, K, N, q.ctypes.data, s.ctypes.data), "q8_repack")
+    fn = lib().q8_repack if scale == "f32" else lib().q8_repack_f16
+    name = "q8_repack" if scale == "f32" else "q8_repack_f16"
+    _check(fn(raw.ctypes.data, K, N, q.ctypes.data, s.ctypes.data), name)
     return q, s
 
 

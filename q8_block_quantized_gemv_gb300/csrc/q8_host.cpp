@@ -68,27 +68,61 @@ extern "C" q8_status q8_quantize(const double *w, int K, int N, int8_t *q, float
     return Q8_OK;
 }
 
-// "from_q8.rs", `Q8Part`: the checkpoint's blocks repacked into the int8 values [K][Np] and the fp32 scales
-// [K/32][Np].  Block layout: column-major by block, 36 bytes each, a little-endian fp32 scale then 32 int8 values.
-extern "C" q8_status q8_repack(const void *blocks, int K, int N, int8_t *q, float *s) {
+namespace {
+
+// An IEEE binary16 bit pattern widened to binary32 (exact: every binary16 value is a binary32 value), from the
+// format's definition: sign, 5-bit exponent (bias 15), 10-bit fraction; exponent 0 holds zeros and subnormals
+// (f * 2^-24), exponent 31 infinities and NaNs.
+float half_to_float(uint16_t h) {
+    const uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    const uint32_t e = (h >> 10) & 0x1Fu;
+    uint32_t f = h & 0x3FFu;
+    uint32_t bits;
+    if (e == 31u) {
+        bits = sign | 0x7F800000u | (f << 13);  // inf or NaN
+    } else if (e != 0u) {
+        bits = sign | ((e + 112u) << 23) | (f << 13);  // normal: exponent re-biased from 15 to 127
+    } else if (f == 0u) {
+        bits = sign;  // signed zero
+    } else {
+        // subnormal f * 2^-24: normalise so that the leading 1 of f sits at bit 10
+        uint32_t shift = 0;
+        while ((f & 0x400u) == 0u) {
+            f <<= 1;
+            ++shift;
+        }
+        bits = sign | ((113u - shift) << 23) | ((f & 0x3FFu) << 13);
+    }
+    float v;
+    memcpy(&v, &bits, sizeof v);
+    return v;
+}
+
+// Both block forms: `scale_bytes` (4: fp32, 2: binary16) little-endian scale, then 32 int8 values.
+q8_status repack_blocks(const void *blocks, int K, int N, int8_t *q, float *s, int scale_bytes) {
     if (!blocks || !q || !s) return Q8_ERR_ARG;
     if (K <= 0 || K % Q8_BLOCK != 0 || N <= 0) return Q8_ERR_SHAPE;
     const int Np = q8_padded_n(N);
     if (Np < 0) return Q8_ERR_SHAPE;
     const int nb = K / Q8_BLOCK;
+    const size_t block_bytes = (size_t)scale_bytes + Q8_BLOCK;
     const unsigned char *src = static_cast<const unsigned char *>(blocks);
     memset(q, 0, (size_t)K * Np);
     memset(s, 0, (size_t)nb * Np * sizeof(float));
     for (int n = 0; n < N; ++n) {
         for (int b = 0; b < nb; ++b) {
-            const unsigned char *blk = src + ((size_t)n * nb + b) * 36;
-            uint32_t bits = (uint32_t)blk[0] | ((uint32_t)blk[1] << 8) | ((uint32_t)blk[2] << 16) |
-                            ((uint32_t)blk[3] << 24);
+            const unsigned char *blk = src + ((size_t)n * nb + b) * block_bytes;
             float d;
-            memcpy(&d, &bits, sizeof d);
+            if (scale_bytes == 4) {
+                const uint32_t bits = (uint32_t)blk[0] | ((uint32_t)blk[1] << 8) | ((uint32_t)blk[2] << 16) |
+                                      ((uint32_t)blk[3] << 24);
+                memcpy(&d, &bits, sizeof d);
+            } else {
+                d = half_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+            }
             if (!isfinite(d)) return Q8_ERR_NOT_Q8_0;
             for (int i = 0; i < Q8_BLOCK; ++i) {
-                const int8_t v = (int8_t)blk[4 + i];
+                const int8_t v = (int8_t)blk[scale_bytes + i];
                 if (v == -128) return Q8_ERR_NOT_Q8_0;
                 q[(size_t)(Q8_BLOCK * b + i) * Np + n] = v;
             }
@@ -97,3 +131,17 @@ extern "C" q8_status q8_repack(const void *blocks, int K, int N, int8_t *q, floa
     }
     return Q8_OK;
 }
+
+}  // namespace
+
+// "from_q8.rs", `Q8Part`: the checkpoint's blocks repacked into the int8 values [K][Np] and the fp32 scales
+// [K/32][Np], column-major by block; q8_repack takes 36-byte blocks (fp32 scale), q8_repack_f16 the GGML-style
+// 34-byte blocks of "plan.rs" `GgmlType::Q8_0` (binary16 scale).
+extern "C" q8_status q8_repack_f16(const void *blocks, int K, int N, int8_t *q, float *s) {
+    return repack_blocks(blocks, K, N, q, s, 2);
+}
+
+extern "C" q8_status q8_repack(const void *blocks, int K, int N, int8_t *q, float *s) {
+    return repack_blocks(blocks, K, N, q, s, 4);
+}
+

@@ -130,6 +130,57 @@ def test_repack_rejects(lib):
         q8.repack(_blocks(q, s2, 8), 64, 8)
 
 
+def _f16_blocks(q, d_bits, N):
+    K = q.shape[0]
+    rec = np.zeros((N, K // 32, 34), dtype=np.uint8)
+    rec[:, :, 0:2] = np.ascontiguousarray(d_bits.T).astype("<u2").view(np.uint8).reshape(N, K // 32, 2)
+    rec[:, :, 2:] = np.ascontiguousarray(q.T).reshape(N, K // 32, 32).view(np.uint8)
+    return rec.tobytes()
+
+
+@pytest.mark.parametrize("K,N", [(32, 1), (96, 40), (512, 300)])
+def test_repack_f16_matches_oracle(lib, K, N):
+    """GGML-style blocks: every finite binary16 scale class (normals, subnormals, zeros of both signs) widened as the
+    oracle (numpy's float16) widens it, bit for bit; the values in place."""
+    rng = np.random.default_rng(K + N)
+    q = rng.integers(-127, 128, size=(K, N)).astype(np.int8)
+    d_bits = rng.integers(0, 0x7C00, size=(K // 32, N)).astype(np.uint16)
+    d_bits |= (rng.integers(0, 2, size=d_bits.shape) << 15).astype(np.uint16)
+    special = np.array([0x0001, 0x83FF, 0x0000, 0x8000], dtype=np.uint16)
+    flat = d_bits.reshape(-1)
+    flat[:min(4, flat.size)] = special[:min(4, flat.size)]
+    blk = _f16_blocks(q, d_bits, N)
+    gq, gs = q8.repack(blk, K, N, scale="f16")
+    oq, os_ = oracle.repack_f16(blk, K, N)
+    assert np.array_equal(gq, oq) and np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
+
+
+def test_repack_f16_every_half_pattern(lib):
+    """All 63,488 finite binary16 patterns as scales: the library's widening equals numpy's for every one."""
+    pats = np.array([b for b in range(0x10000) if (b >> 10) & 0x1F != 0x1F], dtype=np.uint16)
+    N = 128
+    nb = -(-pats.size // N)
+    d_bits = np.zeros(nb * N, dtype=np.uint16)
+    d_bits[:pats.size] = pats
+    d_bits = d_bits.reshape(N, nb).T
+    q = np.ones((32 * nb, N), dtype=np.int8)
+    gq, gs = q8.repack(_f16_blocks(q, d_bits, N), 32 * nb, N, scale="f16")
+    want = d_bits.view(np.float16).astype(np.float32)
+    assert np.array_equal(gs[:, :N].view(np.uint32), want.view(np.uint32))
+
+
+def test_repack_f16_rejects(lib):
+    q = np.ones((64, 8), dtype=np.int8)
+    d = np.full((2, 8), 0x3C00, dtype=np.uint16)
+    q2 = q.copy()
+    q2[5, 1] = -128
+    for qq, dd in ((q2, d), (q, np.where(np.arange(16).reshape(2, 8) == 9, 0x7C00, d).astype(np.uint16)),
+                   (q, np.where(np.arange(16).reshape(2, 8) == 3, 0xFE00, d).astype(np.uint16))):
+        with pytest.raises(q8.Q8Error) as e:
+            q8.repack(_f16_blocks(qq, dd, 8), 64, 8, scale="f16")
+        assert e.value.status == 4
+
+
 # --------------------------------------------------------------------------------------------------------------------
 # device entry points: argument errors come back before any CUDA call
 # --------------------------------------------------------------------------------------------------------------------
