@@ -283,6 +283,12 @@ class Chain:
         # quantized activations: one buffer per width, rewritten before each launch that reads it (stream order)
         self.xa = {K: q8.QuantAct(torch.empty((q8.act_bytes(m, K),), dtype=torch.uint8, device="cuda"), m, K)
                    for K in (HIDDEN, FFN)} if q8act else None
+        # fused layers under --act q8: the norms and the gated pair write the quantized form the next launch reads
+        if fused and q8act:
+            def qa(K):
+                return q8.QuantAct(torch.empty((q8.act_bytes(m, K),), dtype=torch.uint8, device="cuda"), m, K)
+            self.xnq, self.hq = [qa(HIDDEN), qa(HIDDEN)], qa(padded(FFN))
+        self.quant_widths = []  # widths of the quantizer launches of one pass of the layers
         self.g_layers = self.g_head = None
         torch.cuda.synchronize()
 
@@ -291,6 +297,7 @@ class Chain:
         if not self.q8act:
             return x
         import q8_block_quantized_gemv_gb300 as q8
+        self.quant_widths.append(x.shape[1])
         return q8.quantize_act(x, out=self.xa[x.shape[1]])
 
     def layer_calls(self):
@@ -304,6 +311,7 @@ class Chain:
 
     def run_layers(self):
         import q8_block_quantized_gemv_gb300 as q8
+        self.quant_widths = []
         if self.fused:
             return self.run_fused_layers()
         for xi, gis in self.layer_calls():
@@ -323,24 +331,43 @@ class Chain:
         writes the norm the FFN reads; gate/up is the gated pair; down adds into the residual stream and writes the
         norm the next layer reads."""
         import q8_block_quantized_gemv_gb300 as q8
+        if self.q8act:
+            # the producers write the quantized form (no quantizer launch); the drawn inputs are quantized first
+            for layer in range(LAYERS):
+                base, xb = 7 * layer, 4 * layer
+                x_in = self.a(self.x[xb]) if layer == 0 else self.xnq[1]
+                q8.gemv_parts(x_in, [(self.wt[i][0], self.wt[i][1], HIDDEN) for i in (base, base + 1, base + 2)],
+                              ys=[self.y[base], self.y[base + 1], self.y[base + 2]], constant_weights=True,
+                              tiled=True)
+                q8.gemv_residual_norm(self.a(self.x[xb + 1]), self.wt[base + 3][0], self.wt[base + 3][1], HIDDEN,
+                                      self.res, self.gammas[2 * layer], 1e-6, h=self.res, want=(),
+                                      out_q8=self.xnq[0], constant_weights=True)
+                q8.gemv_glu(self.xnq[0], self.wt[base + 4], self.wt[base + 5], FFN, want=(), out_q8=self.hq,
+                            constant_weights=True)
+                q8.gemv_residual_norm(self.hq, self.wt[base + 6][0], self.wt[base + 6][1], HIDDEN, self.res,
+                                      self.gammas[2 * layer + 1], 1e-6, h=self.res, want=(), out_q8=self.xnq[1],
+                                      constant_weights=True)
+            return
         for layer in range(LAYERS):
             base, xb = 7 * layer, 4 * layer
             x_in = self.x[xb] if layer == 0 else self.xn[1]
-            q8.gemv_parts(self.a(x_in), [(self.wt[i][0], self.wt[i][1], HIDDEN) for i in (base, base + 1, base + 2)],
+            q8.gemv_parts(x_in, [(self.wt[i][0], self.wt[i][1], HIDDEN) for i in (base, base + 1, base + 2)],
                           ys=[self.y[base], self.y[base + 1], self.y[base + 2]], constant_weights=True, tiled=True)
-            q8.gemv_residual_norm(self.a(self.x[xb + 1]), self.wt[base + 3][0], self.wt[base + 3][1], HIDDEN,
+            q8.gemv_residual_norm(self.x[xb + 1], self.wt[base + 3][0], self.wt[base + 3][1], HIDDEN,
                                   self.res, self.gammas[2 * layer], 1e-6, h=self.res, out_bf16=self.xn[0],
                                   constant_weights=True)
-            q8.gemv_glu(self.a(self.xn[0]), self.wt[base + 4], self.wt[base + 5], FFN, out_bf16=self.h, want=(),
+            q8.gemv_glu(self.xn[0], self.wt[base + 4], self.wt[base + 5], FFN, out_bf16=self.h, want=(),
                         constant_weights=True)
-            q8.gemv_residual_norm(self.a(self.h), self.wt[base + 6][0], self.wt[base + 6][1], HIDDEN, self.res,
+            q8.gemv_residual_norm(self.h, self.wt[base + 6][0], self.wt[base + 6][1], HIDDEN, self.res,
                                   self.gammas[2 * layer + 1], 1e-6, h=self.res, out_bf16=self.xn[1],
                                   constant_weights=True)
 
     def run_head(self):
         import q8_block_quantized_gemv_gb300 as q8
         q, s = self.head_t
+        layer_quants = len(self.quant_widths)
         q8.gemv_argmax(self.a(self.x[-1]), q, s, VOCAB, idx=self.idx, constant_weights=True, tiled=True)
+        del self.quant_widths[layer_quants:]  # the head's quantizer is counted with the head
 
     def capture(self):
         torch = self.torch
@@ -361,7 +388,7 @@ class Chain:
     def launches_per_step(self):
         # the layers' launches, the head's GEMV kernel and its index decode (and, --act q8, one quantize a launch)
         n = len(self.layer_calls()) + 2
-        return n + (len(self.layer_calls()) + 1 if self.q8act else 0)
+        return n + (len(self.quant_widths) + 1 if self.q8act else 0)
 
     def head_bytes(self):
         m = self.m
@@ -372,18 +399,20 @@ class Chain:
         """Algorithmic bytes of the layers' launches: weights, each activation once, outputs."""
         m = self.m
         total = 0.0
+        # an activation output (the gated pair's, a norm's): bf16, or its quantized form under --act q8
+        out_act = 1.125 if self.q8act else 2
         for xi, gis in self.layer_calls():
             total += act_read_bytes(m, self.x_shapes[xi], self.q8act)
-            if self.q8act:
-                total += quantize_bytes(m, self.x_shapes[xi])
             for i in gis:
                 K, N = self.shapes[i]
                 total += K * padded(N) * 1.125 + m * padded(N) * 4
-            if self.glu and len(gis) == 2:  # one bf16 output instead of two fp32 ones
-                total -= 2 * m * padded(FFN) * 4 - m * padded(FFN) * 2
+            if self.glu and len(gis) == 2:  # one activation output instead of two fp32 ones
+                total -= 2 * m * padded(FFN) * 4 - m * padded(FFN) * out_act
             if self.fused and self.shapes[gis[0]][1] == HIDDEN and len(gis) == 1:
-                # o and down: the residual read, h written over it, the normed bf16 row and the norm's weight
-                total += m * HIDDEN * 4 + m * HIDDEN * 2 + HIDDEN * 4
+                # o and down: the residual read, h written over it, the normed row and the norm's weight
+                total += m * HIDDEN * 4 + m * HIDDEN * out_act + HIDDEN * 4
+        # the quantizer launches of one pass (counted as the layers were captured)
+        total += sum(quantize_bytes(m, K) for K in self.quant_widths)
         return total
 
 

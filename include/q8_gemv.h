@@ -159,6 +159,14 @@ q8_status q8_tile_device(const int8_t *q, const float *s, int K, int N, int8_t *
 q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const int8_t *qu, const float *su, float *out,
                       void *out_bf16, int m, int K, int N, unsigned int flags, q8_stream_t stream);
 
+/* q8_gemv_glu with a third, optional output: out_q8 (device, q8_act_bytes(m, Np) bytes, 16-byte aligned, or NULL)
+ * receives the quantized form of the bf16 output -- exactly what q8_quantize_act of out_bf16 (as [m][Np]) writes --
+ * from the same launch ("plan.rs": a producer writes its result f32, quantized, or both; `GluActMulQuant`), ready for
+ * a Q8_FLAG_Q8_ACT product with K = Np.  At least one of out, out_bf16, out_q8; no two may overlap. */
+q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float *sg, const int8_t *qu, const float *su,
+                         float *out, void *out_bf16, void *out_q8, int m, int K, int N, unsigned int flags,
+                         q8_stream_t stream);
+
 /* A projection folded with the residual add and the next RMS norm ("plan.rs", `Launch::Fold` of a projection with
  * `Launch::Norm`, `gemv_norm_epilogue`: the projection's blocks count in as they finish, and the finishing block
  * reads their results back through L2 and runs the norm; the norm launch is the lane's "rmsnorm"):
@@ -182,6 +190,13 @@ q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const in
 q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const float *s, const float *residual,
                                 const float *gamma, float eps, float *h, void *out_bf16, int m, int K, int N,
                                 unsigned int flags, q8_stream_t stream);
+
+/* q8_gemv_residual_norm with the normed output as bf16 (out_bf16) and/or its quantized form (out_q8, q8_act_bytes(m,
+ * Np) bytes, 16-byte aligned: what q8_quantize_act of the bf16 rows writes; "plan.rs" `AddNormQuant`); at least one of
+ * them, neither overlapping an input, h or the other. */
+q8_status q8_gemv_residual_norm_ex(const void *x, const int8_t *q, const float *s, const float *residual,
+                                   const float *gamma, float eps, float *h, void *out_bf16, void *out_q8, int m,
+                                   int K, int N, unsigned int flags, q8_stream_t stream);
 
 /* One weight of a multi-projection call: its Q8_0 values and scales (row-major, or tiled with Q8_FLAG_TILED), its
  * output y [m][q8_padded_n(N)] (written) and its N. */

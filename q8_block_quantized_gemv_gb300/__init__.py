@@ -54,6 +54,8 @@ SIGNATURES = {
     "q8_gemv_residual_norm": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_act_bytes": (ctypes.c_int64, [_I, _I]),
     "q8_repack_f16": (_I, [_P, _I, _I, _P, _P]),
+    "q8_gemv_glu_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
+    "q8_gemv_residual_norm_ex": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_quantize_act": (_I, [_P, _P, _I, _I, _P]),
 }
 
@@ -297,12 +299,22 @@ def gemv_parts(x, weights, ys=None, constant_weights: bool = False, tiled: bool 
     return outs
 
 
-def gemv_glu(x, gate, up, N: int, out=None, out_bf16=None, want=("f32",), constant_weights: bool = False,
-             stream=None):
-    """The gated pair (q8_gemv_glu, SwiGLU): silu(x.Wg) * (x.Wu) with both weights tiled; gate and up are (q, s).
+def _q8_out(out_q8, m, Np, device):
+    import torch
+    if out_q8 is None:
+        return QuantAct(torch.empty((act_bytes(m, Np),), dtype=torch.uint8, device=device), m, Np)
+    if out_q8.shape != (m, Np) or out_q8.buf.numel() != act_bytes(m, Np):
+        raise ValueError("out_q8 must be a QuantAct of [m, Np]")
+    return out_q8
 
-    ``want``: which outputs to allocate when not given -- "f32" (fp32 [m, Np]) and/or "bf16" (bf16 [m, Np]).
-    Returns (out, out_bf16), either None when not requested."""
+
+def gemv_glu(x, gate, up, N: int, out=None, out_bf16=None, want=("f32",), constant_weights: bool = False,
+             stream=None, out_q8=None):
+    """The gated pair (q8_gemv_glu_ex, SwiGLU): silu(x.Wg) * (x.Wu) with both weights tiled; gate and up are (q, s).
+
+    ``want``: which outputs to allocate when not given -- "f32" (fp32 [m, Np]), "bf16" (bf16 [m, Np]) and/or "q8"
+    (the quantized form of the bf16 output, a QuantAct of [m, Np]).  Returns (out, out_bf16), either None when not
+    requested, or (out, out_bf16, out_q8) when "q8" is wanted or out_q8 given."""
     import torch
     m, K, Np = _check_operands(x, gate[0], gate[1], N, True)
     _check_operands(x, up[0], up[1], N, True)
@@ -310,22 +322,27 @@ def gemv_glu(x, gate, up, N: int, out=None, out_bf16=None, want=("f32",), consta
         out = torch.empty((m, Np), dtype=torch.float32, device=x.device)
     if out_bf16 is None and "bf16" in want:
         out_bf16 = torch.empty((m, Np), dtype=torch.bfloat16, device=x.device)
+    q8out = out_q8 is not None or "q8" in want
+    if q8out:
+        out_q8 = _q8_out(out_q8, m, Np, x.device)
     if out is not None and (out.dtype != torch.float32 or out.shape != (m, Np) or not out.is_contiguous()):
         raise ValueError("out must be a contiguous fp32 CUDA tensor [m, Np]")
     if out_bf16 is not None and (out_bf16.dtype != torch.bfloat16 or out_bf16.shape != (m, Np)
                                  or not out_bf16.is_contiguous()):
         raise ValueError("out_bf16 must be a contiguous bf16 CUDA tensor [m, Np]")
-    _check(lib().q8_gemv_glu(x.data_ptr(), gate[0].data_ptr(), gate[1].data_ptr(), up[0].data_ptr(),
-                             up[1].data_ptr(), out.data_ptr() if out is not None else None,
-                             out_bf16.data_ptr() if out_bf16 is not None else None, m, K, N,
-                             _flags(constant_weights, True, x), _stream_handle(stream)), "q8_gemv_glu")
-    return out, out_bf16
+    _check(lib().q8_gemv_glu_ex(x.data_ptr(), gate[0].data_ptr(), gate[1].data_ptr(), up[0].data_ptr(),
+                                up[1].data_ptr(), out.data_ptr() if out is not None else None,
+                                out_bf16.data_ptr() if out_bf16 is not None else None,
+                                out_q8.data_ptr() if q8out else None, m, K, N,
+                                _flags(constant_weights, True, x), _stream_handle(stream)), "q8_gemv_glu")
+    return (out, out_bf16, out_q8) if q8out else (out, out_bf16)
 
 
 def gemv_residual_norm(x, q, s, N: int, residual, gamma, eps: float, h=None, out_bf16=None,
-                       constant_weights: bool = False, stream=None):
-    """A projection folded with the residual add and the next RMS norm (q8_gemv_residual_norm), tiled weight:
-    h = residual + x.W, out = h / sqrt(mean(h^2) + eps) * gamma.  Returns (h fp32 [m, Np], out bf16 [m, Np]);
+                       constant_weights: bool = False, stream=None, want=("bf16",), out_q8=None):
+    """A projection folded with the residual add and the next RMS norm (q8_gemv_residual_norm_ex), tiled weight:
+    h = residual + x.W, out = h / sqrt(mean(h^2) + eps) * gamma.  Returns (h fp32 [m, Np], out bf16 [m, Np]), or
+    (h, out_bf16 or None, out_q8) when ``want`` holds "q8" or out_q8 is given (the quantized form of the bf16 rows);
     ``h`` may be ``residual`` (in place)."""
     import torch
     m, K, Np = _check_operands(x, q, s, N, True)
@@ -335,13 +352,18 @@ def gemv_residual_norm(x, q, s, N: int, residual, gamma, eps: float, h=None, out
         raise ValueError("gamma must be a contiguous fp32 CUDA tensor of at least N values")
     if h is None:
         h = torch.empty((m, Np), dtype=torch.float32, device=x.device)
-    if out_bf16 is None:
+    if out_bf16 is None and "bf16" in want:
         out_bf16 = torch.empty((m, Np), dtype=torch.bfloat16, device=x.device)
-    _check(lib().q8_gemv_residual_norm(x.data_ptr(), q.data_ptr(), s.data_ptr(), residual.data_ptr(),
-                                       gamma.data_ptr(), float(eps), h.data_ptr(), out_bf16.data_ptr(), m, K, N,
-                                       _flags(constant_weights, True, x), _stream_handle(stream)),
+    q8out = out_q8 is not None or "q8" in want
+    if q8out:
+        out_q8 = _q8_out(out_q8, m, Np, x.device)
+    _check(lib().q8_gemv_residual_norm_ex(x.data_ptr(), q.data_ptr(), s.data_ptr(), residual.data_ptr(),
+                                          gamma.data_ptr(), float(eps), h.data_ptr(),
+                                          out_bf16.data_ptr() if out_bf16 is not None else None,
+                                          out_q8.data_ptr() if q8out else None, m, K, N,
+                                          _flags(constant_weights, True, x), _stream_handle(stream)),
            "q8_gemv_residual_norm")
-    return h, out_bf16
+    return (h, out_bf16, out_q8) if q8out else (h, out_bf16)
 
 
 def device_fault(clear: bool = False) -> int:

@@ -33,18 +33,10 @@ __global__ void quantize_act_kernel(const uint4 *__restrict__ x, uint2 *__restri
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     if (!live) return;
-    float d = 0.0f;
+    const float d = q8::act_scale(mx), inv = q8::act_inv(d);
     uint32_t codes[2] = {0u, 0u};
-    if (mx >= 0x7F800000u) {
-        d = __uint_as_float(0x7FC00000u);  // inf or NaN in the block
-    } else if (mx != 0u) {
-        d = __fdiv_rn(__uint_as_float(mx), 127.0f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float r = fminf(fmaxf(roundf(__fdiv_rn(f[j], d)), -127.0f), 127.0f);
-            codes[j / 4] |= ((uint32_t)(int)r & 0xFFu) << (8 * (j % 4));
-        }
-    }
+    for (int j = 0; j < 8; ++j) codes[j / 4] |= q8::act_code(f[j], d, inv, mx) << (8 * (j % 4));
     xq[id] = make_uint2(codes[0], codes[1]);
     if ((id & 3) == 0) xd[id >> 2] = d;
 }

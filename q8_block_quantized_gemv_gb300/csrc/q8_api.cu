@@ -351,31 +351,33 @@ int plan_glu(long long tiles, int nb, int sms) {
     return (int)ks;
 }
 
-extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const int8_t *qu,
-                                 const float *su, float *out, void *out_bf16, int m, int K, int N, unsigned int flags,
-                                 q8_stream_t stream) {
+extern "C" q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float *sg, const int8_t *qu,
+                                    const float *su, float *out, void *out_bf16, void *out_q8, int m, int K, int N,
+                                    unsigned int flags, q8_stream_t stream) {
     q8_status st = check_gemv_args(x, qg, sg, m, K, N, flags);
     if (st != Q8_OK) return st;
     st = check_gemv_args(x, qu, su, m, K, N, flags);
     if (st != Q8_OK) return st;
-    if (!out && !out_bf16) return Q8_ERR_ARG;
+    if (!out && !out_bf16 && !out_q8) return Q8_ERR_ARG;
     if (!flags_ok(flags)) return Q8_ERR_ARG;
     if (!(flags & Q8_FLAG_TILED)) return Q8_ERR_ARG;  // the gated pair runs on the tiled storage only
     if (q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
-    if ((out && !aligned(out, 16)) || (out_bf16 && !aligned(out_bf16, 16))) return Q8_ERR_ALIGN;
+    if ((out && !aligned(out, 16)) || (out_bf16 && !aligned(out_bf16, 16)) || (out_q8 && !aligned(out_q8, 16)))
+        return Q8_ERR_ALIGN;
     const int Np = q8_padded_n(N);
     const size_t wcols = (size_t)q8_tiled_n(N);
-    const size_t obytes[2] = {(size_t)m * Np * 4, (size_t)m * Np * 2};
-    const void *outs[2] = {out, out_bf16};
-    for (int o = 0; o < 2; ++o) {
+    const size_t obytes[3] = {(size_t)m * Np * 4, (size_t)m * Np * 2, (size_t)q8_act_bytes(m, Np)};
+    const void *outs[3] = {out, out_bf16, out_q8};
+    for (int o = 0; o < 3; ++o) {
         if (!outs[o]) continue;
         if (overlaps(outs[o], obytes[o], x, x_bytes(flags, m, K)) ||
             overlaps(outs[o], obytes[o], qg, (size_t)K * wcols) || overlaps(outs[o], obytes[o], qu, (size_t)K * wcols) ||
             overlaps(outs[o], obytes[o], sg, (size_t)(K / Q8_BLOCK) * wcols * 4) ||
             overlaps(outs[o], obytes[o], su, (size_t)(K / Q8_BLOCK) * wcols * 4))
             return Q8_ERR_ARG;
+        for (int p = 0; p < o; ++p)
+            if (outs[p] && overlaps(outs[o], obytes[o], outs[p], obytes[p])) return Q8_ERR_ARG;
     }
-    if (out && out_bf16 && overlaps(out, obytes[0], out_bf16, obytes[1])) return Q8_ERR_ARG;
     int sms = 0;
     int e = sm_count(&sms);
     if (e != 0) return cuda_fail((cudaError_t)e);
@@ -392,6 +394,10 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
     pt.count = 2;
     Args a = {static_cast<const uint16_t *>(x), qg, sg, out, nullptr, m, K, N, Np, K / Q8_BLOCK, 1,
               static_cast<uint16_t *>(out_bf16)};
+    if (out_q8) {
+        a.yq = static_cast<unsigned char *>(out_q8);
+        a.yd = reinterpret_cast<float *>(a.yq + (size_t)m * Np);
+    }
     a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms);
     cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true,
                                        (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0, (flags & Q8_FLAG_Q8_ACT) != 0);
@@ -399,27 +405,43 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
     return Q8_OK;
 }
 
-extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const float *s, const float *residual,
-                                           const float *gamma, float eps, float *h, void *out_bf16, int m, int K,
-                                           int N, unsigned int flags, q8_stream_t stream) {
+extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const int8_t *qu,
+                                 const float *su, float *out, void *out_bf16, int m, int K, int N, unsigned int flags,
+                                 q8_stream_t stream) {
+    return q8_gemv_glu_ex(x, qg, sg, qu, su, out, out_bf16, nullptr, m, K, N, flags, stream);
+}
+
+extern "C" q8_status q8_gemv_residual_norm_ex(const void *x, const int8_t *q, const float *s, const float *residual,
+                                              const float *gamma, float eps, float *h, void *out_bf16, void *out_q8,
+                                              int m, int K, int N, unsigned int flags, q8_stream_t stream) {
     q8_status st = check_gemv_args(x, q, s, m, K, N, flags);
     if (st != Q8_OK) return st;
-    if (!residual || !gamma || !h || !out_bf16) return Q8_ERR_ARG;
+    if (!residual || !gamma || !h || (!out_bf16 && !out_q8)) return Q8_ERR_ARG;
     if (!flags_ok(flags)) return Q8_ERR_ARG;
     if (!(flags & Q8_FLAG_TILED)) return Q8_ERR_ARG;  // the tiled storage only
     if (!(eps >= 0.0f) || !(eps < INFINITY)) return Q8_ERR_ARG;
     if (q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
-    if (!aligned(h, 16) || !aligned(out_bf16, 16) || !aligned(residual, 4) || !aligned(gamma, 4)) return Q8_ERR_ALIGN;
+    if (!aligned(h, 16) || (out_bf16 && !aligned(out_bf16, 16)) || (out_q8 && !aligned(out_q8, 16)) ||
+        !aligned(residual, 4) || !aligned(gamma, 4))
+        return Q8_ERR_ALIGN;
     const int Np = q8_padded_n(N);
     const size_t wcols = (size_t)q8_tiled_n(N);
-    const size_t hbytes = (size_t)m * Np * 4, obytes = (size_t)m * Np * 2;
+    const size_t hbytes = (size_t)m * Np * 4, obytes = (size_t)m * Np * 2, qbytes = (size_t)q8_act_bytes(m, Np);
     // h may be the residual itself (in place) but may not overlap it otherwise, nor any other operand.
     if (h != residual && overlaps(h, hbytes, residual, hbytes)) return Q8_ERR_ARG;
     const void *ins[4] = {x, q, s, gamma};
     const size_t inb[4] = {x_bytes(flags, m, K), (size_t)K * wcols, (size_t)(K / Q8_BLOCK) * wcols * 4, (size_t)Np * 4};
+    const void *outs[2] = {out_bf16, out_q8};
+    const size_t outb[2] = {obytes, qbytes};
+    for (int o = 0; o < 2; ++o) {
+        if (!outs[o]) continue;
+        for (int i = 0; i < 4; ++i)
+            if (overlaps(outs[o], outb[o], ins[i], inb[i])) return Q8_ERR_ARG;
+        if (overlaps(outs[o], outb[o], h, hbytes) || overlaps(outs[o], outb[o], residual, hbytes)) return Q8_ERR_ARG;
+    }
     for (int i = 0; i < 4; ++i)
-        if (overlaps(h, hbytes, ins[i], inb[i]) || overlaps(out_bf16, obytes, ins[i], inb[i])) return Q8_ERR_ARG;
-    if (overlaps(out_bf16, obytes, h, hbytes) || overlaps(out_bf16, obytes, residual, hbytes)) return Q8_ERR_ARG;
+        if (overlaps(h, hbytes, ins[i], inb[i])) return Q8_ERR_ARG;
+    if (out_bf16 && out_q8 && overlaps(out_bf16, obytes, out_q8, qbytes)) return Q8_ERR_ARG;
     // one completion counter per row group, taken round robin
     static std::atomic<unsigned> next_counter{0};
     const unsigned groups = (unsigned)((m + q8::kGroupRows - 1) / q8::kGroupRows);
@@ -428,6 +450,10 @@ extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const
     if (!count) return cuda_fail(cudaGetLastError());
     Args a = {static_cast<const uint16_t *>(x), q, s, h, nullptr, m, K, N, Np, K / Q8_BLOCK, 1,
               static_cast<uint16_t *>(out_bf16), residual, gamma, eps, count, slot};
+    if (out_q8) {
+        a.yq = static_cast<unsigned char *>(out_q8);
+        a.yd = reinterpret_cast<float *>(a.yq + (size_t)m * Np);
+    }
     int sms = 0;
     int e = sm_count(&sms);
     if (e != 0) return cuda_fail((cudaError_t)e);
@@ -444,6 +470,13 @@ extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const
                                        (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0, (flags & Q8_FLAG_Q8_ACT) != 0);
     if (ce != cudaSuccess) return cuda_fail(ce);
     return Q8_OK;
+}
+
+extern "C" q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const float *s, const float *residual,
+                                           const float *gamma, float eps, float *h, void *out_bf16, int m, int K,
+                                           int N, unsigned int flags, q8_stream_t stream) {
+    if (!out_bf16) return Q8_ERR_ARG;
+    return q8_gemv_residual_norm_ex(x, q, s, residual, gamma, eps, h, out_bf16, nullptr, m, K, N, flags, stream);
 }
 
 extern "C" q8_status q8_device_fault(unsigned int *fault, int clear) {

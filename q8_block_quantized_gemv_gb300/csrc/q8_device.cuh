@@ -42,6 +42,8 @@ struct Args {
     unsigned int *count;       // norm: the completion counters (0 on entry, reset to 0 by the last CTA of a group)
     int count_slot;            // norm: row group g counts in at count[(count_slot + g) % kNormSlots]
     int groups;                // set on the device: the launch's row groups (ceil(m / 16))
+    unsigned char *yq;         // gated pair / norm: the quantized form of the bf16 output, codes [m][Np] (or null)
+    float *yd;                 //   and its scales [m][Np / 32]
 };
 
 constexpr int kGroupRows = 16;   // activation rows of one row group (m > 16 runs ceil(m / 16) groups in one grid)
@@ -61,6 +63,8 @@ __device__ __forceinline__ void apply_group(Args &a, int group, int groups) {
         const size_t off = (size_t)row0 * a.Np;
         if (a.y) a.y += off;
         if (a.ybf) a.ybf += off;
+        if (a.yq) a.yq += off;
+        if (a.yd) a.yd += (size_t)row0 * (a.Np / kBlock);
         if (a.res) a.res += off;
         if (a.keys) a.keys += row0;
         a.count_slot += group;
@@ -238,6 +242,28 @@ __host__ __device__ constexpr int finish_smem_bytes(int MR, int TC) { return fin
 // CTA's column tile `tile` of the output; RS >= TC is the slab row stride) and the CTA has synchronised.  Sums the
 // slabs in order, then (ksplit > 1) the cluster's ranks in order, writes y (0 in the pad columns) and folds this
 // CTA's columns into the per-row arg-max keys.
+// The quantized form of an activation ("plan.rs", `QBLOCK`: 32 values share one scale), the rule of q8_quantize_act:
+// from the bit pattern of the block's largest magnitude, d = amax / 127 (IEEE fp32 quotient), a value's code is
+// value / d rounded half away from zero and clamped to 127; a block of zeros has d = 0, a block holding inf or NaN
+// d = NaN, both with codes 0.
+__device__ __forceinline__ float act_scale(uint32_t amax_bits) {
+    if (amax_bits >= 0x7F800000u) return __uint_as_float(0x7FC00000u);
+    if (amax_bits == 0u) return 0.0f;
+    return __fdiv_rn(__uint_as_float(amax_bits), 127.0f);
+}
+// The code of v with the block's d.  The quotient is taken as v * (1 / d) (both IEEE products, at most about 2.5
+// units in the last place from v / d for |v / d| < 128, i.e. below 2^-15) unless that product lies within 2^-14 of
+// a half-integer, where the rounding could differ; there, and when 1 / d overflows, the IEEE quotient itself is
+// used.  Both give the code of the correctly rounded quotient.
+__device__ __forceinline__ float act_inv(float d) { return __frcp_rn(d); }
+__device__ __forceinline__ uint32_t act_code(float v, float d, float inv, uint32_t amax_bits) {
+    if (amax_bits >= 0x7F800000u || amax_bits == 0u) return 0u;
+    float qv = v * inv;
+    const float a = fabsf(qv);
+    if (!(inv < 3.0e38f) || fabsf(a - floorf(a) - 0.5f) < 6.103515625e-05f) qv = __fdiv_rn(v, d);
+    return (uint32_t)(int)fminf(fmaxf(roundf(qv), -127.0f), 127.0f) & 0xFFu;
+}
+
 template <int NRED, int MR, int TC, int NTHREADS, bool ARGMAX, int RS = TC>
 __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
     namespace cg = cooperative_groups;
@@ -311,7 +337,8 @@ __device__ __forceinline__ void finish_glu(const Args &a, float *red, int tile) 
     }
     cluster.sync();
     const int ks = a.ksplit, p = blockIdx.x & 1, k = blockIdx.y;
-    const int c0 = TC * k / ks, c1 = TC * (k + 1) / ks, width = c1 - c0;
+    // slices of whole 32-column blocks (a warp then holds one block of one row for the quantized output)
+    const int c0 = kBlock * ((TC / kBlock) * k / ks), c1 = kBlock * ((TC / kBlock) * (k + 1) / ks), width = c1 - c0;
     for (int i = threadIdx.x; i < rows * width; i += NTHREADS) {
         const int r = i / width, c = c0 + (i - r * width);
         float v = 0.0f;
@@ -324,11 +351,21 @@ __device__ __forceinline__ void finish_glu(const Args &a, float *red, int tile) 
         for (int i = threadIdx.x; i < rows * width; i += NTHREADS) {
             const int r = i / width, c = c0 + (i - r * width);
             const int n = tile * TC + c;
-            if (n < a.Np) {
+            if (n < a.Np) {  // uniform across the warp: its 32 values are one 32-column block
                 const float g = mine[i];
                 const float o = n < a.N ? g / (1.0f + expf(-g)) * up[i] : 0.0f;
+                const __nv_bfloat16 ob = __float2bfloat16_rn(o);
                 if (a.y) a.y[(size_t)r * a.Np + n] = o;
-                if (a.ybf) a.ybf[(size_t)r * a.Np + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+                if (a.ybf) a.ybf[(size_t)r * a.Np + n] = __bfloat16_as_ushort(ob);
+                if (a.yq) {  // the quantized form of the bf16 output
+                    const float v = __bfloat162float(ob);
+                    uint32_t mx = __float_as_uint(v) & 0x7FFFFFFFu;
+#pragma unroll
+                    for (int o2 = 16; o2 > 0; o2 >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+                    const float d = act_scale(mx);
+                    a.yq[(size_t)r * a.Np + n] = (unsigned char)act_code(v, d, act_inv(d), mx);
+                    if ((n & (kBlock - 1)) == 0) a.yd[(size_t)r * (a.Np / kBlock) + n / kBlock] = d;
+                }
             }
         }
     }
@@ -432,31 +469,80 @@ __device__ __forceinline__ void finish_norm(const Args &a, float *red, int tile)
         rstd[threadIdx.x] = 1.0f / sqrtf(v / (float)a.N + a.eps);
     }
     __syncthreads();
-    // out = h * rstd * gamma, four columns a store; the pad columns get 0.
-    for (int j = threadIdx.x; j < chunks; j += NTHREADS) {
-        const int n = 4 * j;
-        float g[4];
+    if (!a.yq) {
+        // out = h * rstd * gamma as bf16, four columns a store; the pad columns get 0.
+        for (int j = threadIdx.x; j < chunks; j += NTHREADS) {
+            const int n = 4 * j;
+            float g[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) g[e] = n + e < a.N ? a.gamma[n + e] : 0.0f;
-        float4 hv[MR];
+            for (int e = 0; e < 4; ++e) g[e] = n + e < a.N ? a.gamma[n + e] : 0.0f;
+            float4 hv[MR];
 #pragma unroll
-        for (int r = 0; r < MR; ++r)
-            hv[r] = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)(r < rows ? r : rows - 1) * a.Np) + j);
+            for (int r = 0; r < MR; ++r)
+                hv[r] = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)(r < rows ? r : rows - 1) * a.Np) + j);
 #pragma unroll
-        for (int r = 0; r < MR; ++r)
-            if (r < rows) {
-                const float4 v = hv[r];
-                const float rs = rstd[r];
-                const float o0 = n < a.N ? v.x * rs * g[0] : 0.0f;
-                const float o1 = n + 1 < a.N ? v.y * rs * g[1] : 0.0f;
-                const float o2 = n + 2 < a.N ? v.z * rs * g[2] : 0.0f;
-                const float o3 = n + 3 < a.N ? v.w * rs * g[3] : 0.0f;
-                const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o0)) |
-                                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o1)) << 16);
-                const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o2)) |
-                                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o3)) << 16);
-                *reinterpret_cast<uint2 *>(a.ybf + (size_t)r * a.Np + n) = make_uint2(lo, hi);
-            }
+            for (int r = 0; r < MR; ++r)
+                if (r < rows) {
+                    const float4 v = hv[r];
+                    const float rs = rstd[r];
+                    const float o0 = n < a.N ? v.x * rs * g[0] : 0.0f;
+                    const float o1 = n + 1 < a.N ? v.y * rs * g[1] : 0.0f;
+                    const float o2 = n + 2 < a.N ? v.z * rs * g[2] : 0.0f;
+                    const float o3 = n + 3 < a.N ? v.w * rs * g[3] : 0.0f;
+                    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o0)) |
+                                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o1)) << 16);
+                    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o2)) |
+                                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o3)) << 16);
+                    *reinterpret_cast<uint2 *>(a.ybf + (size_t)r * a.Np + n) = make_uint2(lo, hi);
+                }
+        }
+    } else {
+        // With the quantized form: four columns a thread, the loop warp-uniform so that eight consecutive lanes
+        // (one 32-column block; chunks is a multiple of 8) reduce the block's largest magnitude by shuffles; the
+        // bf16 rows too when asked for.
+        for (int j0 = threadIdx.x - lane; j0 < chunks; j0 += NTHREADS) {
+            const int j = j0 + lane;
+            const bool live = j < chunks;
+            const int jc = live ? j : chunks - 1;
+            const int n = 4 * jc;
+            float g[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) g[e] = n + e < a.N ? a.gamma[n + e] : 0.0f;
+            float4 hv[MR];
+#pragma unroll
+            for (int r = 0; r < MR; ++r)
+                hv[r] = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)(r < rows ? r : rows - 1) * a.Np) + jc);
+#pragma unroll
+            for (int r = 0; r < MR; ++r)
+                if (r < rows) {
+                    const float4 v = hv[r];
+                    const float rs = rstd[r];
+                    const __nv_bfloat16 b0 = __float2bfloat16_rn(n < a.N ? v.x * rs * g[0] : 0.0f);
+                    const __nv_bfloat16 b1 = __float2bfloat16_rn(n + 1 < a.N ? v.y * rs * g[1] : 0.0f);
+                    const __nv_bfloat16 b2 = __float2bfloat16_rn(n + 2 < a.N ? v.z * rs * g[2] : 0.0f);
+                    const __nv_bfloat16 b3 = __float2bfloat16_rn(n + 3 < a.N ? v.w * rs * g[3] : 0.0f);
+                    if (a.ybf && live) {
+                        const uint32_t lo =
+                            (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
+                        const uint32_t hi =
+                            (uint32_t)__bfloat16_as_ushort(b2) | ((uint32_t)__bfloat16_as_ushort(b3) << 16);
+                        *reinterpret_cast<uint2 *>(a.ybf + (size_t)r * a.Np + n) = make_uint2(lo, hi);
+                    }
+                    const float v0 = __bfloat162float(b0), v1 = __bfloat162float(b1);
+                    const float v2 = __bfloat162float(b2), v3 = __bfloat162float(b3);
+                    uint32_t mx = max(max(__float_as_uint(v0) & 0x7FFFFFFFu, __float_as_uint(v1) & 0x7FFFFFFFu),
+                                      max(__float_as_uint(v2) & 0x7FFFFFFFu, __float_as_uint(v3) & 0x7FFFFFFFu));
+#pragma unroll
+                    for (int o2 = 1; o2 < 8; o2 <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+                    const float d = act_scale(mx), inv = act_inv(d);
+                    const uint32_t codes = act_code(v0, d, inv, mx) | (act_code(v1, d, inv, mx) << 8) |
+                                           (act_code(v2, d, inv, mx) << 16) | (act_code(v3, d, inv, mx) << 24);
+                    if (live) {
+                        *reinterpret_cast<uint32_t *>(a.yq + (size_t)r * a.Np + n) = codes;
+                        if ((j & 7) == 0) a.yd[(size_t)r * (a.Np / kBlock) + j / 8] = d;
+                    }
+                }
+        }
     }
     if (threadIdx.x == 0) a.count[a.count_slot % kNormSlots] = 0u;  // ready for the next launch that takes it
 }

@@ -263,3 +263,77 @@ def test_deterministic(dev):
     y1 = _product(dev, xa, q, s, 1000)
     y2 = _product(dev, xa, q, s, 1000)
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+# --------------------------------------------------------------------------------------------------------------------
+# producers that write the quantized form in their epilogue (the gated pair, the residual norm)
+# --------------------------------------------------------------------------------------------------------------------
+
+def _assert_form_of(torch, qa, bf16_out, what):
+    """The epilogue's quantized form equals q8_quantize_act's rule (the oracle) applied to its own bf16 output."""
+    bits = bf16_out.view(torch.int16).cpu().numpy().view(np.uint16)
+    xq_o, xd_o = oracle.quantize_act(bits)
+    xq, xd = qa.values().cpu().numpy(), qa.scales().cpu().numpy()
+    assert np.array_equal(xq, xq_o), what
+    nan = np.isnan(xd_o)
+    assert np.array_equal(np.isnan(xd), nan) and np.array_equal(xd[~nan].view(np.uint32),
+                                                                xd_o[~nan].view(np.uint32)), what
+
+
+@pytest.mark.parametrize("ks", [1, 2, 3, 4])
+@pytest.mark.parametrize("m", [1, 8, 16, 40])
+def test_glu_writes_its_quantized_form(dev, m, ks, monkeypatch):
+    """The gated pair's out_q8 is the quantized form of its bf16 output, for every K split (32-column slices) and row
+    groups; the bf16 output itself stays within the bound."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    monkeypatch.setenv("Q8_KSPLIT", str(ks))
+    x, qg, sg = si.case(m, 1024, 1000, 2800 + m)
+    _, qu, su = si.case(m, 1024, 1000, 2900 + m)
+    _, qgd, sgd = _to_dev(torch, x, qg, sg)
+    _, qud, sud = _to_dev(torch, x, qu, su)
+    out, outb, qa = q8.gemv_glu(_x_dev(torch, x), q8.tile_device(qgd, sgd, 1000), q8.tile_device(qud, sud, 1000),
+                                1000, want=("f32", "bf16", "q8"))
+    torch.cuda.synchronize()
+    _glu_check(out.cpu().numpy(), outb.view(torch.int16).cpu().numpy().view(np.uint16), x, qg, sg, qu, su, 1000,
+               what=f"m={m} ks={ks}")
+    _assert_form_of(torch, qa, outb, f"m={m} ks={ks}")
+
+
+@pytest.mark.parametrize("m", [1, 16, 40])
+def test_residual_norm_writes_its_quantized_form(dev, m):
+    """The residual norm's out_q8 is the quantized form of its bf16 rows; asked for alone, it is the same bytes."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    x, q, s, res, gamma = _norm_inputs(m, 2048, 4096, 3500 + m)
+    qt, st = q8.tile_device(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), 4096)
+    xd, gd = _x_dev(torch, x), torch.from_numpy(gamma).cuda()
+    h, outb, qa = q8.gemv_residual_norm(xd, qt, st, 4096, torch.from_numpy(res).cuda(), gd, 1e-6,
+                                        want=("bf16", "q8"))
+    h2, none, qa2 = q8.gemv_residual_norm(xd, qt, st, 4096, torch.from_numpy(res).cuda(), gd, 1e-6, want=("q8",))
+    torch.cuda.synchronize()
+    assert none is None
+    _norm_check(h.cpu().numpy(), outb.view(torch.int16).cpu().numpy().view(np.uint16), x, q, s, res, gamma, 1e-6,
+                4096, what=f"m={m}")
+    _assert_form_of(torch, qa, outb, f"m={m}")
+    assert torch.equal(qa.buf, qa2.buf) and torch.equal(h, h2)
+
+
+def test_fused_form_feeds_the_next_projection(dev):
+    """The gated pair's quantized output read by the down projection (Q8_FLAG_Q8_ACT) gives the same bits as
+    quantizing its bf16 output with q8_quantize_act first."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    m, D, F = 4, 1024, 2048
+    x, qg, sg = si.case(m, D, F, 3600)
+    _, qu, su = si.case(m, D, F, 3601)
+    _, qd, sd = si.case(m, F, D, 3602)
+    _, qgd, sgd = _to_dev(torch, x, qg, sg)
+    _, qud, sud = _to_dev(torch, x, qu, su)
+    down = q8.tile_device(torch.from_numpy(qd).cuda(), torch.from_numpy(sd).cuda(), D)
+    _, hb, hq = q8.gemv_glu(_x_dev(torch, x), q8.tile_device(qgd, sgd, F), q8.tile_device(qud, sud, F), F,
+                            want=("bf16", "q8"))
+    y1 = q8.gemv(hq, down[0], down[1], D, tiled=True)
+    y2 = q8.gemv(q8.quantize_act(hb), down[0], down[1], D, tiled=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))

@@ -399,3 +399,19 @@ def test_row_limits(lib):
     assert lib.q8_gemv_ex(A16, B16, C16, D16, 513, 32, 64, 0, 2, None) == 2
     assert lib.q8_gemv_argmax_ex(A16, B16, C16, D16, None, 17, 32, 64, 0, None) == 2
     assert lib.q8_gemv_argmax_ex(A16, B16, C16, D16, None, 513, 32, 64, 2, None) == 2
+
+
+def test_quantized_output_argument_errors(lib):
+    """The producers' _ex entry points: at least one output; out_q8 16-byte aligned and apart from the others."""
+    import ctypes
+    G, GS, U, US = B16, C16, 0x50000, 0x60000
+    assert lib.q8_gemv_glu_ex(A16, G, GS, U, US, None, None, None, 1, 32, 64, 2, None) == 1
+    assert lib.q8_gemv_glu_ex(A16, G, GS, U, US, None, None, 0x70004, 1, 32, 64, 2, None) == 3
+    assert lib.q8_gemv_glu_ex(A16, G, GS, U, US, None, 0x70000, 0x70000, 1, 32, 64, 2, None) == 1
+    f = ctypes.c_float
+    R, GM, H = 0x50000, 0x60000, 0x70000
+    assert lib.q8_gemv_residual_norm_ex(A16, B16, C16, R, GM, f(1e-6), H, None, None, 2, 64, 96, 2, None) == 1
+    assert lib.q8_gemv_residual_norm_ex(A16, B16, C16, R, GM, f(1e-6), H, None, 0x80008, 2, 64, 96, 2, None) == 3
+    assert lib.q8_gemv_residual_norm_ex(A16, B16, C16, R, GM, f(1e-6), H, 0x80000, 0x80000, 2, 64, 96, 2,
+                                        None) == 1
+    assert lib.q8_gemv_residual_norm_ex(A16, B16, C16, R, GM, f(1e-6), H, None, H, 2, 64, 96, 2, None) == 1
