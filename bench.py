@@ -240,6 +240,21 @@ def run_reference(args, rank, world):
 # our arm
 # ---------------------------------------------------------------------------------------------------------------------
 
+def reduce_max(v: float, world: int, device: str) -> float:
+    """The largest of every rank's v (the step time a replicated run reports: its slowest rank)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job GB/s of N replicas: every rank runs the whole step, the step time is the slowest rank's."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
 class Chain:
     """Device-resident weights, activations and outputs of one decode step, and its CUDA graphs.
 
@@ -432,11 +447,7 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, world, "cuda")
 
     for _ in range(args.warmup):
         chain.g_layers.replay()
@@ -464,7 +475,7 @@ def run_ours(args, rank, world, local_rank):
     head_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     ms = max_over_ranks(ms)
     bytes_step = chain.layer_bytes() + chain.head_bytes()
-    value = world * bytes_step / (ms * 1e-3) / 1e9
+    value = job_throughput(bytes_step, ms, world)
 
     # ---- end-to-end: host activations in, the step's tokens out, every step ----
     x_host = torch.empty(chain.x_all.shape, dtype=torch.bfloat16, pin_memory=True)
