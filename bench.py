@@ -401,8 +401,12 @@ class Chain:
         torch.cuda.synchronize()
 
     def launches_per_step(self):
-        # the layers' launches, the head's GEMV kernel and its index decode (and, --act q8, one quantize a launch)
+        # the layers' launches, the head's GEMV kernel and its index decode (and, --act q8, one quantize a launch);
+        # --fused: a residual norm's own norm launch after each of its two products a layer
+        import q8_block_quantized_gemv_gb300 as q8
         n = len(self.layer_calls()) + 2
+        if self.fused:
+            n += 2 * LAYERS * (q8.residual_norm_launches() - 1)
         return n + (len(self.quant_widths) + 1 if self.q8act else 0)
 
     def head_bytes(self):

@@ -172,9 +172,12 @@ q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float *sg, const
  * reads their results back through L2 and runs the norm; the norm launch is the lane's "rmsnorm"):
  *     y = x . W (the Q8_0 product of q8_gemv),   h = residual + y,
  *     out[r, n] = h[r, n] / sqrt(mean_{n' < N} h[r, n']^2 + eps) * gamma[n]
- * in one launch.  Every CTA writes its columns of h; the last CTA to finish (a completion counter from a fixed set of
- * 64 held in static device memory: the library allocates nothing) reads the rows of h back, forms each row's mean
- * square in a fixed order (the result does not depend on which CTA is last) and writes out.
+ * Every CTA of the product writes its columns of h.  A second launch on the same stream, chained by programmatic
+ * dependent launch (it waits for all of h), then runs the norm with one CTA per row: the row's mean square in a fixed
+ * order, then out.  The one-launch fold of the source, where the product's last CTA to finish (a completion counter
+ * from a fixed set of 64 in static device memory: the library allocates nothing) reads the rows of h back and runs
+ * the norm, is kept for comparison (Q8_NORM_LAUNCH=0 in the environment); measured on GB300 it is slower at every m.
+ * Either way the result depends only on the inputs, never on which CTA finishes last.
  *   x, q, s   as q8_gemv, the weight in the tiled storage (q8_tile)
  *   residual  device, fp32 [m][Np], 4-byte aligned (read)
  *   gamma     device, fp32 [N] (at least N values), 4-byte aligned
@@ -183,10 +186,11 @@ q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float *sg, const
  *   out_bf16  device, bf16 [m][Np] (written: out rounded to nearest even, pads 0), 16-byte aligned -- the next
  *             projection's activation as q8_gemv takes it (row pitch Np)
  *   flags     Q8_FLAG_TILED (required) | Q8_FLAG_CONSTANT_WEIGHTS
- * Each group of 16 rows takes the next of 64 static completion counters in turn (a counter is back to 0 when its
- * launch ends), so at most 64 row groups -- 64 calls of m <= 16 -- may be in flight at once.  Errors: Q8_ERR_ARG (null pointers, flags without Q8_FLAG_TILED or unknown bits, eps < 0 or not
- * finite, outputs overlapping an input or each other other than h == residual), Q8_ERR_SHAPE, Q8_ERR_ALIGN,
- * Q8_ERR_CUDA; nothing is launched on an error. */
+ * Under the one-launch fold each group of 16 rows takes the next of 64 static completion counters in turn (a counter
+ * is back to 0 when its launch ends), so at most 64 row groups may be in flight at once.
+ * Errors: Q8_ERR_ARG (null pointers, flags without Q8_FLAG_TILED or unknown bits, eps < 0 or not finite, outputs
+ * overlapping an input or each other other than h == residual), Q8_ERR_SHAPE, Q8_ERR_ALIGN, Q8_ERR_CUDA; nothing is
+ * launched on an argument error (a Q8_ERR_CUDA from the norm's own launch leaves h written and out unspecified). */
 q8_status q8_gemv_residual_norm(const void *x, const int8_t *q, const float *s, const float *residual,
                                 const float *gamma, float eps, float *h, void *out_bf16, int m, int K, int N,
                                 unsigned int flags, q8_stream_t stream);

@@ -366,6 +366,12 @@ def gemv_residual_norm(x, q, s, N: int, residual, gamma, eps: float, h=None, out
     return (h, out_bf16, out_q8) if q8out else (h, out_bf16)
 
 
+def residual_norm_launches() -> int:
+    """Kernel launches one gemv_residual_norm call makes, by the library's rule: the product, then the norm as a
+    launch of its own (2); 1 when Q8_NORM_LAUNCH=0 in the environment keeps the norm in the product's last CTA."""
+    return 1 if os.environ.get("Q8_NORM_LAUNCH", "").startswith("0") else 2
+
+
 def device_fault(clear: bool = False) -> int:
     """The device fault word (nonzero when a kernel's bounded pipeline wait ran out); see q8_device_fault."""
     word = ctypes.c_uint(0)

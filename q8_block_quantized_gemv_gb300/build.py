@@ -20,7 +20,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "--expt-relaxed-constexpr"]
 SOURCES = ["q8_tma.cu", "q8_stream.cu", "q8_simt.cu", "q8_mma.cu", "q8_api.cu", "q8_tile.cu", "q8_act.cu",
-           "q8_gemm.cu", "q8_host.cpp"]
+           "q8_gemm.cu", "q8_norm.cu", "q8_host.cpp"]
 
 
 def nvcc() -> str:

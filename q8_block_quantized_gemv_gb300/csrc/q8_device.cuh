@@ -39,7 +39,8 @@ struct Args {
     const float *res;          // norm: residual fp32 [m][Np] (h = res + y is written to y; may be y itself)
     const float *gamma;        // norm: fp32 [Np]
     float eps;                 // norm: added to the mean square
-    unsigned int *count;       // norm: the completion counters (0 on entry, reset to 0 by the last CTA of a group)
+    unsigned int *count;       // norm: the completion counters (0 on entry, reset to 0 by the last CTA of a group);
+                               // null: write h only, a launch of its own runs the norm
     int count_slot;            // norm: row group g counts in at count[(count_slot + g) % kNormSlots]
     int groups;                // set on the device: the launch's row groups (ceil(m / 16))
     unsigned char *yq;         // gated pair / norm: the quantized form of the bf16 output, codes [m][Np] (or null)
@@ -417,6 +418,7 @@ __device__ __forceinline__ void finish_norm(const Args &a, float *red, int tile)
         }
     }
     if (ks > 1) cg::this_cluster().sync();  // keep this CTA's shared memory alive until every rank has read it
+    if (!a.count) return;  // the norm runs as a launch of its own (norm_rows_kernel)
 
     // Count in; the last CTA runs the norm.
     __shared__ unsigned int last;

@@ -63,6 +63,19 @@ int gemm_min_rows();  // the row count from which the planner takes it
 cudaError_t launch_gemm(const Args &a, const Parts &parts, cudaStream_t stream);
 cudaError_t read_gemm_fault(unsigned *out, bool clear);
 unsigned int *norm_counters();  // device address of the kNormSlots completion counters (null on a CUDA error)
+
+// Defined in q8_norm.cu: the residual norm's RMS norm as a launch of its own, one CTA per row of h, after a product
+// launch whose epilogue wrote h and stopped there (Args::count null).
+struct NormRows {
+    const float *h;      // [m][Np], pad columns 0
+    const float *gamma;  // [N]
+    float eps;
+    uint16_t *ybf;       // bf16 [m][Np], or null
+    unsigned char *yq;   // quantized form: int8 codes [m][Np], or null
+    float *yd;           // its fp32 scales [m][Np / 32] (with yq)
+    int N, Np;
+};
+cudaError_t launch_norm_rows(const NormRows &a, int m, cudaStream_t stream, bool pdl);
 constexpr int kTmaColumns = 128;
 
 // Widths built for each family (descending), used by the planner.

@@ -142,11 +142,14 @@ def test_glu_rows(dev, m):
                what=f"m={m}")
 
 
+@pytest.mark.parametrize("route", ["0", "1"])
 @pytest.mark.parametrize("m,in_place", [(17, False), (40, True), (100, False)])
-def test_residual_norm_rows(dev, m, in_place):
-    """The residual add and RMS norm with row groups: each group's last CTA norms its own rows."""
+def test_residual_norm_rows(dev, m, in_place, route, monkeypatch):
+    """The residual add and RMS norm with row groups: each group's last CTA norms its own rows (Q8_NORM_LAUNCH=0), or
+    a launch of its own norms every row (Q8_NORM_LAUNCH=1)."""
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
+    monkeypatch.setenv("Q8_NORM_LAUNCH", route)
     x, q, s, res, gamma = _norm_inputs(m, 1024, 4096, 5700 + m)
     qt, st = _tiled(torch, q, s, 4096)
     rd = torch.from_numpy(res.copy()).cuda()
@@ -157,10 +160,12 @@ def test_residual_norm_rows(dev, m, in_place):
                 4096, what=f"m={m}")
 
 
-def test_residual_norm_rows_counters_reused(dev):
-    """Calls of 200 rows (13 groups) back to back, more groups in all than the 64 counters: identical bits."""
+def test_residual_norm_rows_counters_reused(dev, monkeypatch):
+    """Calls of 200 rows (13 groups) back to back with the norm in each group's last CTA, more groups in all than the
+    64 counters: identical bits."""
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
+    monkeypatch.setenv("Q8_NORM_LAUNCH", "0")
     m = 200
     x, q, s, res, gamma = _norm_inputs(m, 1024, 4096, 5800)
     qt, st = _tiled(torch, q, s, 4096)

@@ -658,20 +658,26 @@ def test_residual_norm_hidden_width(dev, m, K):
     _norm_check(h, out, x, q, s, res, gamma, 1e-6, 4096, what=f"m={m} K={K}")
 
 
+@pytest.mark.parametrize("route", ["0", "1"])
 @pytest.mark.parametrize("ks", [1, 2, 3, 8])
-def test_residual_norm_every_cluster_split_and_in_place(dev, ks, monkeypatch):
-    """Ragged width (N = 300, three column tiles) under each K split, with h written over the residual in place."""
+def test_residual_norm_every_cluster_split_and_in_place(dev, ks, route, monkeypatch):
+    """Ragged width (N = 300, three column tiles) under each K split, with h written over the residual in place; the
+    norm in the product's last CTA (Q8_NORM_LAUNCH=0) and as a launch of its own (1)."""
     monkeypatch.setenv("Q8_KSPLIT", str(ks))
+    monkeypatch.setenv("Q8_NORM_LAUNCH", route)
     x, q, s, res, gamma = _norm_inputs(5, 1024, 300, 3200 + ks)
     h, out = _norm_run(dev, x, q, s, res.copy(), gamma, 0.5, 300, in_place=True)
     _norm_check(h, out, x, q, s, res, gamma, 0.5, 300, what=f"ks={ks}")
 
 
-def test_residual_norm_counters_reused_and_deterministic(dev):
+@pytest.mark.parametrize("route", ["0", "1"])
+def test_residual_norm_counters_reused_and_deterministic(dev, route, monkeypatch):
     """More calls than the 64 completion counters, back to back: every call's result is bit-identical (the last CTA's
-    fixed-order mean square does not depend on which CTA is last) and within the bound."""
+    fixed-order mean square does not depend on which CTA is last; nor, with the norm as a launch of its own, on
+    anything but the row) and within the bound."""
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
+    monkeypatch.setenv("Q8_NORM_LAUNCH", route)
     x, q, s, res, gamma = _norm_inputs(3, 2048, 4096, 3300)
     xd, qd, sd = _to_dev(torch, x, q, s)
     qt, st = q8.tile_device(qd, sd, 4096)
@@ -686,3 +692,17 @@ def test_residual_norm_counters_reused_and_deterministic(dev):
         assert np.array_equal(h.cpu().numpy().view(np.uint32), h0.view(np.uint32))
         assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), o0)
     _norm_check(h0, o0, x, q, s, res, gamma, 1e-5, 4096, what="repeated")
+
+
+@pytest.mark.parametrize("m,K,N", [(1, 1024, 4096), (5, 1024, 300), (16, 2048, 5000), (33, 1024, 4096)])
+def test_residual_norm_both_routes(dev, m, K, N, monkeypatch):
+    """The norm in the product's last CTA (Q8_NORM_LAUNCH=0) and as a launch of its own, one CTA per row
+    (Q8_NORM_LAUNCH=1): ragged widths, a row wider than the 4096 columns a CTA keeps in registers (N = 5000), row
+    groups (m = 33).  Both within the bound, one in place; h bit-identical (the same product and add)."""
+    x, q, s, res, gamma = _norm_inputs(m, K, N, 3250 + m + N)
+    got = {}
+    for route in ("0", "1"):
+        monkeypatch.setenv("Q8_NORM_LAUNCH", route)
+        got[route] = _norm_run(dev, x, q, s, res.copy(), gamma, 1e-5, N, in_place=(route == "1"))
+        _norm_check(*got[route], x, q, s, res, gamma, 1e-5, N, what=f"m={m} N={N} route {route}")
+    assert np.array_equal(got["0"][0].view(np.uint32), got["1"][0].view(np.uint32))

@@ -300,11 +300,14 @@ def test_glu_writes_its_quantized_form(dev, m, ks, monkeypatch):
     _assert_form_of(torch, qa, outb, f"m={m} ks={ks}")
 
 
+@pytest.mark.parametrize("route", ["0", "1"])
 @pytest.mark.parametrize("m", [1, 16, 40])
-def test_residual_norm_writes_its_quantized_form(dev, m):
-    """The residual norm's out_q8 is the quantized form of its bf16 rows; asked for alone, it is the same bytes."""
+def test_residual_norm_writes_its_quantized_form(dev, m, route, monkeypatch):
+    """The residual norm's out_q8 is the quantized form of its bf16 rows; asked for alone, it is the same bytes.  The
+    norm in the product's last CTA (Q8_NORM_LAUNCH=0) and as a launch of its own (1)."""
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
+    monkeypatch.setenv("Q8_NORM_LAUNCH", route)
     x, q, s, res, gamma = _norm_inputs(m, 2048, 4096, 3500 + m)
     qt, st = q8.tile_device(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), 4096)
     xd, gd = _x_dev(torch, x), torch.from_numpy(gamma).cuda()

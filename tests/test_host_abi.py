@@ -415,3 +415,14 @@ def test_quantized_output_argument_errors(lib):
     assert lib.q8_gemv_residual_norm_ex(A16, B16, C16, R, GM, f(1e-6), H, 0x80000, 0x80000, 2, 64, 96, 2,
                                         None) == 1
     assert lib.q8_gemv_residual_norm_ex(A16, B16, C16, R, GM, f(1e-6), H, None, H, 2, 64, 96, 2, None) == 1
+
+
+@pytest.mark.parametrize("env,launches", [(None, 2), ("1", 2), ("0", 1)])
+def test_residual_norm_launch_count(env, launches, monkeypatch):
+    """The binding's count of a residual-norm call's launches follows the library's rule: the norm's own launch unless
+    Q8_NORM_LAUNCH=0 keeps it in the product's last CTA."""
+    if env is None:
+        monkeypatch.delenv("Q8_NORM_LAUNCH", raising=False)
+    else:
+        monkeypatch.setenv("Q8_NORM_LAUNCH", env)
+    assert q8.residual_norm_launches() == launches
