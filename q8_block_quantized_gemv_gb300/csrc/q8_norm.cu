@@ -1,11 +1,11 @@
 // The RMS norm that closes a residual-norm call, as a launch of its own: one CTA per row of h.
 //
-// The residual-norm entry point folds the next layer's RMS norm after a projection ("plan.rs", `Fold` with `Norm`,
-// `gemv_norm_epilogue`: out = h / sqrt(mean(h^2) + eps) * gamma).  For a few rows the product's last CTA runs the norm
-// itself (finish_norm); from more rows on, that one CTA's pass over every row is the call's tail, so the product
-// writes h and this kernel, chained by programmatic dependent launch, spreads the rows over CTAs.  The arithmetic is
-// finish_norm's: fp32 sums of squares in a fixed order, rstd = 1 / sqrtf(ss / N + eps), (h * rstd) * gamma rounded to
-// bf16, and the quantized form taken from those bf16 values by the rule of q8_quantize_act.
+// The residual-norm entry point follows a projection with the next layer's RMS norm ("plan.rs", `Fold` with `Norm`,
+// `gemv_norm_epilogue`: out = h / sqrt(mean(h^2) + eps) * gamma).  The product's last CTA can run the norm itself
+// (finish_norm, the one-launch fold), but that one CTA's pass over every row is then the call's tail at any m; so
+// the product writes h and this kernel, chained by programmatic dependent launch, spreads the rows over CTAs.  The
+// arithmetic is finish_norm's: fp32 sums of squares in a fixed order, rstd = 1 / sqrtf(ss / N + eps), (h * rstd) *
+// gamma rounded to bf16, and the quantized form taken from those bf16 values by the rule of q8_quantize_act.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
