@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -84,12 +85,21 @@ def step_bytes(m):
 STREAM_SOURCES = ("q8_stream.cu", "q8_device.cuh")  # the sources of the kernels the traffic record covers
 
 
+def strip_comments(src: str) -> str:
+    """C++ source without its comments and with whitespace runs collapsed: what the compiler sees of it (the kernel
+    sources hold no comment markers inside string literals)."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def source_hash():
+    """Hash of the stream kernels' sources as compiled (comments and layout ignored), the key of the traffic record."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "q8_block_quantized_gemv_gb300", "csrc")
     for name in STREAM_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

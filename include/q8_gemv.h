@@ -106,9 +106,9 @@ q8_status q8_gemv(const void *x, const int8_t *q, const float *s, float *y, int 
 q8_status q8_gemv_ex(const void *x, const int8_t *q, const float *s, float *y, int m, int K, int N, int variant,
                      unsigned int flags, q8_stream_t stream);
 
-/* The product followed by the arg-max that closes a decode step (source: "plan.rs", `Launch::ArgMax`, and
- * "int8_model.rs", `decode_step_lg`: the index of the first maximal logit; its CUDA arg-max sends equal values to the
- * lower index).
+/* The product followed by the arg-max that ends a decode step (source: "plan.rs", `Launch::ArgMax`, and
+ * "int8_model.rs", `decode_step_lg`: the lowest index among the largest logits; its CUDA arg-max sends equal values to
+ * the lower index).
  *   idx     device, int64 [m] (written), 8-byte aligned: idx[r] = the smallest n < N with y[r, n] equal to the
  *           largest y[r, n'] over n' < N, 0-based.  Pad columns never take part.  +0.0 and -0.0 count as equal.
  *           The buffer also serves as the call's cross-block scratch: its contents before the call do not matter.
@@ -142,7 +142,7 @@ q8_status q8_tile(const int8_t *q, const float *s, int K, int N, int8_t *qt, flo
 q8_status q8_tile_device(const int8_t *q, const float *s, int K, int N, int8_t *qt, float *st, q8_stream_t stream);
 
 /* The gated pair ("plan.rs", `Launch::GemvGlu`: two projections of one activation through a gate,
- * out = act(x.wg + bg) * (x.wu + bu), SwiGLU when act is none; here without biases):
+ * out = act(x.wg + bg) * (x.wu + bu), silu gating (SwiGLU) by default; here without biases):
  *     out[r, n] = silu(g[r, n]) * u[r, n],   g = x . Wg,  u = x . Wu,   silu(g) = g / (1 + exp(-g)),
  * g and u each the Q8_0 product of q8_gemv (fp32 accumulation), silu and the product in fp32 (CUDA's expf, IEEE
  * division).  One launch: the gate's and the up projection's CTAs of a column tile run side by side in a cluster.
@@ -161,15 +161,16 @@ q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *sg, const in
 
 /* q8_gemv_glu with a third, optional output: out_q8 (device, q8_act_bytes(m, Np) bytes, 16-byte aligned, or NULL)
  * receives the quantized form of the bf16 output -- exactly what q8_quantize_act of out_bf16 (as [m][Np]) writes --
- * from the same launch ("plan.rs": a producer writes its result f32, quantized, or both; `GluActMulQuant`), ready for
- * a Q8_FLAG_Q8_ACT product with K = Np.  At least one of out, out_bf16, out_q8; no two may overlap. */
+ * from the same launch ("plan.rs": an op may emit fp32, the quantized form, or the two together; `GluActMulQuant`),
+ * ready for a Q8_FLAG_Q8_ACT product with K = Np.  At least one of out, out_bf16, out_q8; no two may overlap. */
 q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float *sg, const int8_t *qu, const float *su,
                          float *out, void *out_bf16, void *out_q8, int m, int K, int N, unsigned int flags,
                          q8_stream_t stream);
 
-/* A projection folded with the residual add and the next RMS norm ("plan.rs", `Launch::Fold` of a projection with
- * `Launch::Norm`, `gemv_norm_epilogue`: the projection's blocks count in as they finish, and the finishing block
- * reads their results back through L2 and runs the norm; the norm launch is the lane's "rmsnorm"):
+/* A projection followed by the residual add and the following RMS norm ("plan.rs", `Launch::Fold` of a projection
+ * with `Launch::Norm`, `gemv_norm_epilogue`: each block of the projection registers on a counter when done, and the
+ * block that registers last fetches every result again from L2 and normalises; the norm launch is the lane's
+ * "rmsnorm"):
  *     y = x . W (the Q8_0 product of q8_gemv),   h = residual + y,
  *     out[r, n] = h[r, n] / sqrt(mean_{n' < N} h[r, n']^2 + eps) * gamma[n]
  * Every CTA of the product writes its columns of h.  A second launch on the same stream, chained by programmatic
@@ -214,7 +215,8 @@ typedef struct q8_part {
 #define Q8_MAX_PARTS 8
 
 /* Several Q8_0 products of one activation: y_p = x . W_p for every part p (source: "plan.rs", `Launch::GemmParts`:
- * projections of one activation -- q/k/v, or gate/up -- as one launch over their outputs side by side).
+ * the projections that share an activation -- q/k/v, or gate/up -- run together, their outputs placed next to each
+ * other).
  *   x      device bf16 [m][K], read once for all parts       parts  host array of nparts q8_part (read during the call)
  *   1 <= nparts <= Q8_MAX_PARTS; every part has the same K; N may differ.  Each y_p is as q8_gemv writes it.
  * With Q8_FLAG_TILED (weights in the q8_tile layout) the parts run as one kernel launch; row-major parts run one
@@ -222,9 +224,9 @@ typedef struct q8_part {
 q8_status q8_gemv_parts(const void *x, const q8_part *parts, int nparts, int m, int K, unsigned int flags,
                         q8_stream_t stream);
 
-/* The quantized form of an activation (source: "plan.rs", `QBLOCK`: the values of an activation's quantized form
- * that share one scale, 32; `Buffer::quantized`: int8 values and a scale per 32; `Launch::projected_input`: a product
- * by checkpoint rows reads its activation quantized under every numerics but the precise one).  One buffer of
+/* The quantized form of an activation (source: "plan.rs", `QBLOCK`: 32 consecutive values of the form share one
+ * scale; `Buffer::quantized`: int8 codes plus one scale for every 32; `Launch::projected_input`: a product over
+ * checkpoint rows takes its activation in this form unless the numerics are the exact ones).  One buffer of
  * q8_act_bytes(m, K) bytes:
  *   values  int8 [m][K]      at byte 0
  *   scales  fp32 [m][K/32]   at byte m * K (16-byte aligned when the buffer is, since K % 32 == 0)

@@ -10,16 +10,17 @@ Contents, each citing the passage it follows (page titles as printed on the page
 * :func:`gemv` -- ``from_q8.rs`` module doc and ``q8_fold``: y[r,n] = sum_b s[b,n] * sum_i x[r,32b+i] q[32b+i,n],
   done in fp64 by the C file ``q8_oracle.c`` (plain loops, the formula's order), with the error scale
   A[r,n] = sum_b |s[b,n]| sum_i |x q|.
-* :func:`argmax` -- ``int8_model.rs`` ``decode_step_lg`` ("the first maximal logit") and the tie rule of its CUDA
+* :func:`argmax` -- ``int8_model.rs`` ``decode_step_lg`` (the lowest index among the largest logits) and the tie rule of its CUDA
   warp arg-max in ``reference_cuda`` (equal values go to the lower index); 0-based here.
 * :func:`quantize` -- ``from_q8.rs`` ``quantize``: the Q8_0 rule and its rejections.
-* :func:`repack` -- ``from_q8.rs`` ``Q8Part`` (the host repacks the checkpoint's blocks into the int8 values and the
-  fp32 scales); the block layout is the reading stated in the design notes (36-byte blocks, fp32 scale first).
+* :func:`repack` -- ``from_q8.rs`` ``Q8Part`` (on the host, the checkpoint's blocks become the int8 values and the fp32
+  scales); the block layout is the reading stated in the design notes (36-byte blocks, fp32 scale first).
 * :func:`repack_f16` -- the same repack from GGML-style blocks (``plan.rs`` names the checkpoint format
   ``GgmlType::Q8_0``): 34-byte blocks, an IEEE binary16 scale then 32 int8 values.
 * :func:`dequantize` -- ``from_q8.rs`` module doc, w = q * d.
 * :func:`residual_norm` -- ``plan.rs`` ``Launch::Fold`` of a projection with ``Launch::Norm`` (``gemv_norm_epilogue``:
-  a projection with the residual add and the next norm in its epilogue; the norm launch is the lane's "rmsnorm"):
+  a projection whose epilogue adds the residual and applies the following norm; the norm launch is the lane's
+  "rmsnorm"):
   h = residual + x.W, out = h / sqrt(mean_n h^2 + eps) * gamma, in fp64.
 * :func:`quantize_act` -- ``plan.rs`` ``QBLOCK`` / ``Buffer::quantized`` and the quantized numerics of
   ``Launch::projected_input`` (an activation a projection reads quantized: int8 values and one scale per 32 values),
@@ -27,7 +28,7 @@ Contents, each citing the passage it follows (page titles as printed on the page
 * :func:`gemv_q8act` -- the product under those numerics: y[r,n] = sum_b s[b,n] d[r,b] sum_i xq[r,32b+i] q[32b+i,n],
   the inner sums exact integers, the rest in fp64, with its error scale.
 * :func:`glu` -- ``plan.rs`` ``Launch::GemvGlu``: two projections of one activation through a gate,
-  out = act(x.wg + bg) * (x.wu + bu), SwiGLU when ``act`` is none; here without biases, so
+  out = act(x.wg + bg) * (x.wu + bu), silu gating (SwiGLU) by default; here without biases, so
   out = silu(g) * u with g = x.Wg, u = x.Wu (each as :func:`gemv`) and silu(g) = g / (1 + exp(-g)), in fp64.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` to facts the pages and the mathematics fix (brute
@@ -258,7 +259,7 @@ def rmsnorm(h: np.ndarray, gamma: np.ndarray, eps: float, N: int) -> np.ndarray:
 
 def residual_norm(x_bits: np.ndarray, q: np.ndarray, s: np.ndarray, residual: np.ndarray, gamma: np.ndarray,
                   eps: float, N: int, act=None):
-    """A projection folded with the residual add and the next norm (``plan.rs`` ``Launch::Fold`` /
+    """A projection followed by the residual add and the following norm (``plan.rs`` ``Launch::Fold`` /
     ``gemv_norm_epilogue``): h = residual + x.W (each output as :func:`gemv`), out = rmsnorm(h) * gamma.
 
     Returns (h, out, y, a): the new residual stream, the normed activation, the product and its error scale.

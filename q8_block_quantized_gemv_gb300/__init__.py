@@ -6,7 +6,7 @@ C++ host code (repack, quantize).  PyTorch supplies device memory and streams.  
 
 * :func:`gemv` -- ``q8_gemv`` / ``q8_gemv_ex``: y[r, n] = sum_b s[b, n] sum_i x[r, 32b+i] q[32b+i, n]
   ("from_q8.rs", module doc), bf16 x [m, K], int8 q [K, Np], fp32 s [K/32, Np] -> fp32 y [m, Np];
-* :func:`gemv_argmax` -- ``q8_gemv_argmax``: the product and the first-maximum arg-max that closes a decode step;
+* :func:`gemv_argmax` -- ``q8_gemv_argmax``: the product and the first-maximum arg-max that ends a decode step;
 * :func:`quantize_act` -- ``q8_quantize_act``: the quantized form of an activation (int8 values and an fp32 scale per
   32, "plan.rs" ``QBLOCK``); every product function takes the :class:`QuantAct` it returns in place of bf16 x
   (``Q8_FLAG_Q8_ACT``, tiled weights);
@@ -340,7 +340,7 @@ def gemv_glu(x, gate, up, N: int, out=None, out_bf16=None, want=("f32",), consta
 
 def gemv_residual_norm(x, q, s, N: int, residual, gamma, eps: float, h=None, out_bf16=None,
                        constant_weights: bool = False, stream=None, want=("bf16",), out_q8=None):
-    """A projection folded with the residual add and the next RMS norm (q8_gemv_residual_norm_ex), tiled weight:
+    """A projection followed by the residual add and the following RMS norm (q8_gemv_residual_norm_ex), tiled weight:
     h = residual + x.W, out = h / sqrt(mean(h^2) + eps) * gamma.  Returns (h fp32 [m, Np], out bf16 [m, Np]), or
     (h, out_bf16 or None, out_q8) when ``want`` holds "q8" or out_q8 is given (the quantized form of the bf16 rows);
     ``h`` may be ``residual`` (in place)."""

@@ -10,8 +10,8 @@
 //   - per block, the 32 lane products are summed first and then multiplied by the block's scale, as the formula
 //     groups them, and added into an fp32 carry that starts at zero;
 //   - the warps' carries are summed in shared memory in warp order, then, when K is split across the CTAs of a
-//     thread-block cluster (N too narrow to fill the SMs: "plan.rs", `split_counts`, k cut to give the chip's blocks
-//     work), each CTA sums one slice of the columns over the cluster's ranks through distributed shared memory, in
+//     thread-block cluster (N too narrow to fill the SMs: "plan.rs", `split_counts`: K divided so that every
+//     SM gets blocks), each CTA sums one slice of the columns over the cluster's ranks through distributed shared memory, in
 //     rank order.  Every sum has a fixed order, so results are bit-reproducible and need no scratch memory.
 #pragma once
 
@@ -73,8 +73,8 @@ __device__ __forceinline__ void apply_group(Args &a, int group, int groups) {
     }
 }
 
-// Several weights that multiply one activation in one launch ("plan.rs", `Launch::GemmParts`: projections of one
-// activation as one launch over their outputs side by side).  Part p owns the column tiles [tile_end[p-1],
+// Several weights that multiply one activation in one launch ("plan.rs", `Launch::GemmParts`: the projections that
+// share an activation run together, their outputs placed next to each other).  Part p owns the column tiles [tile_end[p-1],
 // tile_end[p]) of the launch's grid; q, s and y are its own, as is N.
 constexpr int kMaxParts = 8;
 struct Parts {
@@ -373,9 +373,9 @@ __device__ __forceinline__ void finish_glu(const Args &a, float *red, int tile) 
     cluster.sync();  // the up projection's rank keeps its shared memory until the gate's rank has read it
 }
 
-// A projection folded with the residual add and the next RMS norm ("plan.rs", `Launch::Fold` of a projection with
-// `Launch::Norm`, `gemv_norm_epilogue`: the projection's blocks count in as they finish, and the finishing block
-// reads their results back through L2 and runs the norm).  Every CTA finishes its columns as finish_n does, writing
+// A projection followed by the residual add and the following RMS norm ("plan.rs", `Launch::Fold` of a projection
+// with `Launch::Norm`, `gemv_norm_epilogue`: each block of the projection registers on a counter when done, and the
+// block that registers last fetches every result again from L2 and normalises).  Every CTA finishes its columns as finish_n does, writing
 // h = residual + y to y; then it counts itself in.  The CTA that counts last reads the m rows of h back (through L2),
 // forms each row's sum of squares in a fixed order (so the result does not depend on which CTA is last) and writes
 // out = h / sqrt(mean + eps) * gamma as bf16 (0 in the pad columns).  Nothing waits on another CTA.

@@ -5,8 +5,8 @@
 // The block's scale s[b, n] belongs to each 32-row block and column, so the weight cannot be dequantized into a bf16
 // operand (8 significant bits cannot hold q * s).  Each 32-row block is therefore contracted on its own -- two
 // K = 16 MMAs of M = 128, N = 128 into a fresh accumulator -- and folded into the fp32 carry on the CUDA cores
-// ("from_q8.rs", module doc: the lanes contract over the int8 rows, the sums are folded down each column with their
-// scales into an fp32 carry).  The exact int8 -> bf16 weights and the bf16 activations make every product exact; the
+// ("from_q8.rs", module doc: int8 rows are contracted lane by lane, and each column's block sums are scaled and
+// accumulated into an fp32 carry).  The exact int8 -> bf16 weights and the bf16 activations make every product exact; the
 // block's sums are fp32.
 //
 // Warp roles (576 threads, one CTA per SM; 18 warps, at most five a scheduler, 96 registers a thread):

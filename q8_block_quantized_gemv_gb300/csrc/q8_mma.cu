@@ -10,7 +10,7 @@
 // Each int8 is converted exactly to bf16 (|q| <= 127 needs 8 significant bits, bf16 has 8).  Every product of a bf16
 // activation and an int8 value is exact; the MMA sums the block's 32 products in fp32 into a fresh accumulator, and
 // the block's sum is then multiplied by its scale and added into an fp32 carry on the CUDA cores ("from_q8.rs", module
-// doc: the lanes contracted over the int8 rows, then folded down each column with their scales, into an fp32 carry).
+// doc: int8 rows are contracted lane by lane, and each column's block sums are scaled and accumulated in fp32).
 #include "q8_launch.h"
 
 namespace q8 {

@@ -3,7 +3,7 @@
 // A warp reads one weight row at a time, 32 * V contiguous bytes (16-byte, 8-byte or 4-byte vector loads per lane,
 // bypassing L1), converts each int8 to fp32 exactly, and accumulates x[r, k] * q[k, n] for every row r.  After each
 // 32-row block the lane sums are multiplied by the block's scale and added into the carry ("from_q8.rs", module doc:
-// per block, the lanes contracted over the int8 rows, then folded down each column with their scales).  For M >= 8 the
+// per block, int8 rows are contracted lane by lane, then each column's sum is scaled into the carry).  For M >= 8 the
 // per-block partials would not fit in registers, so the scale is applied to each value first (x * (q * s), the
 // order of the `q8_fold` stage body); both orders give the same real number and stay within the error bound.
 #include "q8_launch.h"

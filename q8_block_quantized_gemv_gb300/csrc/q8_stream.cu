@@ -26,8 +26,8 @@
 //   - MMA reduction index 2t, 2t+1, 2t+8, 2t+9 is weight row 4t .. 4t+3 of the 16-row half, so a lane's activation
 //     fragment is 4 consecutive activations and its weight fragment the 4 bytes of one stored word;
 //   - the block's sums (fresh accumulators) are folded into the fp32 carry with the block's scales, a packed
-//     fp32x2 FMA over the pair of columns a lane holds ("from_q8.rs", module doc: the lanes contracted over the int8
-//     rows, then folded down each column with their scales, into an fp32 carry).
+//     fp32x2 FMA over the pair of columns a lane holds ("from_q8.rs", module doc: int8 rows contracted lane by
+//     lane, each column's block sums scaled and accumulated in an fp32 carry).
 //
 // For m <= 2 the CUDA cores do the contraction instead (stream_simt_kernel): there the per-row FMAs cost less than
 // the MMA operands' conversion and the per-block exponent choice.

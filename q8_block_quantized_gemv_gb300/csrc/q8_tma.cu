@@ -10,8 +10,8 @@
 //   - seven consumer warps (six for m > 8, in pairs that split a block's columns): each converts the int8 values
 //     exactly to bf16, multiplies them with the activations on the tensor cores (m16n8k16, fp32 accumulation into a
 //     fresh accumulator per block), then folds the block sums into an fp32 carry with the block's scales
-//     ("from_q8.rs", module doc: the lanes contracted over the int8 rows, then folded down each column with their
-//     scales, into an fp32 carry).
+//     ("from_q8.rs", module doc: int8 rows contracted lane by lane, each column's block sums scaled and
+//     accumulated in an fp32 carry).
 // The MMA's K order is a relabeling of the block's rows chosen so that a warp's shared-memory reads of the swizzled
 // weight box are bank-conflict-free: lane quad t reads rows 2t, 2t+8, 2t+1, 2t+9 of each 16-row step (MMA reduction
 // index 2t, 2t+1, 2t+8, 2t+9), and its activation fragment pairs x[2t] with x[2t+8] and x[2t+1] with x[2t+9].  MMA

@@ -651,8 +651,8 @@ def _norm_check(h, outb, x, q, s, res, gamma, eps, N, what="", act=None):
 @pytest.mark.parametrize("m", [1, 2, 8, 16])
 @pytest.mark.parametrize("K", [4096, 14336])
 def test_residual_norm_hidden_width(dev, m, K):
-    """The attention output (K = 4096) and FFN down (K = 14336) projections onto the 4096-wide residual stream, folded
-    with the residual add and the next RMS norm; every output of h and of the normed bf16 rows."""
+    """The attention output (K = 4096) and FFN down (K = 14336) projections onto the 4096-wide residual stream,
+    followed by the residual add and the following RMS norm; every output of h and of the normed bf16 rows."""
     x, q, s, res, gamma = _norm_inputs(m, K, 4096, 3100 + m + K)
     h, out = _norm_run(dev, x, q, s, res, gamma, 1e-6, 4096)
     _norm_check(h, out, x, q, s, res, gamma, 1e-6, 4096, what=f"m={m} K={K}")
