@@ -10,8 +10,8 @@ Contents, each citing the passage it follows (page titles as printed on the page
 * :func:`gemv` -- ``from_q8.rs`` module doc and ``q8_fold``: y[r,n] = sum_b s[b,n] * sum_i x[r,32b+i] q[32b+i,n],
   done in fp64 by the C file ``q8_oracle.c`` (plain loops, the formula's order), with the error scale
   A[r,n] = sum_b |s[b,n]| sum_i |x q|.
-* :func:`argmax` -- ``int8_model.rs`` ``decode_step_lg`` (the lowest index among the largest logits) and the tie rule of its CUDA
-  warp arg-max in ``reference_cuda`` (equal values go to the lower index); 0-based here.
+* :func:`argmax` -- ``int8_model.rs`` ``decode_step_lg`` (the lowest index among the largest logits) and the tie
+  rule of its CUDA warp arg-max in ``reference_cuda`` (equal values go to the lower index); 0-based here.
 * :func:`quantize` -- ``from_q8.rs`` ``quantize``: the Q8_0 rule and its rejections.
 * :func:`repack` -- ``from_q8.rs`` ``Q8Part`` (on the host, the checkpoint's blocks become the int8 values and the fp32
   scales); the block layout is the reading stated in the design notes (36-byte blocks, fp32 scale first).

@@ -10,9 +10,9 @@
 //   - per block, the 32 lane products are summed first and then multiplied by the block's scale, as the formula
 //     groups them, and added into an fp32 carry that starts at zero;
 //   - the warps' carries are summed in shared memory in warp order, then, when K is split across the CTAs of a
-//     thread-block cluster (N too narrow to fill the SMs: "plan.rs", `split_counts`: K divided so that every
-//     SM gets blocks), each CTA sums one slice of the columns over the cluster's ranks through distributed shared memory, in
-//     rank order.  Every sum has a fixed order, so results are bit-reproducible and need no scratch memory.
+//     thread-block cluster (N too narrow to fill the SMs: "plan.rs", `split_counts`: K divided so that every SM
+//     gets blocks), each CTA sums one slice of the columns over the cluster's ranks through distributed shared
+//     memory, in rank order.  Every sum has a fixed order, so results are bit-reproducible and need no scratch memory.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -74,8 +74,8 @@ __device__ __forceinline__ void apply_group(Args &a, int group, int groups) {
 }
 
 // Several weights that multiply one activation in one launch ("plan.rs", `Launch::GemmParts`: the projections that
-// share an activation run together, their outputs placed next to each other).  Part p owns the column tiles [tile_end[p-1],
-// tile_end[p]) of the launch's grid; q, s and y are its own, as is N.
+// share an activation run together, their outputs placed next to each other).  Part p owns the column tiles
+// [tile_end[p-1], tile_end[p]) of the launch's grid; q, s and y are its own, as is N.
 constexpr int kMaxParts = 8;
 struct Parts {
     const int8_t *q[kMaxParts];
@@ -106,7 +106,7 @@ __device__ __forceinline__ int select_part(const Parts &pt, int tile, Args &a) {
 constexpr int kEpiStore = 0;   // write y
 constexpr int kEpiArgmax = 1;  // write y (if any) and fold the row arg-max keys
 constexpr int kEpiGlu = 2;     // gated pair: part 0 is the gate, part 1 the up projection; write silu(g) * u
-constexpr int kEpiNorm = 3;    // residual add, then the last CTA writes the rows' RMS norm
+constexpr int kEpiNorm = 3;    // residual add into h; with counters (Args::count) the last CTA also runs the norm
 
 // A gated-pair launch interleaves the two weights' CTAs: grid x = 2 * (tile * groups + group) + part, clusters of 2
 // along x (the gate's and the up projection's CTAs of one tile, row group and K range side by side).
@@ -375,10 +375,11 @@ __device__ __forceinline__ void finish_glu(const Args &a, float *red, int tile) 
 
 // A projection followed by the residual add and the following RMS norm ("plan.rs", `Launch::Fold` of a projection
 // with `Launch::Norm`, `gemv_norm_epilogue`: each block of the projection registers on a counter when done, and the
-// block that registers last fetches every result again from L2 and normalises).  Every CTA finishes its columns as finish_n does, writing
-// h = residual + y to y; then it counts itself in.  The CTA that counts last reads the m rows of h back (through L2),
-// forms each row's sum of squares in a fixed order (so the result does not depend on which CTA is last) and writes
-// out = h / sqrt(mean + eps) * gamma as bf16 (0 in the pad columns).  Nothing waits on another CTA.
+// block that registers last fetches every result again from L2 and normalises).  Every CTA finishes its columns as
+// finish_n does, writing h = residual + y to y; then (with counters) it counts itself in.  The CTA that counts last
+// reads the m rows of h back (through L2), forms each row's sum of squares in a fixed order (so the result does not
+// depend on which CTA is last) and writes out = h / sqrt(mean + eps) * gamma as bf16 (0 in the pad columns).
+// Nothing waits on another CTA.
 template <int NRED, int MR, int TC, int NTHREADS, int RS = TC>
 __device__ __forceinline__ void finish_norm(const Args &a, float *red, int tile) {
     namespace cg = cooperative_groups;

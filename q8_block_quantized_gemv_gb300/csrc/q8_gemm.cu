@@ -6,8 +6,8 @@
 // operand (8 significant bits cannot hold q * s).  Each 32-row block is therefore contracted on its own -- two
 // K = 16 MMAs of M = 128, N = 128 into a fresh accumulator -- and folded into the fp32 carry on the CUDA cores
 // ("from_q8.rs", module doc: int8 rows are contracted lane by lane, and each column's block sums are scaled and
-// accumulated into an fp32 carry).  The exact int8 -> bf16 weights and the bf16 activations make every product exact; the
-// block's sums are fp32.
+// accumulated into an fp32 carry).  The exact int8 -> bf16 weights and the bf16 activations make every product
+// exact; the block's sums are fp32.
 //
 // Warp roles (576 threads, one CTA per SM; 18 warps, at most five a scheduler, 96 registers a thread):
 //   warp 0     one thread loads block b + 4 into a ring stage: the activations (128 rows x 32 values) by a TMA tensor

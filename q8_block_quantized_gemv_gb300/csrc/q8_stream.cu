@@ -733,8 +733,8 @@ cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, 
 
 }  // namespace
 
-// The completion counters of the residual-norm launches: the library's only scratch memory, static so that the
-// entry point allocates nothing.  Each row group of a launch takes one counter (round robin over the calls); the
+// The completion counters of the residual norm's one-launch fold: the library's only scratch memory, static so that
+// the entry point allocates nothing.  Each row group of a launch takes one counter (round robin over the calls); the
 // group's last CTA leaves it at 0 again.
 __device__ __align__(256) unsigned int g_norm_count[kNormSlots];
 
