@@ -515,6 +515,31 @@ def test_gemv_parts(dev, m, tiled, monkeypatch):
             assert np.array_equal(single.view(np.uint32), got.view(np.uint32))
 
 
+@pytest.mark.parametrize("m", [1, 16])
+@pytest.mark.parametrize("Ns", [(4096, 4096, 4096), (14336, 14336)])
+def test_chain_parts_full_size_sampled(dev, m, Ns):
+    """The decode chain's multi-projection launches as the benchmark makes them -- q/k/v (3 x 4096) and gate/up
+    (2 x 14336) over K = 4096, tiled, constant weights, the planner's own K split -- at m = 1 and 16: 160 sampled
+    columns of every part (tile edges, the last columns, random ones) against the oracle."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    K = 4096
+    x, _, _ = si.case(m, K, 32, si.case_seed(4, m, 90))
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    ws, devw = [], []
+    for i, N in enumerate(Ns):
+        _, q, s = si.case(1, K, N, si.case_seed(4, m, 91 + i))
+        ws.append((q, s))
+        devw.append(q8.tile_device(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), N) + (N,))
+    ys = q8.gemv_parts(xd, devw, tiled=True, constant_weights=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(m + len(Ns))
+    for i, N in enumerate(Ns):
+        cols = np.unique(np.r_[0:16, 120:136, N - 16:N, rng.integers(0, N, 112)])
+        y_o, a_o = oracle.gemv(x, ws[i][0], ws[i][1], cols)
+        _assert_close(ys[i].cpu().numpy()[:, cols], y_o, a_o, f"m={m} part {i} of {Ns}")
+
+
 # --------------------------------------------------------------------------------------------------------------------
 # the gated pair (plan.rs `Launch::GemvGlu`, SwiGLU)
 # --------------------------------------------------------------------------------------------------------------------
