@@ -73,9 +73,15 @@ def padded(n):
 
 def gemv_bytes(m, K, N, argmax=False):
     """Algorithmic bytes of one call: the Q8_0 weight (1 byte a value + 4 bytes a 32-value block: 1.125 a weight,
-    "from_q8.rs" module doc), the bf16 activations and the fp32 outputs (the arg-max's int64 indices instead)."""
+    "from_q8.rs" module doc), the bf16 activations and the fp32 outputs (the arg-max's int64 indices instead), over
+    the N real columns: the zero-padded last tile's columns are not counted."""
+    return K * N * 1.125 + m * K * 2 + (m * 8 if argmax else m * N * 4)
+
+
+def padded_gemv_bytes(m, K, N):
+    """The same over the Np = N rounded up to 32 columns that the row-major storage holds (pads included)."""
     Np = padded(N)
-    return K * Np * 1.125 + m * K * 2 + (m * 8 if argmax else m * Np * 4)
+    return K * Np * 1.125 + m * K * 2 + m * Np * 4
 
 
 def step_bytes(m):
@@ -219,8 +225,9 @@ def run_reference(args, rank, world):
     import synth_inputs as si
     # one bounded sample per step: the first layer's seven GEMVs (host draws, prepared before the clock)
     shapes = layer_shapes()
-    cases = [si.case(args.m, K, N, si.case_seed(4, args.m, i)) for i, (K, N) in enumerate(shapes)]
-    per_step = sum(gemv_bytes(args.m, K, N) for K, N in shapes)
+    m = args.m[0]
+    cases = [si.case(m, K, N, si.case_seed(4, m, i)) for i, (K, N) in enumerate(shapes)]
+    per_step = sum(gemv_bytes(m, K, N) for K, N in shapes)
 
     def one_step():
         for x, q, s in cases:
@@ -233,12 +240,12 @@ def run_reference(args, rank, world):
         one_step()
     dt = (time.perf_counter() - t0) / args.steps
     value = per_step / dt / 1e9
-    sample = f"one layer's 7 GEMVs (4 x 4096x4096, 2 x 4096x14336, 14336x4096) per step, m={args.m}"
+    sample = f"one layer's 7 GEMVs (4 x 4096x4096, 2 x 4096x14336, 14336x4096) per step, m={m}"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "m": args.m, "sample": sample},
+        "config": {"workload": WORKLOAD, "m": m, "sample": sample},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -265,23 +272,33 @@ def job_throughput(bytes_per_step: float, ms_per_step: float, world: int) -> flo
     """Whole-job GB/s of N replicas: every rank runs the whole step, the step time is the slowest rank's."""
     return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
+class ChainWeights:
+    """The decode step's Q8_0 weights, drawn on the device once and shared by the row counts the bench times: the
+    row-major tensors as drawn (the CPU baseline reads them back) and the tiled storage the library streams, made
+    once as a model would make it at load time."""
+
+    def __init__(self, seed=4000):
+        import synth_inputs as si
+        import q8_block_quantized_gemv_gb300 as q8
+        self.shapes = chain_shapes()
+        self.w = [si.device_weight(K, N, seed + i) for i, (K, N) in enumerate(self.shapes)]
+        self.head = si.device_weight(HIDDEN, VOCAB, seed + len(self.shapes))
+        self.wt = [q8.tile_device(q, s, N) for (q, s), (_, N) in zip(self.w, self.shapes)]
+        self.head_t = q8.tile_device(self.head[0], self.head[1], VOCAB)
+
+
 class Chain:
-    """Device-resident weights, activations and outputs of one decode step, and its CUDA graphs.
+    """Device-resident activations and outputs of one decode step at m rows over shared weights, and its CUDA graphs.
 
     The step's data flow is a transformer layer's: q, k and v multiply one activation (one q8_gemv_parts launch),
     o its own, gate and up one more (one q8_gemv_parts launch), down its own; then the tied head with its arg-max.
     Weights are stored tiled (q8_tile_device), as a model would store them once at load time."""
 
-    def __init__(self, torch, m, seed=4000, glu=False, fused=False, q8act=False):
-        import synth_inputs as si
+    def __init__(self, torch, m, weights, seed=4000, glu=False, fused=False, q8act=False):
         import q8_block_quantized_gemv_gb300 as q8
         self.torch, self.m, self.glu, self.fused, self.q8act = torch, m, glu or fused, fused, q8act
-        self.shapes = chain_shapes()
-        # row-major weights as drawn, and the tiled storage the library streams
-        self.w = [si.device_weight(K, N, seed + i) for i, (K, N) in enumerate(self.shapes)]
-        self.head = si.device_weight(HIDDEN, VOCAB, seed + len(self.shapes))
-        self.wt = [q8.tile_device(q, s, N) for (q, s), (_, N) in zip(self.w, self.shapes)]
-        self.head_t = q8.tile_device(self.head[0], self.head[1], VOCAB)
+        self.shapes = weights.shapes
+        self.w, self.head, self.wt, self.head_t = weights.w, weights.head, weights.wt, weights.head_t
         # activations: per layer one for q/k/v, one for o, one for gate/up, one for down; then the head's
         self.x_shapes = [K for _ in range(LAYERS) for K in (HIDDEN, HIDDEN, HIDDEN, FFN)] + [HIDDEN]
         sizes = [m * K for K in self.x_shapes]
@@ -434,9 +451,9 @@ class Chain:
             total += act_read_bytes(m, self.x_shapes[xi], self.q8act)
             for i in gis:
                 K, N = self.shapes[i]
-                total += K * padded(N) * 1.125 + m * padded(N) * 4
+                total += K * N * 1.125 + m * N * 4
             if self.glu and len(gis) == 2:  # one activation output instead of two fp32 ones
-                total -= 2 * m * padded(FFN) * 4 - m * padded(FFN) * out_act
+                total -= 2 * m * FFN * 4 - m * FFN * out_act
             if self.fused and self.shapes[gis[0]][1] == HIDDEN and len(gis) == 1:
                 # o and down: the residual read, h written over it, the normed row and the norm's weight
                 total += m * HIDDEN * 4 + m * HIDDEN * out_act + HIDDEN * 4
@@ -445,24 +462,26 @@ class Chain:
         return total
 
 
-def run_ours(args, rank, world, local_rank):
-    import torch
-    import torch.distributed as dist
-    from q8_block_quantized_gemv_gb300 import build
-    build.build()
-    torch.cuda.set_device(local_rank)
-    m = args.m
-    chain = Chain(torch, m, glu=args.ffn == "glu", fused=args.fused, q8act=args.act == "q8")
+def traffic_record(m, default_step):
+    """ncu DRAM bytes per layer launch at m rows (profiles/traffic.json), while the kernel sources match the capture
+    and the step is the one captured (bf16 activations, two-output gate/up, no fused epilogues); else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+        if rec.get("source_hash") == source_hash() and default_step:
+            return rec.get("by_m", {}).get(str(m), {}).get("traffic_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def measure_chain(args, torch, weights, m, world, local_rank, barrier, max_over_ranks):
+    """Time one row count's step: W warm-up replays, then exactly K timed steps (CUDA events on the launching
+    stream, nvidia-smi clocks sampled meanwhile), then the same K steps end to end (the step's activations copied in
+    from pinned host memory and its tokens copied back, every step).  Returns (chain, result dict)."""
+    chain = Chain(torch, m, weights, glu=args.ffn == "glu", fused=args.fused, q8act=args.act == "q8")
     chain.capture()
     stream = torch.cuda.current_stream()
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def max_over_ranks(v):
-        return reduce_max(v, world, "cuda")
-
     for _ in range(args.warmup):
         chain.g_layers.replay()
         chain.g_head.replay()
@@ -489,7 +508,6 @@ def run_ours(args, rank, world, local_rank):
     head_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     ms = max_over_ranks(ms)
     bytes_step = chain.layer_bytes() + chain.head_bytes()
-    value = job_throughput(bytes_step, ms, world)
 
     # ---- end-to-end: host activations in, the step's tokens out, every step ----
     x_host = torch.empty(chain.x_all.shape, dtype=torch.bfloat16, pin_memory=True)
@@ -518,34 +536,15 @@ def run_ours(args, rank, world, local_rank):
     peak = float(peaks.get("hbm_gbs", 6800.0))
     layer_bytes = chain.layer_bytes()
     achieved = layer_bytes / (layers_ms * 1e-3) / 1e9
-    traffic = None  # ncu DRAM bytes per layer launch, while the kernel sources match the capture
-    try:
-        with open(PROFILE_TRAFFIC) as f:
-            rec = json.load(f)
-        # the capture covers the default step (bf16 activations, two-output gate/up, no fused epilogues)
-        default_step = not (chain.q8act or chain.glu or chain.fused)
-        if rec.get("source_hash") == source_hash() and default_step:
-            traffic = rec.get("by_m", {}).get(str(m), {}).get("traffic_bytes_per_launch")
-    except (OSError, ValueError):
-        pass
+    traffic = traffic_record(m, not (chain.q8act or chain.glu or chain.fused))
     n_layer_launches = len(chain.layer_calls())
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD + (FUSED_NOTE if args.fused else GLU_NOTE if args.ffn == "glu" else "")
-                   + (Q8ACT_NOTE if chain.q8act else ""), "m": m,
-                   "gemvs_per_step": len(chain.shapes) + 1,
-                   "launches_per_step": chain.launches_per_step(),
-                   "bytes_per_step": bytes_step, "us_per_gemv": ms * 1e3 / (len(chain.shapes) + 1),
-                   "pct_of_8TBps": 100.0 * bytes_step / (ms * 1e-3) / 8e12,
-                   "layers_ms": layers_ms, "head_ms": head_ms,
-                   "operands": ("x int8 + fp32 scale per 32 values (quantized on the device), W Q8_0 (int8 + fp32 "
-                                "scale per 32 rows), exact integer block sums, fp32 fold" if chain.q8act else
-                                "x bf16, W Q8_0 (int8 + fp32 scale per 32 rows), fp32 accumulation"),
-                   "l2": "inputs larger than L2 (9.4 GB of weights per step against 129 MB)",
-                   "parallelism": f"replicas x{world}"},
+    res = {
+        "m": m,
+        "value": job_throughput(bytes_step, ms, world), "unit": "GB/s", "ms_per_step": ms,
+        "us_per_gemv": ms * 1e3 / (len(chain.shapes) + 1),
+        "pct_of_8TBps": 100.0 * bytes_step / (ms * 1e-3) / 8e12,
+        "bytes_per_step": bytes_step, "layers_ms": layers_ms, "head_ms": head_ms,
+        "launches_per_step": chain.launches_per_step(),
         "roofline": {"bound": "hbm", "kernel": "q8 stream kernel (the 128 layer launches of a step, back to back)"
                      + (", with their activation quantizer launches" if chain.q8act else ""),
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
@@ -556,6 +555,59 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": chain.x_all.numel() * 2, "d2h_bytes_per_step": m * 8},
         "gpu_launches": chain.launches_per_step() * args.steps,
         "clocks": clocks.summary(),
+    }
+    return chain, res
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from q8_block_quantized_gemv_gb300 import build
+    build.build()
+    torch.cuda.set_device(local_rank)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        return reduce_max(v, world, "cuda")
+
+    weights = ChainWeights()
+    torch.cuda.synchronize()
+    results, first = [], None
+    for m in args.m:
+        chain, res = measure_chain(args, torch, weights, m, world, local_rank, barrier, max_over_ranks)
+        results.append(res)
+        if first is None:
+            first = chain  # the headline chain; the CPU baseline reads its inputs back
+        else:
+            del chain
+            torch.cuda.empty_cache()
+    head, chain = results[0], first
+    m = head["m"]
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD + (FUSED_NOTE if args.fused else GLU_NOTE if args.ffn == "glu" else "")
+                   + (Q8ACT_NOTE if chain.q8act else ""), "m": m,
+                   "m_timed": [r["m"] for r in results],
+                   "gemvs_per_step": len(chain.shapes) + 1,
+                   "launches_per_step": head["launches_per_step"],
+                   "bytes_per_step": head["bytes_per_step"], "us_per_gemv": head["us_per_gemv"],
+                   "pct_of_8TBps": head["pct_of_8TBps"],
+                   "layers_ms": head["layers_ms"], "head_ms": head["head_ms"],
+                   "operands": ("x int8 + fp32 scale per 32 values (quantized on the device), W Q8_0 (int8 + fp32 "
+                                "scale per 32 rows), exact integer block sums, fp32 fold" if chain.q8act else
+                                "x bf16, W Q8_0 (int8 + fp32 scale per 32 rows), fp32 accumulation"),
+                   "l2": "inputs larger than L2 (9.4 GB of weights per step against 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": head["roofline"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "per_m": {str(r["m"]): {k: v for k, v in r.items() if k != "m"} for r in results},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         def host_case(i):
@@ -583,37 +635,49 @@ LAUNCHES = {"qkv": (HIDDEN, [HIDDEN] * 3), "o": (HIDDEN, [HIDDEN]), "gateup": (H
 SWEEP_SHAPES = [(4096, 4096), (4096, 14336), (14336, 4096), (5120, 40), (5120, 3000), (5120, 6144)]
 
 
-def _tiled_weights(K, Ns, copies, seed):
+def _weights(K, Ns, copies, seed, layout="tiled"):
+    """copies x [(q, s, N) per projection]: drawn on the device, tiled unless layout is "rowmajor"."""
     import synth_inputs as si
     import q8_block_quantized_gemv_gb300 as q8
-    return [[q8.tile_device(*si.device_weight(K, N, seed + 10 * c + i), N) + (N,) for i, N in enumerate(Ns)]
-            for c in range(copies)]
+    out = []
+    for c in range(copies):
+        row = []
+        for i, N in enumerate(Ns):
+            q, s = si.device_weight(K, N, seed + 10 * c + i)
+            if layout == "tiled":
+                q, s = q8.tile_device(q, s, N)
+            row.append((q, s, N))
+        out.append(row)
+    return out
 
 
 def run_profile_case(args):
-    """A few calls of one launch kind (tiled weights, constant-weights flag, as in the chain), for a profiler to
-    capture the fourth: `ncu ... -k regex:stream -s 3 -c 1 python bench.py --profile-case gateup --m 16`."""
+    """A few calls of one launch kind (constant-weights flag, as in the chain; tiled unless --layout rowmajor), for a
+    profiler to capture the fourth: `ncu ... -k regex:stream -s 3 -c 1 python bench.py --profile-case gateup --m 16`."""
     import torch
     import synth_inputs as si
     import q8_block_quantized_gemv_gb300 as q8
     from q8_block_quantized_gemv_gb300 import build
     build.build()
     K, Ns = LAUNCHES[args.profile_case]
-    w = _tiled_weights(K, Ns, 2, 21)[0]
-    x = si.device_activations(args.m, K, 3)
+    tiled = args.layout == "tiled"
+    w = _weights(K, Ns, 1, 21, args.layout)[0]
+    x = si.device_activations(args.m[0], K, 3)
     for _ in range(4):
         if args.profile_case == "head":
-            q8.gemv_argmax(x, w[0][0], w[0][1], VOCAB, constant_weights=True, tiled=True)
+            q8.gemv_argmax(x, w[0][0], w[0][1], VOCAB, constant_weights=True, tiled=tiled)
         else:
-            q8.gemv_parts(x, w, tiled=True, constant_weights=True)
+            q8.gemv_parts(x, w, tiled=tiled, constant_weights=True)
     torch.cuda.synchronize()
-    print(json.dumps({"profile_case": args.profile_case, "m": args.m, "device_fault": q8.device_fault()}))
+    print(json.dumps({"profile_case": args.profile_case, "m": args.m[0], "layout": args.layout,
+                      "device_fault": q8.device_fault()}))
 
 
 def run_sweep(args):
     """µs per call and GB/s of the single-GEMV workloads at each m: every call reads its own weight copy (copies
     totalling over 4 x L2, so each call streams from HBM), calls back to back in a CUDA graph with the
-    constant-weights flag, CUDA events around 5 replays after 3 warm-up replays.  One JSON line per (shape, m)."""
+    constant-weights flag, CUDA events around 5 replays after 3 warm-up replays.  One JSON line per (shape, m).
+    --layout rowmajor: the weights as q8_gemv takes them ([K][Np] int8, [K/32][Np] fp32), no tiling step."""
     import torch
     import synth_inputs as si
     import q8_block_quantized_gemv_gb300 as q8
@@ -623,10 +687,14 @@ def run_sweep(args):
     peak = float(peaks.get("hbm_gbs", 6800.0))
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     ms = [int(v) for v in args.sweep_m.split(",")]
-    for K, N in SWEEP_SHAPES:
+    tiled = args.layout == "tiled"
+    shapes = SWEEP_SHAPES
+    if args.sweep_shapes:
+        shapes = [tuple(int(v) for v in kn.split("x")) for kn in args.sweep_shapes.split(",")]
+    for K, N in shapes:
         wb = K * padded(N) * 1.125
         copies = max(2, int(4 * l2 // wb) + 1)
-        ws = _tiled_weights(K, [N], copies, 7)
+        ws = _weights(K, [N], copies, 7, args.layout)
         for m in ms:
             x = si.device_activations(m, K, 3)
             y = torch.empty((m, padded(N)), dtype=torch.float32, device="cuda")
@@ -634,8 +702,8 @@ def run_sweep(args):
 
             def calls():
                 for i in range(per):
-                    qt, st, _ = ws[i % copies][0]
-                    q8.gemv(x, qt, st, N, y=y, tiled=True, constant_weights=True)
+                    q, s, _ = ws[i % copies][0]
+                    q8.gemv(x, q, s, N, y=y, tiled=tiled, constant_weights=True)
             calls()
             torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()
@@ -651,10 +719,11 @@ def run_sweep(args):
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1e3 / (5 * per)
             gbs = gemv_bytes(m, K, N) / (us * 1e-6) / 1e9
-            print(json.dumps({"sweep": "single GEMV, tiled, back to back", "K": K, "N": N, "m": m,
+            print(json.dumps({"sweep": f"single GEMV, {args.layout}, back to back", "K": K, "N": N, "m": m,
                               "tflops": 2.0 * m * K * N / (us * 1e-6) / 1e12,
                               "us_per_call": us, "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak,
-                              "peak_kind": peak_kind, "pct_of_8TBps": 100.0 * gbs / 8000.0}), flush=True)
+                              "peak_kind": peak_kind, "pct_of_8TBps": 100.0 * gbs / 8000.0,
+                              "padded_gbs": padded_gemv_bytes(m, K, N) / (us * 1e-6) / 1e9}), flush=True)
             del g
         del ws
         torch.cuda.empty_cache()
@@ -665,7 +734,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--m", type=int, default=1, help="activation rows per call (1..512)")
+    ap.add_argument("--m", default="1,16",
+                    help="activation rows per call (1..512), a comma list: the first is the headline value, every "
+                         "one is timed and reported under per_m (default 1,16: the decode step's two row counts)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
@@ -679,13 +750,24 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step: µs/call of the single-GEMV workloads, one JSON line each")
     ap.add_argument("--sweep-m", default="1,2,4,8,16", help="row counts of --sweep")
+    ap.add_argument("--sweep-shapes", default="",
+                    help="shapes of --sweep as KxN,KxN,... (default: the attention, FFN and ragged workloads)")
+    ap.add_argument("--layout", choices=["tiled", "rowmajor"], default="tiled",
+                    help="weights of --sweep: the tiled storage (q8_tile_device, Q8_FLAG_TILED) or row-major as "
+                         "q8_gemv takes them with no tiling step")
     ap.add_argument("--profile-case", choices=sorted(LAUNCHES),
                     help="instead of the step: four calls of one launch kind of the step, for a profiler")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
-    if not 1 <= args.m <= 512:
+    try:
+        args.m = [int(v) for v in str(args.m).split(",") if v.strip()]
+    except ValueError:
+        ap.error("--m takes a comma list of row counts")
+    if not args.m or not all(1 <= m <= 512 for m in args.m):
         ap.error("m must be in 1..512 (more than 16 rows: the tiled storage's row groups or prefill GEMM)")
+    if args.layout == "rowmajor" and args.sweep and any(int(v) > 16 for v in args.sweep_m.split(",")):
+        ap.error("the row-major kernels take at most 16 rows")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

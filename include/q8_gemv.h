@@ -18,14 +18,19 @@
  * be 0 (q8_repack and q8_quantize write them so); the GEMV writes exactly 0.0f into y's pad columns regardless.
  *
  * Conventions shared by every entry point:
- *   - The caller owns every buffer; the library keeps no state and allocates no memory.
+ *   - The caller owns every buffer and the library allocates no memory.  Its only state is read-only caches (per
+ *     device: SM count, resident clusters), the device fault words (q8_device_fault), the planner overrides of
+ *     q8_set_tuning, and the residual norm's 64 static completion counters (used only by its one-launch fold; see
+ *     q8_gemv_residual_norm for the limit this puts on overlapping calls).
  *   - Device entry points take device pointers and enqueue work on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  They are asynchronous: Q8_OK means the work was enqueued.  An argument error is returned
  *     before anything is enqueued.  A CUDA error at launch returns Q8_ERR_CUDA; q8_last_cuda_error() then gives the
  *     cudaError_t value for the calling thread.
  *   - Host entry points take host pointers and run synchronously on the calling thread.
  *   - No entry point aborts, throws or prints.
- *   - Every call is thread-safe; calls on one stream run in order.
+ *   - Every call is thread-safe; calls on one stream run in order.  The exception is the residual norm's one-launch
+ *     fold (q8_set_tuning Q8_TUNE_NORM_FOLD = 1): at most 64 of its row groups may be in flight at once over all
+ *     streams and threads.
  */
 #ifndef Q8_GEMV_H
 #define Q8_GEMV_H
@@ -177,7 +182,7 @@ q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float *sg, const
  * dependent launch (it waits for all of h), then runs the norm with one CTA per row: the row's mean square in a fixed
  * order, then out.  The one-launch fold of the source, where the product's last CTA to finish (a completion counter
  * from a fixed set of 64 in static device memory: the library allocates nothing) reads the rows of h back and runs
- * the norm, is kept for comparison (Q8_NORM_LAUNCH=0 in the environment); measured on GB300 it is slower at every m.
+ * the norm, is kept for comparison (q8_set_tuning Q8_TUNE_NORM_FOLD = 1); measured on GB300 it is slower at every m.
  * Either way the result depends only on the inputs, never on which CTA finishes last.
  *   x, q, s   as q8_gemv, the weight in the tiled storage (q8_tile)
  *   residual  device, fp32 [m][Np], 4-byte aligned (read)
@@ -272,6 +277,26 @@ q8_status q8_quantize(const double *w, int K, int N, int8_t *q, float *s);
  * wrong.  Synchronous with respect to the
  * device.  `clear` != 0 resets the word to 0.  Returns Q8_ERR_ARG for a NULL `fault`, Q8_ERR_CUDA on a CUDA error. */
 q8_status q8_device_fault(unsigned int *fault, int clear);
+
+/* Planner overrides for tests and benchmarks (no counterpart on the pages).  Process-wide: every later call on every
+ * thread and device sees the value, so set them only while no other thread is enqueuing work.  Each option starts
+ * from an environment variable, read once, at the first call that plans a launch.
+ *   Q8_TUNE_KSPLIT     0: the planner's K split (default); 1..8: every K-split cluster takes this many CTAs (capped
+ *                      at the number of K blocks; the gated pair and the prefill GEMM take at most 4).
+ *                      Environment: Q8_KSPLIT.
+ *   Q8_TUNE_GEMM       -1: the planner's choice (default); 0: calls of 128 rows or more keep the row groups; 1: they
+ *                      run on the tcgen05 GEMM whatever the weight's width.  Environment: Q8_GEMM (0 or 1).
+ *   Q8_TUNE_NORM_FOLD  0: the residual norm as a launch of its own (default); 1: the one-launch fold, where the
+ *                      product's last CTA runs the norm.  Environment: Q8_NORM_LAUNCH=0 selects 1. */
+#define Q8_TUNE_KSPLIT 0
+#define Q8_TUNE_GEMM 1
+#define Q8_TUNE_NORM_FOLD 2
+
+/* Sets an override.  Returns Q8_ERR_ARG for an unknown option or a value outside its range. */
+q8_status q8_set_tuning(int option, int value);
+
+/* The current value of an override (its environment default until set); -2 for an unknown option. */
+int q8_get_tuning(int option);
 
 /* A static, human-readable name for a status code. */
 const char *q8_status_string(q8_status status);

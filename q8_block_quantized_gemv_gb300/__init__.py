@@ -57,6 +57,8 @@ SIGNATURES = {
     "q8_gemv_glu_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_gemv_residual_norm_ex": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_quantize_act": (_I, [_P, _P, _I, _I, _P]),
+    "q8_set_tuning": (_I, [_I, _I]),
+    "q8_get_tuning": (_I, [_I]),
 }
 
 
@@ -366,10 +368,42 @@ def gemv_residual_norm(x, q, s, N: int, residual, gamma, eps: float, h=None, out
     return (h, out_bf16, out_q8) if q8out else (h, out_bf16)
 
 
+# Planner overrides (q8_set_tuning): the K split (0 = the planner's, 1..8 forced), the prefill GEMM (-1 = the
+# planner's, 0 = row groups, 1 = GEMM) and the residual norm's route (0 = own launch, 1 = the one-launch fold).
+TUNING = {"ksplit": 0, "gemm": 1, "norm_fold": 2}
+
+
+def set_tuning(option: str, value: int) -> None:
+    """Set a process-wide planner override (q8_set_tuning) for tests and benchmarks."""
+    _check(lib().q8_set_tuning(TUNING[option], int(value)), "q8_set_tuning")
+
+
+def get_tuning(option: str) -> int:
+    """The current value of a planner override (q8_get_tuning)."""
+    return int(lib().q8_get_tuning(TUNING[option]))
+
+
+class tuning:
+    """Context manager: ``with tuning(ksplit=4): ...`` sets overrides and restores the previous values on exit."""
+
+    def __init__(self, **overrides):
+        self.overrides, self.saved = overrides, {}
+
+    def __enter__(self):
+        for k, v in self.overrides.items():
+            self.saved.setdefault(k, get_tuning(k))
+            set_tuning(k, v)
+        return self
+
+    def __exit__(self, *exc):
+        for k, v in self.saved.items():
+            set_tuning(k, v)
+
+
 def residual_norm_launches() -> int:
-    """Kernel launches one gemv_residual_norm call makes, by the library's rule: the product, then the norm as a
-    launch of its own (2); 1 when Q8_NORM_LAUNCH=0 in the environment keeps the norm in the product's last CTA."""
-    return 1 if os.environ.get("Q8_NORM_LAUNCH", "").startswith("0") else 2
+    """Kernel launches one gemv_residual_norm call makes, by the library's current rule: the product, then the norm as
+    a launch of its own (2); 1 when the one-launch fold is selected (tuning ``norm_fold`` = 1)."""
+    return 1 if get_tuning("norm_fold") == 1 else 2
 
 
 def device_fault(clear: bool = False) -> int:

@@ -49,6 +49,29 @@ int sm_count(int *out) {
     return 0;
 }
 
+// The test and benchmark overrides of the planner (q8_set_tuning): a forced K split, the prefill GEMM forced on or
+// off, and the residual norm's route.  Each starts from its environment variable (Q8_KSPLIT, Q8_GEMM,
+// Q8_NORM_LAUNCH), read once per process at the first call that needs it; a call then reads one relaxed atomic.
+struct Tuning {
+    std::atomic<int> value[3];
+    Tuning() {
+        const char *k = getenv("Q8_KSPLIT");
+        const char *g = getenv("Q8_GEMM");
+        const char *r = getenv("Q8_NORM_LAUNCH");
+        const int ks = k ? atoi(k) : 0;
+        value[Q8_TUNE_KSPLIT].store(ks >= 1 && ks <= 8 ? ks : 0, std::memory_order_relaxed);
+        value[Q8_TUNE_GEMM].store(g && g[0] == '0' ? 0 : g && g[0] == '1' ? 1 : -1, std::memory_order_relaxed);
+        value[Q8_TUNE_NORM_FOLD].store(r && r[0] == '0' ? 1 : 0, std::memory_order_relaxed);
+    }
+};
+
+Tuning &tuning_table() {
+    static Tuning t;  // initialised once, thread-safely, at the first use
+    return t;
+}
+
+int tuning(int option) { return tuning_table().value[option].load(std::memory_order_relaxed); }
+
 constexpr int kVariantStream = 100;  // internal: the tiled-layout kernel
 
 struct Plan {
@@ -81,11 +104,8 @@ Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long
             --ks;
         }
         int best = (int)ks;
-        const char *force = getenv("Q8_KSPLIT");
-        if (force) {
-            const int f = atoi(force);
-            if (f >= 1 && f <= 8 && f <= nb) best = f;
-        }
+        const int f = tuning(Q8_TUNE_KSPLIT);
+        if (f >= 1 && f <= nb) best = f;
         return Plan{kVariantStream, 16, best};
     }
     if (variant == Q8_VARIANT_AUTO) variant = Q8_VARIANT_TMA;
@@ -105,11 +125,8 @@ Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long
                 best = ks;
             }
         }
-        const char *force = getenv("Q8_KSPLIT");
-        if (force) {
-            const int f = atoi(force);
-            if (f >= 1 && f <= 8 && f <= nb) best = f;
-        }
+        const int f = tuning(Q8_TUNE_KSPLIT);
+        if (f >= 1 && f <= nb) best = f;
         return Plan{Q8_VARIANT_TMA, 16, best};
     }
     if (variant == Q8_VARIANT_SIMT && !q8::simt_has(m, 4)) variant = Q8_VARIANT_MMA;
@@ -159,13 +176,13 @@ size_t x_bytes(unsigned flags, int m, int K) {
 // Whether a tiled call runs on the tcgen05 GEMM (prefill chunks of bf16 activations with a plain store) rather than
 // the row groups of the streaming kernel: from gemm_min_rows() rows, when its 128 x 128 tiles (times the largest K
 // split, 4) give at least 64 CTAs; a narrow weight keeps the row groups, whose grid is 8 times finer.  Q8_GEMM=0 in
-// the environment keeps the row groups, Q8_GEMM=1 takes the GEMM for every such call whatever its width (both for
+// the tuning (Q8_TUNE_GEMM) keeps the row groups, 1 takes the GEMM for every such call whatever its width (both for
 // comparison and tests).
 bool use_gemm(int m, int epi, bool qact, long long col_tiles) {
     if (m < q8::gemm_min_rows() || epi != q8::kEpiStore || qact) return false;
-    const char *env = getenv("Q8_GEMM");
-    if (env && env[0] == '0') return false;
-    if (env && env[0] == '1') return true;
+    const int force = tuning(Q8_TUNE_GEMM);
+    if (force == 0) return false;
+    if (force == 1) return true;
     return col_tiles * ((m + 127) / 128) * 4 >= 64;
 }
 
@@ -343,11 +360,8 @@ int plan_glu(long long tiles, int nb, int sms) {
         if (fit <= 0 || tiles <= fit) break;
         --ks;
     }
-    const char *force = getenv("Q8_KSPLIT");
-    if (force) {
-        const int f = atoi(force);
-        if (f >= 1 && f <= 4 && f <= nb) ks = f;
-    }
+    const int f = tuning(Q8_TUNE_KSPLIT);
+    if (f >= 1 && f <= 4 && f <= nb) ks = f;
     return (int)ks;
 }
 
@@ -414,12 +428,9 @@ extern "C" q8_status q8_gemv_glu(const void *x, const int8_t *qg, const float *s
 // Whether a residual-norm call runs its RMS norm as a launch of its own (one CTA per row, chained by programmatic
 // dependent launch) rather than in the product's last CTA.  Measured on GB300 (4096 x 4096, bf16 output), the own
 // launch is faster at every row count: 8.4 against 10.0 us a call at m = 1, 12.8 against 21.9 at m = 16, since the
-// last CTA's pass over every row is the fold's tail.  Q8_NORM_LAUNCH=0 in the environment keeps the norm in the
+// last CTA's pass over every row is the fold's tail.  The tuning Q8_TUNE_NORM_FOLD = 1 keeps the norm in the
 // product's last CTA (for comparison and tests).
-bool norm_own_launch() {
-    const char *env = getenv("Q8_NORM_LAUNCH");
-    return !(env && env[0] == '0');
-}
+bool norm_own_launch() { return tuning(Q8_TUNE_NORM_FOLD) == 0; }
 
 extern "C" q8_status q8_gemv_residual_norm_ex(const void *x, const int8_t *q, const float *s, const float *residual,
                                               const float *gamma, float eps, float *h, void *out_bf16, void *out_q8,
@@ -507,4 +518,23 @@ extern "C" q8_status q8_device_fault(unsigned int *fault, int clear) {
     if (e != cudaSuccess) return cuda_fail(e);
     *fault |= gemm;
     return Q8_OK;
+}
+
+namespace q8 {
+int forced_ksplit() { return tuning(Q8_TUNE_KSPLIT); }
+}  // namespace q8
+
+extern "C" q8_status q8_set_tuning(int option, int value) {
+    if (option < Q8_TUNE_KSPLIT || option > Q8_TUNE_NORM_FOLD) return Q8_ERR_ARG;
+    const bool ok = option == Q8_TUNE_KSPLIT ? (value >= 0 && value <= 8)
+                    : option == Q8_TUNE_GEMM ? (value >= -1 && value <= 1)
+                                             : (value == 0 || value == 1);
+    if (!ok) return Q8_ERR_ARG;
+    tuning_table().value[option].store(value, std::memory_order_relaxed);
+    return Q8_OK;
+}
+
+extern "C" int q8_get_tuning(int option) {
+    if (option < Q8_TUNE_KSPLIT || option > Q8_TUNE_NORM_FOLD) return -2;
+    return tuning(option);
 }

@@ -476,11 +476,8 @@ cudaError_t launch_gemm(const Args &a, const Parts &pt, cudaStream_t stream) {
         if (fit <= 0 || ctas <= fit) break;
         --ks;
     }
-    const char *force = getenv("Q8_KSPLIT");
-    if (force) {
-        const int f = atoi(force);
-        if (f >= 1 && f <= kMaxSplit && f <= a.nb) ks = f;
-    }
+    const int f = forced_ksplit();
+    if (f >= 1 && f <= kMaxSplit && f <= a.nb) ks = f;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pt.tile_end[pt.count - 1], (unsigned)((a.m + kGM - 1) / kGM), (unsigned)ks);
     cfg.blockDim = dim3(kGThreads, 1, 1);

@@ -142,14 +142,14 @@ def test_glu_rows(dev, m):
                what=f"m={m}")
 
 
-@pytest.mark.parametrize("route", ["0", "1"])
+@pytest.mark.parametrize("route", ["fold", "launch"])
 @pytest.mark.parametrize("m,in_place", [(17, False), (40, True), (100, False)])
-def test_residual_norm_rows(dev, m, in_place, route, monkeypatch):
-    """The residual add and RMS norm with row groups: each group's last CTA norms its own rows (Q8_NORM_LAUNCH=0), or
-    a launch of its own norms every row (Q8_NORM_LAUNCH=1)."""
+def test_residual_norm_rows(dev, m, in_place, route, tune):
+    """The residual add and RMS norm with row groups: each group's last CTA norms its own rows (the one-launch fold,
+    tuning norm_fold = 1), or a launch of its own norms every row (norm_fold = 0)."""
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
-    monkeypatch.setenv("Q8_NORM_LAUNCH", route)
+    tune(norm_fold=int(route == "fold"))
     x, q, s, res, gamma = _norm_inputs(m, 1024, 4096, 5700 + m)
     qt, st = _tiled(torch, q, s, 4096)
     rd = torch.from_numpy(res.copy()).cuda()
@@ -160,12 +160,12 @@ def test_residual_norm_rows(dev, m, in_place, route, monkeypatch):
                 4096, what=f"m={m}")
 
 
-def test_residual_norm_rows_counters_reused(dev, monkeypatch):
+def test_residual_norm_rows_counters_reused(dev, tune):
     """Calls of 200 rows (13 groups) back to back with the norm in each group's last CTA, more groups in all than the
     64 counters: identical bits."""
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
-    monkeypatch.setenv("Q8_NORM_LAUNCH", "0")
+    tune(norm_fold=1)
     m = 200
     x, q, s, res, gamma = _norm_inputs(m, 1024, 4096, 5800)
     qt, st = _tiled(torch, q, s, 4096)
@@ -179,9 +179,9 @@ def test_residual_norm_rows_counters_reused(dev, monkeypatch):
     _norm_check(h0, o0, x, q, s, res, gamma, 1e-5, 4096, what="repeated")
 
 
-def test_rows_match_single_groups(dev, monkeypatch):
+def test_rows_match_single_groups(dev, tune):
     """Each 16-row group of a 50-row call gives the same bits as a call of those rows alone (one K split for both)."""
-    monkeypatch.setenv("Q8_KSPLIT", "4")
+    tune(ksplit=4)
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
     x, q, s = si.case(50, 2048, 600, 5900)

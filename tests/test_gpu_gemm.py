@@ -15,9 +15,9 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(autouse=True)
-def _gemm_whatever_the_width(monkeypatch):
+def _gemm_whatever_the_width(tune):
     """Narrow weights would otherwise take the row groups; these tests are about the GEMM."""
-    monkeypatch.setenv("Q8_GEMM", "1")
+    tune(gemm=1)
 
 
 @pytest.fixture(scope="module")
@@ -66,12 +66,12 @@ def test_matches_oracle(dev, m, K, N):
     assert np.all(y[:, N:] == 0.0)
 
 
-def test_same_as_row_groups_within_bound(dev, monkeypatch):
-    """The GEMM and the row groups (Q8_GEMM=0) agree with the oracle on the same 160-row call."""
+def test_same_as_row_groups_within_bound(dev, tune):
+    """The GEMM and the row groups (tuning gemm = 0) agree with the oracle on the same 160-row call."""
     x, q, s = si.case(160, 2048, 500, 6100)
     y_o, a_o = oracle.gemv(x, q, s)
     y_g = _run(dev, x, q, s, 500)
-    monkeypatch.setenv("Q8_GEMM", "0")
+    tune(gemm=0)
     y_r = _run(dev, x, q, s, 500)
     _assert_close(y_g, y_o, a_o, "gemm")
     _assert_close(y_r, y_o, a_o, "row groups")
@@ -103,10 +103,10 @@ def test_deterministic(dev):
 
 
 @pytest.mark.parametrize("ks", [1, 2, 3, 4])
-def test_every_k_split(dev, ks, monkeypatch):
+def test_every_k_split(dev, ks, tune):
     """Each cluster split of K (ranks summed through distributed shared memory in rank order): K = 4096 (128 blocks,
     uneven thirds), 130 rows, 3 column tiles, every output; the integer case stays exact."""
-    monkeypatch.setenv("Q8_KSPLIT", str(ks))
+    tune(ksplit=ks)
     x, q, s = si.case(130, 4096, 300, 6400 + ks)
     y_o, a_o = oracle.gemv(x, q, s)
     y = _run(dev, x, q, s, 300)

@@ -401,11 +401,11 @@ def test_argmax_scratch_contents_do_not_matter(dev):
 
 
 @pytest.mark.parametrize("ks", [1, 2, 3, 5, 8])
-def test_tma_every_cluster_split(dev, ks, monkeypatch):
+def test_tma_every_cluster_split(dev, ks, tune):
     """The pipelined kernel at every K split across a cluster (the planner's choice forced), m = 1 and 16, against
     the oracle; the device fault word stays clear (no bounded wait ran out)."""
     import q8_block_quantized_gemv_gb300 as q8
-    monkeypatch.setenv("Q8_KSPLIT", str(ks))
+    tune(ksplit=ks)
     for m in (1, 16):
         x, q, s = si.case(m, 2048, 1000, 1700 + ks + m)
         y_o, a_o = oracle.gemv(x, q, s)
@@ -483,11 +483,11 @@ def test_tile_device_matches_host(dev, K, N):
 
 @pytest.mark.parametrize("tiled", [True, False])
 @pytest.mark.parametrize("m", [1, 3, 16])
-def test_gemv_parts(dev, m, tiled, monkeypatch):
+def test_gemv_parts(dev, m, tiled, tune):
     """Several weights of one activation in one call (q/k/v-style widths and a ragged one): each output against the
     oracle, and -- with the K split pinned, so that both calls sum in the same order -- bit-identical to the
     single-weight call on the same layout."""
-    monkeypatch.setenv("Q8_KSPLIT", "2")
+    tune(ksplit=2)
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
     K = 2048
@@ -604,9 +604,9 @@ def test_glu_ffn_gate_up_sampled(dev, m):
 
 @pytest.mark.parametrize("ks", [1, 2, 3, 4])
 @pytest.mark.parametrize("m", [2, 16])
-def test_glu_every_cluster_split(dev, ks, m, monkeypatch):
+def test_glu_every_cluster_split(dev, ks, m, tune):
     """Every K split of the gated pair's clusters (2 x ks CTAs): K = 4096 over 3 column tiles, every output."""
-    monkeypatch.setenv("Q8_KSPLIT", str(ks))
+    tune(ksplit=ks)
     x, qg, sg = si.case(m, 4096, 300, 2300 + 10 * ks + m)
     _, qu, su = si.case(m, 4096, 300, 2400 + 10 * ks + m)
     out, outb = _glu_run(dev, x, qg, sg, qu, su, 300)
@@ -683,26 +683,26 @@ def test_residual_norm_hidden_width(dev, m, K):
     _norm_check(h, out, x, q, s, res, gamma, 1e-6, 4096, what=f"m={m} K={K}")
 
 
-@pytest.mark.parametrize("route", ["0", "1"])
+@pytest.mark.parametrize("route", ["fold", "launch"])
 @pytest.mark.parametrize("ks", [1, 2, 3, 8])
-def test_residual_norm_every_cluster_split_and_in_place(dev, ks, route, monkeypatch):
+def test_residual_norm_every_cluster_split_and_in_place(dev, ks, route, tune):
     """Ragged width (N = 300, three column tiles) under each K split, with h written over the residual in place; the
-    norm in the product's last CTA (Q8_NORM_LAUNCH=0) and as a launch of its own (1)."""
-    monkeypatch.setenv("Q8_KSPLIT", str(ks))
-    monkeypatch.setenv("Q8_NORM_LAUNCH", route)
+    norm in the product's last CTA (tuning norm_fold = 1) and as a launch of its own."""
+    tune(ksplit=ks)
+    tune(norm_fold=int(route == "fold"))
     x, q, s, res, gamma = _norm_inputs(5, 1024, 300, 3200 + ks)
     h, out = _norm_run(dev, x, q, s, res.copy(), gamma, 0.5, 300, in_place=True)
     _norm_check(h, out, x, q, s, res, gamma, 0.5, 300, what=f"ks={ks}")
 
 
-@pytest.mark.parametrize("route", ["0", "1"])
-def test_residual_norm_counters_reused_and_deterministic(dev, route, monkeypatch):
+@pytest.mark.parametrize("route", ["fold", "launch"])
+def test_residual_norm_counters_reused_and_deterministic(dev, route, tune):
     """More calls than the 64 completion counters, back to back: every call's result is bit-identical (the last CTA's
     fixed-order mean square does not depend on which CTA is last; nor, with the norm as a launch of its own, on
     anything but the row) and within the bound."""
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
-    monkeypatch.setenv("Q8_NORM_LAUNCH", route)
+    tune(norm_fold=int(route == "fold"))
     x, q, s, res, gamma = _norm_inputs(3, 2048, 4096, 3300)
     xd, qd, sd = _to_dev(torch, x, q, s)
     qt, st = q8.tile_device(qd, sd, 4096)
@@ -720,14 +720,14 @@ def test_residual_norm_counters_reused_and_deterministic(dev, route, monkeypatch
 
 
 @pytest.mark.parametrize("m,K,N", [(1, 1024, 4096), (5, 1024, 300), (16, 2048, 5000), (33, 1024, 4096)])
-def test_residual_norm_both_routes(dev, m, K, N, monkeypatch):
-    """The norm in the product's last CTA (Q8_NORM_LAUNCH=0) and as a launch of its own, one CTA per row
-    (Q8_NORM_LAUNCH=1): ragged widths, a row wider than the 4096 columns a CTA keeps in registers (N = 5000), row
+def test_residual_norm_both_routes(dev, m, K, N, tune):
+    """The norm in the product's last CTA (tuning norm_fold = 1) and as a launch of its own, one CTA per row
+    (norm_fold = 0): ragged widths, a row wider than the 4096 columns a CTA keeps in registers (N = 5000), row
     groups (m = 33).  Both within the bound, one in place; h bit-identical (the same product and add)."""
     x, q, s, res, gamma = _norm_inputs(m, K, N, 3250 + m + N)
     got = {}
-    for route in ("0", "1"):
-        monkeypatch.setenv("Q8_NORM_LAUNCH", route)
-        got[route] = _norm_run(dev, x, q, s, res.copy(), gamma, 1e-5, N, in_place=(route == "1"))
+    for route in ("fold", "launch"):
+        tune(norm_fold=int(route == "fold"))
+        got[route] = _norm_run(dev, x, q, s, res.copy(), gamma, 1e-5, N, in_place=(route == "launch"))
         _norm_check(*got[route], x, q, s, res, gamma, 1e-5, N, what=f"m={m} N={N} route {route}")
-    assert np.array_equal(got["0"][0].view(np.uint32), got["1"][0].view(np.uint32))
+    assert np.array_equal(got["fold"][0].view(np.uint32), got["launch"][0].view(np.uint32))

@@ -282,12 +282,12 @@ def _assert_form_of(torch, qa, bf16_out, what):
 
 @pytest.mark.parametrize("ks", [1, 2, 3, 4])
 @pytest.mark.parametrize("m", [1, 8, 16, 40])
-def test_glu_writes_its_quantized_form(dev, m, ks, monkeypatch):
+def test_glu_writes_its_quantized_form(dev, m, ks, tune):
     """The gated pair's out_q8 is the quantized form of its bf16 output, for every K split (32-column slices) and row
     groups; the bf16 output itself stays within the bound."""
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
-    monkeypatch.setenv("Q8_KSPLIT", str(ks))
+    tune(ksplit=ks)
     x, qg, sg = si.case(m, 1024, 1000, 2800 + m)
     _, qu, su = si.case(m, 1024, 1000, 2900 + m)
     _, qgd, sgd = _to_dev(torch, x, qg, sg)
@@ -300,14 +300,14 @@ def test_glu_writes_its_quantized_form(dev, m, ks, monkeypatch):
     _assert_form_of(torch, qa, outb, f"m={m} ks={ks}")
 
 
-@pytest.mark.parametrize("route", ["0", "1"])
+@pytest.mark.parametrize("route", ["fold", "launch"])
 @pytest.mark.parametrize("m", [1, 16, 40])
-def test_residual_norm_writes_its_quantized_form(dev, m, route, monkeypatch):
+def test_residual_norm_writes_its_quantized_form(dev, m, route, tune):
     """The residual norm's out_q8 is the quantized form of its bf16 rows; asked for alone, it is the same bytes.  The
-    norm in the product's last CTA (Q8_NORM_LAUNCH=0) and as a launch of its own (1)."""
+    norm in the product's last CTA (tuning norm_fold = 1) and as a launch of its own."""
     torch = dev
     import q8_block_quantized_gemv_gb300 as q8
-    monkeypatch.setenv("Q8_NORM_LAUNCH", route)
+    tune(norm_fold=int(route == "fold"))
     x, q, s, res, gamma = _norm_inputs(m, 2048, 4096, 3500 + m)
     qt, st = q8.tile_device(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), 4096)
     xd, gd = _x_dev(torch, x), torch.from_numpy(gamma).cuda()

@@ -11,7 +11,8 @@ import synth_inputs as si
 import q8_block_quantized_gemv_gb300 as q8
 from q8_block_quantized_gemv_gb300 import build as q8build
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "q8_gemv.h")
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q8_gemv.h")
 
 
 @pytest.fixture(scope="module")
@@ -417,12 +418,38 @@ def test_quantized_output_argument_errors(lib):
     assert lib.q8_gemv_residual_norm_ex(A16, B16, C16, R, GM, f(1e-6), H, None, H, 2, 64, 96, 2, None) == 1
 
 
-@pytest.mark.parametrize("env,launches", [(None, 2), ("1", 2), ("0", 1)])
-def test_residual_norm_launch_count(env, launches, monkeypatch):
-    """The binding's count of a residual-norm call's launches follows the library's rule: the norm's own launch unless
-    Q8_NORM_LAUNCH=0 keeps it in the product's last CTA."""
-    if env is None:
-        monkeypatch.delenv("Q8_NORM_LAUNCH", raising=False)
-    else:
-        monkeypatch.setenv("Q8_NORM_LAUNCH", env)
-    assert q8.residual_norm_launches() == launches
+@pytest.mark.parametrize("env,want", [(None, (0, -1, 0)), ({"Q8_NORM_LAUNCH": "0"}, (0, -1, 1)),
+                                      ({"Q8_NORM_LAUNCH": "1", "Q8_KSPLIT": "3", "Q8_GEMM": "1"}, (3, 1, 0)),
+                                      ({"Q8_KSPLIT": "9", "Q8_GEMM": "0"}, (0, 0, 0))])
+def test_tuning_starts_from_the_environment(env, want):
+    """The planner overrides start from Q8_KSPLIT, Q8_GEMM and Q8_NORM_LAUNCH, read once in a fresh process (an
+    out-of-range K split is ignored); the binding's launch count of a residual-norm call follows the route."""
+    import subprocess
+    import sys
+    e = {k: v for k, v in os.environ.items() if k not in ("Q8_NORM_LAUNCH", "Q8_KSPLIT", "Q8_GEMM")}
+    e.update(env or {})
+    code = ("import q8_block_quantized_gemv_gb300 as q8; "
+            "print(q8.get_tuning('ksplit'), q8.get_tuning('gemm'), q8.get_tuning('norm_fold'), "
+            "q8.residual_norm_launches())")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=e, cwd=ROOT, timeout=120)
+    assert out.returncode == 0, out.stderr
+    got = tuple(int(v) for v in out.stdout.split())
+    assert got == want + (1 if want[2] == 1 else 2,)
+
+
+def test_tuning_set_get_and_rejects(lib):
+    saved = [lib.q8_get_tuning(o) for o in range(3)]
+    try:
+        for opt, ok, bad in ((0, (0, 1, 8), (-1, 9)), (1, (-1, 0, 1), (-2, 2)), (2, (0, 1), (-1, 2))):
+            for v in ok:
+                assert lib.q8_set_tuning(opt, v) == 0 and lib.q8_get_tuning(opt) == v
+            for v in bad:
+                assert lib.q8_set_tuning(opt, v) == 1 and lib.q8_get_tuning(opt) == ok[-1]
+        assert lib.q8_set_tuning(3, 0) == 1 and lib.q8_set_tuning(-1, 0) == 1
+        assert lib.q8_get_tuning(3) == -2
+        with q8.tuning(norm_fold=1, ksplit=5):
+            assert q8.residual_norm_launches() == 1 and q8.get_tuning("ksplit") == 5
+    finally:
+        for o, v in enumerate(saved):
+            lib.q8_set_tuning(o, v)
+    assert [lib.q8_get_tuning(o) for o in range(3)] == saved
