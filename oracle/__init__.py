@@ -118,12 +118,18 @@ def gemv(x_bits: np.ndarray, q: np.ndarray, s: np.ndarray, cols=None):
 def argmax(y: np.ndarray, n: int) -> np.ndarray:
     """Per row, the smallest index j < n with y[r, j] equal to the row's maximum over j < n (0-based).
 
-    Pad columns (j >= n) never take part.  +0.0 and -0.0 compare equal.
+    Pad columns (j >= n) never take part.  +0.0 and -0.0 compare equal.  A NaN logit (of either sign) ranks above
+    every number, +inf included, so a row holding NaN gives its first NaN: the pages' logits are never NaN, and this
+    is the reading that extends their first-maximum rule to a total order.
     """
     y = np.asarray(y, dtype=np.float64)
     out = np.empty(y.shape[0], dtype=np.int64)
     for r in range(y.shape[0]):
         row = y[r, :n]
+        nan = np.flatnonzero(np.isnan(row))
+        if nan.size:
+            out[r] = int(nan[0])
+            continue
         best = row.max()
         out[r] = int(np.flatnonzero(row == best)[0])
     return out

@@ -283,6 +283,22 @@ def test_argmax_first_maximum_and_pads():
     assert oracle.argmax(y2, 4)[2] == 0
 
 
+def test_argmax_nan_ranks_above_every_number():
+    """The reading for NaN logits: a NaN of either sign ranks above +inf, the first NaN of a row wins; without NaN,
+    +inf is an ordinary largest value (first one wins) and -inf never beats a number."""
+    import struct
+    neg_nan = struct.unpack("<d", struct.pack("<Q", 0xFFF8000000000000))[0]
+    pos_nan = struct.unpack("<d", struct.pack("<Q", 0x7FF8000000000000))[0]
+    inf = float("inf")
+    y = np.array([[1.0, inf, 2.0, neg_nan, pos_nan, 0.0],    # NaN above +inf: the first NaN (a negative one)
+                  [-inf, 3.0, inf, -2.0, inf, 9.0],          # +inf is the maximum, first one
+                  [-inf, -inf, -5.0, -inf, 0.0, 0.0],        # -inf loses to a finite number; pads never count
+                  [pos_nan, 1.0, 2.0, 3.0, 0.0, 0.0],        # NaN in the first column
+                  [1.0, 2.0, 3.0, 4.0, pos_nan, neg_nan]])   # NaN in the pads does not count
+    assert list(oracle.argmax(y, 4)) == [3, 2, 2, 0, 3]
+    assert np.signbit(neg_nan) and np.isnan(neg_nan)
+
+
 def test_argmax_of_product_with_planted_winner():
     x, q, s = si.case(2, 512, 200, 23)
     y, _ = oracle.gemv(x, q, s)
