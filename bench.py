@@ -602,7 +602,7 @@ def run_ours(args, rank, world, local_rank):
                                 "scale per 32 rows), exact integer block sums, fp32 fold" if chain.q8act else
                                 "x bf16, W Q8_0 (int8 + fp32 scale per 32 rows), fp32 accumulation"),
                    "l2": "inputs larger than L2 (9.4 GB of weights per step against 129 MB)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", **({"tuning": args.tune} if args.tune else {})},
         "roofline": head["roofline"],
         "e2e": head["e2e"],
         "gpu_launches": head["gpu_launches"],
@@ -720,6 +720,7 @@ def run_sweep(args):
             us = e0.elapsed_time(e1) * 1e3 / (5 * per)
             gbs = gemv_bytes(m, K, N) / (us * 1e-6) / 1e9
             print(json.dumps({"sweep": f"single GEMV, {args.layout}, back to back", "K": K, "N": N, "m": m,
+                              **({"tuning": args.tune} if args.tune else {}),
                               "tflops": 2.0 * m * K * N / (us * 1e-6) / 1e12,
                               "us_per_call": us, "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak,
                               "peak_kind": peak_kind, "pct_of_8TBps": 100.0 * gbs / 8000.0,
@@ -755,6 +756,8 @@ def main():
     ap.add_argument("--layout", choices=["tiled", "rowmajor"], default="tiled",
                     help="weights of --sweep: the tiled storage (q8_tile_device, Q8_FLAG_TILED) or row-major as "
                          "q8_gemv takes them with no tiling step")
+    ap.add_argument("--tune", default="",
+                    help="planner overrides as name=value,... (q8_set_tuning: ksplit, gemm, norm_fold, l2_prefetch)")
     ap.add_argument("--profile-case", choices=sorted(LAUNCHES),
                     help="instead of the step: four calls of one launch kind of the step, for a profiler")
     args = ap.parse_args()
@@ -768,12 +771,26 @@ def main():
         ap.error("m must be in 1..512 (more than 16 rows: the tiled storage's row groups or prefill GEMM)")
     if args.layout == "rowmajor" and args.sweep and any(int(v) > 16 for v in args.sweep_m.split(",")):
         ap.error("the row-major kernels take at most 16 rows")
+    tune = {}
+    for item in filter(None, args.tune.split(",")):
+        name, _, value = item.partition("=")
+        try:
+            tune[name.strip()] = int(value)
+        except ValueError:
+            ap.error(f"--tune: {item!r} is not name=integer")
+    args.tune = tune
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
+    if args.tune:
+        import q8_block_quantized_gemv_gb300 as q8
+        from q8_block_quantized_gemv_gb300 import build
+        build.build()
+        for name, value in args.tune.items():
+            q8.set_tuning(name, value)
     if args.profile_case:
         run_profile_case(args)
         return

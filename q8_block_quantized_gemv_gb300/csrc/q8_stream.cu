@@ -152,10 +152,13 @@ __device__ __forceinline__ uint32_t vmin_u16x2(uint32_t a, uint32_t b) {
     asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
-__device__ __forceinline__ uint32_t vdec_u16x2(uint32_t a) {  // a - 1 in each half, 0 wrapping to 0xFFFF
+__device__ __forceinline__ uint32_t vadd_u16x2(uint32_t a, uint32_t b) {  // per-half sum, wrapping
     uint32_t d;
-    asm("add.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(0xFFFFFFFFu));
+    asm("add.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
+}
+__device__ __forceinline__ uint32_t vdec_u16x2(uint32_t a) {  // a - 1 in each half, 0 wrapping to 0xFFFF
+    return vadd_u16x2(a, 0xFFFFFFFFu);
 }
 
 // D = A * B (+ D) on fp16 or bf16 operands, fp32 accumulators; FIRST starts D from zero.
@@ -196,6 +199,19 @@ __device__ __forceinline__ void issue_unit(unsigned char *stage, const int8_t *q
 #pragma unroll
     for (int seg = 0; seg < 8; ++seg) cp_async16(stage + seg * 512 + lane * 16, src + seg * 512);
     cp_async16(stage + kUnit + lane * 16, reinterpret_cast<const unsigned char *>(s + u * kUnitScales) + lane * 16);
+}
+
+// Requests units [u, u + cnt) of the weight (values and scales, two contiguous ranges in the tiled storage) into L2:
+// a hint with no completion to wait for, issued before the dependency wait so that the units stream from HBM while
+// the previous kernel finishes.
+__device__ __forceinline__ void prefetch_units_l2(const int8_t *q, const float *s, size_t u, int cnt) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<const unsigned char *>(q) +
+                                                                  u * kUnit),
+                 "r"((unsigned)(cnt * kUnit))
+                 : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s + u * kUnitScales),
+                 "r"((unsigned)(cnt * kUnitScales * 4))
+                 : "memory");
 }
 
 // How a block's activations enter the MMA: fp16 as they are (plain), scaled fp16, or raw bf16.  scale[i] = 2^p and
@@ -270,6 +286,24 @@ template <int NR, bool PER_ROW> __device__ __forceinline__ XPlan plan_block(cons
     return pl;
 }
 
+// Whether every activation the warp holds for a block (row g, and row g + 8 when live) already is an fp16 normal:
+// magnitudes in [2^-14, 2^16) as bf16 patterns 0x3880 .. 0x477F (the largest, 65280, below fp16's 65504).  Each word
+// costs a mask, a packed 16-bit add of -0x3880 (in range exactly when the sum is below 0x0F00; smaller magnitudes and
+// zeros wrap above it) and a packed max; one vote decides for the warp.  Blocks with zeros or other ranges take the
+// full plan.
+__device__ __forceinline__ bool block_f16_normal(const uint2 (&x)[2][2], bool live1) {
+    uint32_t m0 = 0u, m1 = 0u;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        m0 = vmax_u16x2(m0, vmax_u16x2(vadd_u16x2(x[0][s].x & 0x7FFF7FFFu, 0xC780C780u),
+                                       vadd_u16x2(x[0][s].y & 0x7FFF7FFFu, 0xC780C780u)));
+        m1 = vmax_u16x2(m1, vmax_u16x2(vadd_u16x2(x[1][s].x & 0x7FFF7FFFu, 0xC780C780u),
+                                       vadd_u16x2(x[1][s].y & 0x7FFF7FFFu, 0xC780C780u)));
+    }
+    const uint32_t mx = live1 ? vmax_u16x2(m0, m1) : m0;
+    return __all_sync(0xffffffffu, (mx & 0xFFFFu) < 0x0F00u && (mx >> 16) < 0x0F00u);
+}
+
 // One block of the warp's run: the 16 slices' MMAs over both 16-row halves and the fold into the carry.  `a` holds
 // the A fragments of the two halves (fp16, or raw bf16), `pl` the factors of the block's scales (2^-p per activation
 // row; unused for bf16 and for PLAIN fp16, which is unscaled), ROWS16 whether activation rows 8..15 exist and SAME
@@ -313,7 +347,7 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
 // GROUPS: m > 16, the rows in groups of 16 (grid x = tiles * groups, ROWS16 only).
 template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
-    stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
+    stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights, const int l2_units) {
     static_assert(ROWS16 || !GROUPS, "row groups are groups of 16 rows");
     constexpr int MR = ROWS16 ? 16 : 8;
     constexpr int NR = ROWS16 ? 2 : 1;  // activation rows per lane: g and g + 8
@@ -349,6 +383,8 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
             cp_async_commit();
         }
+        if (lane == 0 && l2_units > 0 && n > kDepthS - 1)
+            prefetch_units_l2(a.q, a.s, unit0 + kDepthS - 1, min(n - (kDepthS - 1), l2_units));
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!prefetch_weights) {
@@ -410,11 +446,15 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             }
         if (i + 2 < n) load_x(xn2, b0 + i + 2);
         XPlan plan;
+        bool f16_normal = false;  // 16-row kernel: every live activation already an fp16 normal (no plan needed)
         if constexpr (QACT) {
             plan.sf[0] = pack_f32x2(__uint_as_float(xc[0][1].x), __uint_as_float(xc[0][1].x));
             plan.sf[1] = pack_f32x2(__uint_as_float(xc[NR - 1][1].x), __uint_as_float(xc[NR - 1][1].x));
+        } else if constexpr (ROWS16) {
+            f16_normal = block_f16_normal(xc, xlive[NR - 1]);
+            if (!f16_normal) plan = plan_block<NR, false>(xc);
         } else {
-            plan = plan_block<NR, !ROWS16>(xc);
+            plan = plan_block<NR, true>(xc);
         }
 
         cp_async_wait<kDepthS - 1>();  // this lane's copies of unit i have landed
@@ -437,7 +477,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 af[s][3] = ROWS16 ? q8x2_to_f16x2<2>(u1) : 0u;
             }
             block_contract<true, ROWS16, false>(st, lane, af, plan, acc);
-        } else if (ROWS16 && plan.plain) {
+        } else if (ROWS16 && (f16_normal || plan.plain)) {
             uint32_t af[2][4];
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
@@ -523,7 +563,7 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // eight codes, the exact integer is converted to fp32 and folded with s[b, n] * d[r, b].
 template <int M, int EPI, bool QACT = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
-    stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
+    stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights, const int l2_units) {
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -554,6 +594,8 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
             cp_async_commit();
         }
+        if (lane == 0 && l2_units > 0 && n > kDepthS - 1)
+            prefetch_units_l2(a.q, a.s, unit0 + kDepthS - 1, min(n - (kDepthS - 1), l2_units));
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!prefetch_weights) {
@@ -701,7 +743,7 @@ static_assert(2 * kSmemS <= 227 * 1024, "two CTAs per SM");
 
 template <typename Kernel>
 cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, cudaStream_t stream, bool pdl,
-                                 bool prefetch, bool pair) {
+                                 bool prefetch, bool pair, int l2_units) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -728,7 +770,7 @@ cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kernel, a, pt, prefetch ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, kernel, a, pt, prefetch ? 1 : 0, prefetch ? l2_units : 0);
 }
 
 }  // namespace
@@ -784,18 +826,20 @@ int stream_max_clusters(int ks) {
 template <int EPI>
 cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, bool p, bool qact) {
     const bool pair = EPI == kEpiGlu;
+    const int l2 = l2_prefetch_units();
+    auto go = [&](auto kernel) { return launch_stream_kernel(kernel, a, pt, stream, pdl, p, pair, l2); };
     if (qact) {
-        if (a.m == 1) return launch_stream_kernel(stream_simt_kernel<1, EPI, true>, a, pt, stream, pdl, p, pair);
-        if (a.m == 2) return launch_stream_kernel(stream_simt_kernel<2, EPI, true>, a, pt, stream, pdl, p, pair);
-        if (a.m <= 8) return launch_stream_kernel(stream_kernel<false, EPI, true>, a, pt, stream, pdl, p, pair);
-        if (a.m <= kGroupRows) return launch_stream_kernel(stream_kernel<true, EPI, true>, a, pt, stream, pdl, p, pair);
-        return launch_stream_kernel(stream_kernel<true, EPI, true, true>, a, pt, stream, pdl, p, pair);
+        if (a.m == 1) return go(stream_simt_kernel<1, EPI, true>);
+        if (a.m == 2) return go(stream_simt_kernel<2, EPI, true>);
+        if (a.m <= 8) return go(stream_kernel<false, EPI, true>);
+        if (a.m <= kGroupRows) return go(stream_kernel<true, EPI, true>);
+        return go(stream_kernel<true, EPI, true, true>);
     }
-    if (a.m == 1) return launch_stream_kernel(stream_simt_kernel<1, EPI>, a, pt, stream, pdl, p, pair);
-    if (a.m == 2) return launch_stream_kernel(stream_simt_kernel<2, EPI>, a, pt, stream, pdl, p, pair);
-    if (a.m <= 8) return launch_stream_kernel(stream_kernel<false, EPI>, a, pt, stream, pdl, p, pair);
-    if (a.m <= kGroupRows) return launch_stream_kernel(stream_kernel<true, EPI>, a, pt, stream, pdl, p, pair);
-    return launch_stream_kernel(stream_kernel<true, EPI, false, true>, a, pt, stream, pdl, p, pair);
+    if (a.m == 1) return go(stream_simt_kernel<1, EPI>);
+    if (a.m == 2) return go(stream_simt_kernel<2, EPI>);
+    if (a.m <= 8) return go(stream_kernel<false, EPI>);
+    if (a.m <= kGroupRows) return go(stream_kernel<true, EPI>);
+    return go(stream_kernel<true, EPI, false, true>);
 }
 
 cudaError_t launch_stream(const Args &a, const Parts &pt, int epi, cudaStream_t stream, bool pdl,
