@@ -213,7 +213,8 @@ __device__ __forceinline__ uint32_t bf16x2_exact(float lo, float hi) {
 // the high word (-0.0 counted as +0.0), 0xFFFFFFFF - n in the low word.  Every real key is nonzero, so 0 is the
 // identity of the max.
 __device__ __forceinline__ unsigned long long argmax_key(float v, int n) {
-    uint32_t b = (v == 0.0f) ? 0u : __float_as_uint(v);
+    // -0.0 keys as +0.0; every NaN (either sign, any payload) as the positive quiet NaN, above +inf
+    uint32_t b = (v == 0.0f) ? 0u : (v != v) ? 0x7FC00000u : __float_as_uint(v);
     const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
     return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)n);
 }

@@ -346,15 +346,17 @@ def test_argmax_tied_head_full(dev, m):
     _argmax_ok(idx3, y_o, a_o, 128256)
 
 
-def test_argmax_head_m16_sampled_rows(dev):
+def test_argmax_head_m16_every_row(dev):
+    """The tied head at m = 16 (K = 4096, N = 128256): every logit of every row against the oracle, and each row's
+    fused arg-max under the rule -- on the row-major and the tiled storage."""
     x, q, s = si.case(16, 4096, 128256, si.case_seed(4, 16))
-    idx, logits = _argmax(dev, x, q, s, 128256)
-    for r in (0, 7, 15):
-        y_o, a_o = oracle.gemv(x[r:r + 1], q, s)
-        _assert_close(logits[r:r + 1], y_o, a_o, f"row {r}")
-        _argmax_ok(idx[r:r + 1], y_o, a_o, 128256)
-    for r in range(16):
-        assert idx[r] == int(np.flatnonzero(logits[r, :128256] == logits[r, :128256].max())[0])
+    y_o, a_o = oracle.gemv(x, q, s)
+    for tiled in (False, True):
+        idx, logits = _argmax(dev, x, q, s, 128256, tiled=tiled)
+        _assert_close(logits, y_o, a_o, f"head logits, tiled={tiled}")
+        _argmax_ok(idx, y_o, a_o, 128256)
+        for r in range(16):
+            assert idx[r] == int(np.flatnonzero(logits[r, :128256] == logits[r, :128256].max())[0])
 
 
 @pytest.mark.parametrize("m", [1, 5, 16])
@@ -384,6 +386,33 @@ def test_argmax_planted_ties_and_pads(dev, m):
     idx, _ = _argmax(dev, xa, qn, s, N)
     assert np.all(idx < N)
     _argmax_ok(idx, y_o, a_o, N)
+
+
+@pytest.mark.parametrize("m", [1, 3, 16])
+def test_argmax_nonfinite_logits(dev, m):
+    """Activations holding inf or NaN make the logits +-inf and NaN (inf * 0 is NaN).  The arg-max follows the
+    oracle's reading exactly: a NaN of either sign ranks above every number (the first NaN wins), +inf above every
+    finite logit (the first +inf wins); the other rows as usual."""
+    K, N = 512, 700
+    x, q, s = si.case(m, K, N, 1400 + m)
+    x[0, 40] = np.uint16(0x7F80)          # row 0: +inf meets q[40, n]: +-inf, NaN where q[40, n] = 0
+    q[40, [100, 300]] = 0
+    if m > 1:
+        x[1, 41] = np.uint16(0x7F80)      # row 1: +inf, every q[41, n] nonzero: +-inf only, the first +inf wins
+        q[41, :N][q[41, :N] == 0] = 1
+        x[2, 7] = np.uint16(0xFFC0)       # row 2: a negative NaN activation: every real logit NaN
+    y_o, a_o = oracle.gemv(x, q, s)
+    want = oracle.argmax(y_o, N)
+    assert want[0] == int(np.flatnonzero(q[40, :N] == 0)[0])
+    special = [0] if m == 1 else [0, 1, 2]
+    for tiled in (False, True):
+        idx, logits = _argmax(dev, x, q, s, N, tiled=tiled)
+        assert np.array_equal(np.isnan(logits[:, :N]), np.isnan(y_o[:, :N])), tiled
+        for r in special:
+            assert idx[r] == want[r], (tiled, r, idx[r], want[r])
+        rest = [r for r in range(m) if r not in special]
+        if rest:
+            _argmax_ok(idx[rest], y_o[rest], a_o[rest], N)
 
 
 def test_argmax_scratch_contents_do_not_matter(dev):
