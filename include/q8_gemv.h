@@ -208,6 +208,30 @@ q8_status q8_gemv_residual_norm_ex(const void *x, const int8_t *q, const float *
                                    const float *gamma, float eps, float *h, void *out_bf16, void *out_q8, int m,
                                    int K, int N, unsigned int flags, q8_stream_t stream);
 
+/* The rows one q8_gemv_residual_norm_noalloc call takes at most: its static scratch holds one completion counter per
+ * group of 16 rows. */
+#define Q8_FOLD_STATIC_MAX_ROWS 512
+
+/* q8_gemv_residual_norm as one kernel launch that needs no device memory beyond its arguments and allocates none.
+ * No counterpart on the pages: it serves callers that cannot call cudaMalloc or take memory from an allocator --
+ * code running where device allocation is forbidden or would stall the pipeline (a real-time loop, a host
+ * framework that owns all device memory and gives its plugins none, a step that must not synchronise the device).
+ * It runs the source's one-launch fold (the product's last CTA per group of 16 rows reads h back and normalises),
+ * whose completion counters live in a fixed array of this library (Q8_FOLD_STATIC_MAX_ROWS / 16 = 32 counters,
+ * 128 bytes held by every GPU that loads the library until the process exits).
+ *   Arguments, layouts, the result and its bound as q8_gemv_residual_norm (tiled storage; Q8_FLAG_TILED required,
+ *   Q8_FLAG_CONSTANT_WEIGHTS and Q8_FLAG_Q8_ACT accepted), with 1 <= m <= Q8_FOLD_STATIC_MAX_ROWS.
+ *   The call enqueues a memset that clears the counters it uses, then the product.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture on the device.  Every call shares the one array: calls whose work
+ * overlaps on a GPU (other streams, other threads) race on the counters and give wrong results; calls on one stream
+ * are ordered and safe.
+ * Errors: Q8_ERR_SHAPE for m > Q8_FOLD_STATIC_MAX_ROWS (and as q8_gemv_residual_norm); Q8_ERR_ARG, Q8_ERR_ALIGN,
+ * Q8_ERR_CUDA as q8_gemv_residual_norm.  Nothing is enqueued on an argument error. */
+q8_status q8_gemv_residual_norm_noalloc(const void *x, const int8_t *q, const float *s, const float *residual,
+                                        const float *gamma, float eps, float *h, void *out_bf16, int m, int K, int N,
+                                        unsigned int flags, q8_stream_t stream);
+
 /* One weight of a multi-projection call: its Q8_0 values and scales (row-major, or tiled with Q8_FLAG_TILED), its
  * output y [m][q8_padded_n(N)] (written) and its N. */
 typedef struct q8_part {

@@ -57,6 +57,8 @@ SIGNATURES = {
     "q8_gemv_glu_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_gemv_residual_norm_ex": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     "q8_quantize_act": (_I, [_P, _P, _I, _I, _P]),
+    "q8_gemv_residual_norm_noalloc": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, ctypes.c_uint,
+                                          _P]),
     "q8_set_tuning": (_I, [_I, _I]),
     "q8_get_tuning": (_I, [_I]),
 }
@@ -399,6 +401,28 @@ class tuning:
     def __exit__(self, *exc):
         for k, v in self.saved.items():
             set_tuning(k, v)
+
+
+def gemv_residual_norm_noalloc(x, q, s, N: int, residual, gamma, eps: float, h, out_bf16,
+                               constant_weights: bool = False, stream=None):
+    """q8_gemv_residual_norm_noalloc: the residual add and RMS norm as one launch whose scratch is the library's own
+    static counters (no device allocation by anyone).  h and out_bf16 must be given (h may be ``residual``); calls
+    that overlap on the GPU race on the shared counters.  Returns (h, out_bf16)."""
+    import torch
+    m, K, Np = _check_operands(x, q, s, N, True)
+    if residual.dtype != torch.float32 or residual.shape != (m, Np) or not residual.is_contiguous():
+        raise ValueError("residual must be a contiguous fp32 CUDA tensor [m, Np]")
+    if gamma.dtype != torch.float32 or gamma.numel() < N or not gamma.is_contiguous():
+        raise ValueError("gamma must be a contiguous fp32 CUDA tensor of at least N values")
+    if h.dtype != torch.float32 or h.shape != (m, Np) or not h.is_contiguous():
+        raise ValueError("h must be a contiguous fp32 CUDA tensor [m, Np]")
+    if out_bf16.dtype != torch.bfloat16 or out_bf16.shape != (m, Np) or not out_bf16.is_contiguous():
+        raise ValueError("out_bf16 must be a contiguous bf16 CUDA tensor [m, Np]")
+    _check(lib().q8_gemv_residual_norm_noalloc(x.data_ptr(), q.data_ptr(), s.data_ptr(), residual.data_ptr(),
+                                               gamma.data_ptr(), float(eps), h.data_ptr(), out_bf16.data_ptr(), m, K,
+                                               N, _flags(constant_weights, True, x), _stream_handle(stream)),
+           "q8_gemv_residual_norm_noalloc")
+    return h, out_bf16
 
 
 def residual_norm_launches() -> int:

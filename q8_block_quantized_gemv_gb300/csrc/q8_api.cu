@@ -544,3 +544,90 @@ extern "C" int q8_get_tuning(int option) {
     if (option < 0 || option >= kTuneOptions) return -2;
     return tuning(option);
 }
+
+// ---------------------------------------------------------------------------------------------------------------------
+// The residual norm's one-launch fold for callers that cannot allocate device memory
+// ---------------------------------------------------------------------------------------------------------------------
+
+namespace {
+
+// The fold's only scratch: one completion counter per group of 16 rows, in this file's own static device array
+// (every GPU that loads the library holds these 128 bytes until the process exits).  Every call uses counters
+// 0 .. groups-1 and clears them first, so calls whose kernels overlap on a GPU race on them.
+constexpr int kFoldStaticGroups = Q8_FOLD_STATIC_MAX_ROWS / q8::kGroupRows;
+static __device__ __align__(256) unsigned int g_fold_static_counters[kFoldStaticGroups];
+static_assert(kFoldStaticGroups <= q8::kNormSlots, "the kernel takes counter (slot + group) % kNormSlots");
+
+// The device address of g_fold_static_counters on the current device.  In host code the array's name stands for a
+// host-side shadow, not for device memory, so the address is asked of the runtime -- once per device, with that
+// device current, on the first call there -- and kept.
+cudaError_t fold_static_counters(unsigned int **out) {
+    static std::atomic<unsigned int *> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) {
+        unsigned int *p = cache[dev].load(std::memory_order_acquire);
+        if (p) {
+            *out = p;
+            return cudaSuccess;
+        }
+    }
+    void *base = nullptr;
+    e = cudaGetSymbolAddress(&base, g_fold_static_counters);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) cache[dev].store(static_cast<unsigned int *>(base), std::memory_order_release);
+    *out = static_cast<unsigned int *>(base);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" q8_status q8_gemv_residual_norm_noalloc(const void *x, const int8_t *q, const float *s,
+                                                   const float *residual, const float *gamma, float eps, float *h,
+                                                   void *out_bf16, int m, int K, int N, unsigned int flags,
+                                                   q8_stream_t stream) {
+    if (m > Q8_FOLD_STATIC_MAX_ROWS) return Q8_ERR_SHAPE;  // more row groups than the static counters
+    q8_status st = check_gemv_args(x, q, s, m, K, N, flags);
+    if (st != Q8_OK) return st;
+    if (!residual || !gamma || !h || !out_bf16) return Q8_ERR_ARG;
+    if (!flags_ok(flags) || !(flags & Q8_FLAG_TILED)) return Q8_ERR_ARG;
+    if (!(eps >= 0.0f) || !(eps < INFINITY)) return Q8_ERR_ARG;
+    if (q8_tiled_n(N) < 0) return Q8_ERR_SHAPE;
+    if (!aligned(h, 16) || !aligned(out_bf16, 16) || !aligned(residual, 4) || !aligned(gamma, 4)) return Q8_ERR_ALIGN;
+    const int Np = q8_padded_n(N);
+    const size_t wcols = (size_t)q8_tiled_n(N);
+    const size_t hbytes = (size_t)m * Np * 4, obytes = (size_t)m * Np * 2;
+    if (h != residual && overlaps(h, hbytes, residual, hbytes)) return Q8_ERR_ARG;
+    const void *ins[4] = {x, q, s, gamma};
+    const size_t inb[4] = {x_bytes(flags, m, K), (size_t)K * wcols, (size_t)(K / Q8_BLOCK) * wcols * 4, (size_t)Np * 4};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(out_bf16, obytes, ins[i], inb[i]) || overlaps(h, hbytes, ins[i], inb[i])) return Q8_ERR_ARG;
+    if (overlaps(out_bf16, obytes, h, hbytes) || overlaps(out_bf16, obytes, residual, hbytes)) return Q8_ERR_ARG;
+
+    unsigned int *counters = nullptr;
+    cudaError_t ce = fold_static_counters(&counters);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    int sms = 0;
+    int e = sm_count(&sms);
+    if (e != 0) return cuda_fail((cudaError_t)e);
+    cudaStream_t cs = (cudaStream_t)stream;
+    const int groups = (m + q8::kGroupRows - 1) / q8::kGroupRows;
+    // the counters must start at zero: a memset node, which allocates nothing
+    ce = cudaMemsetAsync(counters, 0, (size_t)groups * sizeof(unsigned int), cs);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    q8::Parts pt = {};
+    pt.q[0] = q;
+    pt.s[0] = s;
+    pt.y[0] = h;
+    pt.N[0] = N;
+    pt.tile_end[0] = tiles_of(N);
+    pt.count = 1;
+    Args a = {static_cast<const uint16_t *>(x), q, s, h, nullptr, m, K, N, Np, K / Q8_BLOCK, 1,
+              static_cast<uint16_t *>(out_bf16), residual, gamma, eps, counters, 0};
+    a.ksplit = make_plan(m, K, Np, Q8_VARIANT_AUTO, true, sms, pt.tile_end[0]).ksplit;
+    // a plain stream-ordered launch after the memset (no programmatic dependent launch)
+    ce = q8::launch_stream(a, pt, q8::kEpiNorm, cs, false, false, (flags & Q8_FLAG_Q8_ACT) != 0);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    return Q8_OK;
+}

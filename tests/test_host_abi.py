@@ -1,5 +1,6 @@
 """The C ABI on the CPU: the library loads and exports every declared symbol; host entry points agree with the oracle;
 device entry points reject bad arguments before touching CUDA (no compute call runs here)."""
+import ctypes
 import os
 import re
 
@@ -454,3 +455,20 @@ def test_tuning_set_get_and_rejects(lib):
         for o, v in enumerate(saved):
             lib.q8_set_tuning(o, v)
     assert [lib.q8_get_tuning(o) for o in range(4)] == saved
+
+
+def test_residual_norm_noalloc_argument_errors(lib):
+    """The entry point that allocates nothing rejects, before any CUDA call, rows beyond its static counters and the
+    arguments the residual norm rejects."""
+    f = ctypes.c_float
+    X, W, S, R, GM, H, O = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x90000
+    call = lib.q8_gemv_residual_norm_noalloc
+    assert call(X, W, S, R, GM, f(1e-6), H, O, 513, 64, 96, 2, None) == 2      # m > 512: more groups than counters
+    assert call(X, W, S, R, GM, f(1e-6), H, O, 0, 64, 96, 2, None) == 2
+    assert call(X, W, S, R, GM, f(1e-6), H, None, 2, 64, 96, 2, None) == 1     # no bf16 output
+    assert call(X, W, S, R, GM, f(1e-6), None, O, 2, 64, 96, 2, None) == 1     # no h
+    assert call(X, W, S, R, GM, f(1e-6), H, O, 2, 64, 96, 0, None) == 1        # not tiled
+    assert call(X, W, S, R, GM, f(-1.0), H, O, 2, 64, 96, 2, None) == 1        # eps < 0
+    assert call(X, W, S, R, GM, f(1e-6), H + 4, O, 2, 64, 96, 2, None) == 3    # h not 16-byte aligned
+    assert call(X, W, S, R, GM, f(1e-6), H, H, 2, 64, 96, 2, None) == 1        # output over h
+    assert lib.q8_version() > 0  # the library still answers
