@@ -263,6 +263,32 @@ def rmsnorm(h: np.ndarray, gamma: np.ndarray, eps: float, N: int) -> np.ndarray:
     return out
 
 
+def rmsnorm_bound(h: np.ndarray, out: np.ndarray, tol_h: np.ndarray, gamma: np.ndarray, eps: float,
+                  N: int) -> np.ndarray:
+    """How far a bf16 RMS-normed row computed in fp32 may lie from :func:`rmsnorm` of the exact h, per output.
+
+    h, out: the exact (fp64) h and normed row; tol_h: the bound on each computed h.  Terms:
+    * half a bf16 unit: rounding to 8 significant bits moves a value by at most 2^-8 of itself;
+    * the h error carried through the norm: out_n = g_n h_n r with r = (mean h^2 + eps)^-1/2, so
+      |d out_n| <= |g_n| r (|d h_n| + |h_n| sum_k |h_k| |d h_k| / (N (mean h^2 + eps)));
+    * the fp32 arithmetic, in units u = 2^-24: the sum of squares of N values by a tree whose deepest path has
+      D = 4 ceil(Np / 512) + 12 additions (four products a 16-byte chunk, the chunks of one of at least 128 threads
+      in order, five shuffle levels, at most eight warps in order) is within D u of itself; the mean, + eps, the
+      square root and the reciprocal add u, u, u/2 + half the sum's error, and u; the two multiplies 2u; with the
+      bf16 rounding taken on the computed value, D/2 + 7 units in all."""
+    h = np.asarray(h, dtype=np.float64)
+    tol_h = np.asarray(tol_h, dtype=np.float64)
+    g = np.abs(np.asarray(gamma, dtype=np.float64)[:N])
+    Np = h.shape[1]
+    ms = np.mean(h[:, :N] ** 2, axis=1, keepdims=True) + float(eps)
+    r = 1.0 / np.sqrt(ms)
+    carried = np.zeros_like(h)
+    carried[:, :N] = g[None, :] * r * (tol_h[:, :N] + np.abs(h[:, :N]) *
+                                       np.sum(np.abs(h[:, :N]) * tol_h[:, :N], axis=1, keepdims=True) / (N * ms))
+    depth = 4 * -(-Np // 512) + 12
+    return 2.0 ** -8 * np.abs(out) + (1.0 + 2.0 ** -8) * carried + (depth / 2 + 7) * 2.0 ** -24 * np.abs(out)
+
+
 def residual_norm(x_bits: np.ndarray, q: np.ndarray, s: np.ndarray, residual: np.ndarray, gamma: np.ndarray,
                   eps: float, N: int, act=None):
     """A projection followed by the residual add and the following norm (``plan.rs`` ``Launch::Fold`` /

@@ -689,11 +689,7 @@ def _norm_check(h, outb, x, q, s, res, gamma, eps, N, what="", act=None):
     bad = np.abs(h.astype(np.float64) - h_o) > tol_h
     assert not bad.any(), f"{what}: h out of bound at {np.argwhere(bad)[0]}"
     assert np.all(h[:, N:] == 0.0)
-    ms = np.mean(h_o[:, :N] ** 2, axis=1, keepdims=True) + eps
-    rstd = 1.0 / np.sqrt(ms)
-    carried = np.abs(gamma[None, :]) * rstd * (tol_h + np.abs(h_o) * np.sum(np.abs(h_o[:, :N]) * tol_h[:, :N], axis=1,
-                                                                             keepdims=True) / (N * ms))
-    bound = 2.0 ** -8 * np.abs(out_o) + carried + 1e-4 * np.abs(out_o)
+    bound = oracle.rmsnorm_bound(h_o, out_o, tol_h, gamma, eps, N)
     got = si.bf16_bits_to_f32(outb).astype(np.float64)
     bad = np.abs(got - out_o) > bound
     if bad.any():

@@ -502,6 +502,53 @@ def test_norm_pins_catch_planted_mistakes(wrong, monkeypatch):
     assert failed >= 1
 
 
+def _norm_like_the_kernels(h32, gamma32, eps, N, threads):
+    """The RMS norm the way the library's kernels compute it: float32 sums of squares (thread t takes the 16-byte
+    chunks t, t + threads, ... in order, four fused products a chunk), a five-level shuffle tree, the warps in order;
+    the mean, + eps, a correctly rounded square root and reciprocal, two products; then rounding to bf16."""
+    m, Np = h32.shape
+    chunks = Np // 4
+    out = np.zeros((m, Np), dtype=np.float32)
+    for r in range(m):
+        part = np.zeros(threads, dtype=np.float32)
+        for t in range(threads):
+            acc = np.float32(0.0)
+            for j in range(t, chunks, threads):
+                for e in range(4):
+                    v = np.float64(h32[r, 4 * j + e])
+                    acc = np.float32(v * v + np.float64(acc))  # one rounding, as fmaf
+            part[t] = acc
+        warp = part.reshape(threads // 32, 32)
+        for o in (16, 8, 4, 2, 1):
+            warp = (warp + np.roll(warp, -o, axis=1)).astype(np.float32)
+        ss = np.float32(0.0)
+        for w in range(threads // 32):
+            ss = np.float32(ss + warp[w, 0])
+        rstd = np.float32(1.0) / np.sqrt(np.float32(np.float32(ss / np.float32(N)) + np.float32(eps)))
+        out[r, :N] = (h32[r, :N] * rstd).astype(np.float32) * gamma32[:N]
+    return si.bf16_bits_to_f32(si.f32_to_bf16_bits(out)).astype(np.float64)
+
+
+@pytest.mark.parametrize("N,threads", [(300, 256), (4096, 160), (5000, 256)])
+def test_rmsnorm_bound_covers_the_kernels_arithmetic(N, threads):
+    """oracle.rmsnorm_bound holds for the norm computed in fp32 and rounded to bf16 (rows of very different scales,
+    h exact, so only the arithmetic's roundings count), and it is not vacuous: below one bf16 unit of each output."""
+    rng = np.random.default_rng(N)
+    Np = oracle.padded_n(N)
+    h = np.zeros((4, Np))
+    h[:, :N] = rng.standard_normal((4, N)) * np.array([[1.0], [1e3], [1e-3], [7.0]])
+    h32 = h.astype(np.float32)
+    gamma = (0.5 + rng.random(Np)).astype(np.float32)
+    eps = 1e-5
+    got = _norm_like_the_kernels(h32, gamma, eps, N, threads)
+    h64 = h32.astype(np.float64)
+    out_o = oracle.rmsnorm(h64, gamma, eps, N)
+    bound = oracle.rmsnorm_bound(h64, out_o, np.zeros_like(h64), gamma, eps, N)
+    assert np.all(np.abs(got - out_o) <= bound)
+    assert np.all(bound[:, :N] < 2.0 ** -7 * np.abs(out_o[:, :N]))
+    assert np.all(got[:, N:] == 0.0)
+
+
 def test_norm_residual_is_added_to_the_product():
     """h - residual equals the product of gemv, column by column (fp64: the add of an fp32 and an fp64 value is
     exact when their magnitudes are close; here checked to 1 ulp of h)."""

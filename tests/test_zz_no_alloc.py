@@ -49,16 +49,12 @@ def _bf16_ulp(v):
 
 
 def _oracle_bound(h, outb, x, q, s, res, gamma, eps, N):
-    """h within the product's bound plus one fp32 rounding of the add; the normed rows within half a bf16 unit
-    (taken as 2^-8 relative), the h error carried through the norm and 1e-4 relative for the fp32 sums."""
+    """h within the product's bound plus one fp32 rounding of the add; the normed rows within the bound of
+    oracle.rmsnorm_bound (half a bf16 unit, the h error carried through the norm, the fp32 arithmetic's roundings)."""
     h_o, out_o, _, a_o = oracle.residual_norm(x, q, s, res, gamma, eps, N)
     tol_h = TOL * a_o + 2.0 ** -24 * np.abs(h_o)
     assert np.all(np.abs(h.astype(np.float64) - h_o) <= tol_h)
-    ms = np.mean(h_o[:, :N] ** 2, axis=1, keepdims=True) + eps
-    rstd = 1.0 / np.sqrt(ms)
-    carried = np.abs(gamma[None, :]) * rstd * (tol_h + np.abs(h_o) * np.sum(np.abs(h_o[:, :N]) * tol_h[:, :N], axis=1,
-                                                                             keepdims=True) / (N * ms))
-    bound = 2.0 ** -8 * np.abs(out_o) + carried + 1e-4 * np.abs(out_o)
+    bound = oracle.rmsnorm_bound(h_o, out_o, tol_h, gamma, eps, N)
     assert np.all(np.abs(si.bf16_bits_to_f32(outb).astype(np.float64) - out_o) <= bound)
 
 
