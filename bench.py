@@ -757,7 +757,7 @@ def main():
                     help="weights of --sweep: the tiled storage (q8_tile_device, Q8_FLAG_TILED) or row-major as "
                          "q8_gemv takes them with no tiling step")
     ap.add_argument("--tune", default="",
-                    help="planner overrides as name=value,... (q8_set_tuning: ksplit, gemm, norm_fold, l2_prefetch)")
+                    help="planner overrides as name=value,... (q8_set_tuning: ksplit, gemm, norm_fold)")
     ap.add_argument("--profile-case", choices=sorted(LAUNCHES),
                     help="instead of the step: four calls of one launch kind of the step, for a profiler")
     args = ap.parse_args()

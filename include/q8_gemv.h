@@ -311,15 +311,10 @@ q8_status q8_device_fault(unsigned int *fault, int clear);
  *   Q8_TUNE_GEMM       -1: the planner's choice (default); 0: calls of 128 rows or more keep the row groups; 1: they
  *                      run on the tcgen05 GEMM whatever the weight's width.  Environment: Q8_GEMM (0 or 1).
  *   Q8_TUNE_NORM_FOLD  0: the residual norm as a launch of its own (default); 1: the one-launch fold, where the
- *                      product's last CTA runs the norm.  Environment: Q8_NORM_LAUNCH=0 selects 1.
- *   Q8_TUNE_L2_PREFETCH  0..64: weight units (32 x 128 blocks, 4.5 KB) each warp of the tiled kernels requests into
- *                      L2 before it waits for the previous kernel, beyond the two it copies into shared memory; only
- *                      under Q8_FLAG_CONSTANT_WEIGHTS.  Default 0: measured on GB300, any such prefetch made the
- *                      wide projections slower. */
+ *                      product's last CTA runs the norm.  Environment: Q8_NORM_LAUNCH=0 selects 1. */
 #define Q8_TUNE_KSPLIT 0
 #define Q8_TUNE_GEMM 1
 #define Q8_TUNE_NORM_FOLD 2
-#define Q8_TUNE_L2_PREFETCH 3
 
 /* Sets an override.  Returns Q8_ERR_ARG for an unknown option or a value outside its range. */
 q8_status q8_set_tuning(int option, int value);

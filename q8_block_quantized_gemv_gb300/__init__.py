@@ -371,9 +371,8 @@ def gemv_residual_norm(x, q, s, N: int, residual, gamma, eps: float, h=None, out
 
 
 # Planner overrides (q8_set_tuning): the K split (0 = the planner's, 1..8 forced), the prefill GEMM (-1 = the
-# planner's, 0 = row groups, 1 = GEMM), the residual norm's route (0 = own launch, 1 = the one-launch fold) and the
-# weight units per warp requested into L2 before the dependency wait (constant weights).
-TUNING = {"ksplit": 0, "gemm": 1, "norm_fold": 2, "l2_prefetch": 3}
+# planner's, 0 = row groups, 1 = GEMM) and the residual norm's route (0 = own launch, 1 = the one-launch fold).
+TUNING = {"ksplit": 0, "gemm": 1, "norm_fold": 2}
 
 
 def set_tuning(option: str, value: int) -> None:

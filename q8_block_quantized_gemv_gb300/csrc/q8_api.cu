@@ -52,13 +52,11 @@ int sm_count(int *out) {
 // The test and benchmark overrides of the planner (q8_set_tuning): a forced K split, the prefill GEMM forced on or
 // off, and the residual norm's route.  Each starts from its environment variable (Q8_KSPLIT, Q8_GEMM,
 // Q8_NORM_LAUNCH), read once per process at the first call that needs it; a call then reads one relaxed atomic.
-constexpr int kTuneOptions = 4;
-constexpr int kDefaultL2Units = 0;  // see q8_set_tuning: Q8_TUNE_L2_PREFETCH (measured slower when on)
+constexpr int kTuneOptions = 3;
 
 struct Tuning {
     std::atomic<int> value[kTuneOptions];
     Tuning() {
-        value[Q8_TUNE_L2_PREFETCH].store(kDefaultL2Units, std::memory_order_relaxed);
         const char *k = getenv("Q8_KSPLIT");
         const char *g = getenv("Q8_GEMM");
         const char *r = getenv("Q8_NORM_LAUNCH");
@@ -526,15 +524,13 @@ extern "C" q8_status q8_device_fault(unsigned int *fault, int clear) {
 
 namespace q8 {
 int forced_ksplit() { return tuning(Q8_TUNE_KSPLIT); }
-int l2_prefetch_units() { return tuning(Q8_TUNE_L2_PREFETCH); }
 }  // namespace q8
 
 extern "C" q8_status q8_set_tuning(int option, int value) {
     if (option < 0 || option >= kTuneOptions) return Q8_ERR_ARG;
-    const bool ok = option == Q8_TUNE_KSPLIT        ? (value >= 0 && value <= 8)
-                    : option == Q8_TUNE_GEMM        ? (value >= -1 && value <= 1)
-                    : option == Q8_TUNE_NORM_FOLD   ? (value == 0 || value == 1)
-                                                    : (value >= 0 && value <= 64);
+    const bool ok = option == Q8_TUNE_KSPLIT ? (value >= 0 && value <= 8)
+                    : option == Q8_TUNE_GEMM ? (value >= -1 && value <= 1)
+                                             : (value == 0 || value == 1);
     if (!ok) return Q8_ERR_ARG;
     tuning_table().value[option].store(value, std::memory_order_relaxed);
     return Q8_OK;

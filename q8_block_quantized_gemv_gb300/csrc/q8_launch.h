@@ -64,10 +64,8 @@ cudaError_t launch_gemm(const Args &a, const Parts &parts, cudaStream_t stream);
 cudaError_t read_gemm_fault(unsigned *out, bool clear);
 unsigned int *norm_counters();  // device address of the kNormSlots completion counters (null on a CUDA error)
 
-// Defined in q8_api.cu: the K split a test or benchmark forces through q8_set_tuning (0: the planner's), and the
-// weight units per warp the streaming kernels request into L2 before the dependency wait (constant weights only).
+// Defined in q8_api.cu: the K split a test or benchmark forces through q8_set_tuning (0: the planner's).
 int forced_ksplit();
-int l2_prefetch_units();
 
 // Defined in q8_norm.cu: the residual norm's RMS norm as a launch of its own, one CTA per row of h, after a product
 // launch whose epilogue wrote h and stopped there (Args::count null).

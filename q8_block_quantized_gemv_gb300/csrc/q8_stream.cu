@@ -201,19 +201,6 @@ __device__ __forceinline__ void issue_unit(unsigned char *stage, const int8_t *q
     cp_async16(stage + kUnit + lane * 16, reinterpret_cast<const unsigned char *>(s + u * kUnitScales) + lane * 16);
 }
 
-// Requests units [u, u + cnt) of the weight (values and scales, two contiguous ranges in the tiled storage) into L2:
-// a hint with no completion to wait for, issued before the dependency wait so that the units stream from HBM while
-// the previous kernel finishes.
-__device__ __forceinline__ void prefetch_units_l2(const int8_t *q, const float *s, size_t u, int cnt) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<const unsigned char *>(q) +
-                                                                  u * kUnit),
-                 "r"((unsigned)(cnt * kUnit))
-                 : "memory");
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s + u * kUnitScales),
-                 "r"((unsigned)(cnt * kUnitScales * 4))
-                 : "memory");
-}
-
 // How a block's activations enter the MMA: fp16 as they are (plain), scaled fp16, or raw bf16.  scale[i] = 2^p and
 // sf[i] = 2^-p (in both halves of an fp32 pair) for the lane's activation row g + 8i.
 struct XPlan {
@@ -347,7 +334,7 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
 // GROUPS: m > 16, the rows in groups of 16 (grid x = tiles * groups, ROWS16 only).
 template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
-    stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights, const int l2_units) {
+    stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     static_assert(ROWS16 || !GROUPS, "row groups are groups of 16 rows");
     constexpr int MR = ROWS16 ? 16 : 8;
     constexpr int NR = ROWS16 ? 2 : 1;  // activation rows per lane: g and g + 8
@@ -383,8 +370,6 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
             cp_async_commit();
         }
-        if (lane == 0 && l2_units > 0 && n > kDepthS - 1)
-            prefetch_units_l2(a.q, a.s, unit0 + kDepthS - 1, min(n - (kDepthS - 1), l2_units));
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!prefetch_weights) {
@@ -563,7 +548,7 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // eight codes, the exact integer is converted to fp32 and folded with s[b, n] * d[r, b].
 template <int M, int EPI, bool QACT = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
-    stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights, const int l2_units) {
+    stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -594,8 +579,6 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
             cp_async_commit();
         }
-        if (lane == 0 && l2_units > 0 && n > kDepthS - 1)
-            prefetch_units_l2(a.q, a.s, unit0 + kDepthS - 1, min(n - (kDepthS - 1), l2_units));
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!prefetch_weights) {
@@ -743,7 +726,7 @@ static_assert(2 * kSmemS <= 227 * 1024, "two CTAs per SM");
 
 template <typename Kernel>
 cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, cudaStream_t stream, bool pdl,
-                                 bool prefetch, bool pair, int l2_units) {
+                                 bool prefetch, bool pair) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -770,7 +753,7 @@ cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kernel, a, pt, prefetch ? 1 : 0, prefetch ? l2_units : 0);
+    return cudaLaunchKernelEx(&cfg, kernel, a, pt, prefetch ? 1 : 0);
 }
 
 }  // namespace
@@ -826,8 +809,7 @@ int stream_max_clusters(int ks) {
 template <int EPI>
 cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, bool p, bool qact) {
     const bool pair = EPI == kEpiGlu;
-    const int l2 = l2_prefetch_units();
-    auto go = [&](auto kernel) { return launch_stream_kernel(kernel, a, pt, stream, pdl, p, pair, l2); };
+    auto go = [&](auto kernel) { return launch_stream_kernel(kernel, a, pt, stream, pdl, p, pair); };
     if (qact) {
         if (a.m == 1) return go(stream_simt_kernel<1, EPI, true>);
         if (a.m == 2) return go(stream_simt_kernel<2, EPI, true>);

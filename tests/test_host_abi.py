@@ -439,22 +439,21 @@ def test_tuning_starts_from_the_environment(env, want):
 
 
 def test_tuning_set_get_and_rejects(lib):
-    saved = [lib.q8_get_tuning(o) for o in range(4)]
+    saved = [lib.q8_get_tuning(o) for o in range(3)]
     try:
-        for opt, ok, bad in ((0, (0, 1, 8), (-1, 9)), (1, (-1, 0, 1), (-2, 2)), (2, (0, 1), (-1, 2)),
-                             (3, (0, 16, 64), (-1, 65))):
+        for opt, ok, bad in ((0, (0, 1, 8), (-1, 9)), (1, (-1, 0, 1), (-2, 2)), (2, (0, 1), (-1, 2))):
             for v in ok:
                 assert lib.q8_set_tuning(opt, v) == 0 and lib.q8_get_tuning(opt) == v
             for v in bad:
                 assert lib.q8_set_tuning(opt, v) == 1 and lib.q8_get_tuning(opt) == ok[-1]
-        assert lib.q8_set_tuning(4, 0) == 1 and lib.q8_set_tuning(-1, 0) == 1
-        assert lib.q8_get_tuning(4) == -2 and lib.q8_get_tuning(-1) == -2
+        assert lib.q8_set_tuning(3, 0) == 1 and lib.q8_set_tuning(-1, 0) == 1
+        assert lib.q8_get_tuning(3) == -2 and lib.q8_get_tuning(-1) == -2
         with q8.tuning(norm_fold=1, ksplit=5):
             assert q8.residual_norm_launches() == 1 and q8.get_tuning("ksplit") == 5
     finally:
         for o, v in enumerate(saved):
             lib.q8_set_tuning(o, v)
-    assert [lib.q8_get_tuning(o) for o in range(4)] == saved
+    assert [lib.q8_get_tuning(o) for o in range(3)] == saved
 
 
 def test_residual_norm_noalloc_argument_errors(lib):
