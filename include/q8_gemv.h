@@ -67,7 +67,10 @@ typedef enum {
     Q8_ERR_CUDA = 5      /* the CUDA runtime reported an error; see q8_last_cuda_error() */
 } q8_status;
 
-/* Kernel family selector for q8_gemv_ex (benchmarking and testing; q8_gemv picks one by shape). */
+/* Kernel family selector for q8_gemv_ex (benchmarking and testing).  AUTO, what q8_gemv takes, runs the streaming
+ * kernels: each warp copies its 32-row x 128-column blocks of the row-major weight into a shared-memory ring with
+ * cp.async and reads them back transposed (ldmatrix .trans .b8) in the tiled storage's word order, so the row-major
+ * weight streams through the same kernels as the tiled one.  The others are earlier designs kept for comparison. */
 typedef enum {
     Q8_VARIANT_AUTO = 0,
     Q8_VARIANT_SIMT = 1, /* CUDA-core fp32 FMA, m-row accumulators per thread, weights loaded straight to registers */
@@ -248,8 +251,8 @@ typedef struct q8_part {
  * other).
  *   x      device bf16 [m][K], read once for all parts       parts  host array of nparts q8_part (read during the call)
  *   1 <= nparts <= Q8_MAX_PARTS; every part has the same K; N may differ.  Each y_p is as q8_gemv writes it.
- * With Q8_FLAG_TILED (weights in the q8_tile layout) the parts run as one kernel launch; row-major parts run one
- * launch each.  Flags and errors as q8_gemv_ex; an output overlapping x, a weight or another output is Q8_ERR_ARG. */
+ * The parts run as one kernel launch, row-major or (Q8_FLAG_TILED) in the q8_tile layout.  Flags and errors as
+ * q8_gemv_ex; an output overlapping x, a weight or another output is Q8_ERR_ARG. */
 q8_status q8_gemv_parts(const void *x, const q8_part *parts, int nparts, int m, int K, unsigned int flags,
                         q8_stream_t stream);
 

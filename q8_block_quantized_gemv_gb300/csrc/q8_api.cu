@@ -195,8 +195,10 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
     int e = sm_count(&sms);
     if (e != 0) return cuda_fail((cudaError_t)e);
     const bool tiled = (flags & Q8_FLAG_TILED) != 0;
+    // the streaming kernels: tiled weights, and row-major ones when the caller leaves the kernel family to the library
+    const bool streaming = tiled || variant == Q8_VARIANT_AUTO;
     q8::Parts one = {};
-    if (tiled && !parts) {
+    if (streaming && !parts) {
         one.q[0] = a.q;
         one.s[0] = a.s;
         one.y[0] = a.y;
@@ -205,7 +207,7 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
         one.count = 1;
         parts = &one;
     }
-    const Plan p = make_plan(a.m, a.K, a.Np, variant, tiled, sms, parts ? parts->tile_end[parts->count - 1] : 0);
+    const Plan p = make_plan(a.m, a.K, a.Np, variant, streaming, sms, parts ? parts->tile_end[parts->count - 1] : 0);
     Args b = a;
     b.ksplit = p.ksplit;
     const bool prefetch = (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0;
@@ -215,7 +217,8 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
         if (ce != cudaSuccess) return cuda_fail(ce);
         return Q8_OK;
     }
-    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, epi, stream, true, prefetch, qact)
+    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, epi, stream, true, prefetch, qact,
+                                                                        !tiled)
                      : p.variant == Q8_VARIANT_TMA  ? q8::launch_tma(b, argmax, stream, true, prefetch)
                      : p.variant == Q8_VARIANT_SIMT ? q8::launch_simt(b, p.V, argmax, stream)
                                                     : q8::launch_mma(b, p.V, argmax, stream);
@@ -325,14 +328,6 @@ extern "C" q8_status q8_gemv_parts(const void *x, const q8_part *parts, int npar
         }
     }
     cudaStream_t cs = (cudaStream_t)stream;
-    if (!tiled) {  // the row-major kernels take one weight a launch
-        for (int i = 0; i < nparts; ++i) {
-            q8_status st = q8_gemv_ex(x, parts[i].q, parts[i].s, parts[i].y, m, K, parts[i].N, Q8_VARIANT_AUTO,
-                                      flags, stream);
-            if (st != Q8_OK) return st;
-        }
-        return Q8_OK;
-    }
     q8::Parts pt = {};
     int tiles = 0;
     for (int i = 0; i < nparts; ++i) {

@@ -54,8 +54,10 @@ int stream_ctas_per_sm(int m);
 int stream_max_clusters(int ks);  // clusters of ks stream-kernel CTAs resident at once on this device (0: unknown)
 // epi: kEpiStore, kEpiArgmax, kEpiGlu (parts 0 and 1 the gate and up weights, grid x = 2 * tiles) or kEpiNorm.
 // qact: a.x is a quantized activation (int8 values [m][K], then fp32 scales [m][K/32]) instead of bf16 values.
+// rowmajor: the parts' weights are row-major ([K][Np] int8, [K/32][Np] fp32), not tiled (kEpiStore and kEpiArgmax,
+// bf16 activations, m <= 16).
 cudaError_t launch_stream(const Args &a, const Parts &parts, int epi, cudaStream_t stream, bool pdl,
-                          bool prefetch_weights, bool qact);
+                          bool prefetch_weights, bool qact, bool rowmajor = false);
 cudaError_t read_fault_word(unsigned *out, bool clear);
 
 // Defined in q8_gemm.cu: the tcgen05 GEMM for prefill chunks (tiled storage, bf16 activations, plain store).

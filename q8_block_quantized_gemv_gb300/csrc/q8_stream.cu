@@ -201,6 +201,49 @@ __device__ __forceinline__ void issue_unit(unsigned char *stage, const int8_t *q
     cp_async16(stage + kUnit + lane * 16, reinterpret_cast<const unsigned char *>(s + u * kUnitScales) + lane * 16);
 }
 
+// Row-major storage (what q8_gemv takes): block b of column tile t is rows 32b .. 32b + 31 of q [K][Np], bytes
+// 128t .. 128t + 127 of each.  It lands in a stage as [32 rows][128 bytes], the 16-byte chunk c of row r at chunk
+// c ^ (r & 7), so that the transposing loads below read eight rows without bank conflicts; the 128 scales of row b
+// follow as in the tiled unit.  Chunks at or past Np (a ragged last tile) are zero-filled, not read.
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, unsigned bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void issue_block_rm(unsigned char *stage, const int8_t *q, const float *s, int Np, int tile,
+                                               int b, int lane) {
+    const int c = lane & 7;
+    const int col = kTmaColumns * tile + 16 * c;  // Np is a multiple of 32: a chunk is wholly inside or past it
+    const bool ok = col < Np;
+#pragma unroll
+    for (int seg = 0; seg < 8; ++seg) {
+        const int r = 4 * seg + (lane >> 3);
+        const unsigned char *src = reinterpret_cast<const unsigned char *>(q) + (size_t)(kBlock * b + r) * Np;
+        cp_async16_zfill(stage + r * 128 + ((c ^ (r & 7)) << 4), src + (ok ? col : 0), ok ? 16u : 0u);
+    }
+    const int sc = kTmaColumns * tile + 4 * lane;
+    const bool sok = sc < Np;
+    cp_async16_zfill(stage + kUnit + lane * 16, s + (size_t)b * Np + (sok ? sc : 0), sok ? 16u : 0u);
+}
+
+// The four words of the tiled unit's segment (s, h) for this lane, from a row-major stage: one transposing matrix
+// load of the 16 rows 16s .. 16s + 15 and the two 16-column groups 2h, 2h + 1 gives lane (g, t) weight rows
+// 16s + 4t .. + 3 of columns 32h + g, + 8, + 16 and + 24 -- the tiled word order -- and the bytes are moved from int8
+// to the stored form q + 128.
+__device__ __forceinline__ uint4 rm_words(const unsigned char *st, int s, int h, int lane) {
+    const int row = 16 * s + (lane & 15);
+    const int c = 2 * h + (lane >> 4);
+    uint4 w;
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                 : "r"(smem_addr(st + row * 128 + ((c ^ (row & 7)) << 4)))
+                 : "memory");
+    w.x ^= 0x80808080u;
+    w.y ^= 0x80808080u;
+    w.z ^= 0x80808080u;
+    w.w ^= 0x80808080u;
+    return w;
+}
+
 // How a block's activations enter the MMA: fp16 as they are (plain), scaled fp16, or raw bf16.  scale[i] = 2^p and
 // sf[i] = 2^-p (in both halves of an fp32 pair) for the lane's activation row g + 8i.
 struct XPlan {
@@ -278,16 +321,20 @@ template <int NR, bool PER_ROW> __device__ __forceinline__ XPlan plan_block(cons
 // costs a mask, a packed 16-bit add of -0x3880 (in range exactly when the sum is below 0x0F00; smaller magnitudes and
 // zeros wrap above it) and a packed max; one vote decides for the warp.  Blocks with zeros or other ranges take the
 // full plan.
-__device__ __forceinline__ bool block_f16_normal(const uint2 (&x)[2][2], bool live1) {
-    uint32_t m0 = 0u, m1 = 0u;
+template <int NR>
+__device__ __forceinline__ bool block_f16_normal(const uint2 (&x)[NR][2], bool live0, bool live1) {
+    uint32_t m[NR];
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-        m0 = vmax_u16x2(m0, vmax_u16x2(vadd_u16x2(x[0][s].x & 0x7FFF7FFFu, 0xC780C780u),
-                                       vadd_u16x2(x[0][s].y & 0x7FFF7FFFu, 0xC780C780u)));
-        m1 = vmax_u16x2(m1, vmax_u16x2(vadd_u16x2(x[1][s].x & 0x7FFF7FFFu, 0xC780C780u),
-                                       vadd_u16x2(x[1][s].y & 0x7FFF7FFFu, 0xC780C780u)));
+    for (int r = 0; r < NR; ++r) {
+        m[r] = 0u;
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+            m[r] = vmax_u16x2(m[r], vmax_u16x2(vadd_u16x2(x[r][s].x & 0x7FFF7FFFu, 0xC780C780u),
+                                               vadd_u16x2(x[r][s].y & 0x7FFF7FFFu, 0xC780C780u)));
     }
-    const uint32_t mx = live1 ? vmax_u16x2(m0, m1) : m0;
+    // a dead row (at or past m) holds zeros, which would fail the range: it does not count
+    uint32_t mx = live0 ? m[0] : 0u;
+    if (NR == 2 && live1) mx = vmax_u16x2(mx, m[NR - 1]);
     return __all_sync(0xffffffffu, (mx & 0xFFFFu) < 0x0F00u && (mx >> 16) < 0x0F00u);
 }
 
@@ -295,7 +342,7 @@ __device__ __forceinline__ bool block_f16_normal(const uint2 (&x)[2][2], bool li
 // the A fragments of the two halves (fp16, or raw bf16), `pl` the factors of the block's scales (2^-p per activation
 // row; unused for bf16 and for PLAIN fp16, which is unscaled), ROWS16 whether activation rows 8..15 exist and SAME
 // whether both rows share 2^-p.
-template <bool F16, bool ROWS16, bool SAME, bool PLAIN = false>
+template <bool F16, bool ROWS16, bool SAME, bool PLAIN = false, bool RM = false>
 __device__ __forceinline__ void block_contract(const unsigned char *st, int lane, const uint32_t (&a)[2][4],
                                                const XPlan &pl,
                                                unsigned long long (&acc)[ROWS16 ? 2 : 1][kSlices]) {
@@ -303,8 +350,9 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
     const unsigned long long *sp = reinterpret_cast<const unsigned long long *>(st + kUnit) + t;
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-        const uint4 w0 = *reinterpret_cast<const uint4 *>(st + h * 512 + lane * 16);
-        const uint4 w1 = *reinterpret_cast<const uint4 *>(st + (4 + h) * 512 + lane * 16);
+        const uint4 w0 = RM ? rm_words(st, 0, h, lane) : *reinterpret_cast<const uint4 *>(st + h * 512 + lane * 16);
+        const uint4 w1 = RM ? rm_words(st, 1, h, lane)
+                            : *reinterpret_cast<const uint4 *>(st + (4 + h) * 512 + lane * 16);
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const int j = 4 * h + w;
@@ -332,7 +380,8 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
 // int8 codes as exact fp16, its integer sums are exact in the fp32 accumulators (|sum| <= 32 * 127 * 127 < 2^24),
 // and its factor per activation row is that row's scale d.
 // GROUPS: m > 16, the rows in groups of 16 (grid x = tiles * groups, ROWS16 only).
-template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false>
+// RM: the weight is row-major (q8_gemv's layout), not tiled.
+template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false, bool RM = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
     stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     static_assert(ROWS16 || !GROUPS, "row groups are groups of 16 rows");
@@ -355,6 +404,12 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     const int n = b1 - b0;
     unsigned char *ring = smem_s + warp * kDepthS * kStageS;
     const size_t unit0 = (size_t)tile * a.nb + b0;
+    auto issue = [&](unsigned char *stage, int i) {  // block b0 + i of the tile into `stage`
+        if constexpr (RM)
+            issue_block_rm(stage, a.q, a.s, a.Np, tile, b0 + i, lane);
+        else
+            issue_unit(stage, a.q, a.s, unit0 + i, lane);
+    };
 
     // acc[i][j]: rows g + 8i, columns 8j + 2t and 8j + 2t + 1 of the tile
     unsigned long long acc[NR][kSlices];
@@ -367,7 +422,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     if (prefetch_weights) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
-            if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
+            if (i < n) issue(ring + i * kStageS, i);
             cp_async_commit();
         }
     }
@@ -375,7 +430,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     if (!prefetch_weights) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
-            if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
+            if (i < n) issue(ring + i * kStageS, i);
             cp_async_commit();
         }
     }
@@ -419,7 +474,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     for (int i = 0; i < n; ++i) {
         const int ahead = i + kDepthS - 1;
         if (ahead < n)
-            issue_unit(ring + (ROWS16 ? nxt : ahead % kDepthS) * kStageS, a.q, a.s, unit0 + ahead, lane);
+            issue(ring + (ROWS16 ? nxt : ahead % kDepthS) * kStageS, ahead);
         cp_async_commit();
         uint2 xc[NR][2];
 #pragma unroll
@@ -436,7 +491,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             plan.sf[0] = pack_f32x2(__uint_as_float(xc[0][1].x), __uint_as_float(xc[0][1].x));
             plan.sf[1] = pack_f32x2(__uint_as_float(xc[NR - 1][1].x), __uint_as_float(xc[NR - 1][1].x));
         } else if constexpr (ROWS16) {
-            f16_normal = block_f16_normal(xc, xlive[NR - 1]);
+            f16_normal = block_f16_normal<NR>(xc, xlive[0], xlive[NR - 1]);
             if (!f16_normal) plan = plan_block<NR, false>(xc);
         } else {
             plan = plan_block<NR, true>(xc);
@@ -461,17 +516,17 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 af[s][1] = ROWS16 ? q8x2_to_f16x2<0>(u1) : 0u;
                 af[s][3] = ROWS16 ? q8x2_to_f16x2<2>(u1) : 0u;
             }
-            block_contract<true, ROWS16, false>(st, lane, af, plan, acc);
+            block_contract<true, ROWS16, false, false, RM>(st, lane, af, plan, acc);
         } else if (ROWS16 && (f16_normal || plan.plain)) {
             uint32_t af[2][4];
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
                 af[s][0] = bf16x2_to_f16x2_plain(xc[0][s].x);
                 af[s][2] = bf16x2_to_f16x2_plain(xc[0][s].y);
-                af[s][1] = bf16x2_to_f16x2_plain(xc[NR - 1][s].x);
-                af[s][3] = bf16x2_to_f16x2_plain(xc[NR - 1][s].y);
+                af[s][1] = ROWS16 ? bf16x2_to_f16x2_plain(xc[NR - 1][s].x) : 0u;
+                af[s][3] = ROWS16 ? bf16x2_to_f16x2_plain(xc[NR - 1][s].y) : 0u;
             }
-            block_contract<true, ROWS16, ROWS16, true>(st, lane, af, plan, acc);
+            block_contract<true, ROWS16, ROWS16, true, RM>(st, lane, af, plan, acc);
         } else if (plan.f16) {
             uint32_t af[2][4];
 #pragma unroll
@@ -481,7 +536,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 af[s][1] = ROWS16 ? bf16x2_to_f16x2(xc[NR - 1][s].x, plan.scale[1]) : 0u;
                 af[s][3] = ROWS16 ? bf16x2_to_f16x2(xc[NR - 1][s].y, plan.scale[1]) : 0u;
             }
-            block_contract<true, ROWS16, ROWS16>(st, lane, af, plan, acc);
+            block_contract<true, ROWS16, ROWS16, false, RM>(st, lane, af, plan, acc);
         } else {
             uint32_t ab[2][4];
 #pragma unroll
@@ -491,7 +546,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 ab[s][1] = ROWS16 ? xc[NR - 1][s].x : 0u;
                 ab[s][3] = ROWS16 ? xc[NR - 1][s].y : 0u;
             }
-            block_contract<false, ROWS16, ROWS16>(st, lane, ab, plan, acc);
+            block_contract<false, ROWS16, ROWS16, false, RM>(st, lane, ab, plan, acc);
         }
         __syncwarp();  // every lane is done with this stage before it is refilled
     }
@@ -546,7 +601,7 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // QACT (quantized activations, m <= 2): the lane's eight codes of a row and block meet each column's eight stored
 // bytes in two dp4a (integer products, exact); the offset is removed by starting the sum at -128 times the sum of the
 // eight codes, the exact integer is converted to fp32 and folded with s[b, n] * d[r, b].
-template <int M, int EPI, bool QACT = false>
+template <int M, int EPI, bool QACT = false, bool RM = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
     stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     extern __shared__ __align__(16) unsigned char smem_s[];
@@ -562,6 +617,12 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     const int n = b1 - b0;
     unsigned char *ring = smem_s + warp * kDepthS * kStageS;
     const size_t unit0 = (size_t)tile * a.nb + b0;
+    auto issue = [&](unsigned char *stage, int i) {  // block b0 + i of the tile into `stage`
+        if constexpr (RM)
+            issue_block_rm(stage, a.q, a.s, a.Np, tile, b0 + i, lane);
+        else
+            issue_unit(stage, a.q, a.s, unit0 + i, lane);
+    };
 
     unsigned long long acc[M][kSlices];  // per row and column 8j + g: the carry of rows 4t, 4t+2 | 4t+1, 4t+3
     float accq[M][kSlices];              // QACT: per row and column 8j + g, the carry of the lane's rows
@@ -576,7 +637,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     if (prefetch_weights) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
-            if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
+            if (i < n) issue(ring + i * kStageS, i);
             cp_async_commit();
         }
     }
@@ -584,7 +645,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     if (!prefetch_weights) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
-            if (i < n) issue_unit(ring + i * kStageS, a.q, a.s, unit0 + i, lane);
+            if (i < n) issue(ring + i * kStageS, i);
             cp_async_commit();
         }
     }
@@ -612,7 +673,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
 
     for (int i = 0; i < n; ++i) {
         const int ahead = i + kDepthS - 1;
-        if (ahead < n) issue_unit(ring + (ahead % kDepthS) * kStageS, a.q, a.s, unit0 + ahead, lane);
+        if (ahead < n) issue(ring + (ahead % kDepthS) * kStageS, ahead);
         cp_async_commit();
         uint2 xc[M][2];
 #pragma unroll
@@ -634,8 +695,10 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             const float *ss = reinterpret_cast<const float *>(st + kUnit) + g;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                const uint4 w0 = *reinterpret_cast<const uint4 *>(st + h * 512 + lane * 16);
-                const uint4 w1 = *reinterpret_cast<const uint4 *>(st + (4 + h) * 512 + lane * 16);
+                const uint4 w0 = RM ? rm_words(st, 0, h, lane)
+                                    : *reinterpret_cast<const uint4 *>(st + h * 512 + lane * 16);
+                const uint4 w1 = RM ? rm_words(st, 1, h, lane)
+                                    : *reinterpret_cast<const uint4 *>(st + (4 + h) * 512 + lane * 16);
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     const int j = 4 * h + w;
@@ -662,34 +725,32 @@ __global__ void __launch_bounds__(kThreadsS, 2)
         cp_async_wait<kDepthS - 1>();
         __syncwarp();
         const unsigned char *st = ring + (i % kDepthS) * kStageS;
-        unsigned long long part[M][kSlices];
+        const float *ss = reinterpret_cast<const float *>(st + kUnit) + g;
+        // per group h of four slices: both 16-row halves, then the fold, so that only four slices' block sums are
+        // live at a time (each slice's operations run in the same order as half by half over all slices)
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
+        for (int h = 0; h < 4; ++h) {
+            const uint4 w0 = RM ? rm_words(st, 0, h, lane)
+                                : *reinterpret_cast<const uint4 *>(st + h * 512 + lane * 16);
+            const uint4 w1 = RM ? rm_words(st, 1, h, lane)
+                                : *reinterpret_cast<const uint4 *>(st + (4 + h) * 512 + lane * 16);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const uint4 wv = *reinterpret_cast<const uint4 *>(st + (4 * s + h) * 512 + lane * 16);
+            for (int w = 0; w < 4; ++w) {
+                const int j = 4 * h + w;
+                const uint32_t u0 = word_of(w0, w), u1 = word_of(w1, w);
+                const unsigned long long q01a = q8x2_to_f32x2<0>(u0), q23a = q8x2_to_f32x2<2>(u0);
+                const unsigned long long q01b = q8x2_to_f32x2<0>(u1), q23b = q8x2_to_f32x2<2>(u1);
+                const float sv = ss[8 * j];
+                const unsigned long long s2 = pack_f32x2(sv, sv);
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int j = 4 * h + w;
-                    const uint32_t u = word_of(wv, w);
-                    const unsigned long long q01 = q8x2_to_f32x2<0>(u), q23 = q8x2_to_f32x2<2>(u);
-#pragma unroll
-                    for (int r = 0; r < M; ++r) {
-                        if (s == 0)
-                            part[r][j] = mul_f32x2(q01, xp[r][0][0]);
-                        else
-                            part[r][j] = fma_f32x2(q01, xp[r][1][0], part[r][j]);
-                        part[r][j] = fma_f32x2(q23, xp[r][s][1], part[r][j]);
-                    }
+                for (int r = 0; r < M; ++r) {
+                    unsigned long long part = mul_f32x2(q01a, xp[r][0][0]);
+                    part = fma_f32x2(q23a, xp[r][0][1], part);
+                    part = fma_f32x2(q01b, xp[r][1][0], part);
+                    part = fma_f32x2(q23b, xp[r][1][1], part);
+                    acc[r][j] = fma_f32x2(s2, part, acc[r][j]);
                 }
             }
-        const float *ss = reinterpret_cast<const float *>(st + kUnit) + g;
-#pragma unroll
-        for (int j = 0; j < kSlices; ++j) {
-            const float sv = ss[8 * j];
-            const unsigned long long s2 = pack_f32x2(sv, sv);
-#pragma unroll
-            for (int r = 0; r < M; ++r) acc[r][j] = fma_f32x2(s2, part[r][j], acc[r][j]);
         }
         __syncwarp();
     }
@@ -807,9 +868,21 @@ int stream_max_clusters(int ks) {
 }
 
 template <int EPI>
-cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, bool p, bool qact) {
+cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, bool p, bool qact,
+                              bool rowmajor) {
     const bool pair = EPI == kEpiGlu;
     auto go = [&](auto kernel) { return launch_stream_kernel(kernel, a, pt, stream, pdl, p, pair); };
+    if constexpr (EPI == kEpiStore || EPI == kEpiArgmax) {
+        if (rowmajor) {  // at most 16 rows, bf16 activations
+            if (qact || a.m > kGroupRows) return cudaErrorInvalidValue;
+            if (a.m == 1) return go(stream_simt_kernel<1, EPI, false, true>);
+            if (a.m == 2) return go(stream_simt_kernel<2, EPI, false, true>);
+            if (a.m <= 8) return go(stream_kernel<false, EPI, false, false, true>);
+            return go(stream_kernel<true, EPI, false, false, true>);
+        }
+    } else if (rowmajor) {
+        return cudaErrorInvalidValue;  // the fused epilogues take the tiled storage
+    }
     if (qact) {
         if (a.m == 1) return go(stream_simt_kernel<1, EPI, true>);
         if (a.m == 2) return go(stream_simt_kernel<2, EPI, true>);
@@ -825,12 +898,12 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
 }
 
 cudaError_t launch_stream(const Args &a, const Parts &pt, int epi, cudaStream_t stream, bool pdl,
-                          bool prefetch_weights, bool qact) {
+                          bool prefetch_weights, bool qact, bool rowmajor) {
     switch (epi) {
-        case kEpiStore: return launch_stream_epi<kEpiStore>(a, pt, stream, pdl, prefetch_weights, qact);
-        case kEpiArgmax: return launch_stream_epi<kEpiArgmax>(a, pt, stream, pdl, prefetch_weights, qact);
-        case kEpiGlu: return launch_stream_epi<kEpiGlu>(a, pt, stream, pdl, prefetch_weights, qact);
-        case kEpiNorm: return launch_stream_epi<kEpiNorm>(a, pt, stream, pdl, prefetch_weights, qact);
+        case kEpiStore: return launch_stream_epi<kEpiStore>(a, pt, stream, pdl, prefetch_weights, qact, rowmajor);
+        case kEpiArgmax: return launch_stream_epi<kEpiArgmax>(a, pt, stream, pdl, prefetch_weights, qact, rowmajor);
+        case kEpiGlu: return launch_stream_epi<kEpiGlu>(a, pt, stream, pdl, prefetch_weights, qact, rowmajor);
+        case kEpiNorm: return launch_stream_epi<kEpiNorm>(a, pt, stream, pdl, prefetch_weights, qact, rowmajor);
         default: return cudaErrorInvalidValue;
     }
 }
