@@ -730,6 +730,61 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_sweep_launches(args):
+    """µs per call and GB/s of each launch kind of the decode chain (q/k/v and gate/up as multi-projection calls, o,
+    down, the head with its arg-max) at each m of --sweep-m, in the chain's configuration: tiled weights, the
+    constant-weights flag, calls back to back in a CUDA graph, each call on its own weight copy (copies totalling over
+    4 x L2).  One JSON line per (launch, m)."""
+    import torch
+    import synth_inputs as si
+    import q8_block_quantized_gemv_gb300 as q8
+    from q8_block_quantized_gemv_gb300 import build
+    build.build()
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    ms = [int(v) for v in args.sweep_m.split(",")]
+    for name, (K, Ns) in LAUNCHES.items():
+        wb = sum(K * padded(N) * 1.125 for N in Ns)
+        copies = max(2, int(4 * l2 // wb) + 1)
+        ws = _weights(K, Ns, copies, 11, "tiled")
+        for m in ms:
+            x = si.device_activations(m, K, 3)
+            ys = [torch.empty((m, padded(N)), dtype=torch.float32, device="cuda") for N in Ns]
+            idx = torch.empty((m,), dtype=torch.int64, device="cuda")
+            per = max(copies, 16)
+
+            def calls():
+                for i in range(per):
+                    w = ws[i % copies]
+                    if name == "head":
+                        q8.gemv_argmax(x, w[0][0], w[0][1], VOCAB, idx=idx, constant_weights=True, tiled=True)
+                    else:
+                        q8.gemv_parts(x, w, ys=ys, constant_weights=True, tiled=True)
+            calls()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                calls()
+            for _ in range(3):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (5 * per)
+            nbytes = sum(gemv_bytes(m, K, N, argmax=(name == "head")) for N in Ns) - (len(Ns) - 1) * m * K * 2
+            print(json.dumps({"sweep": "chain launch kind, tiled, back to back", "launch": name, "K": K, "N": Ns,
+                              "m": m, "us_per_call": us, "gbs": nbytes / (us * 1e-6) / 1e9,
+                              "frac_of_peak": nbytes / (us * 1e-6) / 1e9 / peak, "peak_kind": peak_kind,
+                              **({"tuning": args.tune} if args.tune else {})}), flush=True)
+            del g
+        del ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -751,6 +806,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step: µs/call of the single-GEMV workloads, one JSON line each")
     ap.add_argument("--sweep-m", default="1,2,4,8,16", help="row counts of --sweep")
+    ap.add_argument("--sweep-launches", action="store_true",
+                    help="instead of the step: µs/call of each launch kind of the chain (q/k/v, o, gate/up, down, "
+                         "head), one JSON line each")
     ap.add_argument("--sweep-shapes", default="",
                     help="shapes of --sweep as KxN,KxN,... (default: the attention, FFN and ragged workloads)")
     ap.add_argument("--layout", choices=["tiled", "rowmajor"], default="tiled",
@@ -796,6 +854,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.sweep_launches:
+        run_sweep_launches(args)
         return
     if world > 1:
         import torch
