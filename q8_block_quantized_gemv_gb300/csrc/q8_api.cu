@@ -83,8 +83,8 @@ struct Plan {
 };
 
 // Kernel family, per-lane width and K split for a shape.  The widest tile that still gives every SM a CTA is
-// preferred; K is split across a cluster (at most 8 CTAs, the portable size) until the grid holds about two CTAs per
-// SM, the residency the kernels are built for.
+// preferred; K is split across a cluster (at most 8 CTAs, the portable size) until the grid holds about as many CTAs
+// as are resident at once (two per SM; one for the 8-row stream kernel).
 Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long tiled_tiles = 0) {
     const int nb = K / Q8_BLOCK;
     if (tiled) {
@@ -101,7 +101,7 @@ Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long
         if (ks > nb) ks = nb;
         if (ks < 1) ks = 1;
         while (ks > 1) {
-            const int fit = q8::stream_max_clusters((int)ks);
+            const int fit = q8::stream_max_clusters(m, (int)ks);
             if (fit <= 0 || tiles <= fit) break;
             --ks;
         }
@@ -346,14 +346,14 @@ extern "C" q8_status q8_gemv_parts(const void *x, const q8_part *parts, int npar
 
 // The K split of a gated-pair launch: its clusters are (2, ks), a gate's and an up projection's CTA for each K range
 // of one column tile, so the one-wave rule counts 2 * tiles * ks CTAs and clusters of 2 * ks (at most 8).
-int plan_glu(long long tiles, int nb, int sms) {
-    const long long slots = (long long)q8::stream_ctas_per_sm(1) * sms;
+int plan_glu(long long tiles, int nb, int sms, int m) {
+    const long long slots = (long long)q8::stream_ctas_per_sm(m) * sms;
     long long ks = slots / (2 * tiles);
     if (ks > 4) ks = 4;
     if (ks > nb) ks = nb;
     if (ks < 1) ks = 1;
     while (ks > 1) {
-        const int fit = q8::stream_max_clusters((int)(2 * ks));
+        const int fit = q8::stream_max_clusters(m, (int)(2 * ks));
         if (fit <= 0 || tiles <= fit) break;
         --ks;
     }
@@ -409,7 +409,7 @@ extern "C" q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float
         a.yq = static_cast<unsigned char *>(out_q8);
         a.yd = reinterpret_cast<float *>(a.yq + (size_t)m * Np);
     }
-    a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms);
+    a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms, m);
     cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true,
                                        (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0, (flags & Q8_FLAG_Q8_ACT) != 0);
     if (ce != cudaSuccess) return cuda_fail(ce);

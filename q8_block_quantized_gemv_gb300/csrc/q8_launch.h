@@ -50,8 +50,8 @@ bool encode_bf16_rows(CUtensorMap *map, const void *base, int rows, int K, int b
 cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl, bool prefetch_weights);
 
 // Defined in q8_stream.cu (the tiled layout).
-int stream_ctas_per_sm(int m);
-int stream_max_clusters(int ks);  // clusters of ks stream-kernel CTAs resident at once on this device (0: unknown)
+int stream_ctas_per_sm(int m);          // resident CTAs per SM of the stream kernel that takes m rows
+int stream_max_clusters(int m, int ks);  // clusters of ks such CTAs resident at once on this device (0: unknown)
 // epi: kEpiStore, kEpiArgmax, kEpiGlu (parts 0 and 1 the gate and up weights, grid x = 2 * tiles) or kEpiNorm.
 // qact: a.x is a quantized activation (int8 values [m][K], then fp32 scales [m][K/32]) instead of bf16 values.
 // rowmajor: the parts' weights are row-major ([K][Np] int8, [K/32][Np] fp32), not tiled (kEpiStore and kEpiArgmax,

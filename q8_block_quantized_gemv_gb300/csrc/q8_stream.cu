@@ -9,9 +9,13 @@
 // owns a run of K blocks of one tile reads one contiguous range of memory.
 //
 // A CTA owns one 128-column tile and a range of its K blocks (split across a thread-block cluster when N is too
-// narrow to fill the SMs); its eight warps split that range again into contiguous runs.  Each warp keeps a private
-// ring of three stages in shared memory, filled with cp.async (16 bytes a lane, bypassing L1): it issues block i + 2
-// while it computes block i, so about two units per warp -- 150 KB per SM -- are in flight without holding registers.
+// narrow to fill the SMs); its warps split that range again into contiguous runs.  Each warp keeps a private ring of
+// three stages in shared memory, filled with cp.async (16 bytes a lane, bypassing L1): it issues block i + 2 while it
+// computes block i, so about two units per warp -- 110 to 150 KB per SM -- are in flight without holding registers.
+// The 16-row and CUDA-core kernels run 8 warps a CTA, two CTAs per SM (128 registers a thread); the 8-row kernel
+// runs 12 warps, one CTA per SM, so that a thread may hold up to 168 registers (measured on GB300, 10-28 % faster per
+// launch at 4 and 8 rows than 8 warps at the 128-register cap; the 16-row kernel gains less there and loses on wide
+// launches, whose one-CTA-per-SM waves are twice as many).
 //
 // The block's contraction runs on m16n8k16 MMAs with the activations as the A operand (rows r and r + 8 of the lane's
 // fragment are activation rows g and g + 8) and the weights as B (one 8-column slice per MMA, fp32 accumulators):
@@ -43,13 +47,16 @@ namespace q8 {
 
 namespace {
 
-constexpr int kWarpsS = 8;
+constexpr int kWarpsS = 8;   // warps of a CTA: 16-row and CUDA-core kernels (two CTAs per SM)
+constexpr int kWarps8 = 12;  //   the 8-row kernel (one CTA per SM)
 constexpr int kThreadsS = 32 * kWarpsS;
+__host__ __device__ constexpr int stream_warps(bool rows16) { return rows16 ? kWarpsS : kWarps8; }
 constexpr int kUnit = kBlock * kTmaColumns;  // 4096 bytes of values per 32 x 128 unit
 constexpr int kUnitScales = kTmaColumns;     // 128 fp32
 constexpr int kStageS = kUnit + kUnitScales * 4;
-constexpr int kDepthS = 3;                   // ring stages per warp (two CTAs per SM)
+constexpr int kDepthS = 3;                   // ring stages per warp
 constexpr int kSmemS = kWarpsS * kDepthS * kStageS;
+__host__ __device__ constexpr int stream_smem(int warps) { return warps * kDepthS * kStageS; }
 constexpr int kSlices = kTmaColumns / 8;     // 8-column MMA slices of a tile
 constexpr int kSlabStride = kTmaColumns + 8; // epilogue slab row stride (floats)
 
@@ -382,9 +389,10 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
 // GROUPS: m > 16, the rows in groups of 16 (grid x = tiles * groups, ROWS16 only).
 // RM: the weight is row-major (q8_gemv's layout), not tiled.
 template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false, bool RM = false>
-__global__ void __launch_bounds__(kThreadsS, 2)
+__global__ void __launch_bounds__(32 * stream_warps(ROWS16), ROWS16 ? 2 : 1)
     stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
     static_assert(ROWS16 || !GROUPS, "row groups are groups of 16 rows");
+    constexpr int W = stream_warps(ROWS16);
     constexpr int MR = ROWS16 ? 16 : 8;
     constexpr int NR = ROWS16 ? 2 : 1;  // activation rows per lane: g and g + 8
     extern __shared__ __align__(16) unsigned char smem_s[];
@@ -399,8 +407,8 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     const int rank = blockIdx.y;
     const int c0 = (int)((long long)a.nb * rank / a.ksplit);
     const int c1 = (int)((long long)a.nb * (rank + 1) / a.ksplit);
-    const int b0 = c0 + (c1 - c0) * warp / kWarpsS;
-    const int b1 = c0 + (c1 - c0) * (warp + 1) / kWarpsS;
+    const int b0 = c0 + (c1 - c0) * warp / W;
+    const int b1 = c0 + (c1 - c0) * (warp + 1) / W;
     const int n = b1 - b0;
     unsigned char *ring = smem_s + warp * kDepthS * kStageS;
     const size_t unit0 = (size_t)tile * a.nb + b0;
@@ -554,7 +562,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();  // every warp is done with its ring: the shared memory holds the epilogue now
 
-    // [kWarpsS][MR][kSlabStride]: rows padded by 8 floats, so that a half-warp's 8-byte stores (rows g, columns
+    // [W][MR][kSlabStride]: rows padded by 8 floats, so that a half-warp's 8-byte stores (rows g, columns
     // 8j + 2t) fall on 32 distinct banks
     float *red = reinterpret_cast<float *>(smem_s);
     float *mine = red + warp * MR * kSlabStride;
@@ -569,11 +577,11 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     __syncthreads();
     apply_cta_group<EPI, GROUPS>(a);
     if constexpr (EPI == kEpiGlu)
-        finish_glu<kWarpsS, MR, kTmaColumns, kThreadsS, kSlabStride>(a, red, tile);
+        finish_glu<W, MR, kTmaColumns, 32 * W, kSlabStride>(a, red, tile);
     else if constexpr (EPI == kEpiNorm)
-        finish_norm<kWarpsS, MR, kTmaColumns, kThreadsS, kSlabStride>(a, red, tile);
+        finish_norm<W, MR, kTmaColumns, 32 * W, kSlabStride>(a, red, tile);
     else
-        finish_n<kWarpsS, MR, kTmaColumns, kThreadsS, EPI == kEpiArgmax, kSlabStride>(a, red, tile);
+        finish_n<W, MR, kTmaColumns, 32 * W, EPI == kEpiArgmax, kSlabStride>(a, red, tile);
 }
 
 // m <= 2 on CUDA cores: in segment (s, h) lane (g, t) holds words w = 0..3, each four weight rows 16s + 4t + 0..3 of
@@ -784,19 +792,23 @@ __global__ void __launch_bounds__(kThreadsS, 2)
 static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns, kSlabStride) <= kSmemS, "the epilogue fits in the rings");
 static_assert((kWarpsS * 16 * kSlabStride + 2 * 16 * kTmaColumns) * 4 <= kSmemS, "the gated pair's epilogue fits");
 static_assert(2 * kSmemS <= 227 * 1024, "two CTAs per SM");
+static_assert(finish_smem_n(kWarps8, 8, kTmaColumns, kSlabStride) <= stream_smem(kWarps8), "8-row epilogue fits");
+static_assert((kWarps8 * 8 * kSlabStride + 2 * 8 * kTmaColumns) * 4 <= stream_smem(kWarps8), "8-row gated pair fits");
+static_assert(stream_smem(kWarps8) <= 227 * 1024, "one 8-row CTA per SM");
 
 template <typename Kernel>
-cudaError_t launch_stream_kernel(Kernel kernel, const Args &a, const Parts &pt, cudaStream_t stream, bool pdl,
-                                 bool prefetch, bool pair) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
+cudaError_t launch_stream_kernel(Kernel kernel, int warps, const Args &a, const Parts &pt, cudaStream_t stream,
+                                 bool pdl, bool prefetch, bool pair) {
+    const int smem = stream_smem(warps);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     const unsigned groups = (unsigned)((a.m + kGroupRows - 1) / kGroupRows);
     cfg.gridDim = dim3((unsigned)pt.tile_end[pt.count - 1] * groups, (unsigned)a.ksplit, 1);
-    cfg.blockDim = dim3(kThreadsS, 1, 1);
-    cfg.dynamicSmemBytes = kSmemS;
+    cfg.blockDim = dim3(32 * (unsigned)warps, 1, 1);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
@@ -830,26 +842,31 @@ unsigned int *norm_counters() {
     return static_cast<unsigned int *>(base);
 }
 
-int stream_ctas_per_sm(int) { return 2; }
+// The 8-row kernel (3 .. 8 rows) runs one CTA per SM, the others two.
+bool rows8_family(int m) { return m >= 3 && m <= 8; }
+int stream_ctas_per_sm(int m) { return rows8_family(m) ? 1 : 2; }
 
-int stream_max_clusters(int ks) {
+int stream_max_clusters(int m, int ks) {
     // Clusters of ks CTAs are placed within one GPC, so fewer of them fit at once than slots / ks.  Asked once per
-    // device and size (a deterministic answer: concurrent first calls store the same value); every stream kernel has
-    // the same block size, registers and shared memory.
-    static std::atomic<int> cache[64][9];  // 0: not asked yet; else the count + 1
+    // device, kernel shape and size (a deterministic answer: concurrent first calls store the same value); the stream
+    // kernels of one shape (8-row: 12 warps, one CTA per SM; the others: 8 warps, two) have the same block size,
+    // register cap and shared memory.
+    static std::atomic<int> cache[64][2][9];  // 0: not asked yet; else the count + 1
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > 8) return 0;
-    const int known = cache[dev][ks].load(std::memory_order_relaxed);
+    const int fam = rows8_family(m) ? 1 : 0;
+    const int known = cache[dev][fam][ks].load(std::memory_order_relaxed);
     if (known > 0) return known - 1;
-    auto kernel = stream_kernel<true, false>;
+    auto kernel = fam ? stream_kernel<false, kEpiStore> : stream_kernel<true, kEpiStore>;
+    const int warps = stream_warps(fam == 0), smem = stream_smem(warps);
     int n = 0;
-    bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS) == cudaSuccess &&
+    bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
               cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
     if (ok) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, (unsigned)ks, 1);
-        cfg.blockDim = dim3(kThreadsS, 1, 1);
-        cfg.dynamicSmemBytes = kSmemS;
+        cfg.blockDim = dim3(32 * (unsigned)warps, 1, 1);
+        cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 1;
@@ -863,7 +880,7 @@ int stream_max_clusters(int ks) {
         cudaGetLastError();  // the failed query's error is not the caller's
         return 0;
     }
-    cache[dev][ks].store(n + 1, std::memory_order_relaxed);
+    cache[dev][fam][ks].store(n + 1, std::memory_order_relaxed);
     return n;
 }
 
@@ -871,13 +888,14 @@ template <int EPI>
 cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, bool p, bool qact,
                               bool rowmajor) {
     const bool pair = EPI == kEpiGlu;
-    auto go = [&](auto kernel) { return launch_stream_kernel(kernel, a, pt, stream, pdl, p, pair); };
+    auto go = [&](auto kernel) { return launch_stream_kernel(kernel, kWarpsS, a, pt, stream, pdl, p, pair); };
+    auto go8 = [&](auto kernel) { return launch_stream_kernel(kernel, kWarps8, a, pt, stream, pdl, p, pair); };
     if constexpr (EPI == kEpiStore || EPI == kEpiArgmax) {
         if (rowmajor) {  // at most 16 rows, bf16 activations
             if (qact || a.m > kGroupRows) return cudaErrorInvalidValue;
             if (a.m == 1) return go(stream_simt_kernel<1, EPI, false, true>);
             if (a.m == 2) return go(stream_simt_kernel<2, EPI, false, true>);
-            if (a.m <= 8) return go(stream_kernel<false, EPI, false, false, true>);
+            if (a.m <= 8) return go8(stream_kernel<false, EPI, false, false, true>);
             return go(stream_kernel<true, EPI, false, false, true>);
         }
     } else if (rowmajor) {
@@ -886,13 +904,13 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
     if (qact) {
         if (a.m == 1) return go(stream_simt_kernel<1, EPI, true>);
         if (a.m == 2) return go(stream_simt_kernel<2, EPI, true>);
-        if (a.m <= 8) return go(stream_kernel<false, EPI, true>);
+        if (a.m <= 8) return go8(stream_kernel<false, EPI, true>);
         if (a.m <= kGroupRows) return go(stream_kernel<true, EPI, true>);
         return go(stream_kernel<true, EPI, true, true>);
     }
     if (a.m == 1) return go(stream_simt_kernel<1, EPI>);
     if (a.m == 2) return go(stream_simt_kernel<2, EPI>);
-    if (a.m <= 8) return go(stream_kernel<false, EPI>);
+    if (a.m <= 8) return go8(stream_kernel<false, EPI>);
     if (a.m <= kGroupRows) return go(stream_kernel<true, EPI>);
     return go(stream_kernel<true, EPI, false, true>);
 }
