@@ -427,13 +427,27 @@ class Chain:
             self.run_head()
         torch.cuda.synchronize()
 
-    def launches_per_step(self):
-        # the layers' launches, the head's GEMV kernel and its index decode (and, --act q8, one quantize a launch);
-        # --fused: a residual norm's own norm launch after each of its two products a layer
+    def layer_launches(self):
+        """Kernel launches of the layers: each product call's (q8_plan_launches: 1, or 2 when the planner splits a
+        plain product in two); the gated pair one; under --fused, o and down as residual norms (the product, then
+        the norm's own launch unless the one-launch fold is selected)."""
         import q8_block_quantized_gemv_gb300 as q8
-        n = len(self.layer_calls()) + 2
-        if self.fused:
-            n += 2 * LAYERS * (q8.residual_norm_launches() - 1)
+        n = 0
+        for _, gis in self.layer_calls():
+            if self.glu and len(gis) == 2:
+                n += 1
+            elif self.fused and len(gis) == 1:
+                n += q8.residual_norm_launches()
+            else:
+                n += q8.plan_launches(self.m, self.shapes[gis[0]][0], [self.shapes[i][1] for i in gis],
+                                      q8_act=self.q8act)
+        return n
+
+    def launches_per_step(self):
+        """The layers' launches, the head's product launch(es) and its index decode, and (--act q8) the quantizer
+        launches."""
+        import q8_block_quantized_gemv_gb300 as q8
+        n = self.layer_launches() + q8.plan_launches(self.m, HIDDEN, (VOCAB,), q8_act=self.q8act) + 1
         return n + (len(self.quant_widths) + 1 if self.q8act else 0)
 
     def head_bytes(self):
@@ -463,13 +477,14 @@ class Chain:
 
 
 def traffic_record(m, default_step):
-    """ncu DRAM bytes per layer launch at m rows (profiles/traffic.json), while the kernel sources match the capture
-    and the step is the one captured (bf16 activations, two-output gate/up, no fused epilogues); else None."""
+    """ncu DRAM bytes per layer call at m rows (the sum over its launches; profiles/traffic.json), while the kernel
+    sources match the capture and the step is the one captured (bf16 activations, two-output gate/up, no fused
+    epilogues); else None."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             rec = json.load(f)
         if rec.get("source_hash") == source_hash() and default_step:
-            return rec.get("by_m", {}).get(str(m), {}).get("traffic_bytes_per_launch")
+            return rec.get("by_m", {}).get(str(m), {}).get("traffic_bytes_per_call")
     except (OSError, ValueError):
         pass
     return None
@@ -537,7 +552,7 @@ def measure_chain(args, torch, weights, m, world, local_rank, barrier, max_over_
     layer_bytes = chain.layer_bytes()
     achieved = layer_bytes / (layers_ms * 1e-3) / 1e9
     traffic = traffic_record(m, not (chain.q8act or chain.glu or chain.fused))
-    n_layer_launches = len(chain.layer_calls())
+    n_layer_calls = len(chain.layer_calls())
     res = {
         "m": m,
         "value": job_throughput(bytes_step, ms, world), "unit": "GB/s", "ms_per_step": ms,
@@ -545,12 +560,13 @@ def measure_chain(args, torch, weights, m, world, local_rank, barrier, max_over_
         "pct_of_8TBps": 100.0 * bytes_step / (ms * 1e-3) / 8e12,
         "bytes_per_step": bytes_step, "layers_ms": layers_ms, "head_ms": head_ms,
         "launches_per_step": chain.launches_per_step(),
-        "roofline": {"bound": "hbm", "kernel": "q8 stream kernel (the 128 layer launches of a step, back to back)"
-                     + (", with their activation quantizer launches" if chain.q8act else ""),
+        "roofline": {"bound": "hbm", "kernel": f"q8 stream kernels (the {n_layer_calls} layer calls of a step, "
+                     f"{chain.layer_launches()} launches, back to back"
+                     + (", with their activation quantizer launches" if chain.q8act else "") + ")",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": layer_bytes / n_layer_launches,
-                     "launch_us": layers_ms * 1e3 / n_layer_launches},
+                     "frac": achieved / peak, "traffic": traffic, "traffic_unit": "DRAM bytes per layer call",
+                     "algorithmic_bytes_per_call": layer_bytes / n_layer_calls,
+                     "call_us": layers_ms * 1e3 / n_layer_calls},
         "e2e": {"value": world * bytes_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": chain.x_all.numel() * 2, "d2h_bytes_per_step": m * 8},
         "gpu_launches": chain.launches_per_step() * args.steps,
@@ -815,7 +831,7 @@ def main():
                     help="weights of --sweep: the tiled storage (q8_tile_device, Q8_FLAG_TILED) or row-major as "
                          "q8_gemv takes them with no tiling step")
     ap.add_argument("--tune", default="",
-                    help="planner overrides as name=value,... (q8_set_tuning: ksplit, gemm, norm_fold)")
+                    help="planner overrides as name=value,... (q8_set_tuning: ksplit, gemm, norm_fold, split)")
     ap.add_argument("--profile-case", choices=sorted(LAUNCHES),
                     help="instead of the step: four calls of one launch kind of the step, for a profiler")
     args = ap.parse_args()

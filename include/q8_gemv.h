@@ -256,6 +256,16 @@ typedef struct q8_part {
 q8_status q8_gemv_parts(const void *x, const q8_part *parts, int nparts, int m, int K, unsigned int flags,
                         q8_stream_t stream);
 
+/* How many product kernels a q8_gemv_ex (Q8_VARIANT_AUTO), q8_gemv_argmax_ex or q8_gemv_parts call of these sizes
+ * launches on the calling thread's current device under the current tuning: 1, or 2 when the planner splits it
+ * (Q8_TUNE_SPLIT; plain products of at most 16 rows whose column tiles do not fill the SMs evenly).  The arg-max's
+ * memset and index decode are not counted.  No counterpart on the pages: for callers that account for the kernels of
+ * a captured graph, and for tests.
+ *   Ns  host array of the nparts output widths N (one for q8_gemv_ex and q8_gemv_argmax_ex); 1 <= nparts <= 8
+ * Returns the count, or a negative status: -Q8_ERR_ARG (null Ns, nparts out of range, unknown flags), -Q8_ERR_SHAPE
+ * (sizes the call would reject), -Q8_ERR_CUDA (the device cannot be queried). */
+int q8_plan_launches(int m, int K, const int *Ns, int nparts, unsigned int flags);
+
 /* The quantized form of an activation (source: "plan.rs", `QBLOCK`: 32 consecutive values of the form share one
  * scale; `Buffer::quantized`: int8 codes plus one scale for every 32; `Launch::projected_input`: a product over
  * checkpoint rows takes its activation in this form unless the numerics are the exact ones).  One buffer of
@@ -314,10 +324,14 @@ q8_status q8_device_fault(unsigned int *fault, int clear);
  *   Q8_TUNE_GEMM       -1: the planner's choice (default); 0: calls of 128 rows or more keep the row groups; 1: they
  *                      run on the tcgen05 GEMM whatever the weight's width.  Environment: Q8_GEMM (0 or 1).
  *   Q8_TUNE_NORM_FOLD  0: the residual norm as a launch of its own (default); 1: the one-launch fold, where the
- *                      product's last CTA runs the norm.  Environment: Q8_NORM_LAUNCH=0 selects 1. */
+ *                      product's last CTA runs the norm.  Environment: Q8_NORM_LAUNCH=0 selects 1.
+ *   Q8_TUNE_SPLIT      1: the planner may run a plain product (q8_gemv, q8_gemv_argmax, q8_gemv_parts; m <= 16) as
+ *                      two launches, the column tiles that do not fill the SMs evenly given their own K split
+ *                      (default); 0: always one launch.  Environment: Q8_SPLIT=0 selects 0. */
 #define Q8_TUNE_KSPLIT 0
 #define Q8_TUNE_GEMM 1
 #define Q8_TUNE_NORM_FOLD 2
+#define Q8_TUNE_SPLIT 3
 
 /* Sets an override.  Returns Q8_ERR_ARG for an unknown option or a value outside its range. */
 q8_status q8_set_tuning(int option, int value);

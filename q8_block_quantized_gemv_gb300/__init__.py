@@ -59,6 +59,7 @@ SIGNATURES = {
     "q8_quantize_act": (_I, [_P, _P, _I, _I, _P]),
     "q8_gemv_residual_norm_noalloc": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, ctypes.c_uint,
                                           _P]),
+    "q8_plan_launches": (_I, [_I, _I, _P, _I, ctypes.c_uint]),
     "q8_set_tuning": (_I, [_I, _I]),
     "q8_get_tuning": (_I, [_I]),
 }
@@ -303,6 +304,17 @@ def gemv_parts(x, weights, ys=None, constant_weights: bool = False, tiled: bool 
     return outs
 
 
+def plan_launches(m: int, K: int, Ns, tiled: bool = True, q8_act: bool = False) -> int:
+    """How many product kernels a gemv / gemv_argmax / gemv_parts call of these sizes launches on the current device
+    (q8_plan_launches): 1, or 2 when the planner splits it in two."""
+    arr = (ctypes.c_int * len(Ns))(*[int(n) for n in Ns])
+    flags = (FLAG_TILED if tiled else 0) | (FLAG_Q8_ACT if q8_act else 0)
+    n = int(lib().q8_plan_launches(int(m), int(K), ctypes.cast(arr, ctypes.c_void_p), len(Ns), flags))
+    if n < 0:
+        raise Q8Error(-n, "q8_plan_launches")
+    return n
+
+
 def _q8_out(out_q8, m, Np, device):
     import torch
     if out_q8 is None:
@@ -371,8 +383,9 @@ def gemv_residual_norm(x, q, s, N: int, residual, gamma, eps: float, h=None, out
 
 
 # Planner overrides (q8_set_tuning): the K split (0 = the planner's, 1..8 forced), the prefill GEMM (-1 = the
-# planner's, 0 = row groups, 1 = GEMM) and the residual norm's route (0 = own launch, 1 = the one-launch fold).
-TUNING = {"ksplit": 0, "gemm": 1, "norm_fold": 2}
+# planner's, 0 = row groups, 1 = GEMM), the residual norm's route (0 = own launch, 1 = the one-launch fold) and the
+# two-launch split of plain products (1 = where the planner finds one, 0 = never).
+TUNING = {"ksplit": 0, "gemm": 1, "norm_fold": 2, "split": 3}
 
 
 def set_tuning(option: str, value: int) -> None:

@@ -50,9 +50,10 @@ int sm_count(int *out) {
 }
 
 // The test and benchmark overrides of the planner (q8_set_tuning): a forced K split, the prefill GEMM forced on or
-// off, and the residual norm's route.  Each starts from its environment variable (Q8_KSPLIT, Q8_GEMM,
-// Q8_NORM_LAUNCH), read once per process at the first call that needs it; a call then reads one relaxed atomic.
-constexpr int kTuneOptions = 3;
+// off, the residual norm's route and the two-launch split.  Each starts from its environment variable (Q8_KSPLIT,
+// Q8_GEMM, Q8_NORM_LAUNCH, Q8_SPLIT), read once per process at the first call that needs it; a call then reads one
+// relaxed atomic.
+constexpr int kTuneOptions = 4;
 
 struct Tuning {
     std::atomic<int> value[kTuneOptions];
@@ -60,10 +61,12 @@ struct Tuning {
         const char *k = getenv("Q8_KSPLIT");
         const char *g = getenv("Q8_GEMM");
         const char *r = getenv("Q8_NORM_LAUNCH");
+        const char *sp = getenv("Q8_SPLIT");
         const int ks = k ? atoi(k) : 0;
         value[Q8_TUNE_KSPLIT].store(ks >= 1 && ks <= 8 ? ks : 0, std::memory_order_relaxed);
         value[Q8_TUNE_GEMM].store(g && g[0] == '0' ? 0 : g && g[0] == '1' ? 1 : -1, std::memory_order_relaxed);
         value[Q8_TUNE_NORM_FOLD].store(r && r[0] == '0' ? 1 : 0, std::memory_order_relaxed);
+        value[Q8_TUNE_SPLIT].store(sp && sp[0] == '0' ? 0 : 1, std::memory_order_relaxed);
     }
 };
 
@@ -188,6 +191,57 @@ bool use_gemm(int m, int epi, bool qact, long long col_tiles) {
     return col_tiles * ((m + 127) / 128) * 4 >= 64;
 }
 
+// A plain product (store or arg-max, at most 16 rows) whose one-launch plan has no K split but whose column tiles do
+// not fill the resident slots evenly runs as two launches on the stream (a balance of the "plan.rs" `split_counts`
+// kind: every SM gets about the same share of the blocks):
+//   - tiles > SMs but below the slots (two CTAs per SM): the first launch takes one tile per SM, its CTAs held to one
+//     per SM by their shared-memory size; the second takes the other tiles with K split over clusters of ks CTAs,
+//     sized to the free half of every SM.  The gate/up pair (224 tiles on 152 SMs) then gives every SM 128 + 64 K
+//     blocks instead of 256 on 72 SMs and 128 on the other 80;
+//   - tiles above the slots: the first launch takes the whole waves, the second the last partial wave's tiles with K
+//     split so that they fill one wave (the tied head's 1002 tiles: 3 waves of 304, then 90 tiles x 3).
+// The first launch releases the second right after its own dependency wait, so the second's CTAs take the slots the
+// first leaves free; the second waits for the first only before it exits, so whatever follows on the stream still
+// sees both complete.  A K split below 2 would gain nothing, so it plans no split.
+struct Split {
+    int tiles_a = 0;  // tiles of the first launch (0: one launch)
+    int ks_b = 1;     // the second launch's K split
+    bool one_per_sm = false;
+};
+Split plan_split(long long tiles, int nb, int m, int sms, int ks) {
+    Split none;
+    // (a forced K split keeps one launch, so that it applies to every tile)
+    if (tuning(Q8_TUNE_SPLIT) == 0 || tuning(Q8_TUNE_KSPLIT) != 0 || ks != 1 || m > q8::kGroupRows || sms <= 0)
+        return none;
+    const long long slots = (long long)q8::stream_ctas_per_sm(m) * sms;
+    long long ta;
+    bool co;
+    if (slots > sms && tiles > sms && tiles < slots) {
+        ta = sms;
+        co = true;
+    } else if (tiles > slots && tiles % slots != 0) {
+        ta = tiles / slots * slots;
+        co = false;
+    } else {
+        return none;
+    }
+    const long long tb = tiles - ta;
+    long long kb = (co ? sms : slots) / tb;
+    if (kb > 8) kb = 8;
+    if (kb > nb) kb = nb;
+    while (kb > 1) {  // clusters that are all resident at once (beside the first launch's CTAs: about half as many)
+        const int fit = q8::stream_max_clusters(m, (int)kb);
+        if (fit > 0 && tb <= (co ? fit / 2 : fit)) break;
+        --kb;
+    }
+    if (kb < 2) return none;
+    Split sp;
+    sp.tiles_a = (int)ta;
+    sp.ks_b = (int)kb;
+    sp.one_per_sm = co;
+    return sp;
+}
+
 q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStream_t stream,
               const q8::Parts *parts = nullptr) {
     const int epi = argmax ? q8::kEpiArgmax : q8::kEpiStore;
@@ -217,7 +271,27 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
         if (ce != cudaSuccess) return cuda_fail(ce);
         return Q8_OK;
     }
-    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, epi, stream, true, prefetch, qact,
+    const int mode = prefetch ? q8::kModePrefetch : 0;
+    if (p.variant == kVariantStream) {
+        const int tiles = parts->tile_end[parts->count - 1];
+        const Split sp = plan_split(tiles, a.nb, a.m, sms, b.ksplit);
+        if (sp.tiles_a > 0) {
+            q8::StreamGrid ga;
+            ga.ntiles = sp.tiles_a;
+            ga.one_per_sm = sp.one_per_sm;
+            cudaError_t ce = q8::launch_stream(b, *parts, epi, stream, true, mode | q8::kModeRelease, qact, !tiled, ga);
+            if (ce != cudaSuccess) return cuda_fail(ce);
+            Args c = b;
+            c.tile0 = sp.tiles_a;
+            c.ksplit = sp.ks_b;
+            q8::StreamGrid gb;
+            gb.ntiles = tiles - sp.tiles_a;
+            ce = q8::launch_stream(c, *parts, epi, stream, true, mode | q8::kModeDeferWait, qact, !tiled, gb);
+            if (ce != cudaSuccess) return cuda_fail(ce);
+            return Q8_OK;
+        }
+    }
+    cudaError_t ce = p.variant == kVariantStream    ? q8::launch_stream(b, *parts, epi, stream, true, mode, qact,
                                                                         !tiled)
                      : p.variant == Q8_VARIANT_TMA  ? q8::launch_tma(b, argmax, stream, true, prefetch)
                      : p.variant == Q8_VARIANT_SIMT ? q8::launch_simt(b, p.V, argmax, stream)
@@ -225,6 +299,26 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
     if (ce != cudaSuccess) return cuda_fail(ce);
     return Q8_OK;
 }
+
+}  // namespace
+
+extern "C" int q8_plan_launches(int m, int K, const int *Ns, int nparts, unsigned int flags) {
+    if (!Ns || nparts < 1 || nparts > Q8_MAX_PARTS || !flags_ok(flags)) return -Q8_ERR_ARG;
+    const bool tiled = (flags & Q8_FLAG_TILED) != 0;
+    const int max_rows = tiled ? Q8_MAX_CHUNK : Q8_MAX_ROWS;
+    if (m < 1 || m > max_rows || K <= 0 || K % Q8_BLOCK != 0) return -Q8_ERR_SHAPE;
+    long long tiles = 0;
+    for (int i = 0; i < nparts; ++i) {
+        if (Ns[i] <= 0 || q8_padded_n(Ns[i]) < 0 || (tiled && q8_tiled_n(Ns[i]) < 0)) return -Q8_ERR_SHAPE;
+        tiles += tiles_of(Ns[i]);
+    }
+    int sms = 0;
+    if (sm_count(&sms) != 0) return -Q8_ERR_CUDA;
+    const Plan p = make_plan(m, K, q8_padded_n(Ns[0]), Q8_VARIANT_AUTO, true, sms, tiles);
+    return plan_split(tiles, K / Q8_BLOCK, m, sms, p.ksplit).tiles_a > 0 ? 2 : 1;
+}
+
+namespace {
 
 // keys[r] (the packed maximum written by the GEMV) -> the 0-based index it encodes, in place.
 __global__ void argmax_decode(int64_t *idx, int m) {
@@ -411,7 +505,8 @@ extern "C" q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float
     }
     a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms, m);
     cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true,
-                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0, (flags & Q8_FLAG_Q8_ACT) != 0);
+                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) ? q8::kModePrefetch : 0,
+                                       (flags & Q8_FLAG_Q8_ACT) != 0);
     if (ce != cudaSuccess) return cuda_fail(ce);
     return Q8_OK;
 }
@@ -491,7 +586,8 @@ extern "C" q8_status q8_gemv_residual_norm_ex(const void *x, const int8_t *q, co
     const Plan p = make_plan(m, K, Np, Q8_VARIANT_AUTO, true, sms, pt.tile_end[0]);
     a.ksplit = p.ksplit;
     cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiNorm, (cudaStream_t)stream, true,
-                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0, (flags & Q8_FLAG_Q8_ACT) != 0);
+                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) ? q8::kModePrefetch : 0,
+                                       (flags & Q8_FLAG_Q8_ACT) != 0);
     if (ce != cudaSuccess) return cuda_fail(ce);
     if (own_launch) {
         ce = q8::launch_norm_rows(nr, m, (cudaStream_t)stream, true);
@@ -618,7 +714,7 @@ extern "C" q8_status q8_gemv_residual_norm_noalloc(const void *x, const int8_t *
               static_cast<uint16_t *>(out_bf16), residual, gamma, eps, counters, 0};
     a.ksplit = make_plan(m, K, Np, Q8_VARIANT_AUTO, true, sms, pt.tile_end[0]).ksplit;
     // a plain stream-ordered launch after the memset (no programmatic dependent launch)
-    ce = q8::launch_stream(a, pt, q8::kEpiNorm, cs, false, false, (flags & Q8_FLAG_Q8_ACT) != 0);
+    ce = q8::launch_stream(a, pt, q8::kEpiNorm, cs, false, 0, (flags & Q8_FLAG_Q8_ACT) != 0);
     if (ce != cudaSuccess) return cuda_fail(ce);
     return Q8_OK;
 }

@@ -52,12 +52,24 @@ cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl
 // Defined in q8_stream.cu (the tiled layout).
 int stream_ctas_per_sm(int m);          // resident CTAs per SM of the stream kernel that takes m rows
 int stream_max_clusters(int m, int ks);  // clusters of ks such CTAs resident at once on this device (0: unknown)
+// How a stream launch takes part in programmatic dependent launch (bits of `mode`):
+constexpr int kModePrefetch = 1;   // request the first ring stages' weights before the dependency wait
+constexpr int kModeRelease = 2;    // release the next launch right after the dependency wait, not after the main loop
+constexpr int kModeDeferWait = 4;  // no dependency wait before the main loop (the launch before released this one
+                                   // only after its own wait); wait just before exiting instead
+// A stream launch's grid: every column tile of the parts (ntiles = 0), or ntiles of them from Args::tile0 (m <= 16,
+// one row group); one_per_sm asks for enough shared memory that an SM holds one CTA of the launch and still one CTA
+// of 8 warps of another.
+struct StreamGrid {
+    int ntiles = 0;
+    bool one_per_sm = false;
+};
 // epi: kEpiStore, kEpiArgmax, kEpiGlu (parts 0 and 1 the gate and up weights, grid x = 2 * tiles) or kEpiNorm.
 // qact: a.x is a quantized activation (int8 values [m][K], then fp32 scales [m][K/32]) instead of bf16 values.
 // rowmajor: the parts' weights are row-major ([K][Np] int8, [K/32][Np] fp32), not tiled (kEpiStore and kEpiArgmax,
 // bf16 activations, m <= 16).
-cudaError_t launch_stream(const Args &a, const Parts &parts, int epi, cudaStream_t stream, bool pdl,
-                          bool prefetch_weights, bool qact, bool rowmajor = false);
+cudaError_t launch_stream(const Args &a, const Parts &parts, int epi, cudaStream_t stream, bool pdl, int mode,
+                          bool qact, bool rowmajor = false, StreamGrid grid = StreamGrid());
 cudaError_t read_fault_word(unsigned *out, bool clear);
 
 // Defined in q8_gemm.cu: the tcgen05 GEMM for prefill chunks (tiled storage, bf16 activations, plain store).

@@ -390,7 +390,7 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
 // RM: the weight is row-major (q8_gemv's layout), not tiled.
 template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false, bool RM = false>
 __global__ void __launch_bounds__(32 * stream_warps(ROWS16), ROWS16 ? 2 : 1)
-    stream_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
+    stream_kernel(Args a, const __grid_constant__ Parts parts, const int mode) {
     static_assert(ROWS16 || !GROUPS, "row groups are groups of 16 rows");
     constexpr int W = stream_warps(ROWS16);
     constexpr int MR = ROWS16 ? 16 : 8;
@@ -427,15 +427,17 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), ROWS16 ? 2 : 1)
         for (int j = 0; j < kSlices; ++j) acc[i][j] = 0ull;
 
     // Prologue: the first kDepthS - 1 units (one commit group each, empty past the run).
-    if (prefetch_weights) {
+    const bool early = (mode & (kModePrefetch | kModeDeferWait)) != 0;  // weights requested before any wait
+    if (early) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
             if (i < n) issue(ring + i * kStageS, i);
             cp_async_commit();
         }
     }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (!prefetch_weights) {
+    if (!(mode & kModeDeferWait)) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (mode & kModeRelease) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!early) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
             if (i < n) issue(ring + i * kStageS, i);
@@ -559,7 +561,7 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), ROWS16 ? 2 : 1)
         __syncwarp();  // every lane is done with this stage before it is refilled
     }
     cp_async_wait<0>();
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!(mode & kModeRelease)) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();  // every warp is done with its ring: the shared memory holds the epilogue now
 
     // [W][MR][kSlabStride]: rows padded by 8 floats, so that a half-warp's 8-byte stores (rows g, columns
@@ -582,6 +584,7 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), ROWS16 ? 2 : 1)
         finish_norm<W, MR, kTmaColumns, 32 * W, kSlabStride>(a, red, tile);
     else
         finish_n<W, MR, kTmaColumns, 32 * W, EPI == kEpiArgmax, kSlabStride>(a, red, tile);
+    if (mode & kModeDeferWait) asm volatile("griddepcontrol.wait;" ::: "memory");  // the first half has completed
 }
 
 // m <= 2 on CUDA cores: in segment (s, h) lane (g, t) holds words w = 0..3, each four weight rows 16s + 4t + 0..3 of
@@ -611,7 +614,7 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // eight codes, the exact integer is converted to fp32 and folded with s[b, n] * d[r, b].
 template <int M, int EPI, bool QACT = false, bool RM = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
-    stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int prefetch_weights) {
+    stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int mode) {
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -642,15 +645,17 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             accq[r][j] = 0.0f;
         }
 
-    if (prefetch_weights) {
+    const bool early = (mode & (kModePrefetch | kModeDeferWait)) != 0;  // weights requested before any wait
+    if (early) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
             if (i < n) issue(ring + i * kStageS, i);
             cp_async_commit();
         }
     }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (!prefetch_weights) {
+    if (!(mode & kModeDeferWait)) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (mode & kModeRelease) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!early) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
             if (i < n) issue(ring + i * kStageS, i);
@@ -763,7 +768,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
         __syncwarp();
     }
     cp_async_wait<0>();
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!(mode & kModeRelease)) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
 
     float *red = reinterpret_cast<float *>(smem_s);  // [kWarpsS][M][128]
@@ -787,6 +792,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
         finish_norm<kWarpsS, M, kTmaColumns, kThreadsS>(a, red, tile);
     else
         finish_n<kWarpsS, M, kTmaColumns, kThreadsS, EPI == kEpiArgmax>(a, red, tile);
+    if (mode & kModeDeferWait) asm volatile("griddepcontrol.wait;" ::: "memory");  // the first half has completed
 }
 
 static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns, kSlabStride) <= kSmemS, "the epilogue fits in the rings");
@@ -795,18 +801,26 @@ static_assert(2 * kSmemS <= 227 * 1024, "two CTAs per SM");
 static_assert(finish_smem_n(kWarps8, 8, kTmaColumns, kSlabStride) <= stream_smem(kWarps8), "8-row epilogue fits");
 static_assert((kWarps8 * 8 * kSlabStride + 2 * 8 * kTmaColumns) * 4 <= stream_smem(kWarps8), "8-row gated pair fits");
 static_assert(stream_smem(kWarps8) <= 227 * 1024, "one 8-row CTA per SM");
+// The shared memory of a launch held to one CTA per SM beside one ordinary CTA of 8 warps: two such CTAs (each with
+// its 1 KB reserve) exceed the SM's 228 KB, one of them and an ordinary one do not.
+constexpr int kSmemOnePerSm = 114 * 1024;
+static_assert(2 * (kSmemOnePerSm + 1024) > 228 * 1024 && kSmemOnePerSm + kSmemS + 2 * 1024 <= 228 * 1024,
+              "one such CTA and one ordinary CTA per SM");
 
 template <typename Kernel>
 cudaError_t launch_stream_kernel(Kernel kernel, int warps, const Args &a, const Parts &pt, cudaStream_t stream,
-                                 bool pdl, bool prefetch, bool pair) {
-    const int smem = stream_smem(warps);
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                 bool pdl, int mode, bool pair, StreamGrid grid) {
+    const int smem = grid.one_per_sm && warps == kWarpsS ? kSmemOnePerSm : stream_smem(warps);
+    // the attribute is the largest size any launch of the kernel asks for, so that concurrent callers agree on it
+    const int smem_max = warps == kWarpsS ? kSmemOnePerSm : stream_smem(warps);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     const unsigned groups = (unsigned)((a.m + kGroupRows - 1) / kGroupRows);
-    cfg.gridDim = dim3((unsigned)pt.tile_end[pt.count - 1] * groups, (unsigned)a.ksplit, 1);
+    const unsigned ntiles = grid.ntiles > 0 ? (unsigned)grid.ntiles : (unsigned)pt.tile_end[pt.count - 1];
+    cfg.gridDim = dim3(ntiles * groups, (unsigned)a.ksplit, 1);
     cfg.blockDim = dim3(32 * (unsigned)warps, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -826,7 +840,7 @@ cudaError_t launch_stream_kernel(Kernel kernel, int warps, const Args &a, const 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kernel, a, pt, prefetch ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, kernel, a, pt, mode);
 }
 
 }  // namespace
@@ -860,7 +874,8 @@ int stream_max_clusters(int m, int ks) {
     auto kernel = fam ? stream_kernel<false, kEpiStore> : stream_kernel<true, kEpiStore>;
     const int warps = stream_warps(fam == 0), smem = stream_smem(warps);
     int n = 0;
-    bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+    bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   fam ? smem : kSmemOnePerSm) == cudaSuccess &&  // as launch_stream_kernel sets it
               cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
     if (ok) {
         cudaLaunchConfig_t cfg = {};
@@ -885,11 +900,15 @@ int stream_max_clusters(int m, int ks) {
 }
 
 template <int EPI>
-cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, bool p, bool qact,
-                              bool rowmajor) {
+cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, int mode, bool qact,
+                              bool rowmajor, StreamGrid grid) {
     const bool pair = EPI == kEpiGlu;
-    auto go = [&](auto kernel) { return launch_stream_kernel(kernel, kWarpsS, a, pt, stream, pdl, p, pair); };
-    auto go8 = [&](auto kernel) { return launch_stream_kernel(kernel, kWarps8, a, pt, stream, pdl, p, pair); };
+    if ((grid.ntiles > 0 || a.tile0 != 0) && (pair || EPI == kEpiNorm || a.m > kGroupRows))
+        return cudaErrorInvalidValue;  // a part of the tiles: plain store and arg-max launches of one row group
+    auto go = [&](auto kernel) { return launch_stream_kernel(kernel, kWarpsS, a, pt, stream, pdl, mode, pair, grid); };
+    auto go8 = [&](auto kernel) {
+        return launch_stream_kernel(kernel, kWarps8, a, pt, stream, pdl, mode, pair, grid);
+    };
     if constexpr (EPI == kEpiStore || EPI == kEpiArgmax) {
         if (rowmajor) {  // at most 16 rows, bf16 activations
             if (qact || a.m > kGroupRows) return cudaErrorInvalidValue;
@@ -915,13 +934,13 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
     return go(stream_kernel<true, EPI, false, true>);
 }
 
-cudaError_t launch_stream(const Args &a, const Parts &pt, int epi, cudaStream_t stream, bool pdl,
-                          bool prefetch_weights, bool qact, bool rowmajor) {
+cudaError_t launch_stream(const Args &a, const Parts &pt, int epi, cudaStream_t stream, bool pdl, int mode,
+                          bool qact, bool rowmajor, StreamGrid grid) {
     switch (epi) {
-        case kEpiStore: return launch_stream_epi<kEpiStore>(a, pt, stream, pdl, prefetch_weights, qact, rowmajor);
-        case kEpiArgmax: return launch_stream_epi<kEpiArgmax>(a, pt, stream, pdl, prefetch_weights, qact, rowmajor);
-        case kEpiGlu: return launch_stream_epi<kEpiGlu>(a, pt, stream, pdl, prefetch_weights, qact, rowmajor);
-        case kEpiNorm: return launch_stream_epi<kEpiNorm>(a, pt, stream, pdl, prefetch_weights, qact, rowmajor);
+        case kEpiStore: return launch_stream_epi<kEpiStore>(a, pt, stream, pdl, mode, qact, rowmajor, grid);
+        case kEpiArgmax: return launch_stream_epi<kEpiArgmax>(a, pt, stream, pdl, mode, qact, rowmajor, grid);
+        case kEpiGlu: return launch_stream_epi<kEpiGlu>(a, pt, stream, pdl, mode, qact, rowmajor, grid);
+        case kEpiNorm: return launch_stream_epi<kEpiNorm>(a, pt, stream, pdl, mode, qact, rowmajor, grid);
         default: return cudaErrorInvalidValue;
     }
 }

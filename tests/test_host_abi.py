@@ -419,19 +419,20 @@ def test_quantized_output_argument_errors(lib):
     assert lib.q8_gemv_residual_norm_ex(A16, B16, C16, R, GM, f(1e-6), H, None, H, 2, 64, 96, 2, None) == 1
 
 
-@pytest.mark.parametrize("env,want", [(None, (0, -1, 0)), ({"Q8_NORM_LAUNCH": "0"}, (0, -1, 1)),
-                                      ({"Q8_NORM_LAUNCH": "1", "Q8_KSPLIT": "3", "Q8_GEMM": "1"}, (3, 1, 0)),
-                                      ({"Q8_KSPLIT": "9", "Q8_GEMM": "0"}, (0, 0, 0))])
+@pytest.mark.parametrize("env,want", [(None, (0, -1, 0, 1)), ({"Q8_NORM_LAUNCH": "0"}, (0, -1, 1, 1)),
+                                      ({"Q8_NORM_LAUNCH": "1", "Q8_KSPLIT": "3", "Q8_GEMM": "1"}, (3, 1, 0, 1)),
+                                      ({"Q8_KSPLIT": "9", "Q8_GEMM": "0", "Q8_SPLIT": "0"}, (0, 0, 0, 0)),
+                                      ({"Q8_SPLIT": "1"}, (0, -1, 0, 1))])
 def test_tuning_starts_from_the_environment(env, want):
-    """The planner overrides start from Q8_KSPLIT, Q8_GEMM and Q8_NORM_LAUNCH, read once in a fresh process (an
-    out-of-range K split is ignored); the binding's launch count of a residual-norm call follows the route."""
+    """The planner overrides start from Q8_KSPLIT, Q8_GEMM, Q8_NORM_LAUNCH and Q8_SPLIT, read once in a fresh process
+    (an out-of-range K split is ignored); the binding's launch count of a residual-norm call follows the route."""
     import subprocess
     import sys
-    e = {k: v for k, v in os.environ.items() if k not in ("Q8_NORM_LAUNCH", "Q8_KSPLIT", "Q8_GEMM")}
+    e = {k: v for k, v in os.environ.items() if k not in ("Q8_NORM_LAUNCH", "Q8_KSPLIT", "Q8_GEMM", "Q8_SPLIT")}
     e.update(env or {})
     code = ("import q8_block_quantized_gemv_gb300 as q8; "
             "print(q8.get_tuning('ksplit'), q8.get_tuning('gemm'), q8.get_tuning('norm_fold'), "
-            "q8.residual_norm_launches())")
+            "q8.get_tuning('split'), q8.residual_norm_launches())")
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=e, cwd=ROOT, timeout=120)
     assert out.returncode == 0, out.stderr
     got = tuple(int(v) for v in out.stdout.split())
@@ -439,21 +440,38 @@ def test_tuning_starts_from_the_environment(env, want):
 
 
 def test_tuning_set_get_and_rejects(lib):
-    saved = [lib.q8_get_tuning(o) for o in range(3)]
+    saved = [lib.q8_get_tuning(o) for o in range(4)]
     try:
-        for opt, ok, bad in ((0, (0, 1, 8), (-1, 9)), (1, (-1, 0, 1), (-2, 2)), (2, (0, 1), (-1, 2))):
+        for opt, ok, bad in ((0, (0, 1, 8), (-1, 9)), (1, (-1, 0, 1), (-2, 2)), (2, (0, 1), (-1, 2)),
+                             (3, (0, 1), (-1, 2))):
             for v in ok:
                 assert lib.q8_set_tuning(opt, v) == 0 and lib.q8_get_tuning(opt) == v
             for v in bad:
                 assert lib.q8_set_tuning(opt, v) == 1 and lib.q8_get_tuning(opt) == ok[-1]
-        assert lib.q8_set_tuning(3, 0) == 1 and lib.q8_set_tuning(-1, 0) == 1
-        assert lib.q8_get_tuning(3) == -2 and lib.q8_get_tuning(-1) == -2
+        assert lib.q8_set_tuning(4, 0) == 1 and lib.q8_set_tuning(-1, 0) == 1
+        assert lib.q8_get_tuning(4) == -2 and lib.q8_get_tuning(-1) == -2
         with q8.tuning(norm_fold=1, ksplit=5):
             assert q8.residual_norm_launches() == 1 and q8.get_tuning("ksplit") == 5
     finally:
         for o, v in enumerate(saved):
             lib.q8_set_tuning(o, v)
-    assert [lib.q8_get_tuning(o) for o in range(3)] == saved
+    assert [lib.q8_get_tuning(o) for o in range(4)] == saved
+
+
+def test_plan_launches_argument_errors(lib):
+    """q8_plan_launches rejects, before any device query, what q8_gemv_parts would reject; valid sizes give a count
+    (1 or 2) on a GPU and -Q8_ERR_CUDA without one."""
+    ns = (ctypes.c_int * 2)(4096, 4096)
+    p = ctypes.cast(ns, ctypes.c_void_p)
+    call = lib.q8_plan_launches
+    assert call(1, 64, None, 1, 2) == -1
+    assert call(1, 64, p, 0, 2) == -1 and call(1, 64, p, 9, 2) == -1
+    assert call(1, 64, p, 1, 0x80) == -1
+    assert call(0, 64, p, 1, 2) == -2 and call(17, 64, p, 1, 0) == -2 and call(513, 64, p, 1, 2) == -2
+    assert call(1, 33, p, 1, 2) == -2 and call(1, 0, p, 1, 2) == -2
+    bad = (ctypes.c_int * 1)(0)
+    assert call(1, 64, ctypes.cast(bad, ctypes.c_void_p), 1, 2) == -2
+    assert call(1, 64, p, 2, 2) in (-5, 1, 2)
 
 
 def test_residual_norm_noalloc_argument_errors(lib):
