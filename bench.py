@@ -4,14 +4,15 @@
 Workload (one step): the projection chain of a 32-layer 7B-class decode step over Q8_0 weights -- per layer q, k, v, o
 (4096 x 4096), gate and up (4096 x 14336) and down (14336 x 4096) -- then the tied head (4096 x 128256) with the
 arg-max over its fp32 logits fused.  Per layer q/k/v read one activation and gate/up another, as in a transformer
-layer, so each pair or triple is one q8_gemv_parts launch; o and down are q8_gemv launches: 128 layer launches and
-one q8_gemv_argmax, m activation rows each (m = 1 by default), 9.36 GB of weights per step at m = 1: every step reads
-far more than the 129 MB L2, so no flush is needed.
+layer, so each pair or triple is one q8_gemv_parts call; o and down are q8_gemv calls: 128 layer calls and one
+q8_gemv_argmax, m activation rows each (m = 1 and 16 by default), 9.36 GB of weights per step at m = 1: every step
+reads far more than the 129 MB L2, so no flush is needed.  The planner runs some calls as two launches
+(q8_plan_launches; the gate/up pairs and the head on 152 SMs), which gpu_launches counts.
 Weights: q uniform int8 in [-127, 127] with a +-127 per block, s = 2^u/127, u ~ U[-8, -2], drawn on the device from a
 seed; activations bf16 N(0,1), drawn per layer.
 
-value = algorithmic bytes per step (K * Np * 1.125 per weight and m * Np * 4 per output, m * K * 2 per activation read
-by a launch; the head writes m * 8 index bytes instead of logits) / device time per step, summed over ranks (replicas:
+value = algorithmic bytes per step (K * N * 1.125 per weight and m * N * 4 per output, m * K * 2 per activation read
+by a call; the head writes m * 8 index bytes instead of logits) / device time per step, summed over ranks (replicas:
 every rank runs the whole step on its own GPU).
 
 Arms:
@@ -118,7 +119,8 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs (one every 100 ms, each stamped
+    with its host arrival time so that the summary keeps those of the region: mark() at its start and end)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -132,7 +134,8 @@ class ClockSampler:
         except Exception:
             pass
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, csv line)
+        self.marks = []
 
     def __enter__(self):
         try:
@@ -148,7 +151,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
 
     def __exit__(self, *exc):
         if self.proc:
@@ -159,9 +165,16 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        """Median SM clock, its maximum and the throttle reasons seen over the samples that arrived between the first
+        and last mark (plus 0.2 s for nvidia-smi's delivery); all samples when fewer than two of those exist."""
         mhz, maxmhz, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        lines = self.lines
+        if len(self.marks) >= 2:
+            inside = [(t, l) for t, l in self.lines if self.marks[0] <= t <= self.marks[-1] + 0.2]
+            if len(inside) >= 2:
+                lines = inside
+        for _, line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -176,7 +189,8 @@ class ClockSampler:
         if not mhz:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxmhz), "reasons": sorted(reasons),
-                "samples": len(mhz)}
+                "samples": len(mhz), "in_timed_region": lines is not self.lines,
+                "timed_region_s": (self.marks[-1] - self.marks[0]) if len(self.marks) >= 2 else None}
 
 
 # ---------------------------------------------------------------------------------------------------------------------
@@ -507,6 +521,7 @@ def measure_chain(args, torch, weights, m, world, local_rank, barrier, max_over_
     with ClockSampler(local_rank) as clocks:
         barrier()
         torch.cuda.synchronize()
+        clocks.mark()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(args.steps):
@@ -517,6 +532,7 @@ def measure_chain(args, torch, weights, m, world, local_rank, barrier, max_over_
             ev[i][2].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
+        clocks.mark()
         barrier()
     ms = start.elapsed_time(end) / args.steps
     layers_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
@@ -804,7 +820,7 @@ def run_sweep_launches(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)  # about 1 s of timed steps at m = 1, 1.3 s at m = 16
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--m", default="1,16",
                     help="activation rows per call (1..512), a comma list: the first is the headline value, every "
