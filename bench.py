@@ -40,7 +40,7 @@ LAYERS = 32
 HIDDEN, FFN, VOCAB = 4096, 14336, 128256
 WORKLOAD = (f"decode-step Q8_0 projection chain: {LAYERS} layers x (q,k,v,o 4096x4096; gate,up 4096x14336; "
             f"down 14336x4096) + tied head 4096x128256 with fused arg-max; per layer q/k/v share one activation and "
-            f"gate/up another (one multi-projection launch each), o and down their own")
+            f"gate/up another (one multi-projection call each), o and down their own")
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 FUSED_NOTE = ("; --fused: q/k/v read the previous layer's normed output, o and down add into the fp32 residual "
               "stream in place and write the next RMS norm (q8_gemv_residual_norm), gate/up is the gated pair")

@@ -88,7 +88,7 @@ struct Plan {
 // Kernel family, per-lane width and K split for a shape.  The widest tile that still gives every SM a CTA is
 // preferred; K is split across a cluster (at most 8 CTAs, the portable size) until the grid holds about as many CTAs
 // as are resident at once (two per SM; one for the 8-row stream kernel).
-Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long tiled_tiles = 0) {
+Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long tiled_tiles = 0, bool qact = false) {
     const int nb = K / Q8_BLOCK;
     if (tiled) {
         // The tiled layout: per-warp cp.async streams, 128-column tiles.  Measured on GB300, the best K split is
@@ -98,13 +98,13 @@ Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long
         // one GPC, so fewer clusters fit than slots / ks).
         const long long groups = (m + q8::kGroupRows - 1) / q8::kGroupRows;
         const long long tiles = groups * (tiled_tiles > 0 ? tiled_tiles : (Np + q8::kTmaColumns - 1) / q8::kTmaColumns);
-        const long long slots = (long long)q8::stream_ctas_per_sm(m) * sms;
+        const long long slots = (long long)q8::stream_ctas_per_sm(m, qact) * sms;
         long long ks = slots / tiles;
         if (ks > 8) ks = 8;
         if (ks > nb) ks = nb;
         if (ks < 1) ks = 1;
         while (ks > 1) {
-            const int fit = q8::stream_max_clusters(m, (int)ks);
+            const int fit = q8::stream_max_clusters(m, qact, (int)ks);
             if (fit <= 0 || tiles <= fit) break;
             --ks;
         }
@@ -208,12 +208,12 @@ struct Split {
     int ks_b = 1;     // the second launch's K split
     bool one_per_sm = false;
 };
-Split plan_split(long long tiles, int nb, int m, int sms, int ks) {
+Split plan_split(long long tiles, int nb, int m, bool qact, int sms, int ks) {
     Split none;
     // (a forced K split keeps one launch, so that it applies to every tile)
     if (tuning(Q8_TUNE_SPLIT) == 0 || tuning(Q8_TUNE_KSPLIT) != 0 || ks != 1 || m > q8::kGroupRows || sms <= 0)
         return none;
-    const long long slots = (long long)q8::stream_ctas_per_sm(m) * sms;
+    const long long slots = (long long)q8::stream_ctas_per_sm(m, qact) * sms;
     long long ta;
     bool co;
     if (slots > sms && tiles > sms && tiles < slots) {
@@ -230,7 +230,7 @@ Split plan_split(long long tiles, int nb, int m, int sms, int ks) {
     if (kb > 8) kb = 8;
     if (kb > nb) kb = nb;
     while (kb > 1) {  // clusters that are all resident at once (beside the first launch's CTAs: about half as many)
-        const int fit = q8::stream_max_clusters(m, (int)kb);
+        const int fit = q8::stream_max_clusters(m, qact, (int)kb);
         if (fit > 0 && tb <= (co ? fit / 2 : fit)) break;
         --kb;
     }
@@ -261,11 +261,12 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
         one.count = 1;
         parts = &one;
     }
-    const Plan p = make_plan(a.m, a.K, a.Np, variant, streaming, sms, parts ? parts->tile_end[parts->count - 1] : 0);
+    const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
+    const Plan p = make_plan(a.m, a.K, a.Np, variant, streaming, sms, parts ? parts->tile_end[parts->count - 1] : 0,
+                             qact);
     Args b = a;
     b.ksplit = p.ksplit;
     const bool prefetch = (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0;
-    const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
     if (p.variant == kVariantStream && use_gemm(a.m, epi, qact, parts->tile_end[parts->count - 1])) {
         cudaError_t ce = q8::launch_gemm(b, *parts, stream);
         if (ce != cudaSuccess) return cuda_fail(ce);
@@ -274,7 +275,7 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
     const int mode = prefetch ? q8::kModePrefetch : 0;
     if (p.variant == kVariantStream) {
         const int tiles = parts->tile_end[parts->count - 1];
-        const Split sp = plan_split(tiles, a.nb, a.m, sms, b.ksplit);
+        const Split sp = plan_split(tiles, a.nb, a.m, qact, sms, b.ksplit);
         if (sp.tiles_a > 0) {
             q8::StreamGrid ga;
             ga.ntiles = sp.tiles_a;
@@ -314,8 +315,9 @@ extern "C" int q8_plan_launches(int m, int K, const int *Ns, int nparts, unsigne
     }
     int sms = 0;
     if (sm_count(&sms) != 0) return -Q8_ERR_CUDA;
-    const Plan p = make_plan(m, K, q8_padded_n(Ns[0]), Q8_VARIANT_AUTO, true, sms, tiles);
-    return plan_split(tiles, K / Q8_BLOCK, m, sms, p.ksplit).tiles_a > 0 ? 2 : 1;
+    const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
+    const Plan p = make_plan(m, K, q8_padded_n(Ns[0]), Q8_VARIANT_AUTO, true, sms, tiles, qact);
+    return plan_split(tiles, K / Q8_BLOCK, m, qact, sms, p.ksplit).tiles_a > 0 ? 2 : 1;
 }
 
 namespace {
@@ -440,14 +442,14 @@ extern "C" q8_status q8_gemv_parts(const void *x, const q8_part *parts, int npar
 
 // The K split of a gated-pair launch: its clusters are (2, ks), a gate's and an up projection's CTA for each K range
 // of one column tile, so the one-wave rule counts 2 * tiles * ks CTAs and clusters of 2 * ks (at most 8).
-int plan_glu(long long tiles, int nb, int sms, int m) {
-    const long long slots = (long long)q8::stream_ctas_per_sm(m) * sms;
+int plan_glu(long long tiles, int nb, int sms, int m, bool qact) {
+    const long long slots = (long long)q8::stream_ctas_per_sm(m, qact) * sms;
     long long ks = slots / (2 * tiles);
     if (ks > 4) ks = 4;
     if (ks > nb) ks = nb;
     if (ks < 1) ks = 1;
     while (ks > 1) {
-        const int fit = q8::stream_max_clusters(m, (int)(2 * ks));
+        const int fit = q8::stream_max_clusters(m, qact, (int)(2 * ks));
         if (fit <= 0 || tiles <= fit) break;
         --ks;
     }
@@ -503,7 +505,7 @@ extern "C" q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float
         a.yq = static_cast<unsigned char *>(out_q8);
         a.yd = reinterpret_cast<float *>(a.yq + (size_t)m * Np);
     }
-    a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms, m);
+    a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms, m, (flags & Q8_FLAG_Q8_ACT) != 0);
     cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true,
                                        (flags & Q8_FLAG_CONSTANT_WEIGHTS) ? q8::kModePrefetch : 0,
                                        (flags & Q8_FLAG_Q8_ACT) != 0);
@@ -583,7 +585,7 @@ extern "C" q8_status q8_gemv_residual_norm_ex(const void *x, const int8_t *q, co
     pt.N[0] = N;
     pt.tile_end[0] = tiles_of(N);
     pt.count = 1;
-    const Plan p = make_plan(m, K, Np, Q8_VARIANT_AUTO, true, sms, pt.tile_end[0]);
+    const Plan p = make_plan(m, K, Np, Q8_VARIANT_AUTO, true, sms, pt.tile_end[0], (flags & Q8_FLAG_Q8_ACT) != 0);
     a.ksplit = p.ksplit;
     cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiNorm, (cudaStream_t)stream, true,
                                        (flags & Q8_FLAG_CONSTANT_WEIGHTS) ? q8::kModePrefetch : 0,
@@ -712,7 +714,7 @@ extern "C" q8_status q8_gemv_residual_norm_noalloc(const void *x, const int8_t *
     pt.count = 1;
     Args a = {static_cast<const uint16_t *>(x), q, s, h, nullptr, m, K, N, Np, K / Q8_BLOCK, 1,
               static_cast<uint16_t *>(out_bf16), residual, gamma, eps, counters, 0};
-    a.ksplit = make_plan(m, K, Np, Q8_VARIANT_AUTO, true, sms, pt.tile_end[0]).ksplit;
+    a.ksplit = make_plan(m, K, Np, Q8_VARIANT_AUTO, true, sms, pt.tile_end[0], (flags & Q8_FLAG_Q8_ACT) != 0).ksplit;
     // a plain stream-ordered launch after the memset (no programmatic dependent launch)
     ce = q8::launch_stream(a, pt, q8::kEpiNorm, cs, false, 0, (flags & Q8_FLAG_Q8_ACT) != 0);
     if (ce != cudaSuccess) return cuda_fail(ce);

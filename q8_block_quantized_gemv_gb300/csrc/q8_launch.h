@@ -50,8 +50,10 @@ bool encode_bf16_rows(CUtensorMap *map, const void *base, int rows, int K, int b
 cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl, bool prefetch_weights);
 
 // Defined in q8_stream.cu (the tiled layout).
-int stream_ctas_per_sm(int m);          // resident CTAs per SM of the stream kernel that takes m rows
-int stream_max_clusters(int m, int ks);  // clusters of ks such CTAs resident at once on this device (0: unknown)
+// Resident CTAs per SM of the stream kernel that takes m rows (qact: of quantized activations), and how many clusters
+// of ks such CTAs are resident at once on this device (0: unknown).
+int stream_ctas_per_sm(int m, bool qact);
+int stream_max_clusters(int m, bool qact, int ks);
 // How a stream launch takes part in programmatic dependent launch (bits of `mode`):
 constexpr int kModePrefetch = 1;   // request the first ring stages' weights before the dependency wait
 constexpr int kModeRelease = 2;    // release the next launch right after the dependency wait, not after the main loop

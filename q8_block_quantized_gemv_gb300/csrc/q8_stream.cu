@@ -33,8 +33,11 @@
 //     fp32x2 FMA over the pair of columns a lane holds ("from_q8.rs", module doc: int8 rows contracted lane by
 //     lane, each column's block sums scaled and accumulated in an fp32 carry).
 //
-// For m <= 2 the CUDA cores do the contraction instead (stream_simt_kernel): there the per-row FMAs cost less than
-// the MMA operands' conversion and the per-block exponent choice.
+// For one row the CUDA cores do the contraction instead (stream_simt_kernel): there the row's FMAs cost less than the
+// MMA operands' conversion and the per-block exponent choice.  From two bf16 rows on the 8-row MMA kernel is the
+// faster one (measured on GB300: 4096 x 14336 at two rows 17.9 us on the CUDA cores, 12.9 on the 8-row kernel); two
+// rows of quantized activations stay on the CUDA cores, whose dp4a products beat it there (the decode chain 3,900
+// against 3,658 GB/s).
 //
 // Activations are read from L2 (ld.global.cg), two blocks ahead.  With programmatic dependent launch every thread
 // waits for the previous kernel (griddepcontrol.wait) before it reads x or writes y; with Q8_FLAG_CONSTANT_WEIGHTS
@@ -587,10 +590,10 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), ROWS16 ? 2 : 1)
     if (mode & kModeDeferWait) asm volatile("griddepcontrol.wait;" ::: "memory");  // the first half has completed
 }
 
-// m <= 2 on CUDA cores: in segment (s, h) lane (g, t) holds words w = 0..3, each four weight rows 16s + 4t + 0..3 of
-// column 8(4h + w) + g; they meet the lane's four activations of each row with two packed fp32x2 FMAs (exact
-// products), the block's sums of a column are folded with its scale, and at the end the four lanes t of a column
-// add their carries.
+// M rows on CUDA cores (one row; two of quantized activations): in segment (s, h) lane (g, t) holds words w = 0..3,
+// each four weight rows 16s + 4t + 0..3 of column 8(4h + w) + g; they meet the lane's four activations of each row
+// with two packed fp32x2 FMAs (exact products), the block's sums of a column are folded with its scale, and at the
+// end the four lanes t of a column add their carries.
 // Stored bytes E, E + 1 of a word as the exact fp32 pair {q_E, q_E+1}: each byte in the low mantissa of 2^23 gives
 // 2^23 + q + 128, and one packed subtract of 2^23 + 128 leaves q.
 template <int E> __device__ __forceinline__ unsigned long long q8x2_to_f32x2(uint32_t u) {
@@ -609,7 +612,7 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
-// QACT (quantized activations, m <= 2): the lane's eight codes of a row and block meet each column's eight stored
+// QACT (quantized activations): the lane's eight codes of a row and block meet each column's eight stored
 // bytes in two dp4a (integer products, exact); the offset is removed by starting the sum at -128 times the sum of the
 // eight codes, the exact integer is converted to fp32 and folded with s[b, n] * d[r, b].
 template <int M, int EPI, bool QACT = false, bool RM = false>
@@ -618,7 +621,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    int group;  // one row group (m <= 2)
+    int group;  // one row group
     const int tile = select_cta<EPI, false>(parts, a, group);
     const int rank = blockIdx.y;
     const int c0 = (int)((long long)a.nb * rank / a.ksplit);
@@ -856,11 +859,11 @@ unsigned int *norm_counters() {
     return static_cast<unsigned int *>(base);
 }
 
-// The 8-row kernel (3 .. 8 rows) runs one CTA per SM, the others two.
-bool rows8_family(int m) { return m >= 3 && m <= 8; }
-int stream_ctas_per_sm(int m) { return rows8_family(m) ? 1 : 2; }
+// The 8-row kernel (2 .. 8 rows; 3 .. 8 of quantized activations) runs one CTA per SM, the others two.
+bool rows8_family(int m, bool qact) { return (m >= 3 && m <= 8) || (m == 2 && !qact); }
+int stream_ctas_per_sm(int m, bool qact) { return rows8_family(m, qact) ? 1 : 2; }
 
-int stream_max_clusters(int m, int ks) {
+int stream_max_clusters(int m, bool qact, int ks) {
     // Clusters of ks CTAs are placed within one GPC, so fewer of them fit at once than slots / ks.  Asked once per
     // device, kernel shape and size (a deterministic answer: concurrent first calls store the same value); the stream
     // kernels of one shape (8-row: 12 warps, one CTA per SM; the others: 8 warps, two) have the same block size,
@@ -868,7 +871,7 @@ int stream_max_clusters(int m, int ks) {
     static std::atomic<int> cache[64][2][9];  // 0: not asked yet; else the count + 1
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > 8) return 0;
-    const int fam = rows8_family(m) ? 1 : 0;
+    const int fam = rows8_family(m, qact) ? 1 : 0;
     const int known = cache[dev][fam][ks].load(std::memory_order_relaxed);
     if (known > 0) return known - 1;
     auto kernel = fam ? stream_kernel<false, kEpiStore> : stream_kernel<true, kEpiStore>;
@@ -913,7 +916,6 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
         if (rowmajor) {  // at most 16 rows, bf16 activations
             if (qact || a.m > kGroupRows) return cudaErrorInvalidValue;
             if (a.m == 1) return go(stream_simt_kernel<1, EPI, false, true>);
-            if (a.m == 2) return go(stream_simt_kernel<2, EPI, false, true>);
             if (a.m <= 8) return go8(stream_kernel<false, EPI, false, false, true>);
             return go(stream_kernel<true, EPI, false, false, true>);
         }
@@ -928,7 +930,6 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
         return go(stream_kernel<true, EPI, true, true>);
     }
     if (a.m == 1) return go(stream_simt_kernel<1, EPI>);
-    if (a.m == 2) return go(stream_simt_kernel<2, EPI>);
     if (a.m <= 8) return go8(stream_kernel<false, EPI>);
     if (a.m <= kGroupRows) return go(stream_kernel<true, EPI>);
     return go(stream_kernel<true, EPI, false, true>);

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 TOL = 1e-5
 
-# (K, Ns) of the two split cases on a GPU of 152 SMs (two CTAs per SM for 1, 2 and 9..16 rows, one for 3..8):
+# (K, Ns) of the two split cases on a GPU of 152 SMs (two CTAs per SM for 1 and 9..16 rows, one for 2..8):
 #   co:    160 tiles, between the SMs and the resident slots: 152 tiles one CTA per SM, then 8 tiles with K split
 #   waves: 330 tiles, above the slots: the whole waves, then the rest with K split
 CASES = {"co": (512, (10240, 10240)), "waves": (256, (42240,))}
@@ -69,17 +69,17 @@ def _assert_close(y_gpu, y_o, a_o, what=""):
 
 
 def test_planner_splits_the_chains_uneven_launches(dev, sms):
-    """On 152 SMs: the gate/up pair (224 tiles) and the tied head (1002 tiles) split at 1, 2 and 16 rows; q/k/v, o and
-    down keep one launch (their K split already fills the SMs); with the 8-row kernel (one CTA per SM) the head keeps
-    one launch (its 90 leftover tiles over 152 slots take no K split) and the pair splits when its 72 clusters of two
-    fit.  Switched off, or under a forced K split, every call is one launch."""
+    """On 152 SMs: the gate/up pair (224 tiles) and the tied head (1002 tiles) split at 1 and 16 rows; q/k/v, o and
+    down keep one launch (their K split already fills the SMs); with the 8-row kernel (2..8 rows, one CTA per SM) the
+    head keeps one launch (its 90 leftover tiles over 152 slots take no K split) and the pair splits when its 72
+    clusters of two fit.  Switched off, or under a forced K split, every call is one launch."""
     import q8_block_quantized_gemv_gb300 as q8
     if sms != 152:
         pytest.skip("expectations for a 152-SM GB300")
     shapes = {"qkv": (4096, (4096, 4096, 4096)), "o": (4096, (4096,)), "gateup": (4096, (14336, 14336)),
               "down": (14336, (4096,)), "head": (4096, (128256,))}
     for m in (1, 2, 4, 8, 16):
-        rows8 = 3 <= m <= 8
+        rows8 = 2 <= m <= 8
         for name, (K, Ns) in shapes.items():
             got = q8.plan_launches(m, K, Ns)
             if name == "gateup":
