@@ -20,8 +20,9 @@
  * Conventions shared by every entry point:
  *   - The caller owns every buffer and the library allocates no memory.  Its only state is read-only caches (per
  *     device: SM count, resident clusters), the device fault words (q8_device_fault), the planner overrides of
- *     q8_set_tuning, and the residual norm's 64 static completion counters (used only by its one-launch fold; see
- *     q8_gemv_residual_norm for the limit this puts on overlapping calls).
+ *     q8_set_tuning, the residual norm's 64 static completion counters (used only by its one-launch fold; see
+ *     q8_gemv_residual_norm for the limit this puts on overlapping calls) and the 32 static counters of
+ *     q8_gemv_residual_norm_noalloc (see there).
  *   - Device entry points take device pointers and enqueue work on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  They are asynchronous: Q8_OK means the work was enqueued.  An argument error is returned
  *     before anything is enqueued.  A CUDA error at launch returns Q8_ERR_CUDA; q8_last_cuda_error() then gives the
