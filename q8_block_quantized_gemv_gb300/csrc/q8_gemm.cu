@@ -294,10 +294,15 @@ __global__ void __maxnreg__(96)
         __syncwarp();
     } else {
         // ---- workers: convert block i, fold block i - kFoldLag ----
-        const int idx = (warp - kWorkWarp0) * 32 + lane;
-        const int c = idx >> 1, half = idx & 1;  // this thread's 16-byte chunk of a unit, and which two of its words
-        const int seg = c >> 5, L = c & 31;
-        const int s = seg >> 2, h = seg & 3, g = L >> 2, u = L & 3;  // segment 4s + h, lane 4g + u
+        // Each thread converts two words of the unit: words 2wp, 2wp + 1 of segment 4s + h, lane 4g + u.  Warp wi
+        // takes group h, columns g0 .. g0 + 3 of each 8-column slice and word pair wp; a lane takes (s, g, u).  Then
+        // the 16 lanes of a half-warp write two adjacent weight columns (rows of B) whole -- their 16 x 8 bytes are
+        // one 128-byte line of banks -- so the conversion stores have no bank conflicts (the raw reads take two
+        // passes a half-warp: its two 16-row halves s sit 2 KB apart).
+        const int wi = warp - kWorkWarp0;
+        const int h = wi & 3, g0 = ((wi >> 2) & 1) * 4, wp = wi >> 3;
+        const int u = lane & 3, s = (lane >> 3) & 1, g = g0 + 2 * ((lane >> 4) & 1) + ((lane >> 2) & 1);
+        const int c = (4 * s + h) * 32 + 4 * g + u;  // this thread's 16-byte chunk of the unit
         auto fold = [&](int f) -> bool {
             const int buf = f % kAccBufs, st = f % kGStages;
             if (!bar_wait(&acc_full[buf], (f / kAccBufs) & 1, abort)) return false;
@@ -329,11 +334,11 @@ __global__ void __maxnreg__(96)
             const int st = i % kGStages;
             if (!bar_wait(&loaded[st], (i / kGStages) & 1, abort)) break;
             unsigned char *sp = smem_g + st * kStageBytes;
-            const uint2 raw = *reinterpret_cast<const uint2 *>(sp + kRawOff + c * 16 + half * 8);
+            const uint2 raw = *reinterpret_cast<const uint2 *>(sp + kRawOff + c * 16 + wp * 8);
             const uint32_t words[2] = {raw.x, raw.y};
 #pragma unroll
             for (int ww = 0; ww < 2; ++ww) {
-                const int w = 2 * half + ww;
+                const int w = 2 * wp + ww;
                 const int j = 4 * h + w;  // 8-column slice: B rows 8j .. 8j + 7, this word's row 8j + g
                 const uint2 cv = make_uint2(stored_to_bf16x2<0>(words[ww]), stored_to_bf16x2<2>(words[ww]));
                 // B row (weight column) nr = 8j + g holds its 32 K values in 64 bytes; 16-byte chunk kc = 2s + u / 2
