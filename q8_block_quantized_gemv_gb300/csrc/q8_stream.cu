@@ -820,6 +820,10 @@ cudaError_t launch_stream_kernel(Kernel kernel, int warps, const Args &a, const 
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
+    if (a.ksplit * (pair ? 2 : 1) > 8) {  // clusters above the portable 8 CTAs (up to 16 on this GPU)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     const unsigned groups = (unsigned)((a.m + kGroupRows - 1) / kGroupRows);
     const unsigned ntiles = grid.ntiles > 0 ? (unsigned)grid.ntiles : (unsigned)pt.tile_end[pt.count - 1];
@@ -868,9 +872,9 @@ int stream_max_clusters(int m, bool qact, int ks) {
     // device, kernel shape and size (a deterministic answer: concurrent first calls store the same value); the stream
     // kernels of one shape (8-row: 12 warps, one CTA per SM; the others: 8 warps, two) have the same block size,
     // register cap and shared memory.
-    static std::atomic<int> cache[64][2][9];  // 0: not asked yet; else the count + 1
+    static std::atomic<int> cache[64][2][kMaxStreamSplit + 1];  // 0: not asked yet; else the count + 1
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > 8) return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > kMaxStreamSplit) return 0;
     const int fam = rows8_family(m, qact) ? 1 : 0;
     const int known = cache[dev][fam][ks].load(std::memory_order_relaxed);
     if (known > 0) return known - 1;
@@ -879,7 +883,9 @@ int stream_max_clusters(int m, bool qact, int ks) {
     int n = 0;
     bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    fam ? smem : kSmemOnePerSm) == cudaSuccess &&  // as launch_stream_kernel sets it
-              cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+              cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
+              (ks <= 8 || cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                              cudaSuccess);
     if (ok) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, (unsigned)ks, 1);
