@@ -271,7 +271,14 @@ __device__ __forceinline__ uint32_t act_code(float v, float d, float inv, uint32
 template <int NRED, int MR, int TC, int NTHREADS, bool ARGMAX, int RS = TC>
 __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
     namespace cg = cooperative_groups;
-    float *part = red + NRED * MR * RS;                                                   // [MR][TC]
+    float *part = red + NRED * MR * RS;  // [MR][TC]
+    // Arg-max: up to 8 rows, the keys of this CTA's outputs, [rows][width], go over the slabs (free once `part` holds
+    // their sum) and one warp a row reduces them; 16 rows fold each key into a row key in shared memory by atomicMax
+    // (measured on GB300: the warp reduction takes the tied head at m = 8 from 119.4 to 114.9 us, but in the 16-row
+    // kernel, which sits at its 128-register cap, its code made the main loop spill and the head slower).
+    constexpr bool kWarpReduce = MR <= 8;
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(red);
+    static_assert(NRED * RS >= 2 * TC, "the keys fit over the slabs");
     unsigned long long *rowkey = reinterpret_cast<unsigned long long *>(part + MR * TC);  // [MR]
     const int rows = a.m < MR ? a.m : MR;
 
@@ -282,7 +289,7 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
         for (int w = 0; w < NRED; ++w) v += red[w * MR * RS + at];
         part[i] = v;
     }
-    if (ARGMAX)
+    if (ARGMAX && !kWarpReduce)
         for (int r = threadIdx.x; r < MR; r += NTHREADS) rowkey[r] = 0ull;
 
     const int ks = a.ksplit;
@@ -310,13 +317,31 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
         if (n < a.Np) {
             const float out = n < a.N ? v : 0.0f;
             if (a.y) a.y[(size_t)r * a.Np + n] = out;
-            if (ARGMAX && n < a.N) atomicMax(&rowkey[r], argmax_key(out, n));
+            if (ARGMAX && !kWarpReduce && n < a.N) atomicMax(&rowkey[r], argmax_key(out, n));
         }
+        if (ARGMAX && kWarpReduce) keys[i] = n < a.N ? argmax_key(v, n) : 0ull;
     }
-    if (ARGMAX) {
+    if (ARGMAX && !kWarpReduce) {
         __syncthreads();
         for (int r = threadIdx.x; r < rows; r += NTHREADS)
             if (rowkey[r]) atomicMax(&a.keys[r], rowkey[r]);
+    }
+    if (ARGMAX && kWarpReduce) {
+        // each row's largest key by one warp (a lane's maximum over its columns, then a shuffle tree), and one
+        // atomic a row into the call's keys: the maximum is the same in any order
+        __syncthreads();
+        constexpr int kWarpsE = NTHREADS / 32;
+        const int lane = threadIdx.x & 31;
+        for (int r = threadIdx.x >> 5; r < rows; r += kWarpsE) {
+            unsigned long long k = 0ull;
+            for (int c = lane; c < width; c += 32) k = k > keys[r * width + c] ? k : keys[r * width + c];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
+                k = k > other ? k : other;
+            }
+            if (lane == 0 && k) atomicMax(&a.keys[r], k);
+        }
     }
     if (ks > 1) cg::this_cluster().sync();  // keep this CTA's shared memory alive until every rank has read it
 }
