@@ -442,14 +442,14 @@ class Chain:
         torch.cuda.synchronize()
 
     def layer_launches(self):
-        """Kernel launches of the layers: each product call's (q8_plan_launches: 1, or 2 when the planner splits a
-        plain product in two); the gated pair one; under --fused, o and down as residual norms (the product, then
-        the norm's own launch unless the one-launch fold is selected)."""
+        """Kernel launches of the layers: each product call's (q8_plan_launches, q8_plan_glu_launches: 1, or 2 when
+        the planner splits a launch in two); under --fused, o and down as residual norms (the product, then the norm's
+        own launch unless the one-launch fold is selected)."""
         import q8_block_quantized_gemv_gb300 as q8
         n = 0
         for _, gis in self.layer_calls():
             if self.glu and len(gis) == 2:
-                n += 1
+                n += q8.plan_glu_launches(self.m, self.shapes[gis[0]][0], FFN, q8_act=self.q8act)
             elif self.fused and len(gis) == 1:
                 n += q8.residual_norm_launches()
             else:

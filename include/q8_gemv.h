@@ -267,6 +267,11 @@ q8_status q8_gemv_parts(const void *x, const q8_part *parts, int nparts, int m, 
  * (sizes the call would reject), -Q8_ERR_CUDA (the device cannot be queried). */
 int q8_plan_launches(int m, int K, const int *Ns, int nparts, unsigned int flags);
 
+/* q8_plan_launches for a q8_gemv_glu(_ex) call of these sizes (flags as that call takes them, Q8_FLAG_TILED among
+ * them): 1, or 2 when the planner splits the gated pair in two.  Returns the count or a negative status as
+ * q8_plan_launches. */
+int q8_plan_glu_launches(int m, int K, int N, unsigned int flags);
+
 /* The quantized form of an activation (source: "plan.rs", `QBLOCK`: 32 consecutive values of the form share one
  * scale; `Buffer::quantized`: int8 codes plus one scale for every 32; `Launch::projected_input`: a product over
  * checkpoint rows takes its activation in this form unless the numerics are the exact ones).  One buffer of
@@ -326,9 +331,10 @@ q8_status q8_device_fault(unsigned int *fault, int clear);
  *                      run on the tcgen05 GEMM whatever the weight's width.  Environment: Q8_GEMM (0 or 1).
  *   Q8_TUNE_NORM_FOLD  0: the residual norm as a launch of its own (default); 1: the one-launch fold, where the
  *                      product's last CTA runs the norm.  Environment: Q8_NORM_LAUNCH=0 selects 1.
- *   Q8_TUNE_SPLIT      1: the planner may run a plain product (q8_gemv, q8_gemv_argmax, q8_gemv_parts; m <= 16) as
- *                      two launches, the column tiles that do not fill the SMs evenly given their own K split
- *                      (default); 0: always one launch.  Environment: Q8_SPLIT=0 selects 0. */
+ *   Q8_TUNE_SPLIT      1: the planner may run a plain product (q8_gemv, q8_gemv_argmax, q8_gemv_parts) or a gated
+ *                      pair (q8_gemv_glu) of m <= 16 rows as two launches, the column tiles that do not fill the
+ *                      SMs evenly given their own K split (default); 0: always one launch.  Environment: Q8_SPLIT=0
+ *                      selects 0. */
 #define Q8_TUNE_KSPLIT 0
 #define Q8_TUNE_GEMM 1
 #define Q8_TUNE_NORM_FOLD 2

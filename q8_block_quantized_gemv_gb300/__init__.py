@@ -60,6 +60,7 @@ SIGNATURES = {
     "q8_gemv_residual_norm_noalloc": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, ctypes.c_uint,
                                           _P]),
     "q8_plan_launches": (_I, [_I, _I, _P, _I, ctypes.c_uint]),
+    "q8_plan_glu_launches": (_I, [_I, _I, _I, ctypes.c_uint]),
     "q8_set_tuning": (_I, [_I, _I]),
     "q8_get_tuning": (_I, [_I]),
 }
@@ -312,6 +313,14 @@ def plan_launches(m: int, K: int, Ns, tiled: bool = True, q8_act: bool = False) 
     n = int(lib().q8_plan_launches(int(m), int(K), ctypes.cast(arr, ctypes.c_void_p), len(Ns), flags))
     if n < 0:
         raise Q8Error(-n, "q8_plan_launches")
+    return n
+
+
+def plan_glu_launches(m: int, K: int, N: int, q8_act: bool = False) -> int:
+    """How many kernels a gemv_glu call of these sizes launches on the current device (q8_plan_glu_launches)."""
+    n = int(lib().q8_plan_glu_launches(int(m), int(K), int(N), FLAG_TILED | (FLAG_Q8_ACT if q8_act else 0)))
+    if n < 0:
+        raise Q8Error(-n, "q8_plan_glu_launches")
     return n
 
 

@@ -461,6 +461,56 @@ int plan_glu(long long tiles, int nb, int sms, int m, bool qact) {
     return (int)ks;
 }
 
+// The two-launch split of a gated pair (as plan_split for a plain product, over tiles of two CTAs each: the gate's
+// and the up projection's, a cluster of 2 x ks): the first launch takes SMs / 2 tiles (one CTA per SM) or the whole
+// waves, the second the rest with K split across clusters of 2 x ks_b (ks_b at most 4).  One row group, no forced K
+// split.
+Split plan_split_glu(long long tiles, int nb, int m, bool qact, int sms, int ks) {
+    Split none;
+    if (tuning(Q8_TUNE_SPLIT) == 0 || tuning(Q8_TUNE_KSPLIT) != 0 || ks != 1 || m > q8::kGroupRows || sms <= 0)
+        return none;
+    const long long slots = (long long)q8::stream_ctas_per_sm(m, qact) * sms;
+    const long long ctas = 2 * tiles;
+    long long ta;
+    bool co;
+    if (slots > sms && ctas > sms && ctas < slots) {
+        ta = sms / 2;
+        co = true;
+    } else if (ctas > slots && ctas % slots != 0) {
+        ta = ctas / slots * slots / 2;
+        co = false;
+    } else {
+        return none;
+    }
+    const long long tb = tiles - ta;
+    long long kb = (co ? sms : slots) / (2 * tb);
+    if (kb > 4) kb = 4;
+    if (kb > nb) kb = nb;
+    while (kb > 1) {
+        const int fit = q8::stream_max_clusters(m, qact, (int)(2 * kb));
+        if (fit > 0 && tb <= (co ? fit / 2 : fit)) break;
+        --kb;
+    }
+    if (kb < 2) return none;
+    Split sp;
+    sp.tiles_a = (int)ta;
+    sp.ks_b = (int)kb;
+    sp.one_per_sm = co;
+    return sp;
+}
+
+extern "C" int q8_plan_glu_launches(int m, int K, int N, unsigned int flags) {
+    if (!flags_ok(flags) || !(flags & Q8_FLAG_TILED)) return -Q8_ERR_ARG;
+    if (m < 1 || m > Q8_MAX_CHUNK || K <= 0 || K % Q8_BLOCK != 0 || N <= 0 || q8_tiled_n(N) < 0) return -Q8_ERR_SHAPE;
+    int sms = 0;
+    if (sm_count(&sms) != 0) return -Q8_ERR_CUDA;
+    const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
+    const int groups = (m + q8::kGroupRows - 1) / q8::kGroupRows;
+    const long long tiles = (long long)tiles_of(N) * groups;
+    const int ks = plan_glu(tiles, K / Q8_BLOCK, sms, m, qact);
+    return plan_split_glu(tiles, K / Q8_BLOCK, m, qact, sms, ks).tiles_a > 0 ? 2 : 1;
+}
+
 extern "C" q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float *sg, const int8_t *qu,
                                     const float *su, float *out, void *out_bf16, void *out_q8, int m, int K, int N,
                                     unsigned int flags, q8_stream_t stream) {
@@ -508,10 +558,28 @@ extern "C" q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float
         a.yq = static_cast<unsigned char *>(out_q8);
         a.yd = reinterpret_cast<float *>(a.yq + (size_t)m * Np);
     }
-    a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms, m, (flags & Q8_FLAG_Q8_ACT) != 0);
-    cudaError_t ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true,
-                                       (flags & Q8_FLAG_CONSTANT_WEIGHTS) ? q8::kModePrefetch : 0,
-                                       (flags & Q8_FLAG_Q8_ACT) != 0);
+    const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
+    const int mode = (flags & Q8_FLAG_CONSTANT_WEIGHTS) ? q8::kModePrefetch : 0;
+    a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms, m, qact);
+    const Split sp = plan_split_glu((long long)tiles * groups, K / Q8_BLOCK, m, qact, sms, a.ksplit);
+    cudaError_t ce;
+    if (sp.tiles_a > 0) {
+        q8::StreamGrid ga;
+        ga.ntiles = 2 * sp.tiles_a;  // grid columns: two CTAs a tile
+        ga.one_per_sm = sp.one_per_sm;
+        ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true, mode | q8::kModeRelease, qact, false,
+                               ga);
+        if (ce != cudaSuccess) return cuda_fail(ce);
+        Args c = a;
+        c.tile0 = 2 * sp.tiles_a;
+        c.ksplit = sp.ks_b;
+        q8::StreamGrid gb;
+        gb.ntiles = 2 * (tiles - sp.tiles_a);
+        ce = q8::launch_stream(c, pt, q8::kEpiGlu, (cudaStream_t)stream, true, mode | q8::kModeDeferWait, qact, false,
+                               gb);
+    } else {
+        ce = q8::launch_stream(a, pt, q8::kEpiGlu, (cudaStream_t)stream, true, mode, qact);
+    }
     if (ce != cudaSuccess) return cuda_fail(ce);
     return Q8_OK;
 }

@@ -45,8 +45,8 @@ struct Args {
     int groups;                // set on the device: the launch's row groups (ceil(m / 16))
     unsigned char *yq;         // gated pair / norm: the quantized form of the bf16 output, codes [m][Np] (or null)
     float *yd;                 //   and its scales [m][Np / 32]
-    int tile0;                 // stream kernels: the column tile of grid x = 0; nonzero only for the second launch of
-                               // a store or arg-max launch split in two (it starts past the first one's tiles)
+    int tile0;                 // stream kernels: added to grid x (column tiles; the gated pair: its CTAs, two a
+                               // tile, so even); nonzero only for the second launch of a launch split in two
 };
 
 constexpr int kGroupRows = 16;   // activation rows of one row group (m > 16 runs ceil(m / 16) groups in one grid)
@@ -137,7 +137,7 @@ template <int EPI, bool GROUPS> __device__ __forceinline__ void apply_cta_group(
         return;
     }
     const int groups = row_groups(a);
-    const int x = (EPI == kEpiGlu ? (int)(blockIdx.x >> 1) : (int)blockIdx.x) + a.tile0;
+    const int x = EPI == kEpiGlu ? (int)(blockIdx.x + a.tile0) >> 1 : (int)blockIdx.x + a.tile0;
     apply_group(a, x % groups, groups);
 }
 

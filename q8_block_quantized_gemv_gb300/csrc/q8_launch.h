@@ -62,9 +62,9 @@ constexpr int kModePrefetch = 1;   // request the first ring stages' weights bef
 constexpr int kModeRelease = 2;    // release the next launch right after the dependency wait, not after the main loop
 constexpr int kModeDeferWait = 4;  // no dependency wait before the main loop (the launch before released this one
                                    // only after its own wait); wait just before exiting instead
-// A stream launch's grid: every column tile of the parts (ntiles = 0), or ntiles of them from Args::tile0 (m <= 16,
-// one row group); one_per_sm asks for enough shared memory that an SM holds one CTA of the launch and still one CTA
-// of 8 warps of another.
+// A stream launch's grid: every column tile of the parts (ntiles = 0), or ntiles grid columns from Args::tile0 (m <= 16,
+// one row group; the gated pair has two columns a tile); one_per_sm asks for enough shared memory that an SM holds one
+// CTA of the launch and still one CTA of 8 warps of another.
 struct StreamGrid {
     int ntiles = 0;
     bool one_per_sm = false;

@@ -912,8 +912,9 @@ template <int EPI>
 cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t stream, bool pdl, int mode, bool qact,
                               bool rowmajor, StreamGrid grid) {
     const bool pair = EPI == kEpiGlu;
-    if ((grid.ntiles > 0 || a.tile0 != 0) && (pair || EPI == kEpiNorm || a.m > kGroupRows))
-        return cudaErrorInvalidValue;  // a part of the tiles: plain store and arg-max launches of one row group
+    if ((grid.ntiles > 0 || a.tile0 != 0) && (EPI == kEpiNorm || a.m > kGroupRows || (pair && (a.tile0 & 1))))
+        return cudaErrorInvalidValue;  // a part of the tiles: store, arg-max and gated-pair launches of one row group
+
     auto go = [&](auto kernel) { return launch_stream_kernel(kernel, kWarpsS, a, pt, stream, pdl, mode, pair, grid); };
     auto go8 = [&](auto kernel) {
         return launch_stream_kernel(kernel, kWarps8, a, pt, stream, pdl, mode, pair, grid);

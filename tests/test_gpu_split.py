@@ -241,3 +241,32 @@ def test_launch_after_the_pair_overwrites_its_input(dev, sms, m, graph):
     y_o, a_o = oracle.gemv(x, host[0][0], host[0][1])
     _assert_close(y.cpu().numpy()[:, :Ns[0]], y_o[:, :Ns[0]], a_o[:, :Ns[0]], f"m={m} product over the original x")
     assert not torch.equal(xd, x0), "the norm did not write its output over x"
+
+
+@pytest.mark.parametrize("m", [1, 4, 16])
+def test_split_gated_pair_matches_the_oracle(dev, sms, m, tune):
+    """The gated pair over 80 column tiles (160 CTAs, two a tile): split in two on 152 SMs (one tile pair per two SMs,
+    then the rest with K split over clusters of 2 x ks), every fp32 output against the oracle's silu(g) * u within the
+    carried bound, the bf16 copy the fp32 output rounded; split and unsplit both, the split twice bit-identical."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    from test_gpu_parity import _glu_check, _to_dev
+    K, N = 512, 10240
+    x, qg, sg = si.case(m, K, N, si.case_seed(20, m))
+    _, qu, su = si.case(1, K, N, si.case_seed(21, m))
+    xd, qgd, sgd = _to_dev(torch, x, qg, sg)
+    _, qud, sud = _to_dev(torch, x, qu, su)
+    gate, up = q8.tile_device(qgd, sgd, N), q8.tile_device(qud, sud, N)
+    if sms == 152:
+        assert q8.plan_glu_launches(m, K, N) == 2, m
+    runs = []
+    for split in (1, 1, 0):
+        tune(split=split)
+        if split == 0:
+            assert q8.plan_glu_launches(m, K, N) == 1
+        out, outb = q8.gemv_glu(xd, gate, up, N, want=("f32", "bf16"), constant_weights=True)
+        torch.cuda.synchronize()
+        runs.append((out.cpu().numpy(), outb.view(torch.int16).cpu().numpy().view(np.uint16)))
+    for r, label in ((0, "split"), (2, "one launch")):
+        _glu_check(runs[r][0], runs[r][1], x, qg, sg, qu, su, N, what=f"m={m} {label}")
+    assert np.array_equal(runs[0][0].view(np.uint32), runs[1][0].view(np.uint32)), "split not reproducible"

@@ -474,6 +474,15 @@ def test_plan_launches_argument_errors(lib):
     assert call(1, 64, p, 2, 2) in (-5, 1, 2)
 
 
+def test_plan_glu_launches_argument_errors(lib):
+    """q8_plan_glu_launches rejects what q8_gemv_glu_ex would (the tiled flag is required) before any device query."""
+    call = lib.q8_plan_glu_launches
+    assert call(1, 64, 96, 0) == -1 and call(1, 64, 96, 0x80 | 2) == -1
+    assert call(0, 64, 96, 2) == -2 and call(513, 64, 96, 2) == -2 and call(1, 33, 96, 2) == -2
+    assert call(1, 64, 0, 2) == -2
+    assert call(1, 64, 96, 2) in (-5, 1, 2)
+
+
 def test_residual_norm_noalloc_argument_errors(lib):
     """The entry point that allocates nothing rejects, before any CUDA call, rows beyond its static counters and the
     arguments the residual norm rejects."""
