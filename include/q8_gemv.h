@@ -154,7 +154,8 @@ q8_status q8_tile_device(const int8_t *q, const float *s, int K, int N, int8_t *
  * out = act(x.wg + bg) * (x.wu + bu), silu gating (SwiGLU) by default; here without biases):
  *     out[r, n] = silu(g[r, n]) * u[r, n],   g = x . Wg,  u = x . Wu,   silu(g) = g / (1 + exp(-g)),
  * g and u each the Q8_0 product of q8_gemv (fp32 accumulation), silu and the product in fp32 (CUDA's expf, IEEE
- * division).  One launch: the gate's and the up projection's CTAs of a column tile run side by side in a cluster.
+ * division).  One launch (two when the planner splits it, Q8_TUNE_SPLIT, q8_plan_glu_launches): the gate's and the
+ * up projection's CTAs of a column tile run side by side in a cluster.
  *   x         device, bf16 [m][K], 16-byte aligned
  *   qg, sg    device, the gate's weight in the tiled storage (q8_tile), 16-byte aligned
  *   qu, su    device, the up projection's weight, tiled, 16-byte aligned
@@ -252,7 +253,8 @@ typedef struct q8_part {
  * other).
  *   x      device bf16 [m][K], read once for all parts       parts  host array of nparts q8_part (read during the call)
  *   1 <= nparts <= Q8_MAX_PARTS; every part has the same K; N may differ.  Each y_p is as q8_gemv writes it.
- * The parts run as one kernel launch, row-major or (Q8_FLAG_TILED) in the q8_tile layout.  Flags and errors as
+ * The parts run as one kernel launch (two when the planner splits it, Q8_TUNE_SPLIT, q8_plan_launches), row-major
+ * or (Q8_FLAG_TILED) in the q8_tile layout.  Flags and errors as
  * q8_gemv_ex; an output overlapping x, a weight or another output is Q8_ERR_ARG. */
 q8_status q8_gemv_parts(const void *x, const q8_part *parts, int nparts, int m, int K, unsigned int flags,
                         q8_stream_t stream);
