@@ -194,9 +194,9 @@ bool use_gemm(int m, int epi, bool qact, long long col_tiles) {
     return col_tiles * ((m + 127) / 128) * 4 >= 64;
 }
 
-// A plain product (store or arg-max, at most 16 rows) whose one-launch plan has no K split but whose column tiles do
-// not fill the resident slots evenly runs as two launches on the stream (a balance of the "plan.rs" `split_counts`
-// kind: every SM gets about the same share of the blocks):
+// A plain product (store or arg-max) or a gated pair of at most 16 rows whose one-launch plan has no K split but whose
+// column tiles do not fill the resident slots evenly runs as two launches on the stream (a balance of the "plan.rs"
+// `split_counts` kind: every SM gets about the same share of the blocks):
 //   - tiles > SMs but below the slots (two CTAs per SM): the first launch takes one tile per SM, its CTAs held to one
 //     per SM by their shared-memory size; the second takes the other tiles with K split over clusters of ks CTAs,
 //     sized to the free half of every SM.  The gate/up pair (224 tiles on 152 SMs) then gives every SM 128 + 64 K
@@ -211,29 +211,33 @@ struct Split {
     int ks_b = 1;     // the second launch's K split
     bool one_per_sm = false;
 };
-Split plan_split(long long tiles, int nb, int m, bool qact, int sms, int ks) {
+// pair: the gated pair, whose tiles are two CTAs each (the gate's and the up projection's, a cluster of 2 x ks, ks at
+// most 4); else one CTA a tile (ks at most 8).
+Split plan_split(long long tiles, int nb, int m, bool qact, int sms, int ks, bool pair = false) {
     Split none;
     // (a forced K split keeps one launch, so that it applies to every tile)
     if (tuning(Q8_TUNE_SPLIT) == 0 || tuning(Q8_TUNE_KSPLIT) != 0 || ks != 1 || m > q8::kGroupRows || sms <= 0)
         return none;
+    const long long per = pair ? 2 : 1;  // CTAs a tile
     const long long slots = (long long)q8::stream_ctas_per_sm(m, qact) * sms;
+    const long long ctas = per * tiles;
     long long ta;
     bool co;
-    if (slots > sms && tiles > sms && tiles < slots) {
-        ta = sms;
+    if (slots > sms && ctas > sms && ctas < slots) {
+        ta = sms / per;
         co = true;
-    } else if (tiles > slots && tiles % slots != 0) {
-        ta = tiles / slots * slots;
+    } else if (ctas > slots && ctas % slots != 0) {
+        ta = ctas / slots * slots / per;
         co = false;
     } else {
         return none;
     }
     const long long tb = tiles - ta;
-    long long kb = (co ? sms : slots) / tb;
-    if (kb > 8) kb = 8;
+    long long kb = (co ? sms : slots) / (per * tb);
+    if (kb > 8 / per) kb = 8 / per;
     if (kb > nb) kb = nb;
     while (kb > 1) {  // clusters that are all resident at once (beside the first launch's CTAs: about half as many)
-        const int fit = q8::stream_max_clusters(m, qact, (int)kb);
+        const int fit = q8::stream_max_clusters(m, qact, (int)(per * kb));
         if (fit > 0 && tb <= (co ? fit / 2 : fit)) break;
         --kb;
     }
@@ -461,44 +465,6 @@ int plan_glu(long long tiles, int nb, int sms, int m, bool qact) {
     return (int)ks;
 }
 
-// The two-launch split of a gated pair (as plan_split for a plain product, over tiles of two CTAs each: the gate's
-// and the up projection's, a cluster of 2 x ks): the first launch takes SMs / 2 tiles (one CTA per SM) or the whole
-// waves, the second the rest with K split across clusters of 2 x ks_b (ks_b at most 4).  One row group, no forced K
-// split.
-Split plan_split_glu(long long tiles, int nb, int m, bool qact, int sms, int ks) {
-    Split none;
-    if (tuning(Q8_TUNE_SPLIT) == 0 || tuning(Q8_TUNE_KSPLIT) != 0 || ks != 1 || m > q8::kGroupRows || sms <= 0)
-        return none;
-    const long long slots = (long long)q8::stream_ctas_per_sm(m, qact) * sms;
-    const long long ctas = 2 * tiles;
-    long long ta;
-    bool co;
-    if (slots > sms && ctas > sms && ctas < slots) {
-        ta = sms / 2;
-        co = true;
-    } else if (ctas > slots && ctas % slots != 0) {
-        ta = ctas / slots * slots / 2;
-        co = false;
-    } else {
-        return none;
-    }
-    const long long tb = tiles - ta;
-    long long kb = (co ? sms : slots) / (2 * tb);
-    if (kb > 4) kb = 4;
-    if (kb > nb) kb = nb;
-    while (kb > 1) {
-        const int fit = q8::stream_max_clusters(m, qact, (int)(2 * kb));
-        if (fit > 0 && tb <= (co ? fit / 2 : fit)) break;
-        --kb;
-    }
-    if (kb < 2) return none;
-    Split sp;
-    sp.tiles_a = (int)ta;
-    sp.ks_b = (int)kb;
-    sp.one_per_sm = co;
-    return sp;
-}
-
 extern "C" int q8_plan_glu_launches(int m, int K, int N, unsigned int flags) {
     if (!flags_ok(flags) || !(flags & Q8_FLAG_TILED)) return -Q8_ERR_ARG;
     if (m < 1 || m > Q8_MAX_CHUNK || K <= 0 || K % Q8_BLOCK != 0 || N <= 0 || q8_tiled_n(N) < 0) return -Q8_ERR_SHAPE;
@@ -508,7 +474,7 @@ extern "C" int q8_plan_glu_launches(int m, int K, int N, unsigned int flags) {
     const int groups = (m + q8::kGroupRows - 1) / q8::kGroupRows;
     const long long tiles = (long long)tiles_of(N) * groups;
     const int ks = plan_glu(tiles, K / Q8_BLOCK, sms, m, qact);
-    return plan_split_glu(tiles, K / Q8_BLOCK, m, qact, sms, ks).tiles_a > 0 ? 2 : 1;
+    return plan_split(tiles, K / Q8_BLOCK, m, qact, sms, ks, true).tiles_a > 0 ? 2 : 1;
 }
 
 extern "C" q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float *sg, const int8_t *qu,
@@ -561,7 +527,7 @@ extern "C" q8_status q8_gemv_glu_ex(const void *x, const int8_t *qg, const float
     const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
     const int mode = (flags & Q8_FLAG_CONSTANT_WEIGHTS) ? q8::kModePrefetch : 0;
     a.ksplit = plan_glu((long long)tiles * groups, K / Q8_BLOCK, sms, m, qact);
-    const Split sp = plan_split_glu((long long)tiles * groups, K / Q8_BLOCK, m, qact, sms, a.ksplit);
+    const Split sp = plan_split((long long)tiles * groups, K / Q8_BLOCK, m, qact, sms, a.ksplit, true);
     cudaError_t ce;
     if (sp.tiles_a > 0) {
         q8::StreamGrid ga;
