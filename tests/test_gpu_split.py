@@ -270,3 +270,63 @@ def test_split_gated_pair_matches_the_oracle(dev, sms, m, tune):
     for r, label in ((0, "split"), (2, "one launch")):
         _glu_check(runs[r][0], runs[r][1], x, qg, sg, qu, su, N, what=f"m={m} {label}")
     assert np.array_equal(runs[0][0].view(np.uint32), runs[1][0].view(np.uint32)), "split not reproducible"
+
+
+@pytest.mark.parametrize("m", [1, 2, 4, 16])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_split_quantized_activations_match_the_oracle(dev, sms, case, m, tune):
+    """Both split cases over quantized activations (Q8_FLAG_Q8_ACT: the dp4a CUDA-core kernel at 1 and 2 rows, the
+    integer-exact tensor-core kernels above): every output against the oracle's quantized product, split and
+    unsplit, the split twice bit-identical."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    from test_gpu_quant_act import _act_from
+    K, Ns = CASES[case]
+    x, _, _ = si.case(m, K, 32, si.case_seed(22, m, len(Ns)))
+    xq, xd = oracle.quantize_act(x)
+    host, devw = _weights(torch, K, Ns, si.case_seed(23, m, K), True)
+    xa = _act_from(torch, xq, xd)
+    if sms == 152:
+        assert q8.plan_launches(m, K, Ns, q8_act=True) == 2, (case, m)
+    runs = []
+    for split in (1, 1, 0):
+        tune(split=split)
+        ys = q8.gemv_parts(xa, devw, tiled=True, constant_weights=True)
+        torch.cuda.synchronize()
+        runs.append([y.cpu().numpy() for y in ys])
+    for i, (q, s) in enumerate(host):
+        N = Ns[i]
+        y_o, a_o = oracle.gemv_q8act(xq, xd, q, s)
+        for r, label in ((0, "split"), (2, "one launch")):
+            _assert_close(runs[r][i][:, :N], y_o[:, :N], a_o[:, :N], f"{case} m={m} part {i} {label}")
+            assert np.all(runs[r][i][:, N:] == 0.0)
+        assert np.array_equal(runs[0][i].view(np.uint32), runs[1][i].view(np.uint32)), "split not reproducible"
+
+
+@pytest.mark.parametrize("m", [1, 16])
+def test_split_argmax_quantized_activations(dev, sms, m):
+    """The arg-max over the waves case with quantized activations and a planted winner per row (one in each launch of
+    the split): exact indices, the logits within the bound."""
+    torch = dev
+    import q8_block_quantized_gemv_gb300 as q8
+    from test_gpu_quant_act import _act_from
+    K, (N,) = CASES["waves"]
+    x, q, s = si.case(m, K, N, si.case_seed(24, m))
+    xq, xd = oracle.quantize_act(x)
+    # winners spread over the first launch's tiles and the second's (tiles 304 .. 329 hold columns 38912 ..)
+    win = np.where(np.arange(m) % 2 == 0, (np.arange(m) * 7919 + 123) % 38912, 38912 + (np.arange(m) * 131) % 3328)
+    for r in range(m):
+        # the winner's column: the row's code signs at full scale and the weight's largest block scale (with K = 256,
+        # eight blocks, a random column with large scales could otherwise beat a planted one with small ones)
+        q[:, win[r]] = np.where(xq[r] >= 0, 127, -127)
+        s[:, win[r]] = s.max()
+    y_o, a_o = oracle.gemv_q8act(xq, xd, q, s)
+    assert np.array_equal(oracle.argmax(y_o, N), win)
+    if sms == 152:
+        assert q8.plan_launches(m, K, (N,), q8_act=True) == 2
+    qt, st = q8.tile_device(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), N)
+    logits = torch.empty((m, oracle.padded_n(N)), dtype=torch.float32, device="cuda")
+    idx = q8.gemv_argmax(_act_from(torch, xq, xd), qt, st, N, logits=logits, tiled=True, constant_weights=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), win)
+    _assert_close(logits.cpu().numpy()[:, :N], y_o[:, :N], a_o[:, :N], f"m={m}")
