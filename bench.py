@@ -441,6 +441,28 @@ class Chain:
             self.run_head()
         torch.cuda.synchronize()
 
+    def capture_second_buffer(self):
+        """A second set of the step's graphs over a second activation buffer (x_all2), so that the end-to-end loop can
+        copy step s + 1's inputs from the host while step s runs on the other buffer."""
+        torch = self.torch
+        first = (self.x_all, self.x)
+        self.x_all2 = torch.empty_like(self.x_all)
+        self.x_all2.copy_(self.x_all)
+        off, self.x = 0, []
+        for xv in first[1]:
+            self.x.append(self.x_all2[off:off + xv.numel()].view(xv.shape))
+            off += xv.numel()
+        try:
+            self.g_layers2, self.g_head2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.g_layers2):
+                self.run_layers()
+            with torch.cuda.graph(self.g_head2):
+                self.run_head()
+            torch.cuda.synchronize()
+        finally:
+            self.x_all, self.x = first
+        self.x_all_bufs = (self.x_all, self.x_all2)
+
     def layer_launches(self):
         """Kernel launches of the layers: each product call's (q8_plan_launches, q8_plan_glu_launches: 1, or 2 when
         the planner splits a launch in two); under --fused, o and down as residual norms (the product, then the norm's
@@ -540,24 +562,43 @@ def measure_chain(args, torch, weights, m, world, local_rank, barrier, max_over_
     ms = max_over_ranks(ms)
     bytes_step = chain.layer_bytes() + chain.head_bytes()
 
-    # ---- end-to-end: host activations in, the step's tokens out, every step ----
+    # ---- end-to-end: host activations in, the step's tokens out, every step.  Two activation buffers, each with its
+    # own graphs: a copy stream brings step s + 1's inputs from pinned host memory into one while step s runs on the
+    # other (the copy waits for the step that last read that buffer; the step waits for its copy). ----
     x_host = torch.empty(chain.x_all.shape, dtype=torch.bfloat16, pin_memory=True)
     x_host.copy_(chain.x_all.cpu())
     idx_host = torch.empty((m,), dtype=torch.int64, pin_memory=True)
-    for _ in range(2):
-        chain.x_all.copy_(x_host, non_blocking=True)
-        chain.g_layers.replay()
-        chain.g_head.replay()
-        idx_host.copy_(chain.idx, non_blocking=True)
+    chain.capture_second_buffer()
+    graphs = ((chain.g_layers, chain.g_head), (chain.g_layers2, chain.g_head2))
+    side = torch.cuda.Stream()
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    used = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def e2e_steps(k):
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            side.wait_event(used[0])
+            chain.x_all_bufs[0].copy_(x_host, non_blocking=True)
+            copied[0].record(side)
+        for i in range(k):
+            b = i % 2
+            stream.wait_event(copied[b])
+            graphs[b][0].replay()
+            graphs[b][1].replay()
+            idx_host.copy_(chain.idx, non_blocking=True)
+            used[b].record(stream)
+            if i + 1 < k:
+                with torch.cuda.stream(side):
+                    side.wait_event(used[1 - b])
+                    chain.x_all_bufs[1 - b].copy_(x_host, non_blocking=True)
+                    copied[1 - b].record(side)
+
+    e2e_steps(2)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        chain.x_all.copy_(x_host, non_blocking=True)
-        chain.g_layers.replay()
-        chain.g_head.replay()
-        idx_host.copy_(chain.idx, non_blocking=True)
+    e2e_steps(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
