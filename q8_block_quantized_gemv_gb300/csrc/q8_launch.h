@@ -64,7 +64,7 @@ constexpr int kModeDeferWait = 4;  // no dependency wait before the main loop (t
                                    // only after its own wait); wait just before exiting instead
 // A stream launch's grid: every column tile of the parts (ntiles = 0), or ntiles grid columns from Args::tile0 (m <= 16,
 // one row group; the gated pair has two columns a tile); one_per_sm asks for enough shared memory that an SM holds one
-// CTA of the launch and still one CTA of 8 warps of another.
+// CTA of the launch and still one ordinary CTA of the same kernel (the kernels that run two CTAs per SM).
 struct StreamGrid {
     int ntiles = 0;
     bool one_per_sm = false;

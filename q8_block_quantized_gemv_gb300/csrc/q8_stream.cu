@@ -11,11 +11,13 @@
 // A CTA owns one 128-column tile and a range of its K blocks (split across a thread-block cluster when N is too
 // narrow to fill the SMs); its warps split that range again into contiguous runs.  Each warp keeps a private ring of
 // three stages in shared memory, filled with cp.async (16 bytes a lane, bypassing L1): it issues block i + 2 while it
-// computes block i, so about two units per warp -- 110 to 150 KB per SM -- are in flight without holding registers.
-// The 16-row and CUDA-core kernels run 8 warps a CTA, two CTAs per SM (128 registers a thread); the 8-row kernel
-// runs 12 warps, one CTA per SM, so that a thread may hold up to 168 registers (measured on GB300, 10-28 % faster per
-// launch at 4 and 8 rows than 8 warps at the 128-register cap; the 16-row kernel gains less there and loses on wide
-// launches, whose one-CTA-per-SM waves are twice as many).
+// computes block i, so about two units per warp -- 80 to 150 KB per SM -- are in flight without holding registers.
+// The CUDA-core kernel runs 8 warps a CTA, two CTAs per SM (128 registers a thread).  The MMA kernels hold more
+// registers a thread, up to 168: the 8-row kernel runs 12 warps, one CTA per SM (measured on GB300, 10-28 % faster
+// per launch at 4 and 8 rows than 8 warps at the 128-register cap), and the 16-row kernel 6 warps, two CTAs per SM
+// (measured on GB300: the 16-row decode chain 3,690 -> 3,850 GB/s against 8 warps at 128 registers, which spilled;
+// 5 warps at 200 registers and 4 at 255 were slower, and so was one 12-warp CTA per SM, whose whole-SM CTAs cannot
+// start beside the previous launch's).
 //
 // The block's contraction runs on m16n8k16 MMAs with the activations as the A operand (rows r and r + 8 of the lane's
 // fragment are activation rows g and g + 8) and the weights as B (one 8-column slice per MMA, fp32 accumulators):
@@ -50,10 +52,11 @@ namespace q8 {
 
 namespace {
 
-constexpr int kWarpsS = 8;   // warps of a CTA: 16-row and CUDA-core kernels (two CTAs per SM)
+constexpr int kWarpsS = 8;   // warps of a CTA: the CUDA-core kernel (two CTAs per SM)
 constexpr int kWarps8 = 12;  //   the 8-row kernel (one CTA per SM)
+constexpr int kWarps16 = 6;  //   the 16-row kernel (two CTAs per SM)
 constexpr int kThreadsS = 32 * kWarpsS;
-__host__ __device__ constexpr int stream_warps(bool rows16) { return rows16 ? kWarpsS : kWarps8; }
+__host__ __device__ constexpr int stream_warps(bool rows16) { return rows16 ? kWarps16 : kWarps8; }
 constexpr int kUnit = kBlock * kTmaColumns;  // 4096 bytes of values per 32 x 128 unit
 constexpr int kUnitScales = kTmaColumns;     // 128 fp32
 constexpr int kStageS = kUnit + kUnitScales * 4;
@@ -802,14 +805,17 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     if (mode & kModeDeferWait) asm volatile("griddepcontrol.wait;" ::: "memory");  // the first half has completed
 }
 
-static_assert(finish_smem_n(kWarpsS, 16, kTmaColumns, kSlabStride) <= kSmemS, "the epilogue fits in the rings");
-static_assert((kWarpsS * 16 * kSlabStride + 2 * 16 * kTmaColumns) * 4 <= kSmemS, "the gated pair's epilogue fits");
-static_assert(2 * kSmemS <= 227 * 1024, "two CTAs per SM");
+static_assert(finish_smem_n(kWarps16, 16, kTmaColumns, kSlabStride) <= stream_smem(kWarps16), "the epilogue fits");
+static_assert((kWarps16 * 16 * kSlabStride + 2 * 16 * kTmaColumns) * 4 <= stream_smem(kWarps16),
+              "the gated pair's epilogue fits");
+static_assert(finish_smem_n(kWarpsS, 2, kTmaColumns) <= kSmemS, "the CUDA-core kernel's epilogue fits");
+static_assert(2 * kSmemS <= 227 * 1024 && 2 * stream_smem(kWarps16) <= 227 * 1024, "two CTAs per SM");
 static_assert(finish_smem_n(kWarps8, 8, kTmaColumns, kSlabStride) <= stream_smem(kWarps8), "8-row epilogue fits");
 static_assert((kWarps8 * 8 * kSlabStride + 2 * 8 * kTmaColumns) * 4 <= stream_smem(kWarps8), "8-row gated pair fits");
 static_assert(stream_smem(kWarps8) <= 227 * 1024, "one 8-row CTA per SM");
-// The shared memory of a launch held to one CTA per SM beside one ordinary CTA of 8 warps: two such CTAs (each with
-// its 1 KB reserve) exceed the SM's 228 KB, one of them and an ordinary one do not.
+// The shared memory of a launch held to one CTA per SM beside one ordinary CTA of the two-per-SM kernels (the
+// CUDA-core kernel's 8 warps, the 16-row kernel's 6): two such CTAs (each with its 1 KB reserve) exceed the SM's
+// 228 KB, one of them and an ordinary one do not.
 constexpr int kSmemOnePerSm = 114 * 1024;
 static_assert(2 * (kSmemOnePerSm + 1024) > 228 * 1024 && kSmemOnePerSm + kSmemS + 2 * 1024 <= 228 * 1024,
               "one such CTA and one ordinary CTA per SM");
@@ -817,9 +823,10 @@ static_assert(2 * (kSmemOnePerSm + 1024) > 228 * 1024 && kSmemOnePerSm + kSmemS 
 template <typename Kernel>
 cudaError_t launch_stream_kernel(Kernel kernel, int warps, const Args &a, const Parts &pt, cudaStream_t stream,
                                  bool pdl, int mode, bool pair, StreamGrid grid) {
-    const int smem = grid.one_per_sm && warps == kWarpsS ? kSmemOnePerSm : stream_smem(warps);
+    const bool two_per_sm = warps != kWarps8;
+    const int smem = grid.one_per_sm && two_per_sm ? kSmemOnePerSm : stream_smem(warps);
     // the attribute is the largest size any launch of the kernel asks for, so that concurrent callers agree on it
-    const int smem_max = warps == kWarpsS ? kSmemOnePerSm : stream_smem(warps);
+    const int smem_max = two_per_sm ? kSmemOnePerSm : stream_smem(warps);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -874,19 +881,21 @@ int stream_ctas_per_sm(int m, bool qact) { return rows8_family(m, qact) ? 1 : 2;
 int stream_max_clusters(int m, bool qact, int ks) {
     // Clusters of ks CTAs are placed within one GPC, so fewer of them fit at once than slots / ks.  Asked once per
     // device, kernel shape and size (a deterministic answer: concurrent first calls store the same value); the stream
-    // kernels of one shape (8-row: 12 warps, one CTA per SM; the others: 8 warps, two) have the same block size,
-    // register cap and shared memory.
-    static std::atomic<int> cache[64][2][kMaxStreamSplit + 1];  // 0: not asked yet; else the count + 1
+    // kernels of one shape (CUDA-core: 8 warps, two CTAs per SM; 8-row: 12 warps, one; 16-row: 6 warps, two) have the
+    // same block size, register cap and shared memory.
+    static std::atomic<int> cache[64][3][kMaxStreamSplit + 1];  // 0: not asked yet; else the count + 1
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > kMaxStreamSplit) return 0;
-    const int fam = rows8_family(m, qact) ? 1 : 0;
+    const int fam = rows8_family(m, qact) ? 1 : (m == 1 || (m == 2 && qact)) ? 0 : 2;
     const int known = cache[dev][fam][ks].load(std::memory_order_relaxed);
     if (known > 0) return known - 1;
-    auto kernel = fam ? stream_kernel<false, kEpiStore> : stream_kernel<true, kEpiStore>;
-    const int warps = stream_warps(fam == 0), smem = stream_smem(warps);
+    auto kernel = fam == 1   ? stream_kernel<false, kEpiStore>
+                  : fam == 2 ? stream_kernel<true, kEpiStore>
+                             : stream_simt_kernel<1, kEpiStore>;
+    const int warps = fam == 1 ? kWarps8 : fam == 2 ? kWarps16 : kWarpsS, smem = stream_smem(warps);
     int n = 0;
     bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   fam ? smem : kSmemOnePerSm) == cudaSuccess &&  // as launch_stream_kernel sets it
+                                   fam == 1 ? smem : kSmemOnePerSm) == cudaSuccess &&  // as launch_stream_kernel sets it
               cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
               (ks <= 8 || cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                               cudaSuccess);
@@ -923,12 +932,15 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
     auto go8 = [&](auto kernel) {
         return launch_stream_kernel(kernel, kWarps8, a, pt, stream, pdl, mode, pair, grid);
     };
+    auto go16 = [&](auto kernel) {
+        return launch_stream_kernel(kernel, kWarps16, a, pt, stream, pdl, mode, pair, grid);
+    };
     if constexpr (EPI == kEpiStore || EPI == kEpiArgmax) {
         if (rowmajor) {  // at most 16 rows, bf16 activations
             if (qact || a.m > kGroupRows) return cudaErrorInvalidValue;
             if (a.m == 1) return go(stream_simt_kernel<1, EPI, false, true>);
             if (a.m <= 8) return go8(stream_kernel<false, EPI, false, false, true>);
-            return go(stream_kernel<true, EPI, false, false, true>);
+            return go16(stream_kernel<true, EPI, false, false, true>);
         }
     } else if (rowmajor) {
         return cudaErrorInvalidValue;  // the fused epilogues take the tiled storage
@@ -937,13 +949,13 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
         if (a.m == 1) return go(stream_simt_kernel<1, EPI, true>);
         if (a.m == 2) return go(stream_simt_kernel<2, EPI, true>);
         if (a.m <= 8) return go8(stream_kernel<false, EPI, true>);
-        if (a.m <= kGroupRows) return go(stream_kernel<true, EPI, true>);
-        return go(stream_kernel<true, EPI, true, true>);
+        if (a.m <= kGroupRows) return go16(stream_kernel<true, EPI, true>);
+        return go16(stream_kernel<true, EPI, true, true>);
     }
     if (a.m == 1) return go(stream_simt_kernel<1, EPI>);
     if (a.m <= 8) return go8(stream_kernel<false, EPI>);
-    if (a.m <= kGroupRows) return go(stream_kernel<true, EPI>);
-    return go(stream_kernel<true, EPI, false, true>);
+    if (a.m <= kGroupRows) return go16(stream_kernel<true, EPI>);
+    return go16(stream_kernel<true, EPI, false, true>);
 }
 
 cudaError_t launch_stream(const Args &a, const Parts &pt, int epi, cudaStream_t stream, bool pdl, int mode,
