@@ -725,8 +725,10 @@ def _weights(K, Ns, copies, seed, layout="tiled"):
 
 
 def run_profile_case(args):
-    """A few calls of one launch kind (constant-weights flag, as in the chain; tiled unless --layout rowmajor), for a
-    profiler to capture the fourth: `ncu ... -k regex:stream -s 3 -c 1 python bench.py --profile-case gateup --m 16`."""
+    """Four calls of one launch kind (constant-weights flag, as in the chain; tiled unless --layout rowmajor), for a
+    profiler to capture the last.  A call the planner splits is two launches (gate/up and the head at every m), so
+    `ncu ... -k regex:stream -s 6 -c 2 python bench.py --profile-case gateup --m 16` takes the fourth call's pair;
+    `-s 3 -c 1` the fourth call of an unsplit kind."""
     import torch
     import synth_inputs as si
     import q8_block_quantized_gemv_gb300 as q8
