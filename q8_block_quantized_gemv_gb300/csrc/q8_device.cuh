@@ -23,7 +23,7 @@
 namespace q8 {
 
 constexpr int kBlock = 32;   // rows of a Q8_0 block
-constexpr int kMaxClusterRanks = 8;  // the largest K split across a cluster (the portable cluster size)
+constexpr int kMaxClusterRanks = 16;  // the largest K split across a cluster (non-portable above 8 CTAs)
 constexpr int kWarps = 8;    // warps per CTA
 constexpr int kThreads = 32 * kWarps;
 
@@ -271,23 +271,33 @@ __device__ __forceinline__ uint32_t act_code(float v, float d, float inv, uint32
 template <int NRED, int MR, int TC, int NTHREADS, bool ARGMAX, int RS = TC>
 __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
     namespace cg = cooperative_groups;
+    static_assert(TC % 4 == 0 && RS % 4 == 0, "four columns a thread: 16-byte rows and slabs");
+    constexpr int TC4 = TC / 4;
     float *part = red + NRED * MR * RS;  // [MR][TC]
-    // Arg-max: up to 8 rows, the keys of this CTA's outputs, [rows][width], go over the slabs (free once `part` holds
-    // their sum) and one warp a row reduces them; 16 rows fold each key into a row key in shared memory by atomicMax
-    // (measured on GB300: the warp reduction takes the tied head at m = 8 from 119.4 to 114.9 us, but in the 16-row
-    // kernel, which sits at its 128-register cap, its code made the main loop spill and the head slower).
+    // Arg-max: up to 8 rows, the keys of this CTA's outputs (one a thread: the largest of its four columns),
+    // [rows][width / 4], go over the slabs (free once `part` holds their sum) and one warp a row reduces them; 16 rows
+    // fold each key into a row key in shared memory by atomicMax (measured on GB300: the warp reduction takes the tied
+    // head at m = 8 from 119.4 to 114.9 us, but in the 16-row kernel its code made the main loop spill and the head
+    // slower).
     constexpr bool kWarpReduce = MR <= 8;
     unsigned long long *keys = reinterpret_cast<unsigned long long *>(red);
     static_assert(NRED * RS >= 2 * TC, "the keys fit over the slabs");
     unsigned long long *rowkey = reinterpret_cast<unsigned long long *>(part + MR * TC);  // [MR]
     const int rows = a.m < MR ? a.m : MR;
 
-    for (int i = threadIdx.x; i < rows * TC; i += NTHREADS) {
-        const int at = (i / TC) * RS + i % TC;
-        float v = 0.0f;
+    // the slabs' sum, four columns a thread (the same additions, in slab order, as one column at a time)
+    for (int i = threadIdx.x; i < rows * TC4; i += NTHREADS) {
+        const int r = i / TC4, c = 4 * (i - r * TC4);
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-        for (int w = 0; w < NRED; ++w) v += red[w * MR * RS + at];
-        part[i] = v;
+        for (int w = 0; w < NRED; ++w) {
+            const float4 p = *reinterpret_cast<const float4 *>(red + (w * MR + r) * RS + c);
+            v.x += p.x;
+            v.y += p.y;
+            v.z += p.z;
+            v.w += p.w;
+        }
+        *reinterpret_cast<float4 *>(part + r * TC + c) = v;
     }
     if (ARGMAX && !kWarpReduce)
         for (int r = threadIdx.x; r < MR; r += NTHREADS) rowkey[r] = 0ull;
@@ -298,28 +308,57 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
     else
         __syncthreads();
 
+    // This rank's slice of the columns, cut at multiples of four; every rank's partial of a column is loaded before
+    // any is added, and the sum is taken in rank order.
     const int rank = blockIdx.y;
-    const int c0 = ks > 1 ? TC * rank / ks : 0;
-    const int c1 = ks > 1 ? TC * (rank + 1) / ks : TC;
-    const int width = c1 - c0;
-    for (int i = threadIdx.x; i < rows * width; i += NTHREADS) {
-        const int r = i / width;
-        const int c = c0 + (i - r * width);
-        float v;
+    const int c0 = ks > 1 ? 4 * (TC4 * rank / ks) : 0;
+    const int c1 = ks > 1 ? 4 * (TC4 * (rank + 1) / ks) : TC;
+    const int width4 = (c1 - c0) / 4;
+    for (int i = threadIdx.x; i < rows * width4; i += NTHREADS) {
+        const int r = i / width4;
+        const int c = c0 + 4 * (i - r * width4);
+        float4 v;
         if (ks > 1) {
             cg::cluster_group cluster = cg::this_cluster();
-            v = 0.0f;
-            for (int p = 0; p < ks; ++p) v += cluster.map_shared_rank(part, p)[r * TC + c];  // rank order
+            v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int h = 0; h < kMaxClusterRanks; h += 8) {  // eight ranks' loads in flight at a time
+                if (h >= ks) break;
+                float4 pv[8];
+#pragma unroll
+                for (int p = 0; p < 8; ++p)
+                    if (h + p < ks)
+                        pv[p] = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(part, h + p) + r * TC + c);
+#pragma unroll
+                for (int p = 0; p < 8; ++p)
+                    if (h + p < ks) {
+                        v.x += pv[p].x;
+                        v.y += pv[p].y;
+                        v.z += pv[p].z;
+                        v.w += pv[p].w;
+                    }
+            }
         } else {
-            v = part[r * TC + c];
+            v = *reinterpret_cast<const float4 *>(part + r * TC + c);
         }
-        const int n = tile * TC + c;
+        const int n = tile * TC + c;  // Np is a multiple of 32: the four columns are all below it or all past it
+        unsigned long long key = 0ull;
         if (n < a.Np) {
-            const float out = n < a.N ? v : 0.0f;
-            if (a.y) a.y[(size_t)r * a.Np + n] = out;
-            if (ARGMAX && !kWarpReduce && n < a.N) atomicMax(&rowkey[r], argmax_key(out, n));
+            const float4 out = make_float4(n < a.N ? v.x : 0.0f, n + 1 < a.N ? v.y : 0.0f, n + 2 < a.N ? v.z : 0.0f,
+                                           n + 3 < a.N ? v.w : 0.0f);
+            if (a.y) *reinterpret_cast<float4 *>(a.y + (size_t)r * a.Np + n) = out;
+            if (ARGMAX) {
+                const float o4[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (n + e < a.N) {
+                        const unsigned long long k = argmax_key(o4[e], n + e);
+                        key = key > k ? key : k;
+                    }
+            }
         }
-        if (ARGMAX && kWarpReduce) keys[i] = n < a.N ? argmax_key(v, n) : 0ull;
+        if (ARGMAX && !kWarpReduce && key) atomicMax(&rowkey[r], key);
+        if (ARGMAX && kWarpReduce) keys[i] = key;
     }
     if (ARGMAX && !kWarpReduce) {
         __syncthreads();
@@ -327,14 +366,14 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
             if (rowkey[r]) atomicMax(&a.keys[r], rowkey[r]);
     }
     if (ARGMAX && kWarpReduce) {
-        // each row's largest key by one warp (a lane's maximum over its columns, then a shuffle tree), and one
+        // each row's largest key by one warp (a lane's maximum over its entries, then a shuffle tree), and one
         // atomic a row into the call's keys: the maximum is the same in any order
         __syncthreads();
         constexpr int kWarpsE = NTHREADS / 32;
         const int lane = threadIdx.x & 31;
         for (int r = threadIdx.x >> 5; r < rows; r += kWarpsE) {
             unsigned long long k = 0ull;
-            for (int c = lane; c < width; c += 32) k = k > keys[r * width + c] ? k : keys[r * width + c];
+            for (int c = lane; c < width4; c += 32) k = k > keys[r * width4 + c] ? k : keys[r * width4 + c];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);

@@ -52,7 +52,7 @@ cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl
 // Defined in q8_stream.cu (the tiled layout).
 // The largest K split of a stream-kernel launch: a cluster of up to 16 CTAs (above 8 the non-portable size, which the
 // launch and the residency query ask for).
-constexpr int kMaxStreamSplit = 16;
+constexpr int kMaxStreamSplit = kMaxClusterRanks;
 // Resident CTAs per SM of the stream kernel that takes m rows (qact: of quantized activations), and how many clusters
 // of ks such CTAs are resident at once on this device (0: unknown).
 int stream_ctas_per_sm(int m, bool qact);
