@@ -268,24 +268,12 @@ __device__ __forceinline__ uint32_t act_code(float v, float d, float inv, uint32
     return (uint32_t)(int)fminf(fmaxf(roundf(qv), -127.0f), 127.0f) & 0xFFu;
 }
 
-template <int NRED, int MR, int TC, int NTHREADS, bool ARGMAX, int RS = TC>
-__device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
-    namespace cg = cooperative_groups;
+// part[r][c] = the sum of the NRED slabs red[w][r][c] (row stride RS), in slab order from 0, four columns a thread
+// (16-byte loads and stores: TC and RS are multiples of 4 and both buffers 16-byte aligned).
+template <int NRED, int MR, int TC, int NTHREADS, int RS>
+__device__ __forceinline__ void sum_slabs(const float *red, float *part, int rows) {
     static_assert(TC % 4 == 0 && RS % 4 == 0, "four columns a thread: 16-byte rows and slabs");
     constexpr int TC4 = TC / 4;
-    float *part = red + NRED * MR * RS;  // [MR][TC]
-    // Arg-max: up to 8 rows, the keys of this CTA's outputs (one a thread: the largest of its four columns),
-    // [rows][width / 4], go over the slabs (free once `part` holds their sum) and one warp a row reduces them; 16 rows
-    // fold each key into a row key in shared memory by atomicMax (measured on GB300: the warp reduction takes the tied
-    // head at m = 8 from 119.4 to 114.9 us, but in the 16-row kernel its code made the main loop spill and the head
-    // slower).
-    constexpr bool kWarpReduce = MR <= 8;
-    unsigned long long *keys = reinterpret_cast<unsigned long long *>(red);
-    static_assert(NRED * RS >= 2 * TC, "the keys fit over the slabs");
-    unsigned long long *rowkey = reinterpret_cast<unsigned long long *>(part + MR * TC);  // [MR]
-    const int rows = a.m < MR ? a.m : MR;
-
-    // the slabs' sum, four columns a thread (the same additions, in slab order, as one column at a time)
     for (int i = threadIdx.x; i < rows * TC4; i += NTHREADS) {
         const int r = i / TC4, c = 4 * (i - r * TC4);
         float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -299,6 +287,50 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
         }
         *reinterpret_cast<float4 *>(part + r * TC + c) = v;
     }
+}
+
+// The sum of the four floats at buf + at in the shared memory of cluster ranks first, first + stride, ... (count of
+// them), in that order from 0; eight ranks' loads are in flight before their adds.
+__device__ __forceinline__ float4 cluster_sum4(cooperative_groups::cluster_group &cluster, float *buf, int at,
+                                               int first, int stride, int count) {
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int h = 0; h < kMaxClusterRanks; h += 8) {
+        if (h >= count) break;
+        float4 pv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (h + j < count)
+                pv[j] = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(buf, first + stride * (h + j)) + at);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (h + j < count) {
+                v.x += pv[j].x;
+                v.y += pv[j].y;
+                v.z += pv[j].z;
+                v.w += pv[j].w;
+            }
+    }
+    return v;
+}
+
+template <int NRED, int MR, int TC, int NTHREADS, bool ARGMAX, int RS = TC>
+__device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
+    namespace cg = cooperative_groups;
+    constexpr int TC4 = TC / 4;
+    float *part = red + NRED * MR * RS;  // [MR][TC]
+    // Arg-max: up to 8 rows, the keys of this CTA's outputs (one a thread: the largest of its four columns),
+    // [rows][width / 4], go over the slabs (free once `part` holds their sum) and one warp a row reduces them; 16 rows
+    // fold each key into a row key in shared memory by atomicMax (measured on GB300: the warp reduction takes the tied
+    // head at m = 8 from 119.4 to 114.9 us, but in the 16-row kernel its code made the main loop spill and the head
+    // slower).
+    constexpr bool kWarpReduce = MR <= 8;
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(red);
+    static_assert(NRED * RS >= 2 * TC, "the keys fit over the slabs");
+    unsigned long long *rowkey = reinterpret_cast<unsigned long long *>(part + MR * TC);  // [MR]
+    const int rows = a.m < MR ? a.m : MR;
+
+    sum_slabs<NRED, MR, TC, NTHREADS, RS>(red, part, rows);
     if (ARGMAX && !kWarpReduce)
         for (int r = threadIdx.x; r < MR; r += NTHREADS) rowkey[r] = 0ull;
 
@@ -320,24 +352,7 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
         float4 v;
         if (ks > 1) {
             cg::cluster_group cluster = cg::this_cluster();
-            v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-            for (int h = 0; h < kMaxClusterRanks; h += 8) {  // eight ranks' loads in flight at a time
-                if (h >= ks) break;
-                float4 pv[8];
-#pragma unroll
-                for (int p = 0; p < 8; ++p)
-                    if (h + p < ks)
-                        pv[p] = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(part, h + p) + r * TC + c);
-#pragma unroll
-                for (int p = 0; p < 8; ++p)
-                    if (h + p < ks) {
-                        v.x += pv[p].x;
-                        v.y += pv[p].y;
-                        v.z += pv[p].z;
-                        v.w += pv[p].w;
-                    }
-            }
+            v = cluster_sum4(cluster, part, r * TC + c, 0, 1, ks);
         } else {
             v = *reinterpret_cast<const float4 *>(part + r * TC + c);
         }
@@ -396,22 +411,15 @@ __device__ __forceinline__ void finish_glu(const Args &a, float *red, int tile) 
     float *part = red + NRED * MR * RS;  // [MR][TC]: this CTA's sums over its K range
     float *mine = part + MR * TC;        // [MR][width]: this rank's slice summed over its part's K ranges
     const int rows = a.m < MR ? a.m : MR;
-    for (int i = threadIdx.x; i < rows * TC; i += NTHREADS) {
-        const int at = (i / TC) * RS + i % TC;
-        float v = 0.0f;
-#pragma unroll
-        for (int w = 0; w < NRED; ++w) v += red[w * MR * RS + at];
-        part[i] = v;
-    }
+    sum_slabs<NRED, MR, TC, NTHREADS, RS>(red, part, rows);
     cluster.sync();
     const int ks = a.ksplit, p = blockIdx.x & 1, k = blockIdx.y;
     // slices of whole 32-column blocks (a warp then holds one block of one row for the quantized output)
     const int c0 = kBlock * ((TC / kBlock) * k / ks), c1 = kBlock * ((TC / kBlock) * (k + 1) / ks), width = c1 - c0;
-    for (int i = threadIdx.x; i < rows * width; i += NTHREADS) {
-        const int r = i / width, c = c0 + (i - r * width);
-        float v = 0.0f;
-        for (int j = 0; j < ks; ++j) v += cluster.map_shared_rank(part, p + 2 * j)[r * TC + c];  // rank order
-        mine[i] = v;
+    const int width4 = width / 4;
+    for (int i = threadIdx.x; i < rows * width4; i += NTHREADS) {  // four columns a thread, ranks in order
+        const int r = i / width4, c = c0 + 4 * (i - r * width4);
+        *reinterpret_cast<float4 *>(mine + r * width + (c - c0)) = cluster_sum4(cluster, part, r * TC + c, p, 2, ks);
     }
     cluster.sync();
     if (p == 0) {
@@ -450,39 +458,39 @@ __device__ __forceinline__ void finish_glu(const Args &a, float *red, int tile) 
 template <int NRED, int MR, int TC, int NTHREADS, int RS = TC>
 __device__ __forceinline__ void finish_norm(const Args &a, float *red, int tile) {
     namespace cg = cooperative_groups;
+    constexpr int TC4 = TC / 4;
     float *part = red + NRED * MR * RS;  // [MR][TC]
     const int rows = a.m < MR ? a.m : MR;
-    for (int i = threadIdx.x; i < rows * TC; i += NTHREADS) {
-        const int at = (i / TC) * RS + i % TC;
-        float v = 0.0f;
-#pragma unroll
-        for (int w = 0; w < NRED; ++w) v += red[w * MR * RS + at];
-        part[i] = v;
-    }
+    sum_slabs<NRED, MR, TC, NTHREADS, RS>(red, part, rows);
     const int ks = a.ksplit;
     if (ks > 1)
         cg::this_cluster().sync();
     else
         __syncthreads();
+    // this rank's slice of the columns, cut at multiples of four, four columns a thread (the residual is read one
+    // value at a time: it need only be 4-byte aligned)
     const int rank = blockIdx.y;
-    const int c0 = ks > 1 ? TC * rank / ks : 0;
-    const int c1 = ks > 1 ? TC * (rank + 1) / ks : TC;
-    const int width = c1 - c0;
-    for (int i = threadIdx.x; i < rows * width; i += NTHREADS) {
-        const int r = i / width;
-        const int c = c0 + (i - r * width);
-        float v;
+    const int c0 = ks > 1 ? 4 * (TC4 * rank / ks) : 0;
+    const int c1 = ks > 1 ? 4 * (TC4 * (rank + 1) / ks) : TC;
+    const int width4 = (c1 - c0) / 4;
+    for (int i = threadIdx.x; i < rows * width4; i += NTHREADS) {
+        const int r = i / width4;
+        const int c = c0 + 4 * (i - r * width4);
+        float4 v;
         if (ks > 1) {
             cg::cluster_group cluster = cg::this_cluster();
-            v = 0.0f;
-            for (int p = 0; p < ks; ++p) v += cluster.map_shared_rank(part, p)[r * TC + c];  // rank order
+            v = cluster_sum4(cluster, part, r * TC + c, 0, 1, ks);
         } else {
-            v = part[r * TC + c];
+            v = *reinterpret_cast<const float4 *>(part + r * TC + c);
         }
-        const int n = tile * TC + c;
+        const int n = tile * TC + c;  // the four columns are all below Np or all past it
         if (n < a.Np) {
             const size_t at = (size_t)r * a.Np + n;
-            a.y[at] = n < a.N ? a.res[at] + v : 0.0f;
+            const float v4[4] = {v.x, v.y, v.z, v.w};
+            float o4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o4[e] = n + e < a.N ? a.res[at + e] + v4[e] : 0.0f;
+            *reinterpret_cast<float4 *>(a.y + at) = make_float4(o4[0], o4[1], o4[2], o4[3]);
         }
     }
     if (ks > 1) cg::this_cluster().sync();  // keep this CTA's shared memory alive until every rank has read it

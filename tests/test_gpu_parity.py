@@ -443,6 +443,21 @@ def test_tma_every_cluster_split(dev, ks, tune):
     assert q8.device_fault() == 0
 
 
+@pytest.mark.parametrize("m", [1, 2, 3, 9, 16])
+def test_single_tile_sixteen_rank_cluster(dev, m):
+    """One column tile (N = 40, K = 5120) on the tiled storage: the planner splits K over a cluster of up to 16 CTAs
+    (above the portable 8 when the residency query allows), whose epilogue loads the ranks' partials in groups of
+    eight and sums them in rank order -- every output against the oracle, the pads exactly 0, and the same bits on a
+    second call."""
+    x, q, s = si.case(m, 5120, 40, 7300 + m)
+    y_o, a_o = oracle.gemv(x, q, s)
+    y1 = _gemv(dev, x, q, s, 40, "tiled")
+    _assert_close(y1, y_o, a_o, f"m={m}")
+    assert np.all(y1[:, 40:] == 0)
+    y2 = _gemv(dev, x, q, s, 40, "tiled")
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
 def test_no_device_fault_after_suite(dev):
     import q8_block_quantized_gemv_gb300 as q8
     assert q8.device_fault(clear=True) == 0
