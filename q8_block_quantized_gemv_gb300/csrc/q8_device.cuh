@@ -6,13 +6,14 @@
 //
 // Work decomposition used by every kernel here:
 //   - a CTA owns one tile of TC output columns for all m rows and a contiguous range of the K/32 blocks;
-//   - its 8 warps split that range again, each streaming whole 32-row blocks of its columns;
+//   - its warps (6, 8 or 12 by kernel) split that range again, each streaming whole 32-row blocks of its columns;
 //   - per block, the 32 lane products are summed first and then multiplied by the block's scale, as the formula
 //     groups them, and added into an fp32 carry that starts at zero;
 //   - the warps' carries are summed in shared memory in warp order, then, when K is split across the CTAs of a
 //     thread-block cluster (N too narrow to fill the SMs: "plan.rs", `split_counts`: K divided so that every SM
 //     gets blocks), each CTA sums one slice of the columns over the cluster's ranks through distributed shared
-//     memory, in rank order.  Every sum has a fixed order, so results are bit-reproducible and need no scratch memory.
+//     memory, in rank order, four columns a thread.  Every sum has a fixed order, so results are bit-reproducible
+//     and need no scratch memory.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -24,7 +25,7 @@ namespace q8 {
 
 constexpr int kBlock = 32;   // rows of a Q8_0 block
 constexpr int kMaxClusterRanks = 16;  // the largest K split across a cluster (non-portable above 8 CTAs)
-constexpr int kWarps = 8;    // warps per CTA
+constexpr int kWarps = 8;    // warps per CTA of the kernels launched through launch_tiles (q8_simt.cu, q8_mma.cu)
 constexpr int kThreads = 32 * kWarps;
 
 struct Args {
