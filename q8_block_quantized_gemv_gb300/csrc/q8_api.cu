@@ -88,7 +88,8 @@ struct Plan {
 // Kernel family, per-lane width and K split for a shape.  The widest tile that still gives every SM a CTA is
 // preferred; K is split across a cluster (at most 8 CTAs, the portable size) until the grid holds about as many CTAs
 // as are resident at once (two per SM; one for the 8-row stream kernel).
-Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long tiled_tiles = 0, bool qact = false) {
+Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long tiled_tiles = 0, bool qact = false,
+               bool rowmajor = false) {
     const int nb = K / Q8_BLOCK;
     if (tiled) {
         // The tiled layout: per-warp cp.async streams, 128-column tiles.  Measured on GB300, the best K split is
@@ -98,7 +99,7 @@ Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long
         // one GPC, so fewer clusters fit than slots / ks).
         const long long groups = (m + q8::kGroupRows - 1) / q8::kGroupRows;
         const long long tiles = groups * (tiled_tiles > 0 ? tiled_tiles : (Np + q8::kTmaColumns - 1) / q8::kTmaColumns);
-        const long long slots = (long long)q8::stream_ctas_per_sm(m, qact) * sms;
+        const long long slots = (long long)q8::stream_ctas_per_sm(m, qact, rowmajor) * sms;
         // Clusters above the portable 8 CTAs only where 8 would leave more than half of the SMs idle (measured:
         // 5120 x 40 at m = 1 3.66 -> 2.83 us with 16; 5120 x 3000 at m = 16 8.90 -> 9.27 us with 12).
         const long long cap = tiles * 8 * 2 < sms ? q8::kMaxStreamSplit : 8;
@@ -107,7 +108,7 @@ Plan make_plan(int m, int K, int Np, int variant, bool tiled, int sms, long long
         if (ks > nb) ks = nb;
         if (ks < 1) ks = 1;
         while (ks > 1) {
-            const int fit = q8::stream_max_clusters(m, qact, (int)ks);
+            const int fit = q8::stream_max_clusters(m, qact, (int)ks, rowmajor);
             if (fit <= 0 || tiles <= fit) break;
             --ks;
         }
@@ -213,13 +214,13 @@ struct Split {
 };
 // pair: the gated pair, whose tiles are two CTAs each (the gate's and the up projection's, a cluster of 2 x ks, ks at
 // most 4); else one CTA a tile (ks at most 8).
-Split plan_split(long long tiles, int nb, int m, bool qact, int sms, int ks, bool pair = false) {
+Split plan_split(long long tiles, int nb, int m, bool qact, int sms, int ks, bool pair = false, bool rowmajor = false) {
     Split none;
     // (a forced K split keeps one launch, so that it applies to every tile)
     if (tuning(Q8_TUNE_SPLIT) == 0 || tuning(Q8_TUNE_KSPLIT) != 0 || ks != 1 || m > q8::kGroupRows || sms <= 0)
         return none;
     const long long per = pair ? 2 : 1;  // CTAs a tile
-    const long long slots = (long long)q8::stream_ctas_per_sm(m, qact) * sms;
+    const long long slots = (long long)q8::stream_ctas_per_sm(m, qact, rowmajor) * sms;
     const long long ctas = per * tiles;
     long long ta;
     bool co;
@@ -237,7 +238,7 @@ Split plan_split(long long tiles, int nb, int m, bool qact, int sms, int ks, boo
     if (kb > 8 / per) kb = 8 / per;
     if (kb > nb) kb = nb;
     while (kb > 1) {  // clusters that are all resident at once (beside the first launch's CTAs: about half as many)
-        const int fit = q8::stream_max_clusters(m, qact, (int)(per * kb));
+        const int fit = q8::stream_max_clusters(m, qact, (int)(per * kb), rowmajor);
         if (fit > 0 && tb <= (co ? fit / 2 : fit)) break;
         --kb;
     }
@@ -270,7 +271,7 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
     }
     const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
     const Plan p = make_plan(a.m, a.K, a.Np, variant, streaming, sms, parts ? parts->tile_end[parts->count - 1] : 0,
-                             qact);
+                             qact, !tiled);
     Args b = a;
     b.ksplit = p.ksplit;
     const bool prefetch = (flags & Q8_FLAG_CONSTANT_WEIGHTS) != 0;
@@ -282,7 +283,7 @@ q8_status run(const Args &a, int variant, unsigned flags, bool argmax, cudaStrea
     const int mode = prefetch ? q8::kModePrefetch : 0;
     if (p.variant == kVariantStream) {
         const int tiles = parts->tile_end[parts->count - 1];
-        const Split sp = plan_split(tiles, a.nb, a.m, qact, sms, b.ksplit);
+        const Split sp = plan_split(tiles, a.nb, a.m, qact, sms, b.ksplit, false, !tiled);
         if (sp.tiles_a > 0) {
             q8::StreamGrid ga;
             ga.ntiles = sp.tiles_a;
@@ -323,8 +324,8 @@ extern "C" int q8_plan_launches(int m, int K, const int *Ns, int nparts, unsigne
     int sms = 0;
     if (sm_count(&sms) != 0) return -Q8_ERR_CUDA;
     const bool qact = (flags & Q8_FLAG_Q8_ACT) != 0;
-    const Plan p = make_plan(m, K, q8_padded_n(Ns[0]), Q8_VARIANT_AUTO, true, sms, tiles, qact);
-    return plan_split(tiles, K / Q8_BLOCK, m, qact, sms, p.ksplit).tiles_a > 0 ? 2 : 1;
+    const Plan p = make_plan(m, K, q8_padded_n(Ns[0]), Q8_VARIANT_AUTO, true, sms, tiles, qact, !tiled);
+    return plan_split(tiles, K / Q8_BLOCK, m, qact, sms, p.ksplit, false, !tiled).tiles_a > 0 ? 2 : 1;
 }
 
 namespace {

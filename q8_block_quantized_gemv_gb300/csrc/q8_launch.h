@@ -53,10 +53,10 @@ cudaError_t launch_tma(const Args &a, bool argmax, cudaStream_t stream, bool pdl
 // The largest K split of a stream-kernel launch: a cluster of up to 16 CTAs (above 8 the non-portable size, which the
 // launch and the residency query ask for).
 constexpr int kMaxStreamSplit = kMaxClusterRanks;
-// Resident CTAs per SM of the stream kernel that takes m rows (qact: of quantized activations), and how many clusters
-// of ks such CTAs are resident at once on this device (0: unknown).
-int stream_ctas_per_sm(int m, bool qact);
-int stream_max_clusters(int m, bool qact, int ks);
+// Resident CTAs per SM of the stream kernel that takes m rows (qact: of quantized activations; rowmajor: of row-major
+// weights), and how many clusters of ks such CTAs are resident at once on this device (0: unknown).
+int stream_ctas_per_sm(int m, bool qact, bool rowmajor = false);
+int stream_max_clusters(int m, bool qact, int ks, bool rowmajor = false);
 // How a stream launch takes part in programmatic dependent launch (bits of `mode`):
 constexpr int kModePrefetch = 1;   // request the first ring stages' weights before the dependency wait
 constexpr int kModeRelease = 2;    // release the next launch right after the dependency wait, not after the main loop

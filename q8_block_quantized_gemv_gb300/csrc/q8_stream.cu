@@ -874,11 +874,17 @@ unsigned int *norm_counters() {
     return static_cast<unsigned int *>(base);
 }
 
-// The 8-row kernel (2 .. 8 rows; 3 .. 8 of quantized activations) runs one CTA per SM, the others two.
-bool rows8_family(int m, bool qact) { return (m >= 3 && m <= 8) || (m == 2 && !qact); }
-int stream_ctas_per_sm(int m, bool qact) { return rows8_family(m, qact) ? 1 : 2; }
+// The 8-row kernel (2 .. 8 rows of tiled weights; 3 .. 8 of quantized activations) runs one CTA per SM, the others
+// two.  Row-major weights take the 16-row kernel from 2 rows: measured on GB300, its row-major instances do not spill
+// where the 8-row kernel's do (12 to 24 bytes at the 168-register cap), and the row-major product at 2, 4 and 8 rows
+// ran 4-14% faster on five of the six shapes of the sweep (5120 x 6144 at m = 8 12.56 -> 10.90 us, 14336 x 4096
+// 16.94 -> 15.59) and within 2% on 4096 x 14336; on tiled weights the 16-row kernel was up to 12% slower there.
+bool rows8_family(int m, bool qact, bool rowmajor = false) {
+    return !rowmajor && ((m >= 3 && m <= 8) || (m == 2 && !qact));
+}
+int stream_ctas_per_sm(int m, bool qact, bool rowmajor) { return rows8_family(m, qact, rowmajor) ? 1 : 2; }
 
-int stream_max_clusters(int m, bool qact, int ks) {
+int stream_max_clusters(int m, bool qact, int ks, bool rowmajor) {
     // Clusters of ks CTAs are placed within one GPC, so fewer of them fit at once than slots / ks.  Asked once per
     // device, kernel shape and size (a deterministic answer: concurrent first calls store the same value); the stream
     // kernels of one shape (CUDA-core: 8 warps, two CTAs per SM; 8-row: 12 warps, one; 16-row: 6 warps, two) have the
@@ -886,7 +892,7 @@ int stream_max_clusters(int m, bool qact, int ks) {
     static std::atomic<int> cache[64][3][kMaxStreamSplit + 1];  // 0: not asked yet; else the count + 1
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > kMaxStreamSplit) return 0;
-    const int fam = rows8_family(m, qact) ? 1 : (m == 1 || (m == 2 && qact)) ? 0 : 2;
+    const int fam = rows8_family(m, qact, rowmajor) ? 1 : (m == 1 || (m == 2 && qact)) ? 0 : 2;
     const int known = cache[dev][fam][ks].load(std::memory_order_relaxed);
     if (known > 0) return known - 1;
     auto kernel = fam == 1   ? stream_kernel<false, kEpiStore>
@@ -939,7 +945,6 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
         if (rowmajor) {  // at most 16 rows, bf16 activations
             if (qact || a.m > kGroupRows) return cudaErrorInvalidValue;
             if (a.m == 1) return go(stream_simt_kernel<1, EPI, false, true>);
-            if (a.m <= 8) return go8(stream_kernel<false, EPI, false, false, true>);
             return go16(stream_kernel<true, EPI, false, false, true>);
         }
     } else if (rowmajor) {
