@@ -269,6 +269,16 @@ __device__ __forceinline__ uint32_t act_code(float v, float d, float inv, uint32
     return (uint32_t)(int)fminf(fmaxf(roundf(qv), -127.0f), 127.0f) & 0xFFu;
 }
 
+// The cluster barrier after a rank's last read of the others' shared memory, which keeps every rank's shared memory
+// alive until then.  Each rank's remote loads feed stores issued before it arrives (the loops below load a column only
+// when they store it), so the arrival needs no release ordering: relaxed, it does not wait for the rank's global stores
+// to be performed, which took the decode chain from 5,036 to 5,115 GB/s at one row and 4,069 to 4,173 at 16 (GB300,
+// three runs each, one box).
+__device__ __forceinline__ void cluster_sync_after_reads() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // part[r][c] = the sum of the NRED slabs red[w][r][c] (row stride RS), in slab order from 0, four columns a thread
 // (16-byte loads and stores: TC and RS are multiples of 4 and both buffers 16-byte aligned).
 template <int NRED, int MR, int TC, int NTHREADS, int RS>
@@ -350,16 +360,16 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
     for (int i = threadIdx.x; i < rows * width4; i += NTHREADS) {
         const int r = i / width4;
         const int c = c0 + 4 * (i - r * width4);
-        float4 v;
-        if (ks > 1) {
-            cg::cluster_group cluster = cg::this_cluster();
-            v = cluster_sum4(cluster, part, r * TC + c, 0, 1, ks);
-        } else {
-            v = *reinterpret_cast<const float4 *>(part + r * TC + c);
-        }
         const int n = tile * TC + c;  // Np is a multiple of 32: the four columns are all below it or all past it
         unsigned long long key = 0ull;
         if (n < a.Np) {
+            float4 v;
+            if (ks > 1) {
+                cg::cluster_group cluster = cg::this_cluster();
+                v = cluster_sum4(cluster, part, r * TC + c, 0, 1, ks);
+            } else {
+                v = *reinterpret_cast<const float4 *>(part + r * TC + c);
+            }
             const float4 out = make_float4(n < a.N ? v.x : 0.0f, n + 1 < a.N ? v.y : 0.0f, n + 2 < a.N ? v.z : 0.0f,
                                            n + 3 < a.N ? v.w : 0.0f);
             if (a.y) *reinterpret_cast<float4 *>(a.y + (size_t)r * a.Np + n) = out;
@@ -398,7 +408,7 @@ __device__ __forceinline__ void finish_n(const Args &a, float *red, int tile) {
             if (lane == 0 && k) atomicMax(&a.keys[r], k);
         }
     }
-    if (ks > 1) cg::this_cluster().sync();  // keep this CTA's shared memory alive until every rank has read it
+    if (ks > 1) cluster_sync_after_reads();
 }
 
 // The gated pair's epilogue ("plan.rs", `Launch::GemvGlu`, SwiGLU: out = silu(x.wg) * (x.wu), silu(g) = g / (1 +
@@ -446,7 +456,7 @@ __device__ __forceinline__ void finish_glu(const Args &a, float *red, int tile) 
             }
         }
     }
-    cluster.sync();  // the up projection's rank keeps its shared memory until the gate's rank has read it
+    cluster_sync_after_reads();  // the up projection's rank keeps its shared memory until the gate's rank has read it
 }
 
 // A projection followed by the residual add and the following RMS norm ("plan.rs", `Launch::Fold` of a projection
@@ -477,15 +487,15 @@ __device__ __forceinline__ void finish_norm(const Args &a, float *red, int tile)
     for (int i = threadIdx.x; i < rows * width4; i += NTHREADS) {
         const int r = i / width4;
         const int c = c0 + 4 * (i - r * width4);
-        float4 v;
-        if (ks > 1) {
-            cg::cluster_group cluster = cg::this_cluster();
-            v = cluster_sum4(cluster, part, r * TC + c, 0, 1, ks);
-        } else {
-            v = *reinterpret_cast<const float4 *>(part + r * TC + c);
-        }
         const int n = tile * TC + c;  // the four columns are all below Np or all past it
         if (n < a.Np) {
+            float4 v;
+            if (ks > 1) {
+                cg::cluster_group cluster = cg::this_cluster();
+                v = cluster_sum4(cluster, part, r * TC + c, 0, 1, ks);
+            } else {
+                v = *reinterpret_cast<const float4 *>(part + r * TC + c);
+            }
             const size_t at = (size_t)r * a.Np + n;
             const float v4[4] = {v.x, v.y, v.z, v.w};
             float o4[4];
@@ -494,7 +504,7 @@ __device__ __forceinline__ void finish_norm(const Args &a, float *red, int tile)
             *reinterpret_cast<float4 *>(a.y + at) = make_float4(o4[0], o4[1], o4[2], o4[3]);
         }
     }
-    if (ks > 1) cg::this_cluster().sync();  // keep this CTA's shared memory alive until every rank has read it
+    if (ks > 1) cluster_sync_after_reads();
     if (!a.count) return;  // the norm runs as a launch of its own (norm_rows_kernel)
 
     // Count in; the last CTA runs the norm.
