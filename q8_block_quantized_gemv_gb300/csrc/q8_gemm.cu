@@ -15,11 +15,10 @@
 //              128 scales by two bulk copies, all completing one `loaded` barrier;
 //   warp 1     one thread issues each block's two MMAs into one of four accumulator buffers and commits them to the
 //              stage's `empty` barrier and the buffer's `full` barrier;
-//   warps 2-17 workers: they turn block b's unit into exact bf16 in the same 64-byte swizzled K-major layout (two
-//              words a thread) and signal the stage full, then fold block b - 3: each
-//              thread reads its accumulator lane (one output row) over a quarter of the columns, multiplies by the
-//              block's scales and adds into its fp32 carry (packed fp32x2); the warp frees the buffer and its share
-//              of the stage.
+//   warps 2-17 workers: they first fold block b - 3 -- each thread reads its accumulator lane (one output row)
+//              over a quarter of the columns, multiplies by the block's scales and adds into its fp32 carry (packed
+//              fp32x2); the warp frees the buffer and its share of the stage -- then turn block b's unit into exact
+//              bf16 in the same 64-byte swizzled K-major layout (two words a thread) and signal the stage full.
 // Four accumulator buffers let the MMAs of later blocks run while a block is folded.  When the tiles are too
 // few to fill the SMs, K is split across a thread-block cluster of up to 4 CTAs; their carries are summed through
 // distributed shared memory in rank order (deterministic).  Every mbarrier wait is bounded (about two seconds); a
@@ -46,7 +45,7 @@ constexpr int kWorkWarp0 = 2;             // warps 2..17: TMEM lane quarters 2, 
 constexpr int kWorkWarps = 16;
 constexpr int kGThreads = 32 * (kWorkWarp0 + kWorkWarps);
 constexpr int kFoldCols = kGN / 4;        // columns one worker folds
-constexpr int kFoldLag = 3;               // a worker folds block b - 3 after converting block b
+constexpr int kFoldLag = 3;               // a worker folds block b - 3 before it converts block b
 
 // Stage layout (bytes): bf16 A [128 rows x 64 bytes] as the TMA writes it (64-byte swizzle), B [128 weight columns x
 // 64 bytes] in the same swizzle, the raw unit, its 128 scales; stages 1024-byte aligned (the swizzle pattern repeats
@@ -293,7 +292,7 @@ __global__ void __maxnreg__(96)
         }
         __syncwarp();
     } else {
-        // ---- workers: convert block i, fold block i - kFoldLag ----
+        // ---- workers: fold block i - kFoldLag, convert block i ----
         // Each thread converts two words of the unit: words 2wp, 2wp + 1 of segment 4s + h, lane 4g + u.  Warp wi
         // takes group h, columns g0 .. g0 + 3 of each 8-column slice and word pair wp; a lane takes (s, g, u).  Then
         // the 16 lanes of a half-warp write two adjacent weight columns (rows of B) whole -- their 16 x 8 bytes are
@@ -331,6 +330,9 @@ __global__ void __maxnreg__(96)
         };
         bool ok = true;
         for (int i = 0; i < n && ok; ++i) {
+            // Fold block i - kFoldLag first: then a stage's refill (after its block's MMAs and folds) does not wait for
+            // a later block's copies (measured on GB300: 2-4% faster on every prefill shape of the sweep).
+            if (i >= kFoldLag && !(ok = fold(i - kFoldLag))) break;
             const int st = i % kGStages;
             if (!bar_wait(&loaded[st], (i / kGStages) & 1, abort)) break;
             unsigned char *sp = smem_g + st * kStageBytes;
@@ -349,7 +351,6 @@ __global__ void __maxnreg__(96)
             fence_async_smem();  // this thread's generic-proxy writes before the MMAs read them
             __syncwarp();
             if (lane == 0) bar_arrive(&full[st]);
-            if (i >= kFoldLag) ok = fold(i - kFoldLag);
         }
         for (int f = n - kFoldLag < 0 ? 0 : n - kFoldLag; f < n && ok; ++f) ok = fold(f);
     }
