@@ -405,22 +405,15 @@ __global__ void __maxnreg__(96)
         const int r0 = kGM * rank / ks, r1 = kGM * (rank + 1) / ks;
         for (int e = threadIdx.x; e < (r1 - r0) * (kGN / 4); e += kGThreads) {
             const int rr = r0 + e / (kGN / 4), c4 = 4 * (e % (kGN / 4));
-            float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            for (int p = 0; p < ks; ++p) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(red, p) + rr * kRedStride + c4);
-                sum.x += v4.x;
-                sum.y += v4.y;
-                sum.z += v4.z;
-                sum.w += v4.w;
-            }
             const int row = row0 + rr, nn = tile * kGN + c4;
-            if (row < a.m && nn < a.Np && !*abort) {
+            if (row < a.m && nn < a.Np && !*abort) {  // the ranks' slabs are read only for a value that is stored
+                const float4 sum = cluster_sum4(cluster, red, rr * kRedStride + c4, 0, 1, ks);
                 float4 o = make_float4(nn < a.N ? sum.x : 0.0f, nn + 1 < a.N ? sum.y : 0.0f,
                                        nn + 2 < a.N ? sum.z : 0.0f, nn + 3 < a.N ? sum.w : 0.0f);
                 *reinterpret_cast<float4 *>(a.y + (size_t)row * a.Np + nn) = o;
             }
         }
-        cluster.sync();  // every rank's slab stays alive until all have read it
+        cluster_sync_after_reads();  // every rank's slab stays alive until all have read it
     }
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols) : "memory");
