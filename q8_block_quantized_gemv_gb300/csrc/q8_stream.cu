@@ -13,11 +13,11 @@
 // three stages in shared memory, filled with cp.async (16 bytes a lane, bypassing L1): it issues block i + 2 while it
 // computes block i, so about two units per warp -- 80 to 150 KB per SM -- are in flight without holding registers.
 // The CUDA-core kernel runs 8 warps a CTA, two CTAs per SM (128 registers a thread).  The MMA kernels hold more
-// registers a thread, up to 168: the 8-row kernel runs 12 warps, one CTA per SM (measured on GB300, 10-28 % faster
-// per launch at 4 and 8 rows than 8 warps at the 128-register cap), and the 16-row kernel 6 warps, two CTAs per SM
-// (measured on GB300: the 16-row decode chain 3,690 -> 3,850 GB/s against 8 warps at 128 registers, which spilled;
-// 5 warps at 200 registers and 4 at 255 were slower, and so was one 12-warp CTA per SM, whose whole-SM CTAs cannot
-// start beside the previous launch's).
+// registers a thread, up to 168, in 6-warp CTAs, two per SM.  Measured on GB300: the 16-row decode chain 3,690 -> 3,850
+// GB/s against 8 warps at 128 registers, which spilled; 5 warps at 200 registers and 4 at 255 were slower, and so
+// was one 12-warp CTA per SM, whose whole-SM CTAs cannot start beside the previous launch's.  The 8-row kernel had
+// run 12 warps, one CTA per SM (10-28 % faster per launch at 4 and 8 rows than 8 warps at the 128-register cap);
+// two 6-warp CTAs per SM took its chains a further 0.4-1.4 % (m = 2 4,739 -> 4,793 GB/s, m = 4 4,654 -> 4,720).
 //
 // The block's contraction runs on m16n8k16 MMAs with the activations as the A operand (rows r and r + 8 of the lane's
 // fragment are activation rows g and g + 8) and the weights as B (one 8-column slice per MMA, fp32 accumulators):
@@ -53,7 +53,7 @@ namespace q8 {
 namespace {
 
 constexpr int kWarpsS = 8;   // warps of a CTA: the CUDA-core kernel (two CTAs per SM)
-constexpr int kWarps8 = 12;  //   the 8-row kernel (one CTA per SM)
+constexpr int kWarps8 = 6;   //   the 8-row kernel (two CTAs per SM)
 constexpr int kWarps16 = 6;  //   the 16-row kernel (two CTAs per SM)
 constexpr int kThreadsS = 32 * kWarpsS;
 __host__ __device__ constexpr int stream_warps(bool rows16) { return rows16 ? kWarps16 : kWarps8; }
@@ -395,7 +395,7 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
 // GROUPS: m > 16, the rows in groups of 16 (grid x = tiles * groups, ROWS16 only).
 // RM: the weight is row-major (q8_gemv's layout), not tiled.
 template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false, bool RM = false>
-__global__ void __launch_bounds__(32 * stream_warps(ROWS16), ROWS16 ? 2 : 1)
+__global__ void __launch_bounds__(32 * stream_warps(ROWS16), 2)
     stream_kernel(Args a, const __grid_constant__ Parts parts, const int mode) {
     static_assert(ROWS16 || !GROUPS, "row groups are groups of 16 rows");
     constexpr int W = stream_warps(ROWS16);
@@ -812,10 +812,10 @@ static_assert(finish_smem_n(kWarpsS, 2, kTmaColumns) <= kSmemS, "the CUDA-core k
 static_assert(2 * kSmemS <= 227 * 1024 && 2 * stream_smem(kWarps16) <= 227 * 1024, "two CTAs per SM");
 static_assert(finish_smem_n(kWarps8, 8, kTmaColumns, kSlabStride) <= stream_smem(kWarps8), "8-row epilogue fits");
 static_assert((kWarps8 * 8 * kSlabStride + 2 * 8 * kTmaColumns) * 4 <= stream_smem(kWarps8), "8-row gated pair fits");
-static_assert(stream_smem(kWarps8) <= 227 * 1024, "one 8-row CTA per SM");
-// The shared memory of a launch held to one CTA per SM beside one ordinary CTA of the two-per-SM kernels (the
-// CUDA-core kernel's 8 warps, the 16-row kernel's 6): two such CTAs (each with its 1 KB reserve) exceed the SM's
-// 228 KB, one of them and an ordinary one do not.
+static_assert(2 * stream_smem(kWarps8) <= 227 * 1024, "two 8-row CTAs per SM");
+// The shared memory of a launch held to one CTA per SM beside one ordinary CTA of the same kernel (the CUDA-core
+// kernel's 8 warps, the MMA kernels' 6): two such CTAs (each with its 1 KB reserve) exceed the SM's 228 KB, one of
+// them and an ordinary one do not.
 constexpr int kSmemOnePerSm = 114 * 1024;
 static_assert(2 * (kSmemOnePerSm + 1024) > 228 * 1024 && kSmemOnePerSm + kSmemS + 2 * 1024 <= 228 * 1024,
               "one such CTA and one ordinary CTA per SM");
@@ -823,10 +823,9 @@ static_assert(2 * (kSmemOnePerSm + 1024) > 228 * 1024 && kSmemOnePerSm + kSmemS 
 template <typename Kernel>
 cudaError_t launch_stream_kernel(Kernel kernel, int warps, const Args &a, const Parts &pt, cudaStream_t stream,
                                  bool pdl, int mode, bool pair, StreamGrid grid) {
-    const bool two_per_sm = warps != kWarps8;
-    const int smem = grid.one_per_sm && two_per_sm ? kSmemOnePerSm : stream_smem(warps);
+    const int smem = grid.one_per_sm ? kSmemOnePerSm : stream_smem(warps);
     // the attribute is the largest size any launch of the kernel asks for, so that concurrent callers agree on it
-    const int smem_max = two_per_sm ? kSmemOnePerSm : stream_smem(warps);
+    const int smem_max = kSmemOnePerSm;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -874,21 +873,22 @@ unsigned int *norm_counters() {
     return static_cast<unsigned int *>(base);
 }
 
-// The 8-row kernel (2 .. 8 rows of tiled weights; 3 .. 8 of quantized activations) runs one CTA per SM, the others
-// two.  Row-major weights take the 16-row kernel from 2 rows: measured on GB300, its row-major instances do not spill
-// where the 8-row kernel's do (12 to 24 bytes at the 168-register cap), and the row-major product at 2, 4 and 8 rows
-// ran 4-14% faster on five of the six shapes of the sweep (5120 x 6144 at m = 8 12.56 -> 10.90 us, 14336 x 4096
-// 16.94 -> 15.59) and within 2% on 4096 x 14336; on tiled weights the 16-row kernel was up to 12% slower there.
+// The 8-row kernel takes 2 .. 8 rows of tiled weights (3 .. 8 of quantized activations).  Row-major weights take the
+// 16-row kernel from 2 rows: measured on GB300, its row-major instances do not spill where the 8-row kernel's do (12
+// to 24 bytes at the 168-register cap), and the row-major product at 2, 4 and 8 rows ran 4-14% faster on five of the
+// six shapes of the sweep (5120 x 6144 at m = 8 12.56 -> 10.90 us, 14336 x 4096 16.94 -> 15.59) and within 2% on
+// 4096 x 14336; on tiled weights the 16-row kernel was up to 12% slower there.  Every stream kernel runs two CTAs per
+// SM.
 bool rows8_family(int m, bool qact, bool rowmajor = false) {
     return !rowmajor && ((m >= 3 && m <= 8) || (m == 2 && !qact));
 }
-int stream_ctas_per_sm(int m, bool qact, bool rowmajor) { return rows8_family(m, qact, rowmajor) ? 1 : 2; }
+int stream_ctas_per_sm(int, bool, bool) { return 2; }
 
 int stream_max_clusters(int m, bool qact, int ks, bool rowmajor) {
     // Clusters of ks CTAs are placed within one GPC, so fewer of them fit at once than slots / ks.  Asked once per
     // device, kernel shape and size (a deterministic answer: concurrent first calls store the same value); the stream
-    // kernels of one shape (CUDA-core: 8 warps, two CTAs per SM; 8-row: 12 warps, one; 16-row: 6 warps, two) have the
-    // same block size, register cap and shared memory.
+    // kernels of one family (CUDA-core: 8 warps; 8-row and 16-row: 6 warps; two CTAs per SM each) have the same block
+    // size, register cap and shared memory.
     static std::atomic<int> cache[64][3][kMaxStreamSplit + 1];  // 0: not asked yet; else the count + 1
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > kMaxStreamSplit) return 0;
@@ -901,7 +901,7 @@ int stream_max_clusters(int m, bool qact, int ks, bool rowmajor) {
     const int warps = fam == 1 ? kWarps8 : fam == 2 ? kWarps16 : kWarpsS, smem = stream_smem(warps);
     int n = 0;
     bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   fam == 1 ? smem : kSmemOnePerSm) == cudaSuccess &&  // as launch_stream_kernel sets it
+                                   kSmemOnePerSm) == cudaSuccess &&  // as launch_stream_kernel sets it
               cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
               (ks <= 8 || cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                               cudaSuccess);

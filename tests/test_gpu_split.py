@@ -69,11 +69,9 @@ def _assert_close(y_gpu, y_o, a_o, what=""):
 
 
 def test_planner_splits_the_chains_uneven_launches(dev, sms):
-    """On 152 SMs: the gate/up pair (224 tiles) and the tied head (1002 tiles) split at 1 and 16 rows; q/k/v, o and
-    down keep one launch (their K split already fills the SMs); with the 8-row kernel (2..8 rows of tiled weights,
-    one CTA per SM) the head keeps one launch (its 90 leftover tiles over 152 slots take no K split) and the pair
-    splits when its 72 clusters of two fit.  Row-major weights take the two-CTAs-per-SM kernels at every row count,
-    so they split as at 1 and 16 rows.  Switched off, or under a forced K split, every call is one launch."""
+    """On 152 SMs, where every stream kernel runs two CTAs per SM: the gate/up pair (224 tiles) and the tied head
+    (1002 tiles) split in two at every row count and on both storages; q/k/v, o and down keep one launch (their K
+    split already fills the SMs).  Switched off, or under a forced K split, every call is one launch."""
     import q8_block_quantized_gemv_gb300 as q8
     if sms != 152:
         pytest.skip("expectations for a 152-SM GB300")
@@ -81,15 +79,9 @@ def test_planner_splits_the_chains_uneven_launches(dev, sms):
               "down": (14336, (4096,)), "head": (4096, (128256,))}
     for m in (1, 2, 4, 8, 16):
         for tiled in (True, False):
-            rows8 = tiled and 2 <= m <= 8
             for name, (K, Ns) in shapes.items():
                 got = q8.plan_launches(m, K, Ns, tiled=tiled)
-                if name == "gateup":
-                    assert got in ((1, 2) if rows8 else (2,)), (m, tiled, name, got)
-                elif name == "head":
-                    assert got == (1 if rows8 else 2), (m, tiled, name, got)
-                else:
-                    assert got == 1, (m, tiled, name, got)
+                assert got == (2 if name in ("gateup", "head") else 1), (m, tiled, name, got)
     with q8.tuning(split=0):
         assert q8.plan_launches(16, 4096, (14336, 14336)) == 1 and q8.plan_launches(1, 4096, (128256,)) == 1
     with q8.tuning(ksplit=2):
