@@ -41,9 +41,10 @@
 // rows of quantized activations stay on the CUDA cores, whose dp4a products beat it there (the decode chain 3,900
 // against 3,658 GB/s).
 //
-// Activations are read from L2 (ld.global.cg), two blocks ahead.  With programmatic dependent launch every thread
-// waits for the previous kernel (griddepcontrol.wait) before it reads x or writes y; with Q8_FLAG_CONSTANT_WEIGHTS
-// the first two stages' weights are already requested before that wait.
+// Activations are read from L2 (ld.global.cg), two blocks ahead; the 8-row kernel's bf16 rows instead travel in the
+// unit's ring stage (cp.async), read back from shared memory with the unit.  With programmatic dependent launch every
+// thread waits for the previous kernel (griddepcontrol.wait) before it reads x or writes y; with
+// Q8_FLAG_CONSTANT_WEIGHTS the first two stages' weights are already requested before that wait.
 #include <atomic>
 
 #include "q8_launch.h"
@@ -62,7 +63,12 @@ constexpr int kUnitScales = kTmaColumns;     // 128 fp32
 constexpr int kStageS = kUnit + kUnitScales * 4;
 constexpr int kDepthS = 3;                   // ring stages per warp
 constexpr int kSmemS = kWarpsS * kDepthS * kStageS;
-__host__ __device__ constexpr int stream_smem(int warps) { return warps * kDepthS * kStageS; }
+constexpr int kStageX = 16 * kBlock * 2;     // MMA kernels: the block's activation rows (up to 16 x 32 bf16)
+constexpr int kStageM = kStageS + kStageX;   //   so their stages hold the unit, its scales and those rows
+// ring: the stages also carry the block's activation rows (the MMA kernels' XR instances)
+__host__ __device__ constexpr int stream_smem(int warps, bool ring = false) {
+    return warps * kDepthS * (ring ? kStageM : kStageS);
+}
 constexpr int kSlices = kTmaColumns / 8;     // 8-column MMA slices of a tile
 constexpr int kSlabStride = kTmaColumns + 8; // epilogue slab row stride (floats)
 
@@ -70,6 +76,10 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8_zfill(void *dst, const void *src, unsigned bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(bytes)
+                 : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N> __device__ __forceinline__ void cp_async_wait() {
@@ -394,11 +404,15 @@ __device__ __forceinline__ void block_contract(const unsigned char *st, int lane
 // and its factor per activation row is that row's scale d.
 // GROUPS: m > 16, the rows in groups of 16 (grid x = tiles * groups, ROWS16 only).
 // RM: the weight is row-major (q8_gemv's layout), not tiled.
-template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false, bool RM = false>
+// XR (bf16 activations): each block's activation rows travel in the unit's ring stage (cp.async, read back from shared
+// memory once the stage has landed) instead of being loaded from L2 into registers two blocks ahead.
+template <bool ROWS16, int EPI, bool QACT = false, bool GROUPS = false, bool RM = false, bool XR = false>
 __global__ void __launch_bounds__(32 * stream_warps(ROWS16), 2)
     stream_kernel(Args a, const __grid_constant__ Parts parts, const int mode) {
     static_assert(ROWS16 || !GROUPS, "row groups are groups of 16 rows");
+    static_assert(!(XR && QACT), "the quantized activations are loaded from L2");
     constexpr int W = stream_warps(ROWS16);
+    constexpr int SS = XR ? kStageM : kStageS;  // bytes of a ring stage
     constexpr int MR = ROWS16 ? 16 : 8;
     constexpr int NR = ROWS16 ? 2 : 1;  // activation rows per lane: g and g + 8
     extern __shared__ __align__(16) unsigned char smem_s[];
@@ -416,13 +430,33 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), 2)
     const int b0 = c0 + (c1 - c0) * warp / W;
     const int b1 = c0 + (c1 - c0) * (warp + 1) / W;
     const int n = b1 - b0;
-    unsigned char *ring = smem_s + warp * kDepthS * kStageS;
+    unsigned char *ring = smem_s + warp * kDepthS * SS;
     const size_t unit0 = (size_t)tile * a.nb + b0;
-    auto issue = [&](unsigned char *stage, int i) {  // block b0 + i of the tile into `stage`
+    auto issue_w = [&](unsigned char *stage, int i) {  // block b0 + i of the tile (values, scales) into `stage`
         if constexpr (RM)
             issue_block_rm(stage, a.q, a.s, a.Np, tile, b0 + i, lane);
         else
             issue_unit(stage, a.q, a.s, unit0 + i, lane);
+    };
+    // The block's bf16 activation rows row0 .. row0 + MR - 1 (the launch's rows; those at or past m zero-filled) into
+    // the stage after the unit: row r's 8-byte word w (values 4w .. 4w + 3) at r * 64 + (w & 3) * 16 + (w >> 2) * 8,
+    // so that lane (g, t) finds its values 4t .. 4t + 3 and 16 + 4t .. 16 + 4t + 3 of a row as one 16-byte chunk.
+    auto issue_x = [&](unsigned char *stage, int i) {
+        if constexpr (XR) {
+            unsigned char *xs = stage + kStageS;
+            const size_t b = (size_t)(b0 + i);
+#pragma unroll
+            for (int k = 0; k < MR * 8 / 32; ++k) {
+                const int c = lane + 32 * k, r = c >> 3, w = c & 7;
+                const bool ok = row0 + r < a.m;
+                const uint16_t *src = a.x + (size_t)(ok ? row0 + r : 0) * a.K + b * kBlock + 4 * w;
+                cp_async8_zfill(xs + r * 64 + (w & 3) * 16 + (w >> 2) * 8, src, ok ? 8u : 0u);
+            }
+        }
+    };
+    auto issue = [&](unsigned char *stage, int i) {
+        issue_w(stage, i);
+        issue_x(stage, i);
     };
 
     // acc[i][j]: rows g + 8i, columns 8j + 2t and 8j + 2t + 1 of the tile
@@ -432,27 +466,34 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), 2)
 #pragma unroll
         for (int j = 0; j < kSlices; ++j) acc[i][j] = 0ull;
 
-    // Prologue: the first kDepthS - 1 units (one commit group each, empty past the run).
+    // Prologue: the first kDepthS - 1 units (one commit group each, empty past the run).  Requested before the
+    // dependency wait, a unit's weights go first and (XR) its activation rows, which the previous kernel may still be
+    // writing, after the wait in a group of their own: the loop's wait for unit i (at most kDepthS - 1 later groups
+    // pending) then covers both.
     const bool early = (mode & (kModePrefetch | kModeDeferWait)) != 0;  // weights requested before any wait
     if (early) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
-            if (i < n) issue(ring + i * kStageS, i);
+            if (i < n) issue_w(ring + i * SS, i);
             cp_async_commit();
         }
     }
     if (!(mode & kModeDeferWait)) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (mode & kModeRelease) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (!early) {
+    if (XR || !early) {
 #pragma unroll
         for (int i = 0; i < kDepthS - 1; ++i) {
-            if (i < n) issue(ring + i * kStageS, i);
+            if (i < n) {
+                if (!early) issue_w(ring + i * SS, i);
+                issue_x(ring + i * SS, i);
+            }
             cp_async_commit();
         }
     }
 
-    // The lane's activations x[g + 8i][32b + 16s + 4t .. + 3] (rows at or past m are zeros).  QACT: [i][0] holds the
-    // two int8 words (s = 0, 1) and [i][1].x the bits of the row's block scale.
+    // The lane's activations x[g + 8i][32b + 16s + 4t .. + 3] (rows at or past m are zeros): XR from the unit's
+    // stage; otherwise from L2, two blocks ahead (QACT: [i][0] holds the two int8 words (s = 0, 1) and [i][1].x the
+    // bits of the row's block scale).
     const uint16_t *xrow[NR];
     const unsigned char *qrow[NR];
     const float *drow[NR];
@@ -481,8 +522,10 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), 2)
             }
         }
     };
-    if (n > 0) load_x(xn1, b0);
-    if (n > 1) load_x(xn2, b0 + 1);
+    if constexpr (!XR) {
+        if (n > 0) load_x(xn1, b0);
+        if (n > 1) load_x(xn2, b0 + 1);
+    }
 
     // Stage indices: counted round for the 16-row kernel (measured faster there), i % depth for the 8-row one (its
     // register allocation is at its limit; the counters cost it more than they save).
@@ -490,35 +533,51 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), 2)
     for (int i = 0; i < n; ++i) {
         const int ahead = i + kDepthS - 1;
         if (ahead < n)
-            issue(ring + (ROWS16 ? nxt : ahead % kDepthS) * kStageS, ahead);
+            issue(ring + (ROWS16 ? nxt : ahead % kDepthS) * SS, ahead);
         cp_async_commit();
         uint2 xc[NR][2];
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                xc[r][s] = xn1[r][s];
-                xn1[r][s] = xn2[r][s];
-            }
-        if (i + 2 < n) load_x(xn2, b0 + i + 2);
         XPlan plan;
         bool f16_normal = false;  // 16-row kernel: every live activation already an fp16 normal (no plan needed)
-        if constexpr (QACT) {
-            plan.sf[0] = pack_f32x2(__uint_as_float(xc[0][1].x), __uint_as_float(xc[0][1].x));
-            plan.sf[1] = pack_f32x2(__uint_as_float(xc[NR - 1][1].x), __uint_as_float(xc[NR - 1][1].x));
-        } else if constexpr (ROWS16) {
-            f16_normal = block_f16_normal<NR>(xc, xlive[0], xlive[NR - 1]);
-            if (!f16_normal) plan = plan_block<NR, false>(xc);
-        } else {
-            plan = plan_block<NR, true>(xc);
+        if constexpr (!XR) {
+#pragma unroll
+            for (int r = 0; r < NR; ++r)
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    xc[r][s] = xn1[r][s];
+                    xn1[r][s] = xn2[r][s];
+                }
+            if (i + 2 < n) load_x(xn2, b0 + i + 2);
+            if constexpr (QACT) {
+                plan.sf[0] = pack_f32x2(__uint_as_float(xc[0][1].x), __uint_as_float(xc[0][1].x));
+                plan.sf[1] = pack_f32x2(__uint_as_float(xc[NR - 1][1].x), __uint_as_float(xc[NR - 1][1].x));
+            } else if constexpr (ROWS16) {
+                f16_normal = block_f16_normal<NR>(xc, xlive[0], xlive[NR - 1]);
+                if (!f16_normal) plan = plan_block<NR, false>(xc);
+            } else {
+                plan = plan_block<NR, true>(xc);
+            }
         }
 
         cp_async_wait<kDepthS - 1>();  // this lane's copies of unit i have landed
         __syncwarp();                  // ... and every other lane's
-        const unsigned char *st = ring + (ROWS16 ? cur : i % kDepthS) * kStageS;
+        const unsigned char *st = ring + (ROWS16 ? cur : i % kDepthS) * SS;
         if (ROWS16) {
             cur = cur == kDepthS - 1 ? 0 : cur + 1;
             nxt = nxt == kDepthS - 1 ? 0 : nxt + 1;
+        }
+        if constexpr (XR) {
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(st + kStageS + (g + 8 * r) * 64 + t * 16);
+                xc[r][0] = make_uint2(v.x, v.y);
+                xc[r][1] = make_uint2(v.z, v.w);
+            }
+            if constexpr (ROWS16) {
+                f16_normal = block_f16_normal<NR>(xc, xlive[0], xlive[NR - 1]);
+                if (!f16_normal) plan = plan_block<NR, false>(xc);
+            } else {
+                plan = plan_block<NR, true>(xc);
+            }
         }
         if constexpr (QACT) {
             // int8 codes as the stored-weight form (x + 128 = x ^ 0x80 per byte), then the same exact fp16 pairs
@@ -813,17 +872,21 @@ static_assert(2 * kSmemS <= 227 * 1024 && 2 * stream_smem(kWarps16) <= 227 * 102
 static_assert(finish_smem_n(kWarps8, 8, kTmaColumns, kSlabStride) <= stream_smem(kWarps8), "8-row epilogue fits");
 static_assert((kWarps8 * 8 * kSlabStride + 2 * 8 * kTmaColumns) * 4 <= stream_smem(kWarps8), "8-row gated pair fits");
 static_assert(2 * stream_smem(kWarps8) <= 227 * 1024, "two 8-row CTAs per SM");
+static_assert(2 * stream_smem(kWarps16, true) <= 227 * 1024 && 2 * stream_smem(kWarps8, true) <= 227 * 1024,
+              "two CTAs per SM whose stages carry the activation rows");
 // The shared memory of a launch held to one CTA per SM beside one ordinary CTA of the same kernel (the CUDA-core
 // kernel's 8 warps, the MMA kernels' 6): two such CTAs (each with its 1 KB reserve) exceed the SM's 228 KB, one of
 // them and an ordinary one do not.
 constexpr int kSmemOnePerSm = 114 * 1024;
+static_assert(stream_smem(kWarps16, true) <= kSmemOnePerSm && stream_smem(kWarps8, true) <= kSmemOnePerSm,
+              "a one-per-SM CTA holds the stages with the activation rows");
 static_assert(2 * (kSmemOnePerSm + 1024) > 228 * 1024 && kSmemOnePerSm + kSmemS + 2 * 1024 <= 228 * 1024,
               "one such CTA and one ordinary CTA per SM");
 
 template <typename Kernel>
-cudaError_t launch_stream_kernel(Kernel kernel, int warps, const Args &a, const Parts &pt, cudaStream_t stream,
-                                 bool pdl, int mode, bool pair, StreamGrid grid) {
-    const int smem = grid.one_per_sm ? kSmemOnePerSm : stream_smem(warps);
+cudaError_t launch_stream_kernel(Kernel kernel, int warps, bool ring, const Args &a, const Parts &pt,
+                                 cudaStream_t stream, bool pdl, int mode, bool pair, StreamGrid grid) {
+    const int smem = grid.one_per_sm ? kSmemOnePerSm : stream_smem(warps, ring);
     // the attribute is the largest size any launch of the kernel asks for, so that concurrent callers agree on it
     const int smem_max = kSmemOnePerSm;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
@@ -895,10 +958,10 @@ int stream_max_clusters(int m, bool qact, int ks, bool rowmajor) {
     const int fam = rows8_family(m, qact, rowmajor) ? 1 : (m == 1 || (m == 2 && qact)) ? 0 : 2;
     const int known = cache[dev][fam][ks].load(std::memory_order_relaxed);
     if (known > 0) return known - 1;
-    auto kernel = fam == 1   ? stream_kernel<false, kEpiStore>
+    auto kernel = fam == 1   ? stream_kernel<false, kEpiStore, false, false, false, true>
                   : fam == 2 ? stream_kernel<true, kEpiStore>
                              : stream_simt_kernel<1, kEpiStore>;
-    const int warps = fam == 1 ? kWarps8 : fam == 2 ? kWarps16 : kWarpsS, smem = stream_smem(warps);
+    const int warps = fam == 1 ? kWarps8 : fam == 2 ? kWarps16 : kWarpsS, smem = stream_smem(warps, fam == 1);
     int n = 0;
     bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kSmemOnePerSm) == cudaSuccess &&  // as launch_stream_kernel sets it
@@ -934,12 +997,14 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
     if ((grid.ntiles > 0 || a.tile0 != 0) && (EPI == kEpiNorm || a.m > kGroupRows || (pair && (a.tile0 & 1))))
         return cudaErrorInvalidValue;  // a part of the tiles: store, arg-max and gated-pair launches of one row group
 
-    auto go = [&](auto kernel) { return launch_stream_kernel(kernel, kWarpsS, a, pt, stream, pdl, mode, pair, grid); };
-    auto go8 = [&](auto kernel) {
-        return launch_stream_kernel(kernel, kWarps8, a, pt, stream, pdl, mode, pair, grid);
+    auto go = [&](auto kernel) {
+        return launch_stream_kernel(kernel, kWarpsS, false, a, pt, stream, pdl, mode, pair, grid);
     };
-    auto go16 = [&](auto kernel) {
-        return launch_stream_kernel(kernel, kWarps16, a, pt, stream, pdl, mode, pair, grid);
+    auto go8 = [&](auto kernel, bool ring = false) {
+        return launch_stream_kernel(kernel, kWarps8, ring, a, pt, stream, pdl, mode, pair, grid);
+    };
+    auto go16 = [&](auto kernel, bool ring = false) {
+        return launch_stream_kernel(kernel, kWarps16, ring, a, pt, stream, pdl, mode, pair, grid);
     };
     if constexpr (EPI == kEpiStore || EPI == kEpiArgmax) {
         if (rowmajor) {  // at most 16 rows, bf16 activations
@@ -957,8 +1022,12 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
         if (a.m <= kGroupRows) return go16(stream_kernel<true, EPI, true>);
         return go16(stream_kernel<true, EPI, true, true>);
     }
+    // 2 .. 8 bf16 rows take their activations through the ring stages (XR).  Measured on GB300 against loading them
+    // into registers two blocks ahead: the decode chain at m = 2 4,777 -> 5,008 GB/s and at m = 8 4,574 -> 4,843, every
+    // launch kind 4-9% faster.  The 16-row kernel keeps the registers: alone its long launches gained as much (the
+    // head at m = 16 -8%, gate/up -4%, down -5%), but its chain fell 4,162 -> 4,090 GB/s.
     if (a.m == 1) return go(stream_simt_kernel<1, EPI>);
-    if (a.m <= 8) return go8(stream_kernel<false, EPI>);
+    if (a.m <= 8) return go8(stream_kernel<false, EPI, false, false, false, true>, true);
     if (a.m <= kGroupRows) return go16(stream_kernel<true, EPI>);
     return go16(stream_kernel<true, EPI, false, true>);
 }
