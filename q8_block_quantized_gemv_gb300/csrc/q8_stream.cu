@@ -63,7 +63,8 @@ constexpr int kUnitScales = kTmaColumns;     // 128 fp32
 constexpr int kStageS = kUnit + kUnitScales * 4;
 constexpr int kDepthS = 3;                   // ring stages per warp
 constexpr int kSmemS = kWarpsS * kDepthS * kStageS;
-constexpr int kStageX = 16 * kBlock * 2;     // MMA kernels: the block's activation rows (up to 16 x 32 bf16)
+constexpr int kXPitch = 96;                  // MMA kernels: the block's activation rows (up to 16 x 32 bf16) at a
+constexpr int kStageX = 16 * kXPitch;        //   row pitch that keeps a half-warp's 8-byte reads conflict-free
 constexpr int kStageM = kStageS + kStageX;   //   so their stages hold the unit, its scales and those rows
 // ring: the stages also carry the block's activation rows (the MMA kernels' XR instances)
 __host__ __device__ constexpr int stream_smem(int warps, bool ring = false) {
@@ -76,10 +77,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async8_zfill(void *dst, const void *src, unsigned bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(bytes)
-                 : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N> __device__ __forceinline__ void cp_async_wait() {
@@ -439,18 +436,17 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), 2)
             issue_unit(stage, a.q, a.s, unit0 + i, lane);
     };
     // The block's bf16 activation rows row0 .. row0 + MR - 1 (the launch's rows; those at or past m zero-filled) into
-    // the stage after the unit: row r's 8-byte word w (values 4w .. 4w + 3) at r * 64 + (w & 3) * 16 + (w >> 2) * 8,
-    // so that lane (g, t) finds its values 4t .. 4t + 3 and 16 + 4t .. 16 + 4t + 3 of a row as one 16-byte chunk.
+    // the stage after the unit, row r at r * kXPitch: four 16-byte copies a row, through L2 like the unit's.
     auto issue_x = [&](unsigned char *stage, int i) {
         if constexpr (XR) {
             unsigned char *xs = stage + kStageS;
             const size_t b = (size_t)(b0 + i);
 #pragma unroll
-            for (int k = 0; k < MR * 8 / 32; ++k) {
-                const int c = lane + 32 * k, r = c >> 3, w = c & 7;
+            for (int k = 0; k < MR * 4 / 32; ++k) {
+                const int c = lane + 32 * k, r = c >> 2, ch = c & 3;
                 const bool ok = row0 + r < a.m;
-                const uint16_t *src = a.x + (size_t)(ok ? row0 + r : 0) * a.K + b * kBlock + 4 * w;
-                cp_async8_zfill(xs + r * 64 + (w & 3) * 16 + (w >> 2) * 8, src, ok ? 8u : 0u);
+                const uint16_t *src = a.x + (size_t)(ok ? row0 + r : 0) * a.K + b * kBlock + 8 * ch;
+                cp_async16_zfill(xs + r * kXPitch + ch * 16, src, ok ? 16u : 0u);
             }
         }
     };
@@ -568,9 +564,9 @@ __global__ void __launch_bounds__(32 * stream_warps(ROWS16), 2)
         if constexpr (XR) {
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(st + kStageS + (g + 8 * r) * 64 + t * 16);
-                xc[r][0] = make_uint2(v.x, v.y);
-                xc[r][1] = make_uint2(v.z, v.w);
+                const unsigned char *row = st + kStageS + (g + 8 * r) * kXPitch;
+                xc[r][0] = *reinterpret_cast<const uint2 *>(row + 8 * t);       // values 4t .. 4t + 3
+                xc[r][1] = *reinterpret_cast<const uint2 *>(row + 32 + 8 * t);  // values 16 + 4t .. 16 + 4t + 3
             }
             if constexpr (ROWS16) {
                 f16_normal = block_f16_normal<NR>(xc, xlive[0], xlive[NR - 1]);
