@@ -66,10 +66,10 @@ constexpr int kSmemS = kWarpsS * kDepthS * kStageS;
 constexpr int kXPitch = 96;                  // MMA kernels: the block's activation rows (up to 16 x 32 bf16) at a
 constexpr int kStageX = 16 * kXPitch;        //   row pitch that keeps a half-warp's 8-byte reads conflict-free
 constexpr int kStageM = kStageS + kStageX;   //   so their stages hold the unit, its scales and those rows
-// ring: the stages also carry the block's activation rows (the MMA kernels' XR instances)
-__host__ __device__ constexpr int stream_smem(int warps, bool ring = false) {
-    return warps * kDepthS * (ring ? kStageM : kStageS);
-}
+constexpr int kStageS1 = kStageS + kBlock * 2;  // the CUDA-core kernel's stages with the block's one bf16 row
+// The ring of a CTA of `warps` warps with stages of `stage` bytes (kStageS; kStageM and kStageS1 for the XR instances,
+// whose stages also carry the block's activation rows).
+__host__ __device__ constexpr int stream_smem(int warps, int stage = kStageS) { return warps * kDepthS * stage; }
 constexpr int kSlices = kTmaColumns / 8;     // 8-column MMA slices of a tile
 constexpr int kSlabStride = kTmaColumns + 8; // epilogue slab row stride (floats)
 
@@ -673,9 +673,12 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // QACT (quantized activations): the lane's eight codes of a row and block meet each column's eight stored
 // bytes in two dp4a (integer products, exact); the offset is removed by starting the sum at -128 times the sum of the
 // eight codes, the exact integer is converted to fp32 and folded with s[b, n] * d[r, b].
-template <int M, int EPI, bool QACT = false, bool RM = false>
+// XR (one bf16 row, tiled weights): the block's row travels in the unit's ring stage, as in the 8-row kernel.
+template <int M, int EPI, bool QACT = false, bool RM = false, bool XR = false>
 __global__ void __launch_bounds__(kThreadsS, 2)
     stream_simt_kernel(Args a, const __grid_constant__ Parts parts, const int mode) {
+    static_assert(!XR || (M == 1 && !QACT && !RM), "the staged row: one bf16 row of tiled weights");
+    constexpr int SS = XR ? kStageS1 : kStageS;  // bytes of a ring stage
     extern __shared__ __align__(16) unsigned char smem_s[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -687,13 +690,21 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     const int b0 = c0 + (c1 - c0) * warp / kWarpsS;
     const int b1 = c0 + (c1 - c0) * (warp + 1) / kWarpsS;
     const int n = b1 - b0;
-    unsigned char *ring = smem_s + warp * kDepthS * kStageS;
+    unsigned char *ring = smem_s + warp * kDepthS * SS;
     const size_t unit0 = (size_t)tile * a.nb + b0;
-    auto issue = [&](unsigned char *stage, int i) {  // block b0 + i of the tile into `stage`
+    auto issue_w = [&](unsigned char *stage, int i) {  // block b0 + i of the tile (values, scales) into `stage`
         if constexpr (RM)
             issue_block_rm(stage, a.q, a.s, a.Np, tile, b0 + i, lane);
         else
             issue_unit(stage, a.q, a.s, unit0 + i, lane);
+    };
+    auto issue_x = [&](unsigned char *stage, int i) {  // XR: the block's 64 bytes of the row, after the unit
+        if constexpr (XR)
+            if (lane < 4) cp_async16(stage + kStageS + 16 * lane, a.x + (size_t)(b0 + i) * kBlock + 8 * lane);
+    };
+    auto issue = [&](unsigned char *stage, int i) {
+        issue_w(stage, i);
+        issue_x(stage, i);
     };
 
     unsigned long long acc[M][kSlices];  // per row and column 8j + g: the carry of rows 4t, 4t+2 | 4t+1, 4t+3
@@ -709,20 +720,25 @@ __global__ void __launch_bounds__(kThreadsS, 2)
     // All kDepthS stages are requested before the dependency wait (unit i + kDepthS is requested once unit i is done):
     // measured on GB300, the one-row decode chain 5,003 -> 5,066 GB/s against requesting kDepthS - 1 first; the MMA
     // kernels keep the request at the top of the loop (there the same change lost 1-12%).
+    // (XR: the rows of those stages follow after the wait, in groups of their own: the loop's wait for unit i, with at
+    // most kDepthS - 1 later groups pending, covers its row too.)
     const bool early = (mode & (kModePrefetch | kModeDeferWait)) != 0;  // weights requested before any wait
     if (early) {
 #pragma unroll
         for (int i = 0; i < kDepthS; ++i) {
-            if (i < n) issue(ring + i * kStageS, i);
+            if (i < n) issue_w(ring + i * SS, i);
             cp_async_commit();
         }
     }
     if (!(mode & kModeDeferWait)) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (mode & kModeRelease) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (!early) {
+    if (XR || !early) {
 #pragma unroll
         for (int i = 0; i < kDepthS; ++i) {
-            if (i < n) issue(ring + i * kStageS, i);
+            if (i < n) {
+                if (!early) issue_w(ring + i * SS, i);
+                issue_x(ring + i * SS, i);
+            }
             cp_async_commit();
         }
     }
@@ -745,19 +761,23 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             }
         }
     };
-    if (n > 0) load_x(xn1, b0);
-    if (n > 1) load_x(xn2, b0 + 1);
+    if constexpr (!XR) {
+        if (n > 0) load_x(xn1, b0);
+        if (n > 1) load_x(xn2, b0 + 1);
+    }
 
     for (int i = 0; i < n; ++i) {
         uint2 xc[M][2];
+        if constexpr (!XR) {
 #pragma unroll
-        for (int r = 0; r < M; ++r)
+            for (int r = 0; r < M; ++r)
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                xc[r][s] = xn1[r][s];
-                xn1[r][s] = xn2[r][s];
-            }
-        if (i + 2 < n) load_x(xn2, b0 + i + 2);
+                for (int s = 0; s < 2; ++s) {
+                    xc[r][s] = xn1[r][s];
+                    xn1[r][s] = xn2[r][s];
+                }
+            if (i + 2 < n) load_x(xn2, b0 + i + 2);
+        }
         if constexpr (QACT) {
             int base[M];  // -128 * (the lane's eight codes of the row summed)
 #pragma unroll
@@ -765,7 +785,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 base[r] = -128 * dp4a_us(0x01010101u, xc[r][0].y, dp4a_us(0x01010101u, xc[r][0].x, 0));
             cp_async_wait<kDepthS - 1>();
             __syncwarp();
-            const unsigned char *st = ring + (i % kDepthS) * kStageS;
+            const unsigned char *st = ring + (i % kDepthS) * SS;
             const float *ss = reinterpret_cast<const float *>(st + kUnit) + g;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -785,9 +805,16 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 }
             }
             __syncwarp();  // every lane is done with this stage: it takes unit i + kDepthS
-            if (i + kDepthS < n) issue(ring + (i % kDepthS) * kStageS, i + kDepthS);
+            if (i + kDepthS < n) issue(ring + (i % kDepthS) * SS, i + kDepthS);
             cp_async_commit();
             continue;
+        }
+        if constexpr (XR) {  // the row's values 4t .. 4t + 3 and 16 + 4t .. 16 + 4t + 3, once the stage has landed
+            cp_async_wait<kDepthS - 1>();
+            __syncwarp();
+            const unsigned char *xs = ring + (i % kDepthS) * SS + kStageS;
+            xc[0][0] = *reinterpret_cast<const uint2 *>(xs + 8 * t);
+            xc[0][1] = *reinterpret_cast<const uint2 *>(xs + 32 + 8 * t);
         }
         // activations as fp32 pairs {x[4t], x[4t+1]} and {x[4t+2], x[4t+3]} of each row and half
         unsigned long long xp[M][2][2];
@@ -798,9 +825,11 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                 xp[r][s][0] = pack_f32x2(bf16_lo(xc[r][s].x), bf16_hi(xc[r][s].x));
                 xp[r][s][1] = pack_f32x2(bf16_lo(xc[r][s].y), bf16_hi(xc[r][s].y));
             }
-        cp_async_wait<kDepthS - 1>();
-        __syncwarp();
-        const unsigned char *st = ring + (i % kDepthS) * kStageS;
+        if constexpr (!XR) {
+            cp_async_wait<kDepthS - 1>();
+            __syncwarp();
+        }
+        const unsigned char *st = ring + (i % kDepthS) * SS;
         const float *ss = reinterpret_cast<const float *>(st + kUnit) + g;
         // per group h of four slices: both 16-row halves, then the fold, so that only four slices' block sums are
         // live at a time (each slice's operations run in the same order as half by half over all slices)
@@ -829,7 +858,7 @@ __global__ void __launch_bounds__(kThreadsS, 2)
             }
         }
         __syncwarp();  // every lane is done with this stage: it takes unit i + kDepthS
-        if (i + kDepthS < n) issue(ring + (i % kDepthS) * kStageS, i + kDepthS);
+        if (i + kDepthS < n) issue(ring + (i % kDepthS) * SS, i + kDepthS);
         cp_async_commit();
     }
     cp_async_wait<0>();
@@ -868,21 +897,22 @@ static_assert(2 * kSmemS <= 227 * 1024 && 2 * stream_smem(kWarps16) <= 227 * 102
 static_assert(finish_smem_n(kWarps8, 8, kTmaColumns, kSlabStride) <= stream_smem(kWarps8), "8-row epilogue fits");
 static_assert((kWarps8 * 8 * kSlabStride + 2 * 8 * kTmaColumns) * 4 <= stream_smem(kWarps8), "8-row gated pair fits");
 static_assert(2 * stream_smem(kWarps8) <= 227 * 1024, "two 8-row CTAs per SM");
-static_assert(2 * stream_smem(kWarps16, true) <= 227 * 1024 && 2 * stream_smem(kWarps8, true) <= 227 * 1024,
+static_assert(2 * stream_smem(kWarps8, kStageM) <= 227 * 1024 && 2 * stream_smem(kWarpsS, kStageS1) <= 227 * 1024,
               "two CTAs per SM whose stages carry the activation rows");
 // The shared memory of a launch held to one CTA per SM beside one ordinary CTA of the same kernel (the CUDA-core
 // kernel's 8 warps, the MMA kernels' 6): two such CTAs (each with its 1 KB reserve) exceed the SM's 228 KB, one of
 // them and an ordinary one do not.
 constexpr int kSmemOnePerSm = 114 * 1024;
-static_assert(stream_smem(kWarps16, true) <= kSmemOnePerSm && stream_smem(kWarps8, true) <= kSmemOnePerSm,
-              "a one-per-SM CTA holds the stages with the activation rows");
+static_assert(stream_smem(kWarps8, kStageM) <= kSmemOnePerSm && stream_smem(kWarpsS, kStageS1) <= kSmemOnePerSm &&
+                  kSmemOnePerSm + stream_smem(kWarpsS, kStageS1) + 2 * 1024 <= 228 * 1024,
+              "a one-per-SM CTA holds the stages with the activation rows, beside an ordinary one");
 static_assert(2 * (kSmemOnePerSm + 1024) > 228 * 1024 && kSmemOnePerSm + kSmemS + 2 * 1024 <= 228 * 1024,
               "one such CTA and one ordinary CTA per SM");
 
 template <typename Kernel>
-cudaError_t launch_stream_kernel(Kernel kernel, int warps, bool ring, const Args &a, const Parts &pt,
+cudaError_t launch_stream_kernel(Kernel kernel, int warps, int stage, const Args &a, const Parts &pt,
                                  cudaStream_t stream, bool pdl, int mode, bool pair, StreamGrid grid) {
-    const int smem = grid.one_per_sm ? kSmemOnePerSm : stream_smem(warps, ring);
+    const int smem = grid.one_per_sm ? kSmemOnePerSm : stream_smem(warps, stage);
     // the attribute is the largest size any launch of the kernel asks for, so that concurrent callers agree on it
     const int smem_max = kSmemOnePerSm;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
@@ -956,8 +986,9 @@ int stream_max_clusters(int m, bool qact, int ks, bool rowmajor) {
     if (known > 0) return known - 1;
     auto kernel = fam == 1   ? stream_kernel<false, kEpiStore, false, false, false, true>
                   : fam == 2 ? stream_kernel<true, kEpiStore>
-                             : stream_simt_kernel<1, kEpiStore>;
-    const int warps = fam == 1 ? kWarps8 : fam == 2 ? kWarps16 : kWarpsS, smem = stream_smem(warps, fam == 1);
+                             : stream_simt_kernel<1, kEpiStore, false, false, true>;
+    const int warps = fam == 1 ? kWarps8 : fam == 2 ? kWarps16 : kWarpsS;
+    const int smem = stream_smem(warps, fam == 1 ? kStageM : fam == 2 ? kStageS : kStageS1);
     int n = 0;
     bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kSmemOnePerSm) == cudaSuccess &&  // as launch_stream_kernel sets it
@@ -993,14 +1024,14 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
     if ((grid.ntiles > 0 || a.tile0 != 0) && (EPI == kEpiNorm || a.m > kGroupRows || (pair && (a.tile0 & 1))))
         return cudaErrorInvalidValue;  // a part of the tiles: store, arg-max and gated-pair launches of one row group
 
-    auto go = [&](auto kernel) {
-        return launch_stream_kernel(kernel, kWarpsS, false, a, pt, stream, pdl, mode, pair, grid);
+    auto go = [&](auto kernel, int stage = kStageS) {
+        return launch_stream_kernel(kernel, kWarpsS, stage, a, pt, stream, pdl, mode, pair, grid);
     };
-    auto go8 = [&](auto kernel, bool ring = false) {
-        return launch_stream_kernel(kernel, kWarps8, ring, a, pt, stream, pdl, mode, pair, grid);
+    auto go8 = [&](auto kernel, int stage = kStageS) {
+        return launch_stream_kernel(kernel, kWarps8, stage, a, pt, stream, pdl, mode, pair, grid);
     };
-    auto go16 = [&](auto kernel, bool ring = false) {
-        return launch_stream_kernel(kernel, kWarps16, ring, a, pt, stream, pdl, mode, pair, grid);
+    auto go16 = [&](auto kernel, int stage = kStageS) {
+        return launch_stream_kernel(kernel, kWarps16, stage, a, pt, stream, pdl, mode, pair, grid);
     };
     if constexpr (EPI == kEpiStore || EPI == kEpiArgmax) {
         if (rowmajor) {  // at most 16 rows, bf16 activations
@@ -1022,8 +1053,8 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
     // into registers two blocks ahead: the decode chain at m = 2 4,777 -> 5,008 GB/s and at m = 8 4,574 -> 4,843, every
     // launch kind 4-9% faster.  The 16-row kernel keeps the registers: alone its long launches gained as much (the
     // head at m = 16 -8%, gate/up -4%, down -5%), but its chain fell 4,162 -> 4,090 GB/s.
-    if (a.m == 1) return go(stream_simt_kernel<1, EPI>);
-    if (a.m <= 8) return go8(stream_kernel<false, EPI, false, false, false, true>, true);
+    if (a.m == 1) return go(stream_simt_kernel<1, EPI, false, false, true>, kStageS1);
+    if (a.m <= 8) return go8(stream_kernel<false, EPI, false, false, false, true>, kStageM);
     if (a.m <= kGroupRows) return go16(stream_kernel<true, EPI>);
     return go16(stream_kernel<true, EPI, false, true>);
 }
