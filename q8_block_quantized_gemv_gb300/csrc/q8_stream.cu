@@ -1053,7 +1053,12 @@ cudaError_t launch_stream_epi(const Args &a, const Parts &pt, cudaStream_t strea
     // into registers two blocks ahead: the decode chain at m = 2 4,777 -> 5,008 GB/s and at m = 8 4,574 -> 4,843, every
     // launch kind 4-9% faster.  The 16-row kernel keeps the registers: alone its long launches gained as much (the
     // head at m = 16 -8%, gate/up -4%, down -5%), but its chain fell 4,162 -> 4,090 GB/s.
-    if (a.m == 1) return go(stream_simt_kernel<1, EPI, false, false, true>, kStageS1);
+    // One bf16 row: through the ring stages too (the one-row chain 5,123 -> 5,143 GB/s), but for the two launches of a
+    // plain product split in two (the gate/up pair), which keep the register loads (5,143 -> 5,210).
+    if (a.m == 1) {
+        if (EPI == kEpiStore && (grid.ntiles > 0 || a.tile0 != 0)) return go(stream_simt_kernel<1, EPI>);
+        return go(stream_simt_kernel<1, EPI, false, false, true>, kStageS1);
+    }
     if (a.m <= 8) return go8(stream_kernel<false, EPI, false, false, false, true>, kStageM);
     if (a.m <= kGroupRows) return go16(stream_kernel<true, EPI>);
     return go16(stream_kernel<true, EPI, false, true>);
