@@ -41,10 +41,11 @@
 // rows of quantized activations stay on the CUDA cores, whose dp4a products beat it there (the decode chain 3,900
 // against 3,658 GB/s).
 //
-// Activations are read from L2 (ld.global.cg), two blocks ahead; the 8-row kernel's bf16 rows instead travel in the
-// unit's ring stage (cp.async), read back from shared memory with the unit.  With programmatic dependent launch every
-// thread waits for the previous kernel (griddepcontrol.wait) before it reads x or writes y; with
-// Q8_FLAG_CONSTANT_WEIGHTS the first two stages' weights are already requested before that wait.
+// Bf16 activations of one row (the CUDA-core kernel) and of 2 .. 8 rows (the 8-row kernel) travel in the unit's ring
+// stage (cp.async through L2), read back from shared memory with the unit; the 16-row kernel, quantized activations
+// and row-major weights read them from L2 (ld.global.cg) into registers two blocks ahead.  With programmatic dependent
+// launch every thread waits for the previous kernel (griddepcontrol.wait) before it reads x or writes y; with
+// Q8_FLAG_CONSTANT_WEIGHTS the first stages' weights are already requested before that wait.
 #include <atomic>
 
 #include "q8_launch.h"
@@ -975,9 +976,9 @@ int stream_ctas_per_sm(int, bool, bool) { return 2; }
 
 int stream_max_clusters(int m, bool qact, int ks, bool rowmajor) {
     // Clusters of ks CTAs are placed within one GPC, so fewer of them fit at once than slots / ks.  Asked once per
-    // device, kernel shape and size (a deterministic answer: concurrent first calls store the same value); the stream
-    // kernels of one family (CUDA-core: 8 warps; 8-row and 16-row: 6 warps; two CTAs per SM each) have the same block
-    // size, register cap and shared memory.
+    // device, kernel shape and size (a deterministic answer: concurrent first calls store the same value) of the
+    // family's main instance; the stream kernels of one family (CUDA-core: 8 warps; 8-row and 16-row: 6 warps; two
+    // CTAs per SM each) have the same block size and register cap, and shared memory within 2% of it.
     static std::atomic<int> cache[64][3][kMaxStreamSplit + 1];  // 0: not asked yet; else the count + 1
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || ks < 1 || ks > kMaxStreamSplit) return 0;
