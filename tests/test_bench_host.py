@@ -26,3 +26,19 @@ def test_source_hash_ignores_comments_not_code(monkeypatch):
     assert bench.source_hash() == base
     edit = lambda t: t.replace("namespace q8 {", "namespace q8 { constexpr int kUnused = 1;", 1)
     assert bench.source_hash() != base
+
+
+def test_traffic_record_matches_the_committed_kernels():
+    """profiles/traffic.json was captured from the stream kernels as they stand (its key is their sources' hash), so
+    the bench line carries its DRAM traffic; and that traffic is the algorithmic bytes to within 2% (no weight byte is
+    read twice)."""
+    import json
+    with open(bench.PROFILE_TRAFFIC) as f:
+        rec = json.load(f)
+    assert rec["source_hash"] == bench.source_hash(), "kernel sources changed since the traffic capture"
+    for m in ("1", "16"):
+        got = bench.traffic_record(int(m), True)
+        assert got is not None
+        alg = rec["by_m"][m]["algorithmic_bytes_per_call"]
+        assert abs(got - alg) <= 0.02 * alg, (m, got, alg)
+    assert bench.traffic_record(1, False) is None  # a variant chain is not the captured step
